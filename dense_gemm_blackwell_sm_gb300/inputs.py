@@ -1,0 +1,105 @@
+"""Seeded synthetic operands for the GEMM / GEMV workloads.
+
+This module draws random numbers and rounds them to fp16 / bf16; it holds none
+of the GEMM's arithmetic.  It is the one piece the CUDA path's tests, the bench
+and the CPU oracle's tests share: both sides read the very same rounded bytes.
+
+Recipe (the pages name no RNG, so this is the plainest reading):
+  * one CPU ``torch.Generator`` seeded with the workload's seed;
+  * A is drawn first, then B, both in fp32, from that one generator;
+  * uniform[-1, 1] is ``2 * rand - 1``; normal(0, s) is ``randn * s``;
+    "normal(0,1)/sqrt(K)" is ``randn * (1/sqrt(K))``;
+  * the fp32 draws are rounded to fp16 / bf16 by ``Tensor.to`` (round to nearest even);
+  * for the decode GEMV, "A" is the activation row block x (M x K) and "B" is
+    the weight (N x K).
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+
+import torch
+
+F16 = "f16"
+BF16 = "bf16"
+F32 = "f32"
+
+_TORCH = {F16: torch.float16, BF16: torch.bfloat16, F32: torch.float32}
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    name: str
+    M: int
+    N: int
+    K: int
+    in_dtype: str          # "f16" | "bf16"
+    out_dtype: str         # "f32" | "bf16"
+    dist_a: tuple          # ("uniform",) | ("normal", sigma) | ("normal_rsqrt_k",)
+    dist_b: tuple
+    seed: int
+
+    @property
+    def flops(self) -> int:
+        return 2 * self.M * self.N * self.K
+
+    @property
+    def algorithmic_bytes(self) -> int:
+        ib = 2
+        ob = 4 if self.out_dtype == F32 else 2
+        return ib * (self.M * self.K + self.N * self.K) + ob * self.M * self.N
+
+
+U = ("uniform",)
+N002 = ("normal", 0.02)
+
+# The five workload families of the dense GEMM / decode GEMV, with their seeds.
+WORKLOADS = {
+    "single_tile_128x128x64_f16_f32": Workload("single_tile_128x128x64_f16_f32", 128, 128, 64, F16, F32, U, U, 0),
+    "kloop_1024x1024x4096_bf16_bf16": Workload("kloop_1024x1024x4096_bf16_bf16", 1024, 1024, 4096, BF16, BF16,
+                                               ("normal_rsqrt_k",), ("normal_rsqrt_k",), 1),
+    "square_4096_f16_f32": Workload("square_4096_f16_f32", 4096, 4096, 4096, F16, F32, U, U, 2),
+    "large_8192_bf16_bf16": Workload("large_8192_bf16_bf16", 8192, 8192, 8192, BF16, BF16, N002, N002, 3),
+    "llm_proj_8192x14336x4096_bf16_bf16": Workload("llm_proj_8192x14336x4096_bf16_bf16", 8192, 14336, 4096,
+                                                   BF16, BF16, N002, N002, 3),
+    "gemv_m1_n4096_k4096_bf16": Workload("gemv_m1_n4096_k4096_bf16", 1, 4096, 4096, BF16, BF16, U, N002, 4),
+    "gemv_m8_n4096_k4096_bf16": Workload("gemv_m8_n4096_k4096_bf16", 8, 4096, 4096, BF16, BF16, U, N002, 4),
+    "gemv_m1_n14336_k4096_bf16": Workload("gemv_m1_n14336_k4096_bf16", 1, 14336, 4096, BF16, BF16, U, N002, 4),
+    "gemv_m8_n14336_k4096_bf16": Workload("gemv_m8_n14336_k4096_bf16", 8, 14336, 4096, BF16, BF16, U, N002, 4),
+}
+
+
+def _draw(gen: torch.Generator, rows: int, cols: int, dist: tuple, K: int) -> torch.Tensor:
+    if dist[0] == "uniform":
+        return torch.rand(rows, cols, generator=gen, dtype=torch.float32) * 2.0 - 1.0
+    if dist[0] == "normal":
+        return torch.randn(rows, cols, generator=gen, dtype=torch.float32) * float(dist[1])
+    if dist[0] == "normal_rsqrt_k":
+        return torch.randn(rows, cols, generator=gen, dtype=torch.float32) * (1.0 / math.sqrt(K))
+    if dist[0] == "int":
+        lo, hi = int(dist[1]), int(dist[2])
+        return torch.randint(lo, hi + 1, (rows, cols), generator=gen).to(torch.float32)
+    raise ValueError("unknown distribution %r" % (dist,))
+
+
+def make_operands(M: int, N: int, K: int, in_dtype: str, dist_a: tuple, dist_b: tuple, seed: int,
+                  rows_a: int | None = None):
+    """Seeded (A, B) as CPU fp16/bf16 tensors: A is M x K, B is N x K (A drawn first)."""
+    gen = torch.Generator().manual_seed(int(seed))
+    a = _draw(gen, M if rows_a is None else rows_a, K, dist_a, K).to(_TORCH[in_dtype])
+    b = _draw(gen, N, K, dist_b, K).to(_TORCH[in_dtype])
+    return a.contiguous(), b.contiguous()
+
+
+def workload_operands(w: Workload):
+    return make_operands(w.M, w.N, w.K, w.in_dtype, w.dist_a, w.dist_b, w.seed)
+
+
+def integer_operands(M: int, N: int, K: int, in_dtype: str, seed: int, lo: int = -2, hi: int = 2):
+    """Integer-valued operands in [lo, hi]: every fp32 partial sum is exact when
+    K * max|a| * max|b| < 2^24, so any summation order gives the same bits."""
+    return make_operands(M, N, K, in_dtype, ("int", lo, hi), ("int", lo, hi), seed)
+
+
+def torch_dtype(name: str) -> torch.dtype:
+    return _TORCH[name]

@@ -1,0 +1,133 @@
+"""CPU oracle for C = A * B^T -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s cpu_baseline /
+reference leg may import this package.  The product (``dense_gemm_blackwell_sm_gb300``)
+never imports it, and the two share no code: the arithmetic lives in
+``gemm_oracle.c`` (plain fp64 triple loop, OpenMP over rows), built into
+``liboracle.so`` next to it by :func:`build`.
+
+Every function here is the plain definition
+``C[i,j] = sum_k a[i,k] * b[j,k]`` (with ``S[i,j] = sum_k |a[i,k] * b[j,k]|``)
+of the dense GEMM that "Modern GPU Programming for MLSys" (reading notes,
+section "9 步优化", steps 1-3) computes tile by tile; see the C file's header.
+
+Pins (tests/test_oracle_pins.py): exact-rational brute force on tiny shapes,
+identity / permutation operands, the rank-1 closed form, transpose symmetry,
+additivity, thread-count invariance and an exhaustive check of both 16-bit
+decoders against numpy's IEEE binary16 / binary32 conversions.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "gemm_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+
+IN_F16 = 0
+IN_BF16 = 1
+
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile ``gemm_oracle.c`` into ``liboracle.so`` (gcc, OpenMP, no fast-math)."""
+    if (not force and os.path.exists(_LIB)
+            and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)):
+        return _LIB
+    tmp = _LIB + ".tmp.%d" % os.getpid()
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp",
+           "-ffp-contract=off", "-fno-fast-math", "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        build()
+        lib = ctypes.CDLL(_LIB)
+        i64, p = ctypes.c_int64, ctypes.c_void_p
+        lib.oracle_gemm_rows_f64.argtypes = [i64, i64, i64, p, p, ctypes.c_int,
+                                             p, i64, p, p, ctypes.c_int]
+        lib.oracle_gemm_rows_f64.restype = ctypes.c_int
+        lib.oracle_gemm_f64.argtypes = [i64, i64, i64, p, p, ctypes.c_int, p, p, ctypes.c_int]
+        lib.oracle_gemm_f64.restype = ctypes.c_int
+        lib.oracle_widen.argtypes = [ctypes.c_uint16, ctypes.c_int]
+        lib.oracle_widen.restype = ctypes.c_double
+        lib.oracle_max_threads.argtypes = []
+        lib.oracle_max_threads.restype = ctypes.c_int
+        _lib = lib
+    return _lib
+
+
+def _bits(x) -> np.ndarray:
+    """Raw 16-bit patterns of a 2-D fp16/bf16 array (torch tensor or uint16 ndarray)."""
+    if isinstance(x, np.ndarray):
+        if x.dtype == np.float16:
+            x = x.view(np.uint16)
+        if x.dtype != np.uint16:
+            raise TypeError("oracle operands must be 16-bit patterns")
+        return np.ascontiguousarray(x)
+    import torch  # only for tensor inputs
+    if x.dtype not in (torch.float16, torch.bfloat16):
+        raise TypeError("oracle operands must be fp16 or bf16")
+    return np.ascontiguousarray(x.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16))
+
+
+def kind_of(x) -> int:
+    """IN_F16 or IN_BF16 for a torch tensor / numpy array."""
+    if isinstance(x, np.ndarray):
+        return IN_F16
+    import torch
+    return IN_BF16 if x.dtype == torch.bfloat16 else IN_F16
+
+
+def max_threads() -> int:
+    return int(_load().oracle_max_threads())
+
+
+def widen(bits: int, kind: int) -> float:
+    """Exact value of one 16-bit pattern (kind IN_F16 or IN_BF16)."""
+    return float(_load().oracle_widen(int(bits) & 0xFFFF, int(kind)))
+
+
+def gemm(a, b, kind: int | None = None, nthreads: int = 0):
+    """Full fp64 C = A * B^T and S = sum_k |a_ik b_jk|; returns (C, S) as float64 arrays."""
+    kind = kind_of(a) if kind is None else kind
+    A, B = _bits(a), _bits(b)
+    M, K = A.shape
+    N, K2 = B.shape
+    if K != K2:
+        raise ValueError("inner dimensions differ")
+    C = np.empty((M, N), dtype=np.float64)
+    S = np.empty((M, N), dtype=np.float64)
+    rc = _load().oracle_gemm_f64(M, N, K, A.ctypes.data, B.ctypes.data, kind,
+                                 C.ctypes.data, S.ctypes.data, int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle_gemm_f64 rejected its arguments")
+    return C, S
+
+
+def gemm_rows(a, b, rows, kind: int | None = None, nthreads: int = 0):
+    """Rows ``rows`` of C and S only (len(rows) x N each)."""
+    kind = kind_of(a) if kind is None else kind
+    A, B = _bits(a), _bits(b)
+    M, K = A.shape
+    N, K2 = B.shape
+    if K != K2:
+        raise ValueError("inner dimensions differ")
+    r = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    C = np.empty((len(r), N), dtype=np.float64)
+    S = np.empty((len(r), N), dtype=np.float64)
+    rc = _load().oracle_gemm_rows_f64(M, N, K, A.ctypes.data, B.ctypes.data, kind,
+                                      r.ctypes.data, len(r), C.ctypes.data, S.ctypes.data,
+                                      int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle_gemm_rows_f64 rejected its arguments")
+    return C, S

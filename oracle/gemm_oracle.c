@@ -1,0 +1,150 @@
+/*
+ * gemm_oracle.c -- the CPU oracle for C = A * B^T.  TEST INFRASTRUCTURE ONLY.
+ *
+ * Only tests/, __graft_entry__.smoke() and bench.py's cpu_baseline / reference
+ * leg may load or call this library.  The product path (the CUDA library under
+ * dense_gemm_blackwell_sm_gb300/) never links, imports or executes it, and this
+ * file shares no code, header, table or constant with that path.
+ *
+ * What it computes (plain definition, fp64):
+ *
+ *     C[i][j] = sum_{k=0}^{K-1} a[i][k] * b[j][k]      0 <= i < M, 0 <= j < N
+ *     S[i][j] = sum_{k=0}^{K-1} |a[i][k] * b[j][k]|
+ *
+ * A is M x K row-major and B is N x K row-major (both K-major), so the result
+ * is A times B-transposed, C being M x N row-major.  This is the tiled GEMM that
+ * "Modern GPU Programming for MLSys" (reading notes, section "9 步优化",
+ * steps 1-3) builds tile by tile: the Tensor Core computes D = A x B + C with
+ * fp32 accumulation in TMEM (section "计算单元", "存储层次: TMEM"), the K loop
+ * adds every K-block's partial product into one accumulator (step 2), and the
+ * split of the output into a tile grid (step 3) cannot change the value of any
+ * element.  So the oracle is the definition itself: a triple loop, i then j
+ * then k innermost, summed sequentially in k order, with no blocking, no
+ * reassociation and no BLAS.  Rows are spread over OpenMP threads, which leaves
+ * the summation order of every element unchanged.
+ *
+ * Inputs arrive as raw 16-bit patterns (IEEE binary16 or bfloat16) and are
+ * widened exactly to double by this file's own decoders.  Every product of two
+ * such values is exact in double (11+11 resp. 8+8 significand bits < 53), so
+ * the only rounding is in the k-sum, bounded by (K-1) * 2^-53 * S.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORACLE_IN_F16 0
+#define ORACLE_IN_BF16 1
+
+/* IEEE 754 binary16: sign bit 15, 5-bit exponent (bias 15), 10-bit fraction. */
+static double widen_binary16(uint16_t h) {
+    int sign = (h >> 15) & 1;
+    int e = (h >> 10) & 0x1F;
+    int f = h & 0x3FF;
+    double v;
+    if (e == 0) {
+        v = ldexp((double)f, -24);                 /* subnormal: f * 2^-14 * 2^-10 */
+    } else if (e == 31) {
+        v = (f == 0) ? INFINITY : NAN;
+    } else {
+        v = ldexp((double)(1024 + f), e - 25);     /* (1 + f/2^10) * 2^(e-15) */
+    }
+    return sign ? -v : v;
+}
+
+/* bfloat16: the upper half of an IEEE binary32 -- sign bit 15, 8-bit exponent
+ * (bias 127), 7-bit fraction. */
+static double widen_bfloat16(uint16_t h) {
+    int sign = (h >> 15) & 1;
+    int e = (h >> 7) & 0xFF;
+    int f = h & 0x7F;
+    double v;
+    if (e == 0) {
+        v = ldexp((double)f, -133);                /* subnormal: f * 2^-126 * 2^-7 */
+    } else if (e == 255) {
+        v = (f == 0) ? INFINITY : NAN;
+    } else {
+        v = ldexp((double)(128 + f), e - 134);     /* (1 + f/2^7) * 2^(e-127) */
+    }
+    return sign ? -v : v;
+}
+
+double oracle_widen(uint16_t bits, int in_kind) {
+    return in_kind == ORACLE_IN_BF16 ? widen_bfloat16(bits) : widen_binary16(bits);
+}
+
+/* A 65536-entry table of the decoded values, so the inner loop reads doubles. */
+static double* make_table(int in_kind) {
+    double* t = (double*)malloc(sizeof(double) * 65536);
+    if (!t) return NULL;
+    for (uint32_t b = 0; b < 65536; ++b) t[b] = oracle_widen((uint16_t)b, in_kind);
+    return t;
+}
+
+static void set_threads(int nthreads) {
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#else
+    (void)nthreads;
+#endif
+}
+
+int oracle_max_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/*
+ * Rows `rows[0..nrows)` of C and S (each nrows x N, row-major).  rows == NULL
+ * means every row 0..M-1 (then nrows must equal M).  S may be NULL.
+ * Returns 0 on success, -1 on a bad argument or allocation failure.
+ */
+int oracle_gemm_rows_f64(int64_t M, int64_t N, int64_t K,
+                         const uint16_t* A, const uint16_t* B, int in_kind,
+                         const int64_t* rows, int64_t nrows,
+                         double* C, double* S, int nthreads) {
+    if (M < 0 || N < 0 || K < 0 || nrows < 0) return -1;
+    if (in_kind != ORACLE_IN_F16 && in_kind != ORACLE_IN_BF16) return -1;
+    if (rows == NULL && nrows != M) return -1;
+    if (rows != NULL) {
+        for (int64_t r = 0; r < nrows; ++r)
+            if (rows[r] < 0 || rows[r] >= M) return -1;
+    }
+    double* tab = make_table(in_kind);
+    if (!tab) return -1;
+    set_threads(nthreads);
+
+    int64_t r;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (r = 0; r < nrows; ++r) {
+        int64_t i = rows ? rows[r] : r;
+        const uint16_t* a = A + i * K;
+        for (int64_t j = 0; j < N; ++j) {
+            const uint16_t* b = B + j * K;
+            double acc = 0.0;
+            double sabs = 0.0;
+            for (int64_t k = 0; k < K; ++k) {
+                double p = tab[a[k]] * tab[b[k]];   /* exact */
+                acc += p;
+                sabs += fabs(p);
+            }
+            C[r * N + j] = acc;
+            if (S) S[r * N + j] = sabs;
+        }
+    }
+    free(tab);
+    return 0;
+}
+
+/* The whole M x N result. */
+int oracle_gemm_f64(int64_t M, int64_t N, int64_t K,
+                    const uint16_t* A, const uint16_t* B, int in_kind,
+                    double* C, double* S, int nthreads) {
+    return oracle_gemm_rows_f64(M, N, K, A, B, in_kind, NULL, M, C, S, nthreads);
+}

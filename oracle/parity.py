@@ -1,0 +1,73 @@
+"""Acceptance rule for comparing a GPU result with the oracle -- TEST INFRASTRUCTURE.
+
+Per element, with ``ref`` and ``S = sum_k |a_ik b_jk|`` from the oracle (fp64):
+
+  * fp32 output:  |c - ref| <= 2^-10 * S
+  * bf16 output:  |c - ref| <= 2^-10 * S + half_ulp_bf16(|ref|)
+  * any NaN / Inf in c fails (the inputs are finite by construction).
+
+``2^-10 * S`` covers an fp32 accumulation of fp16/bf16 products in any order
+(the Tensor Core's internal order is unspecified), with a wide margin: a
+sequential fp32 sum errs by at most about K * 2^-24 * S.  ``half_ulp_bf16`` is
+the last rounding of the fp32 accumulator to bf16 (round to nearest even):
+for |ref| > 0 with |ref| = m * 2^e, 0.5 <= m < 1 (frexp), bf16's 8-bit
+significand gives ulp 2^(e-8) and half an ulp 2^(e-9); for ref == 0 it is 0,
+so an all-zero row (S == 0) must come back as exact zeros.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+TOL_REL = 2.0 ** -10
+
+
+def half_ulp_bf16(ref: np.ndarray) -> np.ndarray:
+    ref = np.abs(np.asarray(ref, dtype=np.float64))
+    _, e = np.frexp(ref)
+    h = np.ldexp(np.ones_like(ref), e.astype(np.int64) - 9)
+    return np.where(ref > 0, h, 0.0)
+
+
+def bound(ref: np.ndarray, S: np.ndarray, out_dtype: str) -> np.ndarray:
+    b = TOL_REL * np.asarray(S, dtype=np.float64)
+    if out_dtype == "bf16":
+        b = b + half_ulp_bf16(ref)
+    elif out_dtype != "f32":
+        raise ValueError(out_dtype)
+    return b
+
+
+def check(c, ref: np.ndarray, S: np.ndarray, out_dtype: str) -> dict:
+    """Compare ``c`` (anything convertible to float64) with the oracle.
+
+    Returns a dict with ``ok`` plus diagnostics: the worst ratio
+    |c-ref| / bound, the count of violations, and the max / RMS of
+    |c-ref| / S (which should stay far below 2^-10).
+    """
+    c = np.asarray(c, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    S = np.asarray(S, dtype=np.float64)
+    if c.shape != ref.shape or S.shape != ref.shape:
+        raise ValueError("shape mismatch %s %s %s" % (c.shape, ref.shape, S.shape))
+    finite = np.isfinite(c)
+    err = np.abs(c - ref)
+    b = bound(ref, S, out_dtype)
+    bad = ~finite | (err > b)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        ratio = np.where(b > 0, err / b, np.where(err > 0, np.inf, 0.0))
+        rel = np.where(S > 0, err / S, np.where(err > 0, np.inf, 0.0))
+    n = max(1, rel.size)
+    out = {
+        "ok": bool(not bad.any()),
+        "n": int(c.size),
+        "violations": int(bad.sum()),
+        "nonfinite": int((~finite).sum()),
+        "worst_ratio": float(np.max(ratio)) if ratio.size else 0.0,
+        "max_rel": float(np.max(rel)) if rel.size else 0.0,
+        "rms_rel": float(np.sqrt(np.sum(np.where(np.isfinite(rel), rel, 0.0) ** 2) / n)),
+    }
+    if bad.any():
+        idx = np.argwhere(bad)[0]
+        out["first_bad"] = {"index": [int(i) for i in idx], "c": float(c[tuple(idx)]),
+                            "ref": float(ref[tuple(idx)]), "S": float(S[tuple(idx)])}
+    return out
