@@ -1,0 +1,416 @@
+"""Throughput of the dense GEMM C = A * B^T (and the decode GEMV) on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--no-extra] [--no-cpu-baseline]
+
+One step is one C = A * B^T over the workload's seeded synthetic operands,
+already resident in HBM: one launch of the planned kernel.  The default
+workload is the 8192^3 bf16 -> bf16 GEMM.  Prints ONE JSON line (rank 0).
+
+--impl reference times the CPU oracle (plain fp64 triple loop, OpenMP over
+rows) on a bounded row sample of the same workload, in the same metric.
+
+Multi-GPU (torchrun): every rank runs its own replica of the workload on its
+own GPU (the output tiles are independent; there is no data exchange), the
+timed region is bracketed by a barrier and device synchronisation, the
+maximum elapsed time over ranks is taken, and the value counts the work of
+all ranks (weak scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from dense_gemm_blackwell_sm_gb300 import inputs, roofline  # noqa: E402
+
+METRIC = "GEMM TFLOP/s (and % of dense peak) at 4096³/8192³ bf16; GEMV GB/s"
+DEFAULT_WORKLOAD = "large_8192_bf16_bf16"
+STATED_PEAK_TFLOPS = 2000.0   # the pages' B200 FP16 figure, used as the stated target
+STATED_HBM_GBS = 8000.0
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+# source files whose change invalidates a stored ncu traffic figure
+KERNEL_SOURCES = {
+    "ws": ["dense_gemm_blackwell_sm_gb300/csrc/kernels_ws.cu", "dense_gemm_blackwell_sm_gb300/csrc/ptx.cuh",
+           "dense_gemm_blackwell_sm_gb300/csrc/kernel_common.cuh"],
+    "gemv": ["dense_gemm_blackwell_sm_gb300/csrc/kernel_gemv.cu",
+             "dense_gemm_blackwell_sm_gb300/csrc/kernel_common.cuh"],
+}
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.json")
+
+
+# ---------------------------------------------------------------------------
+# host helpers (importable without a GPU)
+
+def measured_peaks() -> tuple[dict, str]:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return json.load(f), "measured"
+    return dict(FALLBACK), "fallback"
+
+
+def source_hash(kind: str) -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES[kind]:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def stored_traffic(kind: str, workload: str):
+    """DRAM bytes per launch from a committed ncu capture, if the kernel is unchanged."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            d = json.load(f)
+        e = d.get(kind, {}).get(workload)
+        if e and e.get("source_hash") == source_hash(kind):
+            return float(e["dram_bytes_per_launch"])
+    except (OSError, ValueError, KeyError):
+        pass
+    return None
+
+
+def aggregate(per_rank_seconds: list[float], units_per_rank: float) -> tuple[float, float]:
+    """(max elapsed over ranks, whole-job units per second)."""
+    t = max(per_rank_seconds)
+    return t, units_per_rank * len(per_rank_seconds) / t
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled while the timed region runs."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines: list[str] = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.QUERY,
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        return False
+
+    def summary(self) -> dict:
+        mhz, maxs, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                mhz.append(float(f[1]))
+                maxs.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not mhz:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        mhz.sort()
+        return {"sm_mhz": mhz[len(mhz) // 2], "sm_max_mhz": max(maxs), "reasons": sorted(reasons),
+                "samples": len(mhz)}
+
+
+# ---------------------------------------------------------------------------
+# GPU timing
+
+def _events_time(fn, steps: int, stream) -> float:
+    """Seconds for `steps` calls of fn(i) on `stream`, CUDA events on that stream."""
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for i in range(steps):
+        fn(i)
+    end.record(stream)
+    end.synchronize()
+    return start.elapsed_time(end) / 1e3
+
+
+def bench_gemm(w: inputs.Workload, steps: int, warmup: int, dev, dist_barrier, variant: int = 0) -> dict:
+    from dense_gemm_blackwell_sm_gb300 import gemm
+    code = gemm.dtype_code(w.in_dtype, w.out_dtype)
+    a, b = inputs.workload_operands(w)
+    sets = []
+    for s in range(2):   # two operand sets, alternated: inputs are also larger than L2
+        sets.append((a.to(dev), b.to(dev), torch.empty((w.M, w.N), device=dev, dtype=inputs.torch_dtype(w.out_dtype))))
+    plan = gemm.Plan(w.M, w.N, w.K, code, gemm.make_opts(variant=variant))
+    stream = torch.cuda.current_stream(dev)
+    sp = stream.cuda_stream
+    ptrs = [(x.data_ptr(), y.data_ptr(), z.data_ptr()) for x, y, z in sets]
+
+    def step(i):
+        pa, pb, pc = ptrs[i & 1]
+        st = plan.run_ptr(pa, pb, pc, sp)
+        if st != 0:
+            raise gemm.GemmError(st, "gemm_plan_run")
+
+    for i in range(warmup):
+        step(i)
+    torch.cuda.synchronize(dev)
+    assert plan.check() == gemm.OK
+    dist_barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(dev.index if dev.index is not None else 0) as clk:
+        secs = _events_time(step, steps, stream)
+    torch.cuda.synchronize(dev)
+    dist_barrier()
+    st = plan.check()
+    if st != gemm.OK:
+        raise gemm.GemmError(st, "device status after the timed region")
+    info = plan.info()
+    plan.destroy()
+    del sets
+    return {"seconds": secs, "per_launch_s": secs / steps, "clocks": clk.summary(), "info": info}
+
+
+def bench_gemm_e2e(w: inputs.Workload, steps: int, dev) -> dict:
+    """The same GEMM through gemm_run_host: pinned host operands in, host result out."""
+    from dense_gemm_blackwell_sm_gb300 import gemm
+    code = gemm.dtype_code(w.in_dtype, w.out_dtype)
+    a, b = inputs.workload_operands(w)
+    ah, bh = a.pin_memory(), b.pin_memory()
+    ch = torch.empty((w.M, w.N), dtype=inputs.torch_dtype(w.out_dtype)).pin_memory()
+    da, db = torch.empty_like(a, device=dev), torch.empty_like(b, device=dev)
+    dc = torch.empty((w.M, w.N), device=dev, dtype=inputs.torch_dtype(w.out_dtype))
+    sp = torch.cuda.current_stream(dev).cuda_stream
+
+    def once():
+        st = gemm.gemm_run_host(w.M, w.N, w.K, ah.data_ptr(), bh.data_ptr(), ch.data_ptr(), code,
+                                da.data_ptr(), db.data_ptr(), dc.data_ptr(), sp)
+        if st != 0:
+            raise gemm.GemmError(st, "gemm_run_host")
+
+    once()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        once()   # synchronises the stream itself
+    secs = time.perf_counter() - t0
+    ob = 4 if w.out_dtype == "f32" else 2
+    return {"seconds": secs, "steps": steps, "h2d": 2 * (w.M * w.K + w.N * w.K), "d2h": ob * w.M * w.N}
+
+
+def bench_gemv(w: inputs.Workload, steps: int, warmup: int, dev) -> dict:
+    """GB/s of the decode GEMV; the weight rotates over enough copies to exceed 4x L2."""
+    from dense_gemm_blackwell_sm_gb300 import gemm
+    code = gemm.dtype_code(w.in_dtype, w.out_dtype)
+    x, b = inputs.workload_operands(w)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    wbytes = b.numel() * 2
+    copies = max(2, int((4 * l2 + wbytes - 1) // wbytes))
+    xs = x.to(dev)
+    bs = [b.to(dev) for _ in range(copies)]
+    ys = [torch.empty((w.M, w.N), device=dev, dtype=inputs.torch_dtype(w.out_dtype)) for _ in range(copies)]
+    plan = gemm.Plan(w.M, w.N, w.K, code, gemm.make_opts(variant=gemm.GEMV))
+    sp = torch.cuda.current_stream(dev).cuda_stream
+    ptrs = [(xs.data_ptr(), bb.data_ptr(), yy.data_ptr()) for bb, yy in zip(bs, ys)]
+
+    def step(i):
+        pa, pb, pc = ptrs[i % copies]
+        plan.run_ptr(pa, pb, pc, sp)
+
+    for i in range(warmup):
+        step(i)
+    torch.cuda.synchronize(dev)
+    secs = _events_time(step, steps, torch.cuda.current_stream(dev))
+    assert plan.check() == gemm.OK
+    plan.destroy()
+    nbytes = roofline.gemm_bytes(w.M, w.N, w.K, 2, 4 if w.out_dtype == "f32" else 2)
+    return {"gbs": nbytes * steps / secs / 1e9, "us_per_launch": secs / steps * 1e6, "copies": copies,
+            "bytes_per_launch": nbytes}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (a reported baseline, not the target)
+
+def cpu_oracle_rate(w: inputs.Workload, budget_s: float = 12.0) -> dict:
+    import numpy as np
+    import oracle
+    oracle.build()
+    a, b = inputs.workload_operands(w)
+    threads = oracle.max_threads()
+    rng = np.random.default_rng(0)
+    rows_done, t_spent, batch = 0, 0.0, max(1, threads)
+    while t_spent < budget_s and rows_done < w.M:
+        rows = rng.choice(w.M, size=min(batch, w.M - rows_done), replace=False)
+        t0 = time.perf_counter()
+        oracle.gemm_rows(a, b, rows, nthreads=threads)
+        t_spent += time.perf_counter() - t0
+        rows_done += len(rows)
+        if t_spent < budget_s / 4:
+            batch *= 2
+    flops = 2.0 * rows_done * w.N * w.K
+    return {"tflops": flops / t_spent / 1e12, "rows": rows_done, "seconds": t_spent, "threads": threads,
+            "sample": "%d of %d rows of C (all %d columns, K=%d), seeded random rows, fp64 oracle on %d host "
+                      "threads; rate extrapolates linearly to the full %dx%dx%d product" % (
+                          rows_done, w.M, w.N, w.K, threads, w.M, w.N, w.K)}
+
+
+# ---------------------------------------------------------------------------
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if ws <= 1:
+        return 0, 1, 0, (lambda: None), (lambda xs: xs)
+    import torch.distributed as dist
+    rank = int(os.environ["RANK"])
+    local = int(os.environ.get("LOCAL_RANK", rank))
+    backend = "nccl" if torch.cuda.is_available() else "gloo"
+    if torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    dist.init_process_group(backend)
+
+    def barrier():
+        dist.barrier()
+
+    def gather(x: float):
+        t = torch.tensor([x], dtype=torch.float64, device="cuda" if backend == "nccl" else "cpu")
+        out = [torch.zeros_like(t) for _ in range(ws)]
+        dist.all_gather(out, t)
+        return [float(o.item()) for o in out]
+    return rank, ws, local, barrier, gather
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(inputs.WORKLOADS))
+    ap.add_argument("--variant", type=int, default=0)
+    ap.add_argument("--no-extra", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("at least 3 warm-up steps")
+    w = inputs.WORKLOADS[args.workload]
+    rank, world, local, barrier, gather = _dist()
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        per_step = max(1.0, 60.0 / max(1, args.steps + args.warmup))
+        r = cpu_oracle_rate(w, budget_s=min(12.0, per_step * args.steps))
+        line = {"impl": "reference", "metric": METRIC, "value": round(r["tflops"], 6), "unit": "TFLOP/s",
+                "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": None, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "f64", "data": "synthetic",
+                "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "in": w.in_dtype, "out": w.out_dtype},
+                "cpu_baseline": {"value": round(r["tflops"], 6), "unit": "TFLOP/s", "cores": r["threads"],
+                                 "kind": "oracle", "sample": r["sample"]},
+                "e2e": {"value": round(r["tflops"], 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return 0
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    import __graft_entry__
+    __graft_entry__.build()
+
+    res = bench_gemm(w, args.steps, args.warmup, dev, barrier, args.variant)
+    times = gather(res["seconds"])
+    tmax, flops_per_s = aggregate(times, w.flops * args.steps)
+    tflops = flops_per_s / 1e12
+    per_launch = res["per_launch_s"]
+
+    peaks, peak_src = measured_peaks()
+    long_region = res["seconds"] > 2.0
+    peak_key = "bf16_tflops_sustained" if long_region else "bf16_tflops"
+    # fp16 and bf16 run at the same dense Tensor Core rate
+    peak = float(peaks.get(peak_key, FALLBACK[peak_key]))
+    achieved = w.flops / per_launch / 1e12
+    line = {
+        "metric": METRIC, "value": round(tflops, 3), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(tmax / args.steps * 1e3, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": w.in_dtype, "data": "synthetic",
+        "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "in": w.in_dtype, "out": w.out_dtype,
+                   "variant": res["info"]["variant_name"], "tile": [res["info"]["tile_m"], res["info"]["tile_n"]],
+                   "cluster": res["info"]["cluster"], "stages": res["info"]["stages"],
+                   "grid": res["info"]["grid"], "sched": res["info"]["sched"],
+                   "l2": "inputs larger than L2 (A+B+C = %d MB), two operand sets alternated" % (
+                       w.algorithmic_bytes // 2**20),
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 3), "peak": peak, "unit": "TFLOP/s",
+                     "frac": round(achieved / peak, 4), "traffic": stored_traffic("ws", w.name),
+                     "peak_source": "%s %s" % (peak_key, peak_src),
+                     "frac_of_stated_2000": round(achieved / STATED_PEAK_TFLOPS, 4)},
+        "clocks": res["clocks"],
+        "gpu_launches": args.steps,
+    }
+    if rank == 0 and not args.no_e2e:
+        e = bench_gemm_e2e(w, max(3, min(10, args.steps // 20)), dev)
+        line["e2e"] = {"value": round(w.flops * e["steps"] / e["seconds"] / 1e12, 3), "unit": "TFLOP/s",
+                       "h2d_bytes_per_step": e["h2d"], "d2h_bytes_per_step": e["d2h"]}
+    if rank == 0 and not args.no_extra:
+        also = {}
+        w3 = inputs.WORKLOADS["square_4096_f16_f32"]
+        r3 = bench_gemm(w3, 200, 10, dev, lambda: None)
+        also[w3.name] = {"tflops": round(w3.flops / r3["per_launch_s"] / 1e12, 3),
+                         "frac_of_measured": round(w3.flops / r3["per_launch_s"] / 1e12 / float(peaks.get("bf16_tflops", 1900.0)), 4),
+                         "variant": r3["info"]["variant_name"]}
+        w4 = inputs.WORKLOADS["llm_proj_8192x14336x4096_bf16_bf16"]
+        r4 = bench_gemm(w4, 50, 5, dev, lambda: None)
+        also[w4.name] = {"tflops": round(w4.flops / r4["per_launch_s"] / 1e12, 3),
+                         "variant": r4["info"]["variant_name"]}
+        hbm = float(peaks.get("hbm_gbs", FALLBACK["hbm_gbs"]))
+        for name in ("gemv_m1_n4096_k4096_bf16", "gemv_m8_n4096_k4096_bf16",
+                     "gemv_m1_n14336_k4096_bf16", "gemv_m8_n14336_k4096_bf16"):
+            g = bench_gemv(inputs.WORKLOADS[name], 400, 20, dev)
+            also[name] = {"gbs": round(g["gbs"], 1), "frac_of_measured_hbm": round(g["gbs"] / hbm, 4),
+                          "frac_of_stated_8000": round(g["gbs"] / STATED_HBM_GBS, 4),
+                          "us_per_launch": round(g["us_per_launch"], 2), "weight_copies": g["copies"],
+                          "traffic": stored_traffic("gemv", name)}
+        line["also"] = also
+    if rank == 0 and not args.no_cpu_baseline:
+        r = cpu_oracle_rate(w)
+        line["cpu_baseline"] = {"value": round(r["tflops"], 6), "unit": "TFLOP/s", "cores": r["threads"],
+                                "kind": "oracle", "sample": r["sample"]}
+    if rank == 0:
+        print(json.dumps(line))
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

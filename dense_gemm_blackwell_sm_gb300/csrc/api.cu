@@ -1,0 +1,473 @@
+// api.cu -- the C ABI (include/gemm.h): argument validation, the planner that
+// picks a kernel variant / tile / ring depth / raster / launch size, TMA
+// descriptor encoding and caching, launches, and device-status checks.
+#include <algorithm>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <new>
+#include <tuple>
+
+#include <cudaTypedefs.h>
+
+#include "gemm.h"
+#include "kernel_common.cuh"
+#include "launch.h"
+
+using namespace dgb;
+
+struct gemm_plan_s {
+  int64_t M, N, K;
+  gemm_dtype_t dtype;
+  bool in_bf16, out_f32;
+  int variant, sched, stages, raster_group;
+  int device, num_sms;
+  int grid_units;  // CTAs (variants 3-6) or clusters (7-9) launched
+  int cg, consumers;
+  int tile_m, tile_n, tiles_m, tiles_n;
+  size_t smem;
+  uint64_t timeout_ns;
+  uint32_t debug_flags;
+  uint32_t* scratch;  // [0] status word, [1] tile counter, [2] finished counter
+  int32_t* visits;
+  const void* mapA;
+  const void* mapB;
+  void* mapC;
+  bool maps_valid;
+  CUtensorMap tmA, tmB, tmC;
+};
+
+namespace {
+
+constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
+constexpr int64_t kMaxDim = (int64_t)1 << 31;
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+bool encode_fn_ready() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode != nullptr;
+}
+
+// 2-D row-major tensor [outer][inner], tiles of box_outer x box_inner elements
+// landing in SMEM with the 128-byte swizzle; out-of-range elements read as 0.
+bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, int esize, const void* ptr, uint64_t inner,
+               uint64_t outer, uint32_t box_inner, uint32_t box_outer) {
+  if (!encode_fn_ready()) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {inner * (uint64_t)esize};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(m, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// tcgen05 instruction descriptor, kind::f16: fp32 accumulator, A and B both
+// fp16 or both bf16, both K-major, MMA shape M x N
+uint32_t make_idesc(bool bf16, int M, int N) {
+  const uint32_t ab = bf16 ? 1u : 0u;
+  return (1u << 4)                      // D format: f32
+         | (ab << 7) | (ab << 10)       // A / B format
+         | ((uint32_t)(N >> 3) << 17)   // N / 8
+         | ((uint32_t)(M >> 4) << 24);  // M / 16
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int out_bytes(gemm_dtype_t dt) { return (dt == GEMM_F16_F32 || dt == GEMM_BF16_F32) ? 4 : 2; }
+
+// The TMA-store writeback of variants 7-9 needs rows of C to start 16-byte aligned.
+bool c_rows_tma_ok(int64_t N, gemm_dtype_t dt) { return (N * out_bytes(dt)) % 16 == 0; }
+
+gemm_status_t validate_sizes(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype) {
+  if ((int)dtype < 0 || (int)dtype > 3) return GEMM_ERR_UNSUPPORTED_DTYPE;
+  if (M < 1 || N < 1 || K < 1 || M >= kMaxDim || N >= kMaxDim || K >= kMaxDim) return GEMM_ERR_INVALID_ARG;
+  if (K % 8 != 0) return GEMM_ERR_UNSUPPORTED_SHAPE;
+  return GEMM_OK;
+}
+
+gemm_status_t current_device(int* dev, int* sms) {
+  int n = 0;
+  if (cudaGetDeviceCount(&n) != cudaSuccess || n < 1) {
+    cudaGetLastError();
+    return GEMM_ERR_NO_DEVICE;
+  }
+  if (cudaGetDevice(dev) != cudaSuccess) return GEMM_ERR_CUDA;
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, *dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, *dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, *dev) != cudaSuccess)
+    return GEMM_ERR_CUDA;
+  if (major != 10 || minor != 3) return GEMM_ERR_ARCH;
+  return GEMM_OK;
+}
+
+int ceil_div(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }
+
+// Automatic variant: the decode GEMV for a handful of rows, otherwise the
+// CTA-pair kernel, or the plain-store persistent kernel when C's rows are not
+// 16-byte aligned for TMA stores.
+int auto_variant(int64_t M, int64_t N, int64_t K, gemm_dtype_t dt) {
+  if (M <= 16 && gemv_smem_bytes((int)M, (int)K) <= 200 * 1024) return GEMM_VARIANT_GEMV;
+  if (!c_rows_tma_ok(N, dt)) return GEMM_VARIANT_S6_PERSISTENT;
+  return GEMM_VARIANT_S8_CTA_PAIR;
+}
+
+gemm_status_t build_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, const gemm_opts_t* opts,
+                         gemm_plan_s** out) {
+  gemm_status_t st = validate_sizes(M, N, K, dtype);
+  if (st != GEMM_OK) return st;
+  gemm_opts_t o{};
+  if (opts) o = *opts;
+  if (o.variant < 0 || o.variant > GEMM_VARIANT_GEMV || o.sched < 0 || o.sched > GEMM_SCHED_CLC ||
+      o.stages < 0 || o.stages > 8 || o.raster_group < 0 || o.max_ctas < 0 || o.timeout_ns < 0)
+    return GEMM_ERR_INVALID_ARG;
+
+  int variant = o.variant ? o.variant : auto_variant(M, N, K, dtype);
+  // shape limits of the individual steps
+  if (variant == GEMM_VARIANT_S1_SINGLE_TILE && (M > 128 || N > 128 || K > 64)) return GEMM_ERR_UNSUPPORTED_SHAPE;
+  if (variant == GEMM_VARIANT_S2_KLOOP && (M > 128 || N > 128)) return GEMM_ERR_UNSUPPORTED_SHAPE;
+  if (variant >= GEMM_VARIANT_S7_WARP_SPECIALIZED && variant <= GEMM_VARIANT_S9_TWO_CONSUMERS &&
+      !c_rows_tma_ok(N, dtype))
+    return GEMM_ERR_UNSUPPORTED_SHAPE;
+  if (variant == GEMM_VARIANT_GEMV && (M > 16 || gemv_smem_bytes((int)M, (int)K) > 200 * 1024))
+    return GEMM_ERR_UNSUPPORTED_SHAPE;
+
+  int dev = 0, sms = 0;
+  st = current_device(&dev, &sms);
+  if (st != GEMM_OK) return st;
+
+  gemm_plan_s* p = new (std::nothrow) gemm_plan_s();
+  if (!p) return GEMM_ERR_OOM;
+  p->M = M;
+  p->N = N;
+  p->K = K;
+  p->dtype = dtype;
+  p->in_bf16 = (dtype == GEMM_BF16_F32 || dtype == GEMM_BF16_BF16);
+  p->out_f32 = (out_bytes(dtype) == 4);
+  p->variant = variant;
+  p->device = dev;
+  p->num_sms = sms;
+  p->timeout_ns = o.timeout_ns ? (uint64_t)o.timeout_ns : kDefaultTimeoutNs;
+  p->debug_flags = (uint32_t)o.debug_flags;
+  p->cg = 1;
+  p->consumers = 1;
+  p->sched = 0;
+  p->stages = 1;
+  p->raster_group = 1;
+  p->smem = 0;
+  p->tile_m = 128;
+  p->tile_n = 128;
+
+  const bool persistent = variant >= GEMM_VARIANT_S6_PERSISTENT && variant <= GEMM_VARIANT_S9_TWO_CONSUMERS;
+  if (persistent) p->sched = o.sched ? o.sched : GEMM_SCHED_STATIC;
+
+  if (variant == GEMM_VARIANT_S5_PIPELINE || variant == GEMM_VARIANT_S6_PERSISTENT) {
+    p->stages = o.stages ? o.stages : (variant == GEMM_VARIANT_S5_PIPELINE ? 2 : 4);
+    if (p->stages > 6) p->stages = 6;
+  }
+  if (variant >= GEMM_VARIANT_S7_WARP_SPECIALIZED && variant <= GEMM_VARIANT_S9_TWO_CONSUMERS) {
+    p->cg = (variant == GEMM_VARIANT_S7_WARP_SPECIALIZED) ? 1 : 2;
+    p->consumers = (variant == GEMM_VARIANT_S9_TWO_CONSUMERS) ? 2 : 1;
+    const WsShape sh = ws_shape(p->cg, p->consumers);
+    const int maxs = ws_max_stages(p->cg, p->consumers);
+    p->stages = o.stages ? std::min<int>(o.stages, maxs) : maxs;
+    p->tile_m = sh.tile_m;
+    p->tile_n = sh.tile_n;
+    p->smem = ws_smem_bytes(p->cg, p->consumers, p->stages);
+  } else if (variant == GEMM_VARIANT_S6_PERSISTENT) {
+    p->smem = step6_smem_bytes(p->stages);
+  }
+  p->tiles_m = ceil_div(M, p->tile_m);
+  p->tiles_n = ceil_div(N, p->tile_n);
+  if (persistent) p->raster_group = o.raster_group ? o.raster_group : std::min(8, p->tiles_m);
+  if (p->raster_group > p->tiles_m) p->raster_group = p->tiles_m;
+  if (p->raster_group < 1) p->raster_group = 1;
+
+  const int tiles = p->tiles_m * p->tiles_n;
+  if (variant == GEMM_VARIANT_S6_PERSISTENT) {
+    int units = (p->sched == GEMM_SCHED_CLC) ? tiles : std::min(tiles, sms);
+    if (o.max_ctas && p->sched != GEMM_SCHED_CLC) units = std::min(units, (int)o.max_ctas);
+    p->grid_units = units;
+  } else if (variant >= GEMM_VARIANT_S7_WARP_SPECIALIZED && variant <= GEMM_VARIANT_S9_TWO_CONSUMERS) {
+    int active = ws_max_active_clusters(p->cg, p->consumers, p->sched - 1, p->out_f32, p->stages);
+    if (active < 1) active = std::max(1, sms / p->cg);
+    int units = (p->sched == GEMM_SCHED_CLC) ? tiles : std::min(tiles, active);
+    if (o.max_ctas && p->sched != GEMM_SCHED_CLC) units = std::max(1, std::min(units, (int)o.max_ctas));
+    p->grid_units = units;
+  } else {
+    p->grid_units = tiles;
+  }
+
+  if (cudaMalloc(reinterpret_cast<void**>(&p->scratch), 256) != cudaSuccess) {
+    cudaGetLastError();
+    delete p;
+    return GEMM_ERR_OOM;
+  }
+  if (cudaMemset(p->scratch, 0, 256) != cudaSuccess) {
+    cudaFree(p->scratch);
+    delete p;
+    return GEMM_ERR_CUDA;
+  }
+  *out = p;
+  return GEMM_OK;
+}
+
+gemm_status_t refresh_maps(gemm_plan_s* p, const void* A, const void* B, void* C) {
+  if (p->maps_valid && p->mapA == A && p->mapB == B && p->mapC == C) return GEMM_OK;
+  const CUtensorMapDataType in_t = p->in_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  uint32_t a_rows = 128, b_rows = 128;
+  if (p->variant >= GEMM_VARIANT_S7_WARP_SPECIALIZED && p->variant <= GEMM_VARIANT_S9_TWO_CONSUMERS) {
+    const WsShape sh = ws_shape(p->cg, p->consumers);
+    a_rows = (uint32_t)sh.a_box_rows;
+    b_rows = (uint32_t)sh.b_box_rows;
+  }
+  if (!encode_2d(&p->tmA, in_t, 2, A, (uint64_t)p->K, (uint64_t)p->M, 64, a_rows) ||
+      !encode_2d(&p->tmB, in_t, 2, B, (uint64_t)p->K, (uint64_t)p->N, 64, b_rows))
+    return GEMM_ERR_CUDA;
+  if (p->variant >= GEMM_VARIANT_S7_WARP_SPECIALIZED && p->variant <= GEMM_VARIANT_S9_TWO_CONSUMERS) {
+    const bool ok = p->out_f32
+                        ? encode_2d(&p->tmC, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, C, (uint64_t)p->N,
+                                    (uint64_t)p->M, 32, 32)
+                        : encode_2d(&p->tmC, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, C, (uint64_t)p->N,
+                                    (uint64_t)p->M, 64, 32);
+    if (!ok) return GEMM_ERR_CUDA;
+  }
+  p->mapA = A;
+  p->mapB = B;
+  p->mapC = C;
+  p->maps_valid = true;
+  return GEMM_OK;
+}
+
+gemm_status_t launch_plan(gemm_plan_s* p, const void* A, const void* B, void* C, cudaStream_t s) {
+  if (!A || !B || !C) return GEMM_ERR_INVALID_ARG;
+  if (!aligned16(A) || !aligned16(B) || !aligned16(C)) return GEMM_ERR_MISALIGNED;
+  int cur = -1;
+  if (cudaGetDevice(&cur) != cudaSuccess) return GEMM_ERR_CUDA;
+  if (cur != p->device) return GEMM_ERR_INVALID_ARG;
+  cudaError_t e = cudaSuccess;
+
+  if (p->variant == GEMM_VARIANT_GEMV) {
+    GemvParams g{A, B, C, (int32_t)p->M, (int32_t)p->N, (int32_t)p->K};
+    e = launch_gemv(g, p->in_bf16, p->out_f32, p->num_sms, s);
+    return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+  }
+
+  KParams k{};
+  k.M = (int32_t)p->M;
+  k.N = (int32_t)p->N;
+  k.K = (int32_t)p->K;
+  k.tiles_m = p->tiles_m;
+  k.tiles_n = p->tiles_n;
+  k.raster_group = p->raster_group;
+  k.stages = p->stages;
+  k.status = p->scratch;
+  k.visits = p->visits;
+  k.timeout_ns = p->timeout_ns;
+  k.debug_flags = p->debug_flags;
+  k.out_ld = (int32_t)p->N;
+  k.A = static_cast<const uint16_t*>(A);
+  k.B = static_cast<const uint16_t*>(B);
+  k.C = C;
+
+  if (p->variant <= GEMM_VARIANT_S3_MULTI_CTA) {
+    k.idesc = make_idesc(p->in_bf16, 128, 128);
+    e = launch_step123(k, p->out_f32, s);
+  } else {
+    gemm_status_t st = refresh_maps(p, A, B, C);
+    if (st != GEMM_OK) return st;
+    if (p->variant <= GEMM_VARIANT_S5_PIPELINE) {
+      k.idesc = make_idesc(p->in_bf16, 128, 128);
+      e = launch_step45(k, p->tmA, p->tmB, p->out_f32, s);
+    } else if (p->variant == GEMM_VARIANT_S6_PERSISTENT) {
+      k.idesc = make_idesc(p->in_bf16, 128, 128);
+      e = launch_step6(k, p->tmA, p->tmB, p->out_f32, p->sched - 1, p->grid_units, s);
+    } else {
+      k.idesc = make_idesc(p->in_bf16, 128 * p->cg, 256);
+      e = launch_ws(p->cg, p->consumers, p->sched - 1, k, p->tmA, p->tmB, p->tmC, p->out_f32, p->grid_units, s);
+    }
+  }
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return GEMM_ERR_CUDA;
+  }
+  return GEMM_OK;
+}
+
+gemm_status_t check_plan(gemm_plan_s* p) {
+  uint32_t word = 0;
+  if (cudaMemcpy(&word, p->scratch, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) {
+    cudaGetLastError();
+    return GEMM_ERR_CUDA;
+  }
+  if (word != 0) {
+    // rewind the status word and the scheduler counters for the next launch
+    cudaMemset(p->scratch, 0, 256);
+    return GEMM_ERR_DEVICE_TIMEOUT;
+  }
+  return GEMM_OK;
+}
+
+// plans made by gemm_run, keyed by shape, dtype and device
+std::mutex g_cache_mu;
+std::map<std::tuple<int64_t, int64_t, int64_t, int, int>, gemm_plan_s*> g_cache;
+
+}  // namespace
+
+extern "C" {
+
+gemm_status_t gemm_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, const gemm_opts_t* opts,
+                        gemm_plan_t* out) {
+  if (!out) return GEMM_ERR_INVALID_ARG;
+  *out = nullptr;
+  try {
+    return build_plan(M, N, K, dtype, opts, out);
+  } catch (...) {
+    return GEMM_ERR_OOM;
+  }
+}
+
+gemm_status_t gemm_plan_run(gemm_plan_t plan, const void* A, const void* B, void* C, gemm_stream_t stream) {
+  if (!plan) return GEMM_ERR_INVALID_ARG;
+  return launch_plan(plan, A, B, C, reinterpret_cast<cudaStream_t>(stream));
+}
+
+gemm_status_t gemm_run(int64_t M, int64_t N, int64_t K, const void* A, const void* B, void* C,
+                       gemm_dtype_t dtype, gemm_stream_t stream) {
+  gemm_status_t st = validate_sizes(M, N, K, dtype);
+  if (st != GEMM_OK) return st;
+  if (!A || !B || !C) return GEMM_ERR_INVALID_ARG;
+  if (!aligned16(A) || !aligned16(B) || !aligned16(C)) return GEMM_ERR_MISALIGNED;
+  int dev = 0;
+  {
+    int n = 0;
+    if (cudaGetDeviceCount(&n) != cudaSuccess || n < 1) {
+      cudaGetLastError();
+      return GEMM_ERR_NO_DEVICE;
+    }
+    if (cudaGetDevice(&dev) != cudaSuccess) return GEMM_ERR_CUDA;
+  }
+  gemm_plan_s* p = nullptr;
+  try {
+    std::lock_guard<std::mutex> lock(g_cache_mu);
+    auto key = std::make_tuple(M, N, K, (int)dtype, dev);
+    auto it = g_cache.find(key);
+    if (it != g_cache.end()) {
+      p = it->second;
+    } else {
+      st = build_plan(M, N, K, dtype, nullptr, &p);
+      if (st != GEMM_OK) return st;
+      g_cache[key] = p;
+    }
+  } catch (...) {
+    return GEMM_ERR_OOM;
+  }
+  return launch_plan(p, A, B, C, reinterpret_cast<cudaStream_t>(stream));
+}
+
+gemm_status_t gemm_run_host(int64_t M, int64_t N, int64_t K, const void* A_host, const void* B_host,
+                            void* C_host, gemm_dtype_t dtype, void* dA, void* dB, void* dC,
+                            gemm_stream_t stream) {
+  gemm_status_t st = validate_sizes(M, N, K, dtype);
+  if (st != GEMM_OK) return st;
+  if (!A_host || !B_host || !C_host || !dA || !dB || !dC) return GEMM_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(dA, A_host, (size_t)(M * K * 2), cudaMemcpyHostToDevice, s) != cudaSuccess ||
+      cudaMemcpyAsync(dB, B_host, (size_t)(N * K * 2), cudaMemcpyHostToDevice, s) != cudaSuccess) {
+    cudaGetLastError();
+    return GEMM_ERR_CUDA;
+  }
+  st = gemm_run(M, N, K, dA, dB, dC, dtype, stream);
+  if (st != GEMM_OK) return st;
+  if (cudaMemcpyAsync(C_host, dC, (size_t)(M * N * out_bytes(dtype)), cudaMemcpyDeviceToHost, s) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    return GEMM_ERR_CUDA;
+  }
+  return gemm_check(nullptr, stream);
+}
+
+gemm_status_t gemm_check(gemm_plan_t plan, gemm_stream_t stream) {
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    cudaGetLastError();
+    return GEMM_ERR_CUDA;
+  }
+  if (plan) return check_plan(plan);
+  std::lock_guard<std::mutex> lock(g_cache_mu);
+  gemm_status_t worst = GEMM_OK;
+  for (auto& kv : g_cache) {
+    gemm_status_t st = check_plan(kv.second);
+    if (st != GEMM_OK) worst = st;
+  }
+  return worst;
+}
+
+gemm_status_t gemm_plan_info(gemm_plan_t p, gemm_plan_info_t* info) {
+  if (!p || !info) return GEMM_ERR_INVALID_ARG;
+  std::memset(info, 0, sizeof(*info));
+  info->variant = p->variant;
+  info->sched = p->sched;
+  info->stages = p->stages;
+  info->raster_group = p->raster_group;
+  info->tile_m = p->tile_m;
+  info->tile_n = p->tile_n;
+  info->cluster = p->cg;
+  info->consumers = p->consumers;
+  info->grid = (p->variant >= GEMM_VARIANT_S7_WARP_SPECIALIZED && p->variant <= GEMM_VARIANT_S9_TWO_CONSUMERS)
+                   ? p->grid_units * p->cg
+                   : p->grid_units;
+  info->smem_bytes = (int32_t)p->smem;
+  info->num_sms = p->num_sms;
+  info->tiles = p->tiles_m * p->tiles_n;
+  return GEMM_OK;
+}
+
+gemm_status_t gemm_plan_set_visits(gemm_plan_t p, int32_t* visits) {
+  if (!p) return GEMM_ERR_INVALID_ARG;
+  p->visits = visits;
+  return GEMM_OK;
+}
+
+void gemm_plan_destroy(gemm_plan_t p) {
+  if (!p) return;
+  if (p->scratch) cudaFree(p->scratch);
+  delete p;
+}
+
+void gemm_clear_cache(void) {
+  std::lock_guard<std::mutex> lock(g_cache_mu);
+  for (auto& kv : g_cache) gemm_plan_destroy(kv.second);
+  g_cache.clear();
+}
+
+const char* gemm_status_string(gemm_status_t s) {
+  switch (s) {
+    case GEMM_OK: return "ok";
+    case GEMM_ERR_INVALID_ARG: return "invalid argument";
+    case GEMM_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+    case GEMM_ERR_MISALIGNED: return "operand not 16-byte aligned";
+    case GEMM_ERR_UNSUPPORTED_DTYPE: return "unsupported dtype";
+    case GEMM_ERR_ARCH: return "device is not compute capability 10.3 (sm_103a)";
+    case GEMM_ERR_CUDA: return "CUDA call failed";
+    case GEMM_ERR_OOM: return "out of memory";
+    case GEMM_ERR_DEVICE_TIMEOUT: return "a device-side wait timed out";
+    case GEMM_ERR_NO_DEVICE: return "no CUDA device";
+  }
+  return "unknown status";
+}
+
+const char* gemm_version(void) { return "dgb-gemm 0.1 (sm_103a)"; }
+
+}  // extern "C"

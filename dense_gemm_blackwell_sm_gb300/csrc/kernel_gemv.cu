@@ -1,0 +1,173 @@
+// kernel_gemv.cu -- the decode-shaped product Y (M x N) = X (M x K) * B^T for
+// M <= 16 on CUDA cores.
+//
+// The reading notes of "Modern GPU Programming for MLSys" (section
+// "Roofline：找到天花板") use the decode-stage 1 x 4096 x 4096 vector-matrix
+// product as the bandwidth-bound example: about one FLOP per byte, far below
+// the ridge point, so the Tensor Core is irrelevant and the kernel's only job
+// is to stream the weight B from HBM once at full bandwidth.  Design:
+//   * X (at most 16 rows) is staged once per CTA in shared memory;
+//   * each warp owns R whole rows of B at a time; every lane issues U 16-byte
+//     non-allocating loads per row before using any of them, so each SM keeps
+//     well over 64 KB of B in flight;
+//   * fp32 FMAs per lane, a shuffle reduction per output, one bf16/fp32 store;
+//   * the grid covers the rows exactly once (no atomics, no scratch memory).
+#include <algorithm>
+#include <type_traits>
+
+#include "kernel_common.cuh"
+#include "launch.h"
+
+namespace dgb {
+
+namespace {
+
+constexpr int GV_THREADS = 256;
+constexpr int GV_U = 8;  // 16-byte chunks per lane per row in flight
+
+__device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+template <typename InT>
+__device__ __forceinline__ float2 to_f2(uint32_t w) {
+  if constexpr (sizeof(InT) == 2 && std::is_same<InT, __nv_bfloat16>::value) {
+    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w));
+  } else {
+    return __half22float2(*reinterpret_cast<const __half2*>(&w));
+  }
+}
+
+template <typename InT>
+__device__ __forceinline__ float dot8(const uint4& x, const uint4& b, float acc) {
+  const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
+  const uint32_t bs[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 xf = to_f2<InT>(xs[i]);
+    const float2 bf = to_f2<InT>(bs[i]);
+    acc = fmaf(xf.x, bf.x, acc);
+    acc = fmaf(xf.y, bf.y, acc);
+  }
+  return acc;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+template <typename InT, typename OutT, int MT, int R>
+__global__ void __launch_bounds__(GV_THREADS) k_gemv(GemvParams g) {
+  extern __shared__ uint4 xs[];  // MT rows x K/8 chunks
+  const int K8 = g.K / 8;
+  const uint4 zero = make_uint4(0, 0, 0, 0);
+  const uint4* X = reinterpret_cast<const uint4*>(g.X);
+  for (int i = threadIdx.x; i < MT * K8; i += GV_THREADS) {
+    const int m = i / K8, c = i - m * K8;
+    xs[i] = (m < g.M) ? X[(int64_t)m * K8 + c] : zero;
+  }
+  __syncthreads();
+
+  const uint4* B = reinterpret_cast<const uint4*>(g.B);
+  OutT* Y = reinterpret_cast<OutT*>(g.Y);
+  const int lane = (int)lane_idx();
+  const int warps = GV_THREADS / 32;
+  const int gw = (int)blockIdx.x * warps + (int)warp_idx();
+  const int nw = (int)gridDim.x * warps;
+  for (int n0 = gw * R; n0 < g.N; n0 += nw * R) {
+    float acc[MT][R];
+#pragma unroll
+    for (int m = 0; m < MT; ++m)
+#pragma unroll
+      for (int r = 0; r < R; ++r) acc[m][r] = 0.f;
+    for (int kc0 = 0; kc0 < K8; kc0 += 32 * GV_U) {
+      uint4 bv[R][GV_U];
+#pragma unroll
+      for (int r = 0; r < R; ++r)
+#pragma unroll
+        for (int u = 0; u < GV_U; ++u) {
+          const int c = kc0 + u * 32 + lane;
+          bv[r][u] = (c < K8 && n0 + r < g.N) ? ld_stream_v4(B + (int64_t)(n0 + r) * K8 + c) : zero;
+        }
+#pragma unroll
+      for (int u = 0; u < GV_U; ++u) {
+        const int c = kc0 + u * 32 + lane;
+        if (c < K8) {
+#pragma unroll
+          for (int m = 0; m < MT; ++m) {
+            const uint4 xv = xs[m * K8 + c];
+#pragma unroll
+            for (int r = 0; r < R; ++r) acc[m][r] = dot8<InT>(xv, bv[r][u], acc[m][r]);
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int m = 0; m < MT; ++m)
+#pragma unroll
+      for (int r = 0; r < R; ++r) acc[m][r] = warp_sum(acc[m][r]);
+    if (lane == 0) {
+#pragma unroll
+      for (int m = 0; m < MT; ++m)
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+          if (m < g.M && n0 + r < g.N) {
+            if constexpr (sizeof(OutT) == 4) {
+              Y[(int64_t)m * g.N + n0 + r] = acc[m][r];
+            } else {
+              Y[(int64_t)m * g.N + n0 + r] = __float2bfloat16_rn(acc[m][r]);
+            }
+          }
+        }
+    }
+  }
+}
+
+template <typename InT, typename OutT, int MT, int R>
+cudaError_t launch_t(const GemvParams& g, int num_sms, cudaStream_t st) {
+  auto k = k_gemv<InT, OutT, MT, R>;
+  const size_t smem = (size_t)MT * (size_t)(g.K / 8) * 16;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  int per_sm = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, GV_THREADS, smem);
+  if (e != cudaSuccess) return e;
+  if (per_sm < 1) return cudaErrorInvalidConfiguration;
+  const int rows_per_block = (GV_THREADS / 32) * R;
+  const int need = (g.N + rows_per_block - 1) / rows_per_block;
+  const int grid = std::max(1, std::min(need, per_sm * num_sms));
+  k<<<grid, GV_THREADS, smem, st>>>(g);
+  return cudaGetLastError();
+}
+
+template <typename InT, typename OutT>
+cudaError_t launch_m(const GemvParams& g, int num_sms, cudaStream_t st) {
+  if (g.M <= 1) return launch_t<InT, OutT, 1, 2>(g, num_sms, st);
+  if (g.M <= 2) return launch_t<InT, OutT, 2, 2>(g, num_sms, st);
+  if (g.M <= 4) return launch_t<InT, OutT, 4, 1>(g, num_sms, st);
+  if (g.M <= 8) return launch_t<InT, OutT, 8, 1>(g, num_sms, st);
+  return launch_t<InT, OutT, 16, 1>(g, num_sms, st);
+}
+
+}  // namespace
+
+size_t gemv_smem_bytes(int M, int K) {
+  const int mt = M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : M <= 8 ? 8 : 16;
+  return (size_t)mt * (size_t)(K / 8) * 16;
+}
+
+cudaError_t launch_gemv(const GemvParams& g, bool in_bf16, bool out_f32, int num_sms, cudaStream_t st) {
+  if (in_bf16) {
+    return out_f32 ? launch_m<__nv_bfloat16, float>(g, num_sms, st)
+                   : launch_m<__nv_bfloat16, __nv_bfloat16>(g, num_sms, st);
+  }
+  return out_f32 ? launch_m<__half, float>(g, num_sms, st) : launch_m<__half, __nv_bfloat16>(g, num_sms, st);
+}
+
+}  // namespace dgb

@@ -1,0 +1,170 @@
+/*
+ * gemm.h -- C ABI of the GB300 (sm_103a) dense GEMM library, libdgbgemm.so.
+ *
+ * Computes C = A * B^T on one GPU:
+ *   A  M x K, row-major (K-major), fp16 or bf16
+ *   B  N x K, row-major (K-major), same type as A
+ *   C  M x N, row-major (leading dimension N), fp32 or bf16
+ * with fp32 accumulation in Tensor Memory.  This is the tiled GEMM of
+ * "Modern GPU Programming for MLSys" (reading notes, section "9 步优化"),
+ * whose nine steps are exposed as kernel variants below, and the decode-stage
+ * vector-matrix product of section "Roofline：找到天花板" (1 x 4096 x 4096,
+ * bandwidth-bound) served by a GEMV path for M <= 16.
+ *
+ * Every argument is a plain integer or pointer; no C++ or framework type
+ * crosses this boundary and no exception escapes it.  Device pointers are
+ * owned by the caller; the library never allocates, frees or retains user
+ * buffers.  A plan owns host state (cached TMA descriptors) and 256 bytes of
+ * device scratch (a status word and scheduler counters), released by
+ * gemm_plan_destroy.
+ *
+ * Errors: argument problems are returned at once and nothing is launched.
+ * Kernels never trap: every wait inside them is bounded in time, and a wait
+ * that runs out records a code in the plan's device status word and ends the
+ * kernel early, leaving C undefined.  gemm_check() synchronises the stream and
+ * reports such a code as GEMM_ERR_DEVICE_TIMEOUT.
+ */
+#ifndef DGB_GEMM_H
+#define DGB_GEMM_H
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define GEMM_API __attribute__((visibility("default")))
+#else
+#define GEMM_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A CUDA stream (cudaStream_t); NULL is the legacy default stream. */
+typedef struct CUstream_st* gemm_stream_t;
+
+/* Input / output element types: A and B share the input type. */
+typedef enum {
+  GEMM_F16_F32 = 0,   /* fp16 in, fp32 out */
+  GEMM_F16_BF16 = 1,  /* fp16 in, bf16 out (round to nearest even) */
+  GEMM_BF16_F32 = 2,  /* bf16 in, fp32 out */
+  GEMM_BF16_BF16 = 3  /* bf16 in, bf16 out (round to nearest even) */
+} gemm_dtype_t;
+
+typedef enum {
+  GEMM_OK = 0,
+  GEMM_ERR_INVALID_ARG = 1,       /* NULL pointer, dimension < 1 or >= 2^31, bad option */
+  GEMM_ERR_UNSUPPORTED_SHAPE = 2, /* K % 8 != 0, or a shape the requested variant cannot do */
+  GEMM_ERR_MISALIGNED = 3,        /* A, B or C not 16-byte aligned */
+  GEMM_ERR_UNSUPPORTED_DTYPE = 4, /* dtype outside gemm_dtype_t */
+  GEMM_ERR_ARCH = 5,              /* current device is not compute capability 10.3 */
+  GEMM_ERR_CUDA = 6,              /* a CUDA runtime/driver call failed */
+  GEMM_ERR_OOM = 7,               /* plan scratch could not be allocated */
+  GEMM_ERR_DEVICE_TIMEOUT = 8,    /* a bounded device-side wait gave up */
+  GEMM_ERR_NO_DEVICE = 9          /* no CUDA device is visible */
+} gemm_status_t;
+
+/* Kernel variants: the nine steps of "9 步优化" plus the GEMV. */
+typedef enum {
+  GEMM_VARIANT_AUTO = 0,
+  GEMM_VARIANT_S1_SINGLE_TILE = 1,   /* step 1: one CTA, one 128x128 tile; needs M,N <= 128, K <= 64 */
+  GEMM_VARIANT_S2_KLOOP = 2,         /* step 2: + K loop into one TMEM accumulator; M,N <= 128 */
+  GEMM_VARIANT_S3_MULTI_CTA = 3,     /* step 3: + 2-D grid of 128x128 tiles */
+  GEMM_VARIANT_S4_TMA = 4,           /* step 4: + TMA loads tracked by an mbarrier */
+  GEMM_VARIANT_S5_PIPELINE = 5,      /* step 5: + multi-stage SMEM ring (opts.stages, default 2) */
+  GEMM_VARIANT_S6_PERSISTENT = 6,    /* step 6: + persistent CTAs and a tile scheduler */
+  GEMM_VARIANT_S7_WARP_SPECIALIZED = 7, /* step 7: producer / MMA / writeback warps, 128x256 tiles */
+  GEMM_VARIANT_S8_CTA_PAIR = 8,      /* step 8: 2-CTA cluster, cta_group::2 MMA, 256x256 tiles */
+  GEMM_VARIANT_S9_TWO_CONSUMERS = 9, /* step 9: + second MMA consumer, 512x256 cluster tiles */
+  GEMM_VARIANT_GEMV = 10             /* decode GEMV (CUDA cores), M <= 16 */
+} gemm_variant_t;
+
+/* Tile schedulers of the persistent variants (6-9). */
+typedef enum {
+  GEMM_SCHED_AUTO = 0,
+  GEMM_SCHED_STATIC = 1, /* fixed stride over the raster order */
+  GEMM_SCHED_ATOMIC = 2, /* global atomic tile counter */
+  GEMM_SCHED_CLC = 3     /* hardware cluster launch control (work stealing) */
+} gemm_sched_t;
+
+/* Tuning and test options; zero-initialise and set what you need.
+ * A NULL options pointer means all-automatic. */
+typedef struct {
+  int32_t variant;      /* gemm_variant_t, 0 = automatic choice */
+  int32_t sched;        /* gemm_sched_t, 0 = automatic (static) */
+  int32_t stages;       /* SMEM ring depth, 0 = largest that fits */
+  int32_t raster_group; /* tile rows per L2 raster group, 0 = automatic */
+  int32_t max_ctas;     /* cap on persistent CTAs / clusters, 0 = no cap */
+  int32_t reserved0;
+  int64_t timeout_ns;   /* bound on every device-side wait, 0 = 2 s */
+  int32_t debug_flags;  /* test hooks: 1 = leave out one TMA load (forces a timeout) */
+  int32_t reserved[7];
+} gemm_opts_t;
+
+typedef struct gemm_plan_s* gemm_plan_t;
+
+/* What a plan chose. */
+typedef struct {
+  int32_t variant, sched, stages, raster_group;
+  int32_t tile_m, tile_n;  /* output tile of one CTA (or CTA pair / cluster) */
+  int32_t cluster;         /* CTAs per cluster (1 or 2) */
+  int32_t consumers;       /* MMA consumers per CTA */
+  int32_t grid;            /* CTAs launched */
+  int32_t smem_bytes;      /* dynamic shared memory per CTA */
+  int32_t num_sms;
+  int32_t tiles;           /* output tiles (cluster tiles for variants 8-9) */
+} gemm_plan_info_t;
+
+/* Build a plan for C = A * B^T of the given sizes and types on the current
+ * device.  Validates sizes (M, N, K >= 1 and < 2^31; K % 8 == 0), the dtype,
+ * the options and the device (compute capability 10.3), picks the kernel
+ * variant, tile, ring depth, raster and launch size, and allocates the plan's
+ * device scratch.  On success *out receives the plan. */
+GEMM_API gemm_status_t gemm_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype,
+                        const gemm_opts_t* opts, gemm_plan_t* out);
+
+/* Launch the plan's kernel on `stream` (asynchronous).  A, B and C are device
+ * pointers, 16-byte aligned, laid out as described at the top of this file;
+ * C must not overlap A or B.  One plan runs on one stream at a time. */
+GEMM_API gemm_status_t gemm_plan_run(gemm_plan_t plan, const void* A, const void* B, void* C,
+                            gemm_stream_t stream);
+
+/* One-shot form: plan (cached per shape, dtype and device) and run. */
+GEMM_API gemm_status_t gemm_run(int64_t M, int64_t N, int64_t K, const void* A, const void* B, void* C,
+                       gemm_dtype_t dtype, gemm_stream_t stream);
+
+/* End-to-end form with HOST operands: copies A_host and B_host into the
+ * caller's device buffers dA and dB, runs the GEMM into dC and copies dC back
+ * into C_host, all on `stream`, then synchronises the stream and checks the
+ * device status.  Host buffers should be pinned for full copy speed. */
+GEMM_API gemm_status_t gemm_run_host(int64_t M, int64_t N, int64_t K, const void* A_host,
+                            const void* B_host, void* C_host, gemm_dtype_t dtype, void* dA,
+                            void* dB, void* dC, gemm_stream_t stream);
+
+/* Synchronise `stream`, then report (and clear) a device-side error recorded
+ * by the plan's kernels.  plan == NULL checks every plan gemm_run cached. */
+GEMM_API gemm_status_t gemm_check(gemm_plan_t plan, gemm_stream_t stream);
+
+/* Fill *info with the plan's choices. */
+GEMM_API gemm_status_t gemm_plan_info(gemm_plan_t plan, gemm_plan_info_t* info);
+
+/* Test hook: when `visits` (a device int32 array with one entry per tile) is
+ * non-NULL, persistent variants add 1 to visits[tile] for every tile written. */
+GEMM_API gemm_status_t gemm_plan_set_visits(gemm_plan_t plan, int32_t* visits);
+
+/* Release the plan's device scratch and host state.  NULL is ignored. */
+GEMM_API void gemm_plan_destroy(gemm_plan_t plan);
+
+/* Drop every plan cached by gemm_run. */
+GEMM_API void gemm_clear_cache(void);
+
+/* Static description of a status code. */
+GEMM_API const char* gemm_status_string(gemm_status_t status);
+
+/* Library version string. */
+GEMM_API const char* gemm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DGB_GEMM_H */

@@ -41,8 +41,10 @@ def check(c, ref: np.ndarray, S: np.ndarray, out_dtype: str) -> dict:
     """Compare ``c`` (anything convertible to float64) with the oracle.
 
     Returns a dict with ``ok`` plus diagnostics: the worst ratio
-    |c-ref| / bound, the count of violations, and the max / RMS of
-    |c-ref| / S (which should stay far below 2^-10).
+    |c-ref| / bound, the count of violations, the max / RMS of |c-ref| / S,
+    and ``max_excess_rel``: the largest error beyond the output rounding
+    (half a bf16 ulp of the larger of |c| and |ref|), relative to S, which
+    fp32 accumulation keeps far below 2^-10.
     """
     c = np.asarray(c, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
@@ -56,6 +58,12 @@ def check(c, ref: np.ndarray, S: np.ndarray, out_dtype: str) -> dict:
     with np.errstate(divide="ignore", invalid="ignore"):
         ratio = np.where(b > 0, err / b, np.where(err > 0, np.inf, 0.0))
         rel = np.where(S > 0, err / S, np.where(err > 0, np.inf, 0.0))
+    # the error left after the output rounding is allowed for: with fp32
+    # accumulation it is tiny, so a large value means a lost K block or row
+    allow = half_ulp_bf16(np.maximum(np.abs(ref), np.abs(np.where(finite, c, 0.0)))) if out_dtype == "bf16" else 0.0
+    excess = np.maximum(err - allow, 0.0)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        exc_rel = np.where(S > 0, excess / S, np.where(excess > 0, np.inf, 0.0))
     n = max(1, rel.size)
     out = {
         "ok": bool(not bad.any()),
@@ -65,6 +73,7 @@ def check(c, ref: np.ndarray, S: np.ndarray, out_dtype: str) -> dict:
         "worst_ratio": float(np.max(ratio)) if ratio.size else 0.0,
         "max_rel": float(np.max(rel)) if rel.size else 0.0,
         "rms_rel": float(np.sqrt(np.sum(np.where(np.isfinite(rel), rel, 0.0) ** 2) / n)),
+        "max_excess_rel": float(np.max(np.where(finite, exc_rel, np.inf))) if exc_rel.size else 0.0,
     }
     if bad.any():
         idx = np.argwhere(bad)[0]

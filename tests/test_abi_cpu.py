@@ -1,0 +1,110 @@
+"""The C-ABI library loads without a GPU, exports every symbol include/gemm.h
+declares, and rejects bad arguments before it touches a device."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+from dense_gemm_blackwell_sm_gb300 import build as pkg_build
+from dense_gemm_blackwell_sm_gb300 import gemm
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gemm.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    pkg_build.build()
+    return gemm.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return re.findall(r"GEMM_API\s+[\w\s\*]+?\b(gemm_\w+)\s*\(", text)
+
+
+def test_header_declares_the_boundary():
+    names = set(declared_functions())
+    for required in ("gemm_plan", "gemm_plan_run", "gemm_run", "gemm_run_host", "gemm_check",
+                     "gemm_plan_destroy", "gemm_status_string"):
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 10
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    for code in range(10):
+        s = gemm.status_string(code)
+        assert s and s != "unknown status"
+    assert gemm.status_string(99) == "unknown status"
+    assert "sm_103a" in gemm.version()
+
+
+def _plan_status(lib, M, N, K, dtype, opts=None):
+    h = ctypes.c_void_p()
+    st = lib.gemm_plan(M, N, K, dtype, ctypes.byref(opts) if opts is not None else None, ctypes.byref(h))
+    if h.value:
+        lib.gemm_plan_destroy(h)
+    return st
+
+
+def test_plan_rejects_bad_sizes_without_a_device(lib):
+    assert _plan_status(lib, 0, 16, 16, 0) == gemm.ERR_INVALID_ARG
+    assert _plan_status(lib, 16, -1, 16, 0) == gemm.ERR_INVALID_ARG
+    assert _plan_status(lib, 16, 16, 0, 0) == gemm.ERR_INVALID_ARG
+    assert _plan_status(lib, 1 << 31, 16, 16, 0) == gemm.ERR_INVALID_ARG
+    assert _plan_status(lib, 16, 16, 12, 0) == gemm.ERR_UNSUPPORTED_SHAPE   # K % 8 != 0
+    assert _plan_status(lib, 16, 16, 16, 7) == gemm.ERR_UNSUPPORTED_DTYPE
+    assert _plan_status(lib, 16, 16, 16, -1) == gemm.ERR_UNSUPPORTED_DTYPE
+
+
+def test_plan_rejects_bad_options(lib):
+    assert _plan_status(lib, 64, 64, 64, 0, gemm.make_opts(variant=11)) == gemm.ERR_INVALID_ARG
+    assert _plan_status(lib, 64, 64, 64, 0, gemm.make_opts(sched=9)) == gemm.ERR_INVALID_ARG
+    assert _plan_status(lib, 64, 64, 64, 0, gemm.make_opts(stages=9)) == gemm.ERR_INVALID_ARG
+    # step 1 is one 128x128x64 tile; step 2 one 128x128 tile
+    assert _plan_status(lib, 129, 64, 64, 0, gemm.make_opts(variant=gemm.S1)) == gemm.ERR_UNSUPPORTED_SHAPE
+    assert _plan_status(lib, 64, 64, 72, 0, gemm.make_opts(variant=gemm.S1)) == gemm.ERR_UNSUPPORTED_SHAPE
+    assert _plan_status(lib, 64, 200, 64, 0, gemm.make_opts(variant=gemm.S2)) == gemm.ERR_UNSUPPORTED_SHAPE
+    # TMA-store writeback needs 16-byte aligned rows of C
+    assert _plan_status(lib, 64, 100, 64, 3, gemm.make_opts(variant=gemm.S8)) == gemm.ERR_UNSUPPORTED_SHAPE
+    assert _plan_status(lib, 17, 64, 64, 3, gemm.make_opts(variant=gemm.GEMV)) == gemm.ERR_UNSUPPORTED_SHAPE
+
+
+def test_valid_plan_needs_the_device(lib):
+    st = _plan_status(lib, 256, 256, 256, 3)
+    if torch.cuda.is_available():
+        assert st in (gemm.OK, gemm.ERR_ARCH)
+    else:
+        assert st == gemm.ERR_NO_DEVICE
+
+
+def test_run_validates_pointers_first(lib):
+    assert lib.gemm_run(64, 64, 64, None, 16, 16, 3, None) == gemm.ERR_INVALID_ARG
+    assert lib.gemm_run(64, 64, 64, 0x1008, 0x2000, 0x3000, 3, None) == gemm.ERR_MISALIGNED
+    assert lib.gemm_run(64, 64, 60, 0x1000, 0x2000, 0x3000, 3, None) == gemm.ERR_UNSUPPORTED_SHAPE
+    assert lib.gemm_plan_run(None, 0x1000, 0x2000, 0x3000, None) == gemm.ERR_INVALID_ARG
+    assert lib.gemm_plan_info(None, None) == gemm.ERR_INVALID_ARG
+    lib.gemm_plan_destroy(None)   # ignored
+
+
+def test_matmul_refuses_cpu_tensors(lib):
+    a = torch.zeros(4, 8, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        gemm.matmul(a, a)
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(gemm, "_lib", None)
+    monkeypatch.setattr(gemm, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError):
+        gemm.load()

@@ -1,0 +1,189 @@
+"""GPU parity of every kernel variant against the CPU oracle, through the C ABI.
+
+* integer-valued operands: every fp32 partial sum is exact, so the GPU must
+  match the oracle bit for bit (bf16 output: the oracle's exact integer
+  rounded to nearest even);
+* random operands: the per-element acceptance rule of oracle.parity;
+* ragged shapes that span several tiles in M, N and K;
+* the scheduler covers every tile exactly once;
+* a forced device-side wait timeout is reported and leaves the context usable.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import parity
+from dense_gemm_blackwell_sm_gb300 import gemm, inputs
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+    __graft_entry__.build()
+    torch.cuda.set_device(0)
+
+
+def run_variant(a, b, out, variant, sched=0, stages=0, raster_group=0, max_ctas=0, plan_out=None):
+    M, K = a.shape
+    N = b.shape[0]
+    code = gemm.dtype_code(a.dtype, out)
+    plan = gemm.Plan(M, N, K, code, gemm.make_opts(variant=variant, sched=sched, stages=stages,
+                                                   raster_group=raster_group, max_ctas=max_ctas))
+    c = torch.full((M, N), float("nan"), device=DEV, dtype=inputs.torch_dtype(out))
+    plan.run(a.to(DEV), b.to(DEV), c)
+    st = plan.check()
+    assert st == gemm.OK, gemm.status_string(st)
+    if plan_out is not None:
+        plan_out.append(plan.info())
+    plan.destroy()
+    return c.float().cpu().numpy().astype(np.float64)
+
+
+def expect_bits(ref: np.ndarray, out: str) -> np.ndarray:
+    """The exact result in the output format (bf16: round to nearest even)."""
+    t = torch.tensor(ref, dtype=torch.float64)
+    if out == "bf16":
+        return t.to(torch.bfloat16).to(torch.float64).numpy()
+    return t.to(torch.float32).to(torch.float64).numpy()
+
+
+# variant -> ragged shapes spanning several of its tiles (N % 8 == 0 throughout)
+SHAPES = {
+    gemm.S1: [(128, 128, 64), (100, 72, 40)],
+    gemm.S2: [(128, 128, 512), (77, 120, 136)],
+    gemm.S3: [(300, 264, 520), (129, 8, 72)],
+    gemm.S4: [(300, 264, 520)],
+    gemm.S5: [(300, 264, 520), (257, 392, 1000)],
+    gemm.S6: [(300, 264, 520), (1030, 1288, 264)],
+    gemm.S7: [(300, 520, 200), (700, 1288, 264)],
+    gemm.S8: [(300, 520, 200), (700, 1288, 264), (1, 264, 72)],
+    gemm.S9: [(300, 520, 200), (1100, 1288, 264)],
+    gemm.GEMV: [(1, 1000, 520), (3, 264, 72), (8, 1000, 520), (16, 96, 1024)],
+}
+CASES = [(v, s) for v, shapes in SHAPES.items() for s in shapes]
+IDS = ["%s-%dx%dx%d" % (gemm.VARIANT_NAMES[v], *s) for v, s in CASES]
+
+
+@pytest.mark.parametrize("variant,shape", CASES, ids=IDS)
+@pytest.mark.parametrize("ti,to", [("f16", "f32"), ("bf16", "bf16"), ("bf16", "f32"), ("f16", "bf16")])
+def test_integer_inputs_bit_exact(variant, shape, ti, to):
+    M, N, K = shape
+    a, b = inputs.integer_operands(M, N, K, ti, seed=M * 7 + N * 3 + K)
+    ref, _ = oracle.gemm(a, b)
+    c = run_variant(a, b, to, variant)
+    exp = expect_bits(ref, to)
+    bad = np.argwhere(c != exp)
+    assert bad.size == 0, "first mismatch at %s: got %r expected %r" % (
+        bad[0], c[tuple(bad[0])], exp[tuple(bad[0])])
+
+
+@pytest.mark.parametrize("variant,shape", CASES, ids=IDS)
+@pytest.mark.parametrize("ti,to", [("f16", "f32"), ("bf16", "bf16")])
+def test_random_inputs_parity(variant, shape, ti, to):
+    M, N, K = shape
+    a, b = inputs.make_operands(M, N, K, ti, ("uniform",), ("normal", 1.0), seed=M + N + K)
+    ref, S = oracle.gemm(a, b)
+    c = run_variant(a, b, to, variant)
+    r = parity.check(c, ref, S, to)
+    assert r["ok"], r
+    assert r["max_excess_rel"] < 2.0 ** -12, r   # far inside the bound: no dropped K block
+
+
+@pytest.mark.parametrize("variant", [gemm.S6, gemm.S7, gemm.S8, gemm.S9])
+@pytest.mark.parametrize("sched", [gemm.SCHED_STATIC, gemm.SCHED_ATOMIC, gemm.SCHED_CLC])
+def test_schedulers_visit_every_tile_once(variant, sched):
+    # tile counts below, near and above the number of SMs
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    for M, N in [(512, 512), (2048, 2560), (4096, 4096)]:
+        K = 64
+        a, b = inputs.integer_operands(M, N, K, "bf16", seed=1)
+        code = gemm.dtype_code("bf16", "bf16")
+        plan = gemm.Plan(M, N, K, code, gemm.make_opts(variant=variant, sched=sched))
+        info = plan.info()
+        visits = torch.zeros(info["tiles"], dtype=torch.int32, device=DEV)
+        plan.set_visits(visits)
+        c = torch.empty((M, N), device=DEV, dtype=torch.bfloat16)
+        for _ in range(2):   # twice: the atomic counter must rewind itself
+            visits.zero_()
+            plan.run(a.to(DEV), b.to(DEV), c)
+            assert plan.check() == gemm.OK
+            v = visits.cpu()
+            assert int(v.min()) == 1 and int(v.max()) == 1, (info, sms, v.unique(return_counts=True))
+        ref, _ = oracle.gemm_rows(a, b, [0, M // 2, M - 1])
+        got = c.float().cpu().numpy()[[0, M // 2, M - 1]]
+        assert np.array_equal(got, expect_bits(ref, "bf16"))
+        plan.destroy()
+
+
+@pytest.mark.parametrize("variant", [gemm.S4, gemm.S5, gemm.S7, gemm.S8, gemm.S9])
+def test_forced_wait_timeout_is_reported(variant):
+    M, N, K = 256, 512, 256
+    a, b = inputs.integer_operands(M, N, K, "bf16", seed=2)
+    code = gemm.dtype_code("bf16", "bf16")
+    plan = gemm.Plan(M, N, K, code, gemm.make_opts(variant=variant, timeout_ns=20_000_000,
+                                                   debug_flags=gemm.DEBUG_SKIP_ONE_LOAD))
+    c = torch.empty((M, N), device=DEV, dtype=torch.bfloat16)
+    plan.run(a.to(DEV), b.to(DEV), c)
+    assert plan.check() == gemm.ERR_DEVICE_TIMEOUT
+    plan.destroy()
+    # the context is still usable and the same shape computes correctly
+    ref, _ = oracle.gemm(a, b)
+    got = run_variant(a, b, "bf16", variant)
+    assert np.array_equal(got, expect_bits(ref, "bf16"))
+
+
+def test_zero_rows_give_exact_zeros():
+    a, b = inputs.make_operands(300, 264, 200, "bf16", ("uniform",), ("uniform",), seed=3)
+    a[5].zero_()
+    a[299].zero_()
+    for v in (gemm.S3, gemm.S6, gemm.S8, gemm.S9):
+        c = run_variant(a, b, "bf16", v)
+        assert np.all(c[5] == 0) and np.all(c[299] == 0)
+
+
+def test_misaligned_pointer_rejected():
+    a = torch.zeros(64 * 64 + 8, dtype=torch.bfloat16, device=DEV)
+    b = torch.zeros(64, 64, dtype=torch.bfloat16, device=DEV)
+    c = torch.zeros(64, 64, dtype=torch.bfloat16, device=DEV)
+    st = gemm.gemm_run(64, 64, 64, a.data_ptr() + 2, b.data_ptr(), c.data_ptr(), gemm.BF16_BF16,
+                       torch.cuda.current_stream().cuda_stream)
+    assert st == gemm.ERR_MISALIGNED
+
+
+def test_matmul_on_side_stream_and_auto_choices():
+    a, b = inputs.make_operands(520, 776, 264, "bf16", ("uniform",), ("uniform",), seed=4)
+    ref, S = oracle.gemm(a, b)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        c = gemm.matmul(a.to(DEV), b.to(DEV), torch.bfloat16)
+    s.synchronize()
+    assert parity.check(c.float().cpu().numpy(), ref, S, "bf16")["ok"]
+    # odd N (rows of C not 16-byte aligned): the automatic plan still works
+    a2, b2 = inputs.make_operands(200, 100, 64, "f16", ("uniform",), ("uniform",), seed=5)
+    ref2, S2 = oracle.gemm(a2, b2)
+    c2 = gemm.matmul(a2.to(DEV), b2.to(DEV), torch.float32)
+    torch.cuda.synchronize()
+    assert parity.check(c2.cpu().numpy(), ref2, S2, "f32")["ok"]
+    assert gemm.gemm_check() == gemm.OK
+
+
+def test_run_host_end_to_end():
+    M, N, K = 300, 264, 136
+    a, b = inputs.make_operands(M, N, K, "bf16", ("uniform",), ("uniform",), seed=6)
+    ref, S = oracle.gemm(a, b)
+    ah, bh = a.pin_memory(), b.pin_memory()
+    ch = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
+    da = torch.empty_like(a, device=DEV)
+    db = torch.empty_like(b, device=DEV)
+    dc = torch.empty((M, N), dtype=torch.bfloat16, device=DEV)
+    st = gemm.gemm_run_host(M, N, K, ah.data_ptr(), bh.data_ptr(), ch.data_ptr(), gemm.BF16_BF16,
+                            da.data_ptr(), db.data_ptr(), dc.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    assert st == gemm.OK
+    assert parity.check(ch.float().numpy(), ref, S, "bf16")["ok"]

@@ -355,3 +355,14 @@ def test_workload_table_shapes():
     assert w["single_tile_128x128x64_f16_f32"].seed == 0
     assert w["gemv_m1_n4096_k4096_bf16"].M == 1
     assert w["square_4096_f16_f32"].algorithmic_bytes == 2 * 2 * 4096 * 4096 + 4 * 4096 * 4096
+
+
+def test_parity_diagnostic_flags_a_lost_k_block():
+    a, b = inputs.make_operands(8, 16, 512, "bf16", ("uniform",), ("uniform",), seed=12)
+    C, S = oracle.gemm(a, b)
+    good = torch.tensor(C).to(torch.bfloat16).to(torch.float64).numpy()
+    assert parity.check(good, C, S, "bf16")["max_excess_rel"] < 2.0 ** -16
+    # the same product with the last 64-wide K block left out
+    Cd, _ = oracle.gemm(a[:, :448].contiguous(), b[:, :448].contiguous())
+    lost = torch.tensor(Cd).to(torch.bfloat16).to(torch.float64).numpy()
+    assert parity.check(lost, C, S, "bf16")["max_excess_rel"] > 2.0 ** -12
