@@ -130,7 +130,7 @@ gemm_status_t build_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, co
   if (st != GEMM_OK) return st;
   gemm_opts_t o{};
   if (opts) o = *opts;
-  if (o.variant < 0 || o.variant > GEMM_VARIANT_GEMV || o.sched < 0 || o.sched > GEMM_SCHED_CLC ||
+  if (o.variant < 0 || o.variant > GEMM_VARIANT_GEMV_TC || o.sched < 0 || o.sched > GEMM_SCHED_CLC ||
       o.stages < 0 || o.stages > 8 || o.raster_group < 0 || o.max_ctas < 0 || o.timeout_ns < 0)
     return GEMM_ERR_INVALID_ARG;
 
@@ -143,6 +143,7 @@ gemm_status_t build_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, co
     return GEMM_ERR_UNSUPPORTED_SHAPE;
   if (variant == GEMM_VARIANT_GEMV && (M > 16 || gemv_smem_bytes((int)M, (int)K) > 200 * 1024))
     return GEMM_ERR_UNSUPPORTED_SHAPE;
+  if (variant == GEMM_VARIANT_GEMV_TC && M > 16) return GEMM_ERR_UNSUPPORTED_SHAPE;
 
   int dev = 0, sms = 0;
   st = current_device(&dev, &sms);
@@ -189,6 +190,17 @@ gemm_status_t build_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, co
   } else if (variant == GEMM_VARIANT_S6_PERSISTENT) {
     p->smem = step6_smem_bytes(p->stages);
   }
+  if (variant == GEMM_VARIANT_GEMV_TC) {
+    if (gemv_tc_smem_bytes((int)N, (int)K, sms) > 227 * 1024) {
+      delete p;
+      return GEMM_ERR_UNSUPPORTED_SHAPE;
+    }
+    int split = 1, kpc = 1;
+    gemv_tc_config((int)N, (int)K, sms, &split, &p->stages, &kpc);
+    p->cg = split;
+    p->smem = gemv_tc_smem_bytes((int)N, (int)K, sms);
+    p->tile_m = 16;
+  }
   p->tiles_m = ceil_div(M, p->tile_m);
   p->tiles_n = ceil_div(N, p->tile_n);
   if (persistent) p->raster_group = o.raster_group ? o.raster_group : std::min(8, p->tiles_m);
@@ -227,6 +239,14 @@ gemm_status_t build_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, co
 gemm_status_t refresh_maps(gemm_plan_s* p, const void* A, const void* B, void* C) {
   if (p->maps_valid && p->mapA == A && p->mapB == B && p->mapC == C) return GEMM_OK;
   const CUtensorMapDataType in_t = p->in_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  if (p->variant == GEMM_VARIANT_GEMV_TC) {
+    if (!encode_2d(&p->tmB, in_t, 2, B, (uint64_t)p->K, (uint64_t)p->N, 64, 128)) return GEMM_ERR_CUDA;
+    p->mapA = A;
+    p->mapB = B;
+    p->mapC = C;
+    p->maps_valid = true;
+    return GEMM_OK;
+  }
   uint32_t a_rows = 128, b_rows = 128;
   if (p->variant >= GEMM_VARIANT_S7_WARP_SPECIALIZED && p->variant <= GEMM_VARIANT_S9_TWO_CONSUMERS) {
     const WsShape sh = ws_shape(p->cg, p->consumers);
@@ -263,6 +283,17 @@ gemm_status_t launch_plan(gemm_plan_s* p, const void* A, const void* B, void* C,
     GemvParams g{A, B, C, (int32_t)p->M, (int32_t)p->N, (int32_t)p->K};
     e = launch_gemv(g, p->in_bf16, p->out_f32, p->num_sms, s);
     return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+  }
+  if (p->variant == GEMM_VARIANT_GEMV_TC) {
+    gemm_status_t st = refresh_maps(p, A, B, C);
+    if (st != GEMM_OK) return st;
+    GemvParams g{A, B, C, (int32_t)p->M, (int32_t)p->N, (int32_t)p->K};
+    e = launch_gemv_tc(g, p->tmB, p->in_bf16, p->out_f32, p->num_sms, p->scratch, p->timeout_ns, s);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return GEMM_ERR_CUDA;
+    }
+    return GEMM_OK;
   }
 
   KParams k{};

@@ -1,0 +1,251 @@
+// kernel_gemv_tc.cu -- decode-shaped Y (M x N) = X (M x K) * B^T for M <= 16 on
+// the Tensor Core, with the operands swapped.
+//
+// The decode product is bandwidth-bound (reading notes of "Modern GPU
+// Programming for MLSys", section "Roofline：找到天花板": about one FLOP per
+// byte at M = 1).  With a few activation rows (M = 8) the CUDA cores would
+// still need 4 fp32 FMAs per weight byte, close to their own limit, so here
+// the MMA does the arithmetic: the weight tile (128 rows of B) is the
+// 128-row A operand of tcgen05.mma, the activations (M rows, zero-padded to 16)
+// are the 16-column B operand, and D[n][m] = sum_k B[n][k] X[m][k] lands in 16
+// TMEM columns.  Only the weight stream matters for time:
+//   * K is split over the CTAs of a cluster (up to 8): each CTA streams a
+//     128-row x K/split slab of B through a TMA ring, accumulating in TMEM;
+//   * the partial sums of the cluster are added in rank order through
+//     distributed shared memory by the leader CTA, which writes Y;
+//   * X's K-slice (16 x K/split) is staged once per CTA with plain loads.
+// No global scratch is used.
+#include <algorithm>
+
+#include "kernel_common.cuh"
+#include "launch.h"
+
+namespace dgb {
+
+namespace {
+
+constexpr int TG_THREADS = 128;
+constexpr int TG_BK = 64;
+constexpr uint32_t TG_B_BYTES = 128u * 128u;  // one weight box: 128 rows x 64 K
+constexpr uint32_t TG_X_BYTES = 16u * 128u;   // one activation tile: 16 rows x 64 K
+constexpr int TG_MAX_STAGES = 8;
+
+struct TgParams {
+  const uint16_t* X;
+  void* Y;
+  int32_t M, N, K;
+  int32_t kblocks_per_cta;  // K blocks in one CTA's slice
+  int32_t split;            // CTAs per cluster along K
+  int32_t stages;
+  uint32_t idesc;
+  uint32_t* status;
+  uint64_t timeout_ns;
+};
+
+template <typename OutT>
+__global__ void __launch_bounds__(TG_THREADS, 1)
+    k_gemv_tc(const __grid_constant__ CUtensorMap tmB, TgParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align_1024(smem_raw);
+  const int S = p.stages;
+  const int KS = p.kblocks_per_cta;
+  uint8_t* ring = smem;                                    // S x 16 KB
+  uint8_t* xs = ring + (size_t)S * TG_B_BYTES;             // KS x 2 KB
+  float* partial = reinterpret_cast<float*>(xs + (size_t)KS * TG_X_BYTES);  // 128 x 16 fp32
+  uint64_t* full = reinterpret_cast<uint64_t*>(partial + 128 * 16);
+  uint64_t* empty = full + TG_MAX_STAGES;
+  uint64_t* done = empty + TG_MAX_STAGES;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+  volatile uint32_t* abort_flag = tmem_slot + 1;
+
+  const uint32_t tid = threadIdx.x, warp = warp_idx(), lane = lane_idx();
+  const uint32_t rank = cluster_ctarank();
+  const int32_t rb = (int32_t)(blockIdx.x / (uint32_t)p.split);   // 128-row block of B / Y
+  const int32_t n0 = rb * 128;
+  const int32_t KB = (p.K + TG_BK - 1) / TG_BK;
+  const int32_t kb0 = (int32_t)rank * KS;
+  const int32_t nkb = max(0, min(KS, KB - kb0));
+
+  if (tid == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(smem_u32(full + s), 1);
+      mbar_init(smem_u32(empty + s), 1);
+    }
+    mbar_init(smem_u32(done), 1);
+    *abort_flag = 0u;
+    fence_mbar_init();
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 0) {
+    tmem_alloc<1>(smem_u32(tmem_slot), 32);
+    tmem_relinquish<1>();
+  }
+  // this CTA's activation slice, rows >= M zero, in the 128B-swizzled K-major layout
+  const int32_t K8 = p.K / 8;
+  for (int i = tid; i < nkb * 16 * 8; i += TG_THREADS) {
+    const int j = i / 128, r = (i / 8) & 15, c = i & 7;
+    const int32_t kc = (kb0 + j) * 8 + c;  // 16-byte chunk index along K
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (r < p.M && kc < K8) v = reinterpret_cast<const uint4*>(p.X)[(int64_t)r * K8 + kc];
+    *reinterpret_cast<uint4*>(xs + (size_t)j * TG_X_BYTES + sw128_offset((uint32_t)r, (uint32_t)c)) = v;
+  }
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const WaitCtl w{abort_flag, p.status, p.timeout_ns, 0};
+
+  if (warp == 0 && lane == 0) {
+    // producer
+    for (int32_t j = 0; j < nkb; ++j) {
+      const int s = j % S;
+      const uint32_t ph = (uint32_t)(j / S) & 1u;
+      if (!mbar_wait(smem_u32(empty + s), ph ^ 1u, w, WAIT_PRODUCER_EMPTY)) break;
+      mbar_arrive_expect_tx(smem_u32(full + s), TG_B_BYTES);
+      tma_load_2d(smem_u32(ring + (size_t)s * TG_B_BYTES), &tmB, smem_u32(full + s), (kb0 + j) * TG_BK, n0);
+    }
+  } else if (warp == 1 && lane == 0) {
+    // MMA issuer
+    for (int32_t j = 0; j < nkb; ++j) {
+      const int s = j % S;
+      const uint32_t ph = (uint32_t)(j / S) & 1u;
+      if (!mbar_wait(smem_u32(full + s), ph, w, WAIT_MMA_FULL)) break;
+      tc_fence_after();
+      const uint64_t ad = sdesc_k_sw128(smem_u32(ring + (size_t)s * TG_B_BYTES));
+      const uint64_t bd = sdesc_k_sw128(smem_u32(xs + (size_t)j * TG_X_BYTES));
+#pragma unroll
+      for (int k = 0; k < TG_BK / 16; ++k) mma_f16<1>(tmem, ad + 2 * k, bd + 2 * k, p.idesc, (j | k) != 0);
+      mma_commit(smem_u32(empty + s));
+    }
+    mma_commit(smem_u32(done));
+  }
+  __syncwarp();
+  // every thread: the slab's partial sums (row = TMEM lane) into shared memory
+  bool ok = mbar_wait(smem_u32(done), 0, w, WAIT_LADDER_MMA);
+  ok = __syncthreads_and(ok && *abort_flag == 0u) != 0;
+  const uint32_t row = warp * 32u + lane;
+  if (ok) {
+    tc_fence_after();
+    uint32_t v[16];
+    tmem_ld_32x32b_x16(tmem + ((warp * 32u) << 16), v);
+    tmem_wait_ld();
+    float4* dst = reinterpret_cast<float4*>(partial + row * 16);
+    if (nkb > 0) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        dst[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                             __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+    } else {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) dst[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
+  cluster_sync_all();
+  if (ok && rank == 0) {
+    // leader: add the cluster's partials in rank order and write Y
+    float acc[16];
+#pragma unroll
+    for (int m = 0; m < 16; ++m) acc[m] = 0.f;
+    const uint32_t my = smem_u32(partial + row * 16);
+    for (int r = 0; r < p.split; ++r) {
+      const uint32_t src = mapa_shared(my, (uint32_t)r);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float4 f = ld_cluster_f32x4(src + 16u * q);
+        acc[4 * q] += f.x;
+        acc[4 * q + 1] += f.y;
+        acc[4 * q + 2] += f.z;
+        acc[4 * q + 3] += f.w;
+      }
+    }
+    const int32_t n = n0 + (int32_t)row;
+    if (n < p.N) {
+      OutT* Y = reinterpret_cast<OutT*>(p.Y);
+#pragma unroll
+      for (int m = 0; m < 16; ++m) {
+        if (m < p.M) {
+          if constexpr (sizeof(OutT) == 4) {
+            Y[(int64_t)m * p.N + n] = acc[m];
+          } else {
+            Y[(int64_t)m * p.N + n] = __float2bfloat16_rn(acc[m]);
+          }
+        }
+      }
+    }
+  }
+  if (!ok && tid == 0) {
+    const uint64_t t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < 2000000ull) {}
+  }
+  cluster_sync_all();  // peers keep their partials alive until the leader has read them
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc<1>(tmem, 32);
+  }
+}
+
+size_t tg_smem(int stages, int kblocks_per_cta) {
+  return 1024 + (size_t)stages * TG_B_BYTES + (size_t)kblocks_per_cta * TG_X_BYTES + 128 * 16 * 4 +
+         (2 * TG_MAX_STAGES + 1) * 8 + 16;
+}
+
+}  // namespace
+
+// split along K (CTAs per cluster) and ring depth for a decode shape
+void gemv_tc_config(int N, int K, int num_sms, int* split, int* stages, int* kblocks_per_cta) {
+  const int KB = (K + TG_BK - 1) / TG_BK;
+  const int rbs = (N + 127) / 128;
+  int sp = 1;
+  while (sp < 8 && rbs * sp < 2 * num_sms && sp * 2 <= KB) sp *= 2;
+  const int ks = (KB + sp - 1) / sp;
+  int st = std::min(TG_MAX_STAGES, std::max(2, ks));
+  while (st > 2 && tg_smem(st, ks) > 200 * 1024) --st;
+  *split = sp;
+  *stages = st;
+  *kblocks_per_cta = ks;
+}
+
+size_t gemv_tc_smem_bytes(int N, int K, int num_sms) {
+  int sp, st, ks;
+  gemv_tc_config(N, K, num_sms, &sp, &st, &ks);
+  return tg_smem(st, ks);
+}
+
+cudaError_t launch_gemv_tc(const GemvParams& g, const CUtensorMap& tmB, bool in_bf16, bool out_f32,
+                           int num_sms, uint32_t* status, uint64_t timeout_ns, cudaStream_t st) {
+  TgParams p{};
+  p.X = static_cast<const uint16_t*>(g.X);
+  p.Y = g.Y;
+  p.M = g.M;
+  p.N = g.N;
+  p.K = g.K;
+  gemv_tc_config(g.N, g.K, num_sms, &p.split, &p.stages, &p.kblocks_per_cta);
+  const uint32_t ab = in_bf16 ? 1u : 0u;
+  p.idesc = (1u << 4) | (ab << 7) | (ab << 10) | ((uint32_t)(16 >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+  p.status = status;
+  p.timeout_ns = timeout_ns;
+  const size_t smem = tg_smem(p.stages, p.kblocks_per_cta);
+  void* k = out_f32 ? reinterpret_cast<void*>(k_gemv_tc<float>) : reinterpret_cast<void*>(k_gemv_tc<__nv_bfloat16>);
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg{};
+  const int rbs = (g.N + 127) / 128;
+  cfg.gridDim = dim3((unsigned)(rbs * p.split), 1, 1);
+  cfg.blockDim = dim3(TG_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)p.split;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  void* args[] = {const_cast<CUtensorMap*>(&tmB), &p};
+  return cudaLaunchKernelExC(&cfg, k, args);
+}
+
+}  // namespace dgb

@@ -49,6 +49,12 @@ struct GemvParams {
   int32_t M, N, K;
 };
 size_t gemv_smem_bytes(int M, int K);
+// the same product on the Tensor Core (weight as the 128-row MMA operand),
+// K split over the CTAs of a cluster
+void gemv_tc_config(int N, int K, int num_sms, int* split, int* stages, int* kblocks_per_cta);
+size_t gemv_tc_smem_bytes(int N, int K, int num_sms);
+cudaError_t launch_gemv_tc(const GemvParams& g, const CUtensorMap& tmB, bool in_bf16, bool out_f32,
+                           int num_sms, uint32_t* status, uint64_t timeout_ns, cudaStream_t st);
 cudaError_t launch_gemv(const GemvParams& g, bool in_bf16, bool out_f32, int num_sms, cudaStream_t st);
 
 }  // namespace dgb

@@ -23,10 +23,10 @@ OK, ERR_INVALID_ARG, ERR_UNSUPPORTED_SHAPE, ERR_MISALIGNED, ERR_UNSUPPORTED_DTYP
 ERR_ARCH, ERR_CUDA, ERR_OOM, ERR_DEVICE_TIMEOUT, ERR_NO_DEVICE = 5, 6, 7, 8, 9
 
 # gemm_variant_t
-VARIANT_AUTO, S1, S2, S3, S4, S5, S6, S7, S8, S9, GEMV = range(11)
+VARIANT_AUTO, S1, S2, S3, S4, S5, S6, S7, S8, S9, GEMV, GEMV_TC = range(12)
 VARIANT_NAMES = {0: "auto", 1: "s1_single_tile", 2: "s2_kloop", 3: "s3_multi_cta", 4: "s4_tma",
                  5: "s5_pipeline", 6: "s6_persistent", 7: "s7_warp_specialized", 8: "s8_cta_pair",
-                 9: "s9_two_consumers", 10: "gemv"}
+                 9: "s9_two_consumers", 10: "gemv", 11: "gemv_tc"}
 
 # gemm_sched_t
 SCHED_AUTO, SCHED_STATIC, SCHED_ATOMIC, SCHED_CLC = 0, 1, 2, 3

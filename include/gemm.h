@@ -75,7 +75,9 @@ typedef enum {
   GEMM_VARIANT_S7_WARP_SPECIALIZED = 7, /* step 7: producer / MMA / writeback warps, 128x256 tiles */
   GEMM_VARIANT_S8_CTA_PAIR = 8,      /* step 8: 2-CTA cluster, cta_group::2 MMA, 256x256 tiles */
   GEMM_VARIANT_S9_TWO_CONSUMERS = 9, /* step 9: + second MMA consumer, 512x256 cluster tiles */
-  GEMM_VARIANT_GEMV = 10             /* decode GEMV (CUDA cores), M <= 16 */
+  GEMM_VARIANT_GEMV = 10,            /* decode GEMV (CUDA cores), M <= 16 */
+  GEMM_VARIANT_GEMV_TC = 11          /* decode GEMV on the Tensor Core (weight as the 128-row
+                                        MMA operand, K split over a cluster), M <= 16 */
 } gemm_variant_t;
 
 /* Tile schedulers of the persistent variants (6-9). */

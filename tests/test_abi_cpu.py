@@ -68,7 +68,7 @@ def test_plan_rejects_bad_sizes_without_a_device(lib):
 
 
 def test_plan_rejects_bad_options(lib):
-    assert _plan_status(lib, 64, 64, 64, 0, gemm.make_opts(variant=11)) == gemm.ERR_INVALID_ARG
+    assert _plan_status(lib, 64, 64, 64, 0, gemm.make_opts(variant=12)) == gemm.ERR_INVALID_ARG
     assert _plan_status(lib, 64, 64, 64, 0, gemm.make_opts(sched=9)) == gemm.ERR_INVALID_ARG
     assert _plan_status(lib, 64, 64, 64, 0, gemm.make_opts(stages=9)) == gemm.ERR_INVALID_ARG
     # step 1 is one 128x128x64 tile; step 2 one 128x128 tile

@@ -1,0 +1,87 @@
+"""Host-side logic of bench.py: peaks, traffic bookkeeping, the max-over-ranks
+aggregation across world_size-2 gloo processes, and the single JSON line of
+the reference arm under torchrun (no GPU needed)."""
+from __future__ import annotations
+
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+import torch
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+
+
+def _free_port() -> int:
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    p = s.getsockname()[1]
+    s.close()
+    return p
+
+
+def test_aggregate_takes_the_slowest_rank_and_counts_all_work():
+    t, rate = bench.aggregate([0.5, 0.8, 0.6], 100.0)
+    assert t == 0.8
+    assert rate == pytest.approx(300.0 / 0.8)
+
+
+def test_peaks_and_traffic_lookup():
+    peaks, src = bench.measured_peaks()
+    assert src in ("measured", "fallback")
+    assert peaks["bf16_tflops"] > 0 and peaks["hbm_gbs"] > 0
+    assert len(bench.source_hash("ws")) == 16
+    assert bench.stored_traffic("ws", "no_such_workload") is None
+
+
+def _rank_main(rank, world, port, q):
+    os.environ.update({"RANK": str(rank), "WORLD_SIZE": str(world), "LOCAL_RANK": str(rank),
+                       "MASTER_ADDR": "127.0.0.1", "MASTER_PORT": str(port)})
+    r, ws, local, barrier, gather = bench._dist()
+    barrier()
+    times = gather(0.25 * (r + 1))
+    barrier()
+    q.put((r, ws, times))
+    import torch.distributed as dist
+    dist.destroy_process_group()
+
+
+def test_two_rank_gloo_gather_and_aggregate():
+    if torch.cuda.is_available():
+        pytest.skip("the CPU (gloo) path is exercised on hosts without a GPU")
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    out = [q.get(timeout=120) for _ in range(2)]
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for r, ws, times in out:
+        assert ws == 2 and times == [0.25, 0.5]
+    t, rate = bench.aggregate(out[0][2], 10.0)
+    assert t == 0.5 and rate == pytest.approx(40.0)
+
+
+def test_reference_arm_prints_one_line_under_torchrun():
+    if torch.cuda.is_available():
+        pytest.skip("the CPU (gloo) path is exercised on hosts without a GPU")
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+           "--master-addr", "127.0.0.1", "--master-port", str(_free_port()), os.path.join(ROOT, "bench.py"),
+           "--impl", "reference", "--gpus", "2", "--steps", "3", "--warmup", "3",
+           "--workload", "single_tile_128x128x64_f16_f32"]
+    r = subprocess.run(cmd, capture_output=True, text=True, timeout=300, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["unit"] == "TFLOP/s" and d["value"] > 0
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["e2e"]["h2d_bytes_per_step"] == 0

@@ -66,6 +66,7 @@ SHAPES = {
     gemm.S8: [(300, 520, 200), (700, 1288, 264), (1, 264, 72)],
     gemm.S9: [(300, 520, 200), (1100, 1288, 264)],
     gemm.GEMV: [(1, 1000, 520), (3, 264, 72), (8, 1000, 520), (16, 96, 1024)],
+    gemm.GEMV_TC: [(1, 1000, 520), (3, 264, 72), (8, 1000, 4104), (16, 96, 1024)],
 }
 CASES = [(v, s) for v, shapes in SHAPES.items() for s in shapes]
 IDS = ["%s-%dx%dx%d" % (gemm.VARIANT_NAMES[v], *s) for v, s in CASES]
