@@ -287,7 +287,7 @@ def cpu_oracle_rate(w: inputs.Workload, budget_s: float = 12.0) -> dict:
 def _dist():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     if ws <= 1:
-        return 0, 1, 0, (lambda: None), (lambda xs: xs)
+        return 0, 1, 0, (lambda: None), (lambda x: [x])
     import torch.distributed as dist
     rank = int(os.environ["RANK"])
     local = int(os.environ.get("LOCAL_RANK", rank))
@@ -315,6 +315,8 @@ def main(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(inputs.WORKLOADS))
     ap.add_argument("--variant", type=int, default=0)
+    ap.add_argument("--shape", default=None,
+                    help="M,N,K[,in,out]: a custom bf16 GEMM shape instead of a named workload (profiling)")
     ap.add_argument("--no-extra", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -322,6 +324,12 @@ def main(argv=None):
     if args.warmup < 3:
         ap.error("at least 3 warm-up steps")
     w = inputs.WORKLOADS[args.workload]
+    if args.shape:
+        f = args.shape.split(",")
+        M, N, K = (int(x) for x in f[:3])
+        ti, to = (f[3], f[4]) if len(f) >= 5 else ("bf16", "bf16")
+        w = inputs.Workload("custom_%dx%dx%d_%s_%s" % (M, N, K, ti, to), M, N, K, ti, to,
+                            inputs.N002, inputs.N002, 7)
     rank, world, local, barrier, gather = _dist()
 
     if args.impl == "reference":

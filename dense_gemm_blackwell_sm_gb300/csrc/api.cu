@@ -31,11 +31,20 @@ struct gemm_plan_s {
   uint32_t debug_flags;
   uint32_t* scratch;  // [0] status word, [1] tile counter, [2] finished counter
   int32_t* visits;
-  const void* mapA;
-  const void* mapB;
-  void* mapC;
-  bool maps_valid;
-  CUtensorMap tmA, tmB, tmC;
+  dgb::LaunchSpec spec;   // kernel, launch shape and SMEM, fixed at plan time
+  dgb::KParams kbase;     // kernel parameters that do not depend on the pointers
+  dgb::TgParams tgbase;   // same, for the tensor-core GEMV
+  // TMA descriptors by operand role (0 = A, 1 = B, 2 = C) and pointer, least
+  // recently used replaced first, so rotating between buffers re-encodes nothing
+  struct MapEntry {
+    const void* ptr;
+    int role;
+    uint64_t used;
+    CUtensorMap map;
+  };
+  static constexpr int kMapCache = 24;
+  MapEntry maps[kMapCache];
+  uint64_t map_clock;
 };
 
 namespace {
@@ -115,13 +124,60 @@ gemm_status_t current_device(int* dev, int* sms) {
 
 int ceil_div(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }
 
-// Automatic variant: the decode GEMV for a handful of rows, otherwise the
-// CTA-pair kernel, or the plain-store persistent kernel when C's rows are not
-// 16-byte aligned for TMA stores.
-int auto_variant(int64_t M, int64_t N, int64_t K, gemm_dtype_t dt) {
+// Automatic variant: the decode GEMV for a handful of rows; the plain-store
+// persistent kernel when C's rows are not 16-byte aligned for TMA stores;
+// otherwise the largest warp-specialised tile (step 9's 512x256 cluster tile,
+// then step 8's 256x256, then step 7's 128x256) that still gives every CTA pair
+// of the GPU at least one tile.
+int auto_variant(int64_t M, int64_t N, int64_t K, gemm_dtype_t dt, int sms) {
   if (M <= 16 && gemv_smem_bytes((int)M, (int)K) <= 200 * 1024) return GEMM_VARIANT_GEMV;
   if (!c_rows_tma_ok(N, dt)) return GEMM_VARIANT_S6_PERSISTENT;
-  return GEMM_VARIANT_S8_CTA_PAIR;
+  const int64_t tn = (N + 255) / 256;
+  const int64_t pairs = std::max(1, sms / 2);
+  if (((M + 511) / 512) * tn >= pairs) return GEMM_VARIANT_S9_TWO_CONSUMERS;
+  if (((M + 255) / 256) * tn >= pairs) return GEMM_VARIANT_S8_CTA_PAIR;
+  return GEMM_VARIANT_S7_WARP_SPECIALIZED;
+}
+
+bool is_ws(int v) { return v >= GEMM_VARIANT_S7_WARP_SPECIALIZED && v <= GEMM_VARIANT_S9_TWO_CONSUMERS; }
+
+// Fix the kernel, its launch shape and its pointer-independent parameters.
+gemm_status_t prepare_launch(gemm_plan_s* p) {
+  cudaError_t e = cudaSuccess;
+  const int v = p->variant;
+  if (v == GEMM_VARIANT_GEMV) {
+    e = spec_gemv((int)p->M, (int)p->N, (int)p->K, p->in_bf16, p->out_f32, p->num_sms, &p->spec);
+  } else if (v == GEMM_VARIANT_GEMV_TC) {
+    e = spec_gemv_tc((int)p->M, (int)p->N, (int)p->K, p->in_bf16, p->out_f32, p->num_sms, &p->spec, &p->tgbase);
+    p->tgbase.timeout_ns = p->timeout_ns;
+  } else {
+    KParams& k = p->kbase;
+    k.M = (int32_t)p->M;
+    k.N = (int32_t)p->N;
+    k.K = (int32_t)p->K;
+    k.tiles_m = p->tiles_m;
+    k.tiles_n = p->tiles_n;
+    k.raster_group = p->raster_group;
+    k.stages = p->stages;
+    k.timeout_ns = p->timeout_ns;
+    k.debug_flags = p->debug_flags;
+    k.out_ld = (int32_t)p->N;
+    k.idesc = is_ws(v) ? make_idesc(p->in_bf16, 128 * p->cg, 256) : make_idesc(p->in_bf16, 128, 128);
+    if (v <= GEMM_VARIANT_S3_MULTI_CTA) {
+      e = spec_step123((int)p->M, (int)p->N, p->out_f32, &p->spec);
+    } else if (v <= GEMM_VARIANT_S5_PIPELINE) {
+      e = spec_step45((int)p->M, (int)p->N, p->stages, p->out_f32, &p->spec);
+    } else if (v == GEMM_VARIANT_S6_PERSISTENT) {
+      e = spec_step6(p->sched - 1, p->stages, p->out_f32, p->grid_units, &p->spec);
+    } else {
+      e = spec_ws(p->cg, p->consumers, p->sched - 1, p->out_f32, p->stages, p->grid_units, &p->spec);
+    }
+  }
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return GEMM_ERR_CUDA;
+  }
+  return GEMM_OK;
 }
 
 gemm_status_t build_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, const gemm_opts_t* opts,
@@ -134,7 +190,10 @@ gemm_status_t build_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, co
       o.stages < 0 || o.stages > 8 || o.raster_group < 0 || o.max_ctas < 0 || o.timeout_ns < 0)
     return GEMM_ERR_INVALID_ARG;
 
-  int variant = o.variant ? o.variant : auto_variant(M, N, K, dtype);
+  int dev = 0, sms = 0;
+  st = current_device(&dev, &sms);
+  if (st != GEMM_OK && !o.variant) return st;
+  int variant = o.variant ? o.variant : auto_variant(M, N, K, dtype, sms);
   // shape limits of the individual steps
   if (variant == GEMM_VARIANT_S1_SINGLE_TILE && (M > 128 || N > 128 || K > 64)) return GEMM_ERR_UNSUPPORTED_SHAPE;
   if (variant == GEMM_VARIANT_S2_KLOOP && (M > 128 || N > 128)) return GEMM_ERR_UNSUPPORTED_SHAPE;
@@ -144,9 +203,6 @@ gemm_status_t build_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, co
   if (variant == GEMM_VARIANT_GEMV && (M > 16 || gemv_smem_bytes((int)M, (int)K) > 200 * 1024))
     return GEMM_ERR_UNSUPPORTED_SHAPE;
   if (variant == GEMM_VARIANT_GEMV_TC && M > 16) return GEMM_ERR_UNSUPPORTED_SHAPE;
-
-  int dev = 0, sms = 0;
-  st = current_device(&dev, &sms);
   if (st != GEMM_OK) return st;
 
   gemm_plan_s* p = new (std::nothrow) gemm_plan_s();
@@ -222,6 +278,11 @@ gemm_status_t build_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, co
     p->grid_units = tiles;
   }
 
+  st = prepare_launch(p);
+  if (st != GEMM_OK) {
+    delete p;
+    return st;
+  }
   if (cudaMalloc(reinterpret_cast<void**>(&p->scratch), 256) != cudaSuccess) {
     cudaGetLastError();
     delete p;
@@ -232,102 +293,91 @@ gemm_status_t build_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, co
     delete p;
     return GEMM_ERR_CUDA;
   }
+  p->kbase.status = p->scratch;
+  p->tgbase.status = p->scratch;
   *out = p;
   return GEMM_OK;
 }
 
-gemm_status_t refresh_maps(gemm_plan_s* p, const void* A, const void* B, void* C) {
-  if (p->maps_valid && p->mapA == A && p->mapB == B && p->mapC == C) return GEMM_OK;
+// The TMA descriptor of one operand, from the plan's cache or freshly encoded.
+const CUtensorMap* operand_map(gemm_plan_s* p, int role, const void* ptr) {
+  gemm_plan_s::MapEntry* victim = &p->maps[0];
+  for (auto& m : p->maps) {
+    if (m.ptr == ptr && m.role == role && m.used != 0) {
+      m.used = ++p->map_clock;
+      return &m.map;
+    }
+    if (m.used < victim->used) victim = &m;
+  }
   const CUtensorMapDataType in_t = p->in_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-  if (p->variant == GEMM_VARIANT_GEMV_TC) {
-    if (!encode_2d(&p->tmB, in_t, 2, B, (uint64_t)p->K, (uint64_t)p->N, 64, 128)) return GEMM_ERR_CUDA;
-    p->mapA = A;
-    p->mapB = B;
-    p->mapC = C;
-    p->maps_valid = true;
-    return GEMM_OK;
+  bool ok = false;
+  if (role == 0) {
+    ok = encode_2d(&victim->map, in_t, 2, ptr, (uint64_t)p->K, (uint64_t)p->M, 64, 128);
+  } else if (role == 1) {
+    const uint32_t rows = is_ws(p->variant) ? (uint32_t)ws_shape(p->cg, p->consumers).b_box_rows : 128u;
+    ok = encode_2d(&victim->map, in_t, 2, ptr, (uint64_t)p->K, (uint64_t)p->N, 64, rows);
+  } else {
+    ok = p->out_f32 ? encode_2d(&victim->map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, ptr, (uint64_t)p->N,
+                                (uint64_t)p->M, 32, 32)
+                    : encode_2d(&victim->map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ptr, (uint64_t)p->N,
+                                (uint64_t)p->M, 64, 32);
   }
-  uint32_t a_rows = 128, b_rows = 128;
-  if (p->variant >= GEMM_VARIANT_S7_WARP_SPECIALIZED && p->variant <= GEMM_VARIANT_S9_TWO_CONSUMERS) {
-    const WsShape sh = ws_shape(p->cg, p->consumers);
-    a_rows = (uint32_t)sh.a_box_rows;
-    b_rows = (uint32_t)sh.b_box_rows;
+  if (!ok) {
+    victim->used = 0;
+    return nullptr;
   }
-  if (!encode_2d(&p->tmA, in_t, 2, A, (uint64_t)p->K, (uint64_t)p->M, 64, a_rows) ||
-      !encode_2d(&p->tmB, in_t, 2, B, (uint64_t)p->K, (uint64_t)p->N, 64, b_rows))
-    return GEMM_ERR_CUDA;
-  if (p->variant >= GEMM_VARIANT_S7_WARP_SPECIALIZED && p->variant <= GEMM_VARIANT_S9_TWO_CONSUMERS) {
-    const bool ok = p->out_f32
-                        ? encode_2d(&p->tmC, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, C, (uint64_t)p->N,
-                                    (uint64_t)p->M, 32, 32)
-                        : encode_2d(&p->tmC, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, C, (uint64_t)p->N,
-                                    (uint64_t)p->M, 64, 32);
-    if (!ok) return GEMM_ERR_CUDA;
-  }
-  p->mapA = A;
-  p->mapB = B;
-  p->mapC = C;
-  p->maps_valid = true;
-  return GEMM_OK;
+  victim->ptr = ptr;
+  victim->role = role;
+  victim->used = ++p->map_clock;
+  return &victim->map;
 }
 
 gemm_status_t launch_plan(gemm_plan_s* p, const void* A, const void* B, void* C, cudaStream_t s) {
   if (!A || !B || !C) return GEMM_ERR_INVALID_ARG;
   if (!aligned16(A) || !aligned16(B) || !aligned16(C)) return GEMM_ERR_MISALIGNED;
   int cur = -1;
-  if (cudaGetDevice(&cur) != cudaSuccess) return GEMM_ERR_CUDA;
-  if (cur != p->device) return GEMM_ERR_INVALID_ARG;
+  if (cudaGetDevice(&cur) != cudaSuccess || cur != p->device) return GEMM_ERR_INVALID_ARG;
   cudaError_t e = cudaSuccess;
-
-  if (p->variant == GEMM_VARIANT_GEMV) {
-    GemvParams g{A, B, C, (int32_t)p->M, (int32_t)p->N, (int32_t)p->K};
-    e = launch_gemv(g, p->in_bf16, p->out_f32, p->num_sms, s);
-    return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
-  }
-  if (p->variant == GEMM_VARIANT_GEMV_TC) {
-    gemm_status_t st = refresh_maps(p, A, B, C);
-    if (st != GEMM_OK) return st;
-    GemvParams g{A, B, C, (int32_t)p->M, (int32_t)p->N, (int32_t)p->K};
-    e = launch_gemv_tc(g, p->tmB, p->in_bf16, p->out_f32, p->num_sms, p->scratch, p->timeout_ns, s);
-    if (e != cudaSuccess) {
-      cudaGetLastError();
-      return GEMM_ERR_CUDA;
+  switch (p->spec.kind) {
+    case ARGS_GEMV: {
+      GemvParams g{A, B, C, (int32_t)p->M, (int32_t)p->N, (int32_t)p->K};
+      void* args[] = {&g};
+      e = launch_spec(p->spec, args, s);
+      break;
     }
-    return GEMM_OK;
-  }
-
-  KParams k{};
-  k.M = (int32_t)p->M;
-  k.N = (int32_t)p->N;
-  k.K = (int32_t)p->K;
-  k.tiles_m = p->tiles_m;
-  k.tiles_n = p->tiles_n;
-  k.raster_group = p->raster_group;
-  k.stages = p->stages;
-  k.status = p->scratch;
-  k.visits = p->visits;
-  k.timeout_ns = p->timeout_ns;
-  k.debug_flags = p->debug_flags;
-  k.out_ld = (int32_t)p->N;
-  k.A = static_cast<const uint16_t*>(A);
-  k.B = static_cast<const uint16_t*>(B);
-  k.C = C;
-
-  if (p->variant <= GEMM_VARIANT_S3_MULTI_CTA) {
-    k.idesc = make_idesc(p->in_bf16, 128, 128);
-    e = launch_step123(k, p->out_f32, s);
-  } else {
-    gemm_status_t st = refresh_maps(p, A, B, C);
-    if (st != GEMM_OK) return st;
-    if (p->variant <= GEMM_VARIANT_S5_PIPELINE) {
-      k.idesc = make_idesc(p->in_bf16, 128, 128);
-      e = launch_step45(k, p->tmA, p->tmB, p->out_f32, s);
-    } else if (p->variant == GEMM_VARIANT_S6_PERSISTENT) {
-      k.idesc = make_idesc(p->in_bf16, 128, 128);
-      e = launch_step6(k, p->tmA, p->tmB, p->out_f32, p->sched - 1, p->grid_units, s);
-    } else {
-      k.idesc = make_idesc(p->in_bf16, 128 * p->cg, 256);
-      e = launch_ws(p->cg, p->consumers, p->sched - 1, k, p->tmA, p->tmB, p->tmC, p->out_f32, p->grid_units, s);
+    case ARGS_B_TG: {
+      const CUtensorMap* mb = operand_map(p, 1, B);
+      if (!mb) return GEMM_ERR_CUDA;
+      TgParams t = p->tgbase;
+      t.X = static_cast<const uint16_t*>(A);
+      t.Y = C;
+      void* args[] = {const_cast<CUtensorMap*>(mb), &t};
+      e = launch_spec(p->spec, args, s);
+      break;
+    }
+    default: {
+      KParams k = p->kbase;
+      k.visits = p->visits;
+      k.A = static_cast<const uint16_t*>(A);
+      k.B = static_cast<const uint16_t*>(B);
+      k.C = C;
+      if (p->spec.kind == ARGS_K) {
+        void* args[] = {&k};
+        e = launch_spec(p->spec, args, s);
+        break;
+      }
+      const CUtensorMap* ma = operand_map(p, 0, A);
+      const CUtensorMap* mb = operand_map(p, 1, B);
+      if (!ma || !mb) return GEMM_ERR_CUDA;
+      if (p->spec.kind == ARGS_AB_K) {
+        void* args[] = {const_cast<CUtensorMap*>(ma), const_cast<CUtensorMap*>(mb), &k};
+        e = launch_spec(p->spec, args, s);
+      } else {
+        const CUtensorMap* mc = operand_map(p, 2, C);
+        if (!mc) return GEMM_ERR_CUDA;
+        void* args[] = {const_cast<CUtensorMap*>(ma), const_cast<CUtensorMap*>(mb), const_cast<CUtensorMap*>(mc), &k};
+        e = launch_spec(p->spec, args, s);
+      }
     }
   }
   if (e != cudaSuccess) {
@@ -456,10 +506,8 @@ gemm_status_t gemm_plan_info(gemm_plan_t p, gemm_plan_info_t* info) {
   info->tile_n = p->tile_n;
   info->cluster = p->cg;
   info->consumers = p->consumers;
-  info->grid = (p->variant >= GEMM_VARIANT_S7_WARP_SPECIALIZED && p->variant <= GEMM_VARIANT_S9_TWO_CONSUMERS)
-                   ? p->grid_units * p->cg
-                   : p->grid_units;
-  info->smem_bytes = (int32_t)p->smem;
+  info->grid = (int32_t)(p->spec.grid.x * p->spec.grid.y);
+  info->smem_bytes = (int32_t)p->spec.smem;
   info->num_sms = p->num_sms;
   info->tiles = p->tiles_m * p->tiles_n;
   return GEMM_OK;

@@ -130,9 +130,9 @@ __global__ void __launch_bounds__(GV_THREADS) k_gemv(GemvParams g) {
 }
 
 template <typename InT, typename OutT, int MT, int R>
-cudaError_t launch_t(const GemvParams& g, int num_sms, cudaStream_t st) {
+cudaError_t spec_t(int N, int K, int num_sms, LaunchSpec* out) {
   auto k = k_gemv<InT, OutT, MT, R>;
-  const size_t smem = (size_t)MT * (size_t)(g.K / 8) * 16;
+  const size_t smem = (size_t)MT * (size_t)(K / 8) * 16;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   int per_sm = 0;
@@ -140,19 +140,23 @@ cudaError_t launch_t(const GemvParams& g, int num_sms, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   if (per_sm < 1) return cudaErrorInvalidConfiguration;
   const int rows_per_block = (GV_THREADS / 32) * R;
-  const int need = (g.N + rows_per_block - 1) / rows_per_block;
-  const int grid = std::max(1, std::min(need, per_sm * num_sms));
-  k<<<grid, GV_THREADS, smem, st>>>(g);
-  return cudaGetLastError();
+  const int need = (N + rows_per_block - 1) / rows_per_block;
+  out->func = (const void*)k;
+  out->grid = dim3((unsigned)std::max(1, std::min(need, per_sm * num_sms)), 1, 1);
+  out->block = dim3(GV_THREADS, 1, 1);
+  out->smem = smem;
+  out->cluster = 1;
+  out->kind = ARGS_GEMV;
+  return cudaSuccess;
 }
 
 template <typename InT, typename OutT>
-cudaError_t launch_m(const GemvParams& g, int num_sms, cudaStream_t st) {
-  if (g.M <= 1) return launch_t<InT, OutT, 1, 2>(g, num_sms, st);
-  if (g.M <= 2) return launch_t<InT, OutT, 2, 2>(g, num_sms, st);
-  if (g.M <= 4) return launch_t<InT, OutT, 4, 1>(g, num_sms, st);
-  if (g.M <= 8) return launch_t<InT, OutT, 8, 1>(g, num_sms, st);
-  return launch_t<InT, OutT, 16, 1>(g, num_sms, st);
+cudaError_t spec_m(int M, int N, int K, int num_sms, LaunchSpec* out) {
+  if (M <= 1) return spec_t<InT, OutT, 1, 2>(N, K, num_sms, out);
+  if (M <= 2) return spec_t<InT, OutT, 2, 2>(N, K, num_sms, out);
+  if (M <= 4) return spec_t<InT, OutT, 4, 1>(N, K, num_sms, out);
+  if (M <= 8) return spec_t<InT, OutT, 8, 1>(N, K, num_sms, out);
+  return spec_t<InT, OutT, 16, 1>(N, K, num_sms, out);
 }
 
 }  // namespace
@@ -162,12 +166,12 @@ size_t gemv_smem_bytes(int M, int K) {
   return (size_t)mt * (size_t)(K / 8) * 16;
 }
 
-cudaError_t launch_gemv(const GemvParams& g, bool in_bf16, bool out_f32, int num_sms, cudaStream_t st) {
+cudaError_t spec_gemv(int M, int N, int K, bool in_bf16, bool out_f32, int num_sms, LaunchSpec* out) {
   if (in_bf16) {
-    return out_f32 ? launch_m<__nv_bfloat16, float>(g, num_sms, st)
-                   : launch_m<__nv_bfloat16, __nv_bfloat16>(g, num_sms, st);
+    return out_f32 ? spec_m<__nv_bfloat16, float>(M, N, K, num_sms, out)
+                   : spec_m<__nv_bfloat16, __nv_bfloat16>(M, N, K, num_sms, out);
   }
-  return out_f32 ? launch_m<__half, float>(g, num_sms, st) : launch_m<__half, __nv_bfloat16>(g, num_sms, st);
+  return out_f32 ? spec_m<__half, float>(M, N, K, num_sms, out) : spec_m<__half, __nv_bfloat16>(M, N, K, num_sms, out);
 }
 
 }  // namespace dgb

@@ -30,18 +30,6 @@ constexpr uint32_t TG_B_BYTES = 128u * 128u;  // one weight box: 128 rows x 64 K
 constexpr uint32_t TG_X_BYTES = 16u * 128u;   // one activation tile: 16 rows x 64 K
 constexpr int TG_MAX_STAGES = 8;
 
-struct TgParams {
-  const uint16_t* X;
-  void* Y;
-  int32_t M, N, K;
-  int32_t kblocks_per_cta;  // K blocks in one CTA's slice
-  int32_t split;            // CTAs per cluster along K
-  int32_t stages;
-  uint32_t idesc;
-  uint32_t* status;
-  uint64_t timeout_ns;
-};
-
 template <typename OutT>
 __global__ void __launch_bounds__(TG_THREADS, 1)
     k_gemv_tc(const __grid_constant__ CUtensorMap tmB, TgParams p) {
@@ -214,38 +202,28 @@ size_t gemv_tc_smem_bytes(int N, int K, int num_sms) {
   return tg_smem(st, ks);
 }
 
-cudaError_t launch_gemv_tc(const GemvParams& g, const CUtensorMap& tmB, bool in_bf16, bool out_f32,
-                           int num_sms, uint32_t* status, uint64_t timeout_ns, cudaStream_t st) {
+cudaError_t spec_gemv_tc(int M, int N, int K, bool in_bf16, bool out_f32, int num_sms, LaunchSpec* out,
+                         TgParams* base) {
   TgParams p{};
-  p.X = static_cast<const uint16_t*>(g.X);
-  p.Y = g.Y;
-  p.M = g.M;
-  p.N = g.N;
-  p.K = g.K;
-  gemv_tc_config(g.N, g.K, num_sms, &p.split, &p.stages, &p.kblocks_per_cta);
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  gemv_tc_config(N, K, num_sms, &p.split, &p.stages, &p.kblocks_per_cta);
   const uint32_t ab = in_bf16 ? 1u : 0u;
+  // instruction descriptor: f32 accumulate, fp16/bf16 operands, K-major, M = 128, N = 16
   p.idesc = (1u << 4) | (ab << 7) | (ab << 10) | ((uint32_t)(16 >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
-  p.status = status;
-  p.timeout_ns = timeout_ns;
   const size_t smem = tg_smem(p.stages, p.kblocks_per_cta);
-  void* k = out_f32 ? reinterpret_cast<void*>(k_gemv_tc<float>) : reinterpret_cast<void*>(k_gemv_tc<__nv_bfloat16>);
+  const void* k = out_f32 ? (const void*)k_gemv_tc<float> : (const void*)k_gemv_tc<__nv_bfloat16>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  cudaLaunchConfig_t cfg{};
-  const int rbs = (g.N + 127) / 128;
-  cfg.gridDim = dim3((unsigned)(rbs * p.split), 1, 1);
-  cfg.blockDim = dim3(TG_THREADS, 1, 1);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = (unsigned)p.split;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  void* args[] = {const_cast<CUtensorMap*>(&tmB), &p};
-  return cudaLaunchKernelExC(&cfg, k, args);
+  out->func = k;
+  out->grid = dim3((unsigned)(((N + 127) / 128) * p.split), 1, 1);
+  out->block = dim3(TG_THREADS, 1, 1);
+  out->smem = smem;
+  out->cluster = (unsigned)p.split;
+  out->kind = ARGS_B_TG;
+  *base = p;
+  return cudaSuccess;
 }
 
 }  // namespace dgb

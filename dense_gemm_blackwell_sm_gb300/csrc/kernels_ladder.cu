@@ -365,65 +365,68 @@ __global__ void __launch_bounds__(LT_THREADS, 1) k_step6(const __grid_constant__
 }  // namespace
 
 // ---------------------------------------------------------------------------
-// host launchers
+// launch specs (made once per plan)
 
 static size_t ladder_smem(int stages) {
   return 1024 + (size_t)stages * 2 * LT_TILE_BYTES + (size_t)(2 * stages + 2) * 8 + 64;
 }
 
-cudaError_t launch_step123(const KParams& p, bool out_f32, cudaStream_t st) {
-  const dim3 grid((p.N + LT_N - 1) / LT_N, (p.M + LT_M - 1) / LT_M);
-  const size_t smem = ladder_smem(1);
-  if (out_f32) {
-    auto k = k_step123<float>;
-    cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    k<<<grid, LT_THREADS, smem, st>>>(p);
-  } else {
-    auto k = k_step123<__nv_bfloat16>;
-    cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    k<<<grid, LT_THREADS, smem, st>>>(p);
-  }
-  return cudaGetLastError();
-}
-
-cudaError_t launch_step45(const KParams& p, const CUtensorMap& tmA, const CUtensorMap& tmB,
-                          bool out_f32, cudaStream_t st) {
-  const dim3 grid((p.N + LT_N - 1) / LT_N, (p.M + LT_M - 1) / LT_M);
-  const size_t smem = ladder_smem(p.stages);
-  if (out_f32) {
-    auto k = k_step45<float>;
-    cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    k<<<grid, LT_THREADS, smem, st>>>(tmA, tmB, p);
-  } else {
-    auto k = k_step45<__nv_bfloat16>;
-    cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    k<<<grid, LT_THREADS, smem, st>>>(tmA, tmB, p);
-  }
-  return cudaGetLastError();
-}
-
-template <typename OutT, int SCHED>
-static cudaError_t launch6_t(const KParams& p, const CUtensorMap& tmA, const CUtensorMap& tmB,
-                             int grid, cudaStream_t st) {
-  auto k = k_step6<OutT, SCHED>;
-  const size_t smem = ladder_smem(p.stages) + 32;
-  cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  k<<<grid, LT_THREADS, smem, st>>>(tmA, tmB, p);
-  return cudaGetLastError();
-}
-
 size_t step6_smem_bytes(int stages) { return ladder_smem(stages) + 32; }
 
-cudaError_t launch_step6(const KParams& p, const CUtensorMap& tmA, const CUtensorMap& tmB,
-                         bool out_f32, int sched, int grid, cudaStream_t st) {
+static cudaError_t finish_spec(const void* k, dim3 grid, size_t smem, int kind, LaunchSpec* out) {
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  out->func = k;
+  out->grid = grid;
+  out->block = dim3(LT_THREADS, 1, 1);
+  out->smem = smem;
+  out->cluster = 1;
+  out->kind = kind;
+  return cudaSuccess;
+}
+
+cudaError_t spec_step123(int M, int N, bool out_f32, LaunchSpec* out) {
+  const dim3 grid((N + LT_N - 1) / LT_N, (M + LT_M - 1) / LT_M);
+  const void* k = out_f32 ? (const void*)k_step123<float> : (const void*)k_step123<__nv_bfloat16>;
+  return finish_spec(k, grid, ladder_smem(1), ARGS_K, out);
+}
+
+cudaError_t spec_step45(int M, int N, int stages, bool out_f32, LaunchSpec* out) {
+  const dim3 grid((N + LT_N - 1) / LT_N, (M + LT_M - 1) / LT_M);
+  const void* k = out_f32 ? (const void*)k_step45<float> : (const void*)k_step45<__nv_bfloat16>;
+  return finish_spec(k, grid, ladder_smem(stages), ARGS_AB_K, out);
+}
+
+cudaError_t spec_step6(int sched, int stages, bool out_f32, int grid, LaunchSpec* out) {
+  const void* k;
   if (out_f32) {
-    if (sched == S6_ATOMIC) return launch6_t<float, S6_ATOMIC>(p, tmA, tmB, grid, st);
-    if (sched == S6_CLC) return launch6_t<float, S6_CLC>(p, tmA, tmB, grid, st);
-    return launch6_t<float, S6_STATIC>(p, tmA, tmB, grid, st);
+    k = sched == S6_ATOMIC ? (const void*)k_step6<float, S6_ATOMIC>
+        : sched == S6_CLC  ? (const void*)k_step6<float, S6_CLC>
+                           : (const void*)k_step6<float, S6_STATIC>;
+  } else {
+    k = sched == S6_ATOMIC ? (const void*)k_step6<__nv_bfloat16, S6_ATOMIC>
+        : sched == S6_CLC  ? (const void*)k_step6<__nv_bfloat16, S6_CLC>
+                           : (const void*)k_step6<__nv_bfloat16, S6_STATIC>;
   }
-  if (sched == S6_ATOMIC) return launch6_t<__nv_bfloat16, S6_ATOMIC>(p, tmA, tmB, grid, st);
-  if (sched == S6_CLC) return launch6_t<__nv_bfloat16, S6_CLC>(p, tmA, tmB, grid, st);
-  return launch6_t<__nv_bfloat16, S6_STATIC>(p, tmA, tmB, grid, st);
+  return finish_spec(k, dim3((unsigned)grid, 1, 1), step6_smem_bytes(stages), ARGS_AB_K, out);
+}
+
+cudaError_t launch_spec(const LaunchSpec& s, void** args, cudaStream_t st) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = s.grid;
+  cfg.blockDim = s.block;
+  cfg.dynamicSmemBytes = s.smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  if (s.cluster > 1) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = s.cluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  return cudaLaunchKernelExC(&cfg, s.func, args);
 }
 
 }  // namespace dgb

@@ -453,20 +453,19 @@ int ws_max_active_clusters(int cg, int consumers, int sched, bool out_f32, int s
   return n;
 }
 
-cudaError_t launch_ws(int cg, int consumers, int sched, const KParams& p, const CUtensorMap& tmA,
-                      const CUtensorMap& tmB, const CUtensorMap& tmC, bool out_f32, int clusters,
-                      cudaStream_t st) {
+cudaError_t spec_ws(int cg, int consumers, int sched, bool out_f32, int stages, int clusters, LaunchSpec* out) {
   void* k = ws_kernel(cg, consumers, sched, out_f32);
   if (!k) return cudaErrorInvalidValue;
-  const size_t smem = ws_smem_bytes(cg, consumers, p.stages);
+  const size_t smem = ws_smem_bytes(cg, consumers, stages);
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t cfg = ws_config(cg, clusters, smem, st, attr);
-  KParams pc = p;
-  void* args[] = {const_cast<CUtensorMap*>(&tmA), const_cast<CUtensorMap*>(&tmB),
-                  const_cast<CUtensorMap*>(&tmC), &pc};
-  return cudaLaunchKernelExC(&cfg, k, args);
+  out->func = k;
+  out->grid = dim3((unsigned)(clusters * cg), 1, 1);
+  out->block = dim3(WS_THREADS, 1, 1);
+  out->smem = smem;
+  out->cluster = (unsigned)cg;
+  out->kind = ARGS_ABC_K;
+  return cudaSuccess;
 }
 
 }  // namespace dgb

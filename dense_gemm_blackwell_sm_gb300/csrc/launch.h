@@ -11,12 +11,33 @@ namespace dgb {
 
 struct KParams;
 
+// Everything needed to launch one kernel, fixed when a plan is made: the
+// function, its launch shape and dynamic shared memory (whose attribute is set
+// once, at plan time), and which argument list it takes.
+enum ArgKind {
+  ARGS_K = 0,      // (KParams)
+  ARGS_AB_K = 1,   // (tmA, tmB, KParams)
+  ARGS_ABC_K = 2,  // (tmA, tmB, tmC, KParams)
+  ARGS_GEMV = 3,   // (GemvParams)
+  ARGS_B_TG = 4,   // (tmB, TgParams)
+};
+
+struct LaunchSpec {
+  const void* func = nullptr;
+  dim3 grid{1, 1, 1};
+  dim3 block{1, 1, 1};
+  size_t smem = 0;
+  unsigned cluster = 1;  // CTAs per cluster along x
+  int kind = ARGS_K;
+};
+
+// one launch of a prepared kernel (cluster dimension attached when > 1)
+cudaError_t launch_spec(const LaunchSpec& s, void** args, cudaStream_t st);
+
 // steps 1-3 (thread copies), 4-5 (TMA ring), 6 (persistent + scheduler)
-cudaError_t launch_step123(const KParams& p, bool out_f32, cudaStream_t st);
-cudaError_t launch_step45(const KParams& p, const CUtensorMap& tmA, const CUtensorMap& tmB,
-                          bool out_f32, cudaStream_t st);
-cudaError_t launch_step6(const KParams& p, const CUtensorMap& tmA, const CUtensorMap& tmB,
-                         bool out_f32, int sched, int grid, cudaStream_t st);
+cudaError_t spec_step123(int M, int N, bool out_f32, LaunchSpec* out);
+cudaError_t spec_step45(int M, int N, int stages, bool out_f32, LaunchSpec* out);
+cudaError_t spec_step6(int sched, int stages, bool out_f32, int grid, LaunchSpec* out);
 size_t step6_smem_bytes(int stages);
 
 // steps 7-9: warp-specialised persistent kernels
@@ -36,12 +57,10 @@ struct WsShape {
 WsShape ws_shape(int cg, int consumers);
 size_t ws_smem_bytes(int cg, int consumers, int stages);
 int ws_max_stages(int cg, int consumers);
-cudaError_t launch_ws(int cg, int consumers, int sched, const KParams& p, const CUtensorMap& tmA,
-                      const CUtensorMap& tmB, const CUtensorMap& tmC, bool out_f32, int clusters,
-                      cudaStream_t st);
 int ws_max_active_clusters(int cg, int consumers, int sched, bool out_f32, int stages);
+cudaError_t spec_ws(int cg, int consumers, int sched, bool out_f32, int stages, int clusters, LaunchSpec* out);
 
-// decode GEMV, C (M x N) = X (M x K) * B^T for M <= 16
+// decode GEMV, C (M x N) = X (M x K) * B^T for M <= 16, on CUDA cores
 struct GemvParams {
   const void* X;
   const void* B;
@@ -49,12 +68,24 @@ struct GemvParams {
   int32_t M, N, K;
 };
 size_t gemv_smem_bytes(int M, int K);
+cudaError_t spec_gemv(int M, int N, int K, bool in_bf16, bool out_f32, int num_sms, LaunchSpec* out);
+
 // the same product on the Tensor Core (weight as the 128-row MMA operand),
 // K split over the CTAs of a cluster
+struct TgParams {
+  const uint16_t* X;
+  void* Y;
+  int32_t M, N, K;
+  int32_t kblocks_per_cta;  // K blocks in one CTA's slice
+  int32_t split;            // CTAs per cluster along K
+  int32_t stages;
+  uint32_t idesc;
+  uint32_t* status;
+  uint64_t timeout_ns;
+};
 void gemv_tc_config(int N, int K, int num_sms, int* split, int* stages, int* kblocks_per_cta);
 size_t gemv_tc_smem_bytes(int N, int K, int num_sms);
-cudaError_t launch_gemv_tc(const GemvParams& g, const CUtensorMap& tmB, bool in_bf16, bool out_f32,
-                           int num_sms, uint32_t* status, uint64_t timeout_ns, cudaStream_t st);
-cudaError_t launch_gemv(const GemvParams& g, bool in_bf16, bool out_f32, int num_sms, cudaStream_t st);
+cudaError_t spec_gemv_tc(int M, int N, int K, bool in_bf16, bool out_f32, int num_sms, LaunchSpec* out,
+                         TgParams* base);
 
 }  // namespace dgb
