@@ -107,7 +107,12 @@ class ClockSampler:
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self._t = threading.Thread(target=self._read, daemon=True)
             self._t.start()
-            time.sleep(0.3)
+            # NVML start-up can hold the driver for a moment: start timing only
+            # once the sampler is producing samples
+            t0 = time.time()
+            while not self.lines and time.time() - t0 < 10.0:
+                time.sleep(0.02)
+            time.sleep(0.1)
         except OSError:
             self.proc = None
         return self
