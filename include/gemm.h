@@ -142,6 +142,29 @@ GEMM_API gemm_status_t gemm_run_host(int64_t M, int64_t N, int64_t K, const void
                             const void* B_host, void* C_host, gemm_dtype_t dtype, void* dA,
                             void* dB, void* dC, gemm_stream_t stream);
 
+/* C = A * B^T like gemm_run, for callers that must not allocate memory while
+ * they compute: code running inside an allocator hook or an out-of-memory
+ * handler, while a memory pool is locked or being torn down, in a callback
+ * that must not re-enter the CUDA allocator, or in an embedder whose device
+ * memory is all pre-assigned.  The reading notes have no counterpart of this
+ * entry point; it exists for those callers only.
+ *
+ * It makes no plan and calls no cudaMalloc, cudaFree or other allocating
+ * routine: it runs the warp-specialised kernel of variants 7-9 with the atomic
+ * tile scheduler, whose scratch (a status word and two counters, 12 bytes)
+ * lives in a fixed 256-byte device array inside the library that every GPU
+ * loading the library keeps until the process exits; a shape whose scratch
+ * would exceed the array is refused with GEMM_ERR_UNSUPPORTED_SHAPE.  The first
+ * call on a device, with that device current, looks up the array's device
+ * address; make that first call before any stream capture.  Every call shares
+ * the array and clears it on `stream` before its kernel starts, so calls that
+ * overlap on the GPU (different streams, or different threads) race and must
+ * be serialised by the caller.  Needs N * sizeof(C element) % 16 == 0 besides
+ * the usual preconditions.  Asynchronous on `stream`; a device-side wait that
+ * times out leaves C undefined and is not reported by this entry point. */
+GEMM_API gemm_status_t gemm_run_noalloc(int64_t M, int64_t N, int64_t K, const void* A, const void* B,
+                                        void* C, gemm_dtype_t dtype, gemm_stream_t stream);
+
 /* Synchronise `stream`, then report (and clear) a device-side error recorded
  * by the plan's kernels.  plan == NULL checks every plan gemm_run cached. */
 GEMM_API gemm_status_t gemm_check(gemm_plan_t plan, gemm_stream_t stream);
