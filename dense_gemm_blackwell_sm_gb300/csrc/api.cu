@@ -24,6 +24,7 @@ struct gemm_plan_s {
   int variant, sched, stages, raster_group;
   int device, num_sms;
   int grid_units;  // CTAs (variants 3-6) or clusters (7-9) launched
+  int split_k;     // GEMV_TC: requested CTAs per 128-row block along K (0 = automatic)
   int cg, consumers;
   int tile_m, tile_n, tiles_m, tiles_n;
   size_t smem;
@@ -148,7 +149,8 @@ gemm_status_t prepare_launch(gemm_plan_s* p) {
   if (v == GEMM_VARIANT_GEMV) {
     e = spec_gemv((int)p->M, (int)p->N, (int)p->K, p->in_bf16, p->out_f32, p->num_sms, &p->spec);
   } else if (v == GEMM_VARIANT_GEMV_TC) {
-    e = spec_gemv_tc((int)p->M, (int)p->N, (int)p->K, p->in_bf16, p->out_f32, p->num_sms, &p->spec, &p->tgbase);
+    e = spec_gemv_tc((int)p->M, (int)p->N, (int)p->K, p->in_bf16, p->out_f32, p->num_sms, p->split_k, p->stages,
+                     &p->spec, &p->tgbase);
     p->tgbase.timeout_ns = p->timeout_ns;
   } else {
     KParams& k = p->kbase;
@@ -187,7 +189,8 @@ gemm_status_t build_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, co
   gemm_opts_t o{};
   if (opts) o = *opts;
   if (o.variant < 0 || o.variant > GEMM_VARIANT_GEMV_TC || o.sched < 0 || o.sched > GEMM_SCHED_CLC ||
-      o.stages < 0 || o.stages > 8 || o.raster_group < 0 || o.max_ctas < 0 || o.timeout_ns < 0)
+      o.stages < 0 || o.stages > 12 || o.raster_group < 0 || o.max_ctas < 0 || o.timeout_ns < 0 ||
+      o.split_k < 0 || o.split_k > 8)
     return GEMM_ERR_INVALID_ARG;
 
   int dev = 0, sms = 0;
@@ -247,15 +250,13 @@ gemm_status_t build_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, co
     p->smem = step6_smem_bytes(p->stages);
   }
   if (variant == GEMM_VARIANT_GEMV_TC) {
-    if (gemv_tc_smem_bytes((int)N, (int)K, sms) > 227 * 1024) {
-      delete p;
-      return GEMM_ERR_UNSUPPORTED_SHAPE;
-    }
     int split = 1, kpc = 1;
-    gemv_tc_config((int)N, (int)K, sms, &split, &p->stages, &kpc);
+    gemv_tc_config((int)N, (int)K, sms, o.split_k, o.stages, &split, &p->stages, &kpc);
     p->cg = split;
-    p->smem = gemv_tc_smem_bytes((int)N, (int)K, sms);
+    p->split_k = o.split_k;
+    p->smem = gemv_tc_smem_bytes(p->stages);
     p->tile_m = 16;
+    p->tile_n = 128;
   }
   p->tiles_m = ceil_div(M, p->tile_m);
   p->tiles_n = ceil_div(N, p->tile_n);
@@ -311,7 +312,10 @@ const CUtensorMap* operand_map(gemm_plan_s* p, int role, const void* ptr) {
   }
   const CUtensorMapDataType in_t = p->in_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   bool ok = false;
-  if (role == 0) {
+  if (role == 3) {
+    // activation rows of the tensor-core GEMV: 16-row boxes, rows >= M read as zero
+    ok = encode_2d(&victim->map, in_t, 2, ptr, (uint64_t)p->K, (uint64_t)p->M, 64, 16);
+  } else if (role == 0) {
     ok = encode_2d(&victim->map, in_t, 2, ptr, (uint64_t)p->K, (uint64_t)p->M, 64, 128);
   } else if (role == 1) {
     const uint32_t rows = is_ws(p->variant) ? (uint32_t)ws_shape(p->cg, p->consumers).b_box_rows : 128u;
@@ -345,13 +349,14 @@ gemm_status_t launch_plan(gemm_plan_s* p, const void* A, const void* B, void* C,
       e = launch_spec(p->spec, args, s);
       break;
     }
-    case ARGS_B_TG: {
+    case ARGS_BX_TG: {
       const CUtensorMap* mb = operand_map(p, 1, B);
-      if (!mb) return GEMM_ERR_CUDA;
+      const CUtensorMap* mx = operand_map(p, 3, A);
+      if (!mb || !mx) return GEMM_ERR_CUDA;
       TgParams t = p->tgbase;
       t.X = static_cast<const uint16_t*>(A);
       t.Y = C;
-      void* args[] = {const_cast<CUtensorMap*>(mb), &t};
+      void* args[] = {const_cast<CUtensorMap*>(mb), const_cast<CUtensorMap*>(mx), &t};
       e = launch_spec(p->spec, args, s);
       break;
     }

@@ -6,14 +6,15 @@
 // byte at M = 1).  With a few activation rows (M = 8) the CUDA cores would
 // still need 4 fp32 FMAs per weight byte, close to their own limit, so here
 // the MMA does the arithmetic: the weight tile (128 rows of B) is the
-// 128-row A operand of tcgen05.mma, the activations (M rows, zero-padded to 16)
-// are the 16-column B operand, and D[n][m] = sum_k B[n][k] X[m][k] lands in 16
-// TMEM columns.  Only the weight stream matters for time:
-//   * K is split over the CTAs of a cluster (up to 8): each CTA streams a
-//     128-row x K/split slab of B through a TMA ring, accumulating in TMEM;
-//   * the partial sums of the cluster are added in rank order through
-//     distributed shared memory by the leader CTA, which writes Y;
-//   * X's K-slice (16 x K/split) is staged once per CTA with plain loads.
+// 128-row A operand of tcgen05.mma, the activations (M rows, zero-filled by
+// TMA up to 16) are the 16-column B operand, and D[n][m] = sum_k B[n][k] X[m][k]
+// lands in 16 TMEM columns.  Only the weight stream matters for time:
+//   * one CTA per 128-row block of B, or, when that gives too few CTAs, a
+//     cluster of `split` CTAs that share the block's K range;
+//   * the producer starts the TMA ring (weight box + activation box per stage)
+//     right after barrier set-up, before anything else;
+//   * a split block's partial sums are added in rank order through
+//     distributed shared memory by the leader CTA, which writes Y.
 // No global scratch is used.
 #include <algorithm>
 
@@ -27,19 +28,18 @@ namespace {
 constexpr int TG_THREADS = 128;
 constexpr int TG_BK = 64;
 constexpr uint32_t TG_B_BYTES = 128u * 128u;  // one weight box: 128 rows x 64 K
-constexpr uint32_t TG_X_BYTES = 16u * 128u;   // one activation tile: 16 rows x 64 K
-constexpr int TG_MAX_STAGES = 8;
+constexpr uint32_t TG_X_BYTES = 16u * 128u;   // one activation box: 16 rows x 64 K
+constexpr uint32_t TG_STAGE = TG_B_BYTES + TG_X_BYTES;
+constexpr int TG_MAX_STAGES = 12;
 
 template <typename OutT>
 __global__ void __launch_bounds__(TG_THREADS, 1)
-    k_gemv_tc(const __grid_constant__ CUtensorMap tmB, TgParams p) {
+    k_gemv_tc(const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmX, TgParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align_1024(smem_raw);
   const int S = p.stages;
-  const int KS = p.kblocks_per_cta;
-  uint8_t* ring = smem;                                    // S x 16 KB
-  uint8_t* xs = ring + (size_t)S * TG_B_BYTES;             // KS x 2 KB
-  float* partial = reinterpret_cast<float*>(xs + (size_t)KS * TG_X_BYTES);  // 128 x 16 fp32
+  uint8_t* ring = smem;  // stage s: weight box at s*18K, activation box at s*18K + 16K
+  float* partial = reinterpret_cast<float*>(ring + (size_t)S * TG_STAGE);  // 128 x 16 fp32
   uint64_t* full = reinterpret_cast<uint64_t*>(partial + 128 * 16);
   uint64_t* empty = full + TG_MAX_STAGES;
   uint64_t* done = empty + TG_MAX_STAGES;
@@ -47,12 +47,12 @@ __global__ void __launch_bounds__(TG_THREADS, 1)
   volatile uint32_t* abort_flag = tmem_slot + 1;
 
   const uint32_t tid = threadIdx.x, warp = warp_idx(), lane = lane_idx();
-  const uint32_t rank = cluster_ctarank();
-  const int32_t rb = (int32_t)(blockIdx.x / (uint32_t)p.split);   // 128-row block of B / Y
+  const uint32_t rank = (p.split > 1) ? cluster_ctarank() : 0u;
+  const int32_t rb = (int32_t)(blockIdx.x / (uint32_t)p.split);  // 128-row block of B and Y
   const int32_t n0 = rb * 128;
   const int32_t KB = (p.K + TG_BK - 1) / TG_BK;
-  const int32_t kb0 = (int32_t)rank * KS;
-  const int32_t nkb = max(0, min(KS, KB - kb0));
+  const int32_t kb0 = (int32_t)rank * p.kblocks_per_cta;
+  const int32_t nkb = max(0, min(p.kblocks_per_cta, KB - kb0));
 
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
@@ -63,21 +63,12 @@ __global__ void __launch_bounds__(TG_THREADS, 1)
     *abort_flag = 0u;
     fence_mbar_init();
     tma_prefetch_desc(&tmB);
+    tma_prefetch_desc(&tmX);
   }
   if (warp == 0) {
     tmem_alloc<1>(smem_u32(tmem_slot), 32);
     tmem_relinquish<1>();
   }
-  // this CTA's activation slice, rows >= M zero, in the 128B-swizzled K-major layout
-  const int32_t K8 = p.K / 8;
-  for (int i = tid; i < nkb * 16 * 8; i += TG_THREADS) {
-    const int j = i / 128, r = (i / 8) & 15, c = i & 7;
-    const int32_t kc = (kb0 + j) * 8 + c;  // 16-byte chunk index along K
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (r < p.M && kc < K8) v = reinterpret_cast<const uint4*>(p.X)[(int64_t)r * K8 + kc];
-    *reinterpret_cast<uint4*>(xs + (size_t)j * TG_X_BYTES + sw128_offset((uint32_t)r, (uint32_t)c)) = v;
-  }
-  fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -85,13 +76,16 @@ __global__ void __launch_bounds__(TG_THREADS, 1)
   const WaitCtl w{abort_flag, p.status, p.timeout_ns, 0};
 
   if (warp == 0 && lane == 0) {
-    // producer
+    // producer: weight box + activation box per stage
     for (int32_t j = 0; j < nkb; ++j) {
       const int s = j % S;
       const uint32_t ph = (uint32_t)(j / S) & 1u;
       if (!mbar_wait(smem_u32(empty + s), ph ^ 1u, w, WAIT_PRODUCER_EMPTY)) break;
-      mbar_arrive_expect_tx(smem_u32(full + s), TG_B_BYTES);
-      tma_load_2d(smem_u32(ring + (size_t)s * TG_B_BYTES), &tmB, smem_u32(full + s), (kb0 + j) * TG_BK, n0);
+      const uint32_t fb = smem_u32(full + s);
+      mbar_arrive_expect_tx(fb, TG_STAGE);
+      uint8_t* st = ring + (size_t)s * TG_STAGE;
+      tma_load_2d(smem_u32(st), &tmB, fb, (kb0 + j) * TG_BK, n0);
+      tma_load_2d(smem_u32(st + TG_B_BYTES), &tmX, fb, (kb0 + j) * TG_BK, 0);
     }
   } else if (warp == 1 && lane == 0) {
     // MMA issuer
@@ -100,8 +94,8 @@ __global__ void __launch_bounds__(TG_THREADS, 1)
       const uint32_t ph = (uint32_t)(j / S) & 1u;
       if (!mbar_wait(smem_u32(full + s), ph, w, WAIT_MMA_FULL)) break;
       tc_fence_after();
-      const uint64_t ad = sdesc_k_sw128(smem_u32(ring + (size_t)s * TG_B_BYTES));
-      const uint64_t bd = sdesc_k_sw128(smem_u32(xs + (size_t)j * TG_X_BYTES));
+      const uint32_t sa = smem_u32(ring + (size_t)s * TG_STAGE);
+      const uint64_t ad = sdesc_k_sw128(sa), bd = sdesc_k_sw128(sa + TG_B_BYTES);
 #pragma unroll
       for (int k = 0; k < TG_BK / 16; ++k) mma_f16<1>(tmem, ad + 2 * k, bd + 2 * k, p.idesc, (j | k) != 0);
       mma_commit(smem_u32(empty + s));
@@ -109,55 +103,53 @@ __global__ void __launch_bounds__(TG_THREADS, 1)
     mma_commit(smem_u32(done));
   }
   __syncwarp();
-  // every thread: the slab's partial sums (row = TMEM lane) into shared memory
   bool ok = mbar_wait(smem_u32(done), 0, w, WAIT_LADDER_MMA);
   ok = __syncthreads_and(ok && *abort_flag == 0u) != 0;
-  const uint32_t row = warp * 32u + lane;
-  if (ok) {
+  const uint32_t row = warp * 32u + lane;  // TMEM lane = row of the block
+  float acc[16];
+#pragma unroll
+  for (int m = 0; m < 16; ++m) acc[m] = 0.f;
+  if (ok && nkb > 0) {
     tc_fence_after();
     uint32_t v[16];
     tmem_ld_32x32b_x16(tmem + ((warp * 32u) << 16), v);
     tmem_wait_ld();
-    float4* dst = reinterpret_cast<float4*>(partial + row * 16);
-    if (nkb > 0) {
 #pragma unroll
-      for (int q = 0; q < 4; ++q)
-        dst[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
-                             __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
-    } else {
-#pragma unroll
-      for (int q = 0; q < 4; ++q) dst[q] = make_float4(0.f, 0.f, 0.f, 0.f);
-    }
+    for (int m = 0; m < 16; ++m) acc[m] = __uint_as_float(v[m]);
   }
-  cluster_sync_all();
-  if (ok && rank == 0) {
-    // leader: add the cluster's partials in rank order and write Y
-    float acc[16];
+  if (p.split > 1) {
+    float4* dst = reinterpret_cast<float4*>(partial + row * 16);
 #pragma unroll
-    for (int m = 0; m < 16; ++m) acc[m] = 0.f;
-    const uint32_t my = smem_u32(partial + row * 16);
-    for (int r = 0; r < p.split; ++r) {
-      const uint32_t src = mapa_shared(my, (uint32_t)r);
+    for (int q = 0; q < 4; ++q) dst[q] = make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
+    cluster_sync_all();
+    if (rank == 0) {
+      // leader: add the cluster's partials in rank order
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const float4 f = ld_cluster_f32x4(src + 16u * q);
-        acc[4 * q] += f.x;
-        acc[4 * q + 1] += f.y;
-        acc[4 * q + 2] += f.z;
-        acc[4 * q + 3] += f.w;
+      for (int m = 0; m < 16; ++m) acc[m] = 0.f;
+      const uint32_t my = smem_u32(partial + row * 16);
+      for (int r = 0; r < p.split; ++r) {
+        const uint32_t src = mapa_shared(my, (uint32_t)r);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float4 f = ld_cluster_f32x4(src + 16u * q);
+          acc[4 * q] += f.x;
+          acc[4 * q + 1] += f.y;
+          acc[4 * q + 2] += f.z;
+          acc[4 * q + 3] += f.w;
+        }
       }
     }
-    const int32_t n = n0 + (int32_t)row;
-    if (n < p.N) {
-      OutT* Y = reinterpret_cast<OutT*>(p.Y);
+  }
+  const int32_t n = n0 + (int32_t)row;
+  if (ok && rank == 0 && n < p.N) {
+    OutT* Y = reinterpret_cast<OutT*>(p.Y);
 #pragma unroll
-      for (int m = 0; m < 16; ++m) {
-        if (m < p.M) {
-          if constexpr (sizeof(OutT) == 4) {
-            Y[(int64_t)m * p.N + n] = acc[m];
-          } else {
-            Y[(int64_t)m * p.N + n] = __float2bfloat16_rn(acc[m]);
-          }
+    for (int m = 0; m < 16; ++m) {
+      if (m < p.M) {
+        if constexpr (sizeof(OutT) == 4) {
+          Y[(int64_t)m * p.N + n] = acc[m];
+        } else {
+          Y[(int64_t)m * p.N + n] = __float2bfloat16_rn(acc[m]);
         }
       }
     }
@@ -166,7 +158,7 @@ __global__ void __launch_bounds__(TG_THREADS, 1)
     const uint64_t t0 = globaltimer_ns();
     while (globaltimer_ns() - t0 < 2000000ull) {}
   }
-  cluster_sync_all();  // peers keep their partials alive until the leader has read them
+  if (p.split > 1) cluster_sync_all();  // peers keep their partials until the leader has read them
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
@@ -175,44 +167,44 @@ __global__ void __launch_bounds__(TG_THREADS, 1)
   }
 }
 
-size_t tg_smem(int stages, int kblocks_per_cta) {
-  return 1024 + (size_t)stages * TG_B_BYTES + (size_t)kblocks_per_cta * TG_X_BYTES + 128 * 16 * 4 +
-         (2 * TG_MAX_STAGES + 1) * 8 + 16;
+size_t tg_smem(int stages) {
+  return 1024 + (size_t)stages * TG_STAGE + 128 * 16 * 4 + (2 * TG_MAX_STAGES + 1) * 8 + 16;
 }
 
 }  // namespace
 
-// split along K (CTAs per cluster) and ring depth for a decode shape
-void gemv_tc_config(int N, int K, int num_sms, int* split, int* stages, int* kblocks_per_cta) {
+// CTAs per 128-row block along K (`split`, a cluster when > 1) and ring depth:
+// the largest power-of-two split (at most 8) that keeps every CTA resident at
+// once with one CTA per SM, unless `want_split` asks for one.
+void gemv_tc_config(int N, int K, int num_sms, int want_split, int want_stages, int* split, int* stages,
+                    int* kblocks_per_cta) {
   const int KB = (K + TG_BK - 1) / TG_BK;
   const int rbs = (N + 127) / 128;
   int sp = 1;
-  while (sp < 8 && rbs * sp < 2 * num_sms && sp * 2 <= KB) sp *= 2;
-  const int ks = (KB + sp - 1) / sp;
-  int st = std::min(TG_MAX_STAGES, std::max(2, ks));
-  while (st > 2 && tg_smem(st, ks) > 200 * 1024) --st;
+  if (want_split > 0) {
+    while (sp * 2 <= want_split && sp < 8) sp *= 2;
+  } else {
+    while (sp < 8 && rbs * sp * 2 <= num_sms) sp *= 2;
+  }
+  while (sp > 1 && sp > KB) sp /= 2;
   *split = sp;
-  *stages = st;
-  *kblocks_per_cta = ks;
+  *kblocks_per_cta = (KB + sp - 1) / sp;
+  *stages = want_stages > 0 ? std::min(want_stages, TG_MAX_STAGES) : 8;
 }
 
-size_t gemv_tc_smem_bytes(int N, int K, int num_sms) {
-  int sp, st, ks;
-  gemv_tc_config(N, K, num_sms, &sp, &st, &ks);
-  return tg_smem(st, ks);
-}
+size_t gemv_tc_smem_bytes(int stages) { return tg_smem(stages); }
 
-cudaError_t spec_gemv_tc(int M, int N, int K, bool in_bf16, bool out_f32, int num_sms, LaunchSpec* out,
-                         TgParams* base) {
+cudaError_t spec_gemv_tc(int M, int N, int K, bool in_bf16, bool out_f32, int num_sms, int want_split,
+                         int want_stages, LaunchSpec* out, TgParams* base) {
   TgParams p{};
   p.M = M;
   p.N = N;
   p.K = K;
-  gemv_tc_config(N, K, num_sms, &p.split, &p.stages, &p.kblocks_per_cta);
+  gemv_tc_config(N, K, num_sms, want_split, want_stages, &p.split, &p.stages, &p.kblocks_per_cta);
   const uint32_t ab = in_bf16 ? 1u : 0u;
   // instruction descriptor: f32 accumulate, fp16/bf16 operands, K-major, M = 128, N = 16
   p.idesc = (1u << 4) | (ab << 7) | (ab << 10) | ((uint32_t)(16 >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
-  const size_t smem = tg_smem(p.stages, p.kblocks_per_cta);
+  const size_t smem = tg_smem(p.stages);
   const void* k = out_f32 ? (const void*)k_gemv_tc<float> : (const void*)k_gemv_tc<__nv_bfloat16>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
@@ -221,7 +213,7 @@ cudaError_t spec_gemv_tc(int M, int N, int K, bool in_bf16, bool out_f32, int nu
   out->block = dim3(TG_THREADS, 1, 1);
   out->smem = smem;
   out->cluster = (unsigned)p.split;
-  out->kind = ARGS_B_TG;
+  out->kind = ARGS_BX_TG;
   *base = p;
   return cudaSuccess;
 }

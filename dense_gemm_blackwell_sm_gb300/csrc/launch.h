@@ -19,7 +19,7 @@ enum ArgKind {
   ARGS_AB_K = 1,   // (tmA, tmB, KParams)
   ARGS_ABC_K = 2,  // (tmA, tmB, tmC, KParams)
   ARGS_GEMV = 3,   // (GemvParams)
-  ARGS_B_TG = 4,   // (tmB, TgParams)
+  ARGS_BX_TG = 4,  // (tmB, tmX, TgParams)
 };
 
 struct LaunchSpec {
@@ -83,9 +83,10 @@ struct TgParams {
   uint32_t* status;
   uint64_t timeout_ns;
 };
-void gemv_tc_config(int N, int K, int num_sms, int* split, int* stages, int* kblocks_per_cta);
-size_t gemv_tc_smem_bytes(int N, int K, int num_sms);
-cudaError_t spec_gemv_tc(int M, int N, int K, bool in_bf16, bool out_f32, int num_sms, LaunchSpec* out,
-                         TgParams* base);
+void gemv_tc_config(int N, int K, int num_sms, int want_split, int want_stages, int* split, int* stages,
+                    int* kblocks_per_cta);
+size_t gemv_tc_smem_bytes(int stages);
+cudaError_t spec_gemv_tc(int M, int N, int K, bool in_bf16, bool out_f32, int num_sms, int want_split,
+                         int want_stages, LaunchSpec* out, TgParams* base);
 
 }  // namespace dgb

@@ -42,7 +42,7 @@ class GemmError(RuntimeError):
 
 class Opts(ctypes.Structure):
     _fields_ = [("variant", ctypes.c_int32), ("sched", ctypes.c_int32), ("stages", ctypes.c_int32),
-                ("raster_group", ctypes.c_int32), ("max_ctas", ctypes.c_int32), ("reserved0", ctypes.c_int32),
+                ("raster_group", ctypes.c_int32), ("max_ctas", ctypes.c_int32), ("split_k", ctypes.c_int32),
                 ("timeout_ns", ctypes.c_int64), ("debug_flags", ctypes.c_int32),
                 ("reserved", ctypes.c_int32 * 7)]
 
@@ -111,8 +111,10 @@ def _stream_ptr(stream) -> int:
     return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
 
 
-def make_opts(variant=0, sched=0, stages=0, raster_group=0, max_ctas=0, timeout_ns=0, debug_flags=0) -> Opts:
+def make_opts(variant=0, sched=0, stages=0, raster_group=0, max_ctas=0, timeout_ns=0, debug_flags=0,
+              split_k=0) -> Opts:
     o = Opts()
+    o.split_k = int(split_k)
     o.variant, o.sched, o.stages, o.raster_group = int(variant), int(sched), int(stages), int(raster_group)
     o.max_ctas, o.timeout_ns, o.debug_flags = int(max_ctas), int(timeout_ns), int(debug_flags)
     return o

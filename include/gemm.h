@@ -93,10 +93,11 @@ typedef enum {
 typedef struct {
   int32_t variant;      /* gemm_variant_t, 0 = automatic choice */
   int32_t sched;        /* gemm_sched_t, 0 = automatic (static) */
-  int32_t stages;       /* SMEM ring depth, 0 = largest that fits */
+  int32_t stages;       /* SMEM ring depth, 0 = automatic (at most 12) */
   int32_t raster_group; /* tile rows per L2 raster group, 0 = automatic */
   int32_t max_ctas;     /* cap on persistent CTAs / clusters, 0 = no cap */
-  int32_t reserved0;
+  int32_t split_k;      /* GEMV_TC: CTAs (a cluster) sharing one 128-row block's K range,
+                           1, 2, 4 or 8; 0 = automatic */
   int64_t timeout_ns;   /* bound on every device-side wait, 0 = 2 s */
   int32_t debug_flags;  /* test hooks: 1 = leave out one TMA load (forces a timeout) */
   int32_t reserved[7];

@@ -70,7 +70,7 @@ def test_plan_rejects_bad_sizes_without_a_device(lib):
 def test_plan_rejects_bad_options(lib):
     assert _plan_status(lib, 64, 64, 64, 0, gemm.make_opts(variant=12)) == gemm.ERR_INVALID_ARG
     assert _plan_status(lib, 64, 64, 64, 0, gemm.make_opts(sched=9)) == gemm.ERR_INVALID_ARG
-    assert _plan_status(lib, 64, 64, 64, 0, gemm.make_opts(stages=9)) == gemm.ERR_INVALID_ARG
+    assert _plan_status(lib, 64, 64, 64, 0, gemm.make_opts(stages=13)) == gemm.ERR_INVALID_ARG
     # step 1 is one 128x128x64 tile; step 2 one 128x128 tile
     assert _plan_status(lib, 129, 64, 64, 0, gemm.make_opts(variant=gemm.S1)) == gemm.ERR_UNSUPPORTED_SHAPE
     assert _plan_status(lib, 64, 64, 72, 0, gemm.make_opts(variant=gemm.S1)) == gemm.ERR_UNSUPPORTED_SHAPE
