@@ -30,6 +30,7 @@ struct gemm_plan_s {
   size_t smem;
   uint64_t timeout_ns;
   uint32_t debug_flags;
+  int32_t flags;      // GEMM_FLAG_*
   uint32_t* scratch;  // [0] status word, [1] tile counter, [2] finished counter
   int32_t* visits;
   dgb::LaunchSpec spec;   // kernel, launch shape and SMEM, fixed at plan time
@@ -125,13 +126,15 @@ gemm_status_t current_device(int* dev, int* sms) {
 
 int ceil_div(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }
 
-// Automatic variant: the decode GEMV for a handful of rows; the plain-store
+// Automatic variant: the decode GEMV on CUDA cores for one or two rows, on the
+// Tensor Core for up to 16 rows; the plain-store
 // persistent kernel when C's rows are not 16-byte aligned for TMA stores;
 // otherwise the largest warp-specialised tile (step 9's 512x256 cluster tile,
 // then step 8's 256x256, then step 7's 128x256) that still gives every CTA pair
 // of the GPU at least one tile.
 int auto_variant(int64_t M, int64_t N, int64_t K, gemm_dtype_t dt, int sms) {
-  if (M <= 16 && gemv_smem_bytes((int)M, (int)K) <= 200 * 1024) return GEMM_VARIANT_GEMV;
+  if (M <= 2 && gemv_smem_bytes((int)M, (int)K) <= 200 * 1024) return GEMM_VARIANT_GEMV;
+  if (M <= 16) return GEMM_VARIANT_GEMV_TC;
   if (!c_rows_tma_ok(N, dt)) return GEMM_VARIANT_S6_PERSISTENT;
   const int64_t tn = (N + 255) / 256;
   const int64_t pairs = std::max(1, sms / 2);
@@ -148,10 +151,12 @@ gemm_status_t prepare_launch(gemm_plan_s* p) {
   const int v = p->variant;
   if (v == GEMM_VARIANT_GEMV) {
     e = spec_gemv((int)p->M, (int)p->N, (int)p->K, p->in_bf16, p->out_f32, p->num_sms, &p->spec);
+    p->spec.pdl = (p->flags & GEMM_FLAG_STATIC_B) != 0;
   } else if (v == GEMM_VARIANT_GEMV_TC) {
     e = spec_gemv_tc((int)p->M, (int)p->N, (int)p->K, p->in_bf16, p->out_f32, p->num_sms, p->split_k, p->stages,
                      &p->spec, &p->tgbase);
     p->tgbase.timeout_ns = p->timeout_ns;
+    p->spec.pdl = (p->flags & GEMM_FLAG_STATIC_B) != 0;
   } else {
     KParams& k = p->kbase;
     k.M = (int32_t)p->M;
@@ -190,7 +195,7 @@ gemm_status_t build_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, co
   if (opts) o = *opts;
   if (o.variant < 0 || o.variant > GEMM_VARIANT_GEMV_TC || o.sched < 0 || o.sched > GEMM_SCHED_CLC ||
       o.stages < 0 || o.stages > 12 || o.raster_group < 0 || o.max_ctas < 0 || o.timeout_ns < 0 ||
-      o.split_k < 0 || o.split_k > 8)
+      o.split_k < 0 || o.split_k > 8 || (o.flags & ~GEMM_FLAG_STATIC_B) != 0)
     return GEMM_ERR_INVALID_ARG;
 
   int dev = 0, sms = 0;
@@ -221,6 +226,7 @@ gemm_status_t build_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, co
   p->num_sms = sms;
   p->timeout_ns = o.timeout_ns ? (uint64_t)o.timeout_ns : kDefaultTimeoutNs;
   p->debug_flags = (uint32_t)o.debug_flags;
+  p->flags = o.flags;
   p->cg = 1;
   p->consumers = 1;
   p->sched = 0;

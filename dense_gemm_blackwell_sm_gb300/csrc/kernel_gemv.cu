@@ -6,10 +6,11 @@
 // product as the bandwidth-bound example: about one FLOP per byte, far below
 // the ridge point, so the Tensor Core is irrelevant and the kernel's only job
 // is to stream the weight B from HBM once at full bandwidth.  Design:
-//   * each warp owns one row of B at a time; every lane issues all of its
-//     16-byte non-allocating loads of the row (8 KB per warp at K = 4096)
-//     before using any of them, so each SM keeps well over 64 KB in flight;
-//   * X (at most 16 rows) is read through L1, where every warp finds it;
+//   * each warp owns R rows of B at a time; every lane issues its 16-byte
+//     non-allocating loads of those rows before using any of them, so each SM
+//     keeps well over 64 KB of B in flight;
+//   * X (at most 16 rows) is staged once per CTA in shared memory, after the
+//     first weight loads have been issued;
 //   * fp32 FMAs per lane, a shuffle reduction per output, one bf16/fp32 store;
 //   * the grid covers the rows exactly once (no atomics, no scratch memory).
 #include <algorithm>
@@ -22,8 +23,8 @@ namespace dgb {
 
 namespace {
 
-constexpr int GV_THREADS = 128;
-constexpr int GV_U = 16;  // 16-byte chunks per lane per row in flight: 8 KB per warp
+constexpr int GV_THREADS = 256;
+constexpr int GV_U = 8;  // 16-byte chunks per lane per row in flight
 
 __device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
   uint4 v;
@@ -31,6 +32,16 @@ __device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                : "l"(p));
   return v;
+}
+
+// programmatic dependent launch: let the next kernel in the stream start
+// launching, and wait for the previous one's results (both no-ops when the
+// launch did not ask for it)
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait_prior_grids() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 template <typename InT>
@@ -62,100 +73,129 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-// One warp per row of B: every lane issues all of its (up to GV_U) 16-byte
-// weight loads before it uses any, then reads the matching activation chunks
-// (shared by every warp, so they stay in L1) and accumulates in fp32.
-template <typename InT, typename OutT, int MT>
+// Each warp owns R rows of B at a time; every lane issues its GV_U 16-byte
+// loads of each row before using any of them.  The first rows' loads go out
+// before the activations are staged in shared memory (and, under programmatic
+// dependent launch, before the previous kernel in the stream has finished).
+template <typename InT, typename OutT, int MT, int R>
 __global__ void __launch_bounds__(GV_THREADS) k_gemv(GemvParams g) {
+  extern __shared__ uint4 xs[];  // MT rows x K/8 chunks
   const int K8 = g.K / 8;
+  const uint4 zero = make_uint4(0, 0, 0, 0);
   const uint4* X = reinterpret_cast<const uint4*>(g.X);
   const uint4* B = reinterpret_cast<const uint4*>(g.B);
   OutT* Y = reinterpret_cast<OutT*>(g.Y);
   const int lane = (int)lane_idx();
   const int warps = GV_THREADS / 32;
-  const uint4 zero = make_uint4(0, 0, 0, 0);
-  for (int n = (int)blockIdx.x * warps + (int)warp_idx(); n < g.N; n += (int)gridDim.x * warps) {
-    float acc[MT];
+  const int gw = (int)blockIdx.x * warps + (int)warp_idx();
+  const int nw = (int)gridDim.x * warps;
+
+  uint4 bv[R][GV_U];
+  auto load_rows = [&](int n0, int kc0) {
 #pragma unroll
-    for (int m = 0; m < MT; ++m) acc[m] = 0.f;
-    const uint4* brow = B + (int64_t)n * K8;
-    for (int kc0 = 0; kc0 < K8; kc0 += 32 * GV_U) {
-      uint4 bv[GV_U];
+    for (int r = 0; r < R; ++r)
 #pragma unroll
       for (int u = 0; u < GV_U; ++u) {
         const int c = kc0 + u * 32 + lane;
-        bv[u] = (c < K8) ? ld_stream_v4(brow + c) : zero;
+        bv[r][u] = (c < K8 && n0 + r < g.N) ? ld_stream_v4(B + (int64_t)(n0 + r) * K8 + c) : zero;
       }
+  };
+  pdl_launch_dependents();
+  if (gw * R < g.N) load_rows(gw * R, 0);
+  pdl_wait_prior_grids();
+  for (int i = threadIdx.x; i < MT * K8; i += GV_THREADS) {
+    const int m = i / K8, c = i - m * K8;
+    xs[i] = (m < g.M) ? X[(int64_t)m * K8 + c] : zero;
+  }
+  __syncthreads();
+
+  bool preloaded = true;
+  for (int n0 = gw * R; n0 < g.N; n0 += nw * R) {
+    float acc[MT][R];
+#pragma unroll
+    for (int m = 0; m < MT; ++m)
+#pragma unroll
+      for (int r = 0; r < R; ++r) acc[m][r] = 0.f;
+    for (int kc0 = 0; kc0 < K8; kc0 += 32 * GV_U) {
+      if (!preloaded) load_rows(n0, kc0);
+      preloaded = false;
 #pragma unroll
       for (int u = 0; u < GV_U; ++u) {
         const int c = kc0 + u * 32 + lane;
         if (c < K8) {
 #pragma unroll
           for (int m = 0; m < MT; ++m) {
-            if (m < g.M) acc[m] = dot8<InT>(__ldg(X + (int64_t)m * K8 + c), bv[u], acc[m]);
+            const uint4 xv = xs[m * K8 + c];
+#pragma unroll
+            for (int r = 0; r < R; ++r) acc[m][r] = dot8<InT>(xv, bv[r][u], acc[m][r]);
           }
         }
       }
     }
 #pragma unroll
-    for (int m = 0; m < MT; ++m) acc[m] = warp_sum(acc[m]);
+    for (int m = 0; m < MT; ++m)
+#pragma unroll
+      for (int r = 0; r < R; ++r) acc[m][r] = warp_sum(acc[m][r]);
     if (lane == 0) {
 #pragma unroll
-      for (int m = 0; m < MT; ++m) {
-        if (m < g.M) {
-          if constexpr (sizeof(OutT) == 4) {
-            Y[(int64_t)m * g.N + n] = acc[m];
-          } else {
-            Y[(int64_t)m * g.N + n] = __float2bfloat16_rn(acc[m]);
+      for (int m = 0; m < MT; ++m)
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+          if (m < g.M && n0 + r < g.N) {
+            if constexpr (sizeof(OutT) == 4) {
+              Y[(int64_t)m * g.N + n0 + r] = acc[m][r];
+            } else {
+              Y[(int64_t)m * g.N + n0 + r] = __float2bfloat16_rn(acc[m][r]);
+            }
           }
         }
-      }
     }
   }
 }
 
-template <typename InT, typename OutT, int MT>
-cudaError_t spec_t(int N, int num_sms, LaunchSpec* out) {
-  auto k = k_gemv<InT, OutT, MT>;
+template <typename InT, typename OutT, int MT, int R>
+cudaError_t spec_t(int N, int K, int num_sms, LaunchSpec* out) {
+  auto k = k_gemv<InT, OutT, MT, R>;
+  const size_t smem = (size_t)MT * (size_t)(K / 8) * 16;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
   int per_sm = 0;
-  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, GV_THREADS, 0);
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, GV_THREADS, smem);
   if (e != cudaSuccess) return e;
   if (per_sm < 1) return cudaErrorInvalidConfiguration;
-  const int rows_per_block = GV_THREADS / 32;
+  const int rows_per_block = (GV_THREADS / 32) * R;
   const int need = (N + rows_per_block - 1) / rows_per_block;
   out->func = (const void*)k;
-  out->grid = dim3((unsigned)std::max(1, std::min(need, per_sm * num_sms * 4)), 1, 1);
+  out->grid = dim3((unsigned)std::max(1, std::min(need, per_sm * num_sms)), 1, 1);
   out->block = dim3(GV_THREADS, 1, 1);
-  out->smem = 0;
+  out->smem = smem;
   out->cluster = 1;
   out->kind = ARGS_GEMV;
   return cudaSuccess;
 }
 
 template <typename InT, typename OutT>
-cudaError_t spec_m(int M, int N, int num_sms, LaunchSpec* out) {
-  if (M <= 1) return spec_t<InT, OutT, 1>(N, num_sms, out);
-  if (M <= 2) return spec_t<InT, OutT, 2>(N, num_sms, out);
-  if (M <= 4) return spec_t<InT, OutT, 4>(N, num_sms, out);
-  if (M <= 8) return spec_t<InT, OutT, 8>(N, num_sms, out);
-  return spec_t<InT, OutT, 16>(N, num_sms, out);
+cudaError_t spec_m(int M, int N, int K, int num_sms, LaunchSpec* out) {
+  if (M <= 1) return spec_t<InT, OutT, 1, 2>(N, K, num_sms, out);
+  if (M <= 2) return spec_t<InT, OutT, 2, 2>(N, K, num_sms, out);
+  if (M <= 4) return spec_t<InT, OutT, 4, 1>(N, K, num_sms, out);
+  if (M <= 8) return spec_t<InT, OutT, 8, 1>(N, K, num_sms, out);
+  return spec_t<InT, OutT, 16, 1>(N, K, num_sms, out);
 }
 
 }  // namespace
 
 size_t gemv_smem_bytes(int M, int K) {
-  (void)M;
-  (void)K;
-  return 0;  // the activations are read through L1, nothing is staged
+  const int mt = M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : M <= 8 ? 8 : 16;
+  return (size_t)mt * (size_t)(K / 8) * 16;
 }
 
 cudaError_t spec_gemv(int M, int N, int K, bool in_bf16, bool out_f32, int num_sms, LaunchSpec* out) {
-  (void)K;
   if (in_bf16) {
-    return out_f32 ? spec_m<__nv_bfloat16, float>(M, N, num_sms, out)
-                   : spec_m<__nv_bfloat16, __nv_bfloat16>(M, N, num_sms, out);
+    return out_f32 ? spec_m<__nv_bfloat16, float>(M, N, K, num_sms, out)
+                   : spec_m<__nv_bfloat16, __nv_bfloat16>(M, N, K, num_sms, out);
   }
-  return out_f32 ? spec_m<__half, float>(M, N, num_sms, out) : spec_m<__half, __nv_bfloat16>(M, N, num_sms, out);
+  return out_f32 ? spec_m<__half, float>(M, N, K, num_sms, out) : spec_m<__half, __nv_bfloat16>(M, N, K, num_sms, out);
 }
 
 }  // namespace dgb

@@ -76,8 +76,21 @@ __global__ void __launch_bounds__(TG_THREADS, 1)
   const WaitCtl w{abort_flag, p.status, p.timeout_ns, 0};
 
   if (warp == 0 && lane == 0) {
-    // producer: weight box + activation box per stage
-    for (int32_t j = 0; j < nkb; ++j) {
+    // producer: weight box + activation box per stage.  The first ring's weight
+    // boxes go out before waiting for the previous kernel in the stream (a
+    // no-op unless launched as its programmatic dependent), the activation
+    // boxes only after it.
+    const int32_t pre = min(nkb, S);
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    for (int32_t j = 0; j < pre; ++j) {
+      const uint32_t fb = smem_u32(full + j);
+      mbar_arrive_expect_tx(fb, TG_STAGE);
+      tma_load_2d(smem_u32(ring + (size_t)j * TG_STAGE), &tmB, fb, (kb0 + j) * TG_BK, n0);
+    }
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    for (int32_t j = 0; j < pre; ++j)
+      tma_load_2d(smem_u32(ring + (size_t)j * TG_STAGE + TG_B_BYTES), &tmX, smem_u32(full + j), (kb0 + j) * TG_BK, 0);
+    for (int32_t j = pre; j < nkb; ++j) {
       const int s = j % S;
       const uint32_t ph = (uint32_t)(j / S) & 1u;
       if (!mbar_wait(smem_u32(empty + s), ph ^ 1u, w, WAIT_PRODUCER_EMPTY)) break;
@@ -174,8 +187,9 @@ size_t tg_smem(int stages) {
 }  // namespace
 
 // CTAs per 128-row block along K (`split`, a cluster when > 1) and ring depth:
-// the largest power-of-two split (at most 8) that keeps every CTA resident at
-// once with one CTA per SM, unless `want_split` asks for one.
+// the largest power-of-two split (at most 4) whose CTAs all fit at once with
+// two CTAs per SM; an 8-stage ring when one CTA per SM suffices, else 4
+// stages so that two CTAs share an SM.  `want_split` / `want_stages` override.
 void gemv_tc_config(int N, int K, int num_sms, int want_split, int want_stages, int* split, int* stages,
                     int* kblocks_per_cta) {
   const int KB = (K + TG_BK - 1) / TG_BK;
@@ -184,12 +198,12 @@ void gemv_tc_config(int N, int K, int num_sms, int want_split, int want_stages, 
   if (want_split > 0) {
     while (sp * 2 <= want_split && sp < 8) sp *= 2;
   } else {
-    while (sp < 8 && rbs * sp * 2 <= num_sms) sp *= 2;
+    while (sp < 4 && rbs * sp * 2 <= 2 * num_sms) sp *= 2;
   }
   while (sp > 1 && sp > KB) sp /= 2;
   *split = sp;
   *kblocks_per_cta = (KB + sp - 1) / sp;
-  *stages = want_stages > 0 ? std::min(want_stages, TG_MAX_STAGES) : 8;
+  *stages = want_stages > 0 ? std::min(want_stages, TG_MAX_STAGES) : (rbs * sp <= num_sms ? 8 : 4);
 }
 
 size_t gemv_tc_smem_bytes(int stages) { return tg_smem(stages); }

@@ -29,6 +29,7 @@ struct LaunchSpec {
   size_t smem = 0;
   unsigned cluster = 1;  // CTAs per cluster along x
   int kind = ARGS_K;
+  bool pdl = false;      // launch as a programmatic dependent of the previous kernel
 };
 
 // one launch of a prepared kernel (cluster dimension attached when > 1)

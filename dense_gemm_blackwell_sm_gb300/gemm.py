@@ -32,6 +32,7 @@ VARIANT_NAMES = {0: "auto", 1: "s1_single_tile", 2: "s2_kloop", 3: "s3_multi_cta
 SCHED_AUTO, SCHED_STATIC, SCHED_ATOMIC, SCHED_CLC = 0, 1, 2, 3
 
 DEBUG_SKIP_ONE_LOAD = 1
+FLAG_STATIC_B = 1
 
 
 class GemmError(RuntimeError):
@@ -43,8 +44,8 @@ class GemmError(RuntimeError):
 class Opts(ctypes.Structure):
     _fields_ = [("variant", ctypes.c_int32), ("sched", ctypes.c_int32), ("stages", ctypes.c_int32),
                 ("raster_group", ctypes.c_int32), ("max_ctas", ctypes.c_int32), ("split_k", ctypes.c_int32),
-                ("timeout_ns", ctypes.c_int64), ("debug_flags", ctypes.c_int32),
-                ("reserved", ctypes.c_int32 * 7)]
+                ("timeout_ns", ctypes.c_int64), ("debug_flags", ctypes.c_int32), ("flags", ctypes.c_int32),
+                ("reserved", ctypes.c_int32 * 6)]
 
 
 class PlanInfo(ctypes.Structure):
@@ -112,8 +113,9 @@ def _stream_ptr(stream) -> int:
 
 
 def make_opts(variant=0, sched=0, stages=0, raster_group=0, max_ctas=0, timeout_ns=0, debug_flags=0,
-              split_k=0) -> Opts:
+              split_k=0, flags=0) -> Opts:
     o = Opts()
+    o.flags = int(flags)
     o.split_k = int(split_k)
     o.variant, o.sched, o.stages, o.raster_group = int(variant), int(sched), int(stages), int(raster_group)
     o.max_ctas, o.timeout_ns, o.debug_flags = int(max_ctas), int(timeout_ns), int(debug_flags)

@@ -100,8 +100,15 @@ typedef struct {
                            1, 2, 4 or 8; 0 = automatic */
   int64_t timeout_ns;   /* bound on every device-side wait, 0 = 2 s */
   int32_t debug_flags;  /* test hooks: 1 = leave out one TMA load (forces a timeout) */
-  int32_t reserved[7];
+  int32_t flags;        /* GEMM_FLAG_* */
+  int32_t reserved[6];
 } gemm_opts_t;
+
+/* B is not written by the work queued before the call on the same stream
+ * (weights of a decode step).  The GEMV variants then launch as programmatic
+ * dependents: they start streaming B while the previous kernel still runs and
+ * read A (the activations) only after it has completed. */
+#define GEMM_FLAG_STATIC_B 1
 
 typedef struct gemm_plan_s* gemm_plan_t;
 
