@@ -45,8 +45,8 @@ FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1
 KERNEL_SOURCES = {
     "ws": ["dense_gemm_blackwell_sm_gb300/csrc/kernels_ws.cu", "dense_gemm_blackwell_sm_gb300/csrc/ptx.cuh",
            "dense_gemm_blackwell_sm_gb300/csrc/kernel_common.cuh"],
-    "gemv": ["dense_gemm_blackwell_sm_gb300/csrc/kernel_gemv.cu",
-             "dense_gemm_blackwell_sm_gb300/csrc/kernel_common.cuh"],
+    "gemv": ["dense_gemm_blackwell_sm_gb300/csrc/kernel_gemv.cu", "dense_gemm_blackwell_sm_gb300/csrc/kernel_gemv_tc.cu",
+             "dense_gemm_blackwell_sm_gb300/csrc/kernel_common.cuh", "dense_gemm_blackwell_sm_gb300/csrc/ptx.cuh"],
 }
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.json")
 
