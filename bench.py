@@ -331,6 +331,8 @@ def main(argv=None):
     ap.add_argument("--shape", default=None,
                     help="M,N,K[,in,out]: a custom bf16 GEMM shape instead of a named workload (profiling)")
     ap.add_argument("--no-extra", action="store_true")
+    ap.add_argument("--ladder", action="store_true",
+                    help="time every kernel variant (the nine steps) on the workload and print one JSON line per step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     args = ap.parse_args(argv)
@@ -368,6 +370,16 @@ def main(argv=None):
     torch.cuda.set_device(dev)
     import __graft_entry__
     __graft_entry__.build()
+
+    if args.ladder:
+        from dense_gemm_blackwell_sm_gb300 import gemm as _g
+        for v in range(_g.S3, _g.S9 + 1):
+            r = bench_gemm(w, args.steps, args.warmup, dev, lambda: None, v)
+            print(json.dumps({"ladder_step": v, "variant": r["info"]["variant_name"], "workload": w.name,
+                              "tflops": round(w.flops / r["per_launch_s"] / 1e12, 1),
+                              "us_per_launch": round(r["per_launch_s"] * 1e6, 1), "grid": r["info"]["grid"],
+                              "stages": r["info"]["stages"], "clocks": r["clocks"]}), flush=True)
+        return 0
 
     res = bench_gemm(w, args.steps, args.warmup, dev, barrier, args.variant)
     times = gather(res["seconds"])

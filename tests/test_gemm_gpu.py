@@ -188,3 +188,50 @@ def test_run_host_end_to_end():
                             da.data_ptr(), db.data_ptr(), dc.data_ptr(), torch.cuda.current_stream().cuda_stream)
     assert st == gemm.OK
     assert parity.check(ch.float().numpy(), ref, S, "bf16")["ok"]
+
+
+@pytest.mark.parametrize("variant", [gemm.GEMV, gemm.GEMV_TC])
+def test_static_b_flag_chains_dependent_gemvs(variant):
+    """With GEMM_FLAG_STATIC_B the GEMV launches as a programmatic dependent of
+    the previous kernel and may stream B early, but must read its activations
+    only after that kernel is done: chain y1 = x B1^T, y2 = y1 B2^T."""
+    M, N1, K = (1 if variant == gemm.GEMV else 8), 1024, 512
+    x, b1 = inputs.make_operands(M, N1, K, "bf16", ("uniform",), ("normal", 0.05), seed=21)
+    _, b2 = inputs.make_operands(M, 768, N1, "bf16", ("uniform",), ("normal", 0.05), seed=22)
+    opts = gemm.make_opts(variant=variant, flags=gemm.FLAG_STATIC_B)
+    p1 = gemm.Plan(M, N1, K, gemm.BF16_BF16, opts)
+    p2 = gemm.Plan(M, 768, N1, gemm.BF16_BF16, opts)
+    dx, db1, db2 = x.to(DEV), b1.to(DEV), b2.to(DEV)
+    y1 = torch.empty((M, N1), device=DEV, dtype=torch.bfloat16)
+    y2 = torch.empty((M, 768), device=DEV, dtype=torch.bfloat16)
+    for _ in range(3):
+        y1.fill_(float("nan"))
+        y2.fill_(float("nan"))
+        p1.run(dx, db1, y1)
+        p2.run(y1, db2, y2)
+    torch.cuda.synchronize()
+    assert p1.check() == gemm.OK and p2.check() == gemm.OK
+    ref1, S1 = oracle.gemm(x, b1)
+    assert parity.check(y1.float().cpu().numpy(), ref1, S1, "bf16")["ok"]
+    y1h = y1.cpu()
+    ref2, S2 = oracle.gemm(y1h, b2)
+    assert parity.check(y2.float().cpu().numpy(), ref2, S2, "bf16")["ok"]
+    p1.destroy()
+    p2.destroy()
+
+
+@pytest.mark.parametrize("split", [1, 2, 4, 8])
+@pytest.mark.parametrize("stages", [2, 4, 8])
+def test_gemv_tc_split_and_ring_depth(split, stages):
+    M, N, K = 5, 392, 1032
+    a, b = inputs.make_operands(M, N, K, "f16", ("uniform",), ("normal", 1.0), seed=split * 10 + stages)
+    code = gemm.dtype_code("f16", "f32")
+    plan = gemm.Plan(M, N, K, code, gemm.make_opts(variant=gemm.GEMV_TC, split_k=split, stages=stages))
+    c = torch.full((M, N), float("nan"), device=DEV, dtype=torch.float32)
+    plan.run(a.to(DEV), b.to(DEV), c)
+    assert plan.check() == gemm.OK
+    assert plan.info()["cluster"] == split
+    ref, S = oracle.gemm(a, b)
+    r = parity.check(c.cpu().numpy(), ref, S, "f32")
+    assert r["ok"], r
+    plan.destroy()
