@@ -34,6 +34,8 @@ struct gemm_plan_s {
   uint32_t* scratch;  // [0] status word, [1] tile counter, [2] finished counter
   int32_t* visits;
   dgb::LaunchSpec spec;   // kernel, launch shape and SMEM, fixed at plan time
+  dgb::LaunchSpec spec_epi;  // the fused-epilogue kernel (variants 7-9), made on first use
+  bool epi_ready;
   dgb::KParams kbase;     // kernel parameters that do not depend on the pointers
   dgb::TgParams tgbase;   // same, for the tensor-core GEMV
   // TMA descriptors by operand role (0 = A, 1 = B, 2 = C) and pointer, least
@@ -342,7 +344,8 @@ const CUtensorMap* operand_map(gemm_plan_s* p, int role, const void* ptr) {
   return &victim->map;
 }
 
-gemm_status_t launch_plan(gemm_plan_s* p, const void* A, const void* B, void* C, cudaStream_t s) {
+gemm_status_t launch_plan(gemm_plan_s* p, const void* A, const void* B, void* C, cudaStream_t s,
+                          const gemm_epilogue_t* epi = nullptr) {
   if (!A || !B || !C) return GEMM_ERR_INVALID_ARG;
   if (!aligned16(A) || !aligned16(B) || !aligned16(C)) return GEMM_ERR_MISALIGNED;
   int cur = -1;
@@ -369,6 +372,13 @@ gemm_status_t launch_plan(gemm_plan_s* p, const void* A, const void* B, void* C,
     default: {
       KParams k = p->kbase;
       k.visits = p->visits;
+      const LaunchSpec* spec = &p->spec;
+      if (epi != nullptr) {
+        k.bias = epi->bias;
+        k.residual = epi->residual;
+        k.act = epi->activation;
+        spec = &p->spec_epi;
+      }
       k.A = static_cast<const uint16_t*>(A);
       k.B = static_cast<const uint16_t*>(B);
       k.C = C;
@@ -380,14 +390,14 @@ gemm_status_t launch_plan(gemm_plan_s* p, const void* A, const void* B, void* C,
       const CUtensorMap* ma = operand_map(p, 0, A);
       const CUtensorMap* mb = operand_map(p, 1, B);
       if (!ma || !mb) return GEMM_ERR_CUDA;
-      if (p->spec.kind == ARGS_AB_K) {
+      if (spec->kind == ARGS_AB_K) {
         void* args[] = {const_cast<CUtensorMap*>(ma), const_cast<CUtensorMap*>(mb), &k};
-        e = launch_spec(p->spec, args, s);
+        e = launch_spec(*spec, args, s);
       } else {
         const CUtensorMap* mc = operand_map(p, 2, C);
         if (!mc) return GEMM_ERR_CUDA;
         void* args[] = {const_cast<CUtensorMap*>(ma), const_cast<CUtensorMap*>(mb), const_cast<CUtensorMap*>(mc), &k};
-        e = launch_spec(p->spec, args, s);
+        e = launch_spec(*spec, args, s);
       }
     }
   }
@@ -434,6 +444,24 @@ gemm_status_t gemm_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, con
 gemm_status_t gemm_plan_run(gemm_plan_t plan, const void* A, const void* B, void* C, gemm_stream_t stream) {
   if (!plan) return GEMM_ERR_INVALID_ARG;
   return launch_plan(plan, A, B, C, reinterpret_cast<cudaStream_t>(stream));
+}
+
+gemm_status_t gemm_plan_run_epilogue(gemm_plan_t plan, const void* A, const void* B, void* C,
+                                     const gemm_epilogue_t* epi, gemm_stream_t stream) {
+  if (!plan || !epi) return GEMM_ERR_INVALID_ARG;
+  if (!is_ws(plan->variant)) return GEMM_ERR_UNSUPPORTED_SHAPE;
+  if (epi->activation < GEMM_ACT_NONE || epi->activation > GEMM_ACT_GELU_ERF) return GEMM_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(epi->bias) & 3u) || (reinterpret_cast<uintptr_t>(epi->residual) & 15u))
+    return GEMM_ERR_MISALIGNED;
+  if (!plan->epi_ready) {
+    if (spec_ws(plan->cg, plan->consumers, plan->sched - 1, plan->out_f32, plan->stages, plan->grid_units,
+                &plan->spec_epi, /*fused=*/true) != cudaSuccess) {
+      cudaGetLastError();
+      return GEMM_ERR_CUDA;
+    }
+    plan->epi_ready = true;
+  }
+  return launch_plan(plan, A, B, C, reinterpret_cast<cudaStream_t>(stream), epi);
 }
 
 gemm_status_t gemm_run(int64_t M, int64_t N, int64_t K, const void* A, const void* B, void* C,

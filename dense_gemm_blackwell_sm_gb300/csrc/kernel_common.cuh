@@ -47,7 +47,87 @@ struct KParams {
   const uint16_t* A;     // raw operands for the kernels that copy with threads
   const uint16_t* B;
   void* C;
+  // fused writeback epilogue (steps 7-9): C = act(acc + bias[col]) + residual[row][col]
+  const float* bias;     // N fp32 values, or null
+  const void* residual;  // M x N in C's type, row-major (ld = out_ld), or null
+  int32_t act;           // EPI_ACT_*
 };
+
+// activations of the fused epilogue
+enum : int32_t {
+  EPI_ACT_NONE = 0,
+  EPI_ACT_RELU = 1,
+  EPI_ACT_SILU = 2,       // x * sigmoid(x)
+  EPI_ACT_GELU_TANH = 3,  // 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3)))
+  EPI_ACT_GELU_ERF = 4,   // 0.5 x (1 + erf(x / sqrt(2)))
+};
+
+__device__ __forceinline__ float epi_activation(float x, int32_t act) {
+  switch (act) {
+    case EPI_ACT_RELU: return fmaxf(x, 0.f);
+    case EPI_ACT_SILU: return x / (1.f + expf(-x));
+    case EPI_ACT_GELU_TANH: {
+      const float k0 = 0.7978845608028654f;  // sqrt(2 / pi)
+      return 0.5f * x * (1.f + tanhf(k0 * (x + 0.044715f * x * x * x)));
+    }
+    case EPI_ACT_GELU_ERF: return 0.5f * x * (1.f + erff(x * 0.7071067811865476f));
+    default: return x;
+  }
+}
+
+// Applies the fused epilogue to n consecutive fp32 accumulator values of one row
+// (columns col0 .. col0+n-1), in place.  bias is read through L1 (every lane of
+// a warp reads the same columns); the residual row segment with 16-byte loads
+// when it lies wholly inside C, element by element at the edges.
+template <typename OutT, int n>
+__device__ __forceinline__ void apply_epilogue(uint32_t* v, const KParams& p, int32_t row, int32_t col0) {
+  float x[n];
+#pragma unroll
+  for (int j = 0; j < n; ++j) x[j] = __uint_as_float(v[j]);
+  if (p.bias != nullptr) {
+#pragma unroll
+    for (int j = 0; j < n; ++j) x[j] += (col0 + j < p.N) ? __ldg(p.bias + col0 + j) : 0.f;
+  }
+  if (p.act != EPI_ACT_NONE) {
+#pragma unroll
+    for (int j = 0; j < n; ++j) x[j] = epi_activation(x[j], p.act);
+  }
+  if (p.residual != nullptr && row < p.M) {
+    const OutT* r = reinterpret_cast<const OutT*>(p.residual) + (int64_t)row * p.out_ld + col0;
+    constexpr int per16 = 16 / (int)sizeof(OutT);
+    if (col0 + n <= p.N) {
+#pragma unroll
+      for (int q = 0; q < n / per16; ++q) {
+        const uint4 u = __ldg(reinterpret_cast<const uint4*>(r) + q);
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+        if constexpr (sizeof(OutT) == 4) {
+#pragma unroll
+          for (int t = 0; t < 4; ++t) x[q * 4 + t] += __uint_as_float(w[t]);
+        } else {
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[t]));
+            x[q * 8 + 2 * t] += f.x;
+            x[q * 8 + 2 * t + 1] += f.y;
+          }
+        }
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < n; ++j) {
+        if (col0 + j < p.N) {
+          if constexpr (sizeof(OutT) == 4) {
+            x[j] += r[j];
+          } else {
+            x[j] += __bfloat162float(r[j]);
+          }
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < n; ++j) v[j] = __float_as_uint(x[j]);
+}
 
 // Grouped (L2-aware) raster order: consecutive tile ids walk down a group of
 // `group` tile rows before moving one tile column to the right, so the CTAs

@@ -64,7 +64,7 @@ struct WsCfg {
   static constexpr uint32_t RING_CONSUMERS = (uint32_t)(CG * 5 + NCONS);
 };
 
-template <typename OutT, int CG, int NCONS, int SCHED>
+template <typename OutT, int CG, int NCONS, int SCHED, bool FUSED = false>
 __global__ void __launch_bounds__(WS_THREADS, 1)
     k_ws(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
          const __grid_constant__ CUtensorMap tmC, KParams p) {
@@ -330,6 +330,13 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
               }
             }
           }
+          if constexpr (FUSED) {
+            // bias, activation and residual, in fp32, before the single rounding to C's type
+            const int32_t row = row0 + (int32_t)lane;
+            const int32_t col0 = col_base + ch * CW;
+            apply_epilogue<OutT, 32>(v0, p, row, col0);
+            if constexpr (CW == 64) apply_epilogue<OutT, 32>(v1, p, row, col0 + 32);
+          }
           uint8_t* buf = my_staging + (tog & 1u) * 4096u;
           if (lane == 0) bulk_wait_group_read<1>();  // the store issued from `buf` two chunks ago is done reading
           __syncwarp();
@@ -372,13 +379,18 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
   }
 }
 
-template <typename OutT, int CG, int NCONS, int SCHED>
+template <typename OutT, int CG, int NCONS, int SCHED, bool FUSED = false>
 void* ws_kernel_ptr() {
-  return reinterpret_cast<void*>(k_ws<OutT, CG, NCONS, SCHED>);
+  return reinterpret_cast<void*>(k_ws<OutT, CG, NCONS, SCHED, FUSED>);
 }
 
+// the fused-epilogue kernels exist for the static scheduler only
 template <int CG, int NCONS>
-void* pick_kernel(int sched, bool out_f32) {
+void* pick_kernel(int sched, bool out_f32, bool fused) {
+  if (fused) {
+    return out_f32 ? ws_kernel_ptr<float, CG, NCONS, SCHED_STATIC, true>()
+                   : ws_kernel_ptr<__nv_bfloat16, CG, NCONS, SCHED_STATIC, true>();
+  }
   if (out_f32) {
     if (sched == SCHED_ATOMIC) return ws_kernel_ptr<float, CG, NCONS, SCHED_ATOMIC>();
     if (sched == SCHED_CLC) return ws_kernel_ptr<float, CG, NCONS, SCHED_CLC>();
@@ -389,11 +401,11 @@ void* pick_kernel(int sched, bool out_f32) {
   return ws_kernel_ptr<__nv_bfloat16, CG, NCONS, SCHED_STATIC>();
 }
 
-void* ws_kernel(int cg, int consumers, int sched, bool out_f32) {
-  if (cg == 1 && consumers == 1) return pick_kernel<1, 1>(sched, out_f32);
-  if (cg == 1 && consumers == 2) return pick_kernel<1, 2>(sched, out_f32);
-  if (cg == 2 && consumers == 1) return pick_kernel<2, 1>(sched, out_f32);
-  if (cg == 2 && consumers == 2) return pick_kernel<2, 2>(sched, out_f32);
+void* ws_kernel(int cg, int consumers, int sched, bool out_f32, bool fused = false) {
+  if (cg == 1 && consumers == 1) return pick_kernel<1, 1>(sched, out_f32, fused);
+  if (cg == 1 && consumers == 2) return pick_kernel<1, 2>(sched, out_f32, fused);
+  if (cg == 2 && consumers == 1) return pick_kernel<2, 1>(sched, out_f32, fused);
+  if (cg == 2 && consumers == 2) return pick_kernel<2, 2>(sched, out_f32, fused);
   return nullptr;
 }
 
@@ -453,8 +465,9 @@ int ws_max_active_clusters(int cg, int consumers, int sched, bool out_f32, int s
   return n;
 }
 
-cudaError_t spec_ws(int cg, int consumers, int sched, bool out_f32, int stages, int clusters, LaunchSpec* out) {
-  void* k = ws_kernel(cg, consumers, sched, out_f32);
+cudaError_t spec_ws(int cg, int consumers, int sched, bool out_f32, int stages, int clusters, LaunchSpec* out,
+                    bool fused) {
+  void* k = ws_kernel(cg, consumers, fused ? SCHED_STATIC : sched, out_f32, fused);
   if (!k) return cudaErrorInvalidValue;
   const size_t smem = ws_smem_bytes(cg, consumers, stages);
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

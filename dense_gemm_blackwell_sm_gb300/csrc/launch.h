@@ -59,7 +59,9 @@ WsShape ws_shape(int cg, int consumers);
 size_t ws_smem_bytes(int cg, int consumers, int stages);
 int ws_max_stages(int cg, int consumers);
 int ws_max_active_clusters(int cg, int consumers, int sched, bool out_f32, int stages);
-cudaError_t spec_ws(int cg, int consumers, int sched, bool out_f32, int stages, int clusters, LaunchSpec* out);
+// fused = the writeback applies bias / activation / residual (static scheduler)
+cudaError_t spec_ws(int cg, int consumers, int sched, bool out_f32, int stages, int clusters, LaunchSpec* out,
+                    bool fused = false);
 
 // decode GEMV, C (M x N) = X (M x K) * B^T for M <= 16, on CUDA cores
 struct GemvParams {

@@ -31,6 +31,9 @@ VARIANT_NAMES = {0: "auto", 1: "s1_single_tile", 2: "s2_kloop", 3: "s3_multi_cta
 # gemm_sched_t
 SCHED_AUTO, SCHED_STATIC, SCHED_ATOMIC, SCHED_CLC = 0, 1, 2, 3
 
+# gemm_activation_t
+ACT_NONE, ACT_RELU, ACT_SILU, ACT_GELU_TANH, ACT_GELU_ERF = 0, 1, 2, 3, 4
+
 DEBUG_SKIP_ONE_LOAD = 1
 FLAG_STATIC_B = 1
 
@@ -58,6 +61,11 @@ class PlanInfo(ctypes.Structure):
         return d
 
 
+class Epilogue(ctypes.Structure):
+    _fields_ = [("bias", ctypes.c_void_p), ("residual", ctypes.c_void_p), ("activation", ctypes.c_int32),
+                ("reserved", ctypes.c_int32 * 3)]
+
+
 _lib = None
 
 
@@ -74,6 +82,8 @@ def load():
     lib.gemm_plan.restype = i32
     lib.gemm_plan_run.argtypes = [p, p, p, p, p]
     lib.gemm_plan_run.restype = i32
+    lib.gemm_plan_run_epilogue.argtypes = [p, p, p, p, ctypes.POINTER(Epilogue), p]
+    lib.gemm_plan_run_epilogue.restype = i32
     lib.gemm_run.argtypes = [i64, i64, i64, p, p, p, i32, p]
     lib.gemm_run.restype = i32
     lib.gemm_run_host.argtypes = [i64, i64, i64, p, p, p, i32, p, p, p, p]
@@ -139,6 +149,18 @@ class Plan:
 
     def run(self, a, b, c, stream=None):
         _check(self.run_ptr(a.data_ptr(), b.data_ptr(), c.data_ptr(), _stream_ptr(stream)), "gemm_plan_run")
+        return c
+
+    def run_epilogue(self, a, b, c, bias=None, residual=None, act: int = ACT_NONE, stream=None):
+        """C = act(a @ b.T + bias) + residual in one kernel (variants 7-9).
+        bias: fp32 CUDA tensor of N values; residual: (M, N) CUDA tensor of C's type."""
+        e = Epilogue()
+        e.bias = None if bias is None else bias.data_ptr()
+        e.residual = None if residual is None else residual.data_ptr()
+        e.activation = int(act)
+        st = load().gemm_plan_run_epilogue(self._h, a.data_ptr(), b.data_ptr(), c.data_ptr(), ctypes.byref(e),
+                                           _stream_ptr(stream))
+        _check(st, "gemm_plan_run_epilogue")
         return c
 
     def check(self, stream=None) -> int:

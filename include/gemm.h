@@ -138,6 +138,34 @@ GEMM_API gemm_status_t gemm_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t d
 GEMM_API gemm_status_t gemm_plan_run(gemm_plan_t plan, const void* A, const void* B, void* C,
                             gemm_stream_t stream);
 
+/* Activations of the fused epilogue.  The reading notes list the nonlinear
+ * nodes that follow a linear layer in an LLM's DAG (softmax, layer norm, GeLU /
+ * SiLU); the formulas are the standard definitions. */
+typedef enum {
+  GEMM_ACT_NONE = 0,
+  GEMM_ACT_RELU = 1,      /* max(x, 0) */
+  GEMM_ACT_SILU = 2,      /* x / (1 + exp(-x)) */
+  GEMM_ACT_GELU_TANH = 3, /* 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))) */
+  GEMM_ACT_GELU_ERF = 4   /* 0.5 x (1 + erf(x / sqrt(2))) */
+} gemm_activation_t;
+
+/* Fused epilogue of the writeback: C[i][j] = act(sum_k A[i][k] B[j][k] + bias[j])
+ * + residual[i][j], computed in fp32 and rounded once to C's type. */
+typedef struct {
+  const float* bias;    /* N fp32 values (device, 4-byte aligned), or NULL */
+  const void* residual; /* M x N device array of C's type, row-major, 16-byte aligned, or
+                           NULL; may be C itself (each element is read before it is
+                           overwritten) */
+  int32_t activation;   /* gemm_activation_t */
+  int32_t reserved[3];
+} gemm_epilogue_t;
+
+/* gemm_plan_run with the fused epilogue.  Needs a plan of variant 7, 8 or 9
+ * (the automatic plan of most shapes with M > 16); other plans return
+ * GEMM_ERR_UNSUPPORTED_SHAPE.  The epilogue kernel uses the static scheduler. */
+GEMM_API gemm_status_t gemm_plan_run_epilogue(gemm_plan_t plan, const void* A, const void* B, void* C,
+                                              const gemm_epilogue_t* epilogue, gemm_stream_t stream);
+
 /* One-shot form: plan (cached per shape, dtype and device) and run. */
 GEMM_API gemm_status_t gemm_run(int64_t M, int64_t N, int64_t K, const void* A, const void* B, void* C,
                        gemm_dtype_t dtype, gemm_stream_t stream);

@@ -14,7 +14,9 @@ section "9 步优化", steps 1-3) computes tile by tile; see the C file's header
 Pins (tests/test_oracle_pins.py): exact-rational brute force on tiny shapes,
 identity / permutation operands, the rank-1 closed form, transpose symmetry,
 additivity, thread-count invariance and an exhaustive check of both 16-bit
-decoders against numpy's IEEE binary16 / binary32 conversions.
+decoders against numpy's IEEE binary16 / binary32 conversions.  The fused
+epilogue (``epilogue``: bias, activation, residual) is pinned in
+tests/test_oracle_epilogue_pins.py.
 """
 from __future__ import annotations
 
@@ -60,6 +62,10 @@ def _load():
         lib.oracle_gemm_f64.restype = ctypes.c_int
         lib.oracle_widen.argtypes = [ctypes.c_uint16, ctypes.c_int]
         lib.oracle_widen.restype = ctypes.c_double
+        lib.oracle_epilogue_f64.argtypes = [i64, i64, p, p, p, ctypes.c_int, ctypes.c_int]
+        lib.oracle_epilogue_f64.restype = ctypes.c_int
+        lib.oracle_activation.argtypes = [ctypes.c_double, ctypes.c_int]
+        lib.oracle_activation.restype = ctypes.c_double
         lib.oracle_max_threads.argtypes = []
         lib.oracle_max_threads.restype = ctypes.c_int
         _lib = lib
@@ -131,3 +137,45 @@ def gemm_rows(a, b, rows, kind: int | None = None, nthreads: int = 0):
     if rc != 0:
         raise ValueError("oracle_gemm_rows_f64 rejected its arguments")
     return C, S
+
+
+ACT_NONE, ACT_RELU, ACT_SILU, ACT_GELU_TANH, ACT_GELU_ERF = 0, 1, 2, 3, 4
+
+
+def activation(x: float, act: int) -> float:
+    """The oracle's activation of one value (fp64)."""
+    return float(_load().oracle_activation(float(x), int(act)))
+
+
+def epilogue(C, bias=None, residual=None, act: int = ACT_NONE):
+    """act(C + bias[col]) + residual, in fp64, on a copy of C (M x N).
+
+    bias: N fp32 values (array or tensor) or None; residual: M x N fp32 /
+    bf16 / fp16 (numpy float32 array, or torch tensor) or None."""
+    out = np.ascontiguousarray(np.array(C, dtype=np.float64))
+    M, N = out.shape
+    b = None
+    if bias is not None:
+        if hasattr(bias, "detach"):
+            bias = bias.detach().cpu().numpy()
+        b = np.ascontiguousarray(np.asarray(bias, dtype=np.float32))
+        if b.shape != (N,):
+            raise ValueError("bias must hold N values")
+    r, kind = None, 0
+    if residual is not None:
+        if hasattr(residual, "detach"):
+            import torch
+            t = residual.detach().cpu().contiguous()
+            if t.dtype == torch.float32:
+                r, kind = t.numpy(), 1
+            else:
+                r, kind = _bits(t), (2 if t.dtype == torch.bfloat16 else 3)
+        else:
+            r, kind = np.ascontiguousarray(np.asarray(residual, dtype=np.float32)), 1
+        if r.shape != (M, N):
+            raise ValueError("residual must be M x N")
+    rc = _load().oracle_epilogue_f64(M, N, out.ctypes.data, None if b is None else b.ctypes.data,
+                                     None if r is None else r.ctypes.data, kind, int(act))
+    if rc != 0:
+        raise ValueError("oracle_epilogue_f64 rejected its arguments")
+    return out

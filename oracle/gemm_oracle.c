@@ -28,12 +28,17 @@
  * such values is exact in double (11+11 resp. 8+8 significand bits < 53), so
  * the only rounding is in the k-sum, bounded by (K-1) * 2^-53 * S.
  */
+#define _USE_MATH_DEFINES
 #include <math.h>
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
 #ifdef _OPENMP
 #include <omp.h>
+#endif
+
+#ifndef M_PI
+#define M_PI 3.14159265358979323846
 #endif
 
 #define ORACLE_IN_F16 0
@@ -147,4 +152,55 @@ int oracle_gemm_f64(int64_t M, int64_t N, int64_t K,
                     const uint16_t* A, const uint16_t* B, int in_kind,
                     double* C, double* S, int nthreads) {
     return oracle_gemm_rows_f64(M, N, K, A, B, in_kind, NULL, M, C, S, nthreads);
+}
+
+/*
+ * Fused epilogue of a linear layer, applied in place to an fp64 result C
+ * (M x N, row-major):
+ *
+ *     C[i][j] = act(C[i][j] + bias[j]) + residual[i][j]
+ *
+ * The reading notes (section "LLM 推理本质上是一张有向无环图") describe an LLM's
+ * forward pass as a DAG whose linear nodes (the GEMMs) feed nonlinear ones such
+ * as GeLU and SiLU; the activation formulas below are their standard
+ * definitions, evaluated in fp64 with the C library's exp, tanh and erf.
+ *
+ * bias: N fp32 values or NULL.  residual: M x N values or NULL, of kind
+ * 1 = fp32, 2 = bfloat16 bit patterns, 3 = binary16 bit patterns.
+ * act: 0 none, 1 relu, 2 silu, 3 gelu (tanh form), 4 gelu (erf form).
+ */
+static double oracle_act(double x, int act) {
+    switch (act) {
+        case 1: return x > 0.0 ? x : 0.0;
+        case 2: return x / (1.0 + exp(-x));
+        case 3: return 0.5 * x * (1.0 + tanh(sqrt(2.0 / M_PI) * (x + 0.044715 * x * x * x)));
+        case 4: return 0.5 * x * (1.0 + erf(x / sqrt(2.0)));
+        default: return x;
+    }
+}
+
+double oracle_activation(double x, int act) { return oracle_act(x, act); }
+
+int oracle_epilogue_f64(int64_t M, int64_t N, double* C, const float* bias, const void* residual,
+                        int residual_kind, int act) {
+    if (M < 0 || N < 0 || act < 0 || act > 4) return -1;
+    if (residual != NULL && (residual_kind < 1 || residual_kind > 3)) return -1;
+    for (int64_t i = 0; i < M; ++i) {
+        for (int64_t j = 0; j < N; ++j) {
+            double x = C[i * N + j];
+            if (bias) x += (double)bias[j];
+            x = oracle_act(x, act);
+            if (residual) {
+                const int64_t e = i * N + j;
+                if (residual_kind == 1) {
+                    x += (double)((const float*)residual)[e];
+                } else {
+                    const uint16_t bits = ((const uint16_t*)residual)[e];
+                    x += oracle_widen(bits, residual_kind == 2 ? ORACLE_IN_BF16 : ORACLE_IN_F16);
+                }
+            }
+            C[i * N + j] = x;
+        }
+    }
+    return 0;
 }

@@ -80,3 +80,42 @@ def check(c, ref: np.ndarray, S: np.ndarray, out_dtype: str) -> dict:
         out["first_bad"] = {"index": [int(i) for i in idx], "c": float(c[tuple(idx)]),
                             "ref": float(ref[tuple(idx)]), "S": float(S[tuple(idx)])}
     return out
+
+
+# Largest slope of each activation (0 none, 1 relu, 2 silu, 3 gelu-tanh,
+# 4 gelu-erf): silu' peaks at 1.0998 (x ~ 2.40), both gelu forms at 1.1289
+# (x ~ 1.41 for erf, ~1.44 for tanh); pinned numerically by the oracle tests.
+ACT_SLOPE = {0: 1.0, 1: 1.0, 2: 1.1, 3: 1.13, 4: 1.13}
+EPI_REL = 2.0 ** -17
+
+
+def epilogue_bound(ref_epi, pre, S, residual_abs, out_dtype: str, act: int) -> np.ndarray:
+    """Per-element bound for C = act(acc + bias) + residual.
+
+    An accumulator error e (|e| <= 2^-10 S, the GEMM rule) moves act(.) by at
+    most slope * e; the fp32 additions of bias and residual and the fp32
+    activation (a few ulp of CUDA's expf / tanhf / erff) add at most
+    2^-17 (|acc + bias| + |residual|), since |act(x)| <= |x| for every
+    activation here; bf16 output adds half an ulp of the final value."""
+    b = ACT_SLOPE[act] * TOL_REL * np.asarray(S, dtype=np.float64)
+    b = b + EPI_REL * (np.abs(np.asarray(pre, dtype=np.float64)) + np.asarray(residual_abs, dtype=np.float64))
+    if out_dtype == "bf16":
+        b = b + half_ulp_bf16(ref_epi)
+    return b
+
+
+def check_epilogue(c, ref_epi, pre, S, residual_abs, out_dtype: str, act: int) -> dict:
+    c = np.asarray(c, dtype=np.float64)
+    ref_epi = np.asarray(ref_epi, dtype=np.float64)
+    finite = np.isfinite(c)
+    err = np.abs(c - ref_epi)
+    b = epilogue_bound(np.maximum(np.abs(ref_epi), np.abs(np.where(finite, c, 0.0))), pre, S, residual_abs,
+                       out_dtype, act)
+    bad = ~finite | (err > b)
+    out = {"ok": bool(not bad.any()), "violations": int(bad.sum()),
+           "worst_ratio": float(np.max(np.where(b > 0, err / np.where(b > 0, b, 1.0), np.where(err > 0, np.inf, 0.0))))}
+    if bad.any():
+        idx = np.argwhere(bad)[0]
+        out["first_bad"] = {"index": [int(i) for i in idx], "c": float(c[tuple(idx)]),
+                            "ref": float(ref_epi[tuple(idx)]), "bound": float(b[tuple(idx)])}
+    return out

@@ -1,0 +1,105 @@
+"""GPU parity of the fused writeback epilogue, C = act(A B^T + bias) + residual,
+of the step 7-9 kernels against the CPU oracle's fp64 epilogue."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import parity
+from dense_gemm_blackwell_sm_gb300 import gemm, inputs
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+ACTS = [gemm.ACT_NONE, gemm.ACT_RELU, gemm.ACT_SILU, gemm.ACT_GELU_TANH, gemm.ACT_GELU_ERF]
+SHAPES = {gemm.S7: (300, 520, 200), gemm.S8: (700, 776, 264), gemm.S9: (1100, 520, 136)}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+    __graft_entry__.build()
+    torch.cuda.set_device(0)
+
+
+def _run(variant, a, b, out, bias, residual, act, alias=False):
+    M, K = a.shape
+    N = b.shape[0]
+    plan = gemm.Plan(M, N, K, gemm.dtype_code(a.dtype, out), gemm.make_opts(variant=variant))
+    t = inputs.torch_dtype(out)
+    if alias:
+        c = residual.to(DEV).clone()
+        res = c
+    else:
+        c = torch.full((M, N), float("nan"), device=DEV, dtype=t)
+        res = None if residual is None else residual.to(DEV)
+    plan.run_epilogue(a.to(DEV), b.to(DEV), c, bias=None if bias is None else bias.to(DEV), residual=res, act=act)
+    assert plan.check() == gemm.OK
+    plan.destroy()
+    return c.double().cpu().numpy()
+
+
+@pytest.mark.parametrize("variant", [gemm.S7, gemm.S8, gemm.S9])
+@pytest.mark.parametrize("out", ["bf16", "f32"])
+def test_integer_relu_bias_residual_bit_exact(variant, out):
+    M, N, K = SHAPES[variant]
+    a, b = inputs.integer_operands(M, N, K, "bf16", seed=variant)
+    g = torch.Generator().manual_seed(variant)
+    bias = torch.randint(-20, 21, (N,), generator=g).float()
+    res = torch.randint(-8, 9, (M, N), generator=g).to(inputs.torch_dtype(out))
+    C, _ = oracle.gemm(a, b)
+    ref = oracle.epilogue(C, bias, res, oracle.ACT_RELU)
+    exp = torch.tensor(ref).to(inputs.torch_dtype(out)).double().numpy()
+    got = _run(variant, a, b, out, bias, res, gemm.ACT_RELU)
+    bad = np.argwhere(got != exp)
+    assert bad.size == 0, (bad[:3], got[tuple(bad[0])], exp[tuple(bad[0])])
+
+
+@pytest.mark.parametrize("variant", [gemm.S7, gemm.S8, gemm.S9])
+@pytest.mark.parametrize("act", ACTS)
+@pytest.mark.parametrize("use_bias,use_res", [(True, True), (True, False), (False, True)])
+def test_random_epilogue_parity(variant, act, use_bias, use_res):
+    M, N, K = SHAPES[variant]
+    out = "bf16" if (act + variant) % 2 else "f32"
+    a, b = inputs.make_operands(M, N, K, "bf16", ("uniform",), ("normal", 0.2), seed=act * 7 + variant)
+    g = torch.Generator().manual_seed(act + 100 * variant)
+    bias = (torch.randn(N, generator=g) * 2).float() if use_bias else None
+    res = (torch.randn(M, N, generator=g) * 3).to(inputs.torch_dtype(out)) if use_res else None
+    C, S = oracle.gemm(a, b)
+    ref = oracle.epilogue(C, bias, res, act)
+    pre = C + (bias.double().numpy()[None, :] if use_bias else 0.0)
+    res_abs = np.abs(res.double().numpy()) if use_res else np.zeros_like(C)
+    got = _run(variant, a, b, out, bias, res, act)
+    r = parity.check_epilogue(got, ref, pre, S, res_abs, out, act)
+    assert r["ok"], r
+
+
+@pytest.mark.parametrize("variant", [gemm.S8, gemm.S9])
+def test_residual_may_be_the_output(variant):
+    M, N, K = SHAPES[variant]
+    a, b = inputs.make_operands(M, N, K, "bf16", ("uniform",), ("uniform",), seed=31)
+    res = (torch.randn(M, N, generator=torch.Generator().manual_seed(31))).to(torch.bfloat16)
+    C, S = oracle.gemm(a, b)
+    ref = oracle.epilogue(C, None, res, gemm.ACT_SILU)
+    got = _run(variant, a, b, "bf16", None, res, gemm.ACT_SILU, alias=True)
+    assert parity.check_epilogue(got, ref, C, S, np.abs(res.double().numpy()), "bf16", gemm.ACT_SILU)["ok"]
+
+
+def test_epilogue_argument_checks():
+    a = torch.zeros(64, 64, dtype=torch.bfloat16, device=DEV)
+    c = torch.zeros(64, 64, dtype=torch.bfloat16, device=DEV)
+    gv = gemm.Plan(8, 64, 64, gemm.BF16_BF16, gemm.make_opts(variant=gemm.GEMV))
+    with pytest.raises(gemm.GemmError) as e:
+        gv.run_epilogue(a[:8], a, c[:8], act=gemm.ACT_RELU)
+    assert e.value.status == gemm.ERR_UNSUPPORTED_SHAPE
+    ws = gemm.Plan(64, 64, 64, gemm.BF16_BF16, gemm.make_opts(variant=gemm.S8))
+    with pytest.raises(gemm.GemmError) as e:
+        ws.run_epilogue(a, a, c, act=9)
+    assert e.value.status == gemm.ERR_INVALID_ARG
+    flat = torch.zeros(64 * 64 + 8, dtype=torch.bfloat16, device=DEV)
+    with pytest.raises(gemm.GemmError) as e:
+        ws.run_epilogue(a, a, c, residual=flat[1:], act=gemm.ACT_NONE)
+    assert e.value.status == gemm.ERR_MISALIGNED
+    gv.destroy()
+    ws.destroy()
