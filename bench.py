@@ -168,7 +168,10 @@ def _events_time(fn, steps: int, stream) -> float:
     return start.elapsed_time(end) / 1e3
 
 
-def bench_gemm(w: inputs.Workload, steps: int, warmup: int, dev, dist_barrier, variant: int = 0) -> dict:
+def bench_gemm(w: inputs.Workload, steps: int, warmup: int, dev, dist_barrier, variant: int = 0,
+               epilogue_act=None) -> dict:
+    """Average launch time of the planned GEMM.  With ``epilogue_act`` set, the
+    fused epilogue act(A B^T + bias) + residual runs in the same launch."""
     from dense_gemm_blackwell_sm_gb300 import gemm
     code = gemm.dtype_code(w.in_dtype, w.out_dtype)
     a, b = inputs.workload_operands(w)
@@ -179,10 +182,21 @@ def bench_gemm(w: inputs.Workload, steps: int, warmup: int, dev, dist_barrier, v
     stream = torch.cuda.current_stream(dev)
     sp = stream.cuda_stream
     ptrs = [(x.data_ptr(), y.data_ptr(), z.data_ptr()) for x, y, z in sets]
+    epi = None
+    if epilogue_act is not None:
+        bias = torch.randn(w.N, device=dev, dtype=torch.float32)
+        res = torch.randn(w.M, w.N, device=dev).to(inputs.torch_dtype(w.out_dtype))
+        epi = gemm.Epilogue()
+        epi.bias, epi.residual, epi.activation = bias.data_ptr(), res.data_ptr(), int(epilogue_act)
+        lib = gemm.load()
+        import ctypes
 
     def step(i):
         pa, pb, pc = ptrs[i & 1]
-        st = plan.run_ptr(pa, pb, pc, sp)
+        if epi is None:
+            st = plan.run_ptr(pa, pb, pc, sp)
+        else:
+            st = lib.gemm_plan_run_epilogue(plan._h, pa, pb, pc, ctypes.byref(epi), sp)
         if st != 0:
             raise gemm.GemmError(st, "gemm_plan_run")
 
@@ -296,6 +310,11 @@ def cpu_oracle_rate(w: inputs.Workload, budget_s: float = 12.0) -> dict:
 
 
 # ---------------------------------------------------------------------------
+
+def _g_act_silu() -> int:
+    from dense_gemm_blackwell_sm_gb300 import gemm
+    return gemm.ACT_SILU
+
 
 def _dist():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
@@ -423,6 +442,11 @@ def main(argv=None):
         also[w3.name] = {"tflops": round(w3.flops / r3["per_launch_s"] / 1e12, 3),
                          "frac_of_measured": round(w3.flops / r3["per_launch_s"] / 1e12 / float(peaks.get("bf16_tflops", 1900.0)), 4),
                          "variant": r3["info"]["variant_name"]}
+        re = bench_gemm(w, min(args.steps, 100), 5, dev, lambda: None, epilogue_act=_g_act_silu())
+        also[w.name + "+bias+silu+residual"] = {
+            "tflops": round(w.flops / re["per_launch_s"] / 1e12, 3),
+            "us_per_launch": round(re["per_launch_s"] * 1e6, 1),
+            "note": "fused epilogue act(A B^T + bias) + residual in the writeback warps"}
         w4 = inputs.WORKLOADS["llm_proj_8192x14336x4096_bf16_bf16"]
         r4 = bench_gemm(w4, 50, 5, dev, lambda: None)
         also[w4.name] = {"tflops": round(w4.flops / r4["per_launch_s"] / 1e12, 3),

@@ -31,6 +31,7 @@ struct gemm_plan_s {
   uint64_t timeout_ns;
   uint32_t debug_flags;
   int32_t flags;      // GEMM_FLAG_*
+  int32_t layout;     // GEMM_LAYOUT_*
   uint32_t* scratch;  // [0] status word, [1] tile counter, [2] finished counter
   int32_t* visits;
   dgb::LaunchSpec spec;   // kernel, launch shape and SMEM, fixed at plan time
@@ -172,6 +173,9 @@ gemm_status_t prepare_launch(gemm_plan_s* p) {
     k.debug_flags = p->debug_flags;
     k.out_ld = (int32_t)p->N;
     k.idesc = is_ws(v) ? make_idesc(p->in_bf16, 128 * p->cg, 256) : make_idesc(p->in_bf16, 128, 128);
+    k.layout = (uint32_t)p->layout;
+    if (p->layout & GEMM_LAYOUT_A_MN) k.idesc |= 1u << 15;  // A MN-major
+    if (p->layout & GEMM_LAYOUT_B_MN) k.idesc |= 1u << 16;  // B MN-major
     if (v <= GEMM_VARIANT_S3_MULTI_CTA) {
       e = spec_step123((int)p->M, (int)p->N, p->out_f32, &p->spec);
     } else if (v <= GEMM_VARIANT_S5_PIPELINE) {
@@ -197,13 +201,24 @@ gemm_status_t build_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, co
   if (opts) o = *opts;
   if (o.variant < 0 || o.variant > GEMM_VARIANT_GEMV_TC || o.sched < 0 || o.sched > GEMM_SCHED_CLC ||
       o.stages < 0 || o.stages > 12 || o.raster_group < 0 || o.max_ctas < 0 || o.timeout_ns < 0 ||
-      o.split_k < 0 || o.split_k > 8 || (o.flags & ~GEMM_FLAG_STATIC_B) != 0)
+      o.split_k < 0 || o.split_k > 8 || (o.flags & ~GEMM_FLAG_STATIC_B) != 0 ||
+      (o.layout & ~(GEMM_LAYOUT_A_MN | GEMM_LAYOUT_B_MN)) != 0)
     return GEMM_ERR_INVALID_ARG;
 
   int dev = 0, sms = 0;
   st = current_device(&dev, &sms);
   if (st != GEMM_OK && !o.variant) return st;
   int variant = o.variant ? o.variant : auto_variant(M, N, K, dtype, sms);
+  if (o.layout != 0) {
+    // MN-major operands exist in the warp-specialised kernels only
+    if (!o.variant && !is_ws(variant)) {
+      const int64_t tn = (N + 255) / 256, pairs = std::max(1, sms / 2);
+      variant = (((M + 255) / 256) * tn >= pairs) ? GEMM_VARIANT_S8_CTA_PAIR : GEMM_VARIANT_S7_WARP_SPECIALIZED;
+    }
+    if (!is_ws(variant)) return GEMM_ERR_UNSUPPORTED_SHAPE;
+    if (((o.layout & GEMM_LAYOUT_A_MN) && M % 8 != 0) || ((o.layout & GEMM_LAYOUT_B_MN) && N % 8 != 0))
+      return GEMM_ERR_UNSUPPORTED_SHAPE;
+  }
   // shape limits of the individual steps
   if (variant == GEMM_VARIANT_S1_SINGLE_TILE && (M > 128 || N > 128 || K > 64)) return GEMM_ERR_UNSUPPORTED_SHAPE;
   if (variant == GEMM_VARIANT_S2_KLOOP && (M > 128 || N > 128)) return GEMM_ERR_UNSUPPORTED_SHAPE;
@@ -229,6 +244,7 @@ gemm_status_t build_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, co
   p->timeout_ns = o.timeout_ns ? (uint64_t)o.timeout_ns : kDefaultTimeoutNs;
   p->debug_flags = (uint32_t)o.debug_flags;
   p->flags = o.flags;
+  p->layout = o.layout;
   p->cg = 1;
   p->consumers = 1;
   p->sched = 0;
@@ -323,6 +339,11 @@ const CUtensorMap* operand_map(gemm_plan_s* p, int role, const void* ptr) {
   if (role == 3) {
     // activation rows of the tensor-core GEMV: 16-row boxes, rows >= M read as zero
     ok = encode_2d(&victim->map, in_t, 2, ptr, (uint64_t)p->K, (uint64_t)p->M, 64, 16);
+  } else if (role == 0 && (p->layout & GEMM_LAYOUT_A_MN)) {
+    // A stored K x M: 64-wide boxes along M, 64 rows of K
+    ok = encode_2d(&victim->map, in_t, 2, ptr, (uint64_t)p->M, (uint64_t)p->K, 64, 64);
+  } else if (role == 1 && (p->layout & GEMM_LAYOUT_B_MN)) {
+    ok = encode_2d(&victim->map, in_t, 2, ptr, (uint64_t)p->N, (uint64_t)p->K, 64, 64);
   } else if (role == 0) {
     ok = encode_2d(&victim->map, in_t, 2, ptr, (uint64_t)p->K, (uint64_t)p->M, 64, 128);
   } else if (role == 1) {

@@ -51,7 +51,12 @@ struct KParams {
   const float* bias;     // N fp32 values, or null
   const void* residual;  // M x N in C's type, row-major (ld = out_ld), or null
   int32_t act;           // EPI_ACT_*
+  // operand layouts (steps 7-9): bit 0 = A stored K x M (M-major), bit 1 = B stored K x N (N-major)
+  uint32_t layout;
 };
+
+constexpr uint32_t LAYOUT_A_MN = 1u;
+constexpr uint32_t LAYOUT_B_MN = 2u;
 
 // activations of the fused epilogue
 enum : int32_t {

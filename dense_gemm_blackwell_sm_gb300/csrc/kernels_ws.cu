@@ -135,6 +135,8 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
   const uint32_t peer_abort = (CG == 2) ? mapa_shared(smem_u32((const void*)abort_flag), rank ^ 1u) : 0u;
   const WaitCtl w{abort_flag, p.status, p.timeout_ns, peer_abort};
   const int32_t KB = (p.K + WS_BK - 1) / WS_BK;
+  const bool a_mn = (p.layout & LAYOUT_A_MN) != 0u;
+  const bool b_mn = (p.layout & LAYOUT_B_MN) != 0u;
 
   // one lane takes the next entry of the tile-id ring; -1 ends the stream
   auto ring_get = [&](uint32_t i, int32_t& tile) -> bool {
@@ -221,18 +223,39 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
 #pragma unroll
           for (int c = 0; c < NCONS; ++c) {
             const int32_t row = m_cta + c * 128 * CG;
-            if constexpr (CG == 1) {
-              tma_load_2d(smem_u32(st + c * WS_A_BYTES), &tmA, fb, kb * WS_BK, row);
+            uint8_t* dst = st + c * WS_A_BYTES;
+            if (a_mn) {
+              // K x M in memory: two 64-row-of-K x 64-M boxes, 8 KB apart
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                if constexpr (CG == 1) {
+                  tma_load_2d(smem_u32(dst + h * 8192), &tmA, fb, row + 64 * h, kb * WS_BK);
+                } else {
+                  tma_load_2d_pair(smem_u32(dst + h * 8192), &tmA, mapa_shared(fb, 0), row + 64 * h, kb * WS_BK);
+                }
+              }
+            } else if constexpr (CG == 1) {
+              tma_load_2d(smem_u32(dst), &tmA, fb, kb * WS_BK, row);
             } else {
-              tma_load_2d_pair(smem_u32(st + c * WS_A_BYTES), &tmA, mapa_shared(fb, 0), kb * WS_BK, row);
+              tma_load_2d_pair(smem_u32(dst), &tmA, mapa_shared(fb, 0), kb * WS_BK, row);
             }
           }
+          uint8_t* bdst = st + NCONS * WS_A_BYTES;
           if (skip) {
             skip = false;  // test hook: this stage's B bytes never arrive
+          } else if (b_mn) {
+#pragma unroll
+            for (int h = 0; h < Cfg::B_ROWS / 64; ++h) {
+              if constexpr (CG == 1) {
+                tma_load_2d(smem_u32(bdst + h * 8192), &tmB, fb, n_cta + 64 * h, kb * WS_BK);
+              } else {
+                tma_load_2d_pair(smem_u32(bdst + h * 8192), &tmB, mapa_shared(fb, 0), n_cta + 64 * h, kb * WS_BK);
+              }
+            }
           } else if constexpr (CG == 1) {
-            tma_load_2d(smem_u32(st + NCONS * WS_A_BYTES), &tmB, fb, kb * WS_BK, n_cta);
+            tma_load_2d(smem_u32(bdst), &tmB, fb, kb * WS_BK, n_cta);
           } else {
-            tma_load_2d_pair(smem_u32(st + NCONS * WS_A_BYTES), &tmB, mapa_shared(fb, 0), kb * WS_BK, n_cta);
+            tma_load_2d_pair(smem_u32(bdst), &tmB, mapa_shared(fb, 0), kb * WS_BK, n_cta);
           }
           if (++stage == (uint32_t)S) { stage = 0; sphase ^= 1u; }
         }
@@ -262,10 +285,13 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
           tc_fence_after();
           const uint32_t sa = smem_u32(ring + (size_t)stage * Cfg::STAGE + cons * WS_A_BYTES);
           const uint32_t sb = smem_u32(ring + (size_t)stage * Cfg::STAGE + NCONS * WS_A_BYTES);
-          const uint64_t ad = sdesc_k_sw128(sa), bd = sdesc_k_sw128(sb);
+          // K-major: a K step of 16 moves 32 B inside the swizzle row; MN-major: two 1 KB atoms
+          const uint64_t ad = a_mn ? sdesc_mn_sw128(sa, 8192) : sdesc_k_sw128(sa);
+          const uint64_t bd = b_mn ? sdesc_mn_sw128(sb, 8192) : sdesc_k_sw128(sb);
+          const uint64_t astep = a_mn ? 128 : 2, bstep = b_mn ? 128 : 2;
 #pragma unroll
           for (int k = 0; k < WS_BK / 16; ++k)
-            mma_f16<CG>(d, ad + 2 * k, bd + 2 * k, p.idesc, (kb | k) != 0);
+            mma_f16<CG>(d, ad + astep * k, bd + bstep * k, p.idesc, (kb | k) != 0);
           if constexpr (CG == 1) {
             mma_commit(smem_u32(empty + stage));
           } else {

@@ -435,6 +435,19 @@ __device__ __forceinline__ uint64_t sdesc_k_sw128(uint32_t saddr) {
          | ((uint64_t)2u << 61);               // layout: 128-byte swizzle
 }
 
+// Shared-memory matrix descriptor for an MN-major operand tile written with the
+// 128-byte swizzle: the rows of the tile run along K, each holding 64 16-bit
+// MN-consecutive elements (128 B); 8 K-rows form a 1024-byte atom (stride byte
+// offset), and consecutive 64-element MN groups lie `mn_group_bytes` apart
+// (leading byte offset).  A K step of 16 moves the start by two atoms, 2048 B.
+__device__ __forceinline__ uint64_t sdesc_mn_sw128(uint32_t saddr, uint32_t mn_group_bytes) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4)
+         | ((uint64_t)((mn_group_bytes >> 4) & 0x3FFFu) << 16)  // leading byte offset
+         | ((uint64_t)(1024u >> 4) << 32)                       // stride byte offset: 8 K-rows x 128 B
+         | ((uint64_t)1u << 46)
+         | ((uint64_t)2u << 61);
+}
+
 // byte offset of 16-byte chunk `c` (0..7) of row `r` inside a 128B-swizzled tile
 __device__ __forceinline__ uint32_t sw128_offset(uint32_t r, uint32_t c) {
   return r * 128u + ((c ^ (r & 7u)) << 4);

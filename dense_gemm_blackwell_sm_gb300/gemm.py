@@ -36,6 +36,7 @@ ACT_NONE, ACT_RELU, ACT_SILU, ACT_GELU_TANH, ACT_GELU_ERF = 0, 1, 2, 3, 4
 
 DEBUG_SKIP_ONE_LOAD = 1
 FLAG_STATIC_B = 1
+LAYOUT_A_MN, LAYOUT_B_MN = 1, 2
 
 
 class GemmError(RuntimeError):
@@ -48,7 +49,7 @@ class Opts(ctypes.Structure):
     _fields_ = [("variant", ctypes.c_int32), ("sched", ctypes.c_int32), ("stages", ctypes.c_int32),
                 ("raster_group", ctypes.c_int32), ("max_ctas", ctypes.c_int32), ("split_k", ctypes.c_int32),
                 ("timeout_ns", ctypes.c_int64), ("debug_flags", ctypes.c_int32), ("flags", ctypes.c_int32),
-                ("reserved", ctypes.c_int32 * 6)]
+                ("layout", ctypes.c_int32), ("reserved", ctypes.c_int32 * 5)]
 
 
 class PlanInfo(ctypes.Structure):
@@ -123,9 +124,10 @@ def _stream_ptr(stream) -> int:
 
 
 def make_opts(variant=0, sched=0, stages=0, raster_group=0, max_ctas=0, timeout_ns=0, debug_flags=0,
-              split_k=0, flags=0) -> Opts:
+              split_k=0, flags=0, layout=0) -> Opts:
     o = Opts()
     o.flags = int(flags)
+    o.layout = int(layout)
     o.split_k = int(split_k)
     o.variant, o.sched, o.stages, o.raster_group = int(variant), int(sched), int(stages), int(raster_group)
     o.max_ctas, o.timeout_ns, o.debug_flags = int(max_ctas), int(timeout_ns), int(debug_flags)
@@ -210,10 +212,26 @@ def gemm_check(stream=None) -> int:
     return load().gemm_check(None, _stream_ptr(stream))
 
 
+_layout_plans: dict = {}
+
+
+def _stored(x):
+    """(tensor as stored, is_mn_major) for a logical (rows x K) operand: a
+    contiguous tensor is K-major; a transposed view of a contiguous K x rows
+    tensor is passed as stored, MN-major, without a copy."""
+    if x.is_contiguous():
+        return x, False
+    if x.t().is_contiguous():
+        return x.t(), True
+    return x.contiguous(), False
+
+
 def matmul(a, b, out_dtype=None, out=None, stream=None):
     """C = a @ b.T for CUDA tensors a (M x K) and b (N x K), fp16 or bf16.
 
-    ``out_dtype`` is torch.float32 (default) or torch.bfloat16.
+    ``out_dtype`` is torch.float32 (default) or torch.bfloat16.  An operand that
+    is the transpose of a contiguous tensor (``x.t()``) is read in place as an
+    MN-major operand by the warp-specialised kernels.
     """
     import torch
     if not (a.is_cuda and b.is_cuda):
@@ -224,15 +242,26 @@ def matmul(a, b, out_dtype=None, out=None, stream=None):
         raise ValueError("a and b must share a dtype")
     out_dtype = out_dtype or (out.dtype if out is not None else torch.float32)
     code = dtype_code(a.dtype, out_dtype)
-    a = a.contiguous()
-    b = b.contiguous()
     M, K = a.shape
     N = b.shape[0]
+    a_s, a_mn = _stored(a)
+    b_s, b_mn = _stored(b)
     if out is None:
         out = torch.empty((M, N), device=a.device, dtype=out_dtype)
     elif out.shape != (M, N) or not out.is_contiguous() or out.dtype != out_dtype:
         raise ValueError("out must be a contiguous (M, N) tensor of out_dtype")
-    _check(gemm_run(M, N, K, a.data_ptr(), b.data_ptr(), out.data_ptr(), code, _stream_ptr(stream)), "gemm_run")
+    layout = (LAYOUT_A_MN if a_mn else 0) | (LAYOUT_B_MN if b_mn else 0)
+    if layout and ((a_mn and M % 8) or (b_mn and N % 8)):
+        a_s, b_s, layout = a.contiguous(), b.contiguous(), 0
+    if layout == 0:
+        _check(gemm_run(M, N, K, a_s.data_ptr(), b_s.data_ptr(), out.data_ptr(), code, _stream_ptr(stream)),
+               "gemm_run")
+        return out
+    key = (M, N, K, code, layout, a.device.index)
+    plan = _layout_plans.get(key)
+    if plan is None:
+        plan = _layout_plans[key] = Plan(M, N, K, code, make_opts(layout=layout))
+    _check(plan.run_ptr(a_s.data_ptr(), b_s.data_ptr(), out.data_ptr(), _stream_ptr(stream)), "gemm_plan_run")
     return out
 
 

@@ -101,8 +101,17 @@ typedef struct {
   int64_t timeout_ns;   /* bound on every device-side wait, 0 = 2 s */
   int32_t debug_flags;  /* test hooks: 1 = leave out one TMA load (forces a timeout) */
   int32_t flags;        /* GEMM_FLAG_* */
-  int32_t reserved[6];
+  int32_t layout;       /* GEMM_LAYOUT_* bits; 0 = both operands K-major */
+  int32_t reserved[5];
 } gemm_opts_t;
+
+/* Operand storage (variants 7-9).  C = A * B^T always; by default A is M x K and
+ * B is N x K row-major (K-major).  GEMM_LAYOUT_A_MN: A is stored K x M row-major
+ * (M-major, needs M % 8 == 0); GEMM_LAYOUT_B_MN: B is stored K x N row-major
+ * (N-major, needs N % 8 == 0).  The reading notes name k-major and mn-major as
+ * the two element orders a tile can have (section "三个核心概念", layout). */
+#define GEMM_LAYOUT_A_MN 1
+#define GEMM_LAYOUT_B_MN 2
 
 /* B is not written by the work queued before the call on the same stream
  * (weights of a decode step).  The GEMV variants then launch as programmatic
