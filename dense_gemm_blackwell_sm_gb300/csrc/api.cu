@@ -37,6 +37,8 @@ struct gemm_plan_s {
   dgb::LaunchSpec spec;   // kernel, launch shape and SMEM, fixed at plan time
   dgb::LaunchSpec spec_epi;  // the fused-epilogue kernel (variants 7-9), made on first use
   bool epi_ready;
+  int epi_tiles_m, epi_stages;  // its tiling: one MMA consumer, so the TMEM double buffer lets the
+                                // epilogue of one tile overlap the MMAs of the next
   dgb::KParams kbase;     // kernel parameters that do not depend on the pointers
   dgb::TgParams tgbase;   // same, for the tensor-core GEMV
   // TMA descriptors by operand role (0 = A, 1 = B, 2 = C) and pointer, least
@@ -398,6 +400,8 @@ gemm_status_t launch_plan(gemm_plan_s* p, const void* A, const void* B, void* C,
         k.bias = epi->bias;
         k.residual = epi->residual;
         k.act = epi->activation;
+        k.tiles_m = p->epi_tiles_m;
+        k.stages = p->epi_stages;
         spec = &p->spec_epi;
       }
       k.A = static_cast<const uint16_t*>(A);
@@ -475,8 +479,17 @@ gemm_status_t gemm_plan_run_epilogue(gemm_plan_t plan, const void* A, const void
   if ((reinterpret_cast<uintptr_t>(epi->bias) & 3u) || (reinterpret_cast<uintptr_t>(epi->residual) & 15u))
     return GEMM_ERR_MISALIGNED;
   if (!plan->epi_ready) {
-    if (spec_ws(plan->cg, plan->consumers, plan->sched - 1, plan->out_f32, plan->stages, plan->grid_units,
-                &plan->spec_epi, /*fused=*/true) != cudaSuccess) {
+    // The fused epilogue does real arithmetic per element, so it must hide behind
+    // the MMAs: a step-9 plan (both TMEM accumulators busy) runs it with one
+    // consumer per CTA, i.e. step 8's double-buffered 256x256 tile, same operand boxes.
+    const int cons = 1;
+    plan->epi_stages = ws_max_stages(plan->cg, cons);
+    plan->epi_tiles_m = ceil_div(plan->M, 128 * plan->cg * cons);
+    const int tiles = plan->epi_tiles_m * plan->tiles_n;
+    int active = ws_max_active_clusters(plan->cg, cons, 0, plan->out_f32, plan->epi_stages);
+    if (active < 1) active = std::max(1, plan->num_sms / plan->cg);
+    if (spec_ws(plan->cg, cons, 0, plan->out_f32, plan->epi_stages, std::min(tiles, active), &plan->spec_epi,
+                /*fused=*/true) != cudaSuccess) {
       cudaGetLastError();
       return GEMM_ERR_CUDA;
     }

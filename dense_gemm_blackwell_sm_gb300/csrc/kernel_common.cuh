@@ -70,7 +70,7 @@ enum : int32_t {
 __device__ __forceinline__ float epi_activation(float x, int32_t act) {
   switch (act) {
     case EPI_ACT_RELU: return fmaxf(x, 0.f);
-    case EPI_ACT_SILU: return x / (1.f + expf(-x));
+    case EPI_ACT_SILU: return x * __frcp_rn(1.f + expf(-x));  // correctly rounded reciprocal
     case EPI_ACT_GELU_TANH: {
       const float k0 = 0.7978845608028654f;  // sqrt(2 / pi)
       return 0.5f * x * (1.f + tanhf(k0 * (x + 0.044715f * x * x * x)));
