@@ -35,8 +35,8 @@ struct gemm_plan_s {
   uint32_t* scratch;  // [0] status word, [1] tile counter, [2] finished counter
   int32_t* visits;
   dgb::LaunchSpec spec;   // kernel, launch shape and SMEM, fixed at plan time
-  dgb::LaunchSpec spec_epi;  // the fused-epilogue kernel (variants 7-9), made on first use
-  bool epi_ready;
+  dgb::LaunchSpec spec_epi[5];  // the fused-epilogue kernel per activation, made on first use
+  bool epi_ready[5];
   int epi_tiles_m, epi_stages;  // its tiling: one MMA consumer, so the TMEM double buffer lets the
                                 // epilogue of one tile overlap the MMAs of the next
   dgb::KParams kbase;     // kernel parameters that do not depend on the pointers
@@ -402,7 +402,7 @@ gemm_status_t launch_plan(gemm_plan_s* p, const void* A, const void* B, void* C,
         k.act = epi->activation;
         k.tiles_m = p->epi_tiles_m;
         k.stages = p->epi_stages;
-        spec = &p->spec_epi;
+        spec = &p->spec_epi[epi->activation];
       }
       k.A = static_cast<const uint16_t*>(A);
       k.B = static_cast<const uint16_t*>(B);
@@ -478,7 +478,8 @@ gemm_status_t gemm_plan_run_epilogue(gemm_plan_t plan, const void* A, const void
   if (epi->activation < GEMM_ACT_NONE || epi->activation > GEMM_ACT_GELU_ERF) return GEMM_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(epi->bias) & 3u) || (reinterpret_cast<uintptr_t>(epi->residual) & 15u))
     return GEMM_ERR_MISALIGNED;
-  if (!plan->epi_ready) {
+  const int act = epi->activation;
+  if (!plan->epi_ready[act]) {
     // The fused epilogue does real arithmetic per element, so it must hide behind
     // the MMAs: a step-9 plan (both TMEM accumulators busy) runs it with one
     // consumer per CTA, i.e. step 8's double-buffered 256x256 tile, same operand boxes.
@@ -488,12 +489,12 @@ gemm_status_t gemm_plan_run_epilogue(gemm_plan_t plan, const void* A, const void
     const int tiles = plan->epi_tiles_m * plan->tiles_n;
     int active = ws_max_active_clusters(plan->cg, cons, 0, plan->out_f32, plan->epi_stages);
     if (active < 1) active = std::max(1, plan->num_sms / plan->cg);
-    if (spec_ws(plan->cg, cons, 0, plan->out_f32, plan->epi_stages, std::min(tiles, active), &plan->spec_epi,
-                /*fused=*/true) != cudaSuccess) {
+    if (spec_ws(plan->cg, cons, 0, plan->out_f32, plan->epi_stages, std::min(tiles, active), &plan->spec_epi[act],
+                act) != cudaSuccess) {
       cudaGetLastError();
       return GEMM_ERR_CUDA;
     }
-    plan->epi_ready = true;
+    plan->epi_ready[act] = true;
   }
   return launch_plan(plan, A, B, C, reinterpret_cast<cudaStream_t>(stream), epi);
 }

@@ -67,16 +67,22 @@ enum : int32_t {
   EPI_ACT_GELU_ERF = 4,   // 0.5 x (1 + erf(x / sqrt(2)))
 };
 
-__device__ __forceinline__ float epi_activation(float x, int32_t act) {
-  switch (act) {
-    case EPI_ACT_RELU: return fmaxf(x, 0.f);
-    case EPI_ACT_SILU: return x * __frcp_rn(1.f + expf(-x));  // correctly rounded reciprocal
-    case EPI_ACT_GELU_TANH: {
-      const float k0 = 0.7978845608028654f;  // sqrt(2 / pi)
-      return 0.5f * x * (1.f + tanhf(k0 * (x + 0.044715f * x * x * x)));
-    }
-    case EPI_ACT_GELU_ERF: return 0.5f * x * (1.f + erff(x * 0.7071067811865476f));
-    default: return x;
+// the activation is a compile-time choice: each fused kernel carries the code
+// of one activation only (the writeback code shares the SM's instruction cache
+// with the producer and MMA warps)
+template <int ACT>
+__device__ __forceinline__ float epi_activation(float x) {
+  if constexpr (ACT == EPI_ACT_RELU) {
+    return fmaxf(x, 0.f);
+  } else if constexpr (ACT == EPI_ACT_SILU) {
+    return x * __frcp_rn(1.f + expf(-x));  // correctly rounded reciprocal
+  } else if constexpr (ACT == EPI_ACT_GELU_TANH) {
+    const float k0 = 0.7978845608028654f;  // sqrt(2 / pi)
+    return 0.5f * x * (1.f + tanhf(k0 * (x + 0.044715f * x * x * x)));
+  } else if constexpr (ACT == EPI_ACT_GELU_ERF) {
+    return 0.5f * x * (1.f + erff(x * 0.7071067811865476f));
+  } else {
+    return x;
   }
 }
 
@@ -84,7 +90,7 @@ __device__ __forceinline__ float epi_activation(float x, int32_t act) {
 // (columns col0 .. col0+n-1), in place.  bias is read through L1 (every lane of
 // a warp reads the same columns); the residual row segment with 16-byte loads
 // when it lies wholly inside C, element by element at the edges.
-template <typename OutT, int n>
+template <typename OutT, int n, int ACT>
 __device__ __forceinline__ void apply_epilogue(uint32_t* v, const KParams& p, int32_t row, int32_t col0) {
   float x[n];
 #pragma unroll
@@ -93,9 +99,9 @@ __device__ __forceinline__ void apply_epilogue(uint32_t* v, const KParams& p, in
 #pragma unroll
     for (int j = 0; j < n; ++j) x[j] += (col0 + j < p.N) ? __ldg(p.bias + col0 + j) : 0.f;
   }
-  if (p.act != EPI_ACT_NONE) {
+  if constexpr (ACT != EPI_ACT_NONE) {
 #pragma unroll
-    for (int j = 0; j < n; ++j) x[j] = epi_activation(x[j], p.act);
+    for (int j = 0; j < n; ++j) x[j] = epi_activation<ACT>(x[j]);
   }
   if (p.residual != nullptr && row < p.M) {
     const OutT* r = reinterpret_cast<const OutT*>(p.residual) + (int64_t)row * p.out_ld + col0;

@@ -64,7 +64,8 @@ struct WsCfg {
   static constexpr uint32_t RING_CONSUMERS = (uint32_t)(CG * 5 + NCONS);
 };
 
-template <typename OutT, int CG, int NCONS, int SCHED, bool FUSED = false>
+// EPI < 0: plain writeback; EPI >= 0: fused epilogue with activation EPI
+template <typename OutT, int CG, int NCONS, int SCHED, int EPI = -1>
 __global__ void __launch_bounds__(WS_THREADS, 1)
     k_ws(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
          const __grid_constant__ CUtensorMap tmC, KParams p) {
@@ -356,12 +357,12 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
               }
             }
           }
-          if constexpr (FUSED) {
+          if constexpr (EPI >= 0) {
             // bias, activation and residual, in fp32, before the single rounding to C's type
             const int32_t row = row0 + (int32_t)lane;
             const int32_t col0 = col_base + ch * CW;
-            apply_epilogue<OutT, 32>(v0, p, row, col0);
-            if constexpr (CW == 64) apply_epilogue<OutT, 32>(v1, p, row, col0 + 32);
+            apply_epilogue<OutT, 32, EPI>(v0, p, row, col0);
+            if constexpr (CW == 64) apply_epilogue<OutT, 32, EPI>(v1, p, row, col0 + 32);
           }
           uint8_t* buf = my_staging + (tog & 1u) * 4096u;
           if (lane == 0) bulk_wait_group_read<1>();  // the store issued from `buf` two chunks ago is done reading
@@ -405,17 +406,28 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
   }
 }
 
-template <typename OutT, int CG, int NCONS, int SCHED, bool FUSED = false>
+template <typename OutT, int CG, int NCONS, int SCHED, int EPI = -1>
 void* ws_kernel_ptr() {
-  return reinterpret_cast<void*>(k_ws<OutT, CG, NCONS, SCHED, FUSED>);
+  return reinterpret_cast<void*>(k_ws<OutT, CG, NCONS, SCHED, EPI>);
 }
 
-// the fused-epilogue kernels exist for the static scheduler only
+template <typename OutT, int CG>
+void* pick_fused(int act) {
+  switch (act) {
+    case EPI_ACT_RELU: return ws_kernel_ptr<OutT, CG, 1, SCHED_STATIC, EPI_ACT_RELU>();
+    case EPI_ACT_SILU: return ws_kernel_ptr<OutT, CG, 1, SCHED_STATIC, EPI_ACT_SILU>();
+    case EPI_ACT_GELU_TANH: return ws_kernel_ptr<OutT, CG, 1, SCHED_STATIC, EPI_ACT_GELU_TANH>();
+    case EPI_ACT_GELU_ERF: return ws_kernel_ptr<OutT, CG, 1, SCHED_STATIC, EPI_ACT_GELU_ERF>();
+    default: return ws_kernel_ptr<OutT, CG, 1, SCHED_STATIC, EPI_ACT_NONE>();
+  }
+}
+
+// the fused-epilogue kernels exist for one MMA consumer and the static scheduler
 template <int CG, int NCONS>
-void* pick_kernel(int sched, bool out_f32, bool fused) {
-  if (fused) {
-    return out_f32 ? ws_kernel_ptr<float, CG, NCONS, SCHED_STATIC, true>()
-                   : ws_kernel_ptr<__nv_bfloat16, CG, NCONS, SCHED_STATIC, true>();
+void* pick_kernel(int sched, bool out_f32, int fused_act) {
+  if (fused_act >= 0) {
+    if (NCONS != 1) return nullptr;
+    return out_f32 ? pick_fused<float, CG>(fused_act) : pick_fused<__nv_bfloat16, CG>(fused_act);
   }
   if (out_f32) {
     if (sched == SCHED_ATOMIC) return ws_kernel_ptr<float, CG, NCONS, SCHED_ATOMIC>();
@@ -427,11 +439,11 @@ void* pick_kernel(int sched, bool out_f32, bool fused) {
   return ws_kernel_ptr<__nv_bfloat16, CG, NCONS, SCHED_STATIC>();
 }
 
-void* ws_kernel(int cg, int consumers, int sched, bool out_f32, bool fused = false) {
-  if (cg == 1 && consumers == 1) return pick_kernel<1, 1>(sched, out_f32, fused);
-  if (cg == 1 && consumers == 2) return pick_kernel<1, 2>(sched, out_f32, fused);
-  if (cg == 2 && consumers == 1) return pick_kernel<2, 1>(sched, out_f32, fused);
-  if (cg == 2 && consumers == 2) return pick_kernel<2, 2>(sched, out_f32, fused);
+void* ws_kernel(int cg, int consumers, int sched, bool out_f32, int fused_act = -1) {
+  if (cg == 1 && consumers == 1) return pick_kernel<1, 1>(sched, out_f32, fused_act);
+  if (cg == 1 && consumers == 2) return pick_kernel<1, 2>(sched, out_f32, fused_act);
+  if (cg == 2 && consumers == 1) return pick_kernel<2, 1>(sched, out_f32, fused_act);
+  if (cg == 2 && consumers == 2) return pick_kernel<2, 2>(sched, out_f32, fused_act);
   return nullptr;
 }
 
@@ -492,8 +504,8 @@ int ws_max_active_clusters(int cg, int consumers, int sched, bool out_f32, int s
 }
 
 cudaError_t spec_ws(int cg, int consumers, int sched, bool out_f32, int stages, int clusters, LaunchSpec* out,
-                    bool fused) {
-  void* k = ws_kernel(cg, consumers, fused ? SCHED_STATIC : sched, out_f32, fused);
+                    int fused_act) {
+  void* k = ws_kernel(cg, consumers, fused_act >= 0 ? SCHED_STATIC : sched, out_f32, fused_act);
   if (!k) return cudaErrorInvalidValue;
   const size_t smem = ws_smem_bytes(cg, consumers, stages);
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

@@ -59,9 +59,10 @@ WsShape ws_shape(int cg, int consumers);
 size_t ws_smem_bytes(int cg, int consumers, int stages);
 int ws_max_stages(int cg, int consumers);
 int ws_max_active_clusters(int cg, int consumers, int sched, bool out_f32, int stages);
-// fused = the writeback applies bias / activation / residual (static scheduler)
+// fused_act >= 0: the writeback applies bias / activation fused_act / residual
+// (one MMA consumer, static scheduler); -1: plain writeback
 cudaError_t spec_ws(int cg, int consumers, int sched, bool out_f32, int stages, int clusters, LaunchSpec* out,
-                    bool fused = false);
+                    int fused_act = -1);
 
 // decode GEMV, C (M x N) = X (M x K) * B^T for M <= 16, on CUDA cores
 struct GemvParams {
