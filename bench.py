@@ -347,6 +347,8 @@ def main(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(inputs.WORKLOADS))
     ap.add_argument("--variant", type=int, default=0)
+    ap.add_argument("--epilogue", default=None, choices=["none", "relu", "silu", "gelu_tanh", "gelu_erf"],
+                    help="time the step with the fused epilogue act(A B^T + bias) + residual")
     ap.add_argument("--shape", default=None,
                     help="M,N,K[,in,out]: a custom bf16 GEMM shape instead of a named workload (profiling)")
     ap.add_argument("--no-extra", action="store_true")
@@ -400,7 +402,10 @@ def main(argv=None):
                               "stages": r["info"]["stages"], "clocks": r["clocks"]}), flush=True)
         return 0
 
-    res = bench_gemm(w, args.steps, args.warmup, dev, barrier, args.variant)
+    epi_act = None
+    if args.epilogue is not None:
+        epi_act = ["none", "relu", "silu", "gelu_tanh", "gelu_erf"].index(args.epilogue)
+    res = bench_gemm(w, args.steps, args.warmup, dev, barrier, args.variant, epilogue_act=epi_act)
     times = gather(res["seconds"])
     tmax, flops_per_s = aggregate(times, w.flops * args.steps)
     tflops = flops_per_s / 1e12
@@ -421,6 +426,7 @@ def main(argv=None):
                    "variant": res["info"]["variant_name"], "tile": [res["info"]["tile_m"], res["info"]["tile_n"]],
                    "cluster": res["info"]["cluster"], "stages": res["info"]["stages"],
                    "grid": res["info"]["grid"], "sched": res["info"]["sched"],
+                   "epilogue": args.epilogue or "plain",
                    "l2": "inputs larger than L2 (A+B+C = %d MB), two operand sets alternated" % (
                        w.algorithmic_bytes // 2**20),
                    "parallelism": "replicas" if world > 1 else "single GPU"},
