@@ -21,6 +21,7 @@ struct gemm_plan_s {
   int64_t M, N, K;
   gemm_dtype_t dtype;
   bool in_bf16, out_f32;
+  bool in_f8, in_e5m2;  // 8-bit float inputs (E4M3 or E5M2)
   int variant, sched, stages, raster_group;
   int device, num_sms;
   int grid_units;  // CTAs (variants 3-6) or clusters (7-9) launched
@@ -101,15 +102,21 @@ uint32_t make_idesc(bool bf16, int M, int N) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-int out_bytes(gemm_dtype_t dt) { return (dt == GEMM_F16_F32 || dt == GEMM_BF16_F32) ? 4 : 2; }
+int out_bytes(gemm_dtype_t dt) {
+  return (dt == GEMM_F16_F32 || dt == GEMM_BF16_F32 || dt == GEMM_E4M3_F32 || dt == GEMM_E5M2_F32) ? 4 : 2;
+}
+
+bool is_f8(gemm_dtype_t dt) { return dt >= GEMM_E4M3_F32 && dt <= GEMM_E5M2_BF16; }
+
+int in_bytes(gemm_dtype_t dt) { return is_f8(dt) ? 1 : 2; }
 
 // The TMA-store writeback of variants 7-9 needs rows of C to start 16-byte aligned.
 bool c_rows_tma_ok(int64_t N, gemm_dtype_t dt) { return (N * out_bytes(dt)) % 16 == 0; }
 
 gemm_status_t validate_sizes(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype) {
-  if ((int)dtype < 0 || (int)dtype > 3) return GEMM_ERR_UNSUPPORTED_DTYPE;
+  if ((int)dtype < 0 || (int)dtype > GEMM_E5M2_BF16) return GEMM_ERR_UNSUPPORTED_DTYPE;
   if (M < 1 || N < 1 || K < 1 || M >= kMaxDim || N >= kMaxDim || K >= kMaxDim) return GEMM_ERR_INVALID_ARG;
-  if (K % 8 != 0) return GEMM_ERR_UNSUPPORTED_SHAPE;
+  if ((K * in_bytes(dtype)) % 16 != 0) return GEMM_ERR_UNSUPPORTED_SHAPE;  // TMA row pitch
   return GEMM_OK;
 }
 
@@ -175,6 +182,16 @@ gemm_status_t prepare_launch(gemm_plan_s* p) {
     k.debug_flags = p->debug_flags;
     k.out_ld = (int32_t)p->N;
     k.idesc = is_ws(v) ? make_idesc(p->in_bf16, 128 * p->cg, 256) : make_idesc(p->in_bf16, 128, 128);
+    k.mma_kind = 0;
+    k.bk = 64;
+    if (p->in_f8) {
+      // kind::f8f6f4 descriptor: A / B format E4M3 = 0, E5M2 = 1, fp32 accumulator
+      const uint32_t fmt = p->in_e5m2 ? 1u : 0u;
+      k.idesc = (1u << 4) | (fmt << 7) | (fmt << 10) | ((uint32_t)(256 >> 3) << 17) |
+                ((uint32_t)((128 * p->cg) >> 4) << 24);
+      k.mma_kind = 1;
+      k.bk = 128;
+    }
     k.layout = (uint32_t)p->layout;
     if (p->layout & GEMM_LAYOUT_A_MN) k.idesc |= 1u << 15;  // A MN-major
     if (p->layout & GEMM_LAYOUT_B_MN) k.idesc |= 1u << 16;  // B MN-major
@@ -211,6 +228,15 @@ gemm_status_t build_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, co
   st = current_device(&dev, &sms);
   if (st != GEMM_OK && !o.variant) return st;
   int variant = o.variant ? o.variant : auto_variant(M, N, K, dtype, sms);
+  if (is_f8(dtype)) {
+    // 8-bit inputs run on the warp-specialised kernels only, K-major
+    if (o.layout != 0) return GEMM_ERR_UNSUPPORTED_SHAPE;
+    if (!o.variant && !is_ws(variant)) {
+      const int64_t tn = (N + 255) / 256, pairs = std::max(1, sms / 2);
+      variant = (((M + 255) / 256) * tn >= pairs) ? GEMM_VARIANT_S8_CTA_PAIR : GEMM_VARIANT_S7_WARP_SPECIALIZED;
+    }
+    if (!is_ws(variant)) return GEMM_ERR_UNSUPPORTED_SHAPE;
+  }
   if (o.layout != 0) {
     // MN-major operands exist in the warp-specialised kernels only
     if (!o.variant && !is_ws(variant)) {
@@ -239,6 +265,8 @@ gemm_status_t build_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, co
   p->K = K;
   p->dtype = dtype;
   p->in_bf16 = (dtype == GEMM_BF16_F32 || dtype == GEMM_BF16_BF16);
+  p->in_f8 = is_f8(dtype);
+  p->in_e5m2 = (dtype == GEMM_E5M2_F32 || dtype == GEMM_E5M2_BF16);
   p->out_f32 = (out_bytes(dtype) == 4);
   p->variant = variant;
   p->device = dev;
@@ -336,7 +364,11 @@ const CUtensorMap* operand_map(gemm_plan_s* p, int role, const void* ptr) {
     }
     if (m.used < victim->used) victim = &m;
   }
-  const CUtensorMapDataType in_t = p->in_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const CUtensorMapDataType in_t = p->in_f8    ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                   : p->in_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const int ie = p->in_f8 ? 1 : 2;     // bytes per input element
+  const uint32_t kbox = 128u / ie;     // one 128-byte swizzle row of K
   bool ok = false;
   if (role == 3) {
     // activation rows of the tensor-core GEMV: 16-row boxes, rows >= M read as zero
@@ -347,10 +379,10 @@ const CUtensorMap* operand_map(gemm_plan_s* p, int role, const void* ptr) {
   } else if (role == 1 && (p->layout & GEMM_LAYOUT_B_MN)) {
     ok = encode_2d(&victim->map, in_t, 2, ptr, (uint64_t)p->N, (uint64_t)p->K, 64, 64);
   } else if (role == 0) {
-    ok = encode_2d(&victim->map, in_t, 2, ptr, (uint64_t)p->K, (uint64_t)p->M, 64, 128);
+    ok = encode_2d(&victim->map, in_t, ie, ptr, (uint64_t)p->K, (uint64_t)p->M, kbox, 128);
   } else if (role == 1) {
     const uint32_t rows = is_ws(p->variant) ? (uint32_t)ws_shape(p->cg, p->consumers).b_box_rows : 128u;
-    ok = encode_2d(&victim->map, in_t, 2, ptr, (uint64_t)p->K, (uint64_t)p->N, 64, rows);
+    ok = encode_2d(&victim->map, in_t, ie, ptr, (uint64_t)p->K, (uint64_t)p->N, kbox, rows);
   } else {
     ok = p->out_f32 ? encode_2d(&victim->map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, ptr, (uint64_t)p->N,
                                 (uint64_t)p->M, 32, 32)
@@ -400,6 +432,8 @@ gemm_status_t launch_plan(gemm_plan_s* p, const void* A, const void* B, void* C,
         k.bias = epi->bias;
         k.residual = epi->residual;
         k.act = epi->activation;
+        k.scale_a = epi->scale_a;
+        k.scale_b = epi->scale_b;
         k.tiles_m = p->epi_tiles_m;
         k.stages = p->epi_stages;
         spec = &p->spec_epi[epi->activation];
@@ -476,7 +510,8 @@ gemm_status_t gemm_plan_run_epilogue(gemm_plan_t plan, const void* A, const void
   if (!plan || !epi) return GEMM_ERR_INVALID_ARG;
   if (!is_ws(plan->variant)) return GEMM_ERR_UNSUPPORTED_SHAPE;
   if (epi->activation < GEMM_ACT_NONE || epi->activation > GEMM_ACT_GELU_ERF) return GEMM_ERR_INVALID_ARG;
-  if ((reinterpret_cast<uintptr_t>(epi->bias) & 3u) || (reinterpret_cast<uintptr_t>(epi->residual) & 15u))
+  if ((reinterpret_cast<uintptr_t>(epi->bias) & 3u) || (reinterpret_cast<uintptr_t>(epi->residual) & 15u) ||
+      (reinterpret_cast<uintptr_t>(epi->scale_a) & 3u) || (reinterpret_cast<uintptr_t>(epi->scale_b) & 3u))
     return GEMM_ERR_MISALIGNED;
   const int act = epi->activation;
   if (!plan->epi_ready[act]) {
@@ -539,8 +574,9 @@ gemm_status_t gemm_run_host(int64_t M, int64_t N, int64_t K, const void* A_host,
   if (st != GEMM_OK) return st;
   if (!A_host || !B_host || !C_host || !dA || !dB || !dC) return GEMM_ERR_INVALID_ARG;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (cudaMemcpyAsync(dA, A_host, (size_t)(M * K * 2), cudaMemcpyHostToDevice, s) != cudaSuccess ||
-      cudaMemcpyAsync(dB, B_host, (size_t)(N * K * 2), cudaMemcpyHostToDevice, s) != cudaSuccess) {
+  const int64_t ib = in_bytes(dtype);
+  if (cudaMemcpyAsync(dA, A_host, (size_t)(M * K * ib), cudaMemcpyHostToDevice, s) != cudaSuccess ||
+      cudaMemcpyAsync(dB, B_host, (size_t)(N * K * ib), cudaMemcpyHostToDevice, s) != cudaSuccess) {
     cudaGetLastError();
     return GEMM_ERR_CUDA;
   }

@@ -53,6 +53,12 @@ struct KParams {
   int32_t act;           // EPI_ACT_*
   // operand layouts (steps 7-9): bit 0 = A stored K x M (M-major), bit 1 = B stored K x N (N-major)
   uint32_t layout;
+  // element kind of A and B (steps 7-9): 0 = fp16 / bf16 (kind::f16), 1 = 8-bit float (kind::f8f6f4)
+  int32_t mma_kind;
+  int32_t bk;            // K elements per 128-byte stage row: 64 (16-bit) or 128 (8-bit)
+  // fused-epilogue dequantisation: acc * scale_a[row] * scale_b[col] before the bias
+  const float* scale_a;  // M fp32 values, or null
+  const float* scale_b;  // N fp32 values, or null
 };
 
 constexpr uint32_t LAYOUT_A_MN = 1u;
@@ -95,6 +101,15 @@ __device__ __forceinline__ void apply_epilogue(uint32_t* v, const KParams& p, in
   float x[n];
 #pragma unroll
   for (int j = 0; j < n; ++j) x[j] = __uint_as_float(v[j]);
+  if (p.scale_a != nullptr) {
+    const float sa = (row < p.M) ? __ldg(p.scale_a + row) : 0.f;
+#pragma unroll
+    for (int j = 0; j < n; ++j) x[j] *= sa;
+  }
+  if (p.scale_b != nullptr) {
+#pragma unroll
+    for (int j = 0; j < n; ++j) x[j] *= (col0 + j < p.N) ? __ldg(p.scale_b + col0 + j) : 0.f;
+  }
   if (p.bias != nullptr) {
 #pragma unroll
     for (int j = 0; j < n; ++j) x[j] += (col0 + j < p.N) ? __ldg(p.bias + col0 + j) : 0.f;

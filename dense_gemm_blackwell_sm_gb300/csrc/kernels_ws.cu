@@ -45,7 +45,6 @@ enum SchedWs { SCHED_STATIC = 0, SCHED_ATOMIC = 1, SCHED_CLC = 2 };
 
 constexpr int WS_THREADS = 256;
 constexpr int WS_BN = 256;          // tile columns (MMA N)
-constexpr int WS_BK = 64;           // K block (one 128-byte swizzle row of 16-bit values)
 constexpr uint32_t WS_A_BYTES = 128u * 128u;  // 128 rows x 128 B
 constexpr int WS_RING = 4;          // depth of the tile-id ring
 constexpr int WS_STAGING = 4 * 2 * 4096;      // 4 writeback warps x 2 buffers x 32 rows x 128 B
@@ -135,7 +134,10 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
   const uint32_t tmem = *tmem_slot;
   const uint32_t peer_abort = (CG == 2) ? mapa_shared(smem_u32((const void*)abort_flag), rank ^ 1u) : 0u;
   const WaitCtl w{abort_flag, p.status, p.timeout_ns, peer_abort};
-  const int32_t KB = (p.K + WS_BK - 1) / WS_BK;
+  // K elements per stage: one 128-byte swizzle row of A / B (64 x 16-bit or 128 x 8-bit)
+  const int32_t BKE = (p.bk > 0) ? p.bk : 64;
+  const int32_t KB = (p.K + BKE - 1) / BKE;
+  const bool f8 = (p.mma_kind == 1);
   const bool a_mn = (p.layout & LAYOUT_A_MN) != 0u;
   const bool b_mn = (p.layout & LAYOUT_B_MN) != 0u;
 
@@ -230,15 +232,15 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
 #pragma unroll
               for (int h = 0; h < 2; ++h) {
                 if constexpr (CG == 1) {
-                  tma_load_2d(smem_u32(dst + h * 8192), &tmA, fb, row + 64 * h, kb * WS_BK);
+                  tma_load_2d(smem_u32(dst + h * 8192), &tmA, fb, row + 64 * h, kb * BKE);
                 } else {
-                  tma_load_2d_pair(smem_u32(dst + h * 8192), &tmA, mapa_shared(fb, 0), row + 64 * h, kb * WS_BK);
+                  tma_load_2d_pair(smem_u32(dst + h * 8192), &tmA, mapa_shared(fb, 0), row + 64 * h, kb * BKE);
                 }
               }
             } else if constexpr (CG == 1) {
-              tma_load_2d(smem_u32(dst), &tmA, fb, kb * WS_BK, row);
+              tma_load_2d(smem_u32(dst), &tmA, fb, kb * BKE, row);
             } else {
-              tma_load_2d_pair(smem_u32(dst), &tmA, mapa_shared(fb, 0), kb * WS_BK, row);
+              tma_load_2d_pair(smem_u32(dst), &tmA, mapa_shared(fb, 0), kb * BKE, row);
             }
           }
           uint8_t* bdst = st + NCONS * WS_A_BYTES;
@@ -248,15 +250,15 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
 #pragma unroll
             for (int h = 0; h < Cfg::B_ROWS / 64; ++h) {
               if constexpr (CG == 1) {
-                tma_load_2d(smem_u32(bdst + h * 8192), &tmB, fb, n_cta + 64 * h, kb * WS_BK);
+                tma_load_2d(smem_u32(bdst + h * 8192), &tmB, fb, n_cta + 64 * h, kb * BKE);
               } else {
-                tma_load_2d_pair(smem_u32(bdst + h * 8192), &tmB, mapa_shared(fb, 0), n_cta + 64 * h, kb * WS_BK);
+                tma_load_2d_pair(smem_u32(bdst + h * 8192), &tmB, mapa_shared(fb, 0), n_cta + 64 * h, kb * BKE);
               }
             }
           } else if constexpr (CG == 1) {
-            tma_load_2d(smem_u32(bdst), &tmB, fb, kb * WS_BK, n_cta);
+            tma_load_2d(smem_u32(bdst), &tmB, fb, kb * BKE, n_cta);
           } else {
-            tma_load_2d_pair(smem_u32(bdst), &tmB, mapa_shared(fb, 0), kb * WS_BK, n_cta);
+            tma_load_2d_pair(smem_u32(bdst), &tmB, mapa_shared(fb, 0), kb * BKE, n_cta);
           }
           if (++stage == (uint32_t)S) { stage = 0; sphase ^= 1u; }
         }
@@ -290,9 +292,16 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
           const uint64_t ad = a_mn ? sdesc_mn_sw128(sa, 8192) : sdesc_k_sw128(sa);
           const uint64_t bd = b_mn ? sdesc_mn_sw128(sb, 8192) : sdesc_k_sw128(sb);
           const uint64_t astep = a_mn ? 128 : 2, bstep = b_mn ? 128 : 2;
+          // four MMAs per stage, each over 32 bytes of K (16 x 16-bit or 32 x 8-bit)
+          if (f8) {
 #pragma unroll
-          for (int k = 0; k < WS_BK / 16; ++k)
-            mma_f16<CG>(d, ad + astep * k, bd + bstep * k, p.idesc, (kb | k) != 0);
+            for (int k = 0; k < 4; ++k)
+              mma_f8f6f4<CG>(d, ad + astep * k, bd + bstep * k, p.idesc, (kb | k) != 0);
+          } else {
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              mma_f16<CG>(d, ad + astep * k, bd + bstep * k, p.idesc, (kb | k) != 0);
+          }
           if constexpr (CG == 1) {
             mma_commit(smem_u32(empty + stage));
           } else {

@@ -15,8 +15,11 @@ LIB_PATH = os.path.join(HERE, "libdgbgemm.so")
 
 # gemm_dtype_t
 F16_F32, F16_BF16, BF16_F32, BF16_BF16 = 0, 1, 2, 3
+E4M3_F32, E4M3_BF16, E5M2_F32, E5M2_BF16 = 4, 5, 6, 7
 DTYPES = {("f16", "f32"): F16_F32, ("f16", "bf16"): F16_BF16,
-          ("bf16", "f32"): BF16_F32, ("bf16", "bf16"): BF16_BF16}
+          ("bf16", "f32"): BF16_F32, ("bf16", "bf16"): BF16_BF16,
+          ("e4m3", "f32"): E4M3_F32, ("e4m3", "bf16"): E4M3_BF16,
+          ("e5m2", "f32"): E5M2_F32, ("e5m2", "bf16"): E5M2_BF16}
 
 # gemm_status_t
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED_SHAPE, ERR_MISALIGNED, ERR_UNSUPPORTED_DTYPE = 0, 1, 2, 3, 4
@@ -64,7 +67,7 @@ class PlanInfo(ctypes.Structure):
 
 class Epilogue(ctypes.Structure):
     _fields_ = [("bias", ctypes.c_void_p), ("residual", ctypes.c_void_p), ("activation", ctypes.c_int32),
-                ("reserved", ctypes.c_int32 * 3)]
+                ("reserved", ctypes.c_int32 * 3), ("scale_a", ctypes.c_void_p), ("scale_b", ctypes.c_void_p)]
 
 
 _lib = None
@@ -153,10 +156,14 @@ class Plan:
         _check(self.run_ptr(a.data_ptr(), b.data_ptr(), c.data_ptr(), _stream_ptr(stream)), "gemm_plan_run")
         return c
 
-    def run_epilogue(self, a, b, c, bias=None, residual=None, act: int = ACT_NONE, stream=None):
-        """C = act(a @ b.T + bias) + residual in one kernel (variants 7-9).
-        bias: fp32 CUDA tensor of N values; residual: (M, N) CUDA tensor of C's type."""
+    def run_epilogue(self, a, b, c, bias=None, residual=None, act: int = ACT_NONE, stream=None,
+                     scale_a=None, scale_b=None):
+        """C = act(scale_a[:, None] * scale_b[None, :] * (a @ b.T) + bias) + residual in one
+        kernel (variants 7-9).  bias, scale_b: fp32 CUDA tensors of N values; scale_a: M values;
+        residual: (M, N) CUDA tensor of C's type."""
         e = Epilogue()
+        e.scale_a = None if scale_a is None else scale_a.data_ptr()
+        e.scale_b = None if scale_b is None else scale_b.data_ptr()
         e.bias = None if bias is None else bias.data_ptr()
         e.residual = None if residual is None else residual.data_ptr()
         e.activation = int(act)
@@ -191,7 +198,8 @@ class Plan:
 
 def dtype_code(in_dtype, out_dtype) -> int:
     import torch
-    names = {torch.float16: "f16", torch.bfloat16: "bf16", torch.float32: "f32"}
+    names = {torch.float16: "f16", torch.bfloat16: "bf16", torch.float32: "f32",
+             torch.float8_e4m3fn: "e4m3", torch.float8_e5m2: "e5m2"}
     i = names.get(in_dtype, in_dtype)
     o = names.get(out_dtype, out_dtype)
     if (i, o) not in DTYPES:
@@ -227,11 +235,13 @@ def _stored(x):
 
 
 def matmul(a, b, out_dtype=None, out=None, stream=None):
-    """C = a @ b.T for CUDA tensors a (M x K) and b (N x K), fp16 or bf16.
+    """C = a @ b.T for CUDA tensors a (M x K) and b (N x K), fp16, bf16,
+    float8_e4m3fn or float8_e5m2.
 
-    ``out_dtype`` is torch.float32 (default) or torch.bfloat16.  An operand that
-    is the transpose of a contiguous tensor (``x.t()``) is read in place as an
-    MN-major operand by the warp-specialised kernels.
+    ``out_dtype`` is torch.float32 (default) or torch.bfloat16.  A 16-bit operand
+    that is the transpose of a contiguous tensor (``x.t()``) is read in place as
+    an MN-major operand by the warp-specialised kernels; 8-bit operands are
+    K-major only and are made contiguous first.
     """
     import torch
     if not (a.is_cuda and b.is_cuda):
@@ -251,7 +261,7 @@ def matmul(a, b, out_dtype=None, out=None, stream=None):
     elif out.shape != (M, N) or not out.is_contiguous() or out.dtype != out_dtype:
         raise ValueError("out must be a contiguous (M, N) tensor of out_dtype")
     layout = (LAYOUT_A_MN if a_mn else 0) | (LAYOUT_B_MN if b_mn else 0)
-    if layout and ((a_mn and M % 8) or (b_mn and N % 8)):
+    if layout and ((a_mn and M % 8) or (b_mn and N % 8) or a.element_size() == 1):
         a_s, b_s, layout = a.contiguous(), b.contiguous(), 0
     if layout == 0:
         _check(gemm_run(M, N, K, a_s.data_ptr(), b_s.data_ptr(), out.data_ptr(), code, _stream_ptr(stream)),

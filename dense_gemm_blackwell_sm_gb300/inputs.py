@@ -9,7 +9,8 @@ Recipe (the pages name no RNG, so this is the plainest reading):
   * A is drawn first, then B, both in fp32, from that one generator;
   * uniform[-1, 1] is ``2 * rand - 1``; normal(0, s) is ``randn * s``;
     "normal(0,1)/sqrt(K)" is ``randn * (1/sqrt(K))``;
-  * the fp32 draws are rounded to fp16 / bf16 by ``Tensor.to`` (round to nearest even);
+  * the fp32 draws are rounded to fp16 / bf16 / fp8 (E4M3, E5M2) by ``Tensor.to``
+    (round to nearest even);
   * for the decode GEMV, "A" is the activation row block x (M x K) and "B" is
     the weight (N x K).
 """
@@ -23,8 +24,11 @@ import torch
 F16 = "f16"
 BF16 = "bf16"
 F32 = "f32"
+E4M3 = "e4m3"
+E5M2 = "e5m2"
 
-_TORCH = {F16: torch.float16, BF16: torch.bfloat16, F32: torch.float32}
+_TORCH = {F16: torch.float16, BF16: torch.bfloat16, F32: torch.float32,
+          E4M3: torch.float8_e4m3fn, E5M2: torch.float8_e5m2}
 
 
 @dataclasses.dataclass(frozen=True)
@@ -84,7 +88,7 @@ def _draw(gen: torch.Generator, rows: int, cols: int, dist: tuple, K: int) -> to
 
 def make_operands(M: int, N: int, K: int, in_dtype: str, dist_a: tuple, dist_b: tuple, seed: int,
                   rows_a: int | None = None):
-    """Seeded (A, B) as CPU fp16/bf16 tensors: A is M x K, B is N x K (A drawn first)."""
+    """Seeded (A, B) as CPU fp16 / bf16 / fp8 tensors: A is M x K, B is N x K (A drawn first)."""
     gen = torch.Generator().manual_seed(int(seed))
     a = _draw(gen, M if rows_a is None else rows_a, K, dist_a, K).to(_TORCH[in_dtype])
     b = _draw(gen, N, K, dist_b, K).to(_TORCH[in_dtype])

@@ -2,7 +2,7 @@
  * gemm.h -- C ABI of the GB300 (sm_103a) dense GEMM library, libdgbgemm.so.
  *
  * Computes C = A * B^T on one GPU:
- *   A  M x K, row-major (K-major), fp16 or bf16
+ *   A  M x K, row-major (K-major), fp16, bf16, or 8-bit float (E4M3 / E5M2)
  *   B  N x K, row-major (K-major), same type as A
  *   C  M x N, row-major (leading dimension N), fp32 or bf16
  * with fp32 accumulation in Tensor Memory.  This is the tiled GEMM of
@@ -47,13 +47,17 @@ typedef enum {
   GEMM_F16_F32 = 0,   /* fp16 in, fp32 out */
   GEMM_F16_BF16 = 1,  /* fp16 in, bf16 out (round to nearest even) */
   GEMM_BF16_F32 = 2,  /* bf16 in, fp32 out */
-  GEMM_BF16_BF16 = 3  /* bf16 in, bf16 out (round to nearest even) */
+  GEMM_BF16_BF16 = 3, /* bf16 in, bf16 out (round to nearest even) */
+  GEMM_E4M3_F32 = 4,  /* 8-bit float E4M3 (OCP FP8) in, fp32 out; variants 7-9, K-major */
+  GEMM_E4M3_BF16 = 5, /* E4M3 in, bf16 out */
+  GEMM_E5M2_F32 = 6,  /* 8-bit float E5M2 in, fp32 out */
+  GEMM_E5M2_BF16 = 7  /* E5M2 in, bf16 out */
 } gemm_dtype_t;
 
 typedef enum {
   GEMM_OK = 0,
   GEMM_ERR_INVALID_ARG = 1,       /* NULL pointer, dimension < 1 or >= 2^31, bad option */
-  GEMM_ERR_UNSUPPORTED_SHAPE = 2, /* K % 8 != 0, or a shape the requested variant cannot do */
+  GEMM_ERR_UNSUPPORTED_SHAPE = 2, /* K * sizeof(input) % 16 != 0, or a shape the requested variant cannot do */
   GEMM_ERR_MISALIGNED = 3,        /* A, B or C not 16-byte aligned */
   GEMM_ERR_UNSUPPORTED_DTYPE = 4, /* dtype outside gemm_dtype_t */
   GEMM_ERR_ARCH = 5,              /* current device is not compute capability 10.3 */
@@ -158,8 +162,9 @@ typedef enum {
   GEMM_ACT_GELU_ERF = 4   /* 0.5 x (1 + erf(x / sqrt(2))) */
 } gemm_activation_t;
 
-/* Fused epilogue of the writeback: C[i][j] = act(sum_k A[i][k] B[j][k] + bias[j])
- * + residual[i][j], computed in fp32 and rounded once to C's type. */
+/* Fused epilogue of the writeback:
+ *   C[i][j] = act(scale_a[i] * scale_b[j] * sum_k A[i][k] B[j][k] + bias[j]) + residual[i][j],
+ * computed in fp32 and rounded once to C's type (absent terms are skipped). */
 typedef struct {
   const float* bias;    /* N fp32 values (device, 4-byte aligned), or NULL */
   const void* residual; /* M x N device array of C's type, row-major, 16-byte aligned, or
@@ -167,6 +172,9 @@ typedef struct {
                            overwritten) */
   int32_t activation;   /* gemm_activation_t */
   int32_t reserved[3];
+  const float* scale_a; /* M fp32 values multiplying row i of the product before the bias
+                           (dequantisation of 8-bit inputs), or NULL */
+  const float* scale_b; /* N fp32 values multiplying column j, or NULL */
 } gemm_epilogue_t;
 
 /* gemm_plan_run with the fused epilogue.  Needs a plan of variant 7, 8 or 9
@@ -205,7 +213,8 @@ GEMM_API gemm_status_t gemm_run_host(int64_t M, int64_t N, int64_t K, const void
  * the array and clears it on `stream` before its kernel starts, so calls that
  * overlap on the GPU (different streams, or different threads) race and must
  * be serialised by the caller.  Needs N * sizeof(C element) % 16 == 0 besides
- * the usual preconditions.  Asynchronous on `stream`; a device-side wait that
+ * the usual preconditions, and 16-bit inputs (dtypes 0-3; the 8-bit ones
+ * return GEMM_ERR_UNSUPPORTED_DTYPE).  Asynchronous on `stream`; a device-side wait that
  * times out leaves C undefined and is not reported by this entry point. */
 GEMM_API gemm_status_t gemm_run_noalloc(int64_t M, int64_t N, int64_t K, const void* A, const void* B,
                                         void* C, gemm_dtype_t dtype, gemm_stream_t stream);

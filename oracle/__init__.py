@@ -32,6 +32,8 @@ _LIB = os.path.join(_HERE, "liboracle.so")
 
 IN_F16 = 0
 IN_BF16 = 1
+IN_E4M3 = 2
+IN_E5M2 = 3
 
 _lib = None
 
@@ -62,6 +64,12 @@ def _load():
         lib.oracle_gemm_f64.restype = ctypes.c_int
         lib.oracle_widen.argtypes = [ctypes.c_uint16, ctypes.c_int]
         lib.oracle_widen.restype = ctypes.c_double
+        lib.oracle_gemm8_rows_f64.argtypes = [i64, i64, i64, p, p, ctypes.c_int, p, i64, p, p, ctypes.c_int]
+        lib.oracle_gemm8_rows_f64.restype = ctypes.c_int
+        lib.oracle_widen8.argtypes = [ctypes.c_uint8, ctypes.c_int]
+        lib.oracle_widen8.restype = ctypes.c_double
+        lib.oracle_scale_f64.argtypes = [i64, i64, p, p, p]
+        lib.oracle_scale_f64.restype = ctypes.c_int
         lib.oracle_epilogue_f64.argtypes = [i64, i64, p, p, p, ctypes.c_int, ctypes.c_int]
         lib.oracle_epilogue_f64.restype = ctypes.c_int
         lib.oracle_activation.argtypes = [ctypes.c_double, ctypes.c_int]
@@ -87,11 +95,30 @@ def _bits(x) -> np.ndarray:
 
 
 def kind_of(x) -> int:
-    """IN_F16 or IN_BF16 for a torch tensor / numpy array."""
+    """IN_F16, IN_BF16, IN_E4M3 or IN_E5M2 for a torch tensor / numpy array."""
     if isinstance(x, np.ndarray):
         return IN_F16
     import torch
+    if x.dtype == torch.float8_e4m3fn:
+        return IN_E4M3
+    if x.dtype == torch.float8_e5m2:
+        return IN_E5M2
     return IN_BF16 if x.dtype == torch.bfloat16 else IN_F16
+
+
+def _bytes8(x) -> np.ndarray:
+    """Raw 8-bit patterns of a 2-D fp8 array (torch tensor or uint8 ndarray)."""
+    if isinstance(x, np.ndarray):
+        if x.dtype != np.uint8:
+            raise TypeError("8-bit operands must be uint8 patterns")
+        return np.ascontiguousarray(x)
+    import torch
+    return np.ascontiguousarray(x.detach().cpu().contiguous().view(torch.uint8).numpy())
+
+
+def widen8(bits: int, kind: int) -> float:
+    """Exact value of one 8-bit pattern (kind IN_E4M3 or IN_E5M2)."""
+    return float(_load().oracle_widen8(int(bits) & 0xFF, int(kind)))
 
 
 def max_threads() -> int:
@@ -103,9 +130,29 @@ def widen(bits: int, kind: int) -> float:
     return float(_load().oracle_widen(int(bits) & 0xFFFF, int(kind)))
 
 
+def _gemm8(a, b, kind, rows, nthreads):
+    A, B = _bytes8(a), _bytes8(b)
+    M, K = A.shape
+    N, K2 = B.shape
+    if K != K2:
+        raise ValueError("inner dimensions differ")
+    r = None if rows is None else np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    n = M if r is None else len(r)
+    C = np.empty((n, N), dtype=np.float64)
+    S = np.empty((n, N), dtype=np.float64)
+    rc = _load().oracle_gemm8_rows_f64(M, N, K, A.ctypes.data, B.ctypes.data, kind,
+                                       None if r is None else r.ctypes.data, n, C.ctypes.data,
+                                       S.ctypes.data, int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle_gemm8_rows_f64 rejected its arguments")
+    return C, S
+
+
 def gemm(a, b, kind: int | None = None, nthreads: int = 0):
     """Full fp64 C = A * B^T and S = sum_k |a_ik b_jk|; returns (C, S) as float64 arrays."""
     kind = kind_of(a) if kind is None else kind
+    if kind in (IN_E4M3, IN_E5M2):
+        return _gemm8(a, b, kind, None, nthreads)
     A, B = _bits(a), _bits(b)
     M, K = A.shape
     N, K2 = B.shape
@@ -123,6 +170,8 @@ def gemm(a, b, kind: int | None = None, nthreads: int = 0):
 def gemm_rows(a, b, rows, kind: int | None = None, nthreads: int = 0):
     """Rows ``rows`` of C and S only (len(rows) x N each)."""
     kind = kind_of(a) if kind is None else kind
+    if kind in (IN_E4M3, IN_E5M2):
+        return _gemm8(a, b, kind, rows, nthreads)
     A, B = _bits(a), _bits(b)
     M, K = A.shape
     N, K2 = B.shape
@@ -147,12 +196,41 @@ def activation(x: float, act: int) -> float:
     return float(_load().oracle_activation(float(x), int(act)))
 
 
-def epilogue(C, bias=None, residual=None, act: int = ACT_NONE):
-    """act(C + bias[col]) + residual, in fp64, on a copy of C (M x N).
+def _f32_vector(v, n: int, what: str):
+    if v is None:
+        return None
+    if hasattr(v, "detach"):
+        v = v.detach().cpu().numpy()
+    a = np.ascontiguousarray(np.asarray(v, dtype=np.float32))
+    if a.shape != (n,):
+        raise ValueError("%s must hold %d values" % (what, n))
+    return a
 
-    bias: N fp32 values (array or tensor) or None; residual: M x N fp32 /
-    bf16 / fp16 (numpy float32 array, or torch tensor) or None."""
+
+def scale(C, scale_a=None, scale_b=None):
+    """C[i][j] * scale_a[i] * scale_b[j] in fp64, on a copy of C (M x N); the
+    scales are fp32 vectors (array or tensor) of M and N values, or None."""
     out = np.ascontiguousarray(np.array(C, dtype=np.float64))
+    M, N = out.shape
+    sa = _f32_vector(scale_a, M, "scale_a")
+    sb = _f32_vector(scale_b, N, "scale_b")
+    rc = _load().oracle_scale_f64(M, N, out.ctypes.data, None if sa is None else sa.ctypes.data,
+                                  None if sb is None else sb.ctypes.data)
+    if rc != 0:
+        raise ValueError("oracle_scale_f64 rejected its arguments")
+    return out
+
+
+def epilogue(C, bias=None, residual=None, act: int = ACT_NONE, scale_a=None, scale_b=None):
+    """act(scale_a[row] * scale_b[col] * C + bias[col]) + residual, in fp64, on a
+    copy of C (M x N).
+
+    bias, scale_b: N fp32 values (array or tensor) or None; scale_a: M fp32
+    values or None; residual: M x N fp32 / bf16 / fp16 (numpy float32 array, or
+    torch tensor) or None."""
+    out = np.ascontiguousarray(np.array(C, dtype=np.float64))
+    if scale_a is not None or scale_b is not None:
+        out = scale(out, scale_a, scale_b)
     M, N = out.shape
     b = None
     if bias is not None:

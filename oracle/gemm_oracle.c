@@ -181,6 +181,22 @@ static double oracle_act(double x, int act) {
 
 double oracle_activation(double x, int act) { return oracle_act(x, act); }
 
+/*
+ * Dequantisation scales of the fused epilogue: C[i][j] *= scale_a[i] * scale_b[j]
+ * (either may be NULL).  The product of an fp64 value and two fp32 values.
+ */
+int oracle_scale_f64(int64_t M, int64_t N, double* C, const float* scale_a, const float* scale_b) {
+    if (M < 0 || N < 0) return -1;
+    for (int64_t i = 0; i < M; ++i)
+        for (int64_t j = 0; j < N; ++j) {
+            double x = C[i * N + j];
+            if (scale_a) x *= (double)scale_a[i];
+            if (scale_b) x *= (double)scale_b[j];
+            C[i * N + j] = x;
+        }
+    return 0;
+}
+
 int oracle_epilogue_f64(int64_t M, int64_t N, double* C, const float* bias, const void* residual,
                         int residual_kind, int act) {
     if (M < 0 || N < 0 || act < 0 || act > 4) return -1;
@@ -200,6 +216,73 @@ int oracle_epilogue_f64(int64_t M, int64_t N, double* C, const float* bias, cons
                 }
             }
             C[i * N + j] = x;
+        }
+    }
+    return 0;
+}
+
+/*
+ * 8-bit floating point inputs (the low-precision GEMM).  OCP FP8 formats:
+ *   E4M3: sign bit 7, 4-bit exponent (bias 7), 3-bit fraction; exponent 0 is
+ *         subnormal (f * 2^-9); S.1111.111 is NaN; there is no infinity.
+ *   E5M2: sign bit 7, 5-bit exponent (bias 15), 2-bit fraction; exponent 0 is
+ *         subnormal (f * 2^-16); exponent 31 is infinity (f = 0) or NaN.
+ * Products of two such values carry at most 8 significant bits: exact in fp64.
+ */
+#define ORACLE_IN_E4M3 2
+#define ORACLE_IN_E5M2 3
+
+static double widen_e4m3(uint8_t h) {
+    int sign = (h >> 7) & 1, e = (h >> 3) & 0xF, f = h & 0x7;
+    double v;
+    if (e == 0) v = ldexp((double)f, -9);
+    else if (e == 15 && f == 7) v = NAN;
+    else v = ldexp((double)(8 + f), e - 10);
+    return sign ? -v : v;
+}
+
+static double widen_e5m2(uint8_t h) {
+    int sign = (h >> 7) & 1, e = (h >> 2) & 0x1F, f = h & 0x3;
+    double v;
+    if (e == 0) v = ldexp((double)f, -16);
+    else if (e == 31) v = (f == 0) ? INFINITY : NAN;
+    else v = ldexp((double)(4 + f), e - 17);
+    return sign ? -v : v;
+}
+
+double oracle_widen8(uint8_t bits, int in_kind) {
+    return in_kind == ORACLE_IN_E5M2 ? widen_e5m2(bits) : widen_e4m3(bits);
+}
+
+int oracle_gemm8_rows_f64(int64_t M, int64_t N, int64_t K,
+                          const uint8_t* A, const uint8_t* B, int in_kind,
+                          const int64_t* rows, int64_t nrows,
+                          double* C, double* S, int nthreads) {
+    if (M < 0 || N < 0 || K < 0 || nrows < 0) return -1;
+    if (in_kind != ORACLE_IN_E4M3 && in_kind != ORACLE_IN_E5M2) return -1;
+    if (rows == NULL && nrows != M) return -1;
+    if (rows != NULL) {
+        for (int64_t r = 0; r < nrows; ++r)
+            if (rows[r] < 0 || rows[r] >= M) return -1;
+    }
+    double tab[256];
+    for (int b = 0; b < 256; ++b) tab[b] = oracle_widen8((uint8_t)b, in_kind);
+    set_threads(nthreads);
+    int64_t r;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (r = 0; r < nrows; ++r) {
+        int64_t i = rows ? rows[r] : r;
+        const uint8_t* a = A + i * K;
+        for (int64_t j = 0; j < N; ++j) {
+            const uint8_t* b = B + j * K;
+            double acc = 0.0, sabs = 0.0;
+            for (int64_t k = 0; k < K; ++k) {
+                double p = tab[a[k]] * tab[b[k]];   /* exact */
+                acc += p;
+                sabs += fabs(p);
+            }
+            C[r * N + j] = acc;
+            if (S) S[r * N + j] = sabs;
         }
     }
     return 0;

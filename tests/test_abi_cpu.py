@@ -63,8 +63,31 @@ def test_plan_rejects_bad_sizes_without_a_device(lib):
     assert _plan_status(lib, 16, 16, 0, 0) == gemm.ERR_INVALID_ARG
     assert _plan_status(lib, 1 << 31, 16, 16, 0) == gemm.ERR_INVALID_ARG
     assert _plan_status(lib, 16, 16, 12, 0) == gemm.ERR_UNSUPPORTED_SHAPE   # K % 8 != 0
-    assert _plan_status(lib, 16, 16, 16, 7) == gemm.ERR_UNSUPPORTED_DTYPE
+    assert _plan_status(lib, 16, 16, 16, 8) == gemm.ERR_UNSUPPORTED_DTYPE
     assert _plan_status(lib, 16, 16, 16, -1) == gemm.ERR_UNSUPPORTED_DTYPE
+
+
+def test_fp8_row_pitch_rule(lib):
+    # 8-bit inputs: a row of A / B is K bytes, so K must be a multiple of 16 (not 8)
+    for dt in (gemm.E4M3_F32, gemm.E4M3_BF16, gemm.E5M2_F32, gemm.E5M2_BF16):
+        assert _plan_status(lib, 64, 64, 24, dt) == gemm.ERR_UNSUPPORTED_SHAPE
+        assert _plan_status(lib, 64, 64, 8, dt) == gemm.ERR_UNSUPPORTED_SHAPE
+    assert _plan_status(lib, 64, 64, 24, gemm.BF16_BF16) != gemm.ERR_UNSUPPORTED_SHAPE
+    # 8-bit inputs run on variants 7-9 only, K-major only
+    assert _plan_status(lib, 64, 64, 64, gemm.E4M3_F32, gemm.make_opts(variant=gemm.S3)) == \
+        gemm.ERR_UNSUPPORTED_SHAPE
+    assert _plan_status(lib, 64, 64, 64, gemm.E4M3_F32, gemm.make_opts(variant=gemm.GEMV)) == \
+        gemm.ERR_UNSUPPORTED_SHAPE
+    assert _plan_status(lib, 64, 64, 64, gemm.E5M2_BF16,
+                        gemm.make_opts(variant=gemm.S8, layout=gemm.LAYOUT_A_MN)) == gemm.ERR_UNSUPPORTED_SHAPE
+    assert gemm.dtype_code("e4m3", "f32") == gemm.E4M3_F32
+    assert gemm.dtype_code(torch.float8_e5m2, torch.bfloat16) == gemm.E5M2_BF16
+
+
+def test_epilogue_struct_layout_matches_the_header():
+    import ctypes as ct
+    assert ct.sizeof(gemm.Epilogue) == 48
+    assert gemm.Epilogue.scale_a.offset == 32 and gemm.Epilogue.scale_b.offset == 40
 
 
 def test_plan_rejects_bad_options(lib):
