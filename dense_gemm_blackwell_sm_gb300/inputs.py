@@ -37,7 +37,7 @@ class Workload:
     M: int
     N: int
     K: int
-    in_dtype: str          # "f16" | "bf16"
+    in_dtype: str          # "f16" | "bf16" | "e4m3" | "e5m2"
     out_dtype: str         # "f32" | "bf16"
     dist_a: tuple          # ("uniform",) | ("normal", sigma) | ("normal_rsqrt_k",)
     dist_b: tuple
@@ -49,7 +49,7 @@ class Workload:
 
     @property
     def algorithmic_bytes(self) -> int:
-        ib = 2
+        ib = 1 if self.in_dtype in (E4M3, E5M2) else 2
         ob = 4 if self.out_dtype == F32 else 2
         return ib * (self.M * self.K + self.N * self.K) + ob * self.M * self.N
 
@@ -66,6 +66,7 @@ WORKLOADS = {
     "large_8192_bf16_bf16": Workload("large_8192_bf16_bf16", 8192, 8192, 8192, BF16, BF16, N002, N002, 3),
     "llm_proj_8192x14336x4096_bf16_bf16": Workload("llm_proj_8192x14336x4096_bf16_bf16", 8192, 14336, 4096,
                                                    BF16, BF16, N002, N002, 3),
+    "fp8_8192_e4m3_bf16": Workload("fp8_8192_e4m3_bf16", 8192, 8192, 8192, E4M3, BF16, U, U, 5),
     "gemv_m1_n4096_k4096_bf16": Workload("gemv_m1_n4096_k4096_bf16", 1, 4096, 4096, BF16, BF16, U, N002, 4),
     "gemv_m8_n4096_k4096_bf16": Workload("gemv_m8_n4096_k4096_bf16", 8, 4096, 4096, BF16, BF16, U, N002, 4),
     "gemv_m1_n14336_k4096_bf16": Workload("gemv_m1_n14336_k4096_bf16", 1, 14336, 4096, BF16, BF16, U, N002, 4),

@@ -355,6 +355,7 @@ def test_workload_table_shapes():
     assert w["single_tile_128x128x64_f16_f32"].seed == 0
     assert w["gemv_m1_n4096_k4096_bf16"].M == 1
     assert w["square_4096_f16_f32"].algorithmic_bytes == 2 * 2 * 4096 * 4096 + 4 * 4096 * 4096
+    assert w["fp8_8192_e4m3_bf16"].algorithmic_bytes == 2 * 8192 * 8192 + 2 * 8192 * 8192
 
 
 def test_parity_diagnostic_flags_a_lost_k_block():

@@ -23,7 +23,8 @@ DEV = "cuda:0"
 FULL = ["single_tile_128x128x64_f16_f32", "kloop_1024x1024x4096_bf16_bf16",
         "gemv_m1_n4096_k4096_bf16", "gemv_m8_n4096_k4096_bf16",
         "gemv_m1_n14336_k4096_bf16", "gemv_m8_n14336_k4096_bf16"]
-SAMPLED = ["square_4096_f16_f32", "large_8192_bf16_bf16", "llm_proj_8192x14336x4096_bf16_bf16"]
+SAMPLED = ["square_4096_f16_f32", "large_8192_bf16_bf16", "llm_proj_8192x14336x4096_bf16_bf16",
+           "fp8_8192_e4m3_bf16"]
 
 
 @pytest.fixture(scope="module", autouse=True)
