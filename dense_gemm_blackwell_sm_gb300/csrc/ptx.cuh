@@ -153,6 +153,15 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 }
 
 // ---------------------------------------------------------------------------
+// Plain bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned)
+// from global to this CTA's shared memory, counted on `bar`.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
 // TMA (cp.async.bulk.tensor)
 
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* m) {
@@ -380,6 +389,28 @@ __device__ __forceinline__ void mma_f8f6f4(uint32_t d_tmem, uint64_t adesc, uint
         : "memory");
 }
 
+// D[tmem] (+)= (A[smem] x scale_A) * (B[smem] x scale_B)^T with one UE8M0 scale
+// per 32 K-elements of every row of A and of B (MX block scaling).  The scales
+// live in TMEM at sfa_tmem / sfb_tmem; the instruction descriptor picks which
+// byte of each 32-bit TMEM word holds this MMA's scales.  K = 32 per instruction.
+__device__ __forceinline__ void mma_mxf8f6f4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                             uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
+      ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// Copy 32 rows x 16 bytes of shared memory (described by `sdesc`) into TMEM
+// columns taddr..taddr+3 of lanes 0-31, replicated into each of the four
+// 32-lane quarters.  Asynchronous; ordered before later tcgen05.mma issued by
+// the same thread.
+__device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
 // one arrival on `bar` once every tcgen05 op this thread issued so far is done
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
@@ -467,6 +498,16 @@ __device__ __forceinline__ uint64_t sdesc_mn_sw128(uint32_t saddr, uint32_t mn_g
          | ((uint64_t)(1024u >> 4) << 32)                       // stride byte offset: 8 K-rows x 128 B
          | ((uint64_t)1u << 46)
          | ((uint64_t)2u << 61);
+}
+
+// Shared-memory descriptor of an unswizzled block of rows of 16 bytes each,
+// stored one after another: 8-row core matrices of 128 B, consecutive core
+// matrices 128 B apart (stride byte offset).  Base 16-byte aligned.
+__device__ __forceinline__ uint64_t sdesc_rows16(uint32_t saddr) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4)
+         | ((uint64_t)(128u >> 4) << 16)   // leading byte offset (one 16-byte column: unused)
+         | ((uint64_t)(128u >> 4) << 32)   // stride byte offset: 8 rows x 16 B
+         | ((uint64_t)1u << 46);           // descriptor version; layout 0 = no swizzle
 }
 
 // byte offset of 16-byte chunk `c` (0..7) of row `r` inside a 128B-swizzled tile

@@ -106,5 +106,40 @@ def integer_operands(M: int, N: int, K: int, in_dtype: str, seed: int, lo: int =
     return make_operands(M, N, K, in_dtype, ("int", lo, hi), ("int", lo, hi), seed)
 
 
+def mx_scales(rows: int, K: int, seed: int, e_lo: int = 120, e_hi: int = 134) -> torch.Tensor:
+    """Seeded UE8M0 block scales (exponent bytes uniform in [e_lo, e_hi], i.e.
+    scales 2^(e_lo-127) .. 2^(e_hi-127)), row-major rows x ceil(K/32), uint8."""
+    gen = torch.Generator().manual_seed(int(seed))
+    return torch.randint(e_lo, e_hi + 1, (rows, (K + 31) // 32), generator=gen, dtype=torch.int32).to(torch.uint8)
+
+
+def mx_operands(M: int, N: int, K: int, in_dtype: str, seed: int, dist_a: tuple = ("uniform",),
+                dist_b: tuple = ("normal", 1.0), e_lo: int = 120, e_hi: int = 134):
+    """(A, B, scale_a, scale_b): seeded 8-bit operands plus row-major UE8M0 block
+    scales for every 32 consecutive K elements of each row."""
+    a, b = make_operands(M, N, K, in_dtype, dist_a, dist_b, seed)
+    return a, b, mx_scales(M, K, seed + 1000, e_lo, e_hi), mx_scales(N, K, seed + 2000, e_lo, e_hi)
+
+
+def mx_tiled_bytes(rows: int, K: int) -> int:
+    """Bytes of the tiled scale layout for `rows` rows: 512-byte blocks of 128 rows x 4 scales."""
+    return ((rows + 127) // 128) * ((K + 127) // 128) * 512
+
+
+def mx_tile_scales(s: torch.Tensor, K: int, pad: int = 127) -> torch.Tensor:
+    """Row-major rows x ceil(K/32) scales rearranged (a pure permutation) into the
+    tiled layout the block-scaled kernels read: 512-byte blocks, one per 128 rows
+    x 4 scale columns, blocks ordered by row block then column block; inside a
+    block, scale (r, c) sits at byte (r % 32) * 16 + (r // 32) * 4 + c.  Padding
+    rows and columns hold `pad`."""
+    rows, ks = s.shape
+    rb, cb = (rows + 127) // 128, (K + 127) // 128
+    full = torch.full((rb * 128, cb * 4), pad, dtype=torch.uint8)
+    full[:rows, :ks] = s
+    # (rb, r1, r0, cb, c) with row = rb*128 + r1*32 + r0, col = cb*4 + c
+    t = full.view(rb, 4, 32, cb, 4).permute(0, 3, 2, 1, 4).contiguous()
+    return t.view(-1)
+
+
 def torch_dtype(name: str) -> torch.dtype:
     return _TORCH[name]

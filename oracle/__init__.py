@@ -16,7 +16,9 @@ identity / permutation operands, the rank-1 closed form, transpose symmetry,
 additivity, thread-count invariance and an exhaustive check of both 16-bit
 decoders against numpy's IEEE binary16 / binary32 conversions.  The fused
 epilogue (``epilogue``: bias, activation, residual) is pinned in
-tests/test_oracle_epilogue_pins.py.
+tests/test_oracle_epilogue_pins.py; the 8-bit float inputs (E4M3 / E5M2), the
+dequantisation scales and the MX block-scaled product (``gemm_mx``) in
+tests/test_oracle_fp8_pins.py and tests/test_oracle_mx_pins.py.
 """
 from __future__ import annotations
 
@@ -68,6 +70,11 @@ def _load():
         lib.oracle_gemm8_rows_f64.restype = ctypes.c_int
         lib.oracle_widen8.argtypes = [ctypes.c_uint8, ctypes.c_int]
         lib.oracle_widen8.restype = ctypes.c_double
+        lib.oracle_gemm_mx_rows_f64.argtypes = [i64, i64, i64, p, p, ctypes.c_int, p, p, p, i64, p, p,
+                                                 ctypes.c_int]
+        lib.oracle_gemm_mx_rows_f64.restype = ctypes.c_int
+        lib.oracle_ue8m0.argtypes = [ctypes.c_uint8]
+        lib.oracle_ue8m0.restype = ctypes.c_double
         lib.oracle_scale_f64.argtypes = [i64, i64, p, p, p]
         lib.oracle_scale_f64.restype = ctypes.c_int
         lib.oracle_epilogue_f64.argtypes = [i64, i64, p, p, p, ctypes.c_int, ctypes.c_int]
@@ -145,6 +152,47 @@ def _gemm8(a, b, kind, rows, nthreads):
                                        S.ctypes.data, int(nthreads))
     if rc != 0:
         raise ValueError("oracle_gemm8_rows_f64 rejected its arguments")
+    return C, S
+
+
+def _u8(x) -> np.ndarray:
+    if isinstance(x, np.ndarray):
+        return np.ascontiguousarray(x.astype(np.uint8, copy=False))
+    import torch
+    return np.ascontiguousarray(x.detach().cpu().contiguous().view(torch.uint8).numpy())
+
+
+def ue8m0(e: int) -> float:
+    """Value of one UE8M0 scale byte: 2^(e - 127), NaN for 255."""
+    return float(_load().oracle_ue8m0(int(e) & 0xFF))
+
+
+def gemm_mx(a, b, scale_a, scale_b, rows=None, kind: int | None = None, nthreads: int = 0):
+    """MX block-scaled product of 8-bit operands, in fp64:
+    C[i,j] = sum_k (X_A[i,k//32] a[i,k]) (X_B[j,k//32] b[j,k]), with S the sum of
+    the terms' magnitudes.  scale_a (M x ceil(K/32)) and scale_b (N x ceil(K/32))
+    hold UE8M0 bytes, row-major.  ``rows`` restricts C and S to those rows of A."""
+    kind = kind_of(a) if kind is None else kind
+    if kind not in (IN_E4M3, IN_E5M2):
+        raise ValueError("MX block scaling takes 8-bit float operands")
+    A, B = _bytes8(a), _bytes8(b)
+    M, K = A.shape
+    N, K2 = B.shape
+    if K != K2:
+        raise ValueError("inner dimensions differ")
+    SA, SB = _u8(scale_a), _u8(scale_b)
+    ks = (K + 31) // 32
+    if SA.shape != (M, ks) or SB.shape != (N, ks):
+        raise ValueError("scales must be M x ceil(K/32) and N x ceil(K/32)")
+    r = None if rows is None else np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    n = M if r is None else len(r)
+    C = np.empty((n, N), dtype=np.float64)
+    S = np.empty((n, N), dtype=np.float64)
+    rc = _load().oracle_gemm_mx_rows_f64(M, N, K, A.ctypes.data, B.ctypes.data, kind, SA.ctypes.data,
+                                         SB.ctypes.data, None if r is None else r.ctypes.data, n,
+                                         C.ctypes.data, S.ctypes.data, int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle_gemm_mx_rows_f64 rejected its arguments")
     return C, S
 
 

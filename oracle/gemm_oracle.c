@@ -287,3 +287,55 @@ int oracle_gemm8_rows_f64(int64_t M, int64_t N, int64_t K,
     }
     return 0;
 }
+
+/*
+ * MX block scaling (OCP Microscaling Formats (MX) Specification v1.0, section
+ * 5: an MX block is k = 32 consecutive elements sharing one scale X in the
+ * UE8M0 format, X = 2^(e - 127), e = 255 encoding NaN).  The block-scaled
+ * GEMM multiplies each element by its block's scale before the dot product:
+ *
+ *   C[i][j] = sum_k (X_A[i][k / 32] * a_ik) * (X_B[j][k / 32] * b_jk)
+ *
+ * SA is M x ceil(K/32) and SB is N x ceil(K/32), row-major, one byte per
+ * scale.  Every term is exact in fp64 (8-bit float products times a power of
+ * two between 2^-254 and 2^254).
+ */
+static double ue8m0(uint8_t e) { return e == 255 ? NAN : ldexp(1.0, (int)e - 127); }
+
+double oracle_ue8m0(uint8_t e) { return ue8m0(e); }
+
+int oracle_gemm_mx_rows_f64(int64_t M, int64_t N, int64_t K, const uint8_t* A, const uint8_t* B,
+                            int in_kind, const uint8_t* SA, const uint8_t* SB,
+                            const int64_t* rows, int64_t nrows, double* C, double* S, int nthreads) {
+    if (M < 0 || N < 0 || K < 0 || nrows < 0 || !SA || !SB) return -1;
+    if (in_kind != ORACLE_IN_E4M3 && in_kind != ORACLE_IN_E5M2) return -1;
+    if (rows == NULL && nrows != M) return -1;
+    if (rows != NULL) {
+        for (int64_t r = 0; r < nrows; ++r)
+            if (rows[r] < 0 || rows[r] >= M) return -1;
+    }
+    const int64_t KS = (K + 31) / 32;
+    double tab[256];
+    for (int b = 0; b < 256; ++b) tab[b] = oracle_widen8((uint8_t)b, in_kind);
+    set_threads(nthreads);
+    int64_t r;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (r = 0; r < nrows; ++r) {
+        int64_t i = rows ? rows[r] : r;
+        const uint8_t* a = A + i * K;
+        const uint8_t* sa = SA + i * KS;
+        for (int64_t j = 0; j < N; ++j) {
+            const uint8_t* b = B + j * K;
+            const uint8_t* sb = SB + j * KS;
+            double acc = 0.0, sabs = 0.0;
+            for (int64_t k = 0; k < K; ++k) {
+                double p = (ue8m0(sa[k / 32]) * tab[a[k]]) * (ue8m0(sb[k / 32]) * tab[b[k]]);
+                acc += p;
+                sabs += fabs(p);
+            }
+            C[r * N + j] = acc;
+            if (S) S[r * N + j] = sabs;
+        }
+    }
+    return 0;
+}
