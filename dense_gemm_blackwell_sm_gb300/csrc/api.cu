@@ -22,6 +22,7 @@ struct gemm_plan_s {
   gemm_dtype_t dtype;
   bool in_bf16, out_f32;
   bool in_f8, in_e5m2;  // 8-bit float inputs (E4M3 or E5M2)
+  bool in_mx;           // ... with MX block scales (gemm_plan_run_mx)
   int variant, sched, stages, raster_group;
   int device, num_sms;
   int grid_units;  // CTAs (variants 3-6) or clusters (7-9) launched
@@ -103,10 +104,19 @@ uint32_t make_idesc(bool bf16, int M, int N) {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 int out_bytes(gemm_dtype_t dt) {
-  return (dt == GEMM_F16_F32 || dt == GEMM_BF16_F32 || dt == GEMM_E4M3_F32 || dt == GEMM_E5M2_F32) ? 4 : 2;
+  return (dt == GEMM_F16_F32 || dt == GEMM_BF16_F32 || dt == GEMM_E4M3_F32 || dt == GEMM_E5M2_F32 ||
+          dt == GEMM_MXE4M3_F32 || dt == GEMM_MXE5M2_F32)
+             ? 4
+             : 2;
 }
 
-bool is_f8(gemm_dtype_t dt) { return dt >= GEMM_E4M3_F32 && dt <= GEMM_E5M2_BF16; }
+bool is_mx(gemm_dtype_t dt) { return dt >= GEMM_MXE4M3_F32 && dt <= GEMM_MXE5M2_BF16; }
+
+bool is_f8(gemm_dtype_t dt) { return (dt >= GEMM_E4M3_F32 && dt <= GEMM_E5M2_BF16) || is_mx(dt); }
+
+bool is_e5m2(gemm_dtype_t dt) {
+  return dt == GEMM_E5M2_F32 || dt == GEMM_E5M2_BF16 || dt == GEMM_MXE5M2_F32 || dt == GEMM_MXE5M2_BF16;
+}
 
 int in_bytes(gemm_dtype_t dt) { return is_f8(dt) ? 1 : 2; }
 
@@ -114,7 +124,7 @@ int in_bytes(gemm_dtype_t dt) { return is_f8(dt) ? 1 : 2; }
 bool c_rows_tma_ok(int64_t N, gemm_dtype_t dt) { return (N * out_bytes(dt)) % 16 == 0; }
 
 gemm_status_t validate_sizes(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype) {
-  if ((int)dtype < 0 || (int)dtype > GEMM_E5M2_BF16) return GEMM_ERR_UNSUPPORTED_DTYPE;
+  if ((int)dtype < 0 || (int)dtype > GEMM_MXE5M2_BF16) return GEMM_ERR_UNSUPPORTED_DTYPE;
   if (M < 1 || N < 1 || K < 1 || M >= kMaxDim || N >= kMaxDim || K >= kMaxDim) return GEMM_ERR_INVALID_ARG;
   if ((K * in_bytes(dtype)) % 16 != 0) return GEMM_ERR_UNSUPPORTED_SHAPE;  // TMA row pitch
   return GEMM_OK;
@@ -184,7 +194,15 @@ gemm_status_t prepare_launch(gemm_plan_s* p) {
     k.idesc = is_ws(v) ? make_idesc(p->in_bf16, 128 * p->cg, 256) : make_idesc(p->in_bf16, 128, 128);
     k.mma_kind = 0;
     k.bk = 64;
-    if (p->in_f8) {
+    if (p->in_mx) {
+      // kind::mxf8f6f4 descriptor: A / B format E4M3 = 0, E5M2 = 1 (bits 7-9, 10-12),
+      // N / 8 (17-22), scale type UE8M0 (bit 23), M / 16 (24-28); the scale-byte
+      // selectors (B: bits 4-5, A: bits 29-30) are added per MMA by the kernel
+      const uint32_t fmt = p->in_e5m2 ? 1u : 0u;
+      k.idesc = (fmt << 7) | (fmt << 10) | ((uint32_t)(256 >> 3) << 17) | (1u << 23) | ((uint32_t)(128 >> 4) << 24);
+      k.mma_kind = 2;
+      k.bk = 128;
+    } else if (p->in_f8) {
       // kind::f8f6f4 descriptor: A / B format E4M3 = 0, E5M2 = 1, fp32 accumulator
       const uint32_t fmt = p->in_e5m2 ? 1u : 0u;
       k.idesc = (1u << 4) | (fmt << 7) | (fmt << 10) | ((uint32_t)(256 >> 3) << 17) |
@@ -201,6 +219,8 @@ gemm_status_t prepare_launch(gemm_plan_s* p) {
       e = spec_step45((int)p->M, (int)p->N, p->stages, p->out_f32, &p->spec);
     } else if (v == GEMM_VARIANT_S6_PERSISTENT) {
       e = spec_step6(p->sched - 1, p->stages, p->out_f32, p->grid_units, &p->spec);
+    } else if (p->in_mx) {
+      e = spec_mx(p->sched - 1, p->out_f32, p->stages, p->grid_units, &p->spec);
     } else {
       e = spec_ws(p->cg, p->consumers, p->sched - 1, p->out_f32, p->stages, p->grid_units, &p->spec);
     }
@@ -228,6 +248,11 @@ gemm_status_t build_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, co
   st = current_device(&dev, &sms);
   if (st != GEMM_OK && !o.variant) return st;
   int variant = o.variant ? o.variant : auto_variant(M, N, K, dtype, sms);
+  if (is_mx(dtype)) {
+    // block-scaled inputs run on step 7's one-CTA tile only
+    if (o.variant && o.variant != GEMM_VARIANT_S7_WARP_SPECIALIZED) return GEMM_ERR_UNSUPPORTED_SHAPE;
+    variant = GEMM_VARIANT_S7_WARP_SPECIALIZED;
+  }
   if (is_f8(dtype)) {
     // 8-bit inputs run on the warp-specialised kernels only, K-major
     if (o.layout != 0) return GEMM_ERR_UNSUPPORTED_SHAPE;
@@ -266,7 +291,8 @@ gemm_status_t build_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, co
   p->dtype = dtype;
   p->in_bf16 = (dtype == GEMM_BF16_F32 || dtype == GEMM_BF16_BF16);
   p->in_f8 = is_f8(dtype);
-  p->in_e5m2 = (dtype == GEMM_E5M2_F32 || dtype == GEMM_E5M2_BF16);
+  p->in_e5m2 = is_e5m2(dtype);
+  p->in_mx = is_mx(dtype);
   p->out_f32 = (out_bytes(dtype) == 4);
   p->variant = variant;
   p->device = dev;
@@ -300,6 +326,10 @@ gemm_status_t build_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, co
     p->tile_m = sh.tile_m;
     p->tile_n = sh.tile_n;
     p->smem = ws_smem_bytes(p->cg, p->consumers, p->stages);
+    if (p->in_mx) {
+      p->stages = o.stages ? std::min<int>(o.stages, mx_max_stages()) : mx_max_stages();
+      p->smem = mx_smem_bytes(p->stages);
+    }
   } else if (variant == GEMM_VARIANT_S6_PERSISTENT) {
     p->smem = step6_smem_bytes(p->stages);
   }
@@ -324,7 +354,8 @@ gemm_status_t build_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, co
     if (o.max_ctas && p->sched != GEMM_SCHED_CLC) units = std::min(units, (int)o.max_ctas);
     p->grid_units = units;
   } else if (variant >= GEMM_VARIANT_S7_WARP_SPECIALIZED && variant <= GEMM_VARIANT_S9_TWO_CONSUMERS) {
-    int active = ws_max_active_clusters(p->cg, p->consumers, p->sched - 1, p->out_f32, p->stages);
+    // (the MX kernel's shared memory also allows one CTA per SM)
+    int active = p->in_mx ? sms : ws_max_active_clusters(p->cg, p->consumers, p->sched - 1, p->out_f32, p->stages);
     if (active < 1) active = std::max(1, sms / p->cg);
     int units = (p->sched == GEMM_SCHED_CLC) ? tiles : std::min(tiles, active);
     if (o.max_ctas && p->sched != GEMM_SCHED_CLC) units = std::max(1, std::min(units, (int)o.max_ctas));
@@ -400,8 +431,11 @@ const CUtensorMap* operand_map(gemm_plan_s* p, int role, const void* ptr) {
 }
 
 gemm_status_t launch_plan(gemm_plan_s* p, const void* A, const void* B, void* C, cudaStream_t s,
-                          const gemm_epilogue_t* epi = nullptr) {
+                          const gemm_epilogue_t* epi = nullptr, const void* sfa = nullptr,
+                          const void* sfb = nullptr) {
   if (!A || !B || !C) return GEMM_ERR_INVALID_ARG;
+  // block-scaled plans run with their scale arrays, other plans without
+  if (p->in_mx != (sfa != nullptr) || p->in_mx != (sfb != nullptr)) return GEMM_ERR_INVALID_ARG;
   if (!aligned16(A) || !aligned16(B) || !aligned16(C)) return GEMM_ERR_MISALIGNED;
   int cur = -1;
   if (cudaGetDevice(&cur) != cudaSuccess || cur != p->device) return GEMM_ERR_INVALID_ARG;
@@ -438,6 +472,8 @@ gemm_status_t launch_plan(gemm_plan_s* p, const void* A, const void* B, void* C,
         k.stages = p->epi_stages;
         spec = &p->spec_epi[epi->activation];
       }
+      k.sfa = static_cast<const uint8_t*>(sfa);
+      k.sfb = static_cast<const uint8_t*>(sfb);
       k.A = static_cast<const uint16_t*>(A);
       k.B = static_cast<const uint16_t*>(B);
       k.C = C;
@@ -465,6 +501,45 @@ gemm_status_t launch_plan(gemm_plan_s* p, const void* A, const void* B, void* C,
     return GEMM_ERR_CUDA;
   }
   return GEMM_OK;
+}
+
+// Validate the fused epilogue, make its kernel's launch shape on first use,
+// and launch.
+gemm_status_t run_with_epilogue(gemm_plan_s* plan, const void* A, const void* B, void* C,
+                                const gemm_epilogue_t* epi, cudaStream_t s, const void* sfa, const void* sfb) {
+  if (!is_ws(plan->variant)) return GEMM_ERR_UNSUPPORTED_SHAPE;
+  if (epi->activation < GEMM_ACT_NONE || epi->activation > GEMM_ACT_GELU_ERF) return GEMM_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(epi->bias) & 3u) || (reinterpret_cast<uintptr_t>(epi->residual) & 15u) ||
+      (reinterpret_cast<uintptr_t>(epi->scale_a) & 3u) || (reinterpret_cast<uintptr_t>(epi->scale_b) & 3u))
+    return GEMM_ERR_MISALIGNED;
+  const int act = epi->activation;
+  if (!plan->epi_ready[act]) {
+    cudaError_t e;
+    if (plan->in_mx) {
+      // the block-scaled plan already runs one consumer on one CTA
+      plan->epi_stages = plan->stages;
+      plan->epi_tiles_m = plan->tiles_m;
+      e = spec_mx(0, plan->out_f32, plan->stages, plan->grid_units, &plan->spec_epi[act], act);
+    } else {
+      // The fused epilogue does real arithmetic per element, so it must hide behind
+      // the MMAs: a step-9 plan (both TMEM accumulators busy) runs it with one
+      // consumer per CTA, i.e. step 8's double-buffered 256x256 tile, same operand boxes.
+      const int cons = 1;
+      plan->epi_stages = ws_max_stages(plan->cg, cons);
+      plan->epi_tiles_m = ceil_div(plan->M, 128 * plan->cg * cons);
+      const int tiles = plan->epi_tiles_m * plan->tiles_n;
+      int active = ws_max_active_clusters(plan->cg, cons, 0, plan->out_f32, plan->epi_stages);
+      if (active < 1) active = std::max(1, plan->num_sms / plan->cg);
+      e = spec_ws(plan->cg, cons, 0, plan->out_f32, plan->epi_stages, std::min(tiles, active), &plan->spec_epi[act],
+                  act);
+    }
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return GEMM_ERR_CUDA;
+    }
+    plan->epi_ready[act] = true;
+  }
+  return launch_plan(plan, A, B, C, s, epi, sfa, sfb);
 }
 
 gemm_status_t check_plan(gemm_plan_s* p) {
@@ -508,36 +583,31 @@ gemm_status_t gemm_plan_run(gemm_plan_t plan, const void* A, const void* B, void
 gemm_status_t gemm_plan_run_epilogue(gemm_plan_t plan, const void* A, const void* B, void* C,
                                      const gemm_epilogue_t* epi, gemm_stream_t stream) {
   if (!plan || !epi) return GEMM_ERR_INVALID_ARG;
-  if (!is_ws(plan->variant)) return GEMM_ERR_UNSUPPORTED_SHAPE;
-  if (epi->activation < GEMM_ACT_NONE || epi->activation > GEMM_ACT_GELU_ERF) return GEMM_ERR_INVALID_ARG;
-  if ((reinterpret_cast<uintptr_t>(epi->bias) & 3u) || (reinterpret_cast<uintptr_t>(epi->residual) & 15u) ||
-      (reinterpret_cast<uintptr_t>(epi->scale_a) & 3u) || (reinterpret_cast<uintptr_t>(epi->scale_b) & 3u))
-    return GEMM_ERR_MISALIGNED;
-  const int act = epi->activation;
-  if (!plan->epi_ready[act]) {
-    // The fused epilogue does real arithmetic per element, so it must hide behind
-    // the MMAs: a step-9 plan (both TMEM accumulators busy) runs it with one
-    // consumer per CTA, i.e. step 8's double-buffered 256x256 tile, same operand boxes.
-    const int cons = 1;
-    plan->epi_stages = ws_max_stages(plan->cg, cons);
-    plan->epi_tiles_m = ceil_div(plan->M, 128 * plan->cg * cons);
-    const int tiles = plan->epi_tiles_m * plan->tiles_n;
-    int active = ws_max_active_clusters(plan->cg, cons, 0, plan->out_f32, plan->epi_stages);
-    if (active < 1) active = std::max(1, plan->num_sms / plan->cg);
-    if (spec_ws(plan->cg, cons, 0, plan->out_f32, plan->epi_stages, std::min(tiles, active), &plan->spec_epi[act],
-                act) != cudaSuccess) {
-      cudaGetLastError();
-      return GEMM_ERR_CUDA;
-    }
-    plan->epi_ready[act] = true;
-  }
-  return launch_plan(plan, A, B, C, reinterpret_cast<cudaStream_t>(stream), epi);
+  if (plan->in_mx) return GEMM_ERR_INVALID_ARG;  // needs its scales: gemm_plan_run_mx
+  return run_with_epilogue(plan, A, B, C, epi, reinterpret_cast<cudaStream_t>(stream), nullptr, nullptr);
+}
+
+gemm_status_t gemm_plan_run_mx(gemm_plan_t plan, const void* A, const void* B, void* C, const void* scale_a,
+                               const void* scale_b, const gemm_epilogue_t* epi, gemm_stream_t stream) {
+  if (!plan) return GEMM_ERR_INVALID_ARG;
+  if (!plan->in_mx) return GEMM_ERR_UNSUPPORTED_DTYPE;
+  if (!scale_a || !scale_b) return GEMM_ERR_INVALID_ARG;
+  if (!aligned16(scale_a) || !aligned16(scale_b)) return GEMM_ERR_MISALIGNED;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (epi == nullptr) return launch_plan(plan, A, B, C, s, nullptr, scale_a, scale_b);
+  return run_with_epilogue(plan, A, B, C, epi, s, scale_a, scale_b);
+}
+
+int64_t gemm_mx_scale_bytes(int64_t rows, int64_t K) {
+  if (rows < 1 || K < 1 || rows >= kMaxDim || K >= kMaxDim) return -1;
+  return ((rows + 127) / 128) * ((K + 127) / 128) * 512;
 }
 
 gemm_status_t gemm_run(int64_t M, int64_t N, int64_t K, const void* A, const void* B, void* C,
                        gemm_dtype_t dtype, gemm_stream_t stream) {
   gemm_status_t st = validate_sizes(M, N, K, dtype);
   if (st != GEMM_OK) return st;
+  if (is_mx(dtype)) return GEMM_ERR_INVALID_ARG;  // needs scales: gemm_plan_run_mx
   if (!A || !B || !C) return GEMM_ERR_INVALID_ARG;
   if (!aligned16(A) || !aligned16(B) || !aligned16(C)) return GEMM_ERR_MISALIGNED;
   int dev = 0;
@@ -572,6 +642,7 @@ gemm_status_t gemm_run_host(int64_t M, int64_t N, int64_t K, const void* A_host,
                             gemm_stream_t stream) {
   gemm_status_t st = validate_sizes(M, N, K, dtype);
   if (st != GEMM_OK) return st;
+  if (is_mx(dtype)) return GEMM_ERR_INVALID_ARG;  // needs scales: gemm_plan_run_mx
   if (!A_host || !B_host || !C_host || !dA || !dB || !dC) return GEMM_ERR_INVALID_ARG;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const int64_t ib = in_bytes(dtype);

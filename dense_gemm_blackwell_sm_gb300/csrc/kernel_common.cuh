@@ -53,12 +53,16 @@ struct KParams {
   int32_t act;           // EPI_ACT_*
   // operand layouts (steps 7-9): bit 0 = A stored K x M (M-major), bit 1 = B stored K x N (N-major)
   uint32_t layout;
-  // element kind of A and B (steps 7-9): 0 = fp16 / bf16 (kind::f16), 1 = 8-bit float (kind::f8f6f4)
+  // element kind of A and B (steps 7-9): 0 = fp16 / bf16 (kind::f16), 1 = 8-bit float
+  // (kind::f8f6f4), 2 = 8-bit float with MX block scales (kind::mxf8f6f4)
   int32_t mma_kind;
   int32_t bk;            // K elements per 128-byte stage row: 64 (16-bit) or 128 (8-bit)
   // fused-epilogue dequantisation: acc * scale_a[row] * scale_b[col] before the bias
   const float* scale_a;  // M fp32 values, or null
   const float* scale_b;  // N fp32 values, or null
+  // MX block scales (mma_kind 2): UE8M0 bytes in the tiled 128 x 4 layout
+  const uint8_t* sfa;
+  const uint8_t* sfb;
 };
 
 constexpr uint32_t LAYOUT_A_MN = 1u;

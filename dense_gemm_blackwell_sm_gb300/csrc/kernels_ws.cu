@@ -1,424 +1,10 @@
-// kernels_ws.cu -- steps 7-9 of the tiled GEMM, C = A * B^T: persistent,
-// warp-specialised kernels with TMEM double buffering, CTA pairs and a
-// second MMA consumer.
-//
-// "Modern GPU Programming for MLSys" (reading notes, section "9 步优化",
-// third stage) adds, on top of the persistent TMA pipeline of step 6:
-//
-//   step 7  warp specialisation: a producer warp (TMA), an MMA warp and
-//           writeback warps hand tiles to each other through mbarriers, so
-//           loads, MMAs and stores overlap continuously;
-//   step 8  a 2-CTA cluster computes one 256x256 tile: the pair MMA
-//           (cta_group::2) reads both CTAs' shared memory, the accumulator
-//           spans both CTAs' TMEM, and each loaded byte feeds about twice the
-//           work;
-//   step 9  a second MMA consumer per CTA: both consumers share the B stage,
-//           each owns half of the output rows, so the cluster tile grows to
-//           512x256 with no extra B traffic per stage.
-//
-// Roles (256 threads):
-//   warp 0      producer: one lane issues the TMA loads into a `stages`-deep ring
-//   warp 1      MMA consumer 0 (one lane issues tcgen05.mma); owns TMEM alloc
-//   warp 2      tile scheduler: static stride, a global atomic counter, or
-//               hardware cluster launch control; publishes tile ids to a ring
-//   warp 3      MMA consumer 1 (step 9 only)
-//   warps 4-7   writeback: tcgen05.ld -> fp32 or bf16 -> 128B-swizzled SMEM
-//               staging -> TMA tile stores (vectorised and coalesced by TMA)
-//
-// TMEM holds two 256-column fp32 accumulators.  Steps 7 and 8 alternate them
-// between consecutive tiles (the writeback of tile i overlaps the MMAs of
-// tile i+1); step 9 gives one to each consumer.
-//
-// In a CTA pair, each CTA loads its own 128 rows of A and its own 128 rows of B
-// (the pair MMA splits A along M and B along N) with the cta_group::2 TMA form,
-// whose completion is counted on the leader CTA's barrier; only the leader
-// issues MMAs, and its commits arrive on the barriers of both CTAs.  No load is
-// multicast.  Every wait is bounded (see ptx.cuh).
-#include "kernel_common.cuh"
-#include "launch.h"
+// kernels_ws.cu -- instantiations of the step 7-9 kernels (fp16 / bf16 / 8-bit
+// float inputs) and their launch shapes; the kernel itself is in kernels_ws.cuh.
+#include "kernels_ws.cuh"
 
 namespace dgb {
 
 namespace {
-
-enum SchedWs { SCHED_STATIC = 0, SCHED_ATOMIC = 1, SCHED_CLC = 2 };
-
-constexpr int WS_THREADS = 256;
-constexpr int WS_BN = 256;          // tile columns (MMA N)
-constexpr uint32_t WS_A_BYTES = 128u * 128u;  // 128 rows x 128 B
-constexpr int WS_RING = 4;          // depth of the tile-id ring
-constexpr int WS_STAGING = 4 * 2 * 4096;      // 4 writeback warps x 2 buffers x 32 rows x 128 B
-constexpr int WS_CTRL = 512;        // barriers and small state
-constexpr int WS_MAX_STAGES = 8;
-constexpr size_t WS_SMEM_LIMIT = 232448;  // 227 KB per CTA
-
-template <int CG, int NCONS>
-struct WsCfg {
-  static constexpr int B_ROWS = (CG == 1) ? 256 : 128;
-  static constexpr uint32_t B_BYTES = (uint32_t)B_ROWS * 128u;
-  static constexpr uint32_t STAGE = NCONS * WS_A_BYTES + B_BYTES;  // per CTA
-  static constexpr int TILE_M = 128 * CG * NCONS;
-  // arrivals that free one tile-ring slot: producer + 4 writeback warps in
-  // every CTA of the cluster, plus the leader's MMA consumers
-  static constexpr uint32_t RING_CONSUMERS = (uint32_t)(CG * 5 + NCONS);
-};
-
-// EPI < 0: plain writeback; EPI >= 0: fused epilogue with activation EPI
-template <typename OutT, int CG, int NCONS, int SCHED, int EPI = -1>
-__global__ void __launch_bounds__(WS_THREADS, 1)
-    k_ws(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-         const __grid_constant__ CUtensorMap tmC, KParams p) {
-  using Cfg = WsCfg<CG, NCONS>;
-  constexpr int CW = (sizeof(OutT) == 4) ? 32 : 64;  // output columns per 128-byte staging row
-  constexpr int NCH = WS_BN / CW;
-
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = align_1024(smem_raw);
-  const int S = p.stages;
-  uint8_t* ring = smem;
-  uint8_t* staging = smem + (size_t)S * Cfg::STAGE;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(staging + WS_STAGING);
-  uint64_t* full = bars;                       // [8]  TMA -> MMA
-  uint64_t* empty = bars + 8;                  // [8]  MMA -> TMA
-  uint64_t* acc_full = bars + 16;              // [2]  MMA -> writeback
-  uint64_t* acc_empty = bars + 18;             // [2]  writeback -> MMA
-  uint64_t* ring_full = bars + 20;             // [4]  scheduler -> roles
-  uint64_t* ring_empty = bars + 24;            // [4]  roles -> scheduler
-  uint64_t* clc_bar = bars + 28;
-  uint64_t* drain_bar = bars + 29;
-  uint32_t* clc_resp = reinterpret_cast<uint32_t*>(bars + 30);   // 16 B, 16-aligned
-  volatile int32_t* ring_tile = reinterpret_cast<volatile int32_t*>(clc_resp + 4);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(clc_resp + 4 + WS_RING);
-  volatile uint32_t* abort_flag = tmem_slot + 1;
-  volatile uint32_t* zero_word = tmem_slot + 2;
-
-  const uint32_t warp = warp_idx(), lane = lane_idx();
-  const uint32_t rank = (CG == 2) ? cluster_ctarank() : 0u;
-  const bool leader = (rank == 0);
-
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < S; ++s) {
-      mbar_init(smem_u32(full + s), 1);
-      mbar_init(smem_u32(empty + s), NCONS);
-    }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(smem_u32(acc_full + i), 1);
-      mbar_init(smem_u32(acc_empty + i), 4 * CG);
-    }
-    for (int i = 0; i < WS_RING; ++i) {
-      mbar_init(smem_u32(ring_full + i), 1);
-      mbar_init(smem_u32(ring_empty + i), Cfg::RING_CONSUMERS);
-    }
-    mbar_init(smem_u32(clc_bar), 1);
-    mbar_init(smem_u32(drain_bar), NCONS);
-    *abort_flag = 0u;
-    *zero_word = 0u;
-    fence_mbar_init();
-  }
-  if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(&tmA);
-    tma_prefetch_desc(&tmB);
-    tma_prefetch_desc(&tmC);
-  }
-  if (warp == 1) {
-    tmem_alloc<CG>(smem_u32(tmem_slot), 512);
-    tmem_relinquish<CG>();
-  }
-  tc_fence_before();
-  if constexpr (CG == 2) {
-    cluster_sync_all();
-  } else {
-    __syncthreads();
-  }
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
-  const uint32_t peer_abort = (CG == 2) ? mapa_shared(smem_u32((const void*)abort_flag), rank ^ 1u) : 0u;
-  const WaitCtl w{abort_flag, p.status, p.timeout_ns, peer_abort};
-  // K elements per stage: one 128-byte swizzle row of A / B (64 x 16-bit or 128 x 8-bit)
-  const int32_t BKE = (p.bk > 0) ? p.bk : 64;
-  const int32_t KB = (p.K + BKE - 1) / BKE;
-  const bool f8 = (p.mma_kind == 1);
-  const bool a_mn = (p.layout & LAYOUT_A_MN) != 0u;
-  const bool b_mn = (p.layout & LAYOUT_B_MN) != 0u;
-
-  // one lane takes the next entry of the tile-id ring; -1 ends the stream
-  auto ring_get = [&](uint32_t i, int32_t& tile) -> bool {
-    const uint32_t slot = i % WS_RING, ph = (i / WS_RING) & 1u;
-    if (!mbar_wait<CG == 2>(smem_u32(ring_full + slot), ph, w, WAIT_RING_FULL)) return false;
-    tile = ring_tile[slot];
-    if constexpr (CG == 1) {
-      mbar_arrive(smem_u32(ring_empty + slot));
-    } else {
-      mbar_arrive_cluster(mapa_shared(smem_u32(ring_empty + slot), 0));
-    }
-    return true;
-  };
-
-  if (warp == 2) {
-    // ------------------------------------------------------------- scheduler
-    if (lane == 0 && leader) {
-      const int32_t total = p.tiles_m * p.tiles_n;
-      const int32_t nclusters = (int32_t)(gridDim.x / CG);
-      const int32_t cid = (int32_t)(blockIdx.x / CG);
-      int32_t next_static = cid;
-      uint32_t clc_phase = 0;
-      bool first = true, exhausted = false, ok = true;
-      for (uint32_t i = 0;; ++i) {
-        const uint32_t slot = i % WS_RING, ph = (i / WS_RING) & 1u;
-        if (!mbar_wait<CG == 2>(smem_u32(ring_empty + slot), ph ^ 1u, w, WAIT_RING_EMPTY)) { ok = false; break; }
-        int32_t t = -1;
-        if (!exhausted) {
-          if (SCHED == SCHED_STATIC) {
-            t = next_static;
-            next_static += nclusters;
-          } else if (SCHED == SCHED_ATOMIC) {
-            t = (int32_t)atomicAdd(p.status + 1, 1u);
-          } else if (first) {
-            t = cid;
-          } else {
-            mbar_arrive_expect_tx(smem_u32(clc_bar), 16);
-            clc_try_cancel(smem_u32(clc_resp), smem_u32(clc_bar));
-            if (!mbar_wait(smem_u32(clc_bar), clc_phase, w, WAIT_CLC)) { ok = false; break; }
-            clc_phase ^= 1u;
-            uint32_t x;
-            t = clc_decode(smem_u32(clc_resp), x) ? (int32_t)(x / CG) : -1;
-          }
-          first = false;
-        }
-        if (t >= total) t = -1;
-        if (t < 0) exhausted = true;
-        ring_tile[slot] = t;
-        mbar_arrive(smem_u32(ring_full + slot));
-        if constexpr (CG == 2) {
-          st_cluster_u32(mapa_shared(smem_u32((const void*)(ring_tile + slot)), 1), (uint32_t)t);
-          mbar_arrive_cluster(mapa_shared(smem_u32(ring_full + slot), 1));
-        }
-        if (t < 0) break;
-      }
-      if (SCHED == SCHED_ATOMIC && ok) {
-        // the last cluster to run out of tiles rewinds the counters for the next launch
-        __threadfence();
-        if (atomicAdd(p.status + 2, 1u) == (uint32_t)(nclusters - 1)) {
-          atomicExch(p.status + 1, 0u);
-          atomicExch(p.status + 2, 0u);
-        }
-      }
-    }
-  } else if (warp == 0) {
-    // -------------------------------------------------------------- producer
-    if (lane == 0) {
-      uint32_t stage = 0, sphase = 0;
-      bool skip = (p.debug_flags & DEBUG_SKIP_ONE_LOAD) != 0u;
-      bool ok = true;
-      for (uint32_t i = 0; ok; ++i) {
-        int32_t tile;
-        if (!ring_get(i, tile)) { ok = false; break; }
-        if (tile < 0) break;
-        int32_t tm, tn;
-        raster_tile(tile, p.tiles_m, p.tiles_n, p.raster_group, tm, tn);
-        const int32_t m_cta = tm * Cfg::TILE_M + (int32_t)rank * 128;
-        const int32_t n_cta = tn * WS_BN + (CG == 2 ? (int32_t)rank * 128 : 0);
-        for (int32_t kb = 0; kb < KB; ++kb) {
-          if (!mbar_wait(smem_u32(empty + stage), sphase ^ 1u, w, WAIT_PRODUCER_EMPTY)) { ok = false; break; }
-          const uint32_t fb = smem_u32(full + stage);
-          if (leader) mbar_arrive_expect_tx(fb, Cfg::STAGE * CG);
-          uint8_t* st = ring + (size_t)stage * Cfg::STAGE;
-#pragma unroll
-          for (int c = 0; c < NCONS; ++c) {
-            const int32_t row = m_cta + c * 128 * CG;
-            uint8_t* dst = st + c * WS_A_BYTES;
-            if (a_mn) {
-              // K x M in memory: two 64-row-of-K x 64-M boxes, 8 KB apart
-#pragma unroll
-              for (int h = 0; h < 2; ++h) {
-                if constexpr (CG == 1) {
-                  tma_load_2d(smem_u32(dst + h * 8192), &tmA, fb, row + 64 * h, kb * BKE);
-                } else {
-                  tma_load_2d_pair(smem_u32(dst + h * 8192), &tmA, mapa_shared(fb, 0), row + 64 * h, kb * BKE);
-                }
-              }
-            } else if constexpr (CG == 1) {
-              tma_load_2d(smem_u32(dst), &tmA, fb, kb * BKE, row);
-            } else {
-              tma_load_2d_pair(smem_u32(dst), &tmA, mapa_shared(fb, 0), kb * BKE, row);
-            }
-          }
-          uint8_t* bdst = st + NCONS * WS_A_BYTES;
-          if (skip) {
-            skip = false;  // test hook: this stage's B bytes never arrive
-          } else if (b_mn) {
-#pragma unroll
-            for (int h = 0; h < Cfg::B_ROWS / 64; ++h) {
-              if constexpr (CG == 1) {
-                tma_load_2d(smem_u32(bdst + h * 8192), &tmB, fb, n_cta + 64 * h, kb * BKE);
-              } else {
-                tma_load_2d_pair(smem_u32(bdst + h * 8192), &tmB, mapa_shared(fb, 0), n_cta + 64 * h, kb * BKE);
-              }
-            }
-          } else if constexpr (CG == 1) {
-            tma_load_2d(smem_u32(bdst), &tmB, fb, kb * BKE, n_cta);
-          } else {
-            tma_load_2d_pair(smem_u32(bdst), &tmB, mapa_shared(fb, 0), kb * BKE, n_cta);
-          }
-          if (++stage == (uint32_t)S) { stage = 0; sphase ^= 1u; }
-        }
-      }
-      if (!ok) {
-        // give copies still in flight time to land before SMEM is released
-        const uint64_t t0 = globaltimer_ns();
-        while (globaltimer_ns() - t0 < 2000000ull) {}
-      }
-    }
-  } else if ((warp == 1 || (NCONS == 2 && warp == 3)) && leader) {
-    // ------------------------------------------------------------------ MMA
-    if (lane == 0) {
-      const int cons = (warp == 1) ? 0 : 1;
-      uint32_t stage = 0, sphase = 0;
-      for (uint32_t i = 0;; ++i) {
-        int32_t tile;
-        if (!ring_get(i, tile) || tile < 0) break;
-        const uint32_t slot = (NCONS == 2) ? (uint32_t)cons : (i & 1u);
-        const uint32_t apar = (NCONS == 2) ? (i & 1u) : ((i >> 1) & 1u);
-        if (!mbar_wait<CG == 2>(smem_u32(acc_empty + slot), apar ^ 1u, w, WAIT_MMA_ACC_EMPTY)) break;
-        tc_fence_after();
-        const uint32_t d = tmem + slot * 256u;
-        bool ok = true;
-        for (int32_t kb = 0; kb < KB; ++kb) {
-          if (!mbar_wait(smem_u32(full + stage), sphase, w, WAIT_MMA_FULL)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t sa = smem_u32(ring + (size_t)stage * Cfg::STAGE + cons * WS_A_BYTES);
-          const uint32_t sb = smem_u32(ring + (size_t)stage * Cfg::STAGE + NCONS * WS_A_BYTES);
-          // K-major: a K step of 16 moves 32 B inside the swizzle row; MN-major: two 1 KB atoms
-          const uint64_t ad = a_mn ? sdesc_mn_sw128(sa, 8192) : sdesc_k_sw128(sa);
-          const uint64_t bd = b_mn ? sdesc_mn_sw128(sb, 8192) : sdesc_k_sw128(sb);
-          const uint64_t astep = a_mn ? 128 : 2, bstep = b_mn ? 128 : 2;
-          // four MMAs per stage, each over 32 bytes of K (16 x 16-bit or 32 x 8-bit)
-          if (f8) {
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-              mma_f8f6f4<CG>(d, ad + astep * k, bd + bstep * k, p.idesc, (kb | k) != 0);
-          } else {
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-              mma_f16<CG>(d, ad + astep * k, bd + bstep * k, p.idesc, (kb | k) != 0);
-          }
-          if constexpr (CG == 1) {
-            mma_commit(smem_u32(empty + stage));
-          } else {
-            mma_commit_pair(smem_u32(empty + stage), 3);
-          }
-          if (++stage == (uint32_t)S) { stage = 0; sphase ^= 1u; }
-        }
-        if (!ok) break;
-        if constexpr (CG == 1) {
-          mma_commit(smem_u32(acc_full + slot));
-        } else {
-          mma_commit_pair(smem_u32(acc_full + slot), 3);
-        }
-      }
-      // every MMA this thread issued must be complete before TMEM is released
-      mma_commit_cg<CG>(smem_u32(drain_bar));
-      const WaitCtl wd{zero_word, p.status, p.timeout_ns, 0};
-      mbar_wait(smem_u32(drain_bar), 0, wd, WAIT_DRAIN);
-    }
-  } else if (warp >= 4) {
-    // ------------------------------------------------------------ writeback
-    const uint32_t q = warp & 3u;  // TMEM lane quarter this warp may access
-    uint8_t* my_staging = staging + q * 8192u;
-    uint32_t tog = 0;
-    for (uint32_t i = 0;; ++i) {
-      int32_t tile = -1;
-      uint32_t okr = 1;
-      if (lane == 0) okr = ring_get(i, tile) ? 1u : 0u;
-      okr = __shfl_sync(0xffffffffu, okr, 0);
-      tile = __shfl_sync(0xffffffffu, tile, 0);
-      if (!okr || tile < 0) break;
-      int32_t tm, tn;
-      raster_tile(tile, p.tiles_m, p.tiles_n, p.raster_group, tm, tn);
-      bool ok = true;
-#pragma unroll 1
-      for (int cons = 0; cons < NCONS; ++cons) {
-        const uint32_t slot = (NCONS == 2) ? (uint32_t)cons : (i & 1u);
-        const uint32_t apar = (NCONS == 2) ? (i & 1u) : ((i >> 1) & 1u);
-        uint32_t got = 1;
-        if (lane == 0) got = mbar_wait(smem_u32(acc_full + slot), apar, w, WAIT_EPI_ACC_FULL) ? 1u : 0u;
-        got = __shfl_sync(0xffffffffu, got, 0);
-        if (!got) { ok = false; break; }
-        tc_fence_after();
-        const int32_t row0 = tm * Cfg::TILE_M + cons * 128 * CG + (int32_t)rank * 128 + (int32_t)q * 32;
-        const int32_t col_base = tn * WS_BN;
-        const uint32_t tbase = tmem + ((q * 32u) << 16) + slot * 256u;
-#pragma unroll 1
-        for (int ch = 0; ch < NCH; ++ch) {
-          uint32_t v0[32], v1[32];
-          tmem_ld_32x32b_x32(tbase + (uint32_t)(ch * CW), v0);
-          if constexpr (CW == 64) tmem_ld_32x32b_x32(tbase + (uint32_t)(ch * CW + 32), v1);
-          tmem_wait_ld();
-          if (ch == NCH - 1) {
-            // the whole accumulator is in registers: hand it back to the MMA warp
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) {
-              if constexpr (CG == 1) {
-                mbar_arrive(smem_u32(acc_empty + slot));
-              } else {
-                mbar_arrive_cluster(mapa_shared(smem_u32(acc_empty + slot), 0));
-              }
-            }
-          }
-          if constexpr (EPI >= 0) {
-            // bias, activation and residual, in fp32, before the single rounding to C's type
-            const int32_t row = row0 + (int32_t)lane;
-            const int32_t col0 = col_base + ch * CW;
-            apply_epilogue<OutT, 32, EPI>(v0, p, row, col0);
-            if constexpr (CW == 64) apply_epilogue<OutT, 32, EPI>(v1, p, row, col0 + 32);
-          }
-          uint8_t* buf = my_staging + (tog & 1u) * 4096u;
-          if (lane == 0) bulk_wait_group_read<1>();  // the store issued from `buf` two chunks ago is done reading
-          __syncwarp();
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            uint4 val;
-            if constexpr (CW == 32) {
-              val = make_uint4(v0[4 * j], v0[4 * j + 1], v0[4 * j + 2], v0[4 * j + 3]);
-            } else {
-              const uint32_t* src = (j < 4) ? (v0 + 8 * j) : (v1 + 8 * (j - 4));
-              val = make_uint4(pack_bf16x2(src[0], src[1]), pack_bf16x2(src[2], src[3]),
-                               pack_bf16x2(src[4], src[5]), pack_bf16x2(src[6], src[7]));
-            }
-            *reinterpret_cast<uint4*>(buf + sw128_offset(lane, (uint32_t)j)) = val;
-          }
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            const int32_t col0 = col_base + ch * CW;
-            if (row0 < p.M && col0 < p.N) tma_store_2d(&tmC, smem_u32(buf), col0, row0);
-            bulk_commit_group();
-          }
-          ++tog;
-        }
-      }
-      if (!ok) break;
-      if (p.visits != nullptr && q == 0 && lane == 0 && leader) atomicAdd(p.visits + tile, 1);
-    }
-    if (lane == 0) bulk_wait_group<0>();
-  }
-
-  // ---------------------------------------------------------------- teardown
-  __syncwarp();
-  tc_fence_before();
-  __syncthreads();
-  if constexpr (CG == 2) cluster_sync_all();
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc<CG>(tmem, 512);
-  }
-}
-
-template <typename OutT, int CG, int NCONS, int SCHED, int EPI = -1>
-void* ws_kernel_ptr() {
-  return reinterpret_cast<void*>(k_ws<OutT, CG, NCONS, SCHED, EPI>);
-}
 
 template <typename OutT, int CG>
 void* pick_fused(int act) {

@@ -16,10 +16,13 @@ LIB_PATH = os.path.join(HERE, "libdgbgemm.so")
 # gemm_dtype_t
 F16_F32, F16_BF16, BF16_F32, BF16_BF16 = 0, 1, 2, 3
 E4M3_F32, E4M3_BF16, E5M2_F32, E5M2_BF16 = 4, 5, 6, 7
+MXE4M3_F32, MXE4M3_BF16, MXE5M2_F32, MXE5M2_BF16 = 8, 9, 10, 11
 DTYPES = {("f16", "f32"): F16_F32, ("f16", "bf16"): F16_BF16,
           ("bf16", "f32"): BF16_F32, ("bf16", "bf16"): BF16_BF16,
           ("e4m3", "f32"): E4M3_F32, ("e4m3", "bf16"): E4M3_BF16,
-          ("e5m2", "f32"): E5M2_F32, ("e5m2", "bf16"): E5M2_BF16}
+          ("e5m2", "f32"): E5M2_F32, ("e5m2", "bf16"): E5M2_BF16,
+          ("mxe4m3", "f32"): MXE4M3_F32, ("mxe4m3", "bf16"): MXE4M3_BF16,
+          ("mxe5m2", "f32"): MXE5M2_F32, ("mxe5m2", "bf16"): MXE5M2_BF16}
 
 # gemm_status_t
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED_SHAPE, ERR_MISALIGNED, ERR_UNSUPPORTED_DTYPE = 0, 1, 2, 3, 4
@@ -88,6 +91,10 @@ def load():
     lib.gemm_plan_run.restype = i32
     lib.gemm_plan_run_epilogue.argtypes = [p, p, p, p, ctypes.POINTER(Epilogue), p]
     lib.gemm_plan_run_epilogue.restype = i32
+    lib.gemm_plan_run_mx.argtypes = [p, p, p, p, p, p, ctypes.POINTER(Epilogue), p]
+    lib.gemm_plan_run_mx.restype = i32
+    lib.gemm_mx_scale_bytes.argtypes = [i64, i64]
+    lib.gemm_mx_scale_bytes.restype = i64
     lib.gemm_run.argtypes = [i64, i64, i64, p, p, p, i32, p]
     lib.gemm_run.restype = i32
     lib.gemm_run_host.argtypes = [i64, i64, i64, p, p, p, i32, p, p, p, p]
@@ -172,6 +179,26 @@ class Plan:
         _check(st, "gemm_plan_run_epilogue")
         return c
 
+    def run_mx(self, a, b, c, sf_a, sf_b, bias=None, residual=None, act=None, stream=None,
+               scale_a=None, scale_b=None):
+        """Block-scaled C = (X_A . a) @ (X_B . b).T for a plan of an MX dtype: sf_a / sf_b
+        are uint8 CUDA tensors of UE8M0 scales in the tiled layout (mx_scale_bytes(rows, K)
+        bytes each).  With any of bias / residual / act / scale_a / scale_b the fused
+        epilogue runs as in run_epilogue."""
+        e = None
+        if bias is not None or residual is not None or act is not None or scale_a is not None or \
+                scale_b is not None:
+            e = Epilogue()
+            e.bias = None if bias is None else bias.data_ptr()
+            e.residual = None if residual is None else residual.data_ptr()
+            e.activation = int(act or ACT_NONE)
+            e.scale_a = None if scale_a is None else scale_a.data_ptr()
+            e.scale_b = None if scale_b is None else scale_b.data_ptr()
+        st = load().gemm_plan_run_mx(self._h, a.data_ptr(), b.data_ptr(), c.data_ptr(), sf_a.data_ptr(),
+                                     sf_b.data_ptr(), None if e is None else ctypes.byref(e), _stream_ptr(stream))
+        _check(st, "gemm_plan_run_mx")
+        return c
+
     def check(self, stream=None) -> int:
         return load().gemm_check(self._h, _stream_ptr(stream))
 
@@ -205,6 +232,11 @@ def dtype_code(in_dtype, out_dtype) -> int:
     if (i, o) not in DTYPES:
         raise ValueError("unsupported dtype pair %r -> %r" % (i, o))
     return DTYPES[(i, o)]
+
+
+def mx_scale_bytes(rows: int, K: int) -> int:
+    """Bytes of one tiled MX scale array (gemm_mx_scale_bytes)."""
+    return int(load().gemm_mx_scale_bytes(int(rows), int(K)))
 
 
 def gemm_run(M, N, K, a_ptr, b_ptr, c_ptr, dtype, stream_ptr=0) -> int:

@@ -2,7 +2,8 @@
  * gemm.h -- C ABI of the GB300 (sm_103a) dense GEMM library, libdgbgemm.so.
  *
  * Computes C = A * B^T on one GPU:
- *   A  M x K, row-major (K-major), fp16, bf16, or 8-bit float (E4M3 / E5M2)
+ *   A  M x K, row-major (K-major), fp16, bf16, or 8-bit float (E4M3 / E5M2,
+ *      optionally with MX block scales)
  *   B  N x K, row-major (K-major), same type as A
  *   C  M x N, row-major (leading dimension N), fp32 or bf16
  * with fp32 accumulation in Tensor Memory.  This is the tiled GEMM of
@@ -51,7 +52,14 @@ typedef enum {
   GEMM_E4M3_F32 = 4,  /* 8-bit float E4M3 (OCP FP8) in, fp32 out; variants 7-9, K-major */
   GEMM_E4M3_BF16 = 5, /* E4M3 in, bf16 out */
   GEMM_E5M2_F32 = 6,  /* 8-bit float E5M2 in, fp32 out */
-  GEMM_E5M2_BF16 = 7  /* E5M2 in, bf16 out */
+  GEMM_E5M2_BF16 = 7, /* E5M2 in, bf16 out */
+  /* MX block-scaled 8-bit inputs (OCP Microscaling formats MXFP8): every 32
+   * consecutive K elements of a row of A or B share one UE8M0 scale 2^(e-127);
+   * run with gemm_plan_run_mx, which takes the two scale arrays.  Variant 7. */
+  GEMM_MXE4M3_F32 = 8,  /* MXFP8 E4M3 in, fp32 out */
+  GEMM_MXE4M3_BF16 = 9, /* MXFP8 E4M3 in, bf16 out */
+  GEMM_MXE5M2_F32 = 10, /* MXFP8 E5M2 in, fp32 out */
+  GEMM_MXE5M2_BF16 = 11 /* MXFP8 E5M2 in, bf16 out */
 } gemm_dtype_t;
 
 typedef enum {
@@ -182,6 +190,35 @@ typedef struct {
  * GEMM_ERR_UNSUPPORTED_SHAPE.  The epilogue kernel uses the static scheduler. */
 GEMM_API gemm_status_t gemm_plan_run_epilogue(gemm_plan_t plan, const void* A, const void* B, void* C,
                                               const gemm_epilogue_t* epilogue, gemm_stream_t stream);
+
+/* Block-scaled product of a plan made with an MX dtype (GEMM_MXE4M3_* or
+ * GEMM_MXE5M2_*), the low-precision GEMM named among the kernels that decide
+ * MLSys speed ("Modern GPU Programming for MLSys", background section):
+ *
+ *   C[i][j] = epi( sum_k (X_A[i][k/32] * A[i][k]) * (X_B[j][k/32] * B[j][k]) )
+ *
+ * with X = 2^(e - 127) for the UE8M0 byte e (255 is NaN), accumulated in fp32
+ * in Tensor Memory by tcgen05.mma kind::mxf8f6f4.  A, B and C as for
+ * gemm_plan_run (K-major 8-bit operands, K * 1 % 16 == 0).
+ *
+ * scale_a / scale_b are device arrays of UE8M0 bytes for A's M rows and B's N
+ * rows, 16-byte aligned, each in the tiled layout: 512-byte blocks of 128 rows
+ * x 4 scales (128 K elements), block (rb, cb) at byte (rb * ceil(K/128) + cb) *
+ * 512, and inside a block the scale of row r, scale column c at byte
+ * (r % 32) * 16 + ((r / 32) % 4) * 4 + c % 4.  Each array holds
+ * gemm_mx_scale_bytes(rows, K) bytes; bytes of padding rows and of scale
+ * columns past ceil(K/32) are never used.
+ *
+ * epilogue may be NULL (plain rounding to C's type) or a fused epilogue as for
+ * gemm_plan_run_epilogue.  Plans of other dtypes return GEMM_ERR_UNSUPPORTED_DTYPE;
+ * gemm_plan_run / gemm_run on an MX plan or dtype return GEMM_ERR_INVALID_ARG. */
+GEMM_API gemm_status_t gemm_plan_run_mx(gemm_plan_t plan, const void* A, const void* B, void* C,
+                                        const void* scale_a, const void* scale_b,
+                                        const gemm_epilogue_t* epilogue, gemm_stream_t stream);
+
+/* Bytes of one tiled MX scale array for `rows` rows and inner dimension K:
+ * ceil(rows/128) * ceil(K/128) * 512; -1 for rows < 1 or K < 1. */
+GEMM_API int64_t gemm_mx_scale_bytes(int64_t rows, int64_t K);
 
 /* One-shot form: plan (cached per shape, dtype and device) and run. */
 GEMM_API gemm_status_t gemm_run(int64_t M, int64_t N, int64_t K, const void* A, const void* B, void* C,

@@ -315,8 +315,11 @@ int oracle_gemm_mx_rows_f64(int64_t M, int64_t N, int64_t K, const uint8_t* A, c
             if (rows[r] < 0 || rows[r] >= M) return -1;
     }
     const int64_t KS = (K + 31) / 32;
-    double tab[256];
-    for (int b = 0; b < 256; ++b) tab[b] = oracle_widen8((uint8_t)b, in_kind);
+    double tab[256], x8[256];
+    for (int b = 0; b < 256; ++b) {
+        tab[b] = oracle_widen8((uint8_t)b, in_kind);
+        x8[b] = ue8m0((uint8_t)b);
+    }
     set_threads(nthreads);
     int64_t r;
 #pragma omp parallel for schedule(dynamic, 1)
@@ -329,7 +332,7 @@ int oracle_gemm_mx_rows_f64(int64_t M, int64_t N, int64_t K, const uint8_t* A, c
             const uint8_t* sb = SB + j * KS;
             double acc = 0.0, sabs = 0.0;
             for (int64_t k = 0; k < K; ++k) {
-                double p = (ue8m0(sa[k / 32]) * tab[a[k]]) * (ue8m0(sb[k / 32]) * tab[b[k]]);
+                double p = (x8[sa[k / 32]] * tab[a[k]]) * (x8[sb[k / 32]] * tab[b[k]]);
                 acc += p;
                 sabs += fabs(p);
             }

@@ -63,7 +63,7 @@ def test_plan_rejects_bad_sizes_without_a_device(lib):
     assert _plan_status(lib, 16, 16, 0, 0) == gemm.ERR_INVALID_ARG
     assert _plan_status(lib, 1 << 31, 16, 16, 0) == gemm.ERR_INVALID_ARG
     assert _plan_status(lib, 16, 16, 12, 0) == gemm.ERR_UNSUPPORTED_SHAPE   # K % 8 != 0
-    assert _plan_status(lib, 16, 16, 16, 8) == gemm.ERR_UNSUPPORTED_DTYPE
+    assert _plan_status(lib, 16, 16, 16, 12) == gemm.ERR_UNSUPPORTED_DTYPE
     assert _plan_status(lib, 16, 16, 16, -1) == gemm.ERR_UNSUPPORTED_DTYPE
 
 
@@ -82,6 +82,25 @@ def test_fp8_row_pitch_rule(lib):
                         gemm.make_opts(variant=gemm.S8, layout=gemm.LAYOUT_A_MN)) == gemm.ERR_UNSUPPORTED_SHAPE
     assert gemm.dtype_code("e4m3", "f32") == gemm.E4M3_F32
     assert gemm.dtype_code(torch.float8_e5m2, torch.bfloat16) == gemm.E5M2_BF16
+
+
+def test_mx_rules(lib):
+    for dt in (gemm.MXE4M3_F32, gemm.MXE4M3_BF16, gemm.MXE5M2_F32, gemm.MXE5M2_BF16):
+        assert _plan_status(lib, 64, 64, 24, dt) == gemm.ERR_UNSUPPORTED_SHAPE
+        # block-scaled inputs run on variant 7 only, K-major only
+        for v in (gemm.S3, gemm.S8, gemm.S9, gemm.GEMV):
+            assert _plan_status(lib, 256, 256, 256, dt, gemm.make_opts(variant=v)) == gemm.ERR_UNSUPPORTED_SHAPE
+        assert _plan_status(lib, 256, 256, 256, dt, gemm.make_opts(variant=gemm.S7, layout=gemm.LAYOUT_A_MN)) == \
+            gemm.ERR_UNSUPPORTED_SHAPE
+        # the one-shot entry points have no scale arguments
+        assert lib.gemm_run(64, 64, 64, 0x1000, 0x2000, 0x3000, dt, None) == gemm.ERR_INVALID_ARG
+    assert lib.gemm_plan_run_mx(None, 0x1000, 0x2000, 0x3000, 0x4000, 0x5000, None, None) == gemm.ERR_INVALID_ARG
+    assert gemm.dtype_code("mxe5m2", "bf16") == gemm.MXE5M2_BF16
+    assert gemm.mx_scale_bytes(1, 1) == 512
+    assert gemm.mx_scale_bytes(128, 128) == 512
+    assert gemm.mx_scale_bytes(129, 129) == 4 * 512
+    assert gemm.mx_scale_bytes(8192, 8192) == 64 * 64 * 512
+    assert gemm.mx_scale_bytes(0, 128) == -1
 
 
 def test_epilogue_struct_layout_matches_the_header():
