@@ -175,6 +175,10 @@ def bench_gemm(w: inputs.Workload, steps: int, warmup: int, dev, dist_barrier, v
     from dense_gemm_blackwell_sm_gb300 import gemm
     code = gemm.dtype_code(w.in_dtype, w.out_dtype)
     a, b = inputs.workload_operands(w)
+    mx = w.in_dtype in (inputs.MXE4M3, inputs.MXE5M2)
+    if mx:   # block scales in the kernels' tiled layout, resident like the operands
+        sfa, sfb = inputs.workload_mx_scales(w)
+        sfa, sfb = inputs.mx_tile_scales(sfa, w.K).to(dev), inputs.mx_tile_scales(sfb, w.K).to(dev)
     sets = []
     for s in range(2):   # two operand sets, alternated: inputs are also larger than L2
         sets.append((a.to(dev), b.to(dev), torch.empty((w.M, w.N), device=dev, dtype=inputs.torch_dtype(w.out_dtype))))
@@ -183,17 +187,20 @@ def bench_gemm(w: inputs.Workload, steps: int, warmup: int, dev, dist_barrier, v
     sp = stream.cuda_stream
     ptrs = [(x.data_ptr(), y.data_ptr(), z.data_ptr()) for x, y, z in sets]
     epi = None
+    lib = gemm.load()
+    import ctypes
     if epilogue_act is not None:
         bias = torch.randn(w.N, device=dev, dtype=torch.float32)
         res = torch.randn(w.M, w.N, device=dev).to(inputs.torch_dtype(w.out_dtype))
         epi = gemm.Epilogue()
         epi.bias, epi.residual, epi.activation = bias.data_ptr(), res.data_ptr(), int(epilogue_act)
-        lib = gemm.load()
-        import ctypes
 
     def step(i):
         pa, pb, pc = ptrs[i & 1]
-        if epi is None:
+        if mx:
+            st = lib.gemm_plan_run_mx(plan._h, pa, pb, pc, sfa.data_ptr(), sfb.data_ptr(),
+                                      None if epi is None else ctypes.byref(epi), sp)
+        elif epi is None:
             st = plan.run_ptr(pa, pb, pc, sp)
         else:
             st = lib.gemm_plan_run_epilogue(plan._h, pa, pb, pc, ctypes.byref(epi), sp)
@@ -220,10 +227,16 @@ def bench_gemm(w: inputs.Workload, steps: int, warmup: int, dev, dist_barrier, v
 
 
 def bench_gemm_e2e(w: inputs.Workload, steps: int, dev) -> dict:
-    """The same GEMM through gemm_run_host: pinned host operands in, host result out."""
+    """The same GEMM through gemm_run_host: pinned host operands in, host result out.
+    Block-scaled workloads (no host entry point) copy operands and scales in with
+    torch from pinned memory, run gemm_plan_run_mx and copy C back, every step."""
     from dense_gemm_blackwell_sm_gb300 import gemm
     code = gemm.dtype_code(w.in_dtype, w.out_dtype)
     a, b = inputs.workload_operands(w)
+    ib = 1 if w.in_dtype in inputs.EIGHT_BIT else 2
+    ob = 4 if w.out_dtype == "f32" else 2
+    if w.in_dtype in (inputs.MXE4M3, inputs.MXE5M2):
+        return _bench_mx_e2e(w, a, b, code, steps, dev, ib, ob)
     ah, bh = a.pin_memory(), b.pin_memory()
     ch = torch.empty((w.M, w.N), dtype=inputs.torch_dtype(w.out_dtype)).pin_memory()
     da, db = torch.empty_like(a, device=dev), torch.empty_like(b, device=dev)
@@ -241,8 +254,33 @@ def bench_gemm_e2e(w: inputs.Workload, steps: int, dev) -> dict:
     for _ in range(steps):
         once()   # synchronises the stream itself
     secs = time.perf_counter() - t0
-    ob = 4 if w.out_dtype == "f32" else 2
-    return {"seconds": secs, "steps": steps, "h2d": 2 * (w.M * w.K + w.N * w.K), "d2h": ob * w.M * w.N}
+    return {"seconds": secs, "steps": steps, "h2d": ib * (w.M * w.K + w.N * w.K), "d2h": ob * w.M * w.N}
+
+
+def _bench_mx_e2e(w, a, b, code, steps, dev, ib, ob) -> dict:
+    from dense_gemm_blackwell_sm_gb300 import gemm
+    sfa, sfb = inputs.workload_mx_scales(w)
+    host = [x.pin_memory() for x in (a, b, inputs.mx_tile_scales(sfa, w.K), inputs.mx_tile_scales(sfb, w.K))]
+    devs = [torch.empty_like(x, device=dev) for x in host]
+    ch = torch.empty((w.M, w.N), dtype=inputs.torch_dtype(w.out_dtype)).pin_memory()
+    dc = torch.empty((w.M, w.N), device=dev, dtype=inputs.torch_dtype(w.out_dtype))
+    plan = gemm.Plan(w.M, w.N, w.K, code)
+
+    def once():
+        for d, h in zip(devs, host):
+            d.copy_(h, non_blocking=True)
+        plan.run_mx(devs[0], devs[1], dc, devs[2], devs[3])
+        ch.copy_(dc, non_blocking=True)
+        torch.cuda.synchronize(dev)
+
+    once()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        once()
+    secs = time.perf_counter() - t0
+    plan.destroy()
+    return {"seconds": secs, "steps": steps, "h2d": sum(x.numel() * x.element_size() for x in host),
+            "d2h": ob * w.M * w.N}
 
 
 def bench_gemv(w: inputs.Workload, steps: int, warmup: int, dev, flags: int = 0) -> dict:
@@ -291,13 +329,19 @@ def cpu_oracle_rate(w: inputs.Workload, budget_s: float = 12.0) -> dict:
     import oracle
     oracle.build()
     a, b = inputs.workload_operands(w)
+    mx = w.in_dtype in (inputs.MXE4M3, inputs.MXE5M2)
+    if mx:
+        sfa, sfb = inputs.workload_mx_scales(w)
     threads = oracle.max_threads()
     rng = np.random.default_rng(0)
     rows_done, t_spent, batch = 0, 0.0, max(1, threads)
     while t_spent < budget_s and rows_done < w.M:
         rows = rng.choice(w.M, size=min(batch, w.M - rows_done), replace=False)
         t0 = time.perf_counter()
-        oracle.gemm_rows(a, b, rows, nthreads=threads)
+        if mx:
+            oracle.gemm_mx(a, b, sfa, sfb, rows=rows, nthreads=threads)
+        else:
+            oracle.gemm_rows(a, b, rows, nthreads=threads)
         t_spent += time.perf_counter() - t0
         rows_done += len(rows)
         if t_spent < budget_s / 4:
@@ -417,11 +461,11 @@ def main(argv=None):
     # fp16 and bf16 run at the same dense Tensor Core rate; 8-bit floats at twice it
     # (the nominal fp8 / bf16 dense ratio, 4.5 / 2.25 PFLOP/s, times the measured bf16 peak)
     peak = float(peaks.get(peak_key, FALLBACK[peak_key]))
-    if w.in_dtype in (inputs.E4M3, inputs.E5M2):
+    if w.in_dtype in inputs.EIGHT_BIT:
         peak *= 2.0
         peak_key += " x 2 (fp8)"
     achieved = w.flops / per_launch / 1e12
-    stated = STATED_PEAK_TFLOPS * (2 if w.in_dtype in (inputs.E4M3, inputs.E5M2) else 1)
+    stated = STATED_PEAK_TFLOPS * (2 if w.in_dtype in inputs.EIGHT_BIT else 1)
     line = {
         "metric": METRIC, "value": round(tflops, 3), "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(tmax / args.steps * 1e3, 4),
@@ -465,6 +509,12 @@ def main(argv=None):
         also[w8.name] = {"tflops": round(t8, 3), "frac_of_fp8_peak": round(t8 / fp8_peak, 4),
                          "fp8_peak": fp8_peak, "variant": r8["info"]["variant_name"],
                          "peak_note": "measured bf16 burst x 2 (nominal fp8 / bf16 dense ratio 4.5 / 2.25)"}
+        wm = inputs.WORKLOADS["mxfp8_8192_e4m3_bf16"]
+        rm = bench_gemm(wm, 100, 10, dev, lambda: None)
+        tm = wm.flops / rm["per_launch_s"] / 1e12
+        also[wm.name] = {"tflops": round(tm, 3), "frac_of_fp8_peak": round(tm / fp8_peak, 4),
+                         "fp8_peak": fp8_peak, "variant": rm["info"]["variant_name"],
+                         "note": "MX block scaling: UE8M0 scale per 32 K elements, tcgen05.mma kind::mxf8f6f4"}
         w4 = inputs.WORKLOADS["llm_proj_8192x14336x4096_bf16_bf16"]
         r4 = bench_gemm(w4, 50, 5, dev, lambda: None)
         also[w4.name] = {"tflops": round(w4.flops / r4["per_launch_s"] / 1e12, 3),

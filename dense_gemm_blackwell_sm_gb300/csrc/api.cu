@@ -199,7 +199,8 @@ gemm_status_t prepare_launch(gemm_plan_s* p) {
       // N / 8 (17-22), scale type UE8M0 (bit 23), M / 16 (24-28); the scale-byte
       // selectors (B: bits 4-5, A: bits 29-30) are added per MMA by the kernel
       const uint32_t fmt = p->in_e5m2 ? 1u : 0u;
-      k.idesc = (fmt << 7) | (fmt << 10) | ((uint32_t)(256 >> 3) << 17) | (1u << 23) | ((uint32_t)(128 >> 4) << 24);
+      k.idesc = (fmt << 7) | (fmt << 10) | ((uint32_t)(256 >> 3) << 17) | (1u << 23) |
+                ((uint32_t)((128 * p->cg) >> 4) << 24);
       k.mma_kind = 2;
       k.bk = 128;
     } else if (p->in_f8) {
@@ -220,7 +221,7 @@ gemm_status_t prepare_launch(gemm_plan_s* p) {
     } else if (v == GEMM_VARIANT_S6_PERSISTENT) {
       e = spec_step6(p->sched - 1, p->stages, p->out_f32, p->grid_units, &p->spec);
     } else if (p->in_mx) {
-      e = spec_mx(p->sched - 1, p->out_f32, p->stages, p->grid_units, &p->spec);
+      e = spec_mx(p->cg, p->sched - 1, p->out_f32, p->stages, p->grid_units, &p->spec);
     } else {
       e = spec_ws(p->cg, p->consumers, p->sched - 1, p->out_f32, p->stages, p->grid_units, &p->spec);
     }
@@ -249,9 +250,13 @@ gemm_status_t build_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, co
   if (st != GEMM_OK && !o.variant) return st;
   int variant = o.variant ? o.variant : auto_variant(M, N, K, dtype, sms);
   if (is_mx(dtype)) {
-    // block-scaled inputs run on step 7's one-CTA tile only
-    if (o.variant && o.variant != GEMM_VARIANT_S7_WARP_SPECIALIZED) return GEMM_ERR_UNSUPPORTED_SHAPE;
-    variant = GEMM_VARIANT_S7_WARP_SPECIALIZED;
+    // block-scaled inputs run on step 7's one-CTA tile or step 8's CTA pair (one consumer)
+    if (o.variant && o.variant != GEMM_VARIANT_S7_WARP_SPECIALIZED && o.variant != GEMM_VARIANT_S8_CTA_PAIR)
+      return GEMM_ERR_UNSUPPORTED_SHAPE;
+    if (!o.variant) {
+      const int64_t tn = (N + 255) / 256, pairs = std::max(1, sms / 2);
+      variant = (((M + 255) / 256) * tn >= pairs) ? GEMM_VARIANT_S8_CTA_PAIR : GEMM_VARIANT_S7_WARP_SPECIALIZED;
+    }
   }
   if (is_f8(dtype)) {
     // 8-bit inputs run on the warp-specialised kernels only, K-major
@@ -327,8 +332,8 @@ gemm_status_t build_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, co
     p->tile_n = sh.tile_n;
     p->smem = ws_smem_bytes(p->cg, p->consumers, p->stages);
     if (p->in_mx) {
-      p->stages = o.stages ? std::min<int>(o.stages, mx_max_stages()) : mx_max_stages();
-      p->smem = mx_smem_bytes(p->stages);
+      p->stages = o.stages ? std::min<int>(o.stages, mx_max_stages(p->cg)) : mx_max_stages(p->cg);
+      p->smem = mx_smem_bytes(p->cg, p->stages);
     }
   } else if (variant == GEMM_VARIANT_S6_PERSISTENT) {
     p->smem = step6_smem_bytes(p->stages);
@@ -354,8 +359,9 @@ gemm_status_t build_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, co
     if (o.max_ctas && p->sched != GEMM_SCHED_CLC) units = std::min(units, (int)o.max_ctas);
     p->grid_units = units;
   } else if (variant >= GEMM_VARIANT_S7_WARP_SPECIALIZED && variant <= GEMM_VARIANT_S9_TWO_CONSUMERS) {
-    // (the MX kernel's shared memory also allows one CTA per SM)
-    int active = p->in_mx ? sms : ws_max_active_clusters(p->cg, p->consumers, p->sched - 1, p->out_f32, p->stages);
+    // (the MX kernels' shared memory also allows one CTA per SM)
+    int active = p->in_mx ? sms / p->cg
+                          : ws_max_active_clusters(p->cg, p->consumers, p->sched - 1, p->out_f32, p->stages);
     if (active < 1) active = std::max(1, sms / p->cg);
     int units = (p->sched == GEMM_SCHED_CLC) ? tiles : std::min(tiles, active);
     if (o.max_ctas && p->sched != GEMM_SCHED_CLC) units = std::max(1, std::min(units, (int)o.max_ctas));
@@ -519,7 +525,8 @@ gemm_status_t run_with_epilogue(gemm_plan_s* plan, const void* A, const void* B,
       // the block-scaled plan already runs one consumer on one CTA
       plan->epi_stages = plan->stages;
       plan->epi_tiles_m = plan->tiles_m;
-      e = spec_mx(0, plan->out_f32, plan->stages, plan->grid_units, &plan->spec_epi[act], act);
+      e = spec_mx(plan->cg, 0, plan->out_f32, plan->stages, std::min(plan->grid_units, plan->tiles_m * plan->tiles_n),
+                  &plan->spec_epi[act], act);
     } else {
       // The fused epilogue does real arithmetic per element, so it must hide behind
       // the MMAs: a step-9 plan (both TMEM accumulators busy) runs it with one

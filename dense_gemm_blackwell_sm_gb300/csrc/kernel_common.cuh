@@ -26,6 +26,7 @@ enum : uint32_t {
   WAIT_LADDER_MMA = 0x7108u,
   WAIT_LADDER_TMA = 0x7109u,
   WAIT_DRAIN = 0x710Au,
+  WAIT_MX_FORWARD = 0x710Bu,
 };
 
 // test hook: the producer leaves out one TMA load of the first stage while

@@ -1,52 +1,59 @@
-// kernels_mx.cu -- instantiations of the step-7 kernel (one CTA, 128x256 tile,
-// one MMA consumer) for 8-bit float inputs with MX block scales (a UE8M0 scale
-// per 32 consecutive K elements of every row of A and B, tcgen05.mma
-// kind::mxf8f6f4), with the plain or the fused writeback; the kernel itself is
-// in kernels_ws.cuh.
+// kernels_mx.cu -- instantiations of the step-7 kernel (one CTA, 128x256 tile)
+// and the step-8 kernel (CTA pair, 256x256 tile), one MMA consumer each, for
+// 8-bit float inputs with MX block scales (a UE8M0 scale per 32 consecutive K
+// elements of every row of A and B, tcgen05.mma kind::mxf8f6f4), with the
+// plain or the fused writeback; the kernel itself is in kernels_ws.cuh.
 #include "kernels_ws.cuh"
 
 namespace dgb {
 
 namespace {
 
-template <typename OutT>
+template <typename OutT, int CG>
 void* pick_mx(int sched, int fused_act) {
   switch (fused_act) {
-    case EPI_ACT_NONE: return ws_kernel_ptr<OutT, 1, 1, SCHED_STATIC, EPI_ACT_NONE, true>();
-    case EPI_ACT_RELU: return ws_kernel_ptr<OutT, 1, 1, SCHED_STATIC, EPI_ACT_RELU, true>();
-    case EPI_ACT_SILU: return ws_kernel_ptr<OutT, 1, 1, SCHED_STATIC, EPI_ACT_SILU, true>();
-    case EPI_ACT_GELU_TANH: return ws_kernel_ptr<OutT, 1, 1, SCHED_STATIC, EPI_ACT_GELU_TANH, true>();
-    case EPI_ACT_GELU_ERF: return ws_kernel_ptr<OutT, 1, 1, SCHED_STATIC, EPI_ACT_GELU_ERF, true>();
+    case EPI_ACT_NONE: return ws_kernel_ptr<OutT, CG, 1, SCHED_STATIC, EPI_ACT_NONE, true>();
+    case EPI_ACT_RELU: return ws_kernel_ptr<OutT, CG, 1, SCHED_STATIC, EPI_ACT_RELU, true>();
+    case EPI_ACT_SILU: return ws_kernel_ptr<OutT, CG, 1, SCHED_STATIC, EPI_ACT_SILU, true>();
+    case EPI_ACT_GELU_TANH: return ws_kernel_ptr<OutT, CG, 1, SCHED_STATIC, EPI_ACT_GELU_TANH, true>();
+    case EPI_ACT_GELU_ERF: return ws_kernel_ptr<OutT, CG, 1, SCHED_STATIC, EPI_ACT_GELU_ERF, true>();
     default: break;
   }
-  if (sched == SCHED_ATOMIC) return ws_kernel_ptr<OutT, 1, 1, SCHED_ATOMIC, -1, true>();
-  if (sched == SCHED_CLC) return ws_kernel_ptr<OutT, 1, 1, SCHED_CLC, -1, true>();
-  return ws_kernel_ptr<OutT, 1, 1, SCHED_STATIC, -1, true>();
+  if (sched == SCHED_ATOMIC) return ws_kernel_ptr<OutT, CG, 1, SCHED_ATOMIC, -1, true>();
+  if (sched == SCHED_CLC) return ws_kernel_ptr<OutT, CG, 1, SCHED_CLC, -1, true>();
+  return ws_kernel_ptr<OutT, CG, 1, SCHED_STATIC, -1, true>();
+}
+
+void* mx_kernel(int cg, int sched, bool out_f32, int fused_act) {
+  if (cg == 1) return out_f32 ? pick_mx<float, 1>(sched, fused_act) : pick_mx<__nv_bfloat16, 1>(sched, fused_act);
+  if (cg == 2) return out_f32 ? pick_mx<float, 2>(sched, fused_act) : pick_mx<__nv_bfloat16, 2>(sched, fused_act);
+  return nullptr;
 }
 
 }  // namespace
 
-size_t mx_smem_bytes(int stages) {
-  return 1024 + (size_t)stages * (WsCfg<1, 1>::STAGE + WsCfg<1, 1>::MX_BYTES) + WS_STAGING / 2 + WS_CTRL;
+size_t mx_smem_bytes(int cg, int stages) {
+  const size_t stage = (cg == 1) ? WsCfg<1, 1>::STAGE + WsCfg<1, 1>::MX_BYTES : WsCfg<2, 1>::STAGE + WsCfg<2, 1>::MX_BYTES;
+  return 1024 + (size_t)stages * stage + WS_STAGING / 2 + WS_CTRL;
 }
 
-int mx_max_stages() {
+int mx_max_stages(int cg) {
   int s = WS_MAX_STAGES;
-  while (s > 1 && mx_smem_bytes(s) > WS_SMEM_LIMIT) --s;
+  while (s > 1 && mx_smem_bytes(cg, s) > WS_SMEM_LIMIT) --s;
   return s;
 }
 
-cudaError_t spec_mx(int sched, bool out_f32, int stages, int ctas, LaunchSpec* out, int fused_act) {
-  void* k = out_f32 ? pick_mx<float>(sched, fused_act) : pick_mx<__nv_bfloat16>(sched, fused_act);
-  if (!k || stages < 1 || stages > mx_max_stages()) return cudaErrorInvalidValue;
-  const size_t smem = mx_smem_bytes(stages);
+cudaError_t spec_mx(int cg, int sched, bool out_f32, int stages, int clusters, LaunchSpec* out, int fused_act) {
+  void* k = mx_kernel(cg, sched, out_f32, fused_act);
+  if (!k || stages < 1 || stages > mx_max_stages(cg)) return cudaErrorInvalidValue;
+  const size_t smem = mx_smem_bytes(cg, stages);
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   out->func = k;
-  out->grid = dim3((unsigned)ctas, 1, 1);
+  out->grid = dim3((unsigned)(clusters * cg), 1, 1);
   out->block = dim3(WS_THREADS, 1, 1);
   out->smem = smem;
-  out->cluster = 1;
+  out->cluster = (unsigned)cg;
   out->kind = ARGS_ABC_K;
   return cudaSuccess;
 }

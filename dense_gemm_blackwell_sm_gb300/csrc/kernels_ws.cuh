@@ -29,13 +29,17 @@
 // between consecutive tiles (the writeback of tile i overlaps the MMAs of
 // tile i+1); step 9 gives one to each consumer.
 //
-// MX block scaling (MX template flag, one CTA, one consumer): each stage also
-// brings the UE8M0 scales of its 128 K-elements (one 512-byte block for the
-// CTA's 128 rows of A, two for its 256 rows of B) into shared memory with plain
-// bulk copies; the MMA thread moves them into TMEM with tcgen05.cp and issues
-// the block-scaled MMA.  The scales take TMEM columns 256 and up, so the tile
-// keeps a single accumulator, and the writeback stages through one 4 KB buffer
-// per warp instead of two to leave shared memory for the scale blocks.
+// MX block scaling (MX template flag, one consumer, one CTA or a CTA pair): each
+// stage also brings the UE8M0 scales of its 128 K-elements (one 512-byte block
+// for the CTA's 128 rows of A, two for the tile's 256 rows of B) into shared
+// memory with plain bulk copies; the MMA thread moves them into TMEM with
+// tcgen05.cp and issues the block-scaled MMA.  In a pair each CTA holds the
+// scales of its own A rows and of all the tile's B rows; the second CTA's
+// scale copies complete on its own barrier, and its otherwise idle warp 1
+// forwards that completion to the leader's full barrier.  The scales take TMEM
+// columns 256 and up, so the tile keeps a single accumulator, and the writeback
+// stages through one 4 KB buffer per warp instead of two to leave shared
+// memory for the scale blocks.
 //
 // In a CTA pair, each CTA loads its own 128 rows of A and its own 128 rows of B
 // (the pair MMA splits A along M and B along N) with the cta_group::2 TMA form,
@@ -73,8 +77,9 @@ struct WsCfg {
   // arrivals that free one tile-ring slot: producer + 4 writeback warps in
   // every CTA of the cluster, plus the leader's MMA consumers
   static constexpr uint32_t RING_CONSUMERS = (uint32_t)(CG * 5 + NCONS);
-  // MX scale blocks per stage: one for A's 128 rows, B_ROWS / 128 for B
-  static constexpr uint32_t MX_BYTES = MX_BLOCK * (1u + (uint32_t)B_ROWS / 128u);
+  // MX scale blocks per stage and CTA: one for the CTA's 128 rows of A, two for
+  // the tile's 256 rows of B
+  static constexpr uint32_t MX_BYTES = MX_BLOCK * 3u;
 };
 
 // EPI < 0: plain writeback; EPI >= 0: fused epilogue with activation EPI.
@@ -84,7 +89,10 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
     k_ws(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
          const __grid_constant__ CUtensorMap tmC, KParams p) {
   using Cfg = WsCfg<CG, NCONS>;
-  static_assert(!MX || (CG == 1 && NCONS == 1), "MX block scaling runs on one CTA with one consumer");
+  static_assert(!MX || NCONS == 1, "MX block scaling runs with one MMA consumer");
+  constexpr bool MX_PAIR = MX && CG == 2;
+  // the forwarding warp of the second CTA also takes tile ids from the ring
+  constexpr uint32_t RING_CONS = Cfg::RING_CONSUMERS + (MX_PAIR ? 1u : 0u);
   constexpr uint32_t STAGING = MX ? WS_STAGING / 2 : WS_STAGING;
   constexpr uint32_t WARP_STAGING = STAGING / 4;
   constexpr int CW = (sizeof(OutT) == 4) ? 32 : 64;  // output columns per 128-byte staging row
@@ -105,6 +113,7 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
   uint64_t* ring_empty = bars + 24;            // [4]  roles -> scheduler
   uint64_t* clc_bar = bars + 28;
   uint64_t* drain_bar = bars + 29;
+  uint64_t* sf_full = bars + 36;               // [8]  scale copies of the second CTA (MX pair)
   uint32_t* clc_resp = reinterpret_cast<uint32_t*>(bars + 30);   // 16 B, 16-aligned
   volatile int32_t* ring_tile = reinterpret_cast<volatile int32_t*>(clc_resp + 4);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(clc_resp + 4 + WS_RING);
@@ -117,8 +126,10 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(smem_u32(full + s), 1);
+      // MX pair: the leader's producer plus the second CTA's forwarded scale arrival
+      mbar_init(smem_u32(full + s), MX_PAIR ? 2 : 1);
       mbar_init(smem_u32(empty + s), NCONS);
+      if constexpr (MX_PAIR) mbar_init(smem_u32(sf_full + s), 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(acc_full + i), 1);
@@ -126,7 +137,7 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
     }
     for (int i = 0; i < WS_RING; ++i) {
       mbar_init(smem_u32(ring_full + i), 1);
-      mbar_init(smem_u32(ring_empty + i), Cfg::RING_CONSUMERS);
+      mbar_init(smem_u32(ring_empty + i), RING_CONS);
     }
     mbar_init(smem_u32(clc_bar), 1);
     mbar_init(smem_u32(drain_bar), NCONS);
@@ -242,8 +253,10 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
           const uint32_t fb = smem_u32(full + stage);
           // MX: scale blocks of B rows at or past N are not in the scale array; skip them
           int32_t mx_bblocks = 0;
-          if constexpr (MX) mx_bblocks = min(Cfg::B_ROWS / 128, (p.N + 127) / 128 - n_cta / 128);
-          if (leader) mbar_arrive_expect_tx(fb, Cfg::STAGE * CG + (MX ? MX_BLOCK * (1u + (uint32_t)mx_bblocks) : 0u));
+          const int32_t n_tile = tn * WS_BN;
+          if constexpr (MX) mx_bblocks = min(2, (p.N + 127) / 128 - n_tile / 128);
+          const uint32_t mx_tx = MX ? MX_BLOCK * (1u + (uint32_t)mx_bblocks) : 0u;
+          if (leader) mbar_arrive_expect_tx(fb, Cfg::STAGE * CG + mx_tx);
           uint8_t* st = ring + (size_t)stage * Cfg::STAGE;
 #pragma unroll
           for (int c = 0; c < NCONS; ++c) {
@@ -283,12 +296,18 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
             tma_load_2d_pair(smem_u32(bdst), &tmB, mapa_shared(fb, 0), kb * BKE, n_cta);
           }
           if constexpr (MX) {
-            // tiled scale layout: block (row block, K block) at ((row block) * KB + kb) * 512
+            // tiled scale layout: block (row block, K block) at ((row block) * KB + kb) * 512.
+            // The second CTA of a pair counts its copies on its own barrier.
+            uint32_t sb_bar = fb;
+            if (MX_PAIR && !leader) {
+              sb_bar = smem_u32(sf_full + stage);
+              mbar_arrive_expect_tx(sb_bar, mx_tx);
+            }
             uint8_t* sd = mx_ring + (size_t)stage * Cfg::MX_BYTES;
-            bulk_load(smem_u32(sd), p.sfa + ((size_t)(m_cta / 128) * KB + kb) * MX_BLOCK, MX_BLOCK, fb);
+            bulk_load(smem_u32(sd), p.sfa + ((size_t)(m_cta / 128) * KB + kb) * MX_BLOCK, MX_BLOCK, sb_bar);
             for (int32_t h = 0; h < mx_bblocks; ++h)
-              bulk_load(smem_u32(sd + MX_BLOCK * (1 + h)), p.sfb + ((size_t)(n_cta / 128 + h) * KB + kb) * MX_BLOCK,
-                        MX_BLOCK, fb);
+              bulk_load(smem_u32(sd + MX_BLOCK * (1 + h)), p.sfb + ((size_t)(n_tile / 128 + h) * KB + kb) * MX_BLOCK,
+                        MX_BLOCK, sb_bar);
           }
           if (++stage == (uint32_t)S) { stage = 0; sphase ^= 1u; }
         }
@@ -328,17 +347,17 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
             // rows into 4 columns, B's 256 rows into 8
             const uint32_t sft = tmem + MX_TMEM_COL + stage * MX_TMEM_SLOT;
             const uint32_t sfs = smem_u32(mx_ring + (size_t)stage * Cfg::MX_BYTES);
-            tmem_cp_32x128b_x4(sft, sdesc_rows16(sfs));
-            tmem_cp_32x128b_x4(sft + 4, sdesc_rows16(sfs + MX_BLOCK));
-            tmem_cp_32x128b_x4(sft + 8, sdesc_rows16(sfs + 2 * MX_BLOCK));
+            tmem_cp_32x128b_x4<CG>(sft, sdesc_rows16(sfs));
+            tmem_cp_32x128b_x4<CG>(sft + 4, sdesc_rows16(sfs + MX_BLOCK));
+            tmem_cp_32x128b_x4<CG>(sft + 8, sdesc_rows16(sfs + 2 * MX_BLOCK));
             // byte k of each scale word belongs to the k-th 32-element K block; blocks
             // wholly past K are not issued (their scale bytes are padding)
             const int32_t rem = p.K - kb * BKE;
 #pragma unroll
             for (int k = 0; k < 4; ++k)
               if (k * 32 < rem)
-                mma_mxf8f6f4(d, ad + 2 * k, bd + 2 * k, p.idesc | ((uint32_t)k << 4) | ((uint32_t)k << 29), sft,
-                             sft + 4, (kb | k) != 0);
+                mma_mxf8f6f4<CG>(d, ad + 2 * k, bd + 2 * k, p.idesc | ((uint32_t)k << 4) | ((uint32_t)k << 29), sft,
+                                 sft + 4, (kb | k) != 0);
           } else if (f8) {
 #pragma unroll
             for (int k = 0; k < 4; ++k)
@@ -366,6 +385,21 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
       mma_commit_cg<CG>(smem_u32(drain_bar));
       const WaitCtl wd{zero_word, p.status, p.timeout_ns, 0};
       mbar_wait(smem_u32(drain_bar), 0, wd, WAIT_DRAIN);
+    }
+  } else if (MX_PAIR && warp == 1) {
+    // ------------------------------------ scale forwarding (second CTA, MX pair)
+    if (lane == 0) {
+      uint32_t stage = 0, sphase = 0;
+      bool ok = true;
+      for (uint32_t i = 0; ok; ++i) {
+        int32_t tile;
+        if (!ring_get(i, tile) || tile < 0) break;
+        for (int32_t kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait(smem_u32(sf_full + stage), sphase, w, WAIT_MX_FORWARD)) { ok = false; break; }
+          mbar_arrive_cluster(mapa_shared(smem_u32(full + stage), 0));
+          if (++stage == (uint32_t)S) { stage = 0; sphase ^= 1u; }
+        }
+      }
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ writeback

@@ -64,11 +64,13 @@ int ws_max_active_clusters(int cg, int consumers, int sched, bool out_f32, int s
 cudaError_t spec_ws(int cg, int consumers, int sched, bool out_f32, int stages, int clusters, LaunchSpec* out,
                     int fused_act = -1);
 
-// step 7 with MX block scales (8-bit inputs, UE8M0 scale per 32 K elements):
-// one CTA per 128x256 tile, one consumer, a single TMEM accumulator
-size_t mx_smem_bytes(int stages);
-int mx_max_stages();
-cudaError_t spec_mx(int sched, bool out_f32, int stages, int ctas, LaunchSpec* out, int fused_act = -1);
+// steps 7 and 8 with MX block scales (8-bit inputs, UE8M0 scale per 32 K
+// elements): cg = 1 (one CTA per 128x256 tile) or 2 (CTA pair, 256x256), one
+// consumer, a single TMEM accumulator
+size_t mx_smem_bytes(int cg, int stages);
+int mx_max_stages(int cg);
+cudaError_t spec_mx(int cg, int sched, bool out_f32, int stages, int clusters, LaunchSpec* out,
+                    int fused_act = -1);
 
 // decode GEMV, C (M x N) = X (M x K) * B^T for M <= 16, on CUDA cores
 struct GemvParams {

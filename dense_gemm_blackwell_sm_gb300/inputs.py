@@ -26,9 +26,13 @@ BF16 = "bf16"
 F32 = "f32"
 E4M3 = "e4m3"
 E5M2 = "e5m2"
+MXE4M3 = "mxe4m3"   # E4M3 elements with a UE8M0 scale per 32 K elements
+MXE5M2 = "mxe5m2"
 
 _TORCH = {F16: torch.float16, BF16: torch.bfloat16, F32: torch.float32,
-          E4M3: torch.float8_e4m3fn, E5M2: torch.float8_e5m2}
+          E4M3: torch.float8_e4m3fn, E5M2: torch.float8_e5m2,
+          MXE4M3: torch.float8_e4m3fn, MXE5M2: torch.float8_e5m2}
+EIGHT_BIT = (E4M3, E5M2, MXE4M3, MXE5M2)
 
 
 @dataclasses.dataclass(frozen=True)
@@ -37,7 +41,7 @@ class Workload:
     M: int
     N: int
     K: int
-    in_dtype: str          # "f16" | "bf16" | "e4m3" | "e5m2"
+    in_dtype: str          # "f16" | "bf16" | "e4m3" | "e5m2" | "mxe4m3" | "mxe5m2"
     out_dtype: str         # "f32" | "bf16"
     dist_a: tuple          # ("uniform",) | ("normal", sigma) | ("normal_rsqrt_k",)
     dist_b: tuple
@@ -49,9 +53,10 @@ class Workload:
 
     @property
     def algorithmic_bytes(self) -> int:
-        ib = 1 if self.in_dtype in (E4M3, E5M2) else 2
+        ib = 1 if self.in_dtype in EIGHT_BIT else 2
         ob = 4 if self.out_dtype == F32 else 2
-        return ib * (self.M * self.K + self.N * self.K) + ob * self.M * self.N
+        sc = ((self.M + self.N) * ((self.K + 31) // 32)) if self.in_dtype in (MXE4M3, MXE5M2) else 0
+        return ib * (self.M * self.K + self.N * self.K) + ob * self.M * self.N + sc
 
 
 U = ("uniform",)
@@ -67,6 +72,7 @@ WORKLOADS = {
     "llm_proj_8192x14336x4096_bf16_bf16": Workload("llm_proj_8192x14336x4096_bf16_bf16", 8192, 14336, 4096,
                                                    BF16, BF16, N002, N002, 3),
     "fp8_8192_e4m3_bf16": Workload("fp8_8192_e4m3_bf16", 8192, 8192, 8192, E4M3, BF16, U, U, 5),
+    "mxfp8_8192_e4m3_bf16": Workload("mxfp8_8192_e4m3_bf16", 8192, 8192, 8192, MXE4M3, BF16, U, U, 6),
     "gemv_m1_n4096_k4096_bf16": Workload("gemv_m1_n4096_k4096_bf16", 1, 4096, 4096, BF16, BF16, U, N002, 4),
     "gemv_m8_n4096_k4096_bf16": Workload("gemv_m8_n4096_k4096_bf16", 8, 4096, 4096, BF16, BF16, U, N002, 4),
     "gemv_m1_n14336_k4096_bf16": Workload("gemv_m1_n14336_k4096_bf16", 1, 14336, 4096, BF16, BF16, U, N002, 4),
@@ -98,6 +104,11 @@ def make_operands(M: int, N: int, K: int, in_dtype: str, dist_a: tuple, dist_b: 
 
 def workload_operands(w: Workload):
     return make_operands(w.M, w.N, w.K, w.in_dtype, w.dist_a, w.dist_b, w.seed)
+
+
+def workload_mx_scales(w: Workload):
+    """Row-major UE8M0 block scales (scale_a, scale_b) of a block-scaled workload."""
+    return mx_scales(w.M, w.K, w.seed + 1000), mx_scales(w.N, w.K, w.seed + 2000)
 
 
 def integer_operands(M: int, N: int, K: int, in_dtype: str, seed: int, lo: int = -2, hi: int = 2):

@@ -55,7 +55,9 @@ typedef enum {
   GEMM_E5M2_BF16 = 7, /* E5M2 in, bf16 out */
   /* MX block-scaled 8-bit inputs (OCP Microscaling formats MXFP8): every 32
    * consecutive K elements of a row of A or B share one UE8M0 scale 2^(e-127);
-   * run with gemm_plan_run_mx, which takes the two scale arrays.  Variant 7. */
+   * run with gemm_plan_run_mx, which takes the two scale arrays.  Variants 7
+   * and 8 (one MMA consumer; the automatic plan picks 8 when every CTA pair
+   * gets a tile). */
   GEMM_MXE4M3_F32 = 8,  /* MXFP8 E4M3 in, fp32 out */
   GEMM_MXE4M3_BF16 = 9, /* MXFP8 E4M3 in, bf16 out */
   GEMM_MXE5M2_F32 = 10, /* MXFP8 E5M2 in, fp32 out */

@@ -87,8 +87,8 @@ def test_fp8_row_pitch_rule(lib):
 def test_mx_rules(lib):
     for dt in (gemm.MXE4M3_F32, gemm.MXE4M3_BF16, gemm.MXE5M2_F32, gemm.MXE5M2_BF16):
         assert _plan_status(lib, 64, 64, 24, dt) == gemm.ERR_UNSUPPORTED_SHAPE
-        # block-scaled inputs run on variant 7 only, K-major only
-        for v in (gemm.S3, gemm.S8, gemm.S9, gemm.GEMV):
+        # block-scaled inputs run on variants 7 and 8 only, K-major only
+        for v in (gemm.S3, gemm.S6, gemm.S9, gemm.GEMV):
             assert _plan_status(lib, 256, 256, 256, dt, gemm.make_opts(variant=v)) == gemm.ERR_UNSUPPORTED_SHAPE
         assert _plan_status(lib, 256, 256, 256, dt, gemm.make_opts(variant=gemm.S7, layout=gemm.LAYOUT_A_MN)) == \
             gemm.ERR_UNSUPPORTED_SHAPE

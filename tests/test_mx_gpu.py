@@ -1,7 +1,7 @@
 """GPU parity of the MX block-scaled GEMM (8-bit float operands with one UE8M0
 scale per 32 consecutive K elements of every row of A and B, tcgen05.mma
-kind::mxf8f6f4 on the step-7 tile) against the CPU oracle's fp64 block-scaled
-product, with the plain and the fused writeback."""
+kind::mxf8f6f4 on the step-7 tile and on the step-8 CTA pair) against the CPU
+oracle's fp64 block-scaled product, with the plain and the fused writeback."""
 from __future__ import annotations
 
 import numpy as np
@@ -25,11 +25,11 @@ def _built():
     torch.cuda.set_device(0)
 
 
-def _run(a, b, sa, sb, out, **epi):
+def _run(a, b, sa, sb, out, variant=0, **epi):
     M, K = a.shape
     N = b.shape[0]
     fmt = "mxe4m3" if a.dtype == torch.float8_e4m3fn else "mxe5m2"
-    plan = gemm.Plan(M, N, K, gemm.dtype_code(fmt, out))
+    plan = gemm.Plan(M, N, K, gemm.dtype_code(fmt, out), gemm.make_opts(variant=variant))
     info = plan.info()
     ta = inputs.mx_tile_scales(sa, K).to(DEV)
     tb = inputs.mx_tile_scales(sb, K).to(DEV)
@@ -41,18 +41,19 @@ def _run(a, b, sa, sb, out, **epi):
     return c, info
 
 
+@pytest.mark.parametrize("variant", [gemm.S7, gemm.S8])
 @pytest.mark.parametrize("shape", SHAPES)
 @pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
 @pytest.mark.parametrize("out", ["f32", "bf16"])
-def test_integer_operands_bit_exact(shape, fmt, out):
+def test_integer_operands_bit_exact(variant, shape, fmt, out):
     # integer operands in [-8, 8] and scales 2^-2 .. 2^2: every term and every
     # fp32 partial sum is exact, so the result is unique
     M, N, K = shape
     a, b = inputs.integer_operands(M, N, K, fmt, seed=M + K, lo=-8, hi=8)
     sa = inputs.mx_scales(M, K, seed=1, e_lo=125, e_hi=129)
     sb = inputs.mx_scales(N, K, seed=2, e_lo=125, e_hi=129)
-    c, info = _run(a, b, sa, sb, out)
-    assert info["variant"] == gemm.S7
+    c, info = _run(a, b, sa, sb, out, variant)
+    assert info["variant"] == variant
     C, _ = oracle.gemm_mx(a, b, sa, sb)
     exp = torch.tensor(C).to(inputs.torch_dtype(out)).double().numpy()
     got = c.double().cpu().numpy()
@@ -60,27 +61,29 @@ def test_integer_operands_bit_exact(shape, fmt, out):
     assert bad.size == 0, (bad[:3], got[tuple(bad[0])], exp[tuple(bad[0])])
 
 
+@pytest.mark.parametrize("variant", [gemm.S7, gemm.S8])
 @pytest.mark.parametrize("shape", SHAPES[:3])
 @pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
-def test_random_parity(shape, fmt):
+def test_random_parity(variant, shape, fmt):
     M, N, K = shape
     a, b, sa, sb = inputs.mx_operands(M, N, K, fmt, seed=7 + K)
     out = "bf16" if fmt == "e4m3" else "f32"
-    c, info = _run(a, b, sa, sb, out)
+    c, info = _run(a, b, sa, sb, out, variant)
     C, S = oracle.gemm_mx(a, b, sa, sb)
     r = parity.check(c.double().cpu().numpy(), C, S, out)
     assert r["ok"], (info, r)
 
 
-def test_scales_only_touch_their_own_block():
-    # one scale byte raised by 3 (x8) changes exactly one row's 32-element block
-    M, N, K = 256, 256, 256
+@pytest.mark.parametrize("variant", [gemm.S7, gemm.S8])
+def test_scales_only_touch_their_own_block(variant):
+    # one scale byte of A and one of B changed: only that row and that column move
+    M, N, K = 512, 512, 256
     a, b = inputs.integer_operands(M, N, K, "e4m3", seed=5, lo=-4, hi=4)
     sa = torch.full((M, K // 32), 127, dtype=torch.uint8)
     sb = torch.full((N, K // 32), 127, dtype=torch.uint8)
     sa[77, 5] = 130
     sb[200, 2] = 124
-    c, _ = _run(a, b, sa, sb, "f32")
+    c, _ = _run(a, b, sa, sb, "f32", variant)
     C, _ = oracle.gemm_mx(a, b, sa, sb)
     assert np.array_equal(c.double().cpu().numpy(), C)
     C0, _ = oracle.gemm(a, b)
@@ -89,8 +92,9 @@ def test_scales_only_touch_their_own_block():
     assert (diff[:, 0] == 77).any() and (diff[:, 1] == 200).any()
 
 
+@pytest.mark.parametrize("variant", [gemm.S7, gemm.S8])
 @pytest.mark.parametrize("act", [gemm.ACT_NONE, gemm.ACT_RELU, gemm.ACT_SILU, gemm.ACT_GELU_ERF])
-def test_fused_epilogue(act):
+def test_fused_epilogue(variant, act):
     M, N, K = 700, 776, 336
     out = "bf16" if act % 2 else "f32"
     a, b, sa, sb = inputs.mx_operands(M, N, K, "e4m3", seed=40 + act)
@@ -98,7 +102,8 @@ def test_fused_epilogue(act):
     bias = torch.randn(N, generator=g).float()
     res = torch.randn(M, N, generator=g).to(inputs.torch_dtype(out))
     rs = (torch.rand(M, generator=g) + 0.5).float()
-    c, _ = _run(a, b, sa, sb, out, bias=bias.to(DEV), residual=res.to(DEV), act=act, scale_a=rs.to(DEV))
+    c, _ = _run(a, b, sa, sb, out, variant, bias=bias.to(DEV), residual=res.to(DEV), act=act,
+                scale_a=rs.to(DEV))
     C, S = oracle.gemm_mx(a, b, sa, sb)
     ref = oracle.epilogue(C, bias, res, act, scale_a=rs)
     pre = oracle.epilogue(C, bias, None, oracle.ACT_NONE, scale_a=rs)
@@ -123,6 +128,9 @@ def test_rejections():
     a = torch.zeros(M, K, dtype=torch.float8_e4m3fn, device=DEV)
     s = torch.full((gemm.mx_scale_bytes(M, K),), 127, dtype=torch.uint8, device=DEV)
     c = torch.zeros(M, N, device=DEV)
+    with pytest.raises(gemm.GemmError) as e:
+        gemm.Plan(M, N, K, gemm.MXE4M3_F32, gemm.make_opts(variant=gemm.S9))
+    assert e.value.status == gemm.ERR_UNSUPPORTED_SHAPE
     plan = gemm.Plan(M, N, K, gemm.MXE4M3_F32)
     with pytest.raises(gemm.GemmError) as e:
         plan.run(a, a, c)        # no scales
@@ -141,3 +149,16 @@ def test_rejections():
         p2.run_mx(a, a, c, s, s)
     assert e.value.status == gemm.ERR_UNSUPPORTED_DTYPE
     p2.destroy()
+
+
+def test_bench_workload_sampled_rows():
+    # the 8192^3 block-scaled workload the bench times, in its launch configuration
+    w = inputs.WORKLOADS["mxfp8_8192_e4m3_bf16"]
+    a, b = inputs.workload_operands(w)
+    sa, sb = inputs.workload_mx_scales(w)
+    c, info = _run(a, b, sa, sb, w.out_dtype)
+    rows = [0, 1, 127, 128, 4095, 4096, 8191] + list(range(1000, 8192, 1777))
+    C, S = oracle.gemm_mx(a, b, sa, sb, rows=rows)
+    r = parity.check(c[rows].double().cpu().numpy(), C, S, w.out_dtype)
+    assert r["ok"], (info, r)
+    assert bool(torch.isfinite(c).all())
