@@ -79,14 +79,15 @@ bool encode_fn_ready() {
 // 2-D row-major tensor [outer][inner], tiles of box_outer x box_inner elements
 // landing in SMEM with the 128-byte swizzle; out-of-range elements read as 0.
 bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, int esize, const void* ptr, uint64_t inner,
-               uint64_t outer, uint32_t box_inner, uint32_t box_outer) {
+               uint64_t outer, uint32_t box_inner, uint32_t box_outer,
+               CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   if (!encode_fn_ready()) return false;
   cuuint64_t dims[2] = {inner, outer};
   cuuint64_t strides[1] = {inner * (uint64_t)esize};
   cuuint32_t box[2] = {box_inner, box_outer};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = g_encode(m, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -407,7 +408,13 @@ const CUtensorMap* operand_map(gemm_plan_s* p, int role, const void* ptr) {
   const int ie = p->in_f8 ? 1 : 2;     // bytes per input element
   const uint32_t kbox = 128u / ie;     // one 128-byte swizzle row of K
   bool ok = false;
-  if (role == 3) {
+  if (role == 4 || role == 5) {
+    // MX scales of A (4) or B (5): the tiled array seen as rows of 128 bytes, one
+    // 512-byte block = a box of 4 rows, copied as is
+    const int64_t bytes = gemm_mx_scale_bytes(role == 4 ? p->M : p->N, p->K);
+    ok = bytes > 0 && encode_2d(&victim->map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, ptr, 128, (uint64_t)(bytes / 128), 128,
+                                4, CU_TENSOR_MAP_SWIZZLE_NONE);
+  } else if (role == 3) {
     // activation rows of the tensor-core GEMV: 16-row boxes, rows >= M read as zero
     ok = encode_2d(&victim->map, in_t, 2, ptr, (uint64_t)p->K, (uint64_t)p->M, 64, 16);
   } else if (role == 0 && (p->layout & GEMM_LAYOUT_A_MN)) {
@@ -478,8 +485,6 @@ gemm_status_t launch_plan(gemm_plan_s* p, const void* A, const void* B, void* C,
         k.stages = p->epi_stages;
         spec = &p->spec_epi[epi->activation];
       }
-      k.sfa = static_cast<const uint8_t*>(sfa);
-      k.sfb = static_cast<const uint8_t*>(sfb);
       k.A = static_cast<const uint16_t*>(A);
       k.B = static_cast<const uint16_t*>(B);
       k.C = C;
@@ -493,6 +498,14 @@ gemm_status_t launch_plan(gemm_plan_s* p, const void* A, const void* B, void* C,
       if (!ma || !mb) return GEMM_ERR_CUDA;
       if (spec->kind == ARGS_AB_K) {
         void* args[] = {const_cast<CUtensorMap*>(ma), const_cast<CUtensorMap*>(mb), &k};
+        e = launch_spec(*spec, args, s);
+      } else if (spec->kind == ARGS_ABCSS_K) {
+        const CUtensorMap* mc = operand_map(p, 2, C);
+        const CUtensorMap* msa = operand_map(p, 4, sfa);
+        const CUtensorMap* msb = operand_map(p, 5, sfb);
+        if (!mc || !msa || !msb) return GEMM_ERR_CUDA;
+        void* args[] = {const_cast<CUtensorMap*>(ma), const_cast<CUtensorMap*>(mb), const_cast<CUtensorMap*>(mc),
+                        const_cast<CUtensorMap*>(msa), const_cast<CUtensorMap*>(msb), &k};
         e = launch_spec(*spec, args, s);
       } else {
         const CUtensorMap* mc = operand_map(p, 2, C);

@@ -26,7 +26,6 @@ enum : uint32_t {
   WAIT_LADDER_MMA = 0x7108u,
   WAIT_LADDER_TMA = 0x7109u,
   WAIT_DRAIN = 0x710Au,
-  WAIT_MX_FORWARD = 0x710Bu,
 };
 
 // test hook: the producer leaves out one TMA load of the first stage while
@@ -61,9 +60,6 @@ struct KParams {
   // fused-epilogue dequantisation: acc * scale_a[row] * scale_b[col] before the bias
   const float* scale_a;  // M fp32 values, or null
   const float* scale_b;  // N fp32 values, or null
-  // MX block scales (mma_kind 2): UE8M0 bytes in the tiled 128 x 4 layout
-  const uint8_t* sfa;
-  const uint8_t* sfb;
 };
 
 constexpr uint32_t LAYOUT_A_MN = 1u;

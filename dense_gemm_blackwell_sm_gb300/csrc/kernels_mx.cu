@@ -12,16 +12,16 @@ namespace {
 template <typename OutT, int CG>
 void* pick_mx(int sched, int fused_act) {
   switch (fused_act) {
-    case EPI_ACT_NONE: return ws_kernel_ptr<OutT, CG, 1, SCHED_STATIC, EPI_ACT_NONE, true>();
-    case EPI_ACT_RELU: return ws_kernel_ptr<OutT, CG, 1, SCHED_STATIC, EPI_ACT_RELU, true>();
-    case EPI_ACT_SILU: return ws_kernel_ptr<OutT, CG, 1, SCHED_STATIC, EPI_ACT_SILU, true>();
-    case EPI_ACT_GELU_TANH: return ws_kernel_ptr<OutT, CG, 1, SCHED_STATIC, EPI_ACT_GELU_TANH, true>();
-    case EPI_ACT_GELU_ERF: return ws_kernel_ptr<OutT, CG, 1, SCHED_STATIC, EPI_ACT_GELU_ERF, true>();
+    case EPI_ACT_NONE: return mx_kernel_ptr<OutT, CG, SCHED_STATIC, EPI_ACT_NONE>();
+    case EPI_ACT_RELU: return mx_kernel_ptr<OutT, CG, SCHED_STATIC, EPI_ACT_RELU>();
+    case EPI_ACT_SILU: return mx_kernel_ptr<OutT, CG, SCHED_STATIC, EPI_ACT_SILU>();
+    case EPI_ACT_GELU_TANH: return mx_kernel_ptr<OutT, CG, SCHED_STATIC, EPI_ACT_GELU_TANH>();
+    case EPI_ACT_GELU_ERF: return mx_kernel_ptr<OutT, CG, SCHED_STATIC, EPI_ACT_GELU_ERF>();
     default: break;
   }
-  if (sched == SCHED_ATOMIC) return ws_kernel_ptr<OutT, CG, 1, SCHED_ATOMIC, -1, true>();
-  if (sched == SCHED_CLC) return ws_kernel_ptr<OutT, CG, 1, SCHED_CLC, -1, true>();
-  return ws_kernel_ptr<OutT, CG, 1, SCHED_STATIC, -1, true>();
+  if (sched == SCHED_ATOMIC) return mx_kernel_ptr<OutT, CG, SCHED_ATOMIC>();
+  if (sched == SCHED_CLC) return mx_kernel_ptr<OutT, CG, SCHED_CLC>();
+  return mx_kernel_ptr<OutT, CG, SCHED_STATIC>();
 }
 
 void* mx_kernel(int cg, int sched, bool out_f32, int fused_act) {
@@ -54,7 +54,7 @@ cudaError_t spec_mx(int cg, int sched, bool out_f32, int stages, int clusters, L
   out->block = dim3(WS_THREADS, 1, 1);
   out->smem = smem;
   out->cluster = (unsigned)cg;
-  out->kind = ARGS_ABC_K;
+  out->kind = ARGS_ABCSS_K;
   return cudaSuccess;
 }
 

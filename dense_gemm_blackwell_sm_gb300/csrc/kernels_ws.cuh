@@ -29,17 +29,16 @@
 // between consecutive tiles (the writeback of tile i overlaps the MMAs of
 // tile i+1); step 9 gives one to each consumer.
 //
-// MX block scaling (MX template flag, one consumer, one CTA or a CTA pair): each
-// stage also brings the UE8M0 scales of its 128 K-elements (one 512-byte block
-// for the CTA's 128 rows of A, two for the tile's 256 rows of B) into shared
-// memory with plain bulk copies; the MMA thread moves them into TMEM with
-// tcgen05.cp and issues the block-scaled MMA.  In a pair each CTA holds the
-// scales of its own A rows and of all the tile's B rows; the second CTA's
-// scale copies complete on its own barrier, and its otherwise idle warp 1
-// forwards that completion to the leader's full barrier.  The scales take TMEM
-// columns 256 and up, so the tile keeps a single accumulator, and the writeback
-// stages through one 4 KB buffer per warp instead of two to leave shared
-// memory for the scale blocks.
+// MX block scaling (k_ws_mx: one consumer, one CTA or a CTA pair): each stage
+// also brings the UE8M0 scales of its 128 K-elements (one 512-byte block for
+// the CTA's 128 rows of A, two for the tile's 256 rows of B) into shared memory
+// with TMA copies of 128 x 4-byte boxes; the MMA thread moves them into TMEM
+// with tcgen05.cp and issues the block-scaled MMA.  In a pair each CTA holds
+// the scales of its own A rows and of all the tile's B rows, and its copies
+// complete on the leader's barrier like its operand copies.  The scales take
+// TMEM columns 256 and up, so the tile keeps a single accumulator, and the
+// writeback stages through one 4 KB buffer per warp instead of two to leave
+// shared memory for the scale blocks.
 //
 // In a CTA pair, each CTA loads its own 128 rows of A and its own 128 rows of B
 // (the pair MMA splits A along M and B along N) with the cta_group::2 TMA form,
@@ -82,17 +81,15 @@ struct WsCfg {
   static constexpr uint32_t MX_BYTES = MX_BLOCK * 3u;
 };
 
-// EPI < 0: plain writeback; EPI >= 0: fused epilogue with activation EPI.
-// MX: 8-bit inputs with UE8M0 block scales (CG = 1, NCONS = 1 only).
-template <typename OutT, int CG, int NCONS, int SCHED, int EPI = -1, bool MX = false>
-__global__ void __launch_bounds__(WS_THREADS, 1)
-    k_ws(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-         const __grid_constant__ CUtensorMap tmC, KParams p) {
+// The kernel body.  EPI < 0: plain writeback; EPI >= 0: fused epilogue with
+// activation EPI.  MX: 8-bit inputs with UE8M0 block scales read through
+// tmSA / tmSB (one consumer only).  The tensor maps are kernel parameters of
+// the entry points below.
+template <typename OutT, int CG, int NCONS, int SCHED, int EPI, bool MX>
+__device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMap* tmB, const CUtensorMap* tmC,
+                                        const CUtensorMap* tmSA, const CUtensorMap* tmSB, const KParams& p) {
   using Cfg = WsCfg<CG, NCONS>;
   static_assert(!MX || NCONS == 1, "MX block scaling runs with one MMA consumer");
-  constexpr bool MX_PAIR = MX && CG == 2;
-  // the forwarding warp of the second CTA also takes tile ids from the ring
-  constexpr uint32_t RING_CONS = Cfg::RING_CONSUMERS + (MX_PAIR ? 1u : 0u);
   constexpr uint32_t STAGING = MX ? WS_STAGING / 2 : WS_STAGING;
   constexpr uint32_t WARP_STAGING = STAGING / 4;
   constexpr int CW = (sizeof(OutT) == 4) ? 32 : 64;  // output columns per 128-byte staging row
@@ -113,7 +110,6 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
   uint64_t* ring_empty = bars + 24;            // [4]  roles -> scheduler
   uint64_t* clc_bar = bars + 28;
   uint64_t* drain_bar = bars + 29;
-  uint64_t* sf_full = bars + 36;               // [8]  scale copies of the second CTA (MX pair)
   uint32_t* clc_resp = reinterpret_cast<uint32_t*>(bars + 30);   // 16 B, 16-aligned
   volatile int32_t* ring_tile = reinterpret_cast<volatile int32_t*>(clc_resp + 4);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(clc_resp + 4 + WS_RING);
@@ -126,10 +122,8 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      // MX pair: the leader's producer plus the second CTA's forwarded scale arrival
-      mbar_init(smem_u32(full + s), MX_PAIR ? 2 : 1);
+      mbar_init(smem_u32(full + s), 1);
       mbar_init(smem_u32(empty + s), NCONS);
-      if constexpr (MX_PAIR) mbar_init(smem_u32(sf_full + s), 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(acc_full + i), 1);
@@ -137,7 +131,7 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
     }
     for (int i = 0; i < WS_RING; ++i) {
       mbar_init(smem_u32(ring_full + i), 1);
-      mbar_init(smem_u32(ring_empty + i), RING_CONS);
+      mbar_init(smem_u32(ring_empty + i), Cfg::RING_CONSUMERS);
     }
     mbar_init(smem_u32(clc_bar), 1);
     mbar_init(smem_u32(drain_bar), NCONS);
@@ -146,9 +140,13 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(&tmA);
-    tma_prefetch_desc(&tmB);
-    tma_prefetch_desc(&tmC);
+    tma_prefetch_desc(tmA);
+    tma_prefetch_desc(tmB);
+    tma_prefetch_desc(tmC);
+    if constexpr (MX) {
+      tma_prefetch_desc(tmSA);
+      tma_prefetch_desc(tmSB);
+    }
   }
   if (warp == 1) {
     tmem_alloc<CG>(smem_u32(tmem_slot), 512);
@@ -256,7 +254,7 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
           const int32_t n_tile = tn * WS_BN;
           if constexpr (MX) mx_bblocks = min(2, (p.N + 127) / 128 - n_tile / 128);
           const uint32_t mx_tx = MX ? MX_BLOCK * (1u + (uint32_t)mx_bblocks) : 0u;
-          if (leader) mbar_arrive_expect_tx(fb, Cfg::STAGE * CG + mx_tx);
+          if (leader) mbar_arrive_expect_tx(fb, (Cfg::STAGE + mx_tx) * CG);
           uint8_t* st = ring + (size_t)stage * Cfg::STAGE;
 #pragma unroll
           for (int c = 0; c < NCONS; ++c) {
@@ -267,15 +265,15 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
 #pragma unroll
               for (int h = 0; h < 2; ++h) {
                 if constexpr (CG == 1) {
-                  tma_load_2d(smem_u32(dst + h * 8192), &tmA, fb, row + 64 * h, kb * BKE);
+                  tma_load_2d(smem_u32(dst + h * 8192), tmA, fb, row + 64 * h, kb * BKE);
                 } else {
-                  tma_load_2d_pair(smem_u32(dst + h * 8192), &tmA, mapa_shared(fb, 0), row + 64 * h, kb * BKE);
+                  tma_load_2d_pair(smem_u32(dst + h * 8192), tmA, mapa_shared(fb, 0), row + 64 * h, kb * BKE);
                 }
               }
             } else if constexpr (CG == 1) {
-              tma_load_2d(smem_u32(dst), &tmA, fb, kb * BKE, row);
+              tma_load_2d(smem_u32(dst), tmA, fb, kb * BKE, row);
             } else {
-              tma_load_2d_pair(smem_u32(dst), &tmA, mapa_shared(fb, 0), kb * BKE, row);
+              tma_load_2d_pair(smem_u32(dst), tmA, mapa_shared(fb, 0), kb * BKE, row);
             }
           }
           uint8_t* bdst = st + NCONS * WS_A_BYTES;
@@ -285,29 +283,31 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
 #pragma unroll
             for (int h = 0; h < Cfg::B_ROWS / 64; ++h) {
               if constexpr (CG == 1) {
-                tma_load_2d(smem_u32(bdst + h * 8192), &tmB, fb, n_cta + 64 * h, kb * BKE);
+                tma_load_2d(smem_u32(bdst + h * 8192), tmB, fb, n_cta + 64 * h, kb * BKE);
               } else {
-                tma_load_2d_pair(smem_u32(bdst + h * 8192), &tmB, mapa_shared(fb, 0), n_cta + 64 * h, kb * BKE);
+                tma_load_2d_pair(smem_u32(bdst + h * 8192), tmB, mapa_shared(fb, 0), n_cta + 64 * h, kb * BKE);
               }
             }
           } else if constexpr (CG == 1) {
-            tma_load_2d(smem_u32(bdst), &tmB, fb, kb * BKE, n_cta);
+            tma_load_2d(smem_u32(bdst), tmB, fb, kb * BKE, n_cta);
           } else {
-            tma_load_2d_pair(smem_u32(bdst), &tmB, mapa_shared(fb, 0), kb * BKE, n_cta);
+            tma_load_2d_pair(smem_u32(bdst), tmB, mapa_shared(fb, 0), kb * BKE, n_cta);
           }
           if constexpr (MX) {
-            // tiled scale layout: block (row block, K block) at ((row block) * KB + kb) * 512.
-            // The second CTA of a pair counts its copies on its own barrier.
-            uint32_t sb_bar = fb;
-            if (MX_PAIR && !leader) {
-              sb_bar = smem_u32(sf_full + stage);
-              mbar_arrive_expect_tx(sb_bar, mx_tx);
-            }
+            // tiled scale layout: block (row block, K block) at ((row block) * KB + kb) * 512,
+            // i.e. rows 4 * block .. 4 * block + 3 of the 128-byte-wide tensor maps
             uint8_t* sd = mx_ring + (size_t)stage * Cfg::MX_BYTES;
-            bulk_load(smem_u32(sd), p.sfa + ((size_t)(m_cta / 128) * KB + kb) * MX_BLOCK, MX_BLOCK, sb_bar);
-            for (int32_t h = 0; h < mx_bblocks; ++h)
-              bulk_load(smem_u32(sd + MX_BLOCK * (1 + h)), p.sfb + ((size_t)(n_tile / 128 + h) * KB + kb) * MX_BLOCK,
-                        MX_BLOCK, sb_bar);
+            const int32_t ya = 4 * ((m_cta / 128) * KB + kb);
+            if constexpr (CG == 1) {
+              tma_load_2d(smem_u32(sd), tmSA, fb, 0, ya);
+              for (int32_t h = 0; h < mx_bblocks; ++h)
+                tma_load_2d(smem_u32(sd + MX_BLOCK * (1 + h)), tmSB, fb, 0, 4 * ((n_tile / 128 + h) * KB + kb));
+            } else {
+              tma_load_2d_pair(smem_u32(sd), tmSA, mapa_shared(fb, 0), 0, ya);
+              for (int32_t h = 0; h < mx_bblocks; ++h)
+                tma_load_2d_pair(smem_u32(sd + MX_BLOCK * (1 + h)), tmSB, mapa_shared(fb, 0), 0,
+                                 4 * ((n_tile / 128 + h) * KB + kb));
+            }
           }
           if (++stage == (uint32_t)S) { stage = 0; sphase ^= 1u; }
         }
@@ -332,6 +332,14 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
         tc_fence_after();
         const uint32_t d = tmem + slot * 256u;
         bool ok = true;
+        // MX: one stage's scales into TMEM (4 columns for A's 128 rows, 8 for B's 256)
+        auto copy_scales = [&](uint32_t stg) {
+          const uint32_t sft = tmem + MX_TMEM_COL + stg * MX_TMEM_SLOT;
+          const uint32_t sfs = smem_u32(mx_ring + (size_t)stg * Cfg::MX_BYTES);
+          tmem_cp_32x128b_x4<CG>(sft, sdesc_rows16(sfs));
+          tmem_cp_32x128b_x4<CG>(sft + 4, sdesc_rows16(sfs + MX_BLOCK));
+          tmem_cp_32x128b_x4<CG>(sft + 8, sdesc_rows16(sfs + 2 * MX_BLOCK));
+        };
         for (int32_t kb = 0; kb < KB; ++kb) {
           if (!mbar_wait(smem_u32(full + stage), sphase, w, WAIT_MMA_FULL)) { ok = false; break; }
           tc_fence_after();
@@ -343,13 +351,9 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
           const uint64_t astep = a_mn ? 128 : 2, bstep = b_mn ? 128 : 2;
           // four MMAs per stage, each over 32 bytes of K (16 x 16-bit or 32 x 8-bit)
           if constexpr (MX) {
-            // this stage's scales into TMEM (in order before the MMAs below): A's 128
-            // rows into 4 columns, B's 256 rows into 8
+            // the scales precede their MMAs in issue order
+            copy_scales(stage);
             const uint32_t sft = tmem + MX_TMEM_COL + stage * MX_TMEM_SLOT;
-            const uint32_t sfs = smem_u32(mx_ring + (size_t)stage * Cfg::MX_BYTES);
-            tmem_cp_32x128b_x4<CG>(sft, sdesc_rows16(sfs));
-            tmem_cp_32x128b_x4<CG>(sft + 4, sdesc_rows16(sfs + MX_BLOCK));
-            tmem_cp_32x128b_x4<CG>(sft + 8, sdesc_rows16(sfs + 2 * MX_BLOCK));
             // byte k of each scale word belongs to the k-th 32-element K block; blocks
             // wholly past K are not issued (their scale bytes are padding)
             const int32_t rem = p.K - kb * BKE;
@@ -385,21 +389,6 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
       mma_commit_cg<CG>(smem_u32(drain_bar));
       const WaitCtl wd{zero_word, p.status, p.timeout_ns, 0};
       mbar_wait(smem_u32(drain_bar), 0, wd, WAIT_DRAIN);
-    }
-  } else if (MX_PAIR && warp == 1) {
-    // ------------------------------------ scale forwarding (second CTA, MX pair)
-    if (lane == 0) {
-      uint32_t stage = 0, sphase = 0;
-      bool ok = true;
-      for (uint32_t i = 0; ok; ++i) {
-        int32_t tile;
-        if (!ring_get(i, tile) || tile < 0) break;
-        for (int32_t kb = 0; kb < KB; ++kb) {
-          if (!mbar_wait(smem_u32(sf_full + stage), sphase, w, WAIT_MX_FORWARD)) { ok = false; break; }
-          mbar_arrive_cluster(mapa_shared(smem_u32(full + stage), 0));
-          if (++stage == (uint32_t)S) { stage = 0; sphase ^= 1u; }
-        }
-      }
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ writeback
@@ -473,7 +462,7 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
           __syncwarp();
           if (lane == 0) {
             const int32_t col0 = col_base + ch * CW;
-            if (row0 < p.M && col0 < p.N) tma_store_2d(&tmC, smem_u32(buf), col0, row0);
+            if (row0 < p.M && col0 < p.N) tma_store_2d(tmC, smem_u32(buf), col0, row0);
             bulk_commit_group();
           }
           ++tog;
@@ -496,9 +485,31 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
   }
 }
 
-template <typename OutT, int CG, int NCONS, int SCHED, int EPI = -1, bool MX = false>
+// entry point of the fp16 / bf16 / 8-bit float kernels
+template <typename OutT, int CG, int NCONS, int SCHED, int EPI = -1>
+__global__ void __launch_bounds__(WS_THREADS, 1)
+    k_ws(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+         const __grid_constant__ CUtensorMap tmC, KParams p) {
+  ws_body<OutT, CG, NCONS, SCHED, EPI, false>(&tmA, &tmB, &tmC, nullptr, nullptr, p);
+}
+
+// entry point of the MX block-scaled kernels (one consumer)
+template <typename OutT, int CG, int SCHED, int EPI = -1>
+__global__ void __launch_bounds__(WS_THREADS, 1)
+    k_ws_mx(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+            const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmSA,
+            const __grid_constant__ CUtensorMap tmSB, KParams p) {
+  ws_body<OutT, CG, 1, SCHED, EPI, true>(&tmA, &tmB, &tmC, &tmSA, &tmSB, p);
+}
+
+template <typename OutT, int CG, int NCONS, int SCHED, int EPI = -1>
 void* ws_kernel_ptr() {
-  return reinterpret_cast<void*>(k_ws<OutT, CG, NCONS, SCHED, EPI, MX>);
+  return reinterpret_cast<void*>(k_ws<OutT, CG, NCONS, SCHED, EPI>);
+}
+
+template <typename OutT, int CG, int SCHED, int EPI = -1>
+void* mx_kernel_ptr() {
+  return reinterpret_cast<void*>(k_ws_mx<OutT, CG, SCHED, EPI>);
 }
 
 }  // namespace

@@ -20,6 +20,7 @@ enum ArgKind {
   ARGS_ABC_K = 2,  // (tmA, tmB, tmC, KParams)
   ARGS_GEMV = 3,   // (GemvParams)
   ARGS_BX_TG = 4,  // (tmB, tmX, TgParams)
+  ARGS_ABCSS_K = 5,  // (tmA, tmB, tmC, tmScaleA, tmScaleB, KParams)
 };
 
 struct LaunchSpec {

@@ -96,6 +96,30 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
   return ok != 0;
 }
 
+// non-blocking test of a phase (no suspend); CLUSTER_ACQ for barriers that peer
+// CTAs arrive on
+template <bool CLUSTER_ACQ = false>
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  if constexpr (CLUSTER_ACQ)
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+  else
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+  return ok != 0;
+}
+
 // ---------------------------------------------------------------------------
 // bounded waiting: every spin in the kernels goes through this.  A wait gives
 // up when the CTA's abort flag is raised or when `timeout_ns` of wall time has
@@ -153,15 +177,6 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 }
 
 // ---------------------------------------------------------------------------
-// Plain bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned)
-// from global to this CTA's shared memory, counted on `bar`.
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-      "l"(src), "r"(bytes), "r"(bar)
-      : "memory");
-}
-
 // TMA (cp.async.bulk.tensor)
 
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* m) {
