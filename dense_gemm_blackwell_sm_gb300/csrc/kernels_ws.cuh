@@ -32,8 +32,13 @@
 // MX block scaling (k_ws_mx: one consumer, one CTA or a CTA pair): each stage
 // also brings the UE8M0 scales of its 128 K-elements (one 512-byte block for
 // the CTA's 128 rows of A, two for the tile's 256 rows of B) into shared memory
-// with TMA copies of 128 x 4-byte boxes; the MMA thread moves them into TMEM
-// with tcgen05.cp and issues the block-scaled MMA.  In a pair each CTA holds
+// with TMA copies of 128 x 4-byte boxes, and tcgen05.cp moves them into TMEM
+// ahead of the block-scaled MMAs.  On the CTA pair, warp 3 (idle with one
+// consumer) issues those copies and signals each stage's on a barrier, so the
+// MMA thread only issues MMAs: that single thread's issue rate bounds the pair
+// kernel, and three copies per stage on it cost about a tenth of the
+// throughput.  The one-CTA kernel, whose 4-stage ring leaves less time to hide
+// the extra hand-off, issues the copies from the MMA thread itself.  In a pair each CTA holds
 // the scales of its own A rows and of all the tile's B rows, and its copies
 // complete on the leader's barrier like its operand copies.  The scales take
 // TMEM columns 256 and up, so the tile keeps a single accumulator, and the
@@ -90,6 +95,9 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
                                         const CUtensorMap* tmSA, const CUtensorMap* tmSB, const KParams& p) {
   using Cfg = WsCfg<CG, NCONS>;
   static_assert(!MX || NCONS == 1, "MX block scaling runs with one MMA consumer");
+  // MX on the pair: a separate warp copies the scales and takes tile ids from the ring
+  constexpr bool MX_COPIER = MX && CG == 2;
+  constexpr uint32_t RING_CONS = Cfg::RING_CONSUMERS + (MX_COPIER ? 1u : 0u);
   constexpr uint32_t STAGING = MX ? WS_STAGING / 2 : WS_STAGING;
   constexpr uint32_t WARP_STAGING = STAGING / 4;
   constexpr int CW = (sizeof(OutT) == 4) ? 32 : 64;  // output columns per 128-byte staging row
@@ -110,6 +118,8 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
   uint64_t* ring_empty = bars + 24;            // [4]  roles -> scheduler
   uint64_t* clc_bar = bars + 28;
   uint64_t* drain_bar = bars + 29;
+  uint64_t* sf_ready = bars + 36;              // [8]  scale copies -> MMA (MX)
+  uint64_t* cp_drain = bars + 44;              // scale-copy warp's last copies done (MX)
   uint32_t* clc_resp = reinterpret_cast<uint32_t*>(bars + 30);   // 16 B, 16-aligned
   volatile int32_t* ring_tile = reinterpret_cast<volatile int32_t*>(clc_resp + 4);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(clc_resp + 4 + WS_RING);
@@ -124,14 +134,16 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
     for (int s = 0; s < S; ++s) {
       mbar_init(smem_u32(full + s), 1);
       mbar_init(smem_u32(empty + s), NCONS);
+      if constexpr (MX_COPIER) mbar_init(smem_u32(sf_ready + s), 1);
     }
+    if constexpr (MX_COPIER) mbar_init(smem_u32(cp_drain), 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(acc_full + i), 1);
       mbar_init(smem_u32(acc_empty + i), 4 * CG);
     }
     for (int i = 0; i < WS_RING; ++i) {
       mbar_init(smem_u32(ring_full + i), 1);
-      mbar_init(smem_u32(ring_empty + i), Cfg::RING_CONSUMERS);
+      mbar_init(smem_u32(ring_empty + i), RING_CONS);
     }
     mbar_init(smem_u32(clc_bar), 1);
     mbar_init(smem_u32(drain_bar), NCONS);
@@ -332,16 +344,11 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
         tc_fence_after();
         const uint32_t d = tmem + slot * 256u;
         bool ok = true;
-        // MX: one stage's scales into TMEM (4 columns for A's 128 rows, 8 for B's 256)
-        auto copy_scales = [&](uint32_t stg) {
-          const uint32_t sft = tmem + MX_TMEM_COL + stg * MX_TMEM_SLOT;
-          const uint32_t sfs = smem_u32(mx_ring + (size_t)stg * Cfg::MX_BYTES);
-          tmem_cp_32x128b_x4<CG>(sft, sdesc_rows16(sfs));
-          tmem_cp_32x128b_x4<CG>(sft + 4, sdesc_rows16(sfs + MX_BLOCK));
-          tmem_cp_32x128b_x4<CG>(sft + 8, sdesc_rows16(sfs + 2 * MX_BLOCK));
-        };
         for (int32_t kb = 0; kb < KB; ++kb) {
-          if (!mbar_wait(smem_u32(full + stage), sphase, w, WAIT_MMA_FULL)) { ok = false; break; }
+          // MX pair: this stage's scales are in TMEM; the copy warp saw the stage land
+          // before copying, so this one wait covers the operands too
+          const uint32_t ready = MX_COPIER ? smem_u32(sf_ready + stage) : smem_u32(full + stage);
+          if (!mbar_wait(ready, sphase, w, WAIT_MMA_FULL)) { ok = false; break; }
           tc_fence_after();
           const uint32_t sa = smem_u32(ring + (size_t)stage * Cfg::STAGE + cons * WS_A_BYTES);
           const uint32_t sb = smem_u32(ring + (size_t)stage * Cfg::STAGE + NCONS * WS_A_BYTES);
@@ -351,8 +358,14 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
           const uint64_t astep = a_mn ? 128 : 2, bstep = b_mn ? 128 : 2;
           // four MMAs per stage, each over 32 bytes of K (16 x 16-bit or 32 x 8-bit)
           if constexpr (MX) {
-            // the scales precede their MMAs in issue order
-            copy_scales(stage);
+            if constexpr (!MX_COPIER) {
+              // one CTA: the scales precede their MMAs in this thread's issue order
+              const uint32_t sft0 = tmem + MX_TMEM_COL + stage * MX_TMEM_SLOT;
+              const uint32_t sfs = smem_u32(mx_ring + (size_t)stage * Cfg::MX_BYTES);
+              tmem_cp_32x128b_x4<CG>(sft0, sdesc_rows16(sfs));
+              tmem_cp_32x128b_x4<CG>(sft0 + 4, sdesc_rows16(sfs + MX_BLOCK));
+              tmem_cp_32x128b_x4<CG>(sft0 + 8, sdesc_rows16(sfs + 2 * MX_BLOCK));
+            }
             const uint32_t sft = tmem + MX_TMEM_COL + stage * MX_TMEM_SLOT;
             // byte k of each scale word belongs to the k-th 32-element K block; blocks
             // wholly past K are not issued (their scale bytes are padding)
@@ -390,6 +403,33 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
       const WaitCtl wd{zero_word, p.status, p.timeout_ns, 0};
       mbar_wait(smem_u32(drain_bar), 0, wd, WAIT_DRAIN);
     }
+  } else if (MX_COPIER && warp == 3 && leader) {
+    // --------------------------------------------------- scale copies (MX only)
+    if (lane == 0) {
+      uint32_t stage = 0, sphase = 0;
+      bool ok = true;
+      for (uint32_t i = 0; ok; ++i) {
+        int32_t tile;
+        if (!ring_get(i, tile) || tile < 0) break;
+        for (int32_t kb = 0; kb < KB; ++kb) {
+          // the stage's slot was last read by MMAs that completed before the stage was
+          // refilled, so it is free once the stage has landed
+          if (!mbar_wait(smem_u32(full + stage), sphase, w, WAIT_MMA_FULL)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t sft = tmem + MX_TMEM_COL + stage * MX_TMEM_SLOT;
+          const uint32_t sfs = smem_u32(mx_ring + (size_t)stage * Cfg::MX_BYTES);
+          tmem_cp_32x128b_x4<CG>(sft, sdesc_rows16(sfs));           // A's 128 rows: 4 columns
+          tmem_cp_32x128b_x4<CG>(sft + 4, sdesc_rows16(sfs + MX_BLOCK));      // B's 256 rows: 8
+          tmem_cp_32x128b_x4<CG>(sft + 8, sdesc_rows16(sfs + 2 * MX_BLOCK));
+          mma_commit_cg<CG>(smem_u32(sf_ready + stage));
+          if (++stage == (uint32_t)S) { stage = 0; sphase ^= 1u; }
+        }
+      }
+      // the copies this thread issued must be complete before TMEM is released
+      mma_commit_cg<CG>(smem_u32(cp_drain));
+      const WaitCtl wd{zero_word, p.status, p.timeout_ns, 0};
+      mbar_wait(smem_u32(cp_drain), 0, wd, WAIT_DRAIN);
+    }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ writeback
     const uint32_t q = warp & 3u;  // TMEM lane quarter this warp may access
@@ -417,6 +457,51 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
         const int32_t row0 = tm * Cfg::TILE_M + cons * 128 * CG + (int32_t)rank * 128 + (int32_t)q * 32;
         const int32_t col_base = tn * WS_BN;
         const uint32_t tbase = tmem + ((q * 32u) << 16) + slot * 256u;
+        if constexpr (MX && CW == 64 && EPI < 0) {
+          // single accumulator: first pull this warp's 32 x 256 slice into registers
+          // as packed bf16 and hand the accumulator back, so the next tile's MMAs
+          // start while the stores below drain
+          uint32_t pk[NCH][32];
+#pragma unroll
+          for (int ch = 0; ch < NCH; ++ch) {
+            uint32_t v0[32], v1[32];
+            tmem_ld_32x32b_x32(tbase + (uint32_t)(ch * CW), v0);
+            tmem_ld_32x32b_x32(tbase + (uint32_t)(ch * CW + 32), v1);
+            tmem_wait_ld();
+#pragma unroll
+            for (int m = 0; m < 16; ++m) {
+              pk[ch][m] = pack_bf16x2(v0[2 * m], v0[2 * m + 1]);
+              pk[ch][16 + m] = pack_bf16x2(v1[2 * m], v1[2 * m + 1]);
+            }
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) {
+            if constexpr (CG == 1) {
+              mbar_arrive(smem_u32(acc_empty + slot));
+            } else {
+              mbar_arrive_cluster(mapa_shared(smem_u32(acc_empty + slot), 0));
+            }
+          }
+#pragma unroll
+          for (int ch = 0; ch < NCH; ++ch) {
+            uint8_t* buf = my_staging;
+            if (lane == 0) bulk_wait_group_read<0>();  // the previous store is done reading `buf`
+            __syncwarp();
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              *reinterpret_cast<uint4*>(buf + sw128_offset(lane, (uint32_t)j)) =
+                  make_uint4(pk[ch][4 * j], pk[ch][4 * j + 1], pk[ch][4 * j + 2], pk[ch][4 * j + 3]);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              const int32_t col0 = col_base + ch * CW;
+              if (row0 < p.M && col0 < p.N) tma_store_2d(tmC, smem_u32(buf), col0, row0);
+              bulk_commit_group();
+            }
+          }
+          continue;
+        }
 #pragma unroll 1
         for (int ch = 0; ch < NCH; ++ch) {
           uint32_t v0[32], v1[32];
