@@ -92,6 +92,21 @@ bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, int esize, const void* pt
   return r == CUDA_SUCCESS;
 }
 
+// MX scales of B seen as a 4-D byte tensor [row blocks][K blocks][4 rows][128 B]
+// of 512-byte blocks; one box of 128 x 4 x 1 x 2 brings the blocks of two
+// consecutive 128-row groups for one K block (rows past the array read as 0).
+bool encode_mx_pairs(CUtensorMap* m, const void* ptr, uint64_t k_blocks, uint64_t row_blocks) {
+  if (!encode_fn_ready()) return false;
+  cuuint64_t dims[4] = {128, 4, k_blocks, row_blocks};
+  cuuint64_t strides[3] = {128, 512, 512 * k_blocks};
+  cuuint32_t box[4] = {128, 4, 1, 2};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(ptr), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // tcgen05 instruction descriptor, kind::f16: fp32 accumulator, A and B both
 // fp16 or both bf16, both K-major, MMA shape M x N
 uint32_t make_idesc(bool bf16, int M, int N) {
@@ -408,12 +423,15 @@ const CUtensorMap* operand_map(gemm_plan_s* p, int role, const void* ptr) {
   const int ie = p->in_f8 ? 1 : 2;     // bytes per input element
   const uint32_t kbox = 128u / ie;     // one 128-byte swizzle row of K
   bool ok = false;
-  if (role == 4 || role == 5) {
-    // MX scales of A (4) or B (5): the tiled array seen as rows of 128 bytes, one
-    // 512-byte block = a box of 4 rows, copied as is
-    const int64_t bytes = gemm_mx_scale_bytes(role == 4 ? p->M : p->N, p->K);
+  if (role == 4) {
+    // MX scales of A: the tiled array seen as rows of 128 bytes, one 512-byte
+    // block = a box of 4 rows, copied as is
+    const int64_t bytes = gemm_mx_scale_bytes(p->M, p->K);
     ok = bytes > 0 && encode_2d(&victim->map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, ptr, 128, (uint64_t)(bytes / 128), 128,
                                 4, CU_TENSOR_MAP_SWIZZLE_NONE);
+  } else if (role == 5) {
+    // MX scales of B: the two 128-row blocks of a 256-row tile in one box
+    ok = encode_mx_pairs(&victim->map, ptr, (uint64_t)((p->K + 127) / 128), (uint64_t)((p->N + 127) / 128));
   } else if (role == 3) {
     // activation rows of the tensor-core GEMV: 16-row boxes, rows >= M read as zero
     ok = encode_2d(&victim->map, in_t, 2, ptr, (uint64_t)p->K, (uint64_t)p->M, 64, 16);

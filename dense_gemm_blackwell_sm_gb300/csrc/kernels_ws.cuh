@@ -261,11 +261,10 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
         for (int32_t kb = 0; kb < KB; ++kb) {
           if (!mbar_wait(smem_u32(empty + stage), sphase ^ 1u, w, WAIT_PRODUCER_EMPTY)) { ok = false; break; }
           const uint32_t fb = smem_u32(full + stage);
-          // MX: scale blocks of B rows at or past N are not in the scale array; skip them
-          int32_t mx_bblocks = 0;
+          // MX: one block of A scales and one box holding the two blocks of B scales
+          // (a block past the array's last row group arrives as zeros)
           const int32_t n_tile = tn * WS_BN;
-          if constexpr (MX) mx_bblocks = min(2, (p.N + 127) / 128 - n_tile / 128);
-          const uint32_t mx_tx = MX ? MX_BLOCK * (1u + (uint32_t)mx_bblocks) : 0u;
+          const uint32_t mx_tx = MX ? 3u * MX_BLOCK : 0u;
           if (leader) mbar_arrive_expect_tx(fb, (Cfg::STAGE + mx_tx) * CG);
           uint8_t* st = ring + (size_t)stage * Cfg::STAGE;
 #pragma unroll
@@ -307,18 +306,17 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
           }
           if constexpr (MX) {
             // tiled scale layout: block (row block, K block) at ((row block) * KB + kb) * 512,
-            // i.e. rows 4 * block .. 4 * block + 3 of the 128-byte-wide tensor maps
+            // i.e. rows 4 * block .. 4 * block + 3 of A's 128-byte-wide map, and entry
+            // (0, 0, kb, row block) of B's 4-D map (whose boxes span two row blocks).
+            // Every extra copy on the pair costs throughput, hence the one B box.
             uint8_t* sd = mx_ring + (size_t)stage * Cfg::MX_BYTES;
             const int32_t ya = 4 * ((m_cta / 128) * KB + kb);
             if constexpr (CG == 1) {
               tma_load_2d(smem_u32(sd), tmSA, fb, 0, ya);
-              for (int32_t h = 0; h < mx_bblocks; ++h)
-                tma_load_2d(smem_u32(sd + MX_BLOCK * (1 + h)), tmSB, fb, 0, 4 * ((n_tile / 128 + h) * KB + kb));
+              tma_load_4d(smem_u32(sd + MX_BLOCK), tmSB, fb, 0, 0, kb, n_tile / 128);
             } else {
               tma_load_2d_pair(smem_u32(sd), tmSA, mapa_shared(fb, 0), 0, ya);
-              for (int32_t h = 0; h < mx_bblocks; ++h)
-                tma_load_2d_pair(smem_u32(sd + MX_BLOCK * (1 + h)), tmSB, mapa_shared(fb, 0), 0,
-                                 4 * ((n_tile / 128 + h) * KB + kb));
+              tma_load_4d_pair(smem_u32(sd + MX_BLOCK), tmSB, mapa_shared(fb, 0), 0, 0, kb, n_tile / 128);
             }
           }
           if (++stage == (uint32_t)S) { stage = 0; sphase ^= 1u; }
