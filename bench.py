@@ -43,8 +43,10 @@ FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1
 
 # source files whose change invalidates a stored ncu traffic figure
 KERNEL_SOURCES = {
-    "ws": ["dense_gemm_blackwell_sm_gb300/csrc/kernels_ws.cu", "dense_gemm_blackwell_sm_gb300/csrc/ptx.cuh",
-           "dense_gemm_blackwell_sm_gb300/csrc/kernel_common.cuh"],
+    "ws": ["dense_gemm_blackwell_sm_gb300/csrc/kernels_ws.cu", "dense_gemm_blackwell_sm_gb300/csrc/kernels_ws.cuh",
+           "dense_gemm_blackwell_sm_gb300/csrc/ptx.cuh", "dense_gemm_blackwell_sm_gb300/csrc/kernel_common.cuh"],
+    "mx": ["dense_gemm_blackwell_sm_gb300/csrc/kernels_mx.cu", "dense_gemm_blackwell_sm_gb300/csrc/kernels_ws.cuh",
+           "dense_gemm_blackwell_sm_gb300/csrc/ptx.cuh", "dense_gemm_blackwell_sm_gb300/csrc/kernel_common.cuh"],
     "gemv": ["dense_gemm_blackwell_sm_gb300/csrc/kernel_gemv.cu", "dense_gemm_blackwell_sm_gb300/csrc/kernel_gemv_tc.cu",
              "dense_gemm_blackwell_sm_gb300/csrc/kernel_common.cuh", "dense_gemm_blackwell_sm_gb300/csrc/ptx.cuh"],
 }
@@ -480,7 +482,8 @@ def main(argv=None):
                        w.algorithmic_bytes // 2**20),
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "roofline": {"bound": "tensor", "achieved": round(achieved, 3), "peak": peak, "unit": "TFLOP/s",
-                     "frac": round(achieved / peak, 4), "traffic": stored_traffic("ws", w.name),
+                     "frac": round(achieved / peak, 4),
+                     "traffic": stored_traffic("mx" if w.in_dtype in (inputs.MXE4M3, inputs.MXE5M2) else "ws", w.name),
                      "peak_source": "%s %s" % (peak_key, peak_src),
                      "frac_of_stated_%d" % stated: round(achieved / stated, 4)},
         "clocks": res["clocks"],
