@@ -220,7 +220,7 @@ cudaError_t spec_gemv_tc(int M, int N, int K, bool in_bf16, bool out_f32, int nu
   p.idesc = (1u << 4) | (ab << 7) | (ab << 10) | ((uint32_t)(16 >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
   const size_t smem = tg_smem(p.stages);
   const void* k = out_f32 ? (const void*)k_gemv_tc<float> : (const void*)k_gemv_tc<__nv_bfloat16>;
-  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = allow_dynamic_smem((const void*)k, smem);
   if (e != cudaSuccess) return e;
   out->func = k;
   out->grid = dim3((unsigned)(((N + 127) / 128) * p.split), 1, 1);

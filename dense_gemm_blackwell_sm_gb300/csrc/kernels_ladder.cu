@@ -22,6 +22,8 @@
 // is step 2).  All of them use a 128x128 tile, 128 threads (4 warps: warp w
 // reads TMEM lanes 32w..32w+31 in the epilogue) and K-major operand tiles in
 // the 128-byte swizzled layout that the Tensor Core reads directly.
+#include <mutex>
+
 #include "kernel_common.cuh"
 #include "launch.h"
 
@@ -374,7 +376,7 @@ static size_t ladder_smem(int stages) {
 size_t step6_smem_bytes(int stages) { return ladder_smem(stages) + 32; }
 
 static cudaError_t finish_spec(const void* k, dim3 grid, size_t smem, int kind, LaunchSpec* out) {
-  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = allow_dynamic_smem((const void*)k, smem);
   if (e != cudaSuccess) return e;
   out->func = k;
   out->grid = grid;
@@ -409,6 +411,19 @@ cudaError_t spec_step6(int sched, int stages, bool out_f32, int grid, LaunchSpec
                            : (const void*)k_step6<__nv_bfloat16, S6_STATIC>;
   }
   return finish_spec(k, dim3((unsigned)grid, 1, 1), step6_smem_bytes(stages), ARGS_AB_K, out);
+}
+
+// The dynamic shared-memory limit is an attribute of the kernel, shared by every
+// plan that uses it: raise it when a plan needs more, never lower it (a plan
+// with a shallower ring must not make an earlier, deeper one unlaunchable).
+cudaError_t allow_dynamic_smem(const void* func, size_t bytes) {
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  cudaFuncAttributes a{};
+  cudaError_t e = cudaFuncGetAttributes(&a, func);
+  if (e != cudaSuccess) return e;
+  if ((size_t)a.maxDynamicSharedSizeBytes >= bytes) return cudaSuccess;
+  return cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
 }
 
 cudaError_t launch_spec(const LaunchSpec& s, void** args, cudaStream_t st) {

@@ -47,7 +47,7 @@ cudaError_t spec_mx(int cg, int sched, bool out_f32, int stages, int clusters, L
   void* k = mx_kernel(cg, sched, out_f32, fused_act);
   if (!k || stages < 1 || stages > mx_max_stages(cg)) return cudaErrorInvalidValue;
   const size_t smem = mx_smem_bytes(cg, stages);
-  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = allow_dynamic_smem((const void*)k, smem);
   if (e != cudaSuccess) return e;
   out->func = k;
   out->grid = dim3((unsigned)(clusters * cg), 1, 1);

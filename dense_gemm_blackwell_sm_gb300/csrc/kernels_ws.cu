@@ -87,7 +87,7 @@ int ws_max_active_clusters(int cg, int consumers, int sched, bool out_f32, int s
   void* k = ws_kernel(cg, consumers, sched, out_f32);
   if (!k) return 0;
   const size_t smem = ws_smem_bytes(cg, consumers, stages);
-  if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return 0;
+  if (allow_dynamic_smem((const void*)k, smem) != cudaSuccess) return 0;
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = ws_config(cg, 1, smem, nullptr, attr);
   int n = 0;
@@ -103,7 +103,7 @@ cudaError_t spec_ws(int cg, int consumers, int sched, bool out_f32, int stages, 
   void* k = ws_kernel(cg, consumers, fused_act >= 0 ? SCHED_STATIC : sched, out_f32, fused_act);
   if (!k) return cudaErrorInvalidValue;
   const size_t smem = ws_smem_bytes(cg, consumers, stages);
-  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = allow_dynamic_smem((const void*)k, smem);
   if (e != cudaSuccess) return e;
   out->func = k;
   out->grid = dim3((unsigned)(clusters * cg), 1, 1);

@@ -35,6 +35,8 @@ struct LaunchSpec {
 
 // one launch of a prepared kernel (cluster dimension attached when > 1)
 cudaError_t launch_spec(const LaunchSpec& s, void** args, cudaStream_t st);
+// raise (never lower) a kernel's dynamic shared-memory limit to `bytes`
+cudaError_t allow_dynamic_smem(const void* func, size_t bytes);
 
 // steps 1-3 (thread copies), 4-5 (TMA ring), 6 (persistent + scheduler)
 cudaError_t spec_step123(int M, int N, bool out_f32, LaunchSpec* out);

@@ -65,7 +65,9 @@ SHAPES = {
     gemm.S7: [(300, 520, 200), (700, 1288, 264)],
     gemm.S8: [(300, 520, 200), (700, 1288, 264), (1, 264, 72)],
     gemm.S9: [(300, 520, 200), (1100, 1288, 264)],
-    gemm.GEMV: [(1, 1000, 520), (3, 264, 72), (8, 1000, 520), (16, 96, 1024)],
+    # GEMV: the K-split kernel (M <= 2 and at most 64 rows per SM) and the row kernel
+    gemm.GEMV: [(1, 1000, 520), (3, 264, 72), (8, 1000, 520), (16, 96, 1024), (1, 4096, 4096), (2, 152, 8),
+                (1, 1, 64), (1, 9000, 16384), (2, 777, 4104), (1, 500, 8), (2, 12000, 520)],
     gemm.GEMV_TC: [(1, 1000, 520), (3, 264, 72), (8, 1000, 4104), (16, 96, 1024)],
 }
 CASES = [(v, s) for v, shapes in SHAPES.items() for s in shapes]
@@ -235,3 +237,30 @@ def test_gemv_tc_split_and_ring_depth(split, stages):
     r = parity.check(c.cpu().numpy(), ref, S, "f32")
     assert r["ok"], r
     plan.destroy()
+
+
+def test_plans_sharing_a_kernel_keep_their_shared_memory():
+    """The dynamic shared-memory limit belongs to the kernel, not the plan: a later
+    plan that needs less (a shallower ring, fewer rows per CTA) must not make an
+    earlier plan of the same kernel unlaunchable."""
+    cases = [((512, 512, 256), gemm.make_opts(variant=gemm.S9, stages=4), gemm.make_opts(variant=gemm.S9, stages=2)),
+             ((1, 1024, 512), gemm.make_opts(variant=gemm.GEMV), None)]
+    for (M, N, K), o_big, o_small in cases:
+        a, b = inputs.integer_operands(M, N, K, "bf16", seed=5)
+        big = gemm.Plan(M, N, K, gemm.BF16_F32, o_big)
+        if o_small is not None:
+            small = gemm.Plan(M, N, K, gemm.BF16_F32, o_small)
+            a2, b2 = a, b
+        else:   # same GEMV kernel, fewer rows per CTA
+            a2, b2 = inputs.integer_operands(M, 768, K, "bf16", seed=6)
+            small = gemm.Plan(M, 768, K, gemm.BF16_F32, o_big)
+        c1 = torch.empty((M, N), device=DEV)
+        c2 = torch.empty((a2.shape[0], b2.shape[0]), device=DEV)
+        for _ in range(2):
+            big.run(a.to(DEV), b.to(DEV), c1)
+            small.run(a2.to(DEV), b2.to(DEV), c2)
+        assert big.check() == gemm.OK and small.check() == gemm.OK
+        assert np.array_equal(c1.double().cpu().numpy(), oracle.gemm(a, b)[0])
+        assert np.array_equal(c2.double().cpu().numpy(), oracle.gemm(a2, b2)[0])
+        big.destroy()
+        small.destroy()
