@@ -285,8 +285,8 @@ def _bench_mx_e2e(w, a, b, code, steps, dev, ib, ob) -> dict:
             "d2h": ob * w.M * w.N}
 
 
-def bench_gemv(w: inputs.Workload, steps: int, warmup: int, dev, flags: int = 0) -> dict:
-    """GB/s of the decode GEMV (automatic plan).  The weight rotates over enough
+def bench_gemv(w: inputs.Workload, steps: int, warmup: int, dev, flags: int = 0, variant: int = 0) -> dict:
+    """GB/s of the decode GEMV (automatic plan unless `variant` is given).  The weight rotates over enough
     copies to exceed 4x L2, and the launches are captured in a CUDA graph so that
     the host's launch cost does not stand between these few-microsecond kernels."""
     from dense_gemm_blackwell_sm_gb300 import gemm
@@ -298,7 +298,7 @@ def bench_gemv(w: inputs.Workload, steps: int, warmup: int, dev, flags: int = 0)
     xs = x.to(dev)
     bs = [b.to(dev) for _ in range(copies)]
     ys = [torch.empty((w.M, w.N), device=dev, dtype=inputs.torch_dtype(w.out_dtype)) for _ in range(copies)]
-    plan = gemm.Plan(w.M, w.N, w.K, code, gemm.make_opts(flags=flags))
+    plan = gemm.Plan(w.M, w.N, w.K, code, gemm.make_opts(flags=flags, variant=variant))
     stream = torch.cuda.Stream(dev)
     sp = stream.cuda_stream
     ptrs = [(xs.data_ptr(), bb.data_ptr(), yy.data_ptr()) for bb, yy in zip(bs, ys)]

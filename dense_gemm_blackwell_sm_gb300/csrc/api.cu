@@ -164,14 +164,16 @@ gemm_status_t current_device(int* dev, int* sms) {
 
 int ceil_div(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }
 
-// Automatic variant: the decode GEMV on CUDA cores for one or two rows, on the
-// Tensor Core for up to 16 rows; the plain-store
+// Automatic variant: the decode GEMV with CUDA-core FMAs for one or two rows,
+// with warp-level MMAs on registers for up to 8, on the tcgen05 Tensor Core for
+// up to 16 rows; the plain-store
 // persistent kernel when C's rows are not 16-byte aligned for TMA stores;
 // otherwise the largest warp-specialised tile (step 9's 512x256 cluster tile,
 // then step 8's 256x256, then step 7's 128x256) that still gives every CTA pair
 // of the GPU at least one tile.
 int auto_variant(int64_t M, int64_t N, int64_t K, gemm_dtype_t dt, int sms) {
   if (M <= 2 && gemv_smem_bytes((int)M, (int)K) <= 200 * 1024) return GEMM_VARIANT_GEMV;
+  if (M >= 3 && M <= 8) return GEMM_VARIANT_GEMV;
   if (M <= 16) return GEMM_VARIANT_GEMV_TC;
   if (!c_rows_tma_ok(N, dt)) return GEMM_VARIANT_S6_PERSISTENT;
   const int64_t tn = (N + 255) / 256;

@@ -13,6 +13,18 @@
 //     first weight loads have been issued;
 //   * fp32 FMAs per lane, a shuffle reduction per output, one bf16/fp32 store;
 //   * the grid covers the rows exactly once (no atomics, no scratch memory).
+//
+// For 3 <= M <= 8 the CUDA cores would need M FMAs per weight element, more
+// than they can issue at HBM speed, and the tcgen05 GEMV is fed by TMA, which
+// streams at most about 40 GB/s per SM from DRAM.  k_gemv_mma keeps the load
+// path of k_gemv (16-byte loads by every lane straight into registers) and
+// does the arithmetic with warp-level mma.sync m16n8k16: 8 weight rows as the
+// A operand (rows 8-15 of the fragment are zero), the M <= 8 activation rows
+// as the n8 B operand, fp32 accumulation.  Each lane's 16-byte weight chunk
+// and the matching 16-byte activation chunk feed two MMAs; the order of K
+// inside the fragments is free because A and B use the same order.  A CTA owns
+// 8 weight rows; its 8 warps split K and add their 8 x 8 partial sums in
+// shared memory.
 #include <algorithm>
 #include <type_traits>
 
@@ -153,6 +165,99 @@ __global__ void __launch_bounds__(GV_THREADS) k_gemv(GemvParams g) {
   }
 }
 
+template <typename InT>
+__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1) {
+  // rows 8-15 of A (a1, a3) are zero
+  if constexpr (std::is_same<InT, __nv_bfloat16>::value) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
+  } else {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
+  }
+}
+
+constexpr int GM_ROWS = 8;  // weight rows per CTA
+// 16-byte weight chunks per lane in flight: 4 keeps the kernel near 64
+// registers, so several CTAs share an SM and their loads overlap (16 chunks:
+// one CTA per SM, 2.87 TB/s at 8 x 4096 x 4096; 4 chunks: 4.42 TB/s)
+constexpr int GM_J = 4;
+
+template <typename InT, typename OutT>
+__global__ void __launch_bounds__(GV_THREADS) k_gemv_mma(GemvParams g) {
+  __shared__ float red[GV_THREADS / 32][GM_ROWS][8];
+  const int K8 = g.K / 8;
+  const int warps = GV_THREADS / 32;
+  const int S = (K8 + warps - 1) / warps;  // chunks of each row in this warp's K slice
+  const int w = (int)warp_idx(), lane = (int)lane_idx();
+  const int gr = lane >> 2, c = lane & 3;  // fragment row / column group
+  const int n0 = (int)blockIdx.x * GM_ROWS;
+  const int row = n0 + gr;
+  const uint4 zero = make_uint4(0, 0, 0, 0);
+  const uint4* X = reinterpret_cast<const uint4*>(g.X);
+  const uint4* B = reinterpret_cast<const uint4*>(g.B);
+  // chunk j of this lane: 4 consecutive chunks (32 K-elements) per j across c
+  auto chunk = [&](int j) { return w * S + 4 * j + c; };
+  auto valid = [&](int j) { return 4 * j + c < S && chunk(j) < K8; };
+  float d[4] = {0.f, 0.f, 0.f, 0.f};
+  uint4 bw[GM_J], xv[GM_J];
+  const int JJ = (S + 3) / 4;
+
+  pdl_launch_dependents();
+  bool first = true;
+  for (int j0 = 0; j0 < JJ; j0 += GM_J) {
+#pragma unroll
+    for (int j = 0; j < GM_J; ++j)
+      bw[j] = (j0 + j < JJ && row < g.N && valid(j0 + j)) ? ld_stream_v4(B + (int64_t)row * K8 + chunk(j0 + j)) : zero;
+    if (first) pdl_wait_prior_grids();
+    first = false;
+#pragma unroll
+    for (int j = 0; j < GM_J; ++j)
+      xv[j] = (j0 + j < JJ && gr < g.M && valid(j0 + j)) ? X[(int64_t)gr * K8 + chunk(j0 + j)] : zero;
+#pragma unroll
+    for (int j = 0; j < GM_J; ++j) {
+      mma_16816<InT>(d, bw[j].x, bw[j].y, xv[j].x, xv[j].y);
+      mma_16816<InT>(d, bw[j].z, bw[j].w, xv[j].z, xv[j].w);
+    }
+  }
+  if (first) pdl_wait_prior_grids();
+  // d[0], d[1]: weight row gr, activation rows 2c and 2c + 1 (d[2], d[3]: zero rows)
+  red[w][gr][2 * c] = d[0];
+  red[w][gr][2 * c + 1] = d[1];
+  __syncthreads();
+  if ((int)threadIdx.x < GM_ROWS * 8) {
+    const int r = (int)threadIdx.x >> 3, m = (int)threadIdx.x & 7;
+    float v = 0.f;
+#pragma unroll
+    for (int q = 0; q < warps; ++q) v += red[q][r][m];
+    if (m < g.M && n0 + r < g.N) {
+      if constexpr (sizeof(OutT) == 4) {
+        reinterpret_cast<float*>(g.Y)[(int64_t)m * g.N + n0 + r] = v;
+      } else {
+        reinterpret_cast<__nv_bfloat16*>(g.Y)[(int64_t)m * g.N + n0 + r] = __float2bfloat16_rn(v);
+      }
+    }
+  }
+}
+
+template <typename InT, typename OutT>
+cudaError_t spec_mma(int N, LaunchSpec* out) {
+  auto k = k_gemv_mma<InT, OutT>;
+  out->func = (const void*)k;
+  out->grid = dim3((unsigned)((N + GM_ROWS - 1) / GM_ROWS), 1, 1);
+  out->block = dim3(GV_THREADS, 1, 1);
+  out->smem = 0;
+  out->cluster = 1;
+  out->kind = ARGS_GEMV;
+  return cudaSuccess;
+}
+
 template <typename InT, typename OutT, int MT, int R>
 cudaError_t spec_t(int N, int K, int num_sms, LaunchSpec* out) {
   auto k = k_gemv<InT, OutT, MT, R>;
@@ -181,15 +286,15 @@ cudaError_t spec_m(int M, int N, int K, int num_sms, LaunchSpec* out) {
   // 3.99 -> 4.49 TB/s; 14336 x 4096: 5.70 -> 6.05 TB/s)
   if (M <= 1) return spec_t<InT, OutT, 1, 1>(N, K, num_sms, out);
   if (M <= 2) return spec_t<InT, OutT, 2, 1>(N, K, num_sms, out);
-  if (M <= 4) return spec_t<InT, OutT, 4, 1>(N, K, num_sms, out);
-  if (M <= 8) return spec_t<InT, OutT, 8, 1>(N, K, num_sms, out);
+  if (M <= 8) return spec_mma<InT, OutT>(N, out);
   return spec_t<InT, OutT, 16, 1>(N, K, num_sms, out);
 }
 
 }  // namespace
 
 size_t gemv_smem_bytes(int M, int K) {
-  const int mt = M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : M <= 8 ? 8 : 16;
+  if (M >= 3 && M <= 8) return 0;  // k_gemv_mma keeps its operands in registers
+  const int mt = M <= 1 ? 1 : M <= 2 ? 2 : 16;
   return (size_t)mt * (size_t)(K / 8) * 16;
 }
 
