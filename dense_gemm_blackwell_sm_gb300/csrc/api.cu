@@ -35,6 +35,9 @@ struct gemm_plan_s {
   int32_t flags;      // GEMM_FLAG_*
   int32_t layout;     // GEMM_LAYOUT_*
   uint32_t* scratch;  // [0] status word, [1] tile counter, [2] finished counter
+  float* sk_ws;       // stream-K workspace (one slot per cluster), or null
+  uint32_t* sk_flags; // stream-K flags (one per writeback warp of each slot), or null
+  size_t sk_flag_bytes;
   int32_t* visits;
   dgb::LaunchSpec spec;   // kernel, launch shape and SMEM, fixed at plan time
   dgb::LaunchSpec spec_epi[5];  // the fused-epilogue kernel per activation, made on first use
@@ -257,7 +260,7 @@ gemm_status_t build_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, co
   if (st != GEMM_OK) return st;
   gemm_opts_t o{};
   if (opts) o = *opts;
-  if (o.variant < 0 || o.variant > GEMM_VARIANT_GEMV_TC || o.sched < 0 || o.sched > GEMM_SCHED_CLC ||
+  if (o.variant < 0 || o.variant > GEMM_VARIANT_GEMV_TC || o.sched < 0 || o.sched > GEMM_SCHED_STREAM_K ||
       o.stages < 0 || o.stages > 12 || o.raster_group < 0 || o.max_ctas < 0 || o.timeout_ns < 0 ||
       o.split_k < 0 || o.split_k > 8 || (o.flags & ~GEMM_FLAG_STATIC_B) != 0 ||
       (o.layout & ~(GEMM_LAYOUT_A_MN | GEMM_LAYOUT_B_MN)) != 0)
@@ -335,6 +338,10 @@ gemm_status_t build_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, co
 
   const bool persistent = variant >= GEMM_VARIANT_S6_PERSISTENT && variant <= GEMM_VARIANT_S9_TWO_CONSUMERS;
   if (persistent) p->sched = o.sched ? o.sched : GEMM_SCHED_STATIC;
+  if (o.sched == GEMM_SCHED_STREAM_K && (!is_ws(variant) || is_mx(dtype))) {
+    delete p;
+    return GEMM_ERR_UNSUPPORTED_SHAPE;
+  }
 
   if (variant == GEMM_VARIANT_S5_PIPELINE || variant == GEMM_VARIANT_S6_PERSISTENT) {
     p->stages = o.stages ? o.stages : (variant == GEMM_VARIANT_S5_PIPELINE ? 2 : 4);
@@ -384,6 +391,15 @@ gemm_status_t build_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, co
     int units = (p->sched == GEMM_SCHED_CLC) ? tiles : std::min(tiles, active);
     if (o.max_ctas && p->sched != GEMM_SCHED_CLC) units = std::max(1, std::min(units, (int)o.max_ctas));
     p->grid_units = units;
+    // stream-K by default when whole tiles would leave the clusters idle for over
+    // 30 % of the waves (and every cluster still gets a full tile's work).  Measured
+    // on GB300: 80 tiles on 76 CTA pairs (4096 x 2560 x 8192, step 9) 1115 -> 1507
+    // TFLOP/s; at 84 % (4096^3) the split tiles' partial sums cost more than the
+    // idle clusters (1494 -> 1242), so whole tiles stay the default there.
+    if (!o.sched && !p->in_mx && tiles >= active && active > 0) {
+      const int waves = (tiles + active - 1) / active;
+      if ((double)tiles / ((double)waves * active) < 0.7) p->sched = GEMM_SCHED_STREAM_K;
+    }
   } else {
     p->grid_units = tiles;
   }
@@ -405,6 +421,22 @@ gemm_status_t build_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, co
   }
   p->kbase.status = p->scratch;
   p->tgbase.status = p->scratch;
+  if (p->sched == GEMM_SCHED_STREAM_K) {
+    const size_t slot = ws_sk_slot_floats(p->cg, p->consumers);
+    p->sk_flag_bytes = (size_t)p->grid_units * p->cg * p->consumers * 4 * sizeof(uint32_t);
+    if (cudaMalloc(reinterpret_cast<void**>(&p->sk_ws), (size_t)p->grid_units * slot * sizeof(float)) != cudaSuccess ||
+        cudaMalloc(reinterpret_cast<void**>(&p->sk_flags), p->sk_flag_bytes) != cudaSuccess) {
+      cudaGetLastError();
+      gemm_plan_destroy(p);
+      return GEMM_ERR_OOM;
+    }
+    if (cudaMemset(p->sk_flags, 0, p->sk_flag_bytes) != cudaSuccess) {
+      gemm_plan_destroy(p);
+      return GEMM_ERR_CUDA;
+    }
+    p->kbase.sk_ws = p->sk_ws;
+    p->kbase.sk_flags = p->sk_flags;
+  }
   *out = p;
   return GEMM_OK;
 }
@@ -589,8 +621,10 @@ gemm_status_t check_plan(gemm_plan_s* p) {
     return GEMM_ERR_CUDA;
   }
   if (word != 0) {
-    // rewind the status word and the scheduler counters for the next launch
+    // rewind the status word, the scheduler counters and any stream-K flags left
+    // set by an aborted launch
     cudaMemset(p->scratch, 0, 256);
+    if (p->sk_flags) cudaMemset(p->sk_flags, 0, p->sk_flag_bytes);
     return GEMM_ERR_DEVICE_TIMEOUT;
   }
   return GEMM_OK;
@@ -743,6 +777,8 @@ gemm_status_t gemm_plan_set_visits(gemm_plan_t p, int32_t* visits) {
 void gemm_plan_destroy(gemm_plan_t p) {
   if (!p) return;
   if (p->scratch) cudaFree(p->scratch);
+  if (p->sk_ws) cudaFree(p->sk_ws);
+  if (p->sk_flags) cudaFree(p->sk_flags);
   delete p;
 }
 

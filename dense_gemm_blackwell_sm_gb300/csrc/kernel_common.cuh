@@ -26,6 +26,7 @@ enum : uint32_t {
   WAIT_LADDER_MMA = 0x7108u,
   WAIT_LADDER_TMA = 0x7109u,
   WAIT_DRAIN = 0x710Au,
+  WAIT_SK_PARTIAL = 0x710Bu,
 };
 
 // test hook: the producer leaves out one TMA load of the first stage while
@@ -60,6 +61,10 @@ struct KParams {
   // fused-epilogue dequantisation: acc * scale_a[row] * scale_b[col] before the bias
   const float* scale_a;  // M fp32 values, or null
   const float* scale_b;  // N fp32 values, or null
+  // stream-K (steps 7-9): fp32 workspace of one slot per cluster and one flag per
+  // writeback warp of each slot (zero between launches)
+  float* sk_ws;
+  uint32_t* sk_flags;
 };
 
 constexpr uint32_t LAYOUT_A_MN = 1u;

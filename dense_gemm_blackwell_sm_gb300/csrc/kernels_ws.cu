@@ -24,6 +24,10 @@ void* pick_kernel(int sched, bool out_f32, int fused_act) {
     if (NCONS != 1) return nullptr;
     return out_f32 ? pick_fused<float, CG>(fused_act) : pick_fused<__nv_bfloat16, CG>(fused_act);
   }
+  if (sched == SCHED_STREAM_K) {
+    return out_f32 ? reinterpret_cast<void*>(k_ws_sk<float, CG, NCONS>)
+                   : reinterpret_cast<void*>(k_ws_sk<__nv_bfloat16, CG, NCONS>);
+  }
   if (out_f32) {
     if (sched == SCHED_ATOMIC) return ws_kernel_ptr<float, CG, NCONS, SCHED_ATOMIC>();
     if (sched == SCHED_CLC) return ws_kernel_ptr<float, CG, NCONS, SCHED_CLC>();
@@ -56,6 +60,8 @@ WsShape ws_shape(int cg, int consumers) {
   s.threads = WS_THREADS;
   return s;
 }
+
+size_t ws_sk_slot_floats(int cg, int consumers) { return (size_t)cg * consumers * 4 * SK_WARP_FLOATS; }
 
 size_t ws_smem_bytes(int cg, int consumers, int stages) {
   return 1024 + (size_t)stages * ws_shape(cg, consumers).stage_bytes + WS_STAGING + WS_CTRL;

@@ -45,6 +45,20 @@
 // writeback stages through one 4 KB buffer per warp instead of two to leave
 // shared memory for the scale blocks.
 //
+// Stream-K (SK template flag, static schedule, plain writeback): instead of
+// whole tiles, every cluster takes an equal, contiguous share of the flattened
+// (tile, K block) iterations, so the last wave no longer leaves clusters idle
+// (4096^3 with 512x256 tiles: 128 tiles on 76 CTA pairs are 1.68 waves of
+// whole tiles).  Shares are at least one tile long, so a tile is split between
+// at most two consecutive clusters: the later one computes the tile's last K
+// blocks first ("head" part) and writes that fp32 partial to a workspace slot,
+// one flag per writeback warp; the earlier one computes the first K blocks
+// last ("owner" part), waits (bounded) for the flags, adds the partial and
+// stores the tile.  No cluster waits on one that has not started, the owner
+// clears the flags it consumed, and the layout of a slot follows the
+// writeback warps' own (warp, chunk, lane) order so both sides move whole
+// 4 KB runs.
+//
 // In a CTA pair, each CTA loads its own 128 rows of A and its own 128 rows of B
 // (the pair MMA splits A along M and B along N) with the cta_group::2 TMA form,
 // whose completion is counted on the leader CTA's barrier; only the leader
@@ -58,7 +72,7 @@ namespace dgb {
 
 namespace {
 
-enum SchedWs { SCHED_STATIC = 0, SCHED_ATOMIC = 1, SCHED_CLC = 2 };
+enum SchedWs { SCHED_STATIC = 0, SCHED_ATOMIC = 1, SCHED_CLC = 2, SCHED_STREAM_K = 3 };
 
 constexpr int WS_THREADS = 256;
 constexpr int WS_BN = 256;          // tile columns (MMA N)
@@ -68,9 +82,23 @@ constexpr int WS_STAGING = 4 * 2 * 4096;      // 4 writeback warps x 2 buffers x
 constexpr int WS_CTRL = 512;        // barriers and small state
 constexpr int WS_MAX_STAGES = 8;
 constexpr size_t WS_SMEM_LIMIT = 232448;  // 227 KB per CTA
+constexpr int SK_WARP_FLOATS = (WS_BN / 32) * 32 * 32;  // one writeback warp's 32 x 256 fp32 part
 constexpr uint32_t MX_BLOCK = 512;  // scales of 128 rows x 128 K-elements (4 per row)
 constexpr uint32_t MX_TMEM_COL = 256;  // first TMEM column of the per-stage scale slots
 constexpr uint32_t MX_TMEM_SLOT = 16;  // TMEM columns per stage: 4 for A, 8 for B
+
+// v[j] += part[j] for 32 fp32 values held as bit patterns
+__device__ __forceinline__ void sk_add32(uint32_t (&v)[32], const float* part) {
+  const float4* s4 = reinterpret_cast<const float4*>(part);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const float4 a = s4[j];
+    v[4 * j] = __float_as_uint(__uint_as_float(v[4 * j]) + a.x);
+    v[4 * j + 1] = __float_as_uint(__uint_as_float(v[4 * j + 1]) + a.y);
+    v[4 * j + 2] = __float_as_uint(__uint_as_float(v[4 * j + 2]) + a.z);
+    v[4 * j + 3] = __float_as_uint(__uint_as_float(v[4 * j + 3]) + a.w);
+  }
+}
 
 template <int CG, int NCONS>
 struct WsCfg {
@@ -90,11 +118,12 @@ struct WsCfg {
 // activation EPI.  MX: 8-bit inputs with UE8M0 block scales read through
 // tmSA / tmSB (one consumer only).  The tensor maps are kernel parameters of
 // the entry points below.
-template <typename OutT, int CG, int NCONS, int SCHED, int EPI, bool MX>
+template <typename OutT, int CG, int NCONS, int SCHED, int EPI, bool MX, bool SK = false>
 __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMap* tmB, const CUtensorMap* tmC,
                                         const CUtensorMap* tmSA, const CUtensorMap* tmSB, const KParams& p) {
   using Cfg = WsCfg<CG, NCONS>;
   static_assert(!MX || NCONS == 1, "MX block scaling runs with one MMA consumer");
+  static_assert(!SK || (!MX && EPI < 0 && SCHED == SCHED_STATIC), "stream-K: plain writeback, static schedule");
   // MX on the pair: a separate warp copies the scales and takes tile ids from the ring
   constexpr bool MX_COPIER = MX && CG == 2;
   constexpr uint32_t RING_CONS = Cfg::RING_CONSUMERS + (MX_COPIER ? 1u : 0u);
@@ -181,6 +210,20 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
   const bool a_mn = (p.layout & LAYOUT_A_MN) != 0u;
   const bool b_mn = (p.layout & LAYOUT_B_MN) != 0u;
 
+  // stream-K: this cluster's share [sk_b, sk_e) of the flattened (tile, K block)
+  // iterations, walked as segments of one tile each
+  const int64_t sk_total = (int64_t)p.tiles_m * p.tiles_n * KB;
+  const int64_t sk_units = (int64_t)(gridDim.x / CG), sk_cid = (int64_t)(blockIdx.x / CG);
+  const int64_t sk_b = sk_total * sk_cid / sk_units, sk_e = sk_total * (sk_cid + 1) / sk_units;
+  auto sk_next = [&](int64_t& it, int32_t& tile, int32_t& kb0, int32_t& kb1) -> bool {
+    if (it >= sk_e) return false;
+    tile = (int32_t)(it / KB);
+    kb0 = (int32_t)(it - (int64_t)tile * KB);
+    kb1 = (int32_t)min((int64_t)KB, kb0 + (sk_e - it));
+    it += kb1 - kb0;
+    return true;
+  };
+
   // one lane takes the next entry of the tile-id ring; -1 ends the stream
   auto ring_get = [&](uint32_t i, int32_t& tile) -> bool {
     const uint32_t slot = i % WS_RING, ph = (i / WS_RING) & 1u;
@@ -194,7 +237,7 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
     return true;
   };
 
-  if (warp == 2) {
+  if (warp == 2 && !SK) {
     // ------------------------------------------------------------- scheduler
     if (lane == 0 && leader) {
       const int32_t total = p.tiles_m * p.tiles_n;
@@ -250,15 +293,20 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
       uint32_t stage = 0, sphase = 0;
       bool skip = (p.debug_flags & DEBUG_SKIP_ONE_LOAD) != 0u;
       bool ok = true;
+      int64_t sk_it = sk_b;
       for (uint32_t i = 0; ok; ++i) {
-        int32_t tile;
-        if (!ring_get(i, tile)) { ok = false; break; }
-        if (tile < 0) break;
+        int32_t tile, kb0 = 0, kb1 = KB;
+        if constexpr (SK) {
+          if (!sk_next(sk_it, tile, kb0, kb1)) break;
+        } else {
+          if (!ring_get(i, tile)) { ok = false; break; }
+          if (tile < 0) break;
+        }
         int32_t tm, tn;
         raster_tile(tile, p.tiles_m, p.tiles_n, p.raster_group, tm, tn);
         const int32_t m_cta = tm * Cfg::TILE_M + (int32_t)rank * 128;
         const int32_t n_cta = tn * WS_BN + (CG == 2 ? (int32_t)rank * 128 : 0);
-        for (int32_t kb = 0; kb < KB; ++kb) {
+        for (int32_t kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(smem_u32(empty + stage), sphase ^ 1u, w, WAIT_PRODUCER_EMPTY)) { ok = false; break; }
           const uint32_t fb = smem_u32(full + stage);
           // MX: one block of A scales and one box holding the two blocks of B scales
@@ -333,16 +381,22 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
     if (lane == 0) {
       const int cons = (warp == 1) ? 0 : 1;
       uint32_t stage = 0, sphase = 0;
+      int64_t sk_it = sk_b;
       for (uint32_t i = 0;; ++i) {
-        int32_t tile;
-        if (!ring_get(i, tile) || tile < 0) break;
+        int32_t tile, kb0 = 0, kb1 = KB;
+        if constexpr (SK) {
+          if (!sk_next(sk_it, tile, kb0, kb1)) break;
+        } else {
+          if (!ring_get(i, tile) || tile < 0) break;
+        }
         const uint32_t slot = MX ? 0u : (NCONS == 2) ? (uint32_t)cons : (i & 1u);
         const uint32_t apar = (MX || NCONS == 2) ? (i & 1u) : ((i >> 1) & 1u);
         if (!mbar_wait<CG == 2>(smem_u32(acc_empty + slot), apar ^ 1u, w, WAIT_MMA_ACC_EMPTY)) break;
         tc_fence_after();
         const uint32_t d = tmem + slot * 256u;
         bool ok = true;
-        for (int32_t kb = 0; kb < KB; ++kb) {
+        for (int32_t kb = kb0; kb < kb1; ++kb) {
+          const uint32_t acc0 = (kb != kb0) ? 1u : 0u;  // the segment's first MMA overwrites D
           // MX pair: this stage's scales are in TMEM; the copy warp saw the stage land
           // before copying, so this one wait covers the operands too
           const uint32_t ready = MX_COPIER ? smem_u32(sf_ready + stage) : smem_u32(full + stage);
@@ -372,15 +426,15 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
             for (int k = 0; k < 4; ++k)
               if (k * 32 < rem)
                 mma_mxf8f6f4<CG>(d, ad + 2 * k, bd + 2 * k, p.idesc | ((uint32_t)k << 4) | ((uint32_t)k << 29), sft,
-                                 sft + 4, (kb | k) != 0);
+                                 sft + 4, acc0 | (uint32_t)k);
           } else if (f8) {
 #pragma unroll
             for (int k = 0; k < 4; ++k)
-              mma_f8f6f4<CG>(d, ad + astep * k, bd + bstep * k, p.idesc, (kb | k) != 0);
+              mma_f8f6f4<CG>(d, ad + astep * k, bd + bstep * k, p.idesc, acc0 | (uint32_t)k);
           } else {
 #pragma unroll
             for (int k = 0; k < 4; ++k)
-              mma_f16<CG>(d, ad + astep * k, bd + bstep * k, p.idesc, (kb | k) != 0);
+              mma_f16<CG>(d, ad + astep * k, bd + bstep * k, p.idesc, acc0 | (uint32_t)k);
           }
           if constexpr (CG == 1) {
             mma_commit(smem_u32(empty + stage));
@@ -433,13 +487,18 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
     const uint32_t q = warp & 3u;  // TMEM lane quarter this warp may access
     uint8_t* my_staging = staging + q * WARP_STAGING;
     uint32_t tog = 0;
+    int64_t sk_it = sk_b;
     for (uint32_t i = 0;; ++i) {
-      int32_t tile = -1;
-      uint32_t okr = 1;
-      if (lane == 0) okr = ring_get(i, tile) ? 1u : 0u;
-      okr = __shfl_sync(0xffffffffu, okr, 0);
-      tile = __shfl_sync(0xffffffffu, tile, 0);
-      if (!okr || tile < 0) break;
+      int32_t tile = -1, kb0 = 0, kb1 = KB;
+      if constexpr (SK) {
+        if (!sk_next(sk_it, tile, kb0, kb1)) break;
+      } else {
+        uint32_t okr = 1;
+        if (lane == 0) okr = ring_get(i, tile) ? 1u : 0u;
+        okr = __shfl_sync(0xffffffffu, okr, 0);
+        tile = __shfl_sync(0xffffffffu, tile, 0);
+        if (!okr || tile < 0) break;
+      }
       int32_t tm, tn;
       raster_tile(tile, p.tiles_m, p.tiles_n, p.raster_group, tm, tn);
       bool ok = true;
@@ -455,6 +514,51 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
         const int32_t row0 = tm * Cfg::TILE_M + cons * 128 * CG + (int32_t)rank * 128 + (int32_t)q * 32;
         const int32_t col_base = tn * WS_BN;
         const uint32_t tbase = tmem + ((q * 32u) << 16) + slot * 256u;
+        // stream-K: this warp's 32 x 256 part of a split tile, in a workspace slot of
+        // SK_WARP_FLOATS floats laid out [chunk of 32 columns][lane][32 values]
+        const float* sk_part = nullptr;
+        if constexpr (SK) {
+          const int64_t own = ((sk_cid * CG + rank) * NCONS + cons) * 4 + q;
+          if (kb0 > 0) {
+            // head part (the tile's last K blocks): publish it for the previous cluster
+            float* dst = p.sk_ws + own * SK_WARP_FLOATS;
+#pragma unroll 1
+            for (int c32 = 0; c32 < WS_BN / 32; ++c32) {
+              uint32_t v[32];
+              tmem_ld_32x32b_x32(tbase + (uint32_t)(c32 * 32), v);
+              tmem_wait_ld();
+              if (c32 == WS_BN / 32 - 1) {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                  if constexpr (CG == 1) {
+                    mbar_arrive(smem_u32(acc_empty + slot));
+                  } else {
+                    mbar_arrive_cluster(mapa_shared(smem_u32(acc_empty + slot), 0));
+                  }
+                }
+              }
+              float4* d4 = reinterpret_cast<float4*>(dst + (c32 * 32 + (int)lane) * 32);
+#pragma unroll
+              for (int j = 0; j < 8; ++j)
+                d4[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                    __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+            }
+            __threadfence();
+            __syncwarp();
+            if (lane == 0) st_release_gpu_u32(p.sk_flags + own, 1u);
+            continue;
+          }
+          if (kb1 < KB) {
+            // owner part (the first K blocks): wait for the next cluster's head part
+            const int64_t theirs = own + (int64_t)CG * NCONS * 4;
+            uint32_t okf = 1;
+            if (lane == 0) okf = wait_flag_gpu(p.sk_flags + theirs, w, WAIT_SK_PARTIAL) ? 1u : 0u;
+            okf = __shfl_sync(0xffffffffu, okf, 0);
+            if (!okf) { ok = false; break; }
+            sk_part = p.sk_ws + theirs * SK_WARP_FLOATS;
+          }
+        }
         if constexpr (MX && CW == 64 && EPI < 0) {
           // single accumulator: first pull this warp's 32 x 256 slice into registers
           // as packed bf16 and hand the accumulator back, so the next tile's MMAs
@@ -506,6 +610,13 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
           tmem_ld_32x32b_x32(tbase + (uint32_t)(ch * CW), v0);
           if constexpr (CW == 64) tmem_ld_32x32b_x32(tbase + (uint32_t)(ch * CW + 32), v1);
           tmem_wait_ld();
+          if constexpr (SK) {
+            if (sk_part != nullptr) {
+              // add the other cluster's part of this tile
+              sk_add32(v0, sk_part + ((ch * CW) / 32 * 32 + (int)lane) * 32);
+              if constexpr (CW == 64) sk_add32(v1, sk_part + ((ch * CW) / 32 * 32 + 32 + (int)lane) * 32);
+            }
+          }
           if (ch == NCH - 1) {
             // the whole accumulator is in registers: hand it back to the MMA warp
             tc_fence_before();
@@ -552,7 +663,18 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
         }
       }
       if (!ok) break;
-      if (p.visits != nullptr && q == 0 && lane == 0 && leader) atomicAdd(p.visits + tile, 1);
+      if constexpr (SK) {
+        // the owner part consumed the next cluster's flags: clear them for the next launch
+        if (kb0 == 0 && kb1 < KB) {
+          __syncwarp();
+          if (lane == 0) {
+#pragma unroll 1
+            for (int cons = 0; cons < NCONS; ++cons)
+              p.sk_flags[(((sk_cid + 1) * CG + rank) * NCONS + cons) * 4 + q] = 0u;
+          }
+        }
+      }
+      if (p.visits != nullptr && q == 0 && lane == 0 && leader && (!SK || kb0 == 0)) atomicAdd(p.visits + tile, 1);
     }
     if (lane == 0) bulk_wait_group<0>();
   }
@@ -583,6 +705,14 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
             const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmSA,
             const __grid_constant__ CUtensorMap tmSB, KParams p) {
   ws_body<OutT, CG, 1, SCHED, EPI, true>(&tmA, &tmB, &tmC, &tmSA, &tmSB, p);
+}
+
+// entry point of the stream-K kernels (static schedule, plain writeback)
+template <typename OutT, int CG, int NCONS>
+__global__ void __launch_bounds__(WS_THREADS, 1)
+    k_ws_sk(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+            const __grid_constant__ CUtensorMap tmC, KParams p) {
+  ws_body<OutT, CG, NCONS, SCHED_STATIC, -1, false, true>(&tmA, &tmB, &tmC, nullptr, nullptr, p);
 }
 
 template <typename OutT, int CG, int NCONS, int SCHED, int EPI = -1>

@@ -47,7 +47,7 @@ size_t step6_smem_bytes(int stages);
 // steps 7-9: warp-specialised persistent kernels
 //   cg = 1 (one CTA per 128x256 tile) or 2 (CTA pair, cta_group::2)
 //   consumers = 1 or 2 (second MMA consumer, step 9)
-//   sched: 0 static stride, 1 atomic counter, 2 cluster launch control
+//   sched: 0 static stride, 1 atomic counter, 2 cluster launch control, 3 stream-K
 struct WsShape {
   int cg;
   int consumers;
@@ -62,6 +62,9 @@ WsShape ws_shape(int cg, int consumers);
 size_t ws_smem_bytes(int cg, int consumers, int stages);
 int ws_max_stages(int cg, int consumers);
 int ws_max_active_clusters(int cg, int consumers, int sched, bool out_f32, int stages);
+// stream-K (sched 3): fp32 floats of one cluster's workspace slot; one flag per
+// writeback warp, cg * consumers * 4 per slot
+size_t ws_sk_slot_floats(int cg, int consumers);
 // fused_act >= 0: the writeback applies bias / activation fused_act / residual
 // (one MMA consumer, static scheduler); -1: plain writeback
 cudaError_t spec_ws(int cg, int consumers, int sched, bool out_f32, int stages, int clusters, LaunchSpec* out,

@@ -168,6 +168,30 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const W
   return mbar_wait_slow<CLUSTER_ACQ>(bar, parity, w, code);
 }
 
+// Flags in global memory written by other CTAs of the same grid (all of which
+// are resident): release store, and a bounded acquire-spin for a non-zero value.
+__device__ __forceinline__ void st_release_gpu_u32(uint32_t* f, uint32_t v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(f), "r"(v) : "memory");
+}
+
+static __device__ __noinline__ bool wait_flag_gpu(const uint32_t* f, const WaitCtl& w, uint32_t code) {
+  const uint64_t t0 = globaltimer_ns();
+  uint32_t spins = 0;
+  while (true) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(f) : "memory");
+    if (v != 0u) return true;
+    if ((++spins & 15u) == 0u) {
+      if (*w.abort_flag) return false;
+      if (globaltimer_ns() - t0 > w.timeout_ns) {
+        raise_abort(w, code);
+        return false;
+      }
+    }
+    __nanosleep(32);
+  }
+}
+
 // ---------------------------------------------------------------------------
 // proxies and fences
 

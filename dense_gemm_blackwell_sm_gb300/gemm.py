@@ -35,7 +35,7 @@ VARIANT_NAMES = {0: "auto", 1: "s1_single_tile", 2: "s2_kloop", 3: "s3_multi_cta
                  9: "s9_two_consumers", 10: "gemv", 11: "gemv_tc"}
 
 # gemm_sched_t
-SCHED_AUTO, SCHED_STATIC, SCHED_ATOMIC, SCHED_CLC = 0, 1, 2, 3
+SCHED_AUTO, SCHED_STATIC, SCHED_ATOMIC, SCHED_CLC, SCHED_STREAM_K = 0, 1, 2, 3, 4
 
 # gemm_activation_t
 ACT_NONE, ACT_RELU, ACT_SILU, ACT_GELU_TANH, ACT_GELU_ERF = 0, 1, 2, 3, 4

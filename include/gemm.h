@@ -16,8 +16,10 @@
  * crosses this boundary and no exception escapes it.  Device pointers are
  * owned by the caller; the library never allocates, frees or retains user
  * buffers.  A plan owns host state (cached TMA descriptors) and 256 bytes of
- * device scratch (a status word and scheduler counters), released by
- * gemm_plan_destroy.
+ * device scratch (a status word and scheduler counters), plus, for the
+ * stream-K schedule, a workspace of one fp32 tile per cluster (about 38 MB on
+ * 76 CTA pairs with 512 x 256 tiles), all released by gemm_plan_destroy.  Two
+ * launches of one plan must not overlap on the device.
  *
  * Errors: argument problems are returned at once and nothing is launched.
  * Kernels never trap: every wait inside them is bounded in time, and a wait
@@ -99,7 +101,13 @@ typedef enum {
   GEMM_SCHED_AUTO = 0,
   GEMM_SCHED_STATIC = 1, /* fixed stride over the raster order */
   GEMM_SCHED_ATOMIC = 2, /* global atomic tile counter */
-  GEMM_SCHED_CLC = 3     /* hardware cluster launch control (work stealing) */
+  GEMM_SCHED_CLC = 3,    /* hardware cluster launch control (work stealing) */
+  GEMM_SCHED_STREAM_K = 4 /* variants 7-9: every cluster takes an equal share of the (tile, K
+                             block) iterations; a tile split between two clusters is finished
+                             by the one holding its first K blocks, from the other's fp32
+                             partial in a plan-owned workspace.  The automatic plan uses it
+                             when whole tiles would keep the clusters busy for under 70 % of
+                             the waves.  Fused epilogues and MX plans use whole tiles. */
 } gemm_sched_t;
 
 /* Tuning and test options; zero-initialise and set what you need.

@@ -100,8 +100,10 @@ def test_random_inputs_parity(variant, shape, ti, to):
 
 
 @pytest.mark.parametrize("variant", [gemm.S6, gemm.S7, gemm.S8, gemm.S9])
-@pytest.mark.parametrize("sched", [gemm.SCHED_STATIC, gemm.SCHED_ATOMIC, gemm.SCHED_CLC])
+@pytest.mark.parametrize("sched", [gemm.SCHED_STATIC, gemm.SCHED_ATOMIC, gemm.SCHED_CLC, gemm.SCHED_STREAM_K])
 def test_schedulers_visit_every_tile_once(variant, sched):
+    if variant == gemm.S6 and sched == gemm.SCHED_STREAM_K:
+        pytest.skip("stream-K exists for the warp-specialised kernels only")
     # tile counts below, near and above the number of SMs
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     for M, N in [(512, 512), (2048, 2560), (4096, 4096)]:
@@ -264,3 +266,56 @@ def test_plans_sharing_a_kernel_keep_their_shared_memory():
         assert np.array_equal(c2.double().cpu().numpy(), oracle.gemm(a2, b2)[0])
         big.destroy()
         small.destroy()
+
+
+# stream-K: shapes whose tiles outnumber the resident clusters, with several K
+# blocks per tile, so that tiles are split between two clusters
+SK_SHAPES = {gemm.S7: (1280, 4352, 520), gemm.S8: (1280, 4352, 264), gemm.S9: (2560, 4352, 136)}
+
+
+@pytest.mark.parametrize("variant", [gemm.S7, gemm.S8, gemm.S9])
+@pytest.mark.parametrize("ti,to", [("bf16", "bf16"), ("f16", "f32")])
+def test_stream_k_integer_bit_exact(variant, ti, to):
+    M, N, K = SK_SHAPES[variant]
+    a, b = inputs.integer_operands(M, N, K, ti, seed=variant)
+    plan = gemm.Plan(M, N, K, gemm.dtype_code(ti, to), gemm.make_opts(variant=variant, sched=gemm.SCHED_STREAM_K))
+    info = plan.info()
+    assert info["sched"] == gemm.SCHED_STREAM_K and info["tiles"] > info["grid"] // info["cluster"]
+    c = torch.full((M, N), float("nan"), device=DEV, dtype=inputs.torch_dtype(to))
+    for _ in range(3):   # repeated launches: the flags must be cleared by their consumers
+        c.fill_(float("nan"))
+        plan.run(a.to(DEV), b.to(DEV), c)
+        assert plan.check() == gemm.OK
+    plan.destroy()
+    ref, _ = oracle.gemm(a, b)
+    exp = expect_bits(ref, to)
+    got = c.cpu().numpy() if to == "f32" else c.float().cpu().numpy()
+    bad = np.argwhere(got != exp)
+    assert bad.size == 0, (info, bad[:3])
+
+
+@pytest.mark.parametrize("variant", [gemm.S8, gemm.S9])
+def test_stream_k_random_parity(variant):
+    M, N, K = SK_SHAPES[variant]
+    a, b = inputs.make_operands(M, N, K, "bf16", ("uniform",), ("normal", 1.0), seed=11 + variant)
+    plan = gemm.Plan(M, N, K, gemm.BF16_F32, gemm.make_opts(variant=variant, sched=gemm.SCHED_STREAM_K))
+    c = torch.empty((M, N), device=DEV)
+    plan.run(a.to(DEV), b.to(DEV), c)
+    assert plan.check() == gemm.OK
+    plan.destroy()
+    ref, S = oracle.gemm(a, b)
+    r = parity.check(c.cpu().numpy(), ref, S, "f32")
+    assert r["ok"] and r["max_excess_rel"] < 2.0 ** -12, r
+
+
+def test_stream_k_is_the_default_when_the_last_wave_is_short():
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    pairs = sms // 2
+    # step 9 tiles are 512 x 256: a few more tiles than CTA pairs leaves the second wave nearly empty
+    p = gemm.Plan(512 * 8, 256 * ((pairs + 8) // 8), 1024, gemm.BF16_BF16)
+    info = p.info()
+    p.destroy()
+    assert info["variant"] == gemm.S9 and info["sched"] == gemm.SCHED_STREAM_K, info
+    p = gemm.Plan(8192, 8192, 8192, gemm.BF16_BF16)
+    assert p.info()["sched"] == gemm.SCHED_STATIC       # 512 tiles on 76 pairs: 96 % of seven waves
+    p.destroy()
