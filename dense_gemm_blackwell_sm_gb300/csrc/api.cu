@@ -42,7 +42,7 @@ struct gemm_plan_s {
   dgb::LaunchSpec spec;   // kernel, launch shape and SMEM, fixed at plan time
   dgb::LaunchSpec spec_epi[5];  // the fused-epilogue kernel per activation, made on first use
   bool epi_ready[5];
-  int epi_tiles_m, epi_stages;  // its tiling: one MMA consumer, so the TMEM double buffer lets the
+  int epi_tiles_m, epi_tiles_n, epi_stages;  // its tiling: one MMA consumer, so the TMEM double buffer lets the
                                 // epilogue of one tile overlap the MMAs of the next
   dgb::KParams kbase;     // kernel parameters that do not depend on the pointers
   dgb::TgParams tgbase;   // same, for the tensor-core GEMV
@@ -212,7 +212,7 @@ gemm_status_t prepare_launch(gemm_plan_s* p) {
     k.timeout_ns = p->timeout_ns;
     k.debug_flags = p->debug_flags;
     k.out_ld = (int32_t)p->N;
-    k.idesc = is_ws(v) ? make_idesc(p->in_bf16, 128 * p->cg, 256) : make_idesc(p->in_bf16, 128, 128);
+    k.idesc = is_ws(v) ? make_idesc(p->in_bf16, 128 * p->cg, p->tile_n) : make_idesc(p->in_bf16, 128, 128);
     k.mma_kind = 0;
     k.bk = 64;
     if (p->in_mx) {
@@ -227,7 +227,7 @@ gemm_status_t prepare_launch(gemm_plan_s* p) {
     } else if (p->in_f8) {
       // kind::f8f6f4 descriptor: A / B format E4M3 = 0, E5M2 = 1, fp32 accumulator
       const uint32_t fmt = p->in_e5m2 ? 1u : 0u;
-      k.idesc = (1u << 4) | (fmt << 7) | (fmt << 10) | ((uint32_t)(256 >> 3) << 17) |
+      k.idesc = (1u << 4) | (fmt << 7) | (fmt << 10) | ((uint32_t)(p->tile_n >> 3) << 17) |
                 ((uint32_t)((128 * p->cg) >> 4) << 24);
       k.mma_kind = 1;
       k.bk = 128;
@@ -244,7 +244,7 @@ gemm_status_t prepare_launch(gemm_plan_s* p) {
     } else if (p->in_mx) {
       e = spec_mx(p->cg, p->sched - 1, p->out_f32, p->stages, p->grid_units, &p->spec);
     } else {
-      e = spec_ws(p->cg, p->consumers, p->sched - 1, p->out_f32, p->stages, p->grid_units, &p->spec);
+      e = spec_ws(p->cg, p->consumers, p->sched - 1, p->out_f32, p->stages, p->grid_units, &p->spec, -1, p->tile_n);
     }
   }
   if (e != cudaSuccess) {
@@ -356,6 +356,27 @@ gemm_status_t build_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, co
     p->tile_m = sh.tile_m;
     p->tile_n = sh.tile_n;
     p->smem = ws_smem_bytes(p->cg, p->consumers, p->stages);
+    // Step 9 with whole tiles: switch to 224-column tiles when they fill the waves of
+    // resident CTA pairs clearly better (4096^3: 128 tiles of 512 x 256 on 76 pairs use
+    // 84 % of two waves; 152 tiles of 512 x 224 use both, 96 % of the columns useful)
+    if (variant == GEMM_VARIANT_S9_TWO_CONSUMERS && !p->in_mx && o.layout == 0 &&
+        (o.sched == 0 || o.sched == GEMM_SCHED_STATIC)) {
+      const int units = std::max(1, sms / 2);
+      auto fill = [&](int bn) {
+        const int64_t tn = (N + bn - 1) / bn, tiles = ((M + 511) / 512) * tn;
+        const int64_t u = std::min<int64_t>(tiles, units), waves = (tiles + u - 1) / u;
+        return ((double)N / (double)(tn * bn)) * ((double)tiles / (double)(waves * u));
+      };
+      // (below 70 % with whole 256-column tiles the automatic plan takes stream-K instead)
+      const bool stream_k_instead = !o.sched && fill(256) < 0.7 && ((M + 511) / 512) * ((N + 255) / 256) >= units;
+      if (!stream_k_instead && fill(224) > fill(256) + 0.05) {
+        p->tile_n = 224;
+        const int maxs224 = ws_max_stages(p->cg, p->consumers, 224);
+        p->stages = o.stages ? std::min<int>(o.stages, maxs224) : maxs224;
+        p->smem = ws_smem_bytes(p->cg, p->consumers, p->stages, 224);
+        p->sched = GEMM_SCHED_STATIC;
+      }
+    }
     if (p->in_mx) {
       p->stages = o.stages ? std::min<int>(o.stages, mx_max_stages(p->cg)) : mx_max_stages(p->cg);
       p->smem = mx_smem_bytes(p->cg, p->stages);
@@ -386,7 +407,8 @@ gemm_status_t build_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, co
   } else if (variant >= GEMM_VARIANT_S7_WARP_SPECIALIZED && variant <= GEMM_VARIANT_S9_TWO_CONSUMERS) {
     // (the MX kernels' shared memory also allows one CTA per SM)
     int active = p->in_mx ? sms / p->cg
-                          : ws_max_active_clusters(p->cg, p->consumers, p->sched - 1, p->out_f32, p->stages);
+                          : ws_max_active_clusters(p->cg, p->consumers, p->sched - 1, p->out_f32, p->stages,
+                                                   p->tile_n);
     if (active < 1) active = std::max(1, sms / p->cg);
     int units = (p->sched == GEMM_SCHED_CLC) ? tiles : std::min(tiles, active);
     if (o.max_ctas && p->sched != GEMM_SCHED_CLC) units = std::max(1, std::min(units, (int)o.max_ctas));
@@ -396,7 +418,7 @@ gemm_status_t build_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, co
     // on GB300: 80 tiles on 76 CTA pairs (4096 x 2560 x 8192, step 9) 1115 -> 1507
     // TFLOP/s; at 84 % (4096^3) the split tiles' partial sums cost more than the
     // idle clusters (1494 -> 1242), so whole tiles stay the default there.
-    if (!o.sched && !p->in_mx && tiles >= active && active > 0) {
+    if (!o.sched && !p->in_mx && p->tile_n == 256 && tiles >= active && active > 0) {
       const int waves = (tiles + active - 1) / active;
       if ((double)tiles / ((double)waves * active) < 0.7) p->sched = GEMM_SCHED_STREAM_K;
     }
@@ -476,8 +498,11 @@ const CUtensorMap* operand_map(gemm_plan_s* p, int role, const void* ptr) {
     ok = encode_2d(&victim->map, in_t, 2, ptr, (uint64_t)p->N, (uint64_t)p->K, 64, 64);
   } else if (role == 0) {
     ok = encode_2d(&victim->map, in_t, ie, ptr, (uint64_t)p->K, (uint64_t)p->M, kbox, 128);
-  } else if (role == 1) {
-    const uint32_t rows = is_ws(p->variant) ? (uint32_t)ws_shape(p->cg, p->consumers).b_box_rows : 128u;
+  } else if (role == 1 || role == 6) {
+    // role 6: B for the fused-epilogue kernels (one consumer, 256-column tiles)
+    const uint32_t rows = !is_ws(p->variant) ? 128u
+                          : role == 6        ? (uint32_t)ws_shape(p->cg, 1).b_box_rows
+                                             : (uint32_t)ws_shape(p->cg, p->consumers, p->tile_n).b_box_rows;
     ok = encode_2d(&victim->map, in_t, ie, ptr, (uint64_t)p->K, (uint64_t)p->N, kbox, rows);
   } else {
     ok = p->out_f32 ? encode_2d(&victim->map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, ptr, (uint64_t)p->N,
@@ -534,7 +559,10 @@ gemm_status_t launch_plan(gemm_plan_s* p, const void* A, const void* B, void* C,
         k.scale_a = epi->scale_a;
         k.scale_b = epi->scale_b;
         k.tiles_m = p->epi_tiles_m;
+        k.tiles_n = p->epi_tiles_n;
         k.stages = p->epi_stages;
+        // the fused kernels' MMAs are 256 columns wide whatever the plan's own tile
+        k.idesc = (k.idesc & ~(0x3Fu << 17)) | ((256u >> 3) << 17);
         spec = &p->spec_epi[epi->activation];
       }
       k.A = static_cast<const uint16_t*>(A);
@@ -546,7 +574,8 @@ gemm_status_t launch_plan(gemm_plan_s* p, const void* A, const void* B, void* C,
         break;
       }
       const CUtensorMap* ma = operand_map(p, 0, A);
-      const CUtensorMap* mb = operand_map(p, 1, B);
+      // (the fused kernels read B in 256-column tiles even where the plan's own are narrower)
+      const CUtensorMap* mb = operand_map(p, (epi != nullptr && p->tile_n != 256) ? 6 : 1, B);
       if (!ma || !mb) return GEMM_ERR_CUDA;
       if (spec->kind == ARGS_AB_K) {
         void* args[] = {const_cast<CUtensorMap*>(ma), const_cast<CUtensorMap*>(mb), &k};
@@ -590,6 +619,7 @@ gemm_status_t run_with_epilogue(gemm_plan_s* plan, const void* A, const void* B,
       // the block-scaled plan already runs one consumer on one CTA
       plan->epi_stages = plan->stages;
       plan->epi_tiles_m = plan->tiles_m;
+      plan->epi_tiles_n = plan->tiles_n;
       e = spec_mx(plan->cg, 0, plan->out_f32, plan->stages, std::min(plan->grid_units, plan->tiles_m * plan->tiles_n),
                   &plan->spec_epi[act], act);
     } else {
@@ -599,7 +629,8 @@ gemm_status_t run_with_epilogue(gemm_plan_s* plan, const void* A, const void* B,
       const int cons = 1;
       plan->epi_stages = ws_max_stages(plan->cg, cons);
       plan->epi_tiles_m = ceil_div(plan->M, 128 * plan->cg * cons);
-      const int tiles = plan->epi_tiles_m * plan->tiles_n;
+      plan->epi_tiles_n = ceil_div(plan->N, 256);  // the fused kernels use 256-column tiles
+      const int tiles = plan->epi_tiles_m * plan->epi_tiles_n;
       int active = ws_max_active_clusters(plan->cg, cons, 0, plan->out_f32, plan->epi_stages);
       if (active < 1) active = std::max(1, plan->num_sms / plan->cg);
       e = spec_ws(plan->cg, cons, 0, plan->out_f32, plan->epi_stages, std::min(tiles, active), &plan->spec_epi[act],

@@ -38,7 +38,15 @@ void* pick_kernel(int sched, bool out_f32, int fused_act) {
   return ws_kernel_ptr<__nv_bfloat16, CG, NCONS, SCHED_STATIC>();
 }
 
-void* ws_kernel(int cg, int consumers, int sched, bool out_f32, int fused_act = -1) {
+// The 224-column tile exists for step 9 with the static schedule and the plain
+// writeback (the shapes whose waves it evens out).
+void* ws_kernel(int cg, int consumers, int sched, bool out_f32, int fused_act = -1, int bn = WS_BN) {
+  if (bn == 224) {
+    if (cg != 2 || consumers != 2 || sched != SCHED_STATIC || fused_act >= 0) return nullptr;
+    return out_f32 ? ws_kernel_ptr<float, 2, 2, SCHED_STATIC, -1, 224>()
+                   : ws_kernel_ptr<__nv_bfloat16, 2, 2, SCHED_STATIC, -1, 224>();
+  }
+  if (bn != WS_BN) return nullptr;
   if (cg == 1 && consumers == 1) return pick_kernel<1, 1>(sched, out_f32, fused_act);
   if (cg == 1 && consumers == 2) return pick_kernel<1, 2>(sched, out_f32, fused_act);
   if (cg == 2 && consumers == 1) return pick_kernel<2, 1>(sched, out_f32, fused_act);
@@ -48,14 +56,14 @@ void* ws_kernel(int cg, int consumers, int sched, bool out_f32, int fused_act = 
 
 }  // namespace
 
-WsShape ws_shape(int cg, int consumers) {
+WsShape ws_shape(int cg, int consumers, int bn) {
   WsShape s{};
   s.cg = cg;
   s.consumers = consumers;
   s.tile_m = 128 * cg * consumers;
-  s.tile_n = WS_BN;
+  s.tile_n = bn;
   s.a_box_rows = 128;
-  s.b_box_rows = (cg == 1) ? 256 : 128;
+  s.b_box_rows = (cg == 1) ? bn : bn / 2;
   s.stage_bytes = consumers * (int)WS_A_BYTES + s.b_box_rows * 128;
   s.threads = WS_THREADS;
   return s;
@@ -63,13 +71,13 @@ WsShape ws_shape(int cg, int consumers) {
 
 size_t ws_sk_slot_floats(int cg, int consumers) { return (size_t)cg * consumers * 4 * SK_WARP_FLOATS; }
 
-size_t ws_smem_bytes(int cg, int consumers, int stages) {
-  return 1024 + (size_t)stages * ws_shape(cg, consumers).stage_bytes + WS_STAGING + WS_CTRL;
+size_t ws_smem_bytes(int cg, int consumers, int stages, int bn) {
+  return 1024 + (size_t)stages * ws_shape(cg, consumers, bn).stage_bytes + WS_STAGING + WS_CTRL;
 }
 
-int ws_max_stages(int cg, int consumers) {
+int ws_max_stages(int cg, int consumers, int bn) {
   int s = WS_MAX_STAGES;
-  while (s > 1 && ws_smem_bytes(cg, consumers, s) > WS_SMEM_LIMIT) --s;
+  while (s > 1 && ws_smem_bytes(cg, consumers, s, bn) > WS_SMEM_LIMIT) --s;
   return s;
 }
 
@@ -89,10 +97,10 @@ static cudaLaunchConfig_t ws_config(int cg, int clusters, size_t smem, cudaStrea
   return cfg;
 }
 
-int ws_max_active_clusters(int cg, int consumers, int sched, bool out_f32, int stages) {
-  void* k = ws_kernel(cg, consumers, sched, out_f32);
+int ws_max_active_clusters(int cg, int consumers, int sched, bool out_f32, int stages, int bn) {
+  void* k = ws_kernel(cg, consumers, sched, out_f32, -1, bn);
   if (!k) return 0;
-  const size_t smem = ws_smem_bytes(cg, consumers, stages);
+  const size_t smem = ws_smem_bytes(cg, consumers, stages, bn);
   if (allow_dynamic_smem((const void*)k, smem) != cudaSuccess) return 0;
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = ws_config(cg, 1, smem, nullptr, attr);
@@ -105,10 +113,10 @@ int ws_max_active_clusters(int cg, int consumers, int sched, bool out_f32, int s
 }
 
 cudaError_t spec_ws(int cg, int consumers, int sched, bool out_f32, int stages, int clusters, LaunchSpec* out,
-                    int fused_act) {
-  void* k = ws_kernel(cg, consumers, fused_act >= 0 ? SCHED_STATIC : sched, out_f32, fused_act);
+                    int fused_act, int bn) {
+  void* k = ws_kernel(cg, consumers, fused_act >= 0 ? SCHED_STATIC : sched, out_f32, fused_act, bn);
   if (!k) return cudaErrorInvalidValue;
-  const size_t smem = ws_smem_bytes(cg, consumers, stages);
+  const size_t smem = ws_smem_bytes(cg, consumers, stages, bn);
   cudaError_t e = allow_dynamic_smem((const void*)k, smem);
   if (e != cudaSuccess) return e;
   out->func = k;

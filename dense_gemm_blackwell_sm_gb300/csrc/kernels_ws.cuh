@@ -100,9 +100,11 @@ __device__ __forceinline__ void sk_add32(uint32_t (&v)[32], const float* part) {
   }
 }
 
-template <int CG, int NCONS>
+// BN: tile columns (MMA N), 256 or 224 (the narrower tile evens out the waves
+// of shapes such as 4096^3, whose 512 x 256 tiles fill 1.68 waves of CTA pairs)
+template <int CG, int NCONS, int BN = WS_BN>
 struct WsCfg {
-  static constexpr int B_ROWS = (CG == 1) ? 256 : 128;
+  static constexpr int B_ROWS = (CG == 1) ? BN : BN / 2;
   static constexpr uint32_t B_BYTES = (uint32_t)B_ROWS * 128u;
   static constexpr uint32_t STAGE = NCONS * WS_A_BYTES + B_BYTES;  // per CTA
   static constexpr int TILE_M = 128 * CG * NCONS;
@@ -118,11 +120,12 @@ struct WsCfg {
 // activation EPI.  MX: 8-bit inputs with UE8M0 block scales read through
 // tmSA / tmSB (one consumer only).  The tensor maps are kernel parameters of
 // the entry points below.
-template <typename OutT, int CG, int NCONS, int SCHED, int EPI, bool MX, bool SK = false>
+template <typename OutT, int CG, int NCONS, int SCHED, int EPI, bool MX, bool SK = false, int BN = WS_BN>
 __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMap* tmB, const CUtensorMap* tmC,
                                         const CUtensorMap* tmSA, const CUtensorMap* tmSB, const KParams& p) {
-  using Cfg = WsCfg<CG, NCONS>;
+  using Cfg = WsCfg<CG, NCONS, BN>;
   static_assert(!MX || NCONS == 1, "MX block scaling runs with one MMA consumer");
+  static_assert(BN == WS_BN || (!MX && !SK && EPI < 0), "narrow tiles: plain writeback, whole tiles");
   static_assert(!SK || (!MX && EPI < 0 && SCHED == SCHED_STATIC), "stream-K: plain writeback, static schedule");
   // MX on the pair: a separate warp copies the scales and takes tile ids from the ring
   constexpr bool MX_COPIER = MX && CG == 2;
@@ -130,7 +133,8 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
   constexpr uint32_t STAGING = MX ? WS_STAGING / 2 : WS_STAGING;
   constexpr uint32_t WARP_STAGING = STAGING / 4;
   constexpr int CW = (sizeof(OutT) == 4) ? 32 : 64;  // output columns per 128-byte staging row
-  constexpr int NCH = WS_BN / CW;
+  constexpr int NCH = BN / CW;      // whole 128-byte staging chunks of a row
+  constexpr int TAIL = BN % CW;     // bf16 with BN = 224: 32 more columns, stored from registers
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align_1024(smem_raw);
@@ -305,13 +309,13 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
         int32_t tm, tn;
         raster_tile(tile, p.tiles_m, p.tiles_n, p.raster_group, tm, tn);
         const int32_t m_cta = tm * Cfg::TILE_M + (int32_t)rank * 128;
-        const int32_t n_cta = tn * WS_BN + (CG == 2 ? (int32_t)rank * 128 : 0);
+        const int32_t n_cta = tn * BN + (CG == 2 ? (int32_t)rank * (BN / 2) : 0);
         for (int32_t kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(smem_u32(empty + stage), sphase ^ 1u, w, WAIT_PRODUCER_EMPTY)) { ok = false; break; }
           const uint32_t fb = smem_u32(full + stage);
           // MX: one block of A scales and one box holding the two blocks of B scales
           // (a block past the array's last row group arrives as zeros)
-          const int32_t n_tile = tn * WS_BN;
+          const int32_t n_tile = tn * BN;
           const uint32_t mx_tx = MX ? 3u * MX_BLOCK : 0u;
           if (leader) mbar_arrive_expect_tx(fb, (Cfg::STAGE + mx_tx) * CG);
           uint8_t* st = ring + (size_t)stage * Cfg::STAGE;
@@ -512,7 +516,7 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
         if (!got) { ok = false; break; }
         tc_fence_after();
         const int32_t row0 = tm * Cfg::TILE_M + cons * 128 * CG + (int32_t)rank * 128 + (int32_t)q * 32;
-        const int32_t col_base = tn * WS_BN;
+        const int32_t col_base = tn * BN;
         const uint32_t tbase = tmem + ((q * 32u) << 16) + slot * 256u;
         // stream-K: this warp's 32 x 256 part of a split tile, in a workspace slot of
         // SK_WARP_FLOATS floats laid out [chunk of 32 columns][lane][32 values]
@@ -604,6 +608,22 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
           }
           continue;
         }
+        if constexpr (TAIL > 0) {
+          // bf16 with a 224-column tile: columns 192-223 go straight from registers to
+          // C (64 bytes of the lane's row; N % 8 == 0, so each 8-column group is in or out)
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(tbase + (uint32_t)(NCH * CW), v);
+          tmem_wait_ld();
+          const int32_t row = row0 + (int32_t)lane, col = col_base + NCH * CW;
+          if (row < p.M) {
+            uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<OutT*>(p.C) + (int64_t)row * p.out_ld + col);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              if (col + 8 * j < p.N)
+                dst[j] = make_uint4(pack_bf16x2(v[8 * j], v[8 * j + 1]), pack_bf16x2(v[8 * j + 2], v[8 * j + 3]),
+                                    pack_bf16x2(v[8 * j + 4], v[8 * j + 5]), pack_bf16x2(v[8 * j + 6], v[8 * j + 7]));
+          }
+        }
 #pragma unroll 1
         for (int ch = 0; ch < NCH; ++ch) {
           uint32_t v0[32], v1[32];
@@ -691,11 +711,11 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
 }
 
 // entry point of the fp16 / bf16 / 8-bit float kernels
-template <typename OutT, int CG, int NCONS, int SCHED, int EPI = -1>
+template <typename OutT, int CG, int NCONS, int SCHED, int EPI = -1, int BN = WS_BN>
 __global__ void __launch_bounds__(WS_THREADS, 1)
     k_ws(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
          const __grid_constant__ CUtensorMap tmC, KParams p) {
-  ws_body<OutT, CG, NCONS, SCHED, EPI, false>(&tmA, &tmB, &tmC, nullptr, nullptr, p);
+  ws_body<OutT, CG, NCONS, SCHED, EPI, false, false, BN>(&tmA, &tmB, &tmC, nullptr, nullptr, p);
 }
 
 // entry point of the MX block-scaled kernels (one consumer)
@@ -715,9 +735,9 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
   ws_body<OutT, CG, NCONS, SCHED_STATIC, -1, false, true>(&tmA, &tmB, &tmC, nullptr, nullptr, p);
 }
 
-template <typename OutT, int CG, int NCONS, int SCHED, int EPI = -1>
+template <typename OutT, int CG, int NCONS, int SCHED, int EPI = -1, int BN = WS_BN>
 void* ws_kernel_ptr() {
-  return reinterpret_cast<void*>(k_ws<OutT, CG, NCONS, SCHED, EPI>);
+  return reinterpret_cast<void*>(k_ws<OutT, CG, NCONS, SCHED, EPI, BN>);
 }
 
 template <typename OutT, int CG, int SCHED, int EPI = -1>

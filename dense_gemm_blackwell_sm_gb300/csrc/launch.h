@@ -58,17 +58,19 @@ struct WsShape {
   int stage_bytes;  // per CTA
   int threads;
 };
-WsShape ws_shape(int cg, int consumers);
-size_t ws_smem_bytes(int cg, int consumers, int stages);
-int ws_max_stages(int cg, int consumers);
-int ws_max_active_clusters(int cg, int consumers, int sched, bool out_f32, int stages);
+// bn: tile columns, 256, or 224 for step 9 (cg 2, 2 consumers) with the static
+// schedule and the plain writeback
+WsShape ws_shape(int cg, int consumers, int bn = 256);
+size_t ws_smem_bytes(int cg, int consumers, int stages, int bn = 256);
+int ws_max_stages(int cg, int consumers, int bn = 256);
+int ws_max_active_clusters(int cg, int consumers, int sched, bool out_f32, int stages, int bn = 256);
 // stream-K (sched 3): fp32 floats of one cluster's workspace slot; one flag per
 // writeback warp, cg * consumers * 4 per slot
 size_t ws_sk_slot_floats(int cg, int consumers);
 // fused_act >= 0: the writeback applies bias / activation fused_act / residual
 // (one MMA consumer, static scheduler); -1: plain writeback
 cudaError_t spec_ws(int cg, int consumers, int sched, bool out_f32, int stages, int clusters, LaunchSpec* out,
-                    int fused_act = -1);
+                    int fused_act = -1, int bn = 256);
 
 // steps 7 and 8 with MX block scales (8-bit inputs, UE8M0 scale per 32 K
 // elements): cg = 1 (one CTA per 128x256 tile) or 2 (CTA pair, 256x256), one

@@ -319,3 +319,47 @@ def test_stream_k_is_the_default_when_the_last_wave_is_short():
     p = gemm.Plan(8192, 8192, 8192, gemm.BF16_BF16)
     assert p.info()["sched"] == gemm.SCHED_STATIC       # 512 tiles on 76 pairs: 96 % of seven waves
     p.destroy()
+
+
+# step 9 with 224-column tiles: chosen when they fill the waves of CTA pairs better;
+# N = 18 * 224 + 200 puts the edge inside the last 32-column band of the last tile
+NARROW = [(4096, 4232, 200), (4096, 4096, 136)]
+
+
+@pytest.mark.parametrize("shape", NARROW)
+@pytest.mark.parametrize("ti,to", [("bf16", "bf16"), ("f16", "f32")])
+def test_narrow_tiles_integer_bit_exact(shape, ti, to):
+    M, N, K = shape
+    a, b = inputs.integer_operands(M, N, K, ti, seed=N)
+    plan = gemm.Plan(M, N, K, gemm.dtype_code(ti, to))
+    info = plan.info()
+    assert info["variant"] == gemm.S9 and info["tile_n"] == 224, info
+    c = torch.full((M, N), float("nan"), device=DEV, dtype=inputs.torch_dtype(to))
+    plan.run(a.to(DEV), b.to(DEV), c)
+    assert plan.check() == gemm.OK
+    ref, _ = oracle.gemm(a, b)
+    exp = expect_bits(ref, to)
+    got = c.float().cpu().numpy()
+    bad = np.argwhere(got != exp)
+    assert bad.size == 0, (info, bad[:3])
+    # the fused epilogue on the same plan runs its own 256-column tiles
+    bias = torch.randint(-4, 5, (N,), generator=torch.Generator().manual_seed(1)).float()
+    c2 = torch.full((M, N), float("nan"), device=DEV, dtype=inputs.torch_dtype(to))
+    plan.run_epilogue(a.to(DEV), b.to(DEV), c2, bias=bias.to(DEV), act=gemm.ACT_RELU)
+    assert plan.check() == gemm.OK
+    exp2 = expect_bits(oracle.epilogue(ref, bias, None, oracle.ACT_RELU), to)
+    assert np.array_equal(c2.float().cpu().numpy(), exp2)
+    plan.destroy()
+
+
+def test_narrow_tiles_fp8():
+    M, N, K = 4096, 4232, 256
+    a, b = inputs.integer_operands(M, N, K, "e4m3", seed=3, lo=-4, hi=4)
+    plan = gemm.Plan(M, N, K, gemm.E4M3_BF16)
+    assert plan.info()["tile_n"] == 224
+    c = torch.empty((M, N), device=DEV, dtype=torch.bfloat16)
+    plan.run(a.to(DEV), b.to(DEV), c)
+    assert plan.check() == gemm.OK
+    plan.destroy()
+    ref, _ = oracle.gemm(a, b)
+    assert np.array_equal(c.float().cpu().numpy(), expect_bits(ref, "bf16"))
