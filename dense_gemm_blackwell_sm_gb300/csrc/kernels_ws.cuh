@@ -563,10 +563,11 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
             sk_part = p.sk_ws + theirs * SK_WARP_FLOATS;
           }
         }
-        if constexpr (MX && CW == 64 && EPI < 0) {
-          // single accumulator: first pull this warp's 32 x 256 slice into registers
-          // as packed bf16 and hand the accumulator back, so the next tile's MMAs
-          // start while the stores below drain
+        if constexpr ((MX || (NCONS == 2 && !SK && BN == WS_BN)) && CW == 64 && EPI < 0) {
+          // single accumulator (MX, and each consumer of step 9): first pull this warp's
+          // 32 x 256 slice into registers as packed bf16 and hand the accumulator back,
+          // so the next tile's MMAs start while the stores below drain (step 9,
+          // 8192 x 14336 x 4096: +1 %)
           uint32_t pk[NCH][32];
 #pragma unroll
           for (int ch = 0; ch < NCH; ++ch) {
