@@ -19,6 +19,7 @@ using namespace dgb;
 
 struct gemm_plan_s {
   int64_t M, N, K;
+  int64_t ldc;  // leading dimension of C in elements (N, or wider for a block of a larger C)
   gemm_dtype_t dtype;
   bool in_bf16, out_f32;
   bool in_f8, in_e5m2;  // 8-bit float inputs (E4M3 or E5M2)
@@ -83,10 +84,10 @@ bool encode_fn_ready() {
 // landing in SMEM with the 128-byte swizzle; out-of-range elements read as 0.
 bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, int esize, const void* ptr, uint64_t inner,
                uint64_t outer, uint32_t box_inner, uint32_t box_outer,
-               CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
+               CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B, uint64_t row_elems = 0) {
   if (!encode_fn_ready()) return false;
   cuuint64_t dims[2] = {inner, outer};
-  cuuint64_t strides[1] = {inner * (uint64_t)esize};
+  cuuint64_t strides[1] = {(row_elems ? row_elems : inner) * (uint64_t)esize};
   cuuint32_t box[2] = {box_inner, box_outer};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = g_encode(m, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr,
@@ -211,7 +212,7 @@ gemm_status_t prepare_launch(gemm_plan_s* p) {
     k.stages = p->stages;
     k.timeout_ns = p->timeout_ns;
     k.debug_flags = p->debug_flags;
-    k.out_ld = (int32_t)p->N;
+    k.out_ld = (int32_t)p->ldc;
     k.idesc = is_ws(v) ? make_idesc(p->in_bf16, 128 * p->cg, p->tile_n) : make_idesc(p->in_bf16, 128, 128);
     k.mma_kind = 0;
     k.bk = 64;
@@ -313,6 +314,7 @@ gemm_status_t build_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, co
   if (!p) return GEMM_ERR_OOM;
   p->M = M;
   p->N = N;
+  p->ldc = N;
   p->K = K;
   p->dtype = dtype;
   p->in_bf16 = (dtype == GEMM_BF16_F32 || dtype == GEMM_BF16_BF16);
@@ -506,9 +508,9 @@ const CUtensorMap* operand_map(gemm_plan_s* p, int role, const void* ptr) {
     ok = encode_2d(&victim->map, in_t, ie, ptr, (uint64_t)p->K, (uint64_t)p->N, kbox, rows);
   } else {
     ok = p->out_f32 ? encode_2d(&victim->map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, ptr, (uint64_t)p->N,
-                                (uint64_t)p->M, 32, 32)
+                                (uint64_t)p->M, 32, 32, CU_TENSOR_MAP_SWIZZLE_128B, (uint64_t)p->ldc)
                     : encode_2d(&victim->map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ptr, (uint64_t)p->N,
-                                (uint64_t)p->M, 64, 32);
+                                (uint64_t)p->M, 64, 32, CU_TENSOR_MAP_SWIZZLE_128B, (uint64_t)p->ldc);
   }
   if (!ok) {
     victim->used = 0;
@@ -668,8 +670,8 @@ gemm_status_t check_plan(gemm_plan_s* p) {
 constexpr int kPipePanels = 8;
 struct HostPipe {
   cudaStream_t h2d = nullptr, comp = nullptr, d2h = nullptr;
-  cudaEvent_t start = nullptr, b_in = nullptr;
-  cudaEvent_t a_in[kPipePanels] = {}, c_done[kPipePanels] = {};
+  cudaEvent_t start = nullptr;
+  cudaEvent_t b_in[2] = {}, a_in[kPipePanels] = {}, c_done[kPipePanels][2] = {};
 };
 std::mutex g_pipe_mu;
 std::map<int, HostPipe> g_pipes;
@@ -685,10 +687,12 @@ gemm_status_t host_pipe(int dev, HostPipe** out) {
             cudaStreamCreateWithFlags(&h.comp, cudaStreamNonBlocking) == cudaSuccess &&
             cudaStreamCreateWithFlags(&h.d2h, cudaStreamNonBlocking) == cudaSuccess &&
             cudaEventCreateWithFlags(&h.start, cudaEventDisableTiming) == cudaSuccess &&
-            cudaEventCreateWithFlags(&h.b_in, cudaEventDisableTiming) == cudaSuccess;
+            cudaEventCreateWithFlags(&h.b_in[0], cudaEventDisableTiming) == cudaSuccess &&
+            cudaEventCreateWithFlags(&h.b_in[1], cudaEventDisableTiming) == cudaSuccess;
   for (int i = 0; ok && i < kPipePanels; ++i)
     ok = cudaEventCreateWithFlags(&h.a_in[i], cudaEventDisableTiming) == cudaSuccess &&
-         cudaEventCreateWithFlags(&h.c_done[i], cudaEventDisableTiming) == cudaSuccess;
+         cudaEventCreateWithFlags(&h.c_done[i][0], cudaEventDisableTiming) == cudaSuccess &&
+         cudaEventCreateWithFlags(&h.c_done[i][1], cudaEventDisableTiming) == cudaSuccess;
   if (!ok) {
     cudaGetLastError();
     return GEMM_ERR_CUDA;
@@ -699,7 +703,52 @@ gemm_status_t host_pipe(int dev, HostPipe** out) {
 
 // plans made by gemm_run, keyed by shape, dtype and device
 std::mutex g_cache_mu;
-std::map<std::tuple<int64_t, int64_t, int64_t, int, int>, gemm_plan_s*> g_cache;
+std::map<std::tuple<int64_t, int64_t, int64_t, int64_t, int, int>, gemm_plan_s*> g_cache;
+
+// gemm_run's body, for a C whose rows are `ldc` elements apart (ldc = N, or a
+// block of a wider C for the host pipeline; the GEMV variants need ldc = N)
+gemm_status_t run_cached(int64_t M, int64_t N, int64_t K, int64_t ldc, const void* A, const void* B, void* C,
+                         gemm_dtype_t dtype, cudaStream_t stream) {
+  gemm_status_t st = validate_sizes(M, N, K, dtype);
+  if (st != GEMM_OK) return st;
+  if (is_mx(dtype)) return GEMM_ERR_INVALID_ARG;  // needs scales: gemm_plan_run_mx
+  if (!A || !B || !C) return GEMM_ERR_INVALID_ARG;
+  if (!aligned16(A) || !aligned16(B) || !aligned16(C)) return GEMM_ERR_MISALIGNED;
+  if (ldc < N || (ldc * out_bytes(dtype)) % 16 != 0) return GEMM_ERR_INVALID_ARG;
+  int dev = 0;
+  {
+    int n = 0;
+    if (cudaGetDeviceCount(&n) != cudaSuccess || n < 1) {
+      cudaGetLastError();
+      return GEMM_ERR_NO_DEVICE;
+    }
+    if (cudaGetDevice(&dev) != cudaSuccess) return GEMM_ERR_CUDA;
+  }
+  gemm_plan_s* p = nullptr;
+  try {
+    std::lock_guard<std::mutex> lock(g_cache_mu);
+    auto key = std::make_tuple(M, N, K, ldc, (int)dtype, dev);
+    auto it = g_cache.find(key);
+    if (it != g_cache.end()) {
+      p = it->second;
+    } else {
+      st = build_plan(M, N, K, dtype, nullptr, &p);
+      if (st != GEMM_OK) return st;
+      if (ldc != N) {
+        if (p->variant == GEMM_VARIANT_GEMV || p->variant == GEMM_VARIANT_GEMV_TC) {
+          gemm_plan_destroy(p);
+          return GEMM_ERR_UNSUPPORTED_SHAPE;
+        }
+        p->ldc = ldc;
+        p->kbase.out_ld = (int32_t)ldc;
+      }
+      g_cache[key] = p;
+    }
+  } catch (...) {
+    return GEMM_ERR_OOM;
+  }
+  return launch_plan(p, A, B, C, stream);
+}
 
 }  // namespace
 
@@ -746,42 +795,15 @@ int64_t gemm_mx_scale_bytes(int64_t rows, int64_t K) {
 
 gemm_status_t gemm_run(int64_t M, int64_t N, int64_t K, const void* A, const void* B, void* C,
                        gemm_dtype_t dtype, gemm_stream_t stream) {
-  gemm_status_t st = validate_sizes(M, N, K, dtype);
-  if (st != GEMM_OK) return st;
-  if (is_mx(dtype)) return GEMM_ERR_INVALID_ARG;  // needs scales: gemm_plan_run_mx
-  if (!A || !B || !C) return GEMM_ERR_INVALID_ARG;
-  if (!aligned16(A) || !aligned16(B) || !aligned16(C)) return GEMM_ERR_MISALIGNED;
-  int dev = 0;
-  {
-    int n = 0;
-    if (cudaGetDeviceCount(&n) != cudaSuccess || n < 1) {
-      cudaGetLastError();
-      return GEMM_ERR_NO_DEVICE;
-    }
-    if (cudaGetDevice(&dev) != cudaSuccess) return GEMM_ERR_CUDA;
-  }
-  gemm_plan_s* p = nullptr;
-  try {
-    std::lock_guard<std::mutex> lock(g_cache_mu);
-    auto key = std::make_tuple(M, N, K, (int)dtype, dev);
-    auto it = g_cache.find(key);
-    if (it != g_cache.end()) {
-      p = it->second;
-    } else {
-      st = build_plan(M, N, K, dtype, nullptr, &p);
-      if (st != GEMM_OK) return st;
-      g_cache[key] = p;
-    }
-  } catch (...) {
-    return GEMM_ERR_OOM;
-  }
-  return launch_plan(p, A, B, C, reinterpret_cast<cudaStream_t>(stream));
+  return run_cached(M, N, K, N, A, B, C, dtype, reinterpret_cast<cudaStream_t>(stream));
 }
 
-// Host operands: B goes over first, then A in row panels on the host-to-device
-// stream; each panel's GEMM starts as soon as its rows have landed, and its rows
-// of C return on the device-to-host stream while the next panels are copied and
-// computed (copies in the two directions run concurrently).
+// Host operands, pipelined: the host-to-device stream carries the first half of
+// B's rows (the first half of C's columns), the first row panel of A, the second
+// half of B, then the remaining panels of A; each block of C (a row panel by a
+// column half) is computed as soon as its operands have landed and returns on
+// the device-to-host stream (strided copy) while later panels are copied and
+// computed.  Copies in the two directions run concurrently.
 gemm_status_t gemm_run_host(int64_t M, int64_t N, int64_t K, const void* A_host, const void* B_host,
                             void* C_host, gemm_dtype_t dtype, void* dA, void* dB, void* dC,
                             gemm_stream_t stream) {
@@ -798,7 +820,9 @@ gemm_status_t gemm_run_host(int64_t M, int64_t N, int64_t K, const void* A_host,
   const int64_t ib = in_bytes(dtype), ob = out_bytes(dtype);
   // row panels: kPipePanels for problems whose operands take long enough to copy,
   // 2 for mid sizes, 1 otherwise; panel starts stay 16-byte aligned and on 128-row
-  // bounds
+  // bounds.  With more than one panel and a C at least as large as A and B
+  // together, B (and C's columns) also split in two halves at a multiple of 256
+  // columns.
   int64_t panels = 1;
   const int64_t in_bytes_total = (M * K + N * K) * ib;
   if ((N * ob) % 16 == 0) {
@@ -807,6 +831,13 @@ gemm_status_t gemm_run_host(int64_t M, int64_t N, int64_t K, const void* A_host,
   }
   const int64_t rows = ((M + panels - 1) / panels + 127) / 128 * 128;
   panels = (M + rows - 1) / rows;
+  // (the split only pays when returning C takes at least as long as sending A and
+  // B: 8192 x 14336 x 4096 bf16 482 -> 495 TFLOP/s, while 8192^3 drops 656 -> 635
+  // because its half-width GEMMs then bound the pipeline)
+  const bool split_b = panels > 1 && N >= 1024 && M * N * ob >= in_bytes_total;
+  const int64_t split = split_b ? ((N / 2 + 255) / 256) * 256 : N;
+  const int halves = split < N ? 2 : 1;
+  const int64_t c0[2] = {0, split}, nc[2] = {split, N - split};
 
   std::lock_guard<std::mutex> lock(g_pipe_mu);
   HostPipe* hp = nullptr;
@@ -815,29 +846,37 @@ gemm_status_t gemm_run_host(int64_t M, int64_t N, int64_t K, const void* A_host,
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   bool ok = cudaEventRecord(hp->start, s) == cudaSuccess && cudaStreamWaitEvent(hp->h2d, hp->start, 0) == cudaSuccess &&
             cudaStreamWaitEvent(hp->comp, hp->start, 0) == cudaSuccess &&
-            cudaStreamWaitEvent(hp->d2h, hp->start, 0) == cudaSuccess &&
-            cudaMemcpyAsync(dB, B_host, (size_t)(N * K * ib), cudaMemcpyHostToDevice, hp->h2d) == cudaSuccess &&
-            cudaEventRecord(hp->b_in, hp->h2d) == cudaSuccess && cudaStreamWaitEvent(hp->comp, hp->b_in, 0) == cudaSuccess;
-  for (int64_t i = 0; ok && i < panels; ++i) {
+            cudaStreamWaitEvent(hp->d2h, hp->start, 0) == cudaSuccess;
+  auto copy_b = [&](int j) {
+    return cudaMemcpyAsync(static_cast<char*>(dB) + c0[j] * K * ib, static_cast<const char*>(B_host) + c0[j] * K * ib,
+                           (size_t)(nc[j] * K * ib), cudaMemcpyHostToDevice, hp->h2d) == cudaSuccess &&
+           cudaEventRecord(hp->b_in[j], hp->h2d) == cudaSuccess;
+  };
+  auto copy_a = [&](int64_t i) {
     const int64_t r0 = i * rows, mi = std::min(rows, M - r0);
-    const char* ah = static_cast<const char*>(A_host) + r0 * K * ib;
-    char* ad = static_cast<char*>(dA) + r0 * K * ib;
-    ok = cudaMemcpyAsync(ad, ah, (size_t)(mi * K * ib), cudaMemcpyHostToDevice, hp->h2d) == cudaSuccess &&
-         cudaEventRecord(hp->a_in[i], hp->h2d) == cudaSuccess;
-  }
-  for (int64_t i = 0; ok && i < panels; ++i) {
+    return cudaMemcpyAsync(static_cast<char*>(dA) + r0 * K * ib, static_cast<const char*>(A_host) + r0 * K * ib,
+                           (size_t)(mi * K * ib), cudaMemcpyHostToDevice, hp->h2d) == cudaSuccess &&
+           cudaEventRecord(hp->a_in[i], hp->h2d) == cudaSuccess;
+  };
+  // copy order: B half 0, A panel 0, B half 1, A panels 1..
+  ok = ok && copy_b(0) && copy_a(0) && (halves == 1 || copy_b(1));
+  for (int64_t i = 1; ok && i < panels; ++i) ok = copy_a(i);
+  for (int64_t i = 0; ok && i < panels && st == GEMM_OK; ++i) {
     const int64_t r0 = i * rows, mi = std::min(rows, M - r0);
-    char* ad = static_cast<char*>(dA) + r0 * K * ib;
-    char* cd = static_cast<char*>(dC) + r0 * N * ob;
     ok = cudaStreamWaitEvent(hp->comp, hp->a_in[i], 0) == cudaSuccess;
-    if (ok) {
-      st = gemm_run(mi, N, K, ad, dB, cd, dtype, reinterpret_cast<gemm_stream_t>(hp->comp));
+    for (int j = 0; ok && j < halves; ++j) {
+      char* cd = static_cast<char*>(dC) + (r0 * N + c0[j]) * ob;
+      ok = cudaStreamWaitEvent(hp->comp, hp->b_in[j], 0) == cudaSuccess;
+      if (!ok) break;
+      st = run_cached(mi, nc[j], K, N, static_cast<char*>(dA) + r0 * K * ib, static_cast<char*>(dB) + c0[j] * K * ib,
+                      cd, dtype, hp->comp);
       if (st != GEMM_OK) break;
+      ok = cudaEventRecord(hp->c_done[i][j], hp->comp) == cudaSuccess &&
+           cudaStreamWaitEvent(hp->d2h, hp->c_done[i][j], 0) == cudaSuccess &&
+           cudaMemcpy2DAsync(static_cast<char*>(C_host) + (r0 * N + c0[j]) * ob, (size_t)(N * ob), cd,
+                             (size_t)(N * ob), (size_t)(nc[j] * ob), (size_t)mi, cudaMemcpyDeviceToHost,
+                             hp->d2h) == cudaSuccess;
     }
-    ok = ok && cudaEventRecord(hp->c_done[i], hp->comp) == cudaSuccess &&
-         cudaStreamWaitEvent(hp->d2h, hp->c_done[i], 0) == cudaSuccess &&
-         cudaMemcpyAsync(static_cast<char*>(C_host) + r0 * N * ob, cd, (size_t)(mi * N * ob), cudaMemcpyDeviceToHost,
-                         hp->d2h) == cudaSuccess;
   }
   // drain all three streams whatever happened, then report
   const bool synced = cudaStreamSynchronize(hp->h2d) == cudaSuccess && cudaStreamSynchronize(hp->comp) == cudaSuccess &&

@@ -238,11 +238,12 @@ GEMM_API gemm_status_t gemm_run(int64_t M, int64_t N, int64_t K, const void* A, 
  * caller's device buffers dA and dB, runs the GEMM into dC and copies dC back
  * into C_host, then returns with everything complete and the device status
  * checked.  The work starts after what `stream` holds at the call; internally
- * B is copied first and A, the GEMM and C go in up to 8 row panels on the
- * library's own per-device copy and compute streams, so the copies of later
- * panels and the return of earlier rows of C overlap the GEMMs (host-to-device
- * and device-to-host copies run concurrently).  Calls are serialised per
- * process.  Host buffers should be pinned for full copy speed. */
+ * B is copied first (in two column halves when C is the larger transfer) and
+ * A, the GEMM and C go in up to 8 row panels on the library's own per-device
+ * copy and compute streams, so the copies of later panels and the return of
+ * earlier blocks of C overlap the GEMMs (host-to-device and device-to-host
+ * copies run concurrently).  Calls are serialised per process.  Host buffers
+ * should be pinned for full copy speed. */
 GEMM_API gemm_status_t gemm_run_host(int64_t M, int64_t N, int64_t K, const void* A_host,
                             const void* B_host, void* C_host, gemm_dtype_t dtype, void* dA,
                             void* dB, void* dC, gemm_stream_t stream);

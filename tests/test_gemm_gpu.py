@@ -365,7 +365,9 @@ def test_narrow_tiles_fp8():
     assert np.array_equal(c.float().cpu().numpy(), expect_bits(ref, "bf16"))
 
 
-@pytest.mark.parametrize("shape,dt", [((4096, 4096, 4096), ("bf16", "bf16")), ((2560, 1032, 4104), ("f16", "f32")),
+# (4096, 4096, 4096): 8 row panels; (4096, 4104, 1024) f32: 2 panels and B split in
+# halves of 2304 and 1800 columns (C is the larger transfer); (4100, 2056, 4096): ragged panels
+@pytest.mark.parametrize("shape,dt", [((4096, 4096, 4096), ("bf16", "bf16")), ((4096, 4104, 1024), ("f16", "f32")),
                                       ((4100, 2056, 4096), ("bf16", "f32"))])
 def test_host_entry_point_pipelines_row_panels(shape, dt):
     """gemm_run_host splits large problems into row panels whose copies overlap
