@@ -349,7 +349,21 @@ def cpu_oracle_rate(w: inputs.Workload, budget_s: float = 12.0) -> dict:
         if t_spent < budget_s / 4:
             batch *= 2
     flops = 2.0 * rows_done * w.N * w.K
+    # the same oracle on one thread, over a short fixed sample (a few seconds)
+    t1, rows1 = 0.0, 0
+    while t1 < budget_s / 6 and rows1 < w.M:
+        r1 = [int(rng.integers(0, w.M))]
+        t0 = time.perf_counter()
+        if mx:
+            oracle.gemm_mx(a, b, sfa, sfb, rows=r1, nthreads=1)
+        else:
+            oracle.gemm_rows(a, b, r1, nthreads=1)
+        t1 += time.perf_counter() - t0
+        rows1 += 1
+    import platform
     return {"tflops": flops / t_spent / 1e12, "rows": rows_done, "seconds": t_spent, "threads": threads,
+            "single_thread_tflops": 2.0 * rows1 * w.N * w.K / t1 / 1e12, "single_thread_rows": rows1,
+            "host": "%s, %d logical CPUs" % (platform.machine(), os.cpu_count() or 0),
             "sample": "%d of %d rows of C (all %d columns, K=%d), seeded random rows, fp64 oracle on %d host "
                       "threads; rate extrapolates linearly to the full %dx%dx%d product" % (
                           rows_done, w.M, w.N, w.K, threads, w.M, w.N, w.K)}
@@ -425,6 +439,7 @@ def main(argv=None):
                 "dtype": "f64", "data": "synthetic",
                 "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "in": w.in_dtype, "out": w.out_dtype},
                 "cpu_baseline": {"value": round(r["tflops"], 6), "unit": "TFLOP/s", "cores": r["threads"],
+                                 "single_thread": round(r["single_thread_tflops"], 6), "host": r["host"],
                                  "kind": "oracle", "sample": r["sample"]},
                 "e2e": {"value": round(r["tflops"], 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}}
@@ -539,6 +554,7 @@ def main(argv=None):
     if rank == 0 and not args.no_cpu_baseline:
         r = cpu_oracle_rate(w)
         line["cpu_baseline"] = {"value": round(r["tflops"], 6), "unit": "TFLOP/s", "cores": r["threads"],
+                                "single_thread": round(r["single_thread_tflops"], 6), "host": r["host"],
                                 "kind": "oracle", "sample": r["sample"]}
     if rank == 0:
         print(json.dumps(line))
