@@ -370,7 +370,8 @@ gemm_status_t build_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, co
         return ((double)N / (double)(tn * bn)) * ((double)tiles / (double)(waves * u));
       };
       // (below 70 % with whole 256-column tiles the automatic plan takes stream-K instead)
-      const bool stream_k_instead = !o.sched && fill(256) < 0.7 && ((M + 511) / 512) * ((N + 255) / 256) >= units;
+      const bool stream_k_instead =
+          !o.sched && fill(256) < 0.7 && ((M + 511) / 512) * ((N + 255) / 256) >= units;
       if (!stream_k_instead && fill(224) > fill(256) + 0.05) {
         p->tile_n = 224;
         const int maxs224 = ws_max_stages(p->cg, p->consumers, 224);
@@ -416,13 +417,21 @@ gemm_status_t build_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, co
     if (o.max_ctas && p->sched != GEMM_SCHED_CLC) units = std::max(1, std::min(units, (int)o.max_ctas));
     p->grid_units = units;
     // stream-K by default when whole tiles would leave the clusters idle for over
-    // 30 % of the waves (and every cluster still gets a full tile's work).  Measured
-    // on GB300: 80 tiles on 76 CTA pairs (4096 x 2560 x 8192, step 9) 1115 -> 1507
-    // TFLOP/s; at 84 % (4096^3) the split tiles' partial sums cost more than the
-    // idle clusters (1494 -> 1242), so whole tiles stay the default there.
+    // 30 % of the waves.  Measured on GB300: 80 tiles on 76 CTA pairs (4096 x 2560 x
+    // 8192, step 9) 1115 -> 1507 TFLOP/s; at 84 % (4096^3) the split tiles' partial
+    // sums cost more than the idle clusters (1494 -> 1242), so whole tiles stay the
+    // default there.  Only when every cluster gets at least a tile's work: with
+    // fewer tiles than clusters the shares shrink below half a tile and the
+    // partial sums cost more than the extra SMs bring (1024 x 1024 x 4096 on 152
+    // SMs: 319 TFLOP/s with 32 whole tiles, 191 split over all SMs).  An explicit
+    // GEMM_SCHED_STREAM_K still spreads such shapes over every resident cluster.
     if (!o.sched && !p->in_mx && p->tile_n == 256 && tiles >= active && active > 0) {
       const int waves = (tiles + active - 1) / active;
       if ((double)tiles / ((double)waves * active) < 0.7) p->sched = GEMM_SCHED_STREAM_K;
+    }
+    if (p->sched == GEMM_SCHED_STREAM_K && !o.max_ctas) {
+      const int64_t kb = (K + (p->in_f8 ? 128 : 64) - 1) / (p->in_f8 ? 128 : 64);
+      p->grid_units = (int)std::max<int64_t>(1, std::min<int64_t>(active, (int64_t)tiles * kb / 4));
     }
   } else {
     p->grid_units = tiles;

@@ -48,16 +48,18 @@
 // Stream-K (SK template flag, static schedule, plain writeback): instead of
 // whole tiles, every cluster takes an equal, contiguous share of the flattened
 // (tile, K block) iterations, so the last wave no longer leaves clusters idle
-// (4096^3 with 512x256 tiles: 128 tiles on 76 CTA pairs are 1.68 waves of
-// whole tiles).  Shares are at least one tile long, so a tile is split between
-// at most two consecutive clusters: the later one computes the tile's last K
-// blocks first ("head" part) and writes that fp32 partial to a workspace slot,
-// one flag per writeback warp; the earlier one computes the first K blocks
-// last ("owner" part), waits (bounded) for the flags, adds the partial and
-// stores the tile.  No cluster waits on one that has not started, the owner
-// clears the flags it consumed, and the layout of a slot follows the
-// writeback warps' own (warp, chunk, lane) order so both sides move whole
-// 4 KB runs.
+// (80 tiles on 76 CTA pairs are two waves of whole tiles; a 1024^2 output in
+// 128 x 256 tiles keeps 32 of 152 SMs busy).  A tile is split between
+// consecutive clusters: every cluster but the first whose share covers part of
+// it computes that part as its FIRST segment ("head" part, K blocks from the
+// middle of the tile on) and writes the fp32 partial to its workspace slot,
+// with one flag per writeback warp; the cluster holding the tile's first K
+// blocks does them as its LAST segment ("owner" part), waits (bounded) for the
+// flags of all the following clusters whose shares start inside the tile, adds
+// their partials and stores the tile.  No cluster waits on one that has not
+// started, the owner clears the flags it consumed, and the layout of a slot
+// follows the writeback warps' own (warp, chunk, lane) order so both sides
+// move whole 4 KB runs.
 //
 // In a CTA pair, each CTA loads its own 128 rows of A and its own 128 rows of B
 // (the pair MMA splits A along M and B along N) with the cta_group::2 TMA form,
@@ -519,8 +521,11 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
         const int32_t col_base = tn * BN;
         const uint32_t tbase = tmem + ((q * 32u) << 16) + slot * 256u;
         // stream-K: this warp's 32 x 256 part of a split tile, in a workspace slot of
-        // SK_WARP_FLOATS floats laid out [chunk of 32 columns][lane][32 values]
+        // SK_WARP_FLOATS floats laid out [chunk of 32 columns][lane][32 values]; the
+        // owner adds sk_nparts partials from consecutive slots
         const float* sk_part = nullptr;
+        int32_t sk_nparts = 0;
+        constexpr int64_t SK_SLOT_STRIDE = (int64_t)CG * NCONS * 4;  // flags / warp slots per cluster
         if constexpr (SK) {
           const int64_t own = ((sk_cid * CG + rank) * NCONS + cons) * 4 + q;
           if (kb0 > 0) {
@@ -554,13 +559,19 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
             continue;
           }
           if (kb1 < KB) {
-            // owner part (the first K blocks): wait for the next cluster's head part
-            const int64_t theirs = own + (int64_t)CG * NCONS * 4;
+            // owner part (the first K blocks): wait for the head parts of the following
+            // clusters whose shares start inside this tile (empty shares write nothing)
+            const int64_t tile_end = (int64_t)(tile + 1) * KB;
             uint32_t okf = 1;
-            if (lane == 0) okf = wait_flag_gpu(p.sk_flags + theirs, w, WAIT_SK_PARTIAL) ? 1u : 0u;
+            for (int64_t c2 = sk_cid + 1; c2 < sk_units && sk_total * c2 / sk_units < tile_end; ++c2) {
+              if (sk_total * (c2 + 1) / sk_units == sk_total * c2 / sk_units) continue;
+              ++sk_nparts;
+              if (lane == 0 && okf)
+                okf = wait_flag_gpu(p.sk_flags + own + (c2 - sk_cid) * SK_SLOT_STRIDE, w, WAIT_SK_PARTIAL) ? 1u : 0u;
+            }
             okf = __shfl_sync(0xffffffffu, okf, 0);
             if (!okf) { ok = false; break; }
-            sk_part = p.sk_ws + theirs * SK_WARP_FLOATS;
+            sk_part = p.sk_ws + (own + SK_SLOT_STRIDE) * SK_WARP_FLOATS;
           }
         }
         if constexpr ((MX || (NCONS == 2 && !SK && BN == WS_BN)) && CW == 64 && EPI < 0) {
@@ -632,10 +643,15 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
           if constexpr (CW == 64) tmem_ld_32x32b_x32(tbase + (uint32_t)(ch * CW + 32), v1);
           tmem_wait_ld();
           if constexpr (SK) {
-            if (sk_part != nullptr) {
-              // add the other cluster's part of this tile
-              sk_add32(v0, sk_part + ((ch * CW) / 32 * 32 + (int)lane) * 32);
-              if constexpr (CW == 64) sk_add32(v1, sk_part + ((ch * CW) / 32 * 32 + 32 + (int)lane) * 32);
+            // add the other clusters' parts of this tile (clusters with an empty share
+            // wrote nothing and are skipped, as in the count above)
+            int32_t np = 0;
+            for (int64_t c2 = sk_cid + 1; np < sk_nparts; ++c2) {
+              if (sk_total * (c2 + 1) / sk_units == sk_total * c2 / sk_units) continue;
+              const float* part = sk_part + (c2 - sk_cid - 1) * SK_SLOT_STRIDE * SK_WARP_FLOATS;
+              sk_add32(v0, part + ((ch * CW) / 32 * 32 + (int)lane) * 32);
+              if constexpr (CW == 64) sk_add32(v1, part + ((ch * CW) / 32 * 32 + 32 + (int)lane) * 32);
+              ++np;
             }
           }
           if (ch == NCH - 1) {
@@ -685,13 +701,14 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
       }
       if (!ok) break;
       if constexpr (SK) {
-        // the owner part consumed the next cluster's flags: clear them for the next launch
+        // the owner part consumed the following clusters' flags: clear them for the next launch
         if (kb0 == 0 && kb1 < KB) {
           __syncwarp();
           if (lane == 0) {
+            const int64_t tile_end = (int64_t)(tile + 1) * KB;
+            for (int64_t c2 = sk_cid + 1; c2 < sk_units && sk_total * c2 / sk_units < tile_end; ++c2)
 #pragma unroll 1
-            for (int cons = 0; cons < NCONS; ++cons)
-              p.sk_flags[(((sk_cid + 1) * CG + rank) * NCONS + cons) * 4 + q] = 0u;
+              for (int cons = 0; cons < NCONS; ++cons) p.sk_flags[((c2 * CG + rank) * NCONS + cons) * 4 + q] = 0u;
           }
         }
       }

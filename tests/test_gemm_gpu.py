@@ -388,3 +388,41 @@ def test_host_entry_point_pipelines_row_panels(shape, dt):
     got = ch[rows].double().numpy()
     assert np.array_equal(got, expect_bits(ref, to))
     assert bool(torch.isfinite(ch).all())
+
+
+# stream-K with fewer tiles than clusters: every tile split between several
+# consecutive clusters (the owner adds all their partials)
+SMALL_OUT = [(1024, 1024, 4096, gemm.S7), (512, 4104, 4104, gemm.S7), (1024, 1024, 4096, gemm.S8),
+             (1032, 1024, 2056, gemm.S9)]
+
+
+@pytest.mark.parametrize("M,N,K,variant", SMALL_OUT)
+@pytest.mark.parametrize("ti,to", [("bf16", "bf16"), ("f16", "f32")])
+def test_stream_k_small_outputs_bit_exact(M, N, K, variant, ti, to):
+    a, b = inputs.integer_operands(M, N, K, ti, seed=M + K + variant)
+    plan = gemm.Plan(M, N, K, gemm.dtype_code(ti, to), gemm.make_opts(variant=variant, sched=gemm.SCHED_STREAM_K))
+    info = plan.info()
+    assert info["sched"] == gemm.SCHED_STREAM_K and info["grid"] // info["cluster"] > info["tiles"], info
+    c = torch.full((M, N), float("nan"), device=DEV, dtype=inputs.torch_dtype(to))
+    for _ in range(3):
+        c.fill_(float("nan"))
+        plan.run(a.to(DEV), b.to(DEV), c)
+        assert plan.check() == gemm.OK
+    plan.destroy()
+    ref, _ = oracle.gemm(a, b)
+    bad = np.argwhere(c.float().cpu().numpy() != expect_bits(ref, to))
+    assert bad.size == 0, (info, bad[:3])
+
+
+def test_stream_k_small_output_random_parity():
+    M, N, K = 768, 2048, 8192
+    a, b = inputs.make_operands(M, N, K, "bf16", ("uniform",), ("normal", 1.0), seed=5)
+    plan = gemm.Plan(M, N, K, gemm.BF16_F32, gemm.make_opts(sched=gemm.SCHED_STREAM_K))
+    assert plan.info()["sched"] == gemm.SCHED_STREAM_K
+    c = torch.empty((M, N), device=DEV)
+    plan.run(a.to(DEV), b.to(DEV), c)
+    assert plan.check() == gemm.OK
+    plan.destroy()
+    ref, S = oracle.gemm(a, b)
+    r = parity.check(c.cpu().numpy(), ref, S, "f32")
+    assert r["ok"] and r["max_excess_rel"] < 2.0 ** -12, r
