@@ -96,30 +96,6 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
   return ok != 0;
 }
 
-// non-blocking test of a phase (no suspend); CLUSTER_ACQ for barriers that peer
-// CTAs arrive on
-template <bool CLUSTER_ACQ = false>
-__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  if constexpr (CLUSTER_ACQ)
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-  else
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-  return ok != 0;
-}
-
 // ---------------------------------------------------------------------------
 // bounded waiting: every spin in the kernels goes through this.  A wait gives
 // up when the CTA's abort flag is raised or when `timeout_ns` of wall time has
@@ -337,15 +313,6 @@ __device__ __forceinline__ void clc_try_cancel(uint32_t resp, uint32_t bar) {
   asm volatile(
       "clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.b128"
       " [%0], [%1];" ::"r"(resp),
-      "r"(bar)
-      : "memory");
-}
-
-// same, answer delivered to every CTA of the issuing cluster (same offsets)
-__device__ __forceinline__ void clc_try_cancel_all(uint32_t resp, uint32_t bar) {
-  asm volatile(
-      "clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes"
-      ".multicast::cluster::all.b128 [%0], [%1];" ::"r"(resp),
       "r"(bar)
       : "memory");
 }
