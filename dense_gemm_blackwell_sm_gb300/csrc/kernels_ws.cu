@@ -112,6 +112,21 @@ int ws_max_active_clusters(int cg, int consumers, int sched, bool out_f32, int s
   return n;
 }
 
+cudaError_t spec_ws_ks(bool out_f32, int stages, int tiles, int split, LaunchSpec* out) {
+  void* k = out_f32 ? reinterpret_cast<void*>(k_ws_ks<float>) : reinterpret_cast<void*>(k_ws_ks<__nv_bfloat16>);
+  if (split < 2 || split > 8 || stages < 3) return cudaErrorInvalidValue;  // partials need 128 KB of ring
+  const size_t smem = ws_smem_bytes(1, 1, stages);
+  cudaError_t e = allow_dynamic_smem((const void*)k, smem);
+  if (e != cudaSuccess) return e;
+  out->func = k;
+  out->grid = dim3((unsigned)(tiles * split), 1, 1);
+  out->block = dim3(WS_THREADS, 1, 1);
+  out->smem = smem;
+  out->cluster = (unsigned)split;
+  out->kind = ARGS_ABC_K;
+  return cudaSuccess;
+}
+
 cudaError_t spec_ws(int cg, int consumers, int sched, bool out_f32, int stages, int clusters, LaunchSpec* out,
                     int fused_act, int bn) {
   void* k = ws_kernel(cg, consumers, fused_act >= 0 ? SCHED_STATIC : sched, out_f32, fused_act, bn);

@@ -61,6 +61,16 @@
 // follows the writeback warps' own (warp, chunk, lane) order so both sides
 // move whole 4 KB runs.
 //
+// Split-K within a cluster (KS template flag, step 7's 128x256 tile, plain
+// writeback): for outputs with too few tiles for the GPU, a cluster of 2-8 CTAs
+// shares one tile, CTA r accumulating K blocks [KB r / s, KB (r+1) / s) in its
+// own TMEM.  The other CTAs park their fp32 partials in their own stage ring
+// (idle once their MMAs are done) in the writeback warps' (warp, chunk, lane)
+// order and arrive on the first CTA's barrier; its writeback warps add the
+// partials over distributed shared memory and store the tile.  The cluster
+// synchronises once more before any CTA exits, so no shared memory is read
+// after its owner has gone.
+//
 // In a CTA pair, each CTA loads its own 128 rows of A and its own 128 rows of B
 // (the pair MMA splits A along M and B along N) with the cta_group::2 TMA form,
 // whose completion is counted on the leader CTA's barrier; only the leader
@@ -89,17 +99,32 @@ constexpr uint32_t MX_BLOCK = 512;  // scales of 128 rows x 128 K-elements (4 pe
 constexpr uint32_t MX_TMEM_COL = 256;  // first TMEM column of the per-stage scale slots
 constexpr uint32_t MX_TMEM_SLOT = 16;  // TMEM columns per stage: 4 for A, 8 for B
 
-// v[j] += part[j] for 32 fp32 values held as bit patterns
-__device__ __forceinline__ void sk_add32(uint32_t (&v)[32], const float* part) {
-  const float4* s4 = reinterpret_cast<const float4*>(part);
+// A warp's partial accumulator (32 rows x 256 columns, fp32) is kept as 8 chunks of
+// 32 columns, each [j][lane][4 values]: lane L's values 4j..4j+3 of a chunk sit at
+// float4 index j*32 + L, so each 16-byte access of the warp covers 512 contiguous
+// bytes (coalesced in global memory, free of bank conflicts in shared memory)
+constexpr int SK_CHUNK_FLOATS = 32 * 32;
+
+// v[j] += the lane's 32 values of one partial chunk, for fp32 values held as bit patterns
+__device__ __forceinline__ void sk_add32(uint32_t (&v)[32], const float* chunk, uint32_t lane) {
+  const float4* s4 = reinterpret_cast<const float4*>(chunk) + lane;
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
-    const float4 a = s4[j];
+    const float4 a = s4[j * 32];
     v[4 * j] = __float_as_uint(__uint_as_float(v[4 * j]) + a.x);
     v[4 * j + 1] = __float_as_uint(__uint_as_float(v[4 * j + 1]) + a.y);
     v[4 * j + 2] = __float_as_uint(__uint_as_float(v[4 * j + 2]) + a.z);
     v[4 * j + 3] = __float_as_uint(__uint_as_float(v[4 * j + 3]) + a.w);
   }
+}
+
+// stores the lane's 32 values as one partial chunk in the layout sk_add32 reads
+__device__ __forceinline__ void sk_store32(float* chunk, uint32_t lane, const uint32_t (&v)[32]) {
+  float4* d4 = reinterpret_cast<float4*>(chunk) + lane;
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+    d4[j * 32] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                             __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
 }
 
 // BN: tile columns (MMA N), 256 or 224 (the narrower tile evens out the waves
@@ -122,12 +147,15 @@ struct WsCfg {
 // activation EPI.  MX: 8-bit inputs with UE8M0 block scales read through
 // tmSA / tmSB (one consumer only).  The tensor maps are kernel parameters of
 // the entry points below.
-template <typename OutT, int CG, int NCONS, int SCHED, int EPI, bool MX, bool SK = false, int BN = WS_BN>
+template <typename OutT, int CG, int NCONS, int SCHED, int EPI, bool MX, bool SK = false, int BN = WS_BN,
+          bool KS = false>
 __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMap* tmB, const CUtensorMap* tmC,
                                         const CUtensorMap* tmSA, const CUtensorMap* tmSB, const KParams& p) {
   using Cfg = WsCfg<CG, NCONS, BN>;
   static_assert(!MX || NCONS == 1, "MX block scaling runs with one MMA consumer");
   static_assert(BN == WS_BN || (!MX && !SK && EPI < 0), "narrow tiles: plain writeback, whole tiles");
+  static_assert(!KS || (CG == 1 && NCONS == 1 && !MX && !SK && EPI < 0 && BN == WS_BN),
+                "split-K clusters: step 7 tile, plain writeback");
   static_assert(!SK || (!MX && EPI < 0 && SCHED == SCHED_STATIC), "stream-K: plain writeback, static schedule");
   // MX on the pair: a separate warp copies the scales and takes tile ids from the ring
   constexpr bool MX_COPIER = MX && CG == 2;
@@ -155,6 +183,7 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
   uint64_t* drain_bar = bars + 29;
   uint64_t* sf_ready = bars + 36;              // [8]  scale copies -> MMA (MX)
   uint64_t* cp_drain = bars + 44;              // scale-copy warp's last copies done (MX)
+  uint64_t* red_full = bars + 45;              // split-K partials parked (first CTA of the cluster)
   uint32_t* clc_resp = reinterpret_cast<uint32_t*>(bars + 30);   // 16 B, 16-aligned
   volatile int32_t* ring_tile = reinterpret_cast<volatile int32_t*>(clc_resp + 4);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(clc_resp + 4 + WS_RING);
@@ -164,6 +193,9 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
   const uint32_t warp = warp_idx(), lane = lane_idx();
   const uint32_t rank = (CG == 2) ? cluster_ctarank() : 0u;
   const bool leader = (rank == 0);
+  // split-K: this CTA's place in its cluster and the cluster's size
+  const int32_t ks_n = KS ? (int32_t)cluster_nctarank() : 1;
+  const int32_t ks_r = KS ? (int32_t)cluster_ctarank() : 0;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -172,6 +204,7 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
       if constexpr (MX_COPIER) mbar_init(smem_u32(sf_ready + s), 1);
     }
     if constexpr (MX_COPIER) mbar_init(smem_u32(cp_drain), 1);
+    if constexpr (KS) mbar_init(smem_u32(red_full), 4u * (uint32_t)(ks_n - 1));
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(acc_full + i), 1);
       mbar_init(smem_u32(acc_empty + i), 4 * CG);
@@ -200,7 +233,7 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
     tmem_relinquish<CG>();
   }
   tc_fence_before();
-  if constexpr (CG == 2) {
+  if constexpr (CG == 2 || KS) {
     cluster_sync_all();
   } else {
     __syncthreads();
@@ -243,7 +276,7 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
     return true;
   };
 
-  if (warp == 2 && !SK) {
+  if (warp == 2 && !SK && !KS) {
     // ------------------------------------------------------------- scheduler
     if (lane == 0 && leader) {
       const int32_t total = p.tiles_m * p.tiles_n;
@@ -304,6 +337,11 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
         int32_t tile, kb0 = 0, kb1 = KB;
         if constexpr (SK) {
           if (!sk_next(sk_it, tile, kb0, kb1)) break;
+        } else if constexpr (KS) {
+          if (i > 0) break;  // one tile per cluster, this CTA's share of K
+          tile = (int32_t)(blockIdx.x / (uint32_t)ks_n);
+          kb0 = KB * ks_r / ks_n;
+          kb1 = KB * (ks_r + 1) / ks_n;
         } else {
           if (!ring_get(i, tile)) { ok = false; break; }
           if (tile < 0) break;
@@ -392,6 +430,11 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
         int32_t tile, kb0 = 0, kb1 = KB;
         if constexpr (SK) {
           if (!sk_next(sk_it, tile, kb0, kb1)) break;
+        } else if constexpr (KS) {
+          if (i > 0) break;
+          tile = (int32_t)(blockIdx.x / (uint32_t)ks_n);
+          kb0 = KB * ks_r / ks_n;
+          kb1 = KB * (ks_r + 1) / ks_n;
         } else {
           if (!ring_get(i, tile) || tile < 0) break;
         }
@@ -498,6 +541,9 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
       int32_t tile = -1, kb0 = 0, kb1 = KB;
       if constexpr (SK) {
         if (!sk_next(sk_it, tile, kb0, kb1)) break;
+      } else if constexpr (KS) {
+        if (i > 0) break;
+        tile = (int32_t)(blockIdx.x / (uint32_t)ks_n);
       } else {
         uint32_t okr = 1;
         if (lane == 0) okr = ring_get(i, tile) ? 1u : 0u;
@@ -521,8 +567,8 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
         const int32_t col_base = tn * BN;
         const uint32_t tbase = tmem + ((q * 32u) << 16) + slot * 256u;
         // stream-K: this warp's 32 x 256 part of a split tile, in a workspace slot of
-        // SK_WARP_FLOATS floats laid out [chunk of 32 columns][lane][32 values]; the
-        // owner adds sk_nparts partials from consecutive slots
+        // SK_WARP_FLOATS floats (8 chunks of 32 columns, see sk_add32); the owner adds
+        // sk_nparts partials from consecutive slots
         const float* sk_part = nullptr;
         int32_t sk_nparts = 0;
         constexpr int64_t SK_SLOT_STRIDE = (int64_t)CG * NCONS * 4;  // flags / warp slots per cluster
@@ -547,11 +593,7 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
                   }
                 }
               }
-              float4* d4 = reinterpret_cast<float4*>(dst + (c32 * 32 + (int)lane) * 32);
-#pragma unroll
-              for (int j = 0; j < 8; ++j)
-                d4[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
-                                    __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+              sk_store32(dst + c32 * SK_CHUNK_FLOATS, lane, v);
             }
             __threadfence();
             __syncwarp();
@@ -572,6 +614,30 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
             okf = __shfl_sync(0xffffffffu, okf, 0);
             if (!okf) { ok = false; break; }
             sk_part = p.sk_ws + (own + SK_SLOT_STRIDE) * SK_WARP_FLOATS;
+          }
+        }
+        if constexpr (KS) {
+          // partials of a tile split over the cluster, parked in each CTA's stage ring
+          // as [warp quarter][32-column chunk] in the chunk layout of sk_add32
+          if (ks_r > 0) {
+            float* dst = reinterpret_cast<float*>(ring) + (int64_t)q * SK_WARP_FLOATS;
+#pragma unroll 1
+            for (int c32 = 0; c32 < WS_BN / 32; ++c32) {
+              uint32_t v[32];
+              tmem_ld_32x32b_x32(tbase + (uint32_t)(c32 * 32), v);
+              tmem_wait_ld();
+              sk_store32(dst + c32 * SK_CHUNK_FLOATS, lane, v);
+            }
+            fence_cluster();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(red_full), 0));
+            continue;
+          }
+          if (ks_n > 1) {
+            uint32_t got2 = 1;
+            if (lane == 0) got2 = mbar_wait<true>(smem_u32(red_full), 0, w, WAIT_SK_PARTIAL) ? 1u : 0u;
+            got2 = __shfl_sync(0xffffffffu, got2, 0);
+            if (!got2) { ok = false; break; }
           }
         }
         if constexpr ((MX || (NCONS == 2 && !SK && BN == WS_BN)) && CW == 64 && EPI < 0) {
@@ -642,6 +708,32 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
           tmem_ld_32x32b_x32(tbase + (uint32_t)(ch * CW), v0);
           if constexpr (CW == 64) tmem_ld_32x32b_x32(tbase + (uint32_t)(ch * CW + 32), v1);
           tmem_wait_ld();
+          if constexpr (KS) {
+            // add the other CTAs' partials, read from their shared memory
+            const uint32_t off =
+                (uint32_t)(((int)q * (WS_BN / 32) + (ch * CW) / 32) * SK_CHUNK_FLOATS + (int)lane * 4) * 4u;
+            for (int32_t pr = 1; pr < ks_n; ++pr) {
+              const uint32_t base = mapa_shared(smem_u32(ring), (uint32_t)pr) + off;
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                const float4 a4 = ld_cluster_f32x4(base + 512u * j);
+                v0[4 * j] = __float_as_uint(__uint_as_float(v0[4 * j]) + a4.x);
+                v0[4 * j + 1] = __float_as_uint(__uint_as_float(v0[4 * j + 1]) + a4.y);
+                v0[4 * j + 2] = __float_as_uint(__uint_as_float(v0[4 * j + 2]) + a4.z);
+                v0[4 * j + 3] = __float_as_uint(__uint_as_float(v0[4 * j + 3]) + a4.w);
+              }
+              if constexpr (CW == 64) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                  const float4 a4 = ld_cluster_f32x4(base + SK_CHUNK_FLOATS * 4u + 512u * j);
+                  v1[4 * j] = __float_as_uint(__uint_as_float(v1[4 * j]) + a4.x);
+                  v1[4 * j + 1] = __float_as_uint(__uint_as_float(v1[4 * j + 1]) + a4.y);
+                  v1[4 * j + 2] = __float_as_uint(__uint_as_float(v1[4 * j + 2]) + a4.z);
+                  v1[4 * j + 3] = __float_as_uint(__uint_as_float(v1[4 * j + 3]) + a4.w);
+                }
+              }
+            }
+          }
           if constexpr (SK) {
             // add the other clusters' parts of this tile (clusters with an empty share
             // wrote nothing and are skipped, as in the count above)
@@ -649,8 +741,8 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
             for (int64_t c2 = sk_cid + 1; np < sk_nparts; ++c2) {
               if (sk_total * (c2 + 1) / sk_units == sk_total * c2 / sk_units) continue;
               const float* part = sk_part + (c2 - sk_cid - 1) * SK_SLOT_STRIDE * SK_WARP_FLOATS;
-              sk_add32(v0, part + ((ch * CW) / 32 * 32 + (int)lane) * 32);
-              if constexpr (CW == 64) sk_add32(v1, part + ((ch * CW) / 32 * 32 + 32 + (int)lane) * 32);
+              sk_add32(v0, part + (ch * CW) / 32 * SK_CHUNK_FLOATS, lane);
+              if constexpr (CW == 64) sk_add32(v1, part + ((ch * CW) / 32 + 1) * SK_CHUNK_FLOATS, lane);
               ++np;
             }
           }
@@ -712,7 +804,8 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
           }
         }
       }
-      if (p.visits != nullptr && q == 0 && lane == 0 && leader && (!SK || kb0 == 0)) atomicAdd(p.visits + tile, 1);
+      if (p.visits != nullptr && q == 0 && lane == 0 && leader && (!SK || kb0 == 0) && (!KS || ks_r == 0))
+        atomicAdd(p.visits + tile, 1);
     }
     if (lane == 0) bulk_wait_group<0>();
   }
@@ -721,7 +814,7 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
   __syncwarp();
   tc_fence_before();
   __syncthreads();
-  if constexpr (CG == 2) cluster_sync_all();
+  if constexpr (CG == 2 || KS) cluster_sync_all();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc<CG>(tmem, 512);
@@ -743,6 +836,14 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
             const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmSA,
             const __grid_constant__ CUtensorMap tmSB, KParams p) {
   ws_body<OutT, CG, 1, SCHED, EPI, true>(&tmA, &tmB, &tmC, &tmSA, &tmSB, p);
+}
+
+// entry point of the split-K cluster kernels (step 7 tile, plain writeback)
+template <typename OutT>
+__global__ void __launch_bounds__(WS_THREADS, 1)
+    k_ws_ks(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+            const __grid_constant__ CUtensorMap tmC, KParams p) {
+  ws_body<OutT, 1, 1, SCHED_STATIC, -1, false, false, WS_BN, true>(&tmA, &tmB, &tmC, nullptr, nullptr, p);
 }
 
 // entry point of the stream-K kernels (static schedule, plain writeback)

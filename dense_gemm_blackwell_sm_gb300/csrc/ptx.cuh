@@ -295,6 +295,16 @@ __device__ __forceinline__ uint32_t ld_cluster_u32(uint32_t cluster_addr) {
   return v;
 }
 
+__device__ __forceinline__ uint32_t cluster_nctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return r;
+}
+
+// order this thread's earlier shared-memory writes before its later arrivals
+// that other CTAs of the cluster observe
+__device__ __forceinline__ void fence_cluster() { asm volatile("fence.acq_rel.cluster;" ::: "memory"); }
+
 __device__ __forceinline__ float4 ld_cluster_f32x4(uint32_t cluster_addr) {
   float4 v;
   asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"

@@ -119,7 +119,12 @@ typedef struct {
   int32_t raster_group; /* tile rows per L2 raster group, 0 = automatic */
   int32_t max_ctas;     /* cap on persistent CTAs / clusters, 0 = no cap */
   int32_t split_k;      /* GEMV_TC: CTAs (a cluster) sharing one 128-row block's K range,
-                           1, 2, 4 or 8; 0 = automatic */
+                           1, 2, 4 or 8; variant 7: CTAs (a cluster, 2-8) sharing one
+                           128 x 256 tile's K range, their fp32 partials added over
+                           distributed shared memory, 1 = never; 0 = automatic (variant 7
+                           splits when its tiles would fill at most half the SMs,
+                           into as many CTAs per tile as fit, each keeping at
+                           least 32 K blocks) */
   int64_t timeout_ns;   /* bound on every device-side wait, 0 = 2 s */
   int32_t debug_flags;  /* test hooks: 1 = leave out one TMA load (forces a timeout) */
   int32_t flags;        /* GEMM_FLAG_* */

@@ -426,3 +426,52 @@ def test_stream_k_small_output_random_parity():
     ref, S = oracle.gemm(a, b)
     r = parity.check(c.cpu().numpy(), ref, S, "f32")
     assert r["ok"] and r["max_excess_rel"] < 2.0 ** -12, r
+
+
+# step 7 with K split over a cluster (partials added over distributed shared memory)
+KS_CASES = [(1024, 1024, 4096, 0), (512, 1024, 8192, 0), (300, 520, 1040, 2), (129, 1288, 2056, 3),
+            (640, 264, 4104, 5), (256, 512, 8192, 8)]
+# automatic split: as many CTAs per tile as the SMs hold, each keeping >= 32 K blocks
+KS_AUTO = {(1024, 1024, 4096): 2, (512, 1024, 8192): 4}
+
+
+@pytest.mark.parametrize("M,N,K,split", KS_CASES)
+@pytest.mark.parametrize("ti,to", [("bf16", "bf16"), ("f16", "f32")])
+def test_split_k_cluster_bit_exact(M, N, K, split, ti, to):
+    a, b = inputs.integer_operands(M, N, K, ti, seed=M + split)
+    plan = gemm.Plan(M, N, K, gemm.dtype_code(ti, to), gemm.make_opts(variant=gemm.S7 if split else 0, split_k=split))
+    info = plan.info()
+    assert info["variant"] == gemm.S7 and info["cluster"] == (split or KS_AUTO[(M, N, K)]), info
+    assert info["grid"] == info["tiles"] * info["cluster"], info
+    visits = torch.zeros(info["tiles"], dtype=torch.int32, device=DEV)
+    plan.set_visits(visits)
+    c = torch.full((M, N), float("nan"), device=DEV, dtype=inputs.torch_dtype(to))
+    for _ in range(2):
+        visits.zero_()
+        c.fill_(float("nan"))
+        plan.run(a.to(DEV), b.to(DEV), c)
+        assert plan.check() == gemm.OK
+        assert int(visits.min()) == 1 and int(visits.max()) == 1
+    plan.destroy()
+    ref, _ = oracle.gemm(a, b)
+    bad = np.argwhere(c.float().cpu().numpy() != expect_bits(ref, to))
+    assert bad.size == 0, (info, bad[:3])
+
+
+def test_split_k_cluster_random_parity_and_refusals():
+    M, N, K = 512, 4096, 4096
+    a, b = inputs.make_operands(M, N, K, "bf16", ("uniform",), ("normal", 1.0), seed=9)
+    plan = gemm.Plan(M, N, K, gemm.BF16_F32)
+    assert plan.info()["cluster"] == 2 and plan.info()["variant"] == gemm.S7
+    c = torch.empty((M, N), device=DEV)
+    plan.run(a.to(DEV), b.to(DEV), c)
+    assert plan.check() == gemm.OK
+    plan.destroy()
+    ref, S = oracle.gemm(a, b)
+    r = parity.check(c.cpu().numpy(), ref, S, "f32")
+    assert r["ok"] and r["max_excess_rel"] < 2.0 ** -12, r
+    with pytest.raises(gemm.GemmError):
+        gemm.Plan(M, N, K, gemm.BF16_F32, gemm.make_opts(variant=gemm.S9, split_k=2))
+    p1 = gemm.Plan(M, N, K, gemm.BF16_F32, gemm.make_opts(split_k=1))
+    assert p1.info()["cluster"] == 1
+    p1.destroy()
