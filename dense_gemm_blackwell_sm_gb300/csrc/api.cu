@@ -439,14 +439,16 @@ gemm_status_t build_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, co
     }
     // Step 7 with few tiles for the GPU: split each tile's K over a cluster of CTAs
     // (opts.split_k = 2-8 asks for it, 1 forbids it).  Automatic: as many CTAs per
-    // tile as the SMs hold at once, while each keeps at least 32 K blocks; with
-    // shorter shares the partial sums cost more than the extra SMs bring
-    // (1024 x 1024 x 4096: 320 TFLOP/s whole, 416 split 2, 368 split 4)
+    // tile as the SMs hold at once, at most 4, while each keeps at least 16 K
+    // blocks; with shorter shares the partial sums cost more than the extra SMs
+    // bring (1024 x 1024 x 4096: 320 TFLOP/s whole, 416 split 2, 491 split 4).
+    // Clusters of 8 such CTAs do not all fit at once (512 x 1024 x 8192 on 16
+    // tiles: 416 split 4, 250 split 8).
     if (variant == GEMM_VARIANT_S7_WARP_SPECIALIZED && !p->in_mx && o.layout == 0 &&
         (o.sched == 0 || o.sched == GEMM_SCHED_STATIC) && p->sched != GEMM_SCHED_STREAM_K && o.split_k != 1) {
       const int64_t kb = (K + (p->in_f8 ? 128 : 64) - 1) / (p->in_f8 ? 128 : 64);
       int64_t split = o.split_k;
-      if (!split && tiles > 0) split = std::min<int64_t>(8, std::min<int64_t>(sms / tiles, kb / 32));
+      if (!split && tiles > 0) split = std::min<int64_t>(4, std::min<int64_t>(sms / tiles, kb / 16));
       if (split >= 2 && split <= kb) {
         p->ks_split = (int)split;
         p->sched = GEMM_SCHED_STATIC;

@@ -64,12 +64,12 @@
 // Split-K within a cluster (KS template flag, step 7's 128x256 tile, plain
 // writeback): for outputs with too few tiles for the GPU, a cluster of 2-8 CTAs
 // shares one tile, CTA r accumulating K blocks [KB r / s, KB (r+1) / s) in its
-// own TMEM.  The other CTAs park their fp32 partials in their own stage ring
-// (idle once their MMAs are done) in the writeback warps' (warp, chunk, lane)
-// order and arrive on the first CTA's barrier; its writeback warps add the
-// partials over distributed shared memory and store the tile.  The cluster
-// synchronises once more before any CTA exits, so no shared memory is read
-// after its owner has gone.
+// own TMEM.  Every CTA parks its fp32 partial in its own stage ring (idle once
+// its MMAs are done) in the writeback warps' (warp, chunk, lane) order and
+// arrives on the barrier of every CTA of the cluster; then each CTA adds all the
+// partials of its share of the tile's columns over distributed shared memory
+// and stores that share.  The cluster synchronises once more before any CTA
+// exits, so no shared memory is read after its owner has gone.
 //
 // In a CTA pair, each CTA loads its own 128 rows of A and its own 128 rows of B
 // (the pair MMA splits A along M and B along N) with the cta_group::2 TMA form,
@@ -183,7 +183,7 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
   uint64_t* drain_bar = bars + 29;
   uint64_t* sf_ready = bars + 36;              // [8]  scale copies -> MMA (MX)
   uint64_t* cp_drain = bars + 44;              // scale-copy warp's last copies done (MX)
-  uint64_t* red_full = bars + 45;              // split-K partials parked (first CTA of the cluster)
+  uint64_t* red_full = bars + 45;              // split-K partials parked (every CTA of the cluster)
   uint32_t* clc_resp = reinterpret_cast<uint32_t*>(bars + 30);   // 16 B, 16-aligned
   volatile int32_t* ring_tile = reinterpret_cast<volatile int32_t*>(clc_resp + 4);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(clc_resp + 4 + WS_RING);
@@ -204,7 +204,7 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
       if constexpr (MX_COPIER) mbar_init(smem_u32(sf_ready + s), 1);
     }
     if constexpr (MX_COPIER) mbar_init(smem_u32(cp_drain), 1);
-    if constexpr (KS) mbar_init(smem_u32(red_full), 4u * (uint32_t)(ks_n - 1));
+    if constexpr (KS) mbar_init(smem_u32(red_full), 4u * (uint32_t)ks_n);
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(acc_full + i), 1);
       mbar_init(smem_u32(acc_empty + i), 4 * CG);
@@ -617,28 +617,48 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
           }
         }
         if constexpr (KS) {
-          // partials of a tile split over the cluster, parked in each CTA's stage ring
-          // as [warp quarter][32-column chunk] in the chunk layout of sk_add32
-          if (ks_r > 0) {
-            float* dst = reinterpret_cast<float*>(ring) + (int64_t)q * SK_WARP_FLOATS;
+          // a tile split over the cluster: every CTA parks its fp32 partial in its own
+          // stage ring (idle now), as [warp quarter][32-column chunk] in the chunk
+          // layout of sk_add32, and arrives on every CTA's barrier; then CTA r adds the
+          // ks_n partials of its share of the 32-column chunks, read over distributed
+          // shared memory, and stores them, so the reads and stores are spread over
+          // the cluster instead of converging on one CTA
+          float* dst = reinterpret_cast<float*>(ring) + (int64_t)q * SK_WARP_FLOATS;
 #pragma unroll 1
-            for (int c32 = 0; c32 < WS_BN / 32; ++c32) {
-              uint32_t v[32];
-              tmem_ld_32x32b_x32(tbase + (uint32_t)(c32 * 32), v);
-              tmem_wait_ld();
-              sk_store32(dst + c32 * SK_CHUNK_FLOATS, lane, v);
+          for (int c32 = 0; c32 < WS_BN / 32; ++c32) {
+            uint32_t v[32];
+            tmem_ld_32x32b_x32(tbase + (uint32_t)(c32 * 32), v);
+            tmem_wait_ld();
+            sk_store32(dst + c32 * SK_CHUNK_FLOATS, lane, v);
+          }
+          fence_cluster();
+          __syncwarp();
+          if (lane < (uint32_t)ks_n) mbar_arrive_cluster(mapa_shared(smem_u32(red_full), lane));
+          uint32_t got2 = 1;
+          if (lane == 0) got2 = mbar_wait<true>(smem_u32(red_full), 0, w, WAIT_SK_PARTIAL) ? 1u : 0u;
+          got2 = __shfl_sync(0xffffffffu, got2, 0);
+          if (!got2) { ok = false; break; }
+          const int32_t row = row0 + (int32_t)lane;
+#pragma unroll 1
+          for (int c32 = (WS_BN / 32) * ks_r / ks_n; c32 < (WS_BN / 32) * (ks_r + 1) / ks_n; ++c32) {
+            const uint32_t off = (uint32_t)(((int)q * (WS_BN / 32) + c32) * SK_CHUNK_FLOATS + (int)lane * 4) * 4u;
+            uint32_t v[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = 0u;  // +0.0f
+            for (int32_t pr = 0; pr < ks_n; ++pr) {
+              const uint32_t base = mapa_shared(smem_u32(ring), (uint32_t)pr) + off;
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                const float4 a4 = ld_cluster_f32x4(base + 512u * j);
+                v[4 * j] = __float_as_uint(__uint_as_float(v[4 * j]) + a4.x);
+                v[4 * j + 1] = __float_as_uint(__uint_as_float(v[4 * j + 1]) + a4.y);
+                v[4 * j + 2] = __float_as_uint(__uint_as_float(v[4 * j + 2]) + a4.z);
+                v[4 * j + 3] = __float_as_uint(__uint_as_float(v[4 * j + 3]) + a4.w);
+              }
             }
-            fence_cluster();
-            __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(red_full), 0));
-            continue;
+            if (row < p.M) store_row32<OutT>(reinterpret_cast<OutT*>(p.C), p.out_ld, row, col_base + 32 * c32, p.N, v);
           }
-          if (ks_n > 1) {
-            uint32_t got2 = 1;
-            if (lane == 0) got2 = mbar_wait<true>(smem_u32(red_full), 0, w, WAIT_SK_PARTIAL) ? 1u : 0u;
-            got2 = __shfl_sync(0xffffffffu, got2, 0);
-            if (!got2) { ok = false; break; }
-          }
+          continue;
         }
         if constexpr ((MX || (NCONS == 2 && !SK && BN == WS_BN)) && CW == 64 && EPI < 0) {
           // single accumulator (MX, and each consumer of step 9): first pull this warp's
@@ -708,32 +728,6 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
           tmem_ld_32x32b_x32(tbase + (uint32_t)(ch * CW), v0);
           if constexpr (CW == 64) tmem_ld_32x32b_x32(tbase + (uint32_t)(ch * CW + 32), v1);
           tmem_wait_ld();
-          if constexpr (KS) {
-            // add the other CTAs' partials, read from their shared memory
-            const uint32_t off =
-                (uint32_t)(((int)q * (WS_BN / 32) + (ch * CW) / 32) * SK_CHUNK_FLOATS + (int)lane * 4) * 4u;
-            for (int32_t pr = 1; pr < ks_n; ++pr) {
-              const uint32_t base = mapa_shared(smem_u32(ring), (uint32_t)pr) + off;
-#pragma unroll
-              for (int j = 0; j < 8; ++j) {
-                const float4 a4 = ld_cluster_f32x4(base + 512u * j);
-                v0[4 * j] = __float_as_uint(__uint_as_float(v0[4 * j]) + a4.x);
-                v0[4 * j + 1] = __float_as_uint(__uint_as_float(v0[4 * j + 1]) + a4.y);
-                v0[4 * j + 2] = __float_as_uint(__uint_as_float(v0[4 * j + 2]) + a4.z);
-                v0[4 * j + 3] = __float_as_uint(__uint_as_float(v0[4 * j + 3]) + a4.w);
-              }
-              if constexpr (CW == 64) {
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                  const float4 a4 = ld_cluster_f32x4(base + SK_CHUNK_FLOATS * 4u + 512u * j);
-                  v1[4 * j] = __float_as_uint(__uint_as_float(v1[4 * j]) + a4.x);
-                  v1[4 * j + 1] = __float_as_uint(__uint_as_float(v1[4 * j + 1]) + a4.y);
-                  v1[4 * j + 2] = __float_as_uint(__uint_as_float(v1[4 * j + 2]) + a4.z);
-                  v1[4 * j + 3] = __float_as_uint(__uint_as_float(v1[4 * j + 3]) + a4.w);
-                }
-              }
-            }
-          }
           if constexpr (SK) {
             // add the other clusters' parts of this tile (clusters with an empty share
             // wrote nothing and are skipped, as in the count above)

@@ -123,8 +123,8 @@ typedef struct {
                            128 x 256 tile's K range, their fp32 partials added over
                            distributed shared memory, 1 = never; 0 = automatic (variant 7
                            splits when its tiles would fill at most half the SMs,
-                           into as many CTAs per tile as fit, each keeping at
-                           least 32 K blocks) */
+                           into as many CTAs per tile as fit, at most 4, each
+                           keeping at least 16 K blocks) */
   int64_t timeout_ns;   /* bound on every device-side wait, 0 = 2 s */
   int32_t debug_flags;  /* test hooks: 1 = leave out one TMA load (forces a timeout) */
   int32_t flags;        /* GEMM_FLAG_* */

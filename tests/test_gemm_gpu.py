@@ -429,10 +429,11 @@ def test_stream_k_small_output_random_parity():
 
 
 # step 7 with K split over a cluster (partials added over distributed shared memory)
-KS_CASES = [(1024, 1024, 4096, 0), (512, 1024, 8192, 0), (300, 520, 1040, 2), (129, 1288, 2056, 3),
-            (640, 264, 4104, 5), (256, 512, 8192, 8)]
-# automatic split: as many CTAs per tile as the SMs hold, each keeping >= 32 K blocks
-KS_AUTO = {(1024, 1024, 4096): 2, (512, 1024, 8192): 4}
+KS_CASES = [(1024, 1024, 4096, 0), (512, 1024, 8192, 0), (256, 512, 2048, 0), (300, 520, 1040, 2),
+            (129, 1288, 2056, 3), (640, 264, 4104, 5), (256, 512, 8192, 8)]
+# automatic split: as many CTAs per tile as the SMs hold (152 SMs), at most 4, each keeping
+# >= 16 K blocks
+KS_AUTO = {(1024, 1024, 4096): 4, (512, 1024, 8192): 4, (256, 512, 2048): 2}
 
 
 @pytest.mark.parametrize("M,N,K,split", KS_CASES)

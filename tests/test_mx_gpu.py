@@ -75,6 +75,27 @@ def test_random_parity(variant, shape, fmt):
 
 
 @pytest.mark.parametrize("variant", [gemm.S7, gemm.S8])
+@pytest.mark.parametrize("max_ctas", [1, 3])
+def test_few_clusters_many_tiles(variant, max_ctas):
+    # few clusters, many tiles each, 21 K blocks a tile: the stage ring and the
+    # per-stage TMEM scale slots wrap many times, across tile boundaries
+    M, N, K = 1024, 1024, 2688
+    a, b = inputs.integer_operands(M, N, K, "e4m3", seed=11, lo=-6, hi=6)
+    sa = inputs.mx_scales(M, K, seed=3, e_lo=125, e_hi=129)
+    sb = inputs.mx_scales(N, K, seed=4, e_lo=125, e_hi=129)
+    plan = gemm.Plan(M, N, K, gemm.dtype_code("mxe4m3", "f32"), gemm.make_opts(variant=variant, max_ctas=max_ctas))
+    assert plan.info()["grid"] == max_ctas * plan.info()["cluster"]
+    ta, tb = inputs.mx_tile_scales(sa, K).to(DEV), inputs.mx_tile_scales(sb, K).to(DEV)
+    c = torch.full((M, N), float("nan"), device=DEV)
+    plan.run_mx(a.to(DEV), b.to(DEV), c, ta, tb)
+    assert plan.check() == gemm.OK
+    plan.destroy()
+    C, _ = oracle.gemm_mx(a, b, sa, sb)
+    bad = np.argwhere(c.double().cpu().numpy() != C)
+    assert bad.size == 0, bad[:3]
+
+
+@pytest.mark.parametrize("variant", [gemm.S7, gemm.S8])
 def test_scales_only_touch_their_own_block(variant):
     # one scale byte of A and one of B changed: only that row and that column move
     M, N, K = 512, 512, 256
