@@ -164,3 +164,46 @@ def test_rejections():
                          torch.cuda.current_stream().cuda_stream) == gemm.OK
     torch.cuda.synchronize()
     assert bool((c == 0).all())
+
+
+# stream-K with 8-bit operands: tiles outnumber the resident clusters and are split
+# between clusters (K blocks of 128 elements here)
+SK_SHAPES = {gemm.S7: (1280, 4352, 528), gemm.S8: (1280, 4352, 272), gemm.S9: (2560, 4352, 144)}
+
+
+@pytest.mark.parametrize("variant", [gemm.S7, gemm.S8, gemm.S9])
+@pytest.mark.parametrize("out", ["f32", "bf16"])
+def test_stream_k_integer_bit_exact(variant, out):
+    M, N, K = SK_SHAPES[variant]
+    a, b = inputs.integer_operands(M, N, K, "e4m3", seed=50 + variant, lo=-8, hi=8)
+    plan = gemm.Plan(M, N, K, gemm.dtype_code("e4m3", out), gemm.make_opts(variant=variant, sched=gemm.SCHED_STREAM_K))
+    info = plan.info()
+    assert info["sched"] == gemm.SCHED_STREAM_K and info["tiles"] > info["grid"] // info["cluster"]
+    c = torch.full((M, N), float("nan"), device=DEV, dtype=inputs.torch_dtype(out))
+    for _ in range(2):
+        c.fill_(float("nan"))
+        plan.run(a.to(DEV), b.to(DEV), c)
+        assert plan.check() == gemm.OK
+    plan.destroy()
+    C, _ = oracle.gemm(a, b)
+    exp = torch.tensor(C).to(inputs.torch_dtype(out)).double().numpy()
+    bad = np.argwhere(c.double().cpu().numpy() != exp)
+    assert bad.size == 0, (info, bad[:3])
+
+
+@pytest.mark.parametrize("M,N,K,split", [(1024, 1024, 4096, 0), (300, 520, 1296, 3)])
+@pytest.mark.parametrize("out", ["f32", "bf16"])
+def test_split_k_cluster_integer_bit_exact(M, N, K, split, out):
+    a, b = inputs.integer_operands(M, N, K, "e5m2", seed=60 + split, lo=-4, hi=4)
+    opts = gemm.make_opts(variant=gemm.S7 if split else 0, split_k=split)
+    plan = gemm.Plan(M, N, K, gemm.dtype_code("e5m2", out), opts)
+    info = plan.info()
+    assert info["variant"] == gemm.S7 and info["cluster"] == (split or 2), info
+    c = torch.full((M, N), float("nan"), device=DEV, dtype=inputs.torch_dtype(out))
+    plan.run(a.to(DEV), b.to(DEV), c)
+    assert plan.check() == gemm.OK
+    plan.destroy()
+    C, _ = oracle.gemm(a, b)
+    exp = torch.tensor(C).to(inputs.torch_dtype(out)).double().numpy()
+    bad = np.argwhere(c.double().cpu().numpy() != exp)
+    assert bad.size == 0, (info, bad[:3])

@@ -476,3 +476,38 @@ def test_split_k_cluster_random_parity_and_refusals():
     p1 = gemm.Plan(M, N, K, gemm.BF16_F32, gemm.make_opts(split_k=1))
     assert p1.info()["cluster"] == 1
     p1.destroy()
+
+
+# extreme aspect ratios: a 65536-deep K loop, 512 tile columns of one tile row, 256 tile rows
+# of one (ragged) tile column; integer operands make every result exact
+EXTREME = [(256, 256, 65536), (128, 131072, 64), (131072, 136, 64)]
+
+
+@pytest.mark.parametrize("M,N,K", EXTREME)
+def test_extreme_shapes_bit_exact(M, N, K):
+    a, b = inputs.integer_operands(M, N, K, "bf16", seed=K + 1)
+    info = []
+    c = run_variant(a, b, "bf16", 0, plan_out=info)
+    ref, _ = oracle.gemm(a, b)
+    bad = np.argwhere(c != expect_bits(ref, "bf16"))
+    assert bad.size == 0, (info, bad[:3])
+
+
+def test_output_of_more_than_2_31_elements():
+    # C is 65536 x 65536 bf16 (8 GiB): row offsets past 2^31 elements need 64-bit
+    # addressing in every store path; sampled rows against the oracle, all of C finite
+    M = N = 65536
+    K = 64
+    a, b = inputs.integer_operands(M, N, K, "bf16", seed=3)
+    plan = gemm.Plan(M, N, K, gemm.BF16_BF16)
+    c = torch.full((M, N), float("nan"), device=DEV, dtype=torch.bfloat16)
+    plan.run(a.to(DEV), b.to(DEV), c)
+    assert plan.check() == gemm.OK
+    plan.destroy()
+    assert bool(torch.isfinite(c).all())
+    rows = [0, 1, 32767, 32768, 40000, 65534, 65535]
+    ref, _ = oracle.gemm_rows(a, b, rows)
+    got = c[rows].float().cpu().numpy().astype(np.float64)
+    assert np.array_equal(got, expect_bits(ref, "bf16"))
+    del c
+    torch.cuda.empty_cache()
