@@ -44,8 +44,7 @@ struct gemm_plan_s {
   dgb::LaunchSpec spec;   // kernel, launch shape and SMEM, fixed at plan time
   dgb::LaunchSpec spec_epi[5];  // the fused-epilogue kernel per activation, made on first use
   bool epi_ready[5];
-  int epi_tiles_m, epi_tiles_n, epi_stages;  // its tiling: one MMA consumer, so the TMEM double buffer lets the
-                                // epilogue of one tile overlap the MMAs of the next
+  int epi_tiles_m[5], epi_tiles_n[5], epi_stages[5];  // its tiling, per activation
   dgb::KParams kbase;     // kernel parameters that do not depend on the pointers
   dgb::TgParams tgbase;   // same, for the tensor-core GEMV
   // TMA descriptors by operand role (0 = A, 1 = B, 2 = C) and pointer, least
@@ -538,7 +537,7 @@ const CUtensorMap* operand_map(gemm_plan_s* p, int role, const void* ptr) {
   } else if (role == 0) {
     ok = encode_2d(&victim->map, in_t, ie, ptr, (uint64_t)p->K, (uint64_t)p->M, kbox, 128);
   } else if (role == 1 || role == 6) {
-    // role 6: B for the fused-epilogue kernels (one consumer, 256-column tiles)
+    // role 6: B for the fused-epilogue kernels (256-column tiles)
     const uint32_t rows = !is_ws(p->variant) ? 128u
                           : role == 6        ? (uint32_t)ws_shape(p->cg, 1).b_box_rows
                                              : (uint32_t)ws_shape(p->cg, p->consumers, p->tile_n).b_box_rows;
@@ -597,9 +596,9 @@ gemm_status_t launch_plan(gemm_plan_s* p, const void* A, const void* B, void* C,
         k.act = epi->activation;
         k.scale_a = epi->scale_a;
         k.scale_b = epi->scale_b;
-        k.tiles_m = p->epi_tiles_m;
-        k.tiles_n = p->epi_tiles_n;
-        k.stages = p->epi_stages;
+        k.tiles_m = p->epi_tiles_m[epi->activation];
+        k.tiles_n = p->epi_tiles_n[epi->activation];
+        k.stages = p->epi_stages[epi->activation];
         // the fused kernels' MMAs are 256 columns wide whatever the plan's own tile
         k.idesc = (k.idesc & ~(0x3Fu << 17)) | ((256u >> 3) << 17);
         spec = &p->spec_epi[epi->activation];
@@ -656,24 +655,29 @@ gemm_status_t run_with_epilogue(gemm_plan_s* plan, const void* A, const void* B,
     cudaError_t e;
     if (plan->in_mx) {
       // the block-scaled plan already runs one consumer on one CTA
-      plan->epi_stages = plan->stages;
-      plan->epi_tiles_m = plan->tiles_m;
-      plan->epi_tiles_n = plan->tiles_n;
+      plan->epi_stages[act] = plan->stages;
+      plan->epi_tiles_m[act] = plan->tiles_m;
+      plan->epi_tiles_n[act] = plan->tiles_n;
       e = spec_mx(plan->cg, 0, plan->out_f32, plan->stages, std::min(plan->grid_units, plan->tiles_m * plan->tiles_n),
                   &plan->spec_epi[act], act);
     } else {
-      // The fused epilogue does real arithmetic per element, so it must hide behind
-      // the MMAs: a step-9 plan (both TMEM accumulators busy) runs it with one
-      // consumer per CTA, i.e. step 8's double-buffered 256x256 tile, same operand boxes.
-      const int cons = 1;
-      plan->epi_stages = ws_max_stages(plan->cg, cons);
-      plan->epi_tiles_m = ceil_div(plan->M, 128 * plan->cg * cons);
-      plan->epi_tiles_n = ceil_div(plan->N, 256);  // the fused kernels use 256-column tiles
-      const int tiles = plan->epi_tiles_m * plan->epi_tiles_n;
-      int active = ws_max_active_clusters(plan->cg, cons, 0, plan->out_f32, plan->epi_stages);
+      // The epilogue runs in the writeback warps while the MMAs of the next tile
+      // proceed.  Steps 7 and 8 have a TMEM double buffer for that; step 9's two
+      // consumers have one accumulator each, handed back only once the writeback
+      // has read the tile's last chunk.  With an activation that wait costs more
+      // than the second consumer saves (8192^3 bf16 + bias + SiLU + residual: 1305
+      // TFLOP/s on step 9's tile, 1618 on step 8's), so a step-9 plan runs the
+      // activations on step 8's 256 x 256 tile (same operand boxes) and only
+      // bias / residual / scales on its own (+ residual: 1784 against 1712).
+      const int cons = (plan->cg == 2 && plan->consumers == 2 && act == GEMM_ACT_NONE) ? 2 : 1;
+      plan->epi_stages[act] = ws_max_stages(plan->cg, cons);
+      plan->epi_tiles_m[act] = ceil_div(plan->M, 128 * plan->cg * cons);
+      plan->epi_tiles_n[act] = ceil_div(plan->N, 256);  // the fused kernels use 256-column tiles
+      const int tiles = plan->epi_tiles_m[act] * plan->epi_tiles_n[act];
+      int active = ws_max_active_clusters(plan->cg, cons, 0, plan->out_f32, plan->epi_stages[act]);
       if (active < 1) active = std::max(1, plan->num_sms / plan->cg);
-      e = spec_ws(plan->cg, cons, 0, plan->out_f32, plan->epi_stages, std::min(tiles, active), &plan->spec_epi[act],
-                  act);
+      e = spec_ws(plan->cg, cons, 0, plan->out_f32, plan->epi_stages[act], std::min(tiles, active),
+                  &plan->spec_epi[act], act);
     }
     if (e != cudaSuccess) {
       cudaGetLastError();

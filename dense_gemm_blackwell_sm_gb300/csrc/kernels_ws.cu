@@ -17,12 +17,19 @@ void* pick_fused(int act) {
   }
 }
 
-// the fused-epilogue kernels exist for one MMA consumer and the static scheduler
+// the fused-epilogue kernels exist for the static scheduler: every activation with
+// one MMA consumer (steps 7 and 8), bias / residual / scales alone with two on the
+// CTA pair (step 9)
 template <int CG, int NCONS>
 void* pick_kernel(int sched, bool out_f32, int fused_act) {
   if (fused_act >= 0) {
-    if (NCONS != 1) return nullptr;
-    return out_f32 ? pick_fused<float, CG>(fused_act) : pick_fused<__nv_bfloat16, CG>(fused_act);
+    if constexpr (NCONS == 2) {
+      if (CG != 2 || fused_act != EPI_ACT_NONE) return nullptr;
+      return out_f32 ? ws_kernel_ptr<float, 2, 2, SCHED_STATIC, EPI_ACT_NONE>()
+                     : ws_kernel_ptr<__nv_bfloat16, 2, 2, SCHED_STATIC, EPI_ACT_NONE>();
+    } else {
+      return out_f32 ? pick_fused<float, CG>(fused_act) : pick_fused<__nv_bfloat16, CG>(fused_act);
+    }
   }
   if (sched == SCHED_STREAM_K) {
     return out_f32 ? reinterpret_cast<void*>(k_ws_sk<float, CG, NCONS>)
