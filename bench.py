@@ -441,7 +441,9 @@ def main(argv=None):
         r = cpu_oracle_rate(w, budget_s=min(12.0, per_step * args.steps))
         line = {"impl": "reference", "metric": METRIC, "value": round(r["tflops"], 6), "unit": "TFLOP/s",
                 "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-                "ms_per_step": None, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                # one whole step (the full product) at the sampled rate, extrapolated
+                "ms_per_step": round(w.flops / (r["tflops"] * 1e12) * 1e3, 1),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                 "dtype": "f64", "data": "synthetic",
                 "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "in": w.in_dtype, "out": w.out_dtype},
                 "cpu_baseline": {"value": round(r["tflops"], 6), "unit": "TFLOP/s", "cores": r["threads"],
