@@ -165,6 +165,8 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
   constexpr int CW = (sizeof(OutT) == 4) ? 32 : 64;  // output columns per 128-byte staging row
   constexpr int NCH = BN / CW;      // whole 128-byte staging chunks of a row
   constexpr int TAIL = BN % CW;     // bf16 with BN = 224: 32 more columns, stored from registers
+  // writeback that first drains a single accumulator into registers (see below)
+  constexpr bool DRAIN = (MX || (NCONS == 2 && !SK && BN == WS_BN)) && CW == 64 && EPI < 0;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align_1024(smem_raw);
@@ -660,7 +662,7 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
           }
           continue;
         }
-        if constexpr ((MX || (NCONS == 2 && !SK && BN == WS_BN)) && CW == 64 && EPI < 0) {
+        if constexpr (DRAIN) {
           // single accumulator (MX, and each consumer of step 9): first pull this warp's
           // 32 x 256 slice into registers as packed bf16 and hand the accumulator back,
           // so the next tile's MMAs start while the stores below drain (step 9,
@@ -706,83 +708,85 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
           }
           continue;
         }
-        if constexpr (TAIL > 0) {
-          // bf16 with a 224-column tile: columns 192-223 go straight from registers to
-          // C (64 bytes of the lane's row; N % 8 == 0, so each 8-column group is in or out)
-          uint32_t v[32];
-          tmem_ld_32x32b_x32(tbase + (uint32_t)(NCH * CW), v);
-          tmem_wait_ld();
-          const int32_t row = row0 + (int32_t)lane, col = col_base + NCH * CW;
-          if (row < p.M) {
-            uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<OutT*>(p.C) + (int64_t)row * p.out_ld + col);
+        if constexpr (!KS && !DRAIN) {
+          if constexpr (TAIL > 0) {
+            // bf16 with a 224-column tile: columns 192-223 go straight from registers to
+            // C (64 bytes of the lane's row; N % 8 == 0, so each 8-column group is in or out)
+            uint32_t v[32];
+            tmem_ld_32x32b_x32(tbase + (uint32_t)(NCH * CW), v);
+            tmem_wait_ld();
+            const int32_t row = row0 + (int32_t)lane, col = col_base + NCH * CW;
+            if (row < p.M) {
+              uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<OutT*>(p.C) + (int64_t)row * p.out_ld + col);
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-              if (col + 8 * j < p.N)
-                dst[j] = make_uint4(pack_bf16x2(v[8 * j], v[8 * j + 1]), pack_bf16x2(v[8 * j + 2], v[8 * j + 3]),
-                                    pack_bf16x2(v[8 * j + 4], v[8 * j + 5]), pack_bf16x2(v[8 * j + 6], v[8 * j + 7]));
-          }
-        }
-#pragma unroll 1
-        for (int ch = 0; ch < NCH; ++ch) {
-          uint32_t v0[32], v1[32];
-          tmem_ld_32x32b_x32(tbase + (uint32_t)(ch * CW), v0);
-          if constexpr (CW == 64) tmem_ld_32x32b_x32(tbase + (uint32_t)(ch * CW + 32), v1);
-          tmem_wait_ld();
-          if constexpr (SK) {
-            // add the other clusters' parts of this tile (clusters with an empty share
-            // wrote nothing and are skipped, as in the count above)
-            int32_t np = 0;
-            for (int64_t c2 = sk_cid + 1; np < sk_nparts; ++c2) {
-              if (sk_total * (c2 + 1) / sk_units == sk_total * c2 / sk_units) continue;
-              const float* part = sk_part + (c2 - sk_cid - 1) * SK_SLOT_STRIDE * SK_WARP_FLOATS;
-              sk_add32(v0, part + (ch * CW) / 32 * SK_CHUNK_FLOATS, lane);
-              if constexpr (CW == 64) sk_add32(v1, part + ((ch * CW) / 32 + 1) * SK_CHUNK_FLOATS, lane);
-              ++np;
+              for (int j = 0; j < 4; ++j)
+                if (col + 8 * j < p.N)
+                  dst[j] = make_uint4(pack_bf16x2(v[8 * j], v[8 * j + 1]), pack_bf16x2(v[8 * j + 2], v[8 * j + 3]),
+                                      pack_bf16x2(v[8 * j + 4], v[8 * j + 5]), pack_bf16x2(v[8 * j + 6], v[8 * j + 7]));
             }
           }
-          if (ch == NCH - 1) {
-            // the whole accumulator is in registers: hand it back to the MMA warp
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) {
-              if constexpr (CG == 1) {
-                mbar_arrive(smem_u32(acc_empty + slot));
-              } else {
-                mbar_arrive_cluster(mapa_shared(smem_u32(acc_empty + slot), 0));
+#pragma unroll 1
+          for (int ch = 0; ch < NCH; ++ch) {
+            uint32_t v0[32], v1[32];
+            tmem_ld_32x32b_x32(tbase + (uint32_t)(ch * CW), v0);
+            if constexpr (CW == 64) tmem_ld_32x32b_x32(tbase + (uint32_t)(ch * CW + 32), v1);
+            tmem_wait_ld();
+            if constexpr (SK) {
+              // add the other clusters' parts of this tile (clusters with an empty share
+              // wrote nothing and are skipped, as in the count above)
+              int32_t np = 0;
+              for (int64_t c2 = sk_cid + 1; np < sk_nparts; ++c2) {
+                if (sk_total * (c2 + 1) / sk_units == sk_total * c2 / sk_units) continue;
+                const float* part = sk_part + (c2 - sk_cid - 1) * SK_SLOT_STRIDE * SK_WARP_FLOATS;
+                sk_add32(v0, part + (ch * CW) / 32 * SK_CHUNK_FLOATS, lane);
+                if constexpr (CW == 64) sk_add32(v1, part + ((ch * CW) / 32 + 1) * SK_CHUNK_FLOATS, lane);
+                ++np;
               }
             }
-          }
-          if constexpr (EPI >= 0) {
-            // bias, activation and residual, in fp32, before the single rounding to C's type
-            const int32_t row = row0 + (int32_t)lane;
-            const int32_t col0 = col_base + ch * CW;
-            apply_epilogue<OutT, 32, EPI>(v0, p, row, col0);
-            if constexpr (CW == 64) apply_epilogue<OutT, 32, EPI>(v1, p, row, col0 + 32);
-          }
-          uint8_t* buf = my_staging + (MX ? 0u : (tog & 1u) * 4096u);
-          // the store issued from `buf` (two chunks ago; MX: one) is done reading
-          if (lane == 0) bulk_wait_group_read<MX ? 0 : 1>();
-          __syncwarp();
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            uint4 val;
-            if constexpr (CW == 32) {
-              val = make_uint4(v0[4 * j], v0[4 * j + 1], v0[4 * j + 2], v0[4 * j + 3]);
-            } else {
-              const uint32_t* src = (j < 4) ? (v0 + 8 * j) : (v1 + 8 * (j - 4));
-              val = make_uint4(pack_bf16x2(src[0], src[1]), pack_bf16x2(src[2], src[3]),
-                               pack_bf16x2(src[4], src[5]), pack_bf16x2(src[6], src[7]));
+            if (ch == NCH - 1) {
+              // the whole accumulator is in registers: hand it back to the MMA warp
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) {
+                if constexpr (CG == 1) {
+                  mbar_arrive(smem_u32(acc_empty + slot));
+                } else {
+                  mbar_arrive_cluster(mapa_shared(smem_u32(acc_empty + slot), 0));
+                }
+              }
             }
-            *reinterpret_cast<uint4*>(buf + sw128_offset(lane, (uint32_t)j)) = val;
+            if constexpr (EPI >= 0) {
+              // bias, activation and residual, in fp32, before the single rounding to C's type
+              const int32_t row = row0 + (int32_t)lane;
+              const int32_t col0 = col_base + ch * CW;
+              apply_epilogue<OutT, 32, EPI>(v0, p, row, col0);
+              if constexpr (CW == 64) apply_epilogue<OutT, 32, EPI>(v1, p, row, col0 + 32);
+            }
+            uint8_t* buf = my_staging + (MX ? 0u : (tog & 1u) * 4096u);
+            // the store issued from `buf` (two chunks ago; MX: one) is done reading
+            if (lane == 0) bulk_wait_group_read<MX ? 0 : 1>();
+            __syncwarp();
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              uint4 val;
+              if constexpr (CW == 32) {
+                val = make_uint4(v0[4 * j], v0[4 * j + 1], v0[4 * j + 2], v0[4 * j + 3]);
+              } else {
+                const uint32_t* src = (j < 4) ? (v0 + 8 * j) : (v1 + 8 * (j - 4));
+                val = make_uint4(pack_bf16x2(src[0], src[1]), pack_bf16x2(src[2], src[3]),
+                                 pack_bf16x2(src[4], src[5]), pack_bf16x2(src[6], src[7]));
+              }
+              *reinterpret_cast<uint4*>(buf + sw128_offset(lane, (uint32_t)j)) = val;
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              const int32_t col0 = col_base + ch * CW;
+              if (row0 < p.M && col0 < p.N) tma_store_2d(tmC, smem_u32(buf), col0, row0);
+              bulk_commit_group();
+            }
+            ++tog;
           }
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            const int32_t col0 = col_base + ch * CW;
-            if (row0 < p.M && col0 < p.N) tma_store_2d(tmC, smem_u32(buf), col0, row0);
-            bulk_commit_group();
-          }
-          ++tog;
         }
       }
       if (!ok) break;
