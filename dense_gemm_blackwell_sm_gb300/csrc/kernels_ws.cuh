@@ -167,6 +167,9 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
   constexpr int TAIL = BN % CW;     // bf16 with BN = 224: 32 more columns, stored from registers
   // writeback that first drains a single accumulator into registers (see below)
   constexpr bool DRAIN = (MX || (NCONS == 2 && !SK && BN == WS_BN)) && CW == 64 && EPI < 0;
+  // the same for fp32 C on step 9's 224-column tile: two chunks into the staging
+  // buffers, the other five into registers
+  constexpr bool DRAIN32 = CG == 2 && NCONS == 2 && !SK && !MX && BN == 224 && CW == 32 && EPI < 0;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align_1024(smem_raw);
@@ -662,6 +665,61 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
           }
           continue;
         }
+        if constexpr (DRAIN32) {
+          // fp32 C, 7 chunks of 32 columns: one accumulator per consumer, so hand it back
+          // as early as possible.  Chunks 0 and 1 go to the two staging buffers once the
+          // previous tile's stores have read them, chunks 2-6 into registers; then the
+          // accumulator is free and the stores follow (4096^3 fp16 -> fp32 on 512 x 224
+          // tiles: the next tile's MMAs no longer wait for seven store round trips)
+          if (lane == 0) bulk_wait_group_read<0>();
+          __syncwarp();
+#pragma unroll
+          for (int ch = 0; ch < 2; ++ch) {
+            uint32_t v[32];
+            tmem_ld_32x32b_x32(tbase + (uint32_t)(ch * 32), v);
+            tmem_wait_ld();
+            uint8_t* buf = my_staging + ch * 4096;
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              *reinterpret_cast<uint4*>(buf + sw128_offset(lane, (uint32_t)j)) =
+                  make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+          }
+          uint32_t r[NCH - 2][32];
+#pragma unroll
+          for (int ch = 2; ch < NCH; ++ch) tmem_ld_32x32b_x32(tbase + (uint32_t)(ch * 32), r[ch - 2]);
+          tmem_wait_ld();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(acc_empty + slot), 0));
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+#pragma unroll
+            for (int ch = 0; ch < 2; ++ch) {
+              const int32_t col0 = col_base + ch * 32;
+              if (row0 < p.M && col0 < p.N) tma_store_2d(tmC, smem_u32(my_staging + ch * 4096), col0, row0);
+              bulk_commit_group();
+            }
+          }
+#pragma unroll
+          for (int ch = 2; ch < NCH; ++ch) {
+            uint8_t* buf = my_staging + (ch & 1) * 4096;
+            if (lane == 0) bulk_wait_group_read<1>();  // the store issued from `buf` two chunks ago is done reading
+            __syncwarp();
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              *reinterpret_cast<uint4*>(buf + sw128_offset(lane, (uint32_t)j)) =
+                  make_uint4(r[ch - 2][4 * j], r[ch - 2][4 * j + 1], r[ch - 2][4 * j + 2], r[ch - 2][4 * j + 3]);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              const int32_t col0 = col_base + ch * 32;
+              if (row0 < p.M && col0 < p.N) tma_store_2d(tmC, smem_u32(buf), col0, row0);
+              bulk_commit_group();
+            }
+          }
+          continue;
+        }
         if constexpr (DRAIN) {
           // single accumulator (MX, and each consumer of step 9): first pull this warp's
           // 32 x 256 slice into registers as packed bf16 and hand the accumulator back,
@@ -708,7 +766,7 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
           }
           continue;
         }
-        if constexpr (!KS && !DRAIN) {
+        if constexpr (!KS && !DRAIN && !DRAIN32) {
           if constexpr (TAIL > 0) {
             // bf16 with a 224-column tile: columns 192-223 go straight from registers to
             // C (64 bytes of the lane's row; N % 8 == 0, so each 8-column group is in or out)
