@@ -166,7 +166,7 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
   constexpr int NCH = BN / CW;      // whole 128-byte staging chunks of a row
   constexpr int TAIL = BN % CW;     // bf16 with BN = 224: 32 more columns, stored from registers
   // writeback that first drains a single accumulator into registers (see below)
-  constexpr bool DRAIN = (MX || (NCONS == 2 && !SK && BN == WS_BN)) && CW == 64 && EPI < 0;
+  constexpr bool DRAIN = (MX || (NCONS == 2 && !SK)) && CW == 64 && EPI < 0;
   // the same for fp32 C on step 9's 224-column tile: two chunks into the staging
   // buffers, the other five into registers
   constexpr bool DRAIN32 = CG == 2 && NCONS == 2 && !SK && !MX && BN == 224 && CW == 32 && EPI < 0;
@@ -722,9 +722,9 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
         }
         if constexpr (DRAIN) {
           // single accumulator (MX, and each consumer of step 9): first pull this warp's
-          // 32 x 256 slice into registers as packed bf16 and hand the accumulator back,
-          // so the next tile's MMAs start while the stores below drain (step 9,
-          // 8192 x 14336 x 4096: +1 %)
+          // 32 x 256 (or 224) slice into registers as packed bf16 and hand the
+          // accumulator back, so the next tile's MMAs start while the stores below
+          // drain (step 9, 8192 x 14336 x 4096: +1 %)
           uint32_t pk[NCH][32];
 #pragma unroll
           for (int ch = 0; ch < NCH; ++ch) {
@@ -737,6 +737,14 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
               pk[ch][m] = pack_bf16x2(v0[2 * m], v0[2 * m + 1]);
               pk[ch][16 + m] = pack_bf16x2(v1[2 * m], v1[2 * m + 1]);
             }
+          }
+          uint32_t pt[TAIL > 0 ? 16 : 1];  // 224-column tile: columns 192-223
+          if constexpr (TAIL > 0) {
+            uint32_t v[32];
+            tmem_ld_32x32b_x32(tbase + (uint32_t)(NCH * CW), v);
+            tmem_wait_ld();
+#pragma unroll
+            for (int m = 0; m < 16; ++m) pt[m] = pack_bf16x2(v[2 * m], v[2 * m + 1]);
           }
           tc_fence_before();
           __syncwarp();
@@ -764,25 +772,21 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
               bulk_commit_group();
             }
           }
-          continue;
-        }
-        if constexpr (!KS && !DRAIN && !DRAIN32) {
           if constexpr (TAIL > 0) {
-            // bf16 with a 224-column tile: columns 192-223 go straight from registers to
-            // C (64 bytes of the lane's row; N % 8 == 0, so each 8-column group is in or out)
-            uint32_t v[32];
-            tmem_ld_32x32b_x32(tbase + (uint32_t)(NCH * CW), v);
-            tmem_wait_ld();
+            // straight from registers to C: 64 bytes of the lane's row (N % 8 == 0, so each
+            // 8-column group is wholly in or out)
             const int32_t row = row0 + (int32_t)lane, col = col_base + NCH * CW;
             if (row < p.M) {
               uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<OutT*>(p.C) + (int64_t)row * p.out_ld + col);
 #pragma unroll
               for (int j = 0; j < 4; ++j)
-                if (col + 8 * j < p.N)
-                  dst[j] = make_uint4(pack_bf16x2(v[8 * j], v[8 * j + 1]), pack_bf16x2(v[8 * j + 2], v[8 * j + 3]),
-                                      pack_bf16x2(v[8 * j + 4], v[8 * j + 5]), pack_bf16x2(v[8 * j + 6], v[8 * j + 7]));
+                if (col + 8 * j < p.N) dst[j] = make_uint4(pt[4 * j], pt[4 * j + 1], pt[4 * j + 2], pt[4 * j + 3]);
             }
           }
+          continue;
+        }
+        if constexpr (!KS && !DRAIN && !DRAIN32) {
+          static_assert(TAIL == 0, "224-column tiles drain their accumulator first");
 #pragma unroll 1
           for (int ch = 0; ch < NCH; ++ch) {
             uint32_t v0[32], v1[32];
