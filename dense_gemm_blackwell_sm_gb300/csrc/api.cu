@@ -249,6 +249,10 @@ gemm_status_t prepare_launch(gemm_plan_s* p) {
     } else {
       e = spec_ws(p->cg, p->consumers, p->sched - 1, p->out_f32, p->stages, p->grid_units, &p->spec, -1, p->tile_n);
     }
+    // steps 7-9 launch as programmatic dependents: their set-up (barriers, TMEM,
+    // cluster) overlaps the end of the previous kernel on the stream, and every
+    // thread waits for that kernel to complete before touching global memory
+    if (is_ws(v)) p->spec.pdl = true;
   }
   if (e != cudaSuccess) {
     cudaGetLastError();
@@ -683,6 +687,7 @@ gemm_status_t run_with_epilogue(gemm_plan_s* plan, const void* A, const void* B,
       cudaGetLastError();
       return GEMM_ERR_CUDA;
     }
+    plan->spec_epi[act].pdl = true;
     plan->epi_ready[act] = true;
   }
   return launch_plan(plan, A, B, C, s, epi, sfa, sfb);

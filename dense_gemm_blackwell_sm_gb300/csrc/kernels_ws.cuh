@@ -105,6 +105,14 @@ constexpr uint32_t MX_TMEM_SLOT = 16;  // TMEM columns per stage: 4 for A, 8 for
 // bytes (coalesced in global memory, free of bank conflicts in shared memory)
 constexpr int SK_CHUNK_FLOATS = 32 * 32;
 
+// Programmatic dependent launch: let the next kernel on the stream begin its own
+// set-up, and wait until the previous one has completed and its memory is visible
+// (both are no-ops for a launch that did not ask for it)
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void grid_wait_prior() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // v[j] += the lane's 32 values of one partial chunk, for fp32 values held as bit patterns
 __device__ __forceinline__ void sk_add32(uint32_t (&v)[32], const float* chunk, uint32_t lane) {
   const float4* s4 = reinterpret_cast<const float4*>(chunk) + lane;
@@ -245,6 +253,10 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
   }
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // everything above touched only this CTA's (or cluster's) shared memory and TMEM;
+  // from here on global memory is read and written
+  grid_launch_dependents();
+  grid_wait_prior();
   const uint32_t peer_abort = (CG == 2) ? mapa_shared(smem_u32((const void*)abort_flag), rank ^ 1u) : 0u;
   const WaitCtl w{abort_flag, p.status, p.timeout_ns, peer_abort};
   // K elements per stage: one 128-byte swizzle row of A / B (64 x 16-bit or 128 x 8-bit)

@@ -511,3 +511,44 @@ def test_output_of_more_than_2_31_elements():
     assert np.array_equal(got, expect_bits(ref, "bf16"))
     del c
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("variant", [gemm.S7, gemm.S8, gemm.S9])
+def test_back_to_back_dependent_gemms(variant):
+    # Steps 7-9 launch as programmatic dependents of the previous kernel. Each GEMM
+    # here reads the one before it (as A, and as the residual of a fused epilogue),
+    # and the last one overwrites a buffer the third reads, all on one stream with
+    # no host synchronisation: every launch must see the finished data and must not
+    # overwrite what its predecessor still reads. Integer operands keep every fp32
+    # sum exact, so each bf16 result is unique.
+    M, K1, N1, N2 = 2048, 64, 256, 64
+    a, b1 = inputs.integer_operands(M, N1, K1, "bf16", seed=1)
+    _, b2 = inputs.integer_operands(8, N2, N1, "bf16", seed=2)
+    _, b3 = inputs.integer_operands(8, N1, N2, "bf16", seed=3, lo=-1, hi=1)
+    _, b4 = inputs.integer_operands(8, N1, K1, "bf16", seed=4)
+    opts = gemm.make_opts(variant=variant)
+    p1, p2, p3 = (gemm.Plan(M, n, k, gemm.BF16_BF16, opts) for n, k in ((N1, K1), (N2, N1), (N1, N2)))
+    da, d1, d2, d3, d4 = (x.to(DEV) for x in (a, b1, b2, b3, b4))
+    c1 = torch.empty((M, N1), device=DEV, dtype=torch.bfloat16)
+    c2 = torch.empty((M, N2), device=DEV, dtype=torch.bfloat16)
+    c3 = torch.empty((M, N1), device=DEV, dtype=torch.bfloat16)
+    for _ in range(3):
+        c1.fill_(float("nan")), c2.fill_(float("nan")), c3.fill_(float("nan"))
+        torch.cuda.synchronize()
+        p1.run(da, d1, c1)                        # c1 = a b1^T
+        p2.run(c1, d2, c2)                        # c2 = c1 b2^T
+        p3.run_epilogue(c2, d3, c3, residual=c1)  # c3 = c2 b3^T + c1
+        p1.run(da, d4, c1)                        # c1 = a b4^T, after c1 was read
+        torch.cuda.synchronize()
+        for p in (p1, p2, p3):
+            assert p.check() == gemm.OK
+        r1 = expect_bits(oracle.gemm(a, b1)[0], "bf16")
+        r2 = expect_bits(oracle.gemm(torch.tensor(r1).to(torch.bfloat16), b2)[0], "bf16")
+        pre3, _ = oracle.gemm(torch.tensor(r2).to(torch.bfloat16), b3)
+        r3 = expect_bits(pre3 + r1, "bf16")
+        r4 = expect_bits(oracle.gemm(a, b4)[0], "bf16")
+        assert np.array_equal(c2.float().cpu().numpy(), r2)
+        assert np.array_equal(c3.float().cpu().numpy(), r3)
+        assert np.array_equal(c1.float().cpu().numpy(), r4)
+    for p in (p1, p2, p3):
+        p.destroy()
