@@ -195,7 +195,9 @@ gemm_status_t prepare_launch(gemm_plan_s* p) {
   const int v = p->variant;
   if (v == GEMM_VARIANT_GEMV) {
     e = spec_gemv((int)p->M, (int)p->N, (int)p->K, p->in_bf16, p->out_f32, p->num_sms, &p->spec);
-    p->spec.pdl = (p->flags & GEMM_FLAG_STATIC_B) != 0;
+    // always a programmatic dependent: its CTAs are dispatched while the previous
+    // kernel drains; B is read before that kernel completes only with the flag
+    p->spec.pdl = true;
   } else if (v == GEMM_VARIANT_GEMV_TC) {
     e = spec_gemv_tc((int)p->M, (int)p->N, (int)p->K, p->in_bf16, p->out_f32, p->num_sms, p->split_k, p->stages,
                      &p->spec, &p->tgbase);
@@ -574,7 +576,8 @@ gemm_status_t launch_plan(gemm_plan_s* p, const void* A, const void* B, void* C,
   cudaError_t e = cudaSuccess;
   switch (p->spec.kind) {
     case ARGS_GEMV: {
-      GemvParams g{A, B, C, (int32_t)p->M, (int32_t)p->N, (int32_t)p->K};
+      GemvParams g{A, B, C, (int32_t)p->M, (int32_t)p->N, (int32_t)p->K,
+                   (p->flags & GEMM_FLAG_STATIC_B) ? 1 : 0};
       void* args[] = {&g};
       e = launch_spec(p->spec, args, s);
       break;

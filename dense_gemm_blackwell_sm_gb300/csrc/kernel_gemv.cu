@@ -87,8 +87,8 @@ __device__ __forceinline__ float warp_sum(float v) {
 
 // Each warp owns R rows of B at a time; every lane issues its GV_U 16-byte
 // loads of each row before using any of them.  The first rows' loads go out
-// before the activations are staged in shared memory (and, under programmatic
-// dependent launch, before the previous kernel in the stream has finished).
+// before the activations are staged in shared memory (and, when B is declared
+// static, before the previous kernel in the stream has finished).
 template <typename InT, typename OutT, int MT, int R>
 __global__ void __launch_bounds__(GV_THREADS) k_gemv(GemvParams g) {
   extern __shared__ uint4 xs[];  // MT rows x K/8 chunks
@@ -113,8 +113,9 @@ __global__ void __launch_bounds__(GV_THREADS) k_gemv(GemvParams g) {
       }
   };
   pdl_launch_dependents();
+  if (!g.early_b) pdl_wait_prior_grids();
   if (gw * R < g.N) load_rows(gw * R, 0);
-  pdl_wait_prior_grids();
+  if (g.early_b) pdl_wait_prior_grids();
   for (int i = threadIdx.x; i < MT * K8; i += GV_THREADS) {
     const int m = i / K8, c = i - m * K8;
     xs[i] = (m < g.M) ? X[(int64_t)m * K8 + c] : zero;
@@ -210,7 +211,8 @@ __global__ void __launch_bounds__(GV_THREADS) k_gemv_mma(GemvParams g) {
   const int JJ = (S + 3) / 4;
 
   pdl_launch_dependents();
-  bool first = true;
+  if (!g.early_b) pdl_wait_prior_grids();
+  bool first = g.early_b != 0;  // the wait for the previous kernel is still to come
   for (int j0 = 0; j0 < JJ; j0 += GM_J) {
 #pragma unroll
     for (int j = 0; j < GM_J; ++j)

@@ -89,6 +89,7 @@ struct GemvParams {
   const void* B;
   void* Y;
   int32_t M, N, K;
+  int32_t early_b;  // 1: B may be read before the previous kernel on the stream has completed
 };
 size_t gemv_smem_bytes(int M, int K);
 cudaError_t spec_gemv(int M, int N, int K, bool in_bf16, bool out_f32, int num_sms, LaunchSpec* out);

@@ -141,9 +141,11 @@ typedef struct {
 #define GEMM_LAYOUT_B_MN 2
 
 /* B is not written by the work queued before the call on the same stream
- * (weights of a decode step).  The GEMV variants then launch as programmatic
- * dependents: they start streaming B while the previous kernel still runs and
- * read A (the activations) only after it has completed. */
+ * (weights of a decode step).  The GEMV variants then start streaming B while
+ * the previous kernel still runs and read A (the activations) only after it has
+ * completed.  (Variants 7-9 and the CUDA-core GEMV always launch as programmatic
+ * dependents of the previous kernel, but without the flag they wait for it to
+ * complete before any access to global memory.) */
 #define GEMM_FLAG_STATIC_B 1
 
 typedef struct gemm_plan_s* gemm_plan_t;
