@@ -769,8 +769,11 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
           }
 #pragma unroll
           for (int ch = 0; ch < NCH; ++ch) {
-            uint8_t* buf = my_staging;
-            if (lane == 0) bulk_wait_group_read<0>();  // the previous store is done reading `buf`
+            // two staging buffers in turn (MX: one), so a chunk is staged while the
+            // store of the one before is still reading its buffer; the second
+            // consumer's accumulator is handed back that much sooner
+            uint8_t* buf = my_staging + (MX ? 0u : (tog & 1u) * 4096u);
+            if (lane == 0) bulk_wait_group_read<MX ? 0 : 1>();  // the store issued from `buf` is done reading
             __syncwarp();
 #pragma unroll
             for (int j = 0; j < 8; ++j)
@@ -783,6 +786,7 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
               if (row0 < p.M && col0 < p.N) tma_store_2d(tmC, smem_u32(buf), col0, row0);
               bulk_commit_group();
             }
+            ++tog;
           }
           if constexpr (TAIL > 0) {
             // straight from registers to C: 64 bytes of the lane's row (N % 8 == 0, so each
