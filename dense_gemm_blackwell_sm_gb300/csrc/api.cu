@@ -168,23 +168,51 @@ gemm_status_t current_device(int* dev, int* sms) {
 
 int ceil_div(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }
 
+// Time of the warp-specialised steps in units of one SM's MMA time per output
+// element (up to the common factor K): the waves of resident clusters the tiles
+// take, times a tile's area over the SMs of its cluster, over the step's per-SM
+// rate relative to step 9 on large shapes (8192^3 bf16: 1967, 1750, 1551 TFLOP/s
+// for steps 9, 8, 7).  Stream-K (step 9 only) spreads the whole area evenly.
+double ws_tile_cost(int64_t M, int64_t N, int tile_m, int tile_n, int cluster_sms, int units, double rate) {
+  const int64_t tiles = ((M + tile_m - 1) / tile_m) * ((N + tile_n - 1) / tile_n);
+  const int64_t waves = (tiles + units - 1) / units;
+  return (double)waves * tile_m * tile_n / cluster_sms / rate;
+}
+double ws_stream_k_cost(int64_t M, int64_t N, int units) {
+  const int64_t tiles = ((M + 511) / 512) * ((N + 255) / 256);
+  return (double)tiles * 512 * 256 / 2 / units / 0.92;  // partial sums and fix-ups: ~8 %
+}
+bool ws_stream_k_applies(int64_t M, int64_t N, int units) {
+  const int64_t tiles = ((M + 511) / 512) * ((N + 255) / 256);
+  const int64_t waves = (tiles + units - 1) / units;
+  return tiles >= units && (double)tiles / ((double)waves * units) < 0.7;
+}
+
 // Automatic variant: the decode GEMV with CUDA-core FMAs for one or two rows,
 // with warp-level MMAs on registers for up to 8, on the tcgen05 Tensor Core for
-// up to 16 rows; the plain-store
-// persistent kernel when C's rows are not 16-byte aligned for TMA stores;
-// otherwise the largest warp-specialised tile (step 9's 512x256 cluster tile,
-// then step 8's 256x256, then step 7's 128x256) that still gives every CTA pair
-// of the GPU at least one tile.
+// up to 16 rows; the plain-store persistent kernel when C's rows are not 16-byte
+// aligned for TMA stores; step 7 (with its K split over a cluster) for outputs
+// whose 128 x 256 tiles fill at most half the SMs and have K blocks to split;
+// otherwise the warp-specialised step whose tiles finish soonest by ws_tile_cost
+// (step 9 with 512 x 256 or 512 x 224 tiles or stream-K, step 8, step 7).
+// Measured against the former rule (the largest tile that gives every CTA pair a
+// tile): 2048 x 4096 x 4096 step 9 1550 TFLOP/s against step 8 1364; 256 x 14336 x
+// 4096 step 8 970 against step 7 862; 1024 x 8192 x 8192 step 9 1682 against 1466.
 int auto_variant(int64_t M, int64_t N, int64_t K, gemm_dtype_t dt, int sms) {
   if (M <= 2 && gemv_smem_bytes((int)M, (int)K) <= 200 * 1024) return GEMM_VARIANT_GEMV;
   if (M >= 3 && M <= 8) return GEMM_VARIANT_GEMV;
   if (M <= 16) return GEMM_VARIANT_GEMV_TC;
   if (!c_rows_tma_ok(N, dt)) return GEMM_VARIANT_S6_PERSISTENT;
-  const int64_t tn = (N + 255) / 256;
-  const int64_t pairs = std::max(1, sms / 2);
-  if (((M + 511) / 512) * tn >= pairs) return GEMM_VARIANT_S9_TWO_CONSUMERS;
-  if (((M + 255) / 256) * tn >= pairs) return GEMM_VARIANT_S8_CTA_PAIR;
-  return GEMM_VARIANT_S7_WARP_SPECIALIZED;
+  const int pairs = std::max(1, sms / 2);
+  const int64_t tiles7 = ((M + 127) / 128) * ((N + 255) / 256);
+  const int64_t kb = (K + (is_f8(dt) ? 127 : 63)) / (is_f8(dt) ? 128 : 64);
+  if (tiles7 * 2 <= sms && kb >= 32) return GEMM_VARIANT_S7_WARP_SPECIALIZED;
+  double c9 = std::min(ws_tile_cost(M, N, 512, 256, 2, pairs, 1.0), ws_tile_cost(M, N, 512, 224, 2, pairs, 1.0));
+  if (ws_stream_k_applies(M, N, pairs)) c9 = std::min(c9, ws_stream_k_cost(M, N, pairs));
+  const double c8 = ws_tile_cost(M, N, 256, 256, 2, pairs, 0.9);
+  const double c7 = ws_tile_cost(M, N, 128, 256, 1, std::max(1, sms), 0.8);
+  if (c9 <= c8 && c9 <= c7) return GEMM_VARIANT_S9_TWO_CONSUMERS;
+  return (c8 <= c7) ? GEMM_VARIANT_S8_CTA_PAIR : GEMM_VARIANT_S7_WARP_SPECIALIZED;
 }
 
 bool is_ws(int v) { return v >= GEMM_VARIANT_S7_WARP_SPECIALIZED && v <= GEMM_VARIANT_S9_TWO_CONSUMERS; }
@@ -377,15 +405,11 @@ gemm_status_t build_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, co
     if (variant == GEMM_VARIANT_S9_TWO_CONSUMERS && !p->in_mx && o.layout == 0 &&
         (o.sched == 0 || o.sched == GEMM_SCHED_STATIC)) {
       const int units = std::max(1, sms / 2);
-      auto fill = [&](int bn) {
-        const int64_t tn = (N + bn - 1) / bn, tiles = ((M + 511) / 512) * tn;
-        const int64_t u = std::min<int64_t>(tiles, units), waves = (tiles + u - 1) / u;
-        return ((double)N / (double)(tn * bn)) * ((double)tiles / (double)(waves * u));
-      };
-      // (below 70 % with whole 256-column tiles the automatic plan takes stream-K instead)
-      const bool stream_k_instead =
-          !o.sched && fill(256) < 0.7 && ((M + 511) / 512) * ((N + 255) / 256) >= units;
-      if (!stream_k_instead && fill(224) > fill(256) + 0.05) {
+      // (below 70 % wave fill with whole 256-column tiles the automatic plan takes
+      // stream-K instead); the narrower tile needs a clear margin (3 %) by ws_tile_cost
+      const bool stream_k_instead = !o.sched && ws_stream_k_applies(M, N, units);
+      if (!stream_k_instead &&
+          ws_tile_cost(M, N, 512, 224, 2, units, 1.0) < 0.97 * ws_tile_cost(M, N, 512, 256, 2, units, 1.0)) {
         p->tile_n = 224;
         const int maxs224 = ws_max_stages(p->cg, p->consumers, 224);
         p->stages = o.stages ? std::min<int>(o.stages, maxs224) : maxs224;
