@@ -217,6 +217,29 @@ int auto_variant(int64_t M, int64_t N, int64_t K, gemm_dtype_t dt, int sms) {
 
 bool is_ws(int v) { return v >= GEMM_VARIANT_S7_WARP_SPECIALIZED && v <= GEMM_VARIANT_S9_TWO_CONSUMERS; }
 
+// The automatic variant for a dtype and operand layout: auto_variant, then the
+// restrictions of the inputs.  Block-scaled inputs run on step 7 or 8 (the one
+// whose tiles finish soonest, with the block-scaled kernels' rates: 8192^3 step 8
+// 3140, step 7 2678 TFLOP/s); 8-bit inputs and MN-major operands have no GEMV or
+// ladder kernel, so a shape that would take one takes step 7 or 8 instead; an
+// explicit K split (split_k >= 2) runs on step 7.
+int choose_variant(int64_t M, int64_t N, int64_t K, gemm_dtype_t dt, int sms, int32_t layout, int32_t split_k) {
+  int v = auto_variant(M, N, K, dt, sms);
+  const int pairs = std::max(1, sms / 2);
+  auto step8_or_7 = [&](double rate8, double rate7) {
+    return ws_tile_cost(M, N, 256, 256, 2, pairs, rate8) <= ws_tile_cost(M, N, 128, 256, 1, std::max(1, sms), rate7)
+               ? GEMM_VARIANT_S8_CTA_PAIR
+               : GEMM_VARIANT_S7_WARP_SPECIALIZED;
+  };
+  if (is_mx(dt)) {
+    v = step8_or_7(1.0, 0.85);
+  } else if ((is_f8(dt) || layout != 0) && !is_ws(v)) {
+    v = step8_or_7(0.9, 0.8);
+  }
+  if (split_k >= 2 && is_ws(v) && !is_mx(dt)) v = GEMM_VARIANT_S7_WARP_SPECIALIZED;
+  return v;
+}
+
 // Fix the kernel, its launch shape and its pointer-independent parameters.
 gemm_status_t prepare_launch(gemm_plan_s* p) {
   cudaError_t e = cudaSuccess;
@@ -306,40 +329,23 @@ gemm_status_t build_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, co
   int dev = 0, sms = 0;
   st = current_device(&dev, &sms);
   if (st != GEMM_OK && !o.variant) return st;
-  int variant = o.variant ? o.variant : auto_variant(M, N, K, dtype, sms);
+  int variant = o.variant ? o.variant : choose_variant(M, N, K, dtype, sms, o.layout, o.split_k);
   if (is_mx(dtype)) {
     // block-scaled inputs run on step 7's one-CTA tile or step 8's CTA pair (one consumer)
-    if (o.variant && o.variant != GEMM_VARIANT_S7_WARP_SPECIALIZED && o.variant != GEMM_VARIANT_S8_CTA_PAIR)
+    if (variant != GEMM_VARIANT_S7_WARP_SPECIALIZED && variant != GEMM_VARIANT_S8_CTA_PAIR)
       return GEMM_ERR_UNSUPPORTED_SHAPE;
-    if (!o.variant) {
-      // the step whose tiles finish soonest (per-SM rates of the block-scaled kernels on
-      // 8192^3: step 8 3140, step 7 2678 TFLOP/s)
-      const int pairs = std::max(1, sms / 2);
-      variant = ws_tile_cost(M, N, 256, 256, 2, pairs, 1.0) <= ws_tile_cost(M, N, 128, 256, 1, std::max(1, sms), 0.85)
-                    ? GEMM_VARIANT_S8_CTA_PAIR
-                    : GEMM_VARIANT_S7_WARP_SPECIALIZED;
-    }
   }
   if (is_f8(dtype)) {
     // 8-bit inputs run on the warp-specialised kernels only, K-major
     if (o.layout != 0) return GEMM_ERR_UNSUPPORTED_SHAPE;
-    if (!o.variant && !is_ws(variant)) {
-      const int64_t tn = (N + 255) / 256, pairs = std::max(1, sms / 2);
-      variant = (((M + 255) / 256) * tn >= pairs) ? GEMM_VARIANT_S8_CTA_PAIR : GEMM_VARIANT_S7_WARP_SPECIALIZED;
-    }
     if (!is_ws(variant)) return GEMM_ERR_UNSUPPORTED_SHAPE;
   }
   if (o.split_k >= 2 && is_ws(variant) && !is_mx(dtype)) {
     // a K split over a cluster exists for step 7's tile (and the tensor-core GEMV)
-    if (!o.variant) variant = GEMM_VARIANT_S7_WARP_SPECIALIZED;
     if (variant != GEMM_VARIANT_S7_WARP_SPECIALIZED) return GEMM_ERR_UNSUPPORTED_SHAPE;
   }
   if (o.layout != 0) {
     // MN-major operands exist in the warp-specialised kernels only
-    if (!o.variant && !is_ws(variant)) {
-      const int64_t tn = (N + 255) / 256, pairs = std::max(1, sms / 2);
-      variant = (((M + 255) / 256) * tn >= pairs) ? GEMM_VARIANT_S8_CTA_PAIR : GEMM_VARIANT_S7_WARP_SPECIALIZED;
-    }
     if (!is_ws(variant)) return GEMM_ERR_UNSUPPORTED_SHAPE;
     if (((o.layout & GEMM_LAYOUT_A_MN) && M % 8 != 0) || ((o.layout & GEMM_LAYOUT_B_MN) && N % 8 != 0))
       return GEMM_ERR_UNSUPPORTED_SHAPE;
@@ -830,6 +836,17 @@ gemm_status_t run_cached(int64_t M, int64_t N, int64_t K, int64_t ldc, const voi
 }  // namespace
 
 extern "C" {
+
+gemm_status_t gemm_auto_variant(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, int32_t num_sms,
+                                int32_t* variant) {
+  if (!variant) return GEMM_ERR_INVALID_ARG;
+  *variant = 0;
+  const gemm_status_t st = validate_sizes(M, N, K, dtype);
+  if (st != GEMM_OK) return st;
+  if (num_sms < 2) return GEMM_ERR_INVALID_ARG;
+  *variant = choose_variant(M, N, K, dtype, num_sms, 0, 0);
+  return GEMM_OK;
+}
 
 gemm_status_t gemm_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, const gemm_opts_t* opts,
                         gemm_plan_t* out) {

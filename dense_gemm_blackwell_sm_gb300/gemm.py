@@ -95,6 +95,8 @@ def load():
     lib.gemm_plan_run_mx.restype = i32
     lib.gemm_mx_scale_bytes.argtypes = [i64, i64]
     lib.gemm_mx_scale_bytes.restype = i64
+    lib.gemm_auto_variant.argtypes = [i64, i64, i64, i32, i32, ctypes.POINTER(i32)]
+    lib.gemm_auto_variant.restype = i32
     lib.gemm_run.argtypes = [i64, i64, i64, p, p, p, i32, p]
     lib.gemm_run.restype = i32
     lib.gemm_run_host.argtypes = [i64, i64, i64, p, p, p, i32, p, p, p, p]
@@ -232,6 +234,15 @@ def dtype_code(in_dtype, out_dtype) -> int:
     if (i, o) not in DTYPES:
         raise ValueError("unsupported dtype pair %r -> %r" % (i, o))
     return DTYPES[(i, o)]
+
+
+def auto_variant(M: int, N: int, K: int, dtype: int, num_sms: int) -> int:
+    """The variant the automatic plan takes on a GPU with num_sms SMs (gemm_auto_variant);
+    needs no device.  Raises GemmError for invalid arguments."""
+    v = ctypes.c_int32(0)
+    _check(load().gemm_auto_variant(int(M), int(N), int(K), int(dtype), int(num_sms), ctypes.byref(v)),
+           "gemm_auto_variant")
+    return int(v.value)
 
 
 def mx_scale_bytes(rows: int, K: int) -> int:

@@ -162,6 +162,20 @@ typedef struct {
   int32_t tiles;           /* output tiles (cluster tiles for variants 8-9) */
 } gemm_plan_info_t;
 
+/* The kernel variant the automatic plan (opts.variant = 0, K-major operands)
+ * takes for these sizes and types on a GPU with num_sms SMs, without a device:
+ * the decode GEMVs for M <= 16, the plain-store persistent kernel when C's rows
+ * are not 16-byte aligned, step 7 with its K split over a cluster for outputs
+ * whose 128 x 256 tiles fill at most half the SMs (and K has at least 32 blocks),
+ * otherwise step 9, 8 or 7, whichever a cost model (waves of resident clusters x
+ * a tile's area per SM / the step's per-SM rate) says finishes soonest.  The tile
+ * width, schedule and split are settled by gemm_plan with the device's
+ * occupancy.  Errors: GEMM_ERR_INVALID_ARG (null variant, sizes out of range,
+ * num_sms < 2), GEMM_ERR_UNSUPPORTED_DTYPE, GEMM_ERR_UNSUPPORTED_SHAPE (K's row
+ * pitch); *variant is 0 then. */
+GEMM_API gemm_status_t gemm_auto_variant(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype,
+                                         int32_t num_sms, int32_t* variant);
+
 /* Build a plan for C = A * B^T of the given sizes and types on the current
  * device.  Validates sizes (M, N, K >= 1 and < 2^31; K % 8 == 0), the dtype,
  * the options and the device (compute capability 10.3), picks the kernel

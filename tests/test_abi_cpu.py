@@ -150,3 +150,40 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(gemm, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError):
         gemm.load()
+
+
+# The automatic plan's kernel choice, computed without a device, for a 152-SM GB300.
+AUTO_CASES = [
+    ((1, 4096, 4096, gemm.BF16_BF16), gemm.GEMV),       # decode GEMV, CUDA-core FMAs
+    ((8, 14336, 4096, gemm.BF16_BF16), gemm.GEMV),      # decode GEMV, warp-level MMAs
+    ((12, 4096, 4096, gemm.BF16_BF16), gemm.GEMV_TC),   # tcgen05 GEMV
+    ((200, 100, 64, gemm.F16_BF16), gemm.S6),           # C rows of 200 B: no TMA stores
+    ((8192, 8192, 8192, gemm.BF16_BF16), gemm.S9),      # 512 tiles of 512 x 256: 96 % of 7 waves
+    ((8192, 14336, 4096, gemm.BF16_BF16), gemm.S9),
+    ((4096, 4096, 4096, gemm.F16_F32), gemm.S9),        # (512 x 224 tiles chosen by the plan)
+    ((2048, 4096, 4096, gemm.BF16_BF16), gemm.S9),      # one wave of 76 (or 64) pair tiles
+    ((1024, 1024, 4096, gemm.BF16_BF16), gemm.S7),      # 32 tiles: split-K over clusters
+    ((1024, 1024, 1024, gemm.BF16_BF16), gemm.S8),      # too few K blocks to split
+    ((256, 14336, 4096, gemm.BF16_BF16), gemm.S8),      # 56 pair tiles beat 112 single tiles
+    ((1024, 4096, 4096, gemm.BF16_BF16), gemm.S8),
+    ((8, 4096, 4096, gemm.E4M3_BF16), gemm.S8),         # 8-bit inputs have no GEMV
+    ((8192, 8192, 8192, gemm.MXE4M3_BF16), gemm.S8),    # block-scaled: step 7 or 8 only
+    ((128, 25600, 4096, gemm.MXE4M3_BF16), gemm.S7),    # 100 tiles: one wave of 152 CTAs, two of 76 pairs
+]
+
+
+@pytest.mark.parametrize("args,variant", AUTO_CASES)
+def test_automatic_variant_without_a_device(lib, args, variant):
+    M, N, K, dt = args
+    assert gemm.auto_variant(M, N, K, dt, 152) == variant
+
+
+def test_automatic_variant_rejects_bad_arguments(lib):
+    import ctypes
+    v = ctypes.c_int32(7)
+    assert lib.gemm_auto_variant(0, 16, 16, gemm.BF16_BF16, 152, ctypes.byref(v)) == gemm.ERR_INVALID_ARG
+    assert v.value == 0
+    assert lib.gemm_auto_variant(16, 16, 16, gemm.BF16_BF16, 1, ctypes.byref(v)) == gemm.ERR_INVALID_ARG
+    assert lib.gemm_auto_variant(16, 16, 16, 99, 152, ctypes.byref(v)) == gemm.ERR_UNSUPPORTED_DTYPE
+    assert lib.gemm_auto_variant(16, 16, 12, gemm.BF16_BF16, 152, ctypes.byref(v)) == gemm.ERR_UNSUPPORTED_SHAPE
+    assert lib.gemm_auto_variant(16, 16, 16, gemm.BF16_BF16, 152, None) == gemm.ERR_INVALID_ARG
