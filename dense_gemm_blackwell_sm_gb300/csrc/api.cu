@@ -139,6 +139,8 @@ bool is_e5m2(gemm_dtype_t dt) {
 }
 
 int in_bytes(gemm_dtype_t dt) { return is_f8(dt) ? 1 : 2; }
+// K blocks of one 128-byte stage row (64 16-bit or 128 8-bit elements)
+int64_t k_blocks(int64_t K, gemm_dtype_t dt) { return (K + (is_f8(dt) ? 127 : 63)) / (is_f8(dt) ? 128 : 64); }
 
 // The TMA-store writeback of variants 7-9 needs rows of C to start 16-byte aligned.
 bool c_rows_tma_ok(int64_t N, gemm_dtype_t dt) { return (N * out_bytes(dt)) % 16 == 0; }
@@ -168,19 +170,27 @@ gemm_status_t current_device(int* dev, int* sms) {
 
 int ceil_div(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }
 
-// Time of the warp-specialised steps in units of one SM's MMA time per output
-// element (up to the common factor K): the waves of resident clusters the tiles
-// take, times a tile's area over the SMs of its cluster, over the step's per-SM
-// rate relative to step 9 on large shapes (8192^3 bf16: 1967, 1750, 1551 TFLOP/s
-// for steps 9, 8, 7).  Stream-K (step 9 only) spreads the whole area evenly.
-double ws_tile_cost(int64_t M, int64_t N, int tile_m, int tile_n, int cluster_sms, int units, double rate) {
+// Time of the warp-specialised steps, in units of one SM's MMA time per output
+// element and K block: the waves of resident clusters the tiles take, times a
+// tile's area over the SMs of its cluster, times (K blocks + the step's fixed
+// cost per tile, in K blocks), over the step's per-SM rate relative to step 9.
+// Fitted on GB300 bf16: step 8 against step 7 at equal SM counts (1024 x 4096,
+// 2048 x 2048, 512 x 8192 with K = 1024 ... 8192) gives a rate ratio of 1.21 and
+// fixed costs of 23 and 12 K blocks; 8192^3 (1967, 1750, 1551 TFLOP/s for steps 9,
+// 8, 7) puts step 9 at 1.12 x step 8, and short K on large outputs (4096 x 14336 x
+// 1024: step 9 1456, step 7 1323; 8192^2 x 1024: 1412, 1353) gives step 9 a fixed
+// cost near 22 K blocks.  Stream-K (step 9 only) spreads the whole area evenly.
+constexpr double kRate9 = 1.0, kRate8 = 0.89, kRate7 = 0.735;
+constexpr double kFixed9 = 22.0, kFixed8 = 24.0, kFixed7 = 12.0;
+double ws_tile_cost(int64_t M, int64_t N, int tile_m, int tile_n, int cluster_sms, int units, double rate,
+                    int64_t kb, double fixed) {
   const int64_t tiles = ((M + tile_m - 1) / tile_m) * ((N + tile_n - 1) / tile_n);
   const int64_t waves = (tiles + units - 1) / units;
-  return (double)waves * tile_m * tile_n / cluster_sms / rate;
+  return (double)waves * tile_m * tile_n / cluster_sms * ((double)kb + fixed) / rate;
 }
-double ws_stream_k_cost(int64_t M, int64_t N, int units) {
+double ws_stream_k_cost(int64_t M, int64_t N, int units, int64_t kb) {
   const int64_t tiles = ((M + 511) / 512) * ((N + 255) / 256);
-  return (double)tiles * 512 * 256 / 2 / units / 0.92;  // partial sums and fix-ups: ~8 %
+  return (double)tiles * 512 * 256 / 2 / units * ((double)kb + kFixed9) / (kRate9 * 0.92);  // partial sums: ~8 %
 }
 bool ws_stream_k_applies(int64_t M, int64_t N, int units) {
   const int64_t tiles = ((M + 511) / 512) * ((N + 255) / 256);
@@ -205,12 +215,13 @@ int auto_variant(int64_t M, int64_t N, int64_t K, gemm_dtype_t dt, int sms) {
   if (!c_rows_tma_ok(N, dt)) return GEMM_VARIANT_S6_PERSISTENT;
   const int pairs = std::max(1, sms / 2);
   const int64_t tiles7 = ((M + 127) / 128) * ((N + 255) / 256);
-  const int64_t kb = (K + (is_f8(dt) ? 127 : 63)) / (is_f8(dt) ? 128 : 64);
+  const int64_t kb = k_blocks(K, dt);
   if (tiles7 * 2 <= sms && kb >= 32) return GEMM_VARIANT_S7_WARP_SPECIALIZED;
-  double c9 = std::min(ws_tile_cost(M, N, 512, 256, 2, pairs, 1.0), ws_tile_cost(M, N, 512, 224, 2, pairs, 1.0));
-  if (ws_stream_k_applies(M, N, pairs)) c9 = std::min(c9, ws_stream_k_cost(M, N, pairs));
-  const double c8 = ws_tile_cost(M, N, 256, 256, 2, pairs, 0.9);
-  const double c7 = ws_tile_cost(M, N, 128, 256, 1, std::max(1, sms), 0.8);
+  double c9 = std::min(ws_tile_cost(M, N, 512, 256, 2, pairs, kRate9, kb, kFixed9),
+                       ws_tile_cost(M, N, 512, 224, 2, pairs, kRate9, kb, kFixed9));
+  if (ws_stream_k_applies(M, N, pairs)) c9 = std::min(c9, ws_stream_k_cost(M, N, pairs, kb));
+  const double c8 = ws_tile_cost(M, N, 256, 256, 2, pairs, kRate8, kb, kFixed8);
+  const double c7 = ws_tile_cost(M, N, 128, 256, 1, std::max(1, sms), kRate7, kb, kFixed7);
   if (c9 <= c8 && c9 <= c7) return GEMM_VARIANT_S9_TWO_CONSUMERS;
   return (c8 <= c7) ? GEMM_VARIANT_S8_CTA_PAIR : GEMM_VARIANT_S7_WARP_SPECIALIZED;
 }
@@ -226,15 +237,17 @@ bool is_ws(int v) { return v >= GEMM_VARIANT_S7_WARP_SPECIALIZED && v <= GEMM_VA
 int choose_variant(int64_t M, int64_t N, int64_t K, gemm_dtype_t dt, int sms, int32_t layout, int32_t split_k) {
   int v = auto_variant(M, N, K, dt, sms);
   const int pairs = std::max(1, sms / 2);
+  const int64_t kb = k_blocks(K, dt);
   auto step8_or_7 = [&](double rate8, double rate7) {
-    return ws_tile_cost(M, N, 256, 256, 2, pairs, rate8) <= ws_tile_cost(M, N, 128, 256, 1, std::max(1, sms), rate7)
+    return ws_tile_cost(M, N, 256, 256, 2, pairs, rate8, kb, kFixed8) <=
+                   ws_tile_cost(M, N, 128, 256, 1, std::max(1, sms), rate7, kb, kFixed7)
                ? GEMM_VARIANT_S8_CTA_PAIR
                : GEMM_VARIANT_S7_WARP_SPECIALIZED;
   };
   if (is_mx(dt)) {
-    v = step8_or_7(1.0, 0.85);
+    v = step8_or_7(1.0, 0.76);  // block-scaled rates: 8192^3 3140 / 2678, 1024 x 4096 x 4096 1735 / 1686
   } else if ((is_f8(dt) || layout != 0) && !is_ws(v)) {
-    v = step8_or_7(0.9, 0.8);
+    v = step8_or_7(kRate8, kRate7);
   }
   if (split_k >= 2 && is_ws(v) && !is_mx(dt)) v = GEMM_VARIANT_S7_WARP_SPECIALIZED;
   return v;
@@ -418,8 +431,9 @@ gemm_status_t build_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, co
       // (below 70 % wave fill with whole 256-column tiles the automatic plan takes
       // stream-K instead); the narrower tile needs a clear margin (3 %) by ws_tile_cost
       const bool stream_k_instead = !o.sched && ws_stream_k_applies(M, N, units);
-      if (!stream_k_instead &&
-          ws_tile_cost(M, N, 512, 224, 2, units, 1.0) < 0.97 * ws_tile_cost(M, N, 512, 256, 2, units, 1.0)) {
+      const int64_t kb = k_blocks(K, dtype);
+      if (!stream_k_instead && ws_tile_cost(M, N, 512, 224, 2, units, kRate9, kb, kFixed9) <
+                                   0.97 * ws_tile_cost(M, N, 512, 256, 2, units, kRate9, kb, kFixed9)) {
         p->tile_n = 224;
         const int maxs224 = ws_max_stages(p->cg, p->consumers, 224);
         p->stages = o.stages ? std::min<int>(o.stages, maxs224) : maxs224;

@@ -163,12 +163,15 @@ AUTO_CASES = [
     ((4096, 4096, 4096, gemm.F16_F32), gemm.S9),        # (512 x 224 tiles chosen by the plan)
     ((2048, 4096, 4096, gemm.BF16_BF16), gemm.S9),      # one wave of 76 (or 64) pair tiles
     ((1024, 1024, 4096, gemm.BF16_BF16), gemm.S7),      # 32 tiles: split-K over clusters
-    ((1024, 1024, 1024, gemm.BF16_BF16), gemm.S8),      # too few K blocks to split
+    ((1024, 1024, 1024, gemm.BF16_BF16), gemm.S7),      # too few K blocks to split; short K favours step 7
     ((256, 14336, 4096, gemm.BF16_BF16), gemm.S8),      # 56 pair tiles beat 112 single tiles
     ((1024, 4096, 4096, gemm.BF16_BF16), gemm.S8),
-    ((8, 4096, 4096, gemm.E4M3_BF16), gemm.S8),         # 8-bit inputs have no GEMV
+    ((8, 4096, 4096, gemm.E4M3_BF16), gemm.S7),         # 8-bit inputs have no GEMV (32 K blocks)
     ((8192, 8192, 8192, gemm.MXE4M3_BF16), gemm.S8),    # block-scaled: step 7 or 8 only
     ((128, 25600, 4096, gemm.MXE4M3_BF16), gemm.S7),    # 100 tiles: one wave of 152 CTAs, two of 76 pairs
+    ((2048, 2048, 2048, gemm.BF16_BF16), gemm.S7),      # 32 K blocks: the pair's fixed cost per tile shows
+    ((2048, 2048, 8192, gemm.BF16_BF16), gemm.S8),      # 128 K blocks: the pair's rate wins
+    ((1024, 8192, 8192, gemm.BF16_BF16), gemm.S9),
 ]
 
 

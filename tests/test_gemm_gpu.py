@@ -321,7 +321,7 @@ def test_stream_k_is_the_default_when_the_last_wave_is_short():
     p.destroy()
 
 
-# step 9 with 224-column tiles: chosen when they fill the waves of CTA pairs better;
+# step 9 with 224-column tiles: chosen when they finish the waves of CTA pairs sooner;
 # N = 18 * 224 + 200 puts the edge inside the last 32-column band of the last tile
 NARROW = [(4096, 4232, 200), (4096, 4096, 136)]
 
@@ -331,7 +331,7 @@ NARROW = [(4096, 4232, 200), (4096, 4096, 136)]
 def test_narrow_tiles_integer_bit_exact(shape, ti, to):
     M, N, K = shape
     a, b = inputs.integer_operands(M, N, K, ti, seed=N)
-    plan = gemm.Plan(M, N, K, gemm.dtype_code(ti, to))
+    plan = gemm.Plan(M, N, K, gemm.dtype_code(ti, to), gemm.make_opts(variant=gemm.S9))
     info = plan.info()
     assert info["variant"] == gemm.S9 and info["tile_n"] == 224, info
     c = torch.full((M, N), float("nan"), device=DEV, dtype=inputs.torch_dtype(to))
@@ -355,7 +355,7 @@ def test_narrow_tiles_integer_bit_exact(shape, ti, to):
 def test_narrow_tiles_fp8():
     M, N, K = 4096, 4232, 256
     a, b = inputs.integer_operands(M, N, K, "e4m3", seed=3, lo=-4, hi=4)
-    plan = gemm.Plan(M, N, K, gemm.E4M3_BF16)
+    plan = gemm.Plan(M, N, K, gemm.E4M3_BF16, gemm.make_opts(variant=gemm.S9))
     assert plan.info()["tile_n"] == 224
     c = torch.empty((M, N), device=DEV, dtype=torch.bfloat16)
     plan.run(a.to(DEV), b.to(DEV), c)
