@@ -27,7 +27,13 @@
 //
 // TMEM holds two 256-column fp32 accumulators.  Steps 7 and 8 alternate them
 // between consecutive tiles (the writeback of tile i overlaps the MMAs of
-// tile i+1); step 9 gives one to each consumer.
+// tile i+1); step 9 gives one to each consumer, so its writeback first drains
+// the accumulator into registers (bf16 C: packed; fp32 C on 224-column tiles:
+// two chunks staged, five held) and hands it back before the stores.
+//
+// All of steps 7-9 launch as programmatic dependents of the previous kernel on
+// the stream: the set-up below overlaps that kernel's end, and every thread
+// waits for it to complete before its first access to global memory.
 //
 // MX block scaling (k_ws_mx: one consumer, one CTA or a CTA pair): each stage
 // also brings the UE8M0 scales of its 128 K-elements (one 512-byte block for
@@ -57,9 +63,9 @@
 // blocks does them as its LAST segment ("owner" part), waits (bounded) for the
 // flags of all the following clusters whose shares start inside the tile, adds
 // their partials and stores the tile.  No cluster waits on one that has not
-// started, the owner clears the flags it consumed, and the layout of a slot
-// follows the writeback warps' own (warp, chunk, lane) order so both sides
-// move whole 4 KB runs.
+// started, the owner clears the flags it consumed, and a slot holds each
+// writeback warp's 32-column chunks in the layout of sk_add32, so both sides
+// move whole 4 KB runs with 512 contiguous bytes per warp access.
 //
 // Split-K within a cluster (KS template flag, step 7's 128x256 tile, plain
 // writeback): for outputs with too few tiles for the GPU, a cluster of 2-8 CTAs
