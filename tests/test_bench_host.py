@@ -85,3 +85,5 @@ def test_reference_arm_prints_one_line_under_torchrun():
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["unit"] == "TFLOP/s" and d["value"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle" and d["e2e"]["h2d_bytes_per_step"] == 0
+    assert d["ms_per_step"] > 0 and d["higher_is_better"] is True and d["config"]["workload"] == \
+        "single_tile_128x128x64_f16_f32"
