@@ -552,3 +552,39 @@ def test_back_to_back_dependent_gemms(variant):
         assert np.array_equal(c1.float().cpu().numpy(), r4)
     for p in (p1, p2, p3):
         p.destroy()
+
+
+def test_dependent_gemms_captured_in_a_cuda_graph():
+    # the programmatic launch of steps 7-9 inside stream capture: two GEMMs, the
+    # second reading the first's output, captured once and replayed
+    M, K1, N1, N2 = 2048, 64, 512, 64
+    a, b1 = inputs.integer_operands(M, N1, K1, "bf16", seed=21)
+    _, b2 = inputs.integer_operands(8, N2, N1, "bf16", seed=22)
+    opts = gemm.make_opts(variant=gemm.S9)
+    p1, p2 = gemm.Plan(M, N1, K1, gemm.BF16_BF16, opts), gemm.Plan(M, N2, N1, gemm.BF16_BF16, opts)
+    da, d1, d2 = a.to(DEV), b1.to(DEV), b2.to(DEV)
+    c1 = torch.empty((M, N1), device=DEV, dtype=torch.bfloat16)
+    c2 = torch.empty((M, N2), device=DEV, dtype=torch.bfloat16)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        p1.run(da, d1, c1, stream=s)   # first use outside the capture (operand descriptors)
+        p2.run(c1, d2, c2, stream=s)
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        p1.run(da, d1, c1, stream=s)
+        p2.run(c1, d2, c2, stream=s)
+    r1 = expect_bits(oracle.gemm(a, b1)[0], "bf16")
+    r2 = expect_bits(oracle.gemm(torch.tensor(r1).to(torch.bfloat16), b2)[0], "bf16")
+    for _ in range(3):
+        c1.fill_(float("nan"))
+        c2.fill_(float("nan"))
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        assert p1.check() == gemm.OK and p2.check() == gemm.OK
+        assert np.array_equal(c1.float().cpu().numpy(), r1)
+        assert np.array_equal(c2.float().cpu().numpy(), r2)
+    del g
+    p1.destroy()
+    p2.destroy()
