@@ -58,8 +58,8 @@ typedef enum {
   /* MX block-scaled 8-bit inputs (OCP Microscaling formats MXFP8): every 32
    * consecutive K elements of a row of A or B share one UE8M0 scale 2^(e-127);
    * run with gemm_plan_run_mx, which takes the two scale arrays.  Variants 7
-   * and 8 (one MMA consumer; the automatic plan picks 8 when every CTA pair
-   * gets a tile). */
+   * and 8 (one MMA consumer; the automatic plan picks the one whose tiles
+   * finish first, see gemm_auto_variant). */
   GEMM_MXE4M3_F32 = 8,  /* MXFP8 E4M3 in, fp32 out */
   GEMM_MXE4M3_BF16 = 9, /* MXFP8 E4M3 in, bf16 out */
   GEMM_MXE5M2_F32 = 10, /* MXFP8 E5M2 in, fp32 out */
@@ -218,7 +218,10 @@ typedef struct {
 
 /* gemm_plan_run with the fused epilogue.  Needs a plan of variant 7, 8 or 9
  * (the automatic plan of most shapes with M > 16); other plans return
- * GEMM_ERR_UNSUPPORTED_SHAPE.  The epilogue kernel uses the static scheduler. */
+ * GEMM_ERR_UNSUPPORTED_SHAPE.  The epilogue kernel uses the static scheduler;
+ * with an activation it runs on one MMA consumer per CTA (a variant-9 plan then
+ * uses variant 8's 256 x 256 tile), bias / residual / scales alone keep the
+ * plan's own variant. */
 GEMM_API gemm_status_t gemm_plan_run_epilogue(gemm_plan_t plan, const void* A, const void* B, void* C,
                                               const gemm_epilogue_t* epilogue, gemm_stream_t stream);
 
