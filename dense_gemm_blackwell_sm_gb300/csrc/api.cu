@@ -12,6 +12,7 @@
 #include <cudaTypedefs.h>
 
 #include "gemm.h"
+#include "idesc.h"
 #include "kernel_common.cuh"
 #include "launch.h"
 
@@ -36,6 +37,7 @@ struct gemm_plan_s {
   uint32_t debug_flags;
   int32_t flags;      // GEMM_FLAG_*
   int32_t layout;     // GEMM_LAYOUT_*
+  int32_t gemv_pf_rows;  // GEMV: weight rows prefetched into L2 before the programmatic wait
   uint32_t* scratch;  // [0] status word, [1] tile counter, [2] finished counter
   float* sk_ws;       // stream-K workspace (one slot per cluster), or null
   uint32_t* sk_flags; // stream-K flags (one per writeback warp of each slot), or null
@@ -109,16 +111,6 @@ bool encode_mx_pairs(CUtensorMap* m, const void* ptr, uint64_t k_blocks, uint64_
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
-}
-
-// tcgen05 instruction descriptor, kind::f16: fp32 accumulator, A and B both
-// fp16 or both bf16, both K-major, MMA shape M x N
-uint32_t make_idesc(bool bf16, int M, int N) {
-  const uint32_t ab = bf16 ? 1u : 0u;
-  return (1u << 4)                      // D format: f32
-         | (ab << 7) | (ab << 10)       // A / B format
-         | ((uint32_t)(N >> 3) << 17)   // N / 8
-         | ((uint32_t)(M >> 4) << 24);  // M / 16
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -258,7 +250,8 @@ gemm_status_t prepare_launch(gemm_plan_s* p) {
   cudaError_t e = cudaSuccess;
   const int v = p->variant;
   if (v == GEMM_VARIANT_GEMV) {
-    e = spec_gemv((int)p->M, (int)p->N, (int)p->K, p->in_bf16, p->out_f32, p->num_sms, &p->spec);
+    e = spec_gemv((int)p->M, (int)p->N, (int)p->K, p->in_bf16, p->out_f32, p->num_sms,
+                  (p->flags & GEMM_FLAG_STATIC_B) != 0, &p->spec, &p->gemv_pf_rows);
     // always a programmatic dependent: its CTAs are dispatched while the previous
     // kernel drains; B is read before that kernel completes only with the flag
     p->spec.pdl = true;
@@ -279,29 +272,21 @@ gemm_status_t prepare_launch(gemm_plan_s* p) {
     k.timeout_ns = p->timeout_ns;
     k.debug_flags = p->debug_flags;
     k.out_ld = (int32_t)p->ldc;
-    k.idesc = is_ws(v) ? make_idesc(p->in_bf16, 128 * p->cg, p->tile_n) : make_idesc(p->in_bf16, 128, 128);
+    k.idesc = is_ws(v) ? idesc_f16(p->in_bf16, 128 * p->cg, p->tile_n) : idesc_f16(p->in_bf16, 128, 128);
     k.mma_kind = 0;
     k.bk = 64;
     if (p->in_mx) {
-      // kind::mxf8f6f4 descriptor: A / B format E4M3 = 0, E5M2 = 1 (bits 7-9, 10-12),
-      // N / 8 (17-22), scale type UE8M0 (bit 23), M / 16 (24-28); the scale-byte
-      // selectors (B: bits 4-5, A: bits 29-30) are added per MMA by the kernel
-      const uint32_t fmt = p->in_e5m2 ? 1u : 0u;
-      k.idesc = (fmt << 7) | (fmt << 10) | ((uint32_t)(256 >> 3) << 17) | (1u << 23) |
-                ((uint32_t)((128 * p->cg) >> 4) << 24);
+      k.idesc = idesc_mx(p->in_e5m2, 128 * p->cg, 256);
       k.mma_kind = 2;
       k.bk = 128;
     } else if (p->in_f8) {
-      // kind::f8f6f4 descriptor: A / B format E4M3 = 0, E5M2 = 1, fp32 accumulator
-      const uint32_t fmt = p->in_e5m2 ? 1u : 0u;
-      k.idesc = (1u << 4) | (fmt << 7) | (fmt << 10) | ((uint32_t)(p->tile_n >> 3) << 17) |
-                ((uint32_t)((128 * p->cg) >> 4) << 24);
+      k.idesc = idesc_f8(p->in_e5m2, 128 * p->cg, p->tile_n);
       k.mma_kind = 1;
       k.bk = 128;
     }
     k.layout = (uint32_t)p->layout;
-    if (p->layout & GEMM_LAYOUT_A_MN) k.idesc |= 1u << 15;  // A MN-major
-    if (p->layout & GEMM_LAYOUT_B_MN) k.idesc |= 1u << 16;  // B MN-major
+    if (p->layout & GEMM_LAYOUT_A_MN) k.idesc |= IDESC_A_MN_MAJOR;
+    if (p->layout & GEMM_LAYOUT_B_MN) k.idesc |= IDESC_B_MN_MAJOR;
     if (v <= GEMM_VARIANT_S3_MULTI_CTA) {
       e = spec_step123((int)p->M, (int)p->N, p->out_f32, &p->spec);
     } else if (v <= GEMM_VARIANT_S5_PIPELINE) {
@@ -625,7 +610,7 @@ gemm_status_t launch_plan(gemm_plan_s* p, const void* A, const void* B, void* C,
   switch (p->spec.kind) {
     case ARGS_GEMV: {
       GemvParams g{A, B, C, (int32_t)p->M, (int32_t)p->N, (int32_t)p->K,
-                   (p->flags & GEMM_FLAG_STATIC_B) ? 1 : 0};
+                   (p->flags & GEMM_FLAG_STATIC_B) ? 1 : 0, p->gemv_pf_rows};
       void* args[] = {&g};
       e = launch_spec(p->spec, args, s);
       break;
@@ -655,7 +640,7 @@ gemm_status_t launch_plan(gemm_plan_s* p, const void* A, const void* B, void* C,
         k.tiles_n = p->epi_tiles_n[epi->activation];
         k.stages = p->epi_stages[epi->activation];
         // the fused kernels' MMAs are 256 columns wide whatever the plan's own tile
-        k.idesc = (k.idesc & ~(0x3Fu << 17)) | ((256u >> 3) << 17);
+        k.idesc = idesc_with_n(k.idesc, 256);
         spec = &p->spec_epi[epi->activation];
       }
       k.A = static_cast<const uint16_t*>(A);

@@ -5,26 +5,39 @@
 // "Roofline：找到天花板") use the decode-stage 1 x 4096 x 4096 vector-matrix
 // product as the bandwidth-bound example: about one FLOP per byte, far below
 // the ridge point, so the Tensor Core is irrelevant and the kernel's only job
-// is to stream the weight B from HBM once at full bandwidth.  Design:
-//   * each warp owns R rows of B at a time; every lane issues its 16-byte
-//     non-allocating loads of those rows before using any of them, so each SM
-//     keeps well over 64 KB of B in flight;
-//   * X (at most 16 rows) is staged once per CTA in shared memory, after the
-//     first weight loads have been issued;
-//   * fp32 FMAs per lane, a shuffle reduction per output, one bf16/fp32 store;
-//   * the grid covers the rows exactly once (no atomics, no scratch memory).
+// is to stream the weight B from HBM once at full bandwidth.  Every weight
+// byte is read once with 16-byte non-allocating loads by every lane straight
+// into registers; X (at most 16 rows) is staged in shared memory; fp32 FMAs
+// per lane, a shuffle reduction per output, one bf16/fp32 store; the grid
+// covers the rows exactly once (no atomics, no scratch memory).
+//
+// The kernels launch as programmatic dependents of the previous kernel on the
+// stream, and two cases differ in what they may do before that kernel has
+// completed:
+//   * B may be written by the previous kernel (the default).  Nothing of B may
+//     be read before griddepcontrol.wait, so the kernel asks L2 to prefetch
+//     the first 2 KB of each warp's rows while it waits (a prefetch returns no
+//     data, and L2 is coherent for every SM, so a later load still sees what
+//     the previous kernel wrote).  After the wait each lane keeps two groups
+//     of four 16-byte loads in flight and refills a group as soon as it has
+//     been consumed (k_gemv_roll, k_gemv_mma_roll), so the weight stream
+//     does not stall between the halves of a row.  In a chain of dependent
+//     1 x 4096 x 4096 launches this took a launch from 7.45 us (whole half
+//     rows in flight, refilled after each half) to 6.5 us.
+//   * B is declared static (GEMM_FLAG_STATIC_B): the first half row of every
+//     warp is loaded into registers before the wait (k_gemv, k_gemv_mma), so
+//     the weights stream while the previous kernel drains.
 //
 // For 3 <= M <= 8 the CUDA cores would need M FMAs per weight element, more
 // than they can issue at HBM speed, and the tcgen05 GEMV is fed by TMA, which
 // streams at most about 40 GB/s per SM from DRAM.  k_gemv_mma keeps the load
-// path of k_gemv (16-byte loads by every lane straight into registers) and
-// does the arithmetic with warp-level mma.sync m16n8k16: 8 weight rows as the
-// A operand (rows 8-15 of the fragment are zero), the M <= 8 activation rows
-// as the n8 B operand, fp32 accumulation.  Each lane's 16-byte weight chunk
-// and the matching 16-byte activation chunk feed two MMAs; the order of K
-// inside the fragments is free because A and B use the same order.  A CTA owns
-// 8 weight rows; its 8 warps split K and add their 8 x 8 partial sums in
-// shared memory.
+// path (16-byte loads by every lane straight into registers) and does the
+// arithmetic with warp-level mma.sync m16n8k16: 8 weight rows as the A operand
+// (rows 8-15 of the fragment are zero), the M <= 8 activation rows as the n8 B
+// operand, fp32 accumulation.  Each lane's 16-byte weight chunk and the
+// matching 16-byte activation chunk feed two MMAs; the order of K inside the
+// fragments is free because A and B use the same order.  A CTA owns 8 weight
+// rows; its 8 warps split K and add their 8 x 8 partial sums in shared memory.
 #include <algorithm>
 #include <type_traits>
 
@@ -54,6 +67,11 @@ __device__ __forceinline__ void pdl_launch_dependents() {
 }
 __device__ __forceinline__ void pdl_wait_prior_grids() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// ask L2 to fetch the 128-byte line holding p (no data returned)
+__device__ __forceinline__ void prefetch_l2_line(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 
 template <typename InT>
@@ -166,6 +184,81 @@ __global__ void __launch_bounds__(GV_THREADS) k_gemv(GemvParams g) {
   }
 }
 
+// B possibly written by the previous kernel, one activation row, K a multiple
+// of 1024: two groups of GR_V 16-byte loads per lane in flight over the warp's
+// stream of groups (a group is GR_V consecutive 512-byte segments of one row;
+// the warp's rows are gw, gw + nw, ...), each group refilled as soon as it has
+// been consumed.  Before the wait, L2 prefetches the first pf groups of the
+// stream.  Four CTAs must fit an SM (512 CTAs give every warp of 1 x 4096 x
+// 4096 one row in one wave), hence the register bound and the outer loop kept
+// rolled: left to itself the compiler spent 76-112 registers on this loop,
+// three CTAs per SM or fewer, and the launch took a microsecond longer.
+constexpr int GR_G = 2;  // groups in flight per lane
+constexpr int GR_V = 4;  // 16-byte loads per group
+
+template <typename InT, typename OutT>
+__global__ void __launch_bounds__(GV_THREADS, 4) k_gemv_roll(GemvParams g) {
+  extern __shared__ uint4 xs[];  // the activation row, K/8 chunks
+  const int K8 = g.K / 8;
+  const int HPR = K8 / (32 * GR_V);  // groups per row
+  const uint4* X = reinterpret_cast<const uint4*>(g.X);
+  const uint4* B = reinterpret_cast<const uint4*>(g.B);
+  const int lane = threadIdx.x & 31;
+  const int gw = blockIdx.x * (GV_THREADS / 32) + (threadIdx.x >> 5);
+  const int nw = gridDim.x * (GV_THREADS / 32);
+  const int nrows = gw < g.N ? (g.N - gw + nw - 1) / nw : 0;
+  const int H = nrows * HPR;  // groups of this warp
+
+  uint4 buf[GR_G][GR_V];
+  auto load_grp = [&](int h, uint4 (&b)[GR_V]) {
+    if (h < H) {
+      const int r = h / HPR, j = h - r * HPR;
+      const uint4* src = B + (int64_t)(gw + r * nw) * K8 + j * GR_V * 32 + lane;
+#pragma unroll
+      for (int v = 0; v < GR_V; ++v) b[v] = ld_stream_v4(src + v * 32);
+    }
+  };
+  pdl_launch_dependents();
+  if (g.pf_rows) {
+    for (int h = 0; h < g.pf_rows && h < H; ++h) {
+      const int r = h / HPR, j = h - r * HPR;
+      const char* base = reinterpret_cast<const char*>(B + (int64_t)(gw + r * nw) * K8 + j * GR_V * 32);
+      if (lane < GR_V * 4) prefetch_l2_line(base + lane * 128);  // the group's 16 lines
+    }
+  }
+  if (!g.early_b) pdl_wait_prior_grids();
+#pragma unroll
+  for (int i = 0; i < GR_G; ++i) load_grp(i, buf[i]);
+  if (g.early_b) pdl_wait_prior_grids();
+  for (int i = threadIdx.x; i < K8; i += GV_THREADS) xs[i] = X[i];
+  __syncthreads();
+  float acc = 0.f;
+#pragma unroll 1
+  for (int h0 = 0; h0 < H; h0 += GR_G) {
+#pragma unroll
+    for (int i = 0; i < GR_G; ++i) {
+      const int h = h0 + i;
+      if (h < H) {
+        const int r = h / HPR, j = h - r * HPR;
+#pragma unroll
+        for (int v = 0; v < GR_V; ++v) acc = dot8<InT>(xs[j * GR_V * 32 + v * 32 + lane], buf[i][v], acc);
+        load_grp(h + GR_G, buf[i]);
+        if (j == HPR - 1) {
+          acc = warp_sum(acc);
+          if (lane == 0) {
+            if constexpr (sizeof(OutT) == 4) {
+              reinterpret_cast<float*>(g.Y)[gw + r * nw] = acc;
+            } else {
+              reinterpret_cast<__nv_bfloat16*>(g.Y)[gw + r * nw] = __float2bfloat16_rn(acc);
+            }
+          }
+          acc = 0.f;
+        }
+      }
+    }
+  }
+}
+
 template <typename InT>
 __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1) {
   // rows 8-15 of A (a1, a3) are zero
@@ -248,48 +341,146 @@ __global__ void __launch_bounds__(GV_THREADS) k_gemv_mma(GemvParams g) {
   }
 }
 
+// B possibly written by the previous kernel: the same product with the weight
+// chunks of each lane in two groups of GM_J loads, each group refilled as soon
+// as it has been consumed; the activation chunks are read when a group is
+// consumed (they are small and stay in L1).  Before the wait, L2 prefetches
+// the first pf groups of each row slice.
 template <typename InT, typename OutT>
-cudaError_t spec_mma(int N, LaunchSpec* out) {
-  auto k = k_gemv_mma<InT, OutT>;
-  out->func = (const void*)k;
+__global__ void __launch_bounds__(GV_THREADS, 4) k_gemv_mma_roll(GemvParams g) {
+  __shared__ float red[GV_THREADS / 32][GM_ROWS][8];
+  constexpr int MG = 2;  // groups in flight per lane
+  const int K8 = g.K / 8;
+  const int warps = GV_THREADS / 32;
+  const int S = (K8 + warps - 1) / warps;  // chunks of each row in this warp's K slice
+  const int w = (int)warp_idx(), lane = (int)lane_idx();
+  const int gr = lane >> 2, c = lane & 3;  // fragment row / column group
+  const int n0 = (int)blockIdx.x * GM_ROWS;
+  const int row = n0 + gr;
+  const uint4 zero = make_uint4(0, 0, 0, 0);
+  const uint4* X = reinterpret_cast<const uint4*>(g.X);
+  const uint4* B = reinterpret_cast<const uint4*>(g.B);
+  // chunk j of this lane: 4 consecutive chunks (32 K-elements) per j across c
+  auto chunk = [&](int j) { return w * S + 4 * j + c; };
+  auto valid = [&](int j) { return 4 * j + c < S && chunk(j) < K8; };
+  const int JJ = (S + 3) / 4;
+  const int NG = (JJ + GM_J - 1) / GM_J;  // groups of GM_J chunks per lane
+  uint4 bw[MG][GM_J];
+  auto load_grp = [&](int q, uint4 (&b)[GM_J]) {
+    if (q < NG) {
+#pragma unroll
+      for (int v = 0; v < GM_J; ++v) {
+        const int j = q * GM_J + v;
+        b[v] = (j < JJ && row < g.N && valid(j)) ? ld_stream_v4(B + (int64_t)row * K8 + chunk(j)) : zero;
+      }
+    }
+  };
+
+  pdl_launch_dependents();
+  // a group spans 4 * GM_J chunks (two 128-byte lines) of each of the 8 rows
+  for (int q = 0; q < g.pf_rows && q < NG; ++q) {
+    const int k8 = w * S + q * 4 * GM_J + 8 * c;
+    if (c < 2 && row < g.N && q * 4 * GM_J + 8 * c < S && k8 < K8) prefetch_l2_line(B + (int64_t)row * K8 + k8);
+  }
+  pdl_wait_prior_grids();
+#pragma unroll
+  for (int i = 0; i < MG; ++i) load_grp(i, bw[i]);
+  float d[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int q0 = 0; q0 < NG; q0 += MG) {
+#pragma unroll
+    for (int i = 0; i < MG; ++i) {
+      const int q = q0 + i;
+      if (q < NG) {
+        uint4 xv[GM_J];
+#pragma unroll
+        for (int v = 0; v < GM_J; ++v) {
+          const int j = q * GM_J + v;
+          xv[v] = (j < JJ && gr < g.M && valid(j)) ? X[(int64_t)gr * K8 + chunk(j)] : zero;
+        }
+#pragma unroll
+        for (int v = 0; v < GM_J; ++v) {
+          mma_16816<InT>(d, bw[i][v].x, bw[i][v].y, xv[v].x, xv[v].y);
+          mma_16816<InT>(d, bw[i][v].z, bw[i][v].w, xv[v].z, xv[v].w);
+        }
+        load_grp(q + MG, bw[i]);
+      }
+    }
+  }
+  // d[0], d[1]: weight row gr, activation rows 2c and 2c + 1 (d[2], d[3]: zero rows)
+  red[w][gr][2 * c] = d[0];
+  red[w][gr][2 * c + 1] = d[1];
+  __syncthreads();
+  if ((int)threadIdx.x < GM_ROWS * 8) {
+    const int r = (int)threadIdx.x >> 3, m = (int)threadIdx.x & 7;
+    float v = 0.f;
+#pragma unroll
+    for (int q = 0; q < warps; ++q) v += red[q][r][m];
+    if (m < g.M && n0 + r < g.N) {
+      if constexpr (sizeof(OutT) == 4) {
+        reinterpret_cast<float*>(g.Y)[(int64_t)m * g.N + n0 + r] = v;
+      } else {
+        reinterpret_cast<__nv_bfloat16*>(g.Y)[(int64_t)m * g.N + n0 + r] = __float2bfloat16_rn(v);
+      }
+    }
+  }
+}
+
+// L2 prefetch before the wait: one group per warp (or row slice) of the
+// weight stream, two when each warp streams more than four groups.  Larger
+// prefetches slowed the chain of dependent 1 x 4096 x 4096 launches: the
+// prefetched lines compete with the previous kernel's own loads.
+int prefetch_groups(int groups_per_warp) { return groups_per_warp > 4 ? 2 : 1; }
+
+template <typename InT, typename OutT>
+cudaError_t spec_mma(int N, int K, bool static_b, LaunchSpec* out, int* pf) {
+  out->func = static_b ? (const void*)k_gemv_mma<InT, OutT> : (const void*)k_gemv_mma_roll<InT, OutT>;
   out->grid = dim3((unsigned)((N + GM_ROWS - 1) / GM_ROWS), 1, 1);
   out->block = dim3(GV_THREADS, 1, 1);
   out->smem = 0;
   out->cluster = 1;
   out->kind = ARGS_GEMV;
+  const int S = (K / 8 + 7) / 8, JJ = (S + 3) / 4;
+  *pf = static_b ? 0 : prefetch_groups((JJ + GM_J - 1) / GM_J);
   return cudaSuccess;
 }
 
-template <typename InT, typename OutT, int MT, int R>
-cudaError_t spec_t(int N, int K, int num_sms, LaunchSpec* out) {
-  auto k = k_gemv<InT, OutT, MT, R>;
+template <typename InT, typename OutT, int MT>
+cudaError_t spec_t(int N, int K, int num_sms, bool static_b, LaunchSpec* out, int* pf) {
+  // rows of a warp: one at a time; the rolling kernel for one activation row
+  // unless B is static
+  const bool roll = !static_b && MT == 1 && K % (8 * 32 * GR_V) == 0;
+  const void* k = roll ? (const void*)k_gemv_roll<InT, OutT> : (const void*)k_gemv<InT, OutT, MT, 1>;
   const size_t smem = (size_t)MT * (size_t)(K / 8) * 16;
-  cudaError_t e = allow_dynamic_smem((const void*)k, smem);
+  cudaError_t e = allow_dynamic_smem(k, smem);
   if (e != cudaSuccess) return e;
   int per_sm = 0;
   e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, GV_THREADS, smem);
   if (e != cudaSuccess) return e;
   if (per_sm < 1) return cudaErrorInvalidConfiguration;
-  const int rows_per_block = (GV_THREADS / 32) * R;
+  const int rows_per_block = GV_THREADS / 32;
   const int need = (N + rows_per_block - 1) / rows_per_block;
-  out->func = (const void*)k;
-  out->grid = dim3((unsigned)std::max(1, std::min(need, per_sm * num_sms)), 1, 1);
+  const int grid = std::max(1, std::min(need, per_sm * num_sms));
+  out->func = k;
+  out->grid = dim3((unsigned)grid, 1, 1);
   out->block = dim3(GV_THREADS, 1, 1);
   out->smem = smem;
   out->cluster = 1;
   out->kind = ARGS_GEMV;
+  const int warps = grid * rows_per_block;
+  const int rows_per_warp = (N + warps - 1) / warps;
+  *pf = roll ? prefetch_groups(rows_per_warp * (K / 8) / (32 * GR_V)) : 0;
   return cudaSuccess;
 }
 
 template <typename InT, typename OutT>
-cudaError_t spec_m(int M, int N, int K, int num_sms, LaunchSpec* out) {
+cudaError_t spec_m(int M, int N, int K, int num_sms, bool static_b, LaunchSpec* out, int* pf) {
   // one row per warp at a time for M <= 2: twice the CTAs of two rows per warp,
   // which spreads short weight streams more evenly over the SMs (4096 x 4096:
   // 3.99 -> 4.49 TB/s; 14336 x 4096: 5.70 -> 6.05 TB/s)
-  if (M <= 1) return spec_t<InT, OutT, 1, 1>(N, K, num_sms, out);
-  if (M <= 2) return spec_t<InT, OutT, 2, 1>(N, K, num_sms, out);
-  if (M <= 8) return spec_mma<InT, OutT>(N, out);
-  return spec_t<InT, OutT, 16, 1>(N, K, num_sms, out);
+  if (M <= 1) return spec_t<InT, OutT, 1>(N, K, num_sms, static_b, out, pf);
+  if (M <= 2) return spec_t<InT, OutT, 2>(N, K, num_sms, static_b, out, pf);
+  if (M <= 8) return spec_mma<InT, OutT>(N, K, static_b, out, pf);
+  return spec_t<InT, OutT, 16>(N, K, num_sms, static_b, out, pf);
 }
 
 }  // namespace
@@ -300,12 +491,14 @@ size_t gemv_smem_bytes(int M, int K) {
   return (size_t)mt * (size_t)(K / 8) * 16;
 }
 
-cudaError_t spec_gemv(int M, int N, int K, bool in_bf16, bool out_f32, int num_sms, LaunchSpec* out) {
+cudaError_t spec_gemv(int M, int N, int K, bool in_bf16, bool out_f32, int num_sms, bool static_b, LaunchSpec* out,
+                      int* pf_groups) {
   if (in_bf16) {
-    return out_f32 ? spec_m<__nv_bfloat16, float>(M, N, K, num_sms, out)
-                   : spec_m<__nv_bfloat16, __nv_bfloat16>(M, N, K, num_sms, out);
+    return out_f32 ? spec_m<__nv_bfloat16, float>(M, N, K, num_sms, static_b, out, pf_groups)
+                   : spec_m<__nv_bfloat16, __nv_bfloat16>(M, N, K, num_sms, static_b, out, pf_groups);
   }
-  return out_f32 ? spec_m<__half, float>(M, N, K, num_sms, out) : spec_m<__half, __nv_bfloat16>(M, N, K, num_sms, out);
+  return out_f32 ? spec_m<__half, float>(M, N, K, num_sms, static_b, out, pf_groups)
+                 : spec_m<__half, __nv_bfloat16>(M, N, K, num_sms, static_b, out, pf_groups);
 }
 
 }  // namespace dgb

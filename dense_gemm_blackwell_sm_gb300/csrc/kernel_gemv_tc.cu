@@ -18,6 +18,7 @@
 // No global scratch is used.
 #include <algorithm>
 
+#include "idesc.h"
 #include "kernel_common.cuh"
 #include "launch.h"
 
@@ -215,9 +216,8 @@ cudaError_t spec_gemv_tc(int M, int N, int K, bool in_bf16, bool out_f32, int nu
   p.N = N;
   p.K = K;
   gemv_tc_config(N, K, num_sms, want_split, want_stages, &p.split, &p.stages, &p.kblocks_per_cta);
-  const uint32_t ab = in_bf16 ? 1u : 0u;
   // instruction descriptor: f32 accumulate, fp16/bf16 operands, K-major, M = 128, N = 16
-  p.idesc = (1u << 4) | (ab << 7) | (ab << 10) | ((uint32_t)(16 >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+  p.idesc = idesc_f16(in_bf16, 128, 16);
   const size_t smem = tg_smem(p.stages);
   const void* k = out_f32 ? (const void*)k_gemv_tc<float> : (const void*)k_gemv_tc<__nv_bfloat16>;
   cudaError_t e = allow_dynamic_smem((const void*)k, smem);

@@ -90,9 +90,14 @@ struct GemvParams {
   void* Y;
   int32_t M, N, K;
   int32_t early_b;  // 1: B may be read before the previous kernel on the stream has completed
+  int32_t pf_rows;  // groups of each warp's weight stream prefetched into L2 before waiting for
+                    // the previous kernel (the rolling kernels, early_b == 0)
 };
 size_t gemv_smem_bytes(int M, int K);
-cudaError_t spec_gemv(int M, int N, int K, bool in_bf16, bool out_f32, int num_sms, LaunchSpec* out);
+// static_b: B is not written by the previous kernel on the stream (it may be
+// read before that kernel completes); *pf_groups receives GemvParams::pf_rows
+cudaError_t spec_gemv(int M, int N, int K, bool in_bf16, bool out_f32, int num_sms, bool static_b, LaunchSpec* out,
+                      int* pf_groups);
 
 // the same product on the Tensor Core (weight as the 128-row MMA operand),
 // K split over the CTAs of a cluster

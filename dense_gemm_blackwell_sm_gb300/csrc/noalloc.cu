@@ -15,16 +15,22 @@
 // directly, but host code must not: on the host its name is only a stand-in,
 // not a device address.  So the first call on each device, with that device
 // current, asks the runtime for the array's device address
-// (cudaGetSymbolAddress) and keeps it; make that first call before any stream
-// capture.
+// (cudaGetSymbolAddress) and keeps it.  The same first call also resolves the
+// six kernels this entry point can launch (three tiles, two output types) and
+// sets their shared-memory limits, so that any code loading the driver does
+// lazily happens then and never on a later call.  That first call may
+// therefore let the driver reserve memory for code: make it once per device
+// outside any no-allocation region (or run with CUDA_MODULE_LOADING=EAGER),
+// and before any stream capture.  A first call that fails is not remembered:
+// the next call tries the set-up again.
 #include <algorithm>
 #include <atomic>
-#include <functional>
 #include <mutex>
 
 #include <cudaTypedefs.h>
 
 #include "gemm.h"
+#include "idesc.h"
 #include "kernel_common.cuh"
 #include "launch.h"
 
@@ -34,15 +40,17 @@ constexpr size_t NOALLOC_SCRATCH_BYTES = 256;
 constexpr int kMaxDevices = 64;
 
 // status word, tile counter, finished-cluster counter (3 of the 64 words used)
+constexpr size_t NOALLOC_SCRATCH_USED = 3 * sizeof(uint32_t);
+static_assert(NOALLOC_SCRATCH_USED <= NOALLOC_SCRATCH_BYTES, "the scheduler's scratch must fit the fixed array");
 static __device__ __align__(256) uint32_t g_noalloc_scratch[NOALLOC_SCRATCH_BYTES / sizeof(uint32_t)];
 
 struct DeviceSetup {
-  std::once_flag once;
+  std::mutex mu;
+  std::atomic<bool> done{false};  // set only once the set-up has succeeded
   void* scratch = nullptr;  // device address of g_noalloc_scratch on this device
   int sms = 0;
   bool arch_ok = false;
-  cudaError_t err = cudaSuccess;
-  std::atomic<int> clusters[3][2];  // active clusters per (variant 7/8/9, out fp32?), 0 = unknown
+  int clusters[3][2] = {};  // active clusters per (variant 7/8/9, out fp32?)
 };
 
 DeviceSetup g_dev[kMaxDevices];
@@ -73,24 +81,35 @@ bool encode(CUtensorMap* m, CUtensorMapDataType dt, int esize, const void* ptr, 
            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// once per device, with that device current
-void setup_device(int dev, DeviceSetup& d) {
-  int major = 0, minor = 0;
-  d.err = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
-  if (d.err == cudaSuccess) d.err = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
-  if (d.err == cudaSuccess) d.err = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
-  if (d.err != cudaSuccess) return;
+// (variant 7 / 8 / 9) -> (CTAs per cluster, MMA consumers)
+constexpr int kCg[3] = {1, 2, 2};
+constexpr int kCons[3] = {1, 1, 2};
+
+// once per device, with that device current; on failure nothing is kept and
+// the next call tries again
+cudaError_t setup_device(int dev, DeviceSetup& d) {
+  int major = 0, minor = 0, sms = 0;
+  cudaError_t e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  d.sms = sms;
   d.arch_ok = (major == 10 && minor == 3);
-  if (!d.arch_ok) return;
+  if (!d.arch_ok) return cudaSuccess;
   void* ptr = nullptr;
-  d.err = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
-  if (d.err != cudaSuccess) {
-    cudaGetLastError();
-    return;
-  }
+  e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+  if (e != cudaSuccess) return e;
+  // resolve every kernel this entry point launches now (loading its code and
+  // setting its shared-memory limit), not on the first call that needs it
+  for (int vi = 0; vi < 3; ++vi)
+    for (int of = 0; of < 2; ++of) {
+      const int stages = dgb::ws_max_stages(kCg[vi], kCons[vi]);
+      int n = dgb::ws_max_active_clusters(kCg[vi], kCons[vi], /*atomic scheduler*/ 1, of != 0, stages);
+      if (n < 1) return cudaErrorInvalidConfiguration;
+      d.clusters[vi][of] = n;
+    }
   d.scratch = ptr;
-  for (auto& row : d.clusters)
-    for (auto& c : row) c.store(0);
+  return cudaSuccess;
 }
 
 }  // namespace
@@ -117,13 +136,17 @@ extern "C" GEMM_API gemm_status_t gemm_run_noalloc(int64_t M, int64_t N, int64_t
   }
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GEMM_ERR_CUDA;
   DeviceSetup& d = g_dev[dev];
-  std::call_once(d.once, setup_device, dev, std::ref(d));
-  if (d.err != cudaSuccess) return GEMM_ERR_CUDA;
+  if (!d.done.load(std::memory_order_acquire)) {
+    std::lock_guard<std::mutex> lock(d.mu);
+    if (!d.done.load(std::memory_order_relaxed)) {
+      if (setup_device(dev, d) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+      }
+      d.done.store(true, std::memory_order_release);
+    }
+  }
   if (!d.arch_ok) return GEMM_ERR_ARCH;
-
-  // the kernel needs three 32-bit words of scratch, whatever the shape
-  const size_t need = 3 * sizeof(uint32_t);
-  if (need > NOALLOC_SCRATCH_BYTES) return GEMM_ERR_UNSUPPORTED_SHAPE;
 
   // tile: the largest cluster tile that still gives every CTA pair a tile
   const int64_t tn = (N + 255) / 256;
@@ -138,12 +161,7 @@ extern "C" GEMM_API gemm_status_t gemm_run_noalloc(int64_t M, int64_t N, int64_t
   const WsShape sh = ws_shape(cg, cons);
   const int stages = ws_max_stages(cg, cons);
   const int vi = (cg == 1) ? 0 : (cons == 1 ? 1 : 2);
-  int active = d.clusters[vi][out_f32 ? 1 : 0].load();
-  if (active == 0) {
-    active = ws_max_active_clusters(cg, cons, /*atomic scheduler*/ 1, out_f32, stages);
-    if (active < 1) active = std::max(1, d.sms / cg);
-    d.clusters[vi][out_f32 ? 1 : 0].store(active);
-  }
+  const int active = d.clusters[vi][out_f32 ? 1 : 0];
 
   KParams k{};
   k.M = (int32_t)M;
@@ -161,8 +179,7 @@ extern "C" GEMM_API gemm_status_t gemm_run_noalloc(int64_t M, int64_t N, int64_t
   k.A = static_cast<const uint16_t*>(A);
   k.B = static_cast<const uint16_t*>(B);
   k.C = C;
-  const uint32_t ab = in_bf16 ? 1u : 0u;
-  k.idesc = (1u << 4) | (ab << 7) | (ab << 10) | ((uint32_t)(256 >> 3) << 17) | ((uint32_t)((128 * cg) >> 4) << 24);
+  k.idesc = idesc_f16(in_bf16, 128 * cg, 256);
 
   CUtensorMap tmA, tmB, tmC;
   const CUtensorMapDataType in_t = in_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
@@ -181,7 +198,7 @@ extern "C" GEMM_API gemm_status_t gemm_run_noalloc(int64_t M, int64_t N, int64_t
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   // the array keeps the previous call's contents: the status word and both
   // counters must start at zero
-  if (cudaMemsetAsync(d.scratch, 0, need, s) != cudaSuccess) {
+  if (cudaMemsetAsync(d.scratch, 0, NOALLOC_SCRATCH_USED, s) != cudaSuccess) {
     cudaGetLastError();
     return GEMM_ERR_CUDA;
   }

@@ -281,18 +281,24 @@ GEMM_API gemm_status_t gemm_run_host(int64_t M, int64_t N, int64_t K, const void
  *
  * It makes no plan and calls no cudaMalloc, cudaFree or other allocating
  * routine: it runs the warp-specialised kernel of variants 7-9 with the atomic
- * tile scheduler, whose scratch (a status word and two counters, 12 bytes)
- * lives in a fixed 256-byte device array inside the library that every GPU
- * loading the library keeps until the process exits; a shape whose scratch
- * would exceed the array is refused with GEMM_ERR_UNSUPPORTED_SHAPE.  The first
- * call on a device, with that device current, looks up the array's device
- * address; make that first call before any stream capture.  Every call shares
- * the array and clears it on `stream` before its kernel starts, so calls that
- * overlap on the GPU (different streams, or different threads) race and must
- * be serialised by the caller.  Needs N * sizeof(C element) % 16 == 0 besides
- * the usual preconditions, and 16-bit inputs (dtypes 0-3; the 8-bit ones
- * return GEMM_ERR_UNSUPPORTED_DTYPE).  Asynchronous on `stream`; a device-side wait that
- * times out leaves C undefined and is not reported by this entry point. */
+ * tile scheduler, whose scratch (a status word and two counters, 12 bytes,
+ * whatever the shape) lives in a fixed 256-byte device array inside the
+ * library that every GPU loading the library keeps until the process exits.
+ * The first call on a device, with that device current, looks up the array's
+ * device address and loads the six kernels this entry point can launch (three
+ * tiles, two output types) and sets their shared-memory limits, so any lazy
+ * code loading by the driver happens then and never in a later call.  That
+ * first call may therefore let the driver reserve memory for code: make it
+ * once per device outside any no-allocation region (or run the process with
+ * CUDA_MODULE_LOADING=EAGER), and before any stream capture.  If it fails
+ * (GEMM_ERR_CUDA), nothing is kept and the next call tries again.  Every call
+ * shares the array and clears it on `stream` before its kernel starts, so calls
+ * that overlap on the GPU (different streams, or different threads) race and
+ * must be serialised by the caller.  Needs N * sizeof(C element) % 16 == 0
+ * besides the usual preconditions, and 16-bit inputs (dtypes 0-3; the 8-bit
+ * ones return GEMM_ERR_UNSUPPORTED_DTYPE).  Asynchronous on `stream`; a
+ * device-side wait that times out leaves C undefined and is not reported by
+ * this entry point. */
 GEMM_API gemm_status_t gemm_run_noalloc(int64_t M, int64_t N, int64_t K, const void* A, const void* B,
                                         void* C, gemm_dtype_t dtype, gemm_stream_t stream);
 

@@ -67,7 +67,10 @@ SHAPES = {
     gemm.S9: [(300, 520, 200), (1100, 1288, 264)],
     # GEMV: the K-split kernel (M <= 2 and at most 64 rows per SM) and the row kernel
     gemm.GEMV: [(1, 1000, 520), (3, 264, 72), (8, 1000, 520), (16, 96, 1024), (1, 4096, 4096), (2, 152, 8),
-                (1, 1, 64), (1, 9000, 16384), (2, 777, 4104), (1, 500, 8), (2, 12000, 520)],
+                (1, 1, 64), (1, 9000, 16384), (2, 777, 4104), (1, 500, 8), (2, 12000, 520),
+                # one activation row, K a multiple of 1024: the rolling kernel, with a
+                # whole row per load group (K = 1024) and several rows per warp
+                (1, 1000, 1024), (1, 20000, 2048)],
     gemm.GEMV_TC: [(1, 1000, 520), (3, 264, 72), (8, 1000, 4104), (16, 96, 1024)],
 }
 CASES = [(v, s) for v, shapes in SHAPES.items() for s in shapes]
@@ -222,6 +225,42 @@ def test_static_b_flag_chains_dependent_gemvs(variant):
     assert parity.check(y2.float().cpu().numpy(), ref2, S2, "bf16")["ok"]
     p1.destroy()
     p2.destroy()
+
+
+@pytest.mark.parametrize("M", [1, 8])
+def test_default_gemv_reads_weights_the_previous_kernel_wrote(M):
+    """Without GEMM_FLAG_STATIC_B the GEMV may ask L2 to prefetch its weights
+    before the previous kernel on the stream has completed, but every value it
+    uses must be the one that kernel wrote: a GEMM writes W = P Q^T, and the
+    GEMV y = x W^T reads W at once.  P alternates between two integer matrices
+    (W is then exact in bf16 and known from the oracle), so a stale W would
+    give the other iteration's product."""
+    N2, K2, KP = 1024, 2048, 16
+    x, _ = inputs.make_operands(M, 8, K2, "bf16", ("uniform",), ("uniform",), seed=31)
+    p_a, q = inputs.integer_operands(N2, K2, KP, "bf16", seed=32)
+    p_b, _ = inputs.integer_operands(N2, K2, KP, "bf16", seed=33)
+    w_ref = [torch.from_numpy(oracle.gemm(pp, q)[0]).to(torch.bfloat16) for pp in (p_a, p_b)]  # |w| <= 64: exact
+    make_w = gemm.Plan(N2, K2, KP, gemm.BF16_BF16)
+    gemv = gemm.Plan(M, N2, K2, gemm.BF16_BF16, gemm.make_opts(variant=gemm.GEMV))
+    dx, dq = x.to(DEV), q.to(DEV)
+    dps = [p_a.to(DEV), p_b.to(DEV)]
+    ws = [torch.empty((N2, K2), device=DEV, dtype=torch.bfloat16) for _ in range(2)]
+    ys = [torch.empty((M, N2), device=DEV, dtype=torch.bfloat16) for _ in range(4)]
+    for i, y in enumerate(ys):
+        w = ws[i % 2]
+        w.fill_(float("nan"))
+        make_w.run(dps[i % 2], dq, w)
+        gemv.run(dx, w, y)
+    torch.cuda.synchronize()
+    assert make_w.check() == gemm.OK and gemv.check() == gemm.OK
+    for k in range(2):
+        assert torch.equal(ws[k].cpu(), w_ref[k])
+    for i, y in enumerate(ys):
+        ref, S = oracle.gemm(x, w_ref[i % 2])
+        r = parity.check(y.float().cpu().numpy(), ref, S, "bf16")
+        assert r["ok"], (i, r)
+    make_w.destroy()
+    gemv.destroy()
 
 
 @pytest.mark.parametrize("split", [1, 2, 4, 8])

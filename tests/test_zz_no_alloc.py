@@ -6,8 +6,11 @@ Its results must agree with gemm_run's -- within the per-element tolerance of
 the parity tests, S = sum_k |a_ik b_jk| coming from the CPU oracle -- on calls
 made one right after the other, which share the library's fixed scratch array
 (so each call must clear what the previous one left there).  The shapes take
-the 128x256, 256x256 and 512x256 tile paths.  This file is collected last, and
-passes both alone in a fresh process and after the other tests.
+the 128x256, 256x256 and 512x256 tile paths.  The first test makes the entry
+point's first call on the device before any gemm_run, and checks that a later
+call changes neither torch's allocated bytes nor the device's free memory.
+This file is collected last, and passes both alone in a fresh process and
+after the other tests.
 """
 from __future__ import annotations
 
@@ -40,6 +43,38 @@ def noalloc():
                   ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p]
     f.restype = ctypes.c_int
     return f
+
+
+def test_first_call_sets_up_and_later_calls_allocate_nothing(noalloc):
+    """The first call on a device resolves the scratch array and loads every
+    kernel the entry point can launch (it may let the driver reserve memory for
+    code); every later call -- including the first with another output type and
+    tile -- must leave device memory exactly as it was."""
+    stream = torch.cuda.current_stream().cuda_stream
+    M, N, K = 700, 1288, 264
+    a, b = inputs.make_operands(M, N, K, "bf16", ("uniform",), ("normal", 1.0), seed=7)
+    da, db = a.to(DEV), b.to(DEV)
+    c16 = torch.full((M, N), float("nan"), device=DEV, dtype=torch.bfloat16)
+    c32 = torch.full((M, N), float("nan"), device=DEV, dtype=torch.float32)
+    # a shape for the 512 x 256 tile: outputs allocated before anything is measured
+    M2, N2, K2 = 4096, 4096, 128
+    a2, b2 = inputs.make_operands(M2, N2, K2, "bf16", ("uniform",), ("normal", 1.0), seed=8)
+    da2, db2 = a2.to(DEV), b2.to(DEV)
+    c2 = torch.full((M2, N2), float("nan"), device=DEV, dtype=torch.float32)
+    assert noalloc(M, N, K, da.data_ptr(), db.data_ptr(), c16.data_ptr(), gemm.BF16_BF16, stream) == gemm.OK
+    torch.cuda.synchronize()
+    before = (torch.cuda.memory_allocated(), torch.cuda.mem_get_info()[0])
+    assert noalloc(M, N, K, da.data_ptr(), db.data_ptr(), c32.data_ptr(), gemm.BF16_F32, stream) == gemm.OK
+    assert noalloc(M2, N2, K2, da2.data_ptr(), db2.data_ptr(), c2.data_ptr(), gemm.BF16_F32, stream) == gemm.OK
+    assert noalloc(M, N, K, da.data_ptr(), db.data_ptr(), c16.data_ptr(), gemm.BF16_BF16, stream) == gemm.OK
+    torch.cuda.synchronize()
+    after = (torch.cuda.memory_allocated(), torch.cuda.mem_get_info()[0])
+    assert after == before
+    ref, S = oracle.gemm(a, b)
+    assert parity.check(c16.double().cpu().numpy(), ref, S, "bf16")["ok"]
+    assert parity.check(c32.double().cpu().numpy(), ref, S, "f32")["ok"]
+    ref2, S2 = oracle.gemm(a2, b2)
+    assert parity.check(c2.double().cpu().numpy(), ref2, S2, "f32")["ok"]
 
 
 def test_noalloc_agrees_with_gemm_run_on_consecutive_calls(noalloc):
