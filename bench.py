@@ -92,10 +92,14 @@ def aggregate(per_rank_seconds: list[float], units_per_rank: float) -> tuple[flo
 
 
 class ClockSampler:
-    """nvidia-smi clocks / throttle reasons sampled while the timed region runs."""
-    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    """nvidia-smi clocks / power / throttle reasons sampled every 50 ms while
+    work runs.  Each sample carries nvidia-smi's own timestamp, so a summary
+    can be restricted to the host-time window of one timed region."""
+    QUERY = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,enforced.power.limit,"
+             "clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+             "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+             "clocks_event_reasons.sw_power_cap")
+    REASONS = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
 
     def __init__(self, index: int):
         self.index = index
@@ -133,26 +137,46 @@ class ClockSampler:
                 self.proc.kill()
         return False
 
-    def summary(self) -> dict:
-        mhz, maxs, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+    @staticmethod
+    def parse(lines: list[str]) -> list[dict]:
+        out = []
+        for ln in lines:
             f = [x.strip() for x in ln.split(",")]
-            if len(f) < 9:
+            if len(f) < 11:
                 continue
             try:
-                mhz.append(float(f[1]))
-                maxs.append(float(f[2]))
+                t = time.mktime(time.strptime(f[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                if "." in f[0]:
+                    t += float("0." + f[0].split(".")[1])
+                smp = {"t": t, "mhz": float(f[2]), "max_mhz": float(f[3])}
             except ValueError:
                 continue
-            for n, v in zip(names, f[5:9]):
-                if v.lower().startswith("active"):
-                    reasons.add(n)
-        if not mhz:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        mhz.sort()
-        return {"sm_mhz": mhz[len(mhz) // 2], "sm_max_mhz": max(maxs), "reasons": sorted(reasons),
-                "samples": len(mhz)}
+            try:
+                smp["w"] = float(f[4])
+                smp["limit_w"] = float(f[5])
+            except ValueError:
+                smp["w"], smp["limit_w"] = None, None
+            smp["reasons"] = [n for n, v in zip(ClockSampler.REASONS, f[7:11]) if v.lower().startswith("active")]
+            out.append(smp)
+        return out
+
+    def summary(self, t0: float | None = None, t1: float | None = None) -> dict:
+        """Median SM clock (all samples and those under load), power and throttle
+        reasons, over the samples within [t0, t1] (host time.time()) if given.
+        A sample is under load when it draws more than 40 % of the power limit."""
+        smp = self.parse(self.lines)
+        if t0 is not None:
+            smp = [x for x in smp if t0 - 0.05 <= x["t"] <= t1 + 0.05]
+        if not smp:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "samples_under_load": 0}
+        mhz = sorted(x["mhz"] for x in smp)
+        load = sorted(x["mhz"] for x in smp if x["w"] is not None and x["limit_w"] and x["w"] > 0.4 * x["limit_w"])
+        reasons = sorted({r for x in smp for r in x["reasons"]})
+        pw = [x["w"] for x in smp if x["w"] is not None]
+        return {"sm_mhz": mhz[len(mhz) // 2], "sm_max_mhz": max(x["max_mhz"] for x in smp), "reasons": reasons,
+                "samples": len(smp), "samples_under_load": len(load),
+                "sm_mhz_under_load": load[len(load) // 2] if load else None,
+                "power_w_max": max(pw) if pw else None, "power_limit_w": smp[-1]["limit_w"]}
 
 
 # ---------------------------------------------------------------------------
@@ -221,7 +245,9 @@ def bench_gemm(w: inputs.Workload, steps: int, warmup: int, dev, dist_barrier, v
     dist_barrier()
     torch.cuda.synchronize(dev)
     with ClockSampler(dev.index if dev.index is not None else 0) as clk:
+        h0 = time.time()
         secs = _events_time(step, steps, stream)
+        h1 = time.time()
     torch.cuda.synchronize(dev)
     dist_barrier()
     st = plan.check()
@@ -230,7 +256,13 @@ def bench_gemm(w: inputs.Workload, steps: int, warmup: int, dev, dist_barrier, v
     info = plan.info()
     plan.destroy()
     del sets
-    return {"seconds": secs, "per_launch_s": secs / steps, "clocks": clk.summary(), "info": info,
+    clocks = clk.summary(h0, h1)
+    clocks["scope"] = "timed region"
+    if clocks["samples"] == 0:
+        # the region is shorter than one 50 ms sample: report the sampler's whole run
+        clocks = clk.summary()
+        clocks["scope"] = "sampler run around a timed region shorter than one sample"
+    return {"seconds": secs, "per_launch_s": secs / steps, "clocks": clocks, "info": info,
             "operand_sets": nsets}
 
 
@@ -262,7 +294,38 @@ def bench_gemm_e2e(w: inputs.Workload, steps: int, dev) -> dict:
     for _ in range(steps):
         once()   # synchronises the stream itself
     secs = time.perf_counter() - t0
-    return {"seconds": secs, "steps": steps, "h2d": ib * (w.M * w.K + w.N * w.K), "d2h": ob * w.M * w.N}
+    return {"seconds": secs, "steps": steps, "h2d": ib * (w.M * w.K + w.N * w.K), "d2h": ob * w.M * w.N,
+            "copy_only": copy_ceiling(dev, [(ah, da), (bh, db)], [(ch, dc)])}
+
+
+def copy_ceiling(dev, h2d: list, d2h: list, reps: int = 5) -> dict:
+    """The host-link floor of one end-to-end step: the same bytes copied in
+    (pinned host -> device) and out (device -> pinned host) on two streams at
+    once, with no GEMM; best of `reps`.  Also each direction alone."""
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+
+    def run(do_in, do_out):
+        best = None
+        for _ in range(reps):
+            torch.cuda.synchronize(dev)
+            t0 = time.perf_counter()
+            if do_in:
+                with torch.cuda.stream(s_in):
+                    for h, d in h2d:
+                        d.copy_(h, non_blocking=True)
+            if do_out:
+                with torch.cuda.stream(s_out):
+                    for h, d in d2h:
+                        h.copy_(d, non_blocking=True)
+            torch.cuda.synchronize(dev)
+            t = time.perf_counter() - t0
+            best = t if best is None else min(best, t)
+        return best
+    bi = sum(h.numel() * h.element_size() for h, _ in h2d)
+    bo = sum(h.numel() * h.element_size() for h, _ in d2h)
+    t_in, t_out, t_both = run(True, False), run(False, True), run(True, True)
+    return {"ms_both": round(t_both * 1e3, 3), "ms_in": round(t_in * 1e3, 3), "ms_out": round(t_out * 1e3, 3),
+            "gbs_in": round(bi / t_in / 1e9, 1), "gbs_out": round(bo / t_out / 1e9, 1)}
 
 
 def _bench_mx_e2e(w, a, b, code, steps, dev, ib, ob) -> dict:
@@ -332,6 +395,73 @@ def bench_gemv(w: inputs.Workload, steps: int, warmup: int, dev, flags: int = 0,
 # ---------------------------------------------------------------------------
 # CPU oracle timing (a reported baseline, not the target)
 
+def host_cpu() -> dict:
+    """The host CPU: model name (lscpu, else /proc/cpuinfo), the cores this
+    process may run on (affinity) and the logical CPU count."""
+    import platform
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.lower().startswith("model name:"):
+                model = ln.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    if model is None:
+        try:
+            with open("/proc/cpuinfo") as f:
+                for ln in f:
+                    if ln.lower().startswith("model name"):
+                        model = ln.split(":", 1)[1].strip()
+                        break
+        except OSError:
+            pass
+    try:
+        aff = len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        aff = os.cpu_count() or 0
+    return {"model": model or platform.processor() or "unknown", "machine": platform.machine(),
+            "affinity_cores": aff, "logical_cpus": os.cpu_count() or 0}
+
+
+def oracle_steps(w: inputs.Workload, steps: int, warmup: int, step_s: float) -> dict:
+    """The CPU oracle as a sequence of steps, each a bounded sample of the
+    workload: the same number of seeded random rows of C (all N columns) per
+    step, chosen from the first warm-up step so that one step takes about
+    `step_s` seconds on all host threads.  Returns the timed steps' totals."""
+    import numpy as np
+    import oracle
+    oracle.build()
+    a, b = inputs.workload_operands(w)
+    mx = w.in_dtype in (inputs.MXE4M3, inputs.MXE5M2)
+    if mx:
+        sfa, sfb = inputs.workload_mx_scales(w)
+    threads = oracle.max_threads()
+    rng = np.random.default_rng(0)
+
+    def step(nrows):
+        rows = rng.choice(w.M, size=min(nrows, w.M), replace=False)
+        t0 = time.perf_counter()
+        if mx:
+            oracle.gemm_mx(a, b, sfa, sfb, rows=rows, nthreads=threads)
+        else:
+            oracle.gemm_rows(a, b, rows, nthreads=threads)
+        return time.perf_counter() - t0, len(rows)
+
+    t_cal, n_cal = step(threads)   # first warm-up step: one row per thread
+    rows = max(1, min(w.M, int(n_cal * step_s / max(t_cal, 1e-6))))
+    for _ in range(max(0, warmup - 1)):
+        step(rows)
+    t_tot, r_tot = 0.0, 0
+    for _ in range(steps):
+        t, n = step(rows)
+        t_tot += t
+        r_tot += n
+    return {"tflops": 2.0 * r_tot * w.N * w.K / t_tot / 1e12, "seconds": t_tot, "rows_per_step": rows,
+            "threads": threads}
+
+
 def cpu_oracle_rate(w: inputs.Workload, budget_s: float = 12.0) -> dict:
     import numpy as np
     import oracle
@@ -366,10 +496,9 @@ def cpu_oracle_rate(w: inputs.Workload, budget_s: float = 12.0) -> dict:
             oracle.gemm_rows(a, b, r1, nthreads=1)
         t1 += time.perf_counter() - t0
         rows1 += 1
-    import platform
     return {"tflops": flops / t_spent / 1e12, "rows": rows_done, "seconds": t_spent, "threads": threads,
             "single_thread_tflops": 2.0 * rows1 * w.N * w.K / t1 / 1e12, "single_thread_rows": rows1,
-            "host": "%s, %d logical CPUs" % (platform.machine(), os.cpu_count() or 0),
+            "host": host_cpu(),
             "sample": "%d of %d rows of C (all %d columns, K=%d), seeded random rows, fp64 oracle on %d host "
                       "threads; rate extrapolates linearly to the full %dx%dx%d product" % (
                           rows_done, w.M, w.N, w.K, threads, w.M, w.N, w.K)}
@@ -437,18 +566,21 @@ def main(argv=None):
     if args.impl == "reference":
         if rank != 0:
             return 0
-        per_step = max(1.0, 60.0 / max(1, args.steps + args.warmup))
-        r = cpu_oracle_rate(w, budget_s=min(12.0, per_step * args.steps))
+        # every step is the same bounded row sample; all steps together take about a minute
+        step_s = min(3.0, 60.0 / max(1, args.steps + args.warmup))
+        r = oracle_steps(w, args.steps, args.warmup, step_s)
+        host = host_cpu()
+        sample = ("each step: %d seeded random rows of C (all %d columns, K=%d) of the %dx%dx%d product, "
+                  "fp64 oracle on %d host threads" % (r["rows_per_step"], w.N, w.K, w.M, w.N, w.K, r["threads"]))
         line = {"impl": "reference", "metric": METRIC, "value": round(r["tflops"], 6), "unit": "TFLOP/s",
                 "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-                # one whole step (the full product) at the sampled rate, extrapolated
-                "ms_per_step": round(w.flops / (r["tflops"] * 1e12) * 1e3, 1),
+                "ms_per_step": round(r["seconds"] / args.steps * 1e3, 3),
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                 "dtype": "f64", "data": "synthetic",
-                "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "in": w.in_dtype, "out": w.out_dtype},
+                "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "in": w.in_dtype, "out": w.out_dtype,
+                           "rows_per_step": r["rows_per_step"]},
                 "cpu_baseline": {"value": round(r["tflops"], 6), "unit": "TFLOP/s", "cores": r["threads"],
-                                 "single_thread": round(r["single_thread_tflops"], 6), "host": r["host"],
-                                 "kind": "oracle", "sample": r["sample"]},
+                                 "host": host, "kind": "oracle", "sample": sample},
                 "e2e": {"value": round(r["tflops"], 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}}
         print(json.dumps(line))
@@ -515,9 +647,30 @@ def main(argv=None):
     if rank == 0 and not args.no_e2e:
         e = bench_gemm_e2e(w, max(3, min(10, args.steps // 20)), dev)
         line["e2e"] = {"value": round(w.flops * e["steps"] / e["seconds"] / 1e12, 3), "unit": "TFLOP/s",
-                       "h2d_bytes_per_step": e["h2d"], "d2h_bytes_per_step": e["d2h"]}
+                       "h2d_bytes_per_step": e["h2d"], "d2h_bytes_per_step": e["d2h"],
+                       "ms_per_step": round(e["seconds"] / e["steps"] * 1e3, 3)}
+        if e.get("copy_only"):
+            c = e["copy_only"]
+            # the step can finish no sooner than its copies alone (both directions at once)
+            line["e2e"]["copy_only_ceiling"] = dict(c, tflops=round(w.flops / (c["ms_both"] * 1e-3) / 1e12, 3),
+                                                    frac=round(c["ms_both"] / line["e2e"]["ms_per_step"], 4))
     if rank == 0 and not args.no_extra:
         also = {}
+        # the same step back to back for at least 3 s, against the sustained peak,
+        # with the clocks and power seen under load
+        n_sus = max(args.steps, int(3.2 / max(per_launch, 1e-6)))
+        rs = bench_gemm(w, n_sus, 10, dev, lambda: None, args.variant, epilogue_act=epi_act)
+        ts = w.flops / rs["per_launch_s"] / 1e12
+        sus_peak = float(peaks.get("bf16_tflops_sustained", FALLBACK["bf16_tflops_sustained"]))
+        if w.in_dtype in inputs.EIGHT_BIT:
+            sus_peak *= 2.0
+        ck = rs["clocks"]
+        also["sustained_" + w.name] = {
+            "tflops": round(ts, 3), "launches": n_sus, "seconds": round(rs["seconds"], 3),
+            "peak": sus_peak, "peak_source": "bf16_tflops_sustained %s" % peak_src, "frac": round(ts / sus_peak, 4),
+            "clocks": ck,
+            # time x clock: launch time normalised to the median SM clock under load
+            "us_x_ghz": round(rs["per_launch_s"] * 1e6 * (ck.get("sm_mhz_under_load") or ck.get("sm_mhz") or 0) / 1e3, 1)}
         w3 = inputs.WORKLOADS["square_4096_f16_f32"]
         r3 = bench_gemm(w3, 200, 10, dev, lambda: None)
         also[w3.name] = {"tflops": round(w3.flops / r3["per_launch_s"] / 1e12, 3),
@@ -561,10 +714,13 @@ def main(argv=None):
             also[name] = {"gbs": round(g["gbs"], 1), "frac_of_measured_hbm": round(g["gbs"] / hbm, 4),
                           "frac_of_stated_8000": round(g["gbs"] / STATED_HBM_GBS, 4),
                           "us_per_launch": round(g["us_per_launch"], 2), "variant": g["variant"],
+                          "roofline": {"bound": "hbm", "achieved": round(g["gbs"], 1), "peak": hbm, "unit": "GB/s",
+                                       "frac": round(g["gbs"] / hbm, 4), "traffic": stored_traffic("gemv", name),
+                                       "peak_source": "hbm_gbs %s" % peak_src,
+                                       "bytes_per_launch": g["bytes_per_launch"]},
                           "static_b_pdl": {"gbs": round(gp["gbs"], 1), "frac_of_measured_hbm": round(gp["gbs"] / hbm, 4),
                                            "us_per_launch": round(gp["us_per_launch"], 2)},
-                          "weight_copies": g["copies"], "timing": "CUDA graph of 200 launches, replayed 3x",
-                          "traffic": stored_traffic("gemv", name)}
+                          "weight_copies": g["copies"], "timing": "CUDA graph of 200 dependent launches, replayed 3x"}
         line["also"] = also
     if rank == 0 and not args.no_cpu_baseline:
         r = cpu_oracle_rate(w)

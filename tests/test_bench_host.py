@@ -8,6 +8,7 @@ import os
 import socket
 import subprocess
 import sys
+import time
 
 import pytest
 import torch
@@ -87,3 +88,45 @@ def test_reference_arm_prints_one_line_under_torchrun():
     assert d["cpu_baseline"]["kind"] == "oracle" and d["e2e"]["h2d_bytes_per_step"] == 0
     assert d["ms_per_step"] > 0 and d["higher_is_better"] is True and d["config"]["workload"] == \
         "single_tile_128x128x64_f16_f32"
+
+
+def test_reference_arm_steps_fit_the_run():
+    """--impl reference reports the steps it ran: steps x ms_per_step is the
+    time of its timed steps, inside the wall time of the whole run."""
+    if torch.cuda.is_available():
+        pytest.skip("the CPU path is exercised on hosts without a GPU")
+    cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "4", "--warmup", "3",
+           "--workload", "kloop_1024x1024x4096_bf16_bf16"]
+    t0 = time.time()
+    r = subprocess.run(cmd, capture_output=True, text=True, timeout=300, cwd=ROOT)
+    wall = time.time() - t0
+    assert r.returncode == 0, r.stderr[-2000:]
+    d = json.loads([ln for ln in r.stdout.splitlines() if ln.startswith("{")][-1])
+    assert d["steps"] == 4
+    timed = d["steps"] * d["ms_per_step"] / 1e3
+    assert 0 < timed < wall
+    rows = d["config"]["rows_per_step"]
+    assert 1 <= rows <= 1024
+    # the value is the rate of the sampled work
+    assert d["value"] == pytest.approx(2.0 * rows * 1024 * 4096 * d["steps"] / timed / 1e12, rel=1e-3)
+    host = d["cpu_baseline"]["host"]
+    assert host["affinity_cores"] >= 1 and host["model"]
+
+
+def test_clock_sampler_windows_and_load():
+    """Samples are matched to a timed window by nvidia-smi's timestamp, and a
+    sample counts as under load above 40 % of the power limit."""
+    lines = ["2026/12/03 05:00:00.000, 0, 1000, 2070, 300.0, 1400.0, 0x0, Not Active, Not Active, Not Active, Not Active",
+             "2026/12/03 05:00:00.050, 0, 1900, 2070, 1300.0, 1400.0, 0x4, Not Active, Not Active, Not Active, Active",
+             "2026/12/03 05:00:00.100, 0, 1800, 2070, 1350.0, 1400.0, 0x4, Not Active, Not Active, Not Active, Active",
+             "2026/12/03 05:00:02.000, 0, 900, 2070, 250.0, 1400.0, 0x0, Not Active, Not Active, Not Active, Not Active"]
+    c = bench.ClockSampler(0)
+    c.lines = lines
+    smp = c.parse(lines)
+    t = smp[0]["t"]
+    assert smp[1]["t"] - t == pytest.approx(0.05, abs=1e-6)
+    s = c.summary(t + 0.1, t + 0.11)   # the window is widened by half a sample period on each side
+    assert s["samples"] == 2 and s["samples_under_load"] == 2 and s["sm_mhz_under_load"] in (1800.0, 1900.0)
+    assert s["reasons"] == ["sw_power_cap"] and s["power_w_max"] == 1350.0
+    a = c.summary()
+    assert a["samples"] == 4 and a["samples_under_load"] == 2 and a["sm_max_mhz"] == 2070.0
