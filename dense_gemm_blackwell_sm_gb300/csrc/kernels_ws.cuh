@@ -119,6 +119,17 @@ __device__ __forceinline__ void grid_launch_dependents() {
 }
 __device__ __forceinline__ void grid_wait_prior() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
+// The K blocks of a cluster's i-th tile run backwards when i is odd.  A wave of
+// tiles streams its A and B panels through L2 from the first K block to the
+// last; the next wave, started at the last K block, first asks for the blocks
+// the previous wave loaded most recently, which are the ones still in L2.  The
+// order of the K blocks changes only the fp32 summation order.  Stream-K and
+// split-K segments keep the forward order.
+template <bool PARTIAL_K>
+__device__ __forceinline__ bool k_reversed(uint32_t i) {
+  return !PARTIAL_K && (i & 1u) != 0u;
+}
+
 // v[j] += the lane's 32 values of one partial chunk, for fp32 values held as bit patterns
 __device__ __forceinline__ void sk_add32(uint32_t (&v)[32], const float* chunk, uint32_t lane) {
   const float4* s4 = reinterpret_cast<const float4*>(chunk) + lane;
@@ -373,7 +384,9 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
         raster_tile(tile, p.tiles_m, p.tiles_n, p.raster_group, tm, tn);
         const int32_t m_cta = tm * Cfg::TILE_M + (int32_t)rank * 128;
         const int32_t n_cta = tn * BN + (CG == 2 ? (int32_t)rank * (BN / 2) : 0);
-        for (int32_t kb = kb0; kb < kb1; ++kb) {
+        const bool rev = k_reversed<SK || KS>(i);
+        for (int32_t it = 0; it < kb1 - kb0; ++it) {
+          const int32_t kb = rev ? kb1 - 1 - it : kb0 + it;
           if (!mbar_wait(smem_u32(empty + stage), sphase ^ 1u, w, WAIT_PRODUCER_EMPTY)) { ok = false; break; }
           const uint32_t fb = smem_u32(full + stage);
           // MX: one block of A scales and one box holding the two blocks of B scales
@@ -467,8 +480,10 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
         tc_fence_after();
         const uint32_t d = tmem + slot * 256u;
         bool ok = true;
-        for (int32_t kb = kb0; kb < kb1; ++kb) {
-          const uint32_t acc0 = (kb != kb0) ? 1u : 0u;  // the segment's first MMA overwrites D
+        const bool rev = k_reversed<SK || KS>(i);
+        for (int32_t it = 0; it < kb1 - kb0; ++it) {
+          const int32_t kb = rev ? kb1 - 1 - it : kb0 + it;
+          const uint32_t acc0 = (it != 0) ? 1u : 0u;  // the segment's first MMA overwrites D
           // MX pair: this stage's scales are in TMEM; the copy warp saw the stage land
           // before copying, so this one wait covers the operands too
           const uint32_t ready = MX_COPIER ? smem_u32(sf_ready + stage) : smem_u32(full + stage);

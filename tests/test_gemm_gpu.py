@@ -90,6 +90,23 @@ def test_integer_inputs_bit_exact(variant, shape, ti, to):
         bad[0], c[tuple(bad[0])], exp[tuple(bad[0])])
 
 
+@pytest.mark.parametrize("variant,shape", [(gemm.S7, (2048, 8192, 264)), (gemm.S8, (2048, 8192, 264)),
+                                           (gemm.S9, (4096, 8192, 264))], ids=["s7", "s8", "s9"])
+@pytest.mark.parametrize("sched", [gemm.SCHED_STATIC, gemm.SCHED_ATOMIC])
+def test_several_tiles_per_cluster_bit_exact(variant, shape, sched):
+    """Every cluster takes three or more tiles, so its odd-numbered tiles run
+    their K blocks backwards (starting with the ragged last block): the result
+    must still be exact."""
+    M, N, K = shape
+    a, b = inputs.integer_operands(M, N, K, "bf16", seed=41)
+    ref, _ = oracle.gemm(a, b)
+    info = []
+    c = run_variant(a, b, "f32", variant, sched=sched, plan_out=info)
+    assert info[0]["tiles"] >= 3 * (info[0]["grid"] // info[0]["cluster"])
+    bad = np.argwhere(c != expect_bits(ref, "f32"))
+    assert bad.size == 0, bad[:3]
+
+
 @pytest.mark.parametrize("variant,shape", CASES, ids=IDS)
 @pytest.mark.parametrize("ti,to", [("f16", "f32"), ("bf16", "bf16")])
 def test_random_inputs_parity(variant, shape, ti, to):
