@@ -363,7 +363,7 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
   } else if (warp == 0) {
     // -------------------------------------------------------------- producer
     if (lane == 0) {
-      uint32_t stage = 0, sphase = 0;
+      uint32_t stage = 0, sphase = 0, issued = 0;
       bool skip = (p.debug_flags & DEBUG_SKIP_ONE_LOAD) != 0u;
       bool ok = true;
       int64_t sk_it = sk_b;
@@ -447,13 +447,32 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
               tma_load_4d_pair(smem_u32(sd + MX_BLOCK), tmSB, mapa_shared(fb, 0), 0, 0, kb, n_tile / 128);
             }
           }
+          ++issued;
           if (++stage == (uint32_t)S) { stage = 0; sphase ^= 1u; }
         }
       }
       if (!ok) {
-        // give copies still in flight time to land before SMEM is released
-        const uint64_t t0 = globaltimer_ns();
-        while (globaltimer_ns() - t0 < 2000000ull) {}
+        // Copies may still be in flight into this CTA's ring: they must land before
+        // its shared memory is released.  Each issued stage's full barrier (in this
+        // CTA, or in the leader of a pair) completes when its bytes have arrived, so
+        // where this thread can see the barrier it waits for the last min(S, issued)
+        // stages, each wait bounded (a stage whose load was never issued, as in the
+        // missing-load test, gives up after the bound).  The other CTA of a pair
+        // cannot wait on the leader's barriers; it waits the same bound in wall time,
+        // far longer than a ring of at most 8 x 48 KB takes to land at the slowest
+        // per-SM copy rate seen (about 40 GB/s: 10 us).
+        volatile uint32_t never = 0u;  // a timeout here sets this flag only
+        const WaitCtl wd{&never, nullptr, 2000000ull, 0};
+        if (CG == 1 || leader) {
+          const uint32_t n = issued < (uint32_t)S ? issued : (uint32_t)S;
+          for (uint32_t back = 1; back <= n; ++back) {
+            const uint32_t sb = (stage + (uint32_t)S - back) % (uint32_t)S;
+            mbar_wait(smem_u32(full + sb), back <= stage ? sphase : sphase ^ 1u, wd, 0u);
+          }
+        } else {
+          const uint64_t t0 = globaltimer_ns();
+          while (globaltimer_ns() - t0 < wd.timeout_ns) {}
+        }
       }
     }
   } else if ((warp == 1 || (NCONS == 2 && warp == 3)) && leader) {
