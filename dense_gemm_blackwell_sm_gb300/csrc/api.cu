@@ -99,13 +99,14 @@ bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, int esize, const void* pt
 }
 
 // MX scales of B seen as a 4-D byte tensor [row blocks][K blocks][4 rows][128 B]
-// of 512-byte blocks; one box of 128 x 4 x 1 x 2 brings the blocks of two
-// consecutive 128-row groups for one K block (rows past the array read as 0).
-bool encode_mx_pairs(CUtensorMap* m, const void* ptr, uint64_t k_blocks, uint64_t row_blocks) {
+// of 512-byte blocks; one box of 128 x 4 x 1 x `box_blocks` brings the blocks of
+// that many consecutive 128-row groups for one K block (rows past the array read
+// as 0).
+bool encode_mx_pairs(CUtensorMap* m, const void* ptr, uint64_t k_blocks, uint64_t row_blocks, uint32_t box_blocks) {
   if (!encode_fn_ready()) return false;
   cuuint64_t dims[4] = {128, 4, k_blocks, row_blocks};
   cuuint64_t strides[3] = {128, 512, 512 * k_blocks};
-  cuuint32_t box[4] = {128, 4, 1, 2};
+  cuuint32_t box[4] = {128, 4, 1, box_blocks};
   cuuint32_t estr[4] = {1, 1, 1, 1};
   CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(ptr), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
@@ -222,8 +223,7 @@ bool is_ws(int v) { return v >= GEMM_VARIANT_S7_WARP_SPECIALIZED && v <= GEMM_VA
 
 // The automatic variant for a dtype and operand layout: auto_variant, then the
 // restrictions of the inputs.  Block-scaled inputs run on step 7 or 8 (the one
-// whose tiles finish soonest, with the block-scaled kernels' rates: 8192^3 step 8
-// 3140, step 7 2678 TFLOP/s); 8-bit inputs and MN-major operands have no GEMV or
+// whose tiles finish soonest, with the block-scaled kernels' rates); 8-bit inputs and MN-major operands have no GEMV or
 // ladder kernel, so a shape that would take one takes step 7 or 8 instead; an
 // explicit K split (split_k >= 2) runs on step 7.
 int choose_variant(int64_t M, int64_t N, int64_t K, gemm_dtype_t dt, int sms, int32_t layout, int32_t split_k) {
@@ -237,7 +237,9 @@ int choose_variant(int64_t M, int64_t N, int64_t K, gemm_dtype_t dt, int sms, in
                : GEMM_VARIANT_S7_WARP_SPECIALIZED;
   };
   if (is_mx(dt)) {
-    v = step8_or_7(1.0, 0.76);  // block-scaled rates: 8192^3 3140 / 2678, 1024 x 4096 x 4096 1735 / 1686
+    // block-scaled rates: 8192^3 3140 / 2678, 1024 x 4096 x 4096 1735 / 1686; step 9
+    // (bf16 C only, 512 x 224 tiles) runs at 1935 on 8192^3 and is taken only on request
+    v = step8_or_7(1.0, 0.76);
   } else if ((is_f8(dt) || layout != 0) && !is_ws(v)) {
     v = step8_or_7(kRate8, kRate7);
   }
@@ -276,7 +278,7 @@ gemm_status_t prepare_launch(gemm_plan_s* p) {
     k.mma_kind = 0;
     k.bk = 64;
     if (p->in_mx) {
-      k.idesc = idesc_mx(p->in_e5m2, 128 * p->cg, 256);
+      k.idesc = idesc_mx(p->in_e5m2, 128 * p->cg, p->tile_n);
       k.mma_kind = 2;
       k.bk = 128;
     } else if (p->in_f8) {
@@ -294,7 +296,7 @@ gemm_status_t prepare_launch(gemm_plan_s* p) {
     } else if (v == GEMM_VARIANT_S6_PERSISTENT) {
       e = spec_step6(p->sched - 1, p->stages, p->out_f32, p->grid_units, &p->spec);
     } else if (p->in_mx) {
-      e = spec_mx(p->cg, p->sched - 1, p->out_f32, p->stages, p->grid_units, &p->spec);
+      e = spec_mx(p->cg, p->sched - 1, p->out_f32, p->stages, p->grid_units, &p->spec, -1, p->consumers);
     } else if (p->ks_split >= 2) {
       e = spec_ws_ks(p->out_f32, p->stages, p->tiles_m * p->tiles_n, p->ks_split, &p->spec);
     } else {
@@ -329,8 +331,11 @@ gemm_status_t build_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, co
   if (st != GEMM_OK && !o.variant) return st;
   int variant = o.variant ? o.variant : choose_variant(M, N, K, dtype, sms, o.layout, o.split_k);
   if (is_mx(dtype)) {
-    // block-scaled inputs run on step 7's one-CTA tile or step 8's CTA pair (one consumer)
-    if (variant != GEMM_VARIANT_S7_WARP_SPECIALIZED && variant != GEMM_VARIANT_S8_CTA_PAIR)
+    // block-scaled inputs run on step 7's one-CTA tile, step 8's CTA pair (one
+    // consumer) or, for bf16 C with the static schedule, step 9's two consumers
+    const bool s9_ok = variant == GEMM_VARIANT_S9_TWO_CONSUMERS && out_bytes(dtype) == 2 &&
+                       (o.sched == 0 || o.sched == GEMM_SCHED_STATIC);
+    if (variant != GEMM_VARIANT_S7_WARP_SPECIALIZED && variant != GEMM_VARIANT_S8_CTA_PAIR && !s9_ok)
       return GEMM_ERR_UNSUPPORTED_SHAPE;
   }
   if (is_f8(dtype)) {
@@ -427,8 +432,13 @@ gemm_status_t build_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, co
       }
     }
     if (p->in_mx) {
-      p->stages = o.stages ? std::min<int>(o.stages, mx_max_stages(p->cg)) : mx_max_stages(p->cg);
-      p->smem = mx_smem_bytes(p->cg, p->stages);
+      if (p->consumers == 2) {
+        p->tile_n = 224;  // 448 TMEM columns of accumulators leave 64 for the scale slots
+        p->sched = GEMM_SCHED_STATIC;
+      }
+      const int maxs = mx_max_stages(p->cg, p->consumers);
+      p->stages = o.stages ? std::min<int>(o.stages, maxs) : maxs;
+      p->smem = mx_smem_bytes(p->cg, p->stages, p->consumers);
     }
   } else if (variant == GEMM_VARIANT_S6_PERSISTENT) {
     p->smem = step6_smem_bytes(p->stages);
@@ -562,9 +572,11 @@ const CUtensorMap* operand_map(gemm_plan_s* p, int role, const void* ptr) {
     const int64_t bytes = gemm_mx_scale_bytes(p->M, p->K);
     ok = bytes > 0 && encode_2d(&victim->map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, ptr, 128, (uint64_t)(bytes / 128), 128,
                                 4, CU_TENSOR_MAP_SWIZZLE_NONE);
-  } else if (role == 5) {
-    // MX scales of B: the two 128-row blocks of a 256-row tile in one box
-    ok = encode_mx_pairs(&victim->map, ptr, (uint64_t)((p->K + 127) / 128), (uint64_t)((p->N + 127) / 128));
+  } else if (role == 5 || role == 7) {
+    // MX scales of B: the two 128-row blocks of a 256-row tile in one box; role 7
+    // (step 9's 224-row tiles): the three blocks that hold a tile's rows
+    ok = encode_mx_pairs(&victim->map, ptr, (uint64_t)((p->K + 127) / 128), (uint64_t)((p->N + 127) / 128),
+                         role == 7 ? 3u : 2u);
   } else if (role == 3) {
     // activation rows of the tensor-core GEMV: 16-row boxes, rows >= M read as zero
     ok = encode_2d(&victim->map, in_t, 2, ptr, (uint64_t)p->K, (uint64_t)p->M, 64, 16);
@@ -661,7 +673,7 @@ gemm_status_t launch_plan(gemm_plan_s* p, const void* A, const void* B, void* C,
       } else if (spec->kind == ARGS_ABCSS_K) {
         const CUtensorMap* mc = operand_map(p, 2, C);
         const CUtensorMap* msa = operand_map(p, 4, sfa);
-        const CUtensorMap* msb = operand_map(p, 5, sfb);
+        const CUtensorMap* msb = operand_map(p, (epi == nullptr && p->in_mx && p->consumers == 2) ? 7 : 5, sfb);
         if (!mc || !msa || !msb) return GEMM_ERR_CUDA;
         void* args[] = {const_cast<CUtensorMap*>(ma), const_cast<CUtensorMap*>(mb), const_cast<CUtensorMap*>(mc),
                         const_cast<CUtensorMap*>(msa), const_cast<CUtensorMap*>(msb), &k};
@@ -693,13 +705,21 @@ gemm_status_t run_with_epilogue(gemm_plan_s* plan, const void* A, const void* B,
   const int act = epi->activation;
   if (!plan->epi_ready[act]) {
     cudaError_t e;
-    if (plan->in_mx) {
+    if (plan->in_mx && plan->consumers == 1) {
       // the block-scaled plan already runs one consumer on one CTA
       plan->epi_stages[act] = plan->stages;
       plan->epi_tiles_m[act] = plan->tiles_m;
       plan->epi_tiles_n[act] = plan->tiles_n;
       e = spec_mx(plan->cg, 0, plan->out_f32, plan->stages, std::min(plan->grid_units, plan->tiles_m * plan->tiles_n),
                   &plan->spec_epi[act], act);
+    } else if (plan->in_mx) {
+      // step 9's block-scaled kernel has no fused epilogue: step 8's (256 x 256 tiles)
+      plan->epi_stages[act] = mx_max_stages(2, 1);
+      plan->epi_tiles_m[act] = ceil_div(plan->M, 256);
+      plan->epi_tiles_n[act] = ceil_div(plan->N, 256);
+      e = spec_mx(2, 0, plan->out_f32, plan->epi_stages[act],
+                  std::min(plan->grid_units, plan->epi_tiles_m[act] * plan->epi_tiles_n[act]), &plan->spec_epi[act],
+                  act);
     } else {
       // The epilogue runs in the writeback warps while the MMAs of the next tile
       // proceed.  Steps 7 and 8 have a TMEM double buffer for that; step 9's two

@@ -103,7 +103,10 @@ constexpr size_t WS_SMEM_LIMIT = 232448;  // 227 KB per CTA
 constexpr int SK_WARP_FLOATS = (WS_BN / 32) * 32 * 32;  // one writeback warp's 32 x 256 fp32 part
 constexpr uint32_t MX_BLOCK = 512;  // scales of 128 rows x 128 K-elements (4 per row)
 constexpr uint32_t MX_TMEM_COL = 256;  // first TMEM column of the per-stage scale slots
-constexpr uint32_t MX_TMEM_SLOT = 16;  // TMEM columns per stage: 4 for A, 8 for B
+constexpr uint32_t MX_TMEM_SLOT = 16;  // TMEM columns per stage: 4 for A, 8 for B (step 9: 4 + 4 + 8)
+// threads of the MX kernels: 8 warps, and a ninth on step 9 (two consumers) that
+// regroups the B scales and copies every scale block into TMEM
+__host__ __device__ constexpr int mx_threads(int consumers) { return consumers == 2 ? 288 : 256; }
 
 // A warp's partial accumulator (32 rows x 256 columns, fp32) is kept as 8 chunks of
 // 32 columns, each [j][lane][4 values]: lane L's values 4j..4j+3 of a chunk sit at
@@ -164,8 +167,10 @@ struct WsCfg {
   // every CTA of the cluster, plus the leader's MMA consumers
   static constexpr uint32_t RING_CONSUMERS = (uint32_t)(CG * 5 + NCONS);
   // MX scale blocks per stage and CTA: one for the CTA's 128 rows of A, two for
-  // the tile's 256 rows of B
-  static constexpr uint32_t MX_BYTES = MX_BLOCK * 3u;
+  // the tile's 256 rows of B; on step 9 (224-column tiles) two for A (one per
+  // consumer), the three 128-row blocks of B holding the tile's 224 rows as
+  // loaded, and the two blocks they are regrouped into
+  static constexpr uint32_t MX_BYTES = MX_BLOCK * (NCONS == 2 ? 7u : 3u);
 };
 
 // The kernel body.  EPI < 0: plain writeback; EPI >= 0: fused epilogue with
@@ -177,14 +182,28 @@ template <typename OutT, int CG, int NCONS, int SCHED, int EPI, bool MX, bool SK
 __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMap* tmB, const CUtensorMap* tmC,
                                         const CUtensorMap* tmSA, const CUtensorMap* tmSB, const KParams& p) {
   using Cfg = WsCfg<CG, NCONS, BN>;
-  static_assert(!MX || NCONS == 1, "MX block scaling runs with one MMA consumer");
-  static_assert(BN == WS_BN || (!MX && !SK && EPI < 0), "narrow tiles: plain writeback, whole tiles");
+  // MX on step 9: two consumers on the CTA pair's 512 x 224 tile
+  constexpr bool MX9 = MX && NCONS == 2;
+  static_assert(!MX9 || (CG == 2 && BN == 224 && EPI < 0 && sizeof(OutT) == 2 && !SK && !KS),
+                "MX with two consumers: CTA pair, 224-column tiles, plain bf16 writeback");
+  static_assert(BN == WS_BN || ((!MX || MX9) && !SK && EPI < 0), "narrow tiles: plain writeback, whole tiles");
   static_assert(!KS || (CG == 1 && NCONS == 1 && !MX && !SK && EPI < 0 && BN == WS_BN),
                 "split-K clusters: step 7 tile, plain writeback");
   static_assert(!SK || (!MX && EPI < 0 && SCHED == SCHED_STATIC), "stream-K: plain writeback, static schedule");
   // MX on the pair: a separate warp copies the scales and takes tile ids from the ring
-  constexpr bool MX_COPIER = MX && CG == 2;
-  constexpr uint32_t RING_CONS = Cfg::RING_CONSUMERS + (MX_COPIER ? 1u : 0u);
+  // (warp 3 of the leader with one consumer; warp 8 of both CTAs on step 9)
+  constexpr bool MX_COPIER = MX && CG == 2 && !MX9;
+  constexpr uint32_t RING_CONS = Cfg::RING_CONSUMERS + (MX_COPIER ? 1u : 0u) + (MX9 ? (uint32_t)CG : 0u);
+  // TMEM columns: consumer c's accumulator at c * 256; the per-stage scale slots
+  // from MX_TMEM_COL, or on step 9 MX in the two 32-column gaps the 224-column
+  // accumulators leave (columns 224-255 and 480-511, two 16-column slots each)
+  auto sf_slot_col = [&](uint32_t st) -> uint32_t {
+    if constexpr (MX9) {
+      return (st < 2u ? (uint32_t)BN : 256u + (uint32_t)BN) + (st & 1u) * MX_TMEM_SLOT;
+    } else {
+      return MX_TMEM_COL + st * MX_TMEM_SLOT;
+    }
+  };
   constexpr uint32_t STAGING = MX ? WS_STAGING / 2 : WS_STAGING;
   constexpr uint32_t WARP_STAGING = STAGING / 4;
   constexpr int CW = (sizeof(OutT) == 4) ? 32 : 64;  // output columns per 128-byte staging row
@@ -214,6 +233,8 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
   uint64_t* sf_ready = bars + 36;              // [8]  scale copies -> MMA (MX)
   uint64_t* cp_drain = bars + 44;              // scale-copy warp's last copies done (MX)
   uint64_t* red_full = bars + 45;              // split-K partials parked (every CTA of the cluster)
+  uint64_t* sf_land = bars + 46;               // [8]  this CTA's B scale blocks landed (step 9 MX)
+  uint64_t* sf_grouped = bars + 54;            // [8]  B scales regrouped in both CTAs (step 9 MX, leader)
   uint32_t* clc_resp = reinterpret_cast<uint32_t*>(bars + 30);   // 16 B, 16-aligned
   volatile int32_t* ring_tile = reinterpret_cast<volatile int32_t*>(clc_resp + 4);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(clc_resp + 4 + WS_RING);
@@ -231,9 +252,13 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
     for (int s = 0; s < S; ++s) {
       mbar_init(smem_u32(full + s), 1);
       mbar_init(smem_u32(empty + s), NCONS);
-      if constexpr (MX_COPIER) mbar_init(smem_u32(sf_ready + s), 1);
+      if constexpr (MX_COPIER || MX9) mbar_init(smem_u32(sf_ready + s), 1);
+      if constexpr (MX9) {
+        mbar_init(smem_u32(sf_land + s), 1);
+        mbar_init(smem_u32(sf_grouped + s), CG);
+      }
     }
-    if constexpr (MX_COPIER) mbar_init(smem_u32(cp_drain), 1);
+    if constexpr (MX_COPIER || MX9) mbar_init(smem_u32(cp_drain), 1);
     if constexpr (KS) mbar_init(smem_u32(red_full), 4u * (uint32_t)ks_n);
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(acc_full + i), 1);
@@ -392,7 +417,8 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
           // MX: one block of A scales and one box holding the two blocks of B scales
           // (a block past the array's last row group arrives as zeros)
           const int32_t n_tile = tn * BN;
-          const uint32_t mx_tx = MX ? 3u * MX_BLOCK : 0u;
+          // (step 9: the scales count on this CTA's own barrier instead)
+          const uint32_t mx_tx = MX9 ? 0u : MX ? 3u * MX_BLOCK : 0u;
           if (leader) mbar_arrive_expect_tx(fb, (Cfg::STAGE + mx_tx) * CG);
           uint8_t* st = ring + (size_t)stage * Cfg::STAGE;
 #pragma unroll
@@ -439,7 +465,18 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
             // Every extra copy on the pair costs throughput, hence the one B box.
             uint8_t* sd = mx_ring + (size_t)stage * Cfg::MX_BYTES;
             const int32_t ya = 4 * ((m_cta / 128) * KB + kb);
-            if constexpr (CG == 1) {
+            if constexpr (MX9) {
+              // A: the 128-row block of each consumer (rows m_cta and m_cta + 256);
+              // B: the three 128-row blocks from the one holding the tile's first row;
+              // all on this CTA's own barrier, which the regrouping warp waits on, so
+              // the scales travel to TMEM while the operands are still landing
+              const uint32_t lb = smem_u32(sf_land + stage);
+              mbar_arrive_expect_tx(lb, 5u * MX_BLOCK);
+#pragma unroll
+              for (int c = 0; c < 2; ++c)
+                tma_load_2d(smem_u32(sd + c * MX_BLOCK), tmSA, lb, 0, 4 * (((m_cta + c * 256) / 128) * KB + kb));
+              tma_load_4d(smem_u32(sd + 2 * MX_BLOCK), tmSB, lb, 0, 0, kb, n_tile / 128);
+            } else if constexpr (CG == 1) {
               tma_load_2d(smem_u32(sd), tmSA, fb, 0, ya);
               tma_load_4d(smem_u32(sd + MX_BLOCK), tmSB, fb, 0, 0, kb, n_tile / 128);
             } else {
@@ -463,8 +500,15 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
         // per-SM copy rate seen (about 40 GB/s: 10 us).
         volatile uint32_t never = 0u;  // a timeout here sets this flag only
         const WaitCtl wd{&never, nullptr, 2000000ull, 0};
+        const uint32_t n = issued < (uint32_t)S ? issued : (uint32_t)S;
+        if constexpr (MX9) {
+          // the scale blocks land on this CTA's own barriers
+          for (uint32_t back = 1; back <= n; ++back) {
+            const uint32_t sb = (stage + (uint32_t)S - back) % (uint32_t)S;
+            mbar_wait(smem_u32(sf_land + sb), back <= stage ? sphase : sphase ^ 1u, wd, 0u);
+          }
+        }
         if (CG == 1 || leader) {
-          const uint32_t n = issued < (uint32_t)S ? issued : (uint32_t)S;
           for (uint32_t back = 1; back <= n; ++back) {
             const uint32_t sb = (stage + (uint32_t)S - back) % (uint32_t)S;
             mbar_wait(smem_u32(full + sb), back <= stage ? sphase : sphase ^ 1u, wd, 0u);
@@ -493,7 +537,7 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
         } else {
           if (!ring_get(i, tile) || tile < 0) break;
         }
-        const uint32_t slot = MX ? 0u : (NCONS == 2) ? (uint32_t)cons : (i & 1u);
+        const uint32_t slot = (NCONS == 2) ? (uint32_t)cons : MX ? 0u : (i & 1u);
         const uint32_t apar = (MX || NCONS == 2) ? (i & 1u) : ((i >> 1) & 1u);
         if (!mbar_wait<CG == 2>(smem_u32(acc_empty + slot), apar ^ 1u, w, WAIT_MMA_ACC_EMPTY)) break;
         tc_fence_after();
@@ -505,8 +549,10 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
           const uint32_t acc0 = (it != 0) ? 1u : 0u;  // the segment's first MMA overwrites D
           // MX pair: this stage's scales are in TMEM; the copy warp saw the stage land
           // before copying, so this one wait covers the operands too
-          const uint32_t ready = MX_COPIER ? smem_u32(sf_ready + stage) : smem_u32(full + stage);
+          const uint32_t ready = (MX_COPIER || MX9) ? smem_u32(sf_ready + stage) : smem_u32(full + stage);
           if (!mbar_wait(ready, sphase, w, WAIT_MMA_FULL)) { ok = false; break; }
+          // step 9 MX: the scales were copied on their own; the operands land on `full`
+          if (MX9 && !mbar_wait(smem_u32(full + stage), sphase, w, WAIT_MMA_FULL)) { ok = false; break; }
           tc_fence_after();
           const uint32_t sa = smem_u32(ring + (size_t)stage * Cfg::STAGE + cons * WS_A_BYTES);
           const uint32_t sb = smem_u32(ring + (size_t)stage * Cfg::STAGE + NCONS * WS_A_BYTES);
@@ -516,7 +562,7 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
           const uint64_t astep = a_mn ? 128 : 2, bstep = b_mn ? 128 : 2;
           // four MMAs per stage, each over 32 bytes of K (16 x 16-bit or 32 x 8-bit)
           if constexpr (MX) {
-            if constexpr (!MX_COPIER) {
+            if constexpr (!MX_COPIER && !MX9) {
               // one CTA: the scales precede their MMAs in this thread's issue order
               const uint32_t sft0 = tmem + MX_TMEM_COL + stage * MX_TMEM_SLOT;
               const uint32_t sfs = smem_u32(mx_ring + (size_t)stage * Cfg::MX_BYTES);
@@ -524,15 +570,17 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
               tmem_cp_32x128b_x4<CG>(sft0 + 4, sdesc_rows16(sfs + MX_BLOCK));
               tmem_cp_32x128b_x4<CG>(sft0 + 8, sdesc_rows16(sfs + 2 * MX_BLOCK));
             }
-            const uint32_t sft = tmem + MX_TMEM_COL + stage * MX_TMEM_SLOT;
+            const uint32_t sft = tmem + sf_slot_col(stage);
+            // A scales: 4 columns (step 9: 4 per consumer), then B's
+            const uint32_t sfa = sft + (MX9 ? 4u * (uint32_t)cons : 0u), sfb = sft + (MX9 ? 8u : 4u);
             // byte k of each scale word belongs to the k-th 32-element K block; blocks
             // wholly past K are not issued (their scale bytes are padding)
             const int32_t rem = p.K - kb * BKE;
 #pragma unroll
             for (int k = 0; k < 4; ++k)
               if (k * 32 < rem)
-                mma_mxf8f6f4<CG>(d, ad + 2 * k, bd + 2 * k, p.idesc | ((uint32_t)k << 4) | ((uint32_t)k << 29), sft,
-                                 sft + 4, acc0 | (uint32_t)k);
+                mma_mxf8f6f4<CG>(d, ad + 2 * k, bd + 2 * k, p.idesc | ((uint32_t)k << 4) | ((uint32_t)k << 29), sfa,
+                                 sfb, acc0 | (uint32_t)k);
           } else if (f8) {
 #pragma unroll
             for (int k = 0; k < 4; ++k)
@@ -588,7 +636,95 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
       const WaitCtl wd{zero_word, p.status, p.timeout_ns, 0};
       mbar_wait(smem_u32(cp_drain), 0, wd, WAIT_DRAIN);
     }
-  } else if (warp >= 4) {
+  } else if (MX9 && warp == 8) {
+    // ------------------------------- B scale regrouping and scale copies (step 9 MX)
+    // The tile's 224 B rows start at a multiple of 32 but not of 128, so their
+    // scales, loaded as the three 128-row blocks that hold them, are regrouped into
+    // the two blocks of 128 rows the MMA reads: in the tiled layout a block holds
+    // 32 rows of 16 bytes, word j of row l being the four K scales of matrix row
+    // 32 j + l, so 32-row group G of the tile (global group 7 tn + G) moves from
+    // word (7 tn + G) % 4 of loaded block (7 tn + G) / 4 - (7 tn) / 4 to word G % 4
+    // of block G / 4; lane l moves row l of every group, and group 7 (rows 224-255,
+    // outside the tile) is zeroed.  Both CTAs regroup their own copy and arrive on
+    // the leader's barrier.  The leader's lane 0 copies a stage's four blocks into
+    // the TMEM slot of both CTAs one stage later, after regrouping the next, so
+    // the other CTA's arrival has a stage's time to travel instead of holding up
+    // every stage; the MMA warps wait for the copies and, separately, the operands.
+    uint32_t stage = 0, sphase = 0;
+    bool ok = true, pending = false;
+    uint32_t pstage = 0, pphase = 0;
+    // the copies of the stage regrouped last: the leader's lane 0 only
+    auto copy_scales = [&](uint32_t st, uint32_t ph) -> bool {
+      if (!mbar_wait<true>(smem_u32(sf_grouped + st), ph, w, WAIT_MMA_FULL)) return false;
+      tc_fence_after();
+      const uint32_t sft = tmem + sf_slot_col(st);
+      const uint32_t sfs = smem_u32(mx_ring + (size_t)st * Cfg::MX_BYTES);
+      tmem_cp_32x128b_x4<CG>(sft, sdesc_rows16(sfs));                      // consumer 0's A rows
+      tmem_cp_32x128b_x4<CG>(sft + 4, sdesc_rows16(sfs + MX_BLOCK));       // consumer 1's A rows
+      tmem_cp_32x128b_x4<CG>(sft + 8, sdesc_rows16(sfs + 5 * MX_BLOCK));   // B rows 0-127
+      tmem_cp_32x128b_x4<CG>(sft + 12, sdesc_rows16(sfs + 6 * MX_BLOCK));  // B rows 128-223
+      mma_commit_cg<CG>(smem_u32(sf_ready + st));
+      return true;
+    };
+    for (uint32_t i = 0; ok; ++i) {
+      int32_t tile = -1;
+      uint32_t okr = 1;
+      if (lane == 0) okr = ring_get(i, tile) ? 1u : 0u;
+      okr = __shfl_sync(0xffffffffu, okr, 0);
+      tile = __shfl_sync(0xffffffffu, tile, 0);
+      if (!okr || tile < 0) break;
+      int32_t tm, tn;
+      raster_tile(tile, p.tiles_m, p.tiles_n, p.raster_group, tm, tn);
+      const int32_t g0 = tn * (BN / 32);  // the tile's first 32-row group of B
+      for (int32_t kb = 0; kb < KB; ++kb) {
+        uint32_t got = 1;
+        if (lane == 0) got = mbar_wait(smem_u32(sf_land + stage), sphase, w, WAIT_MMA_FULL) ? 1u : 0u;
+        got = __shfl_sync(0xffffffffu, got, 0);
+        if (!got) { ok = false; break; }
+        uint8_t* sd = mx_ring + (size_t)stage * Cfg::MX_BYTES;
+        const uint8_t* loaded = sd + 2 * MX_BLOCK;
+        uint8_t* grouped = sd + 5 * MX_BLOCK;
+#pragma unroll
+        for (int32_t G = 0; G < 8; ++G) {
+          uint32_t v = 0u;
+          if (G < BN / 32) {
+            const int32_t gg = g0 + G;
+            v = *reinterpret_cast<const uint32_t*>(loaded + ((gg >> 2) - (g0 >> 2)) * MX_BLOCK + lane * 16u +
+                                                   (uint32_t)(gg & 3) * 4u);
+          }
+          *reinterpret_cast<uint32_t*>(grouped + (G >> 2) * MX_BLOCK + lane * 16u + (uint32_t)(G & 3) * 4u) = v;
+        }
+        // the regrouped blocks are read by tcgen05.cp (async proxy)
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          if (leader) {
+            mbar_arrive(smem_u32(sf_grouped + stage));
+          } else {
+            mbar_arrive_cluster(mapa_shared(smem_u32(sf_grouped + stage), 0));
+          }
+        }
+        if (leader && lane == 0) {
+          // the TMEM slot of a stage was last read by MMAs that completed before this
+          // stage's loads were issued
+          if (pending && !copy_scales(pstage, pphase)) ok = false;
+          pending = true;
+          pstage = stage;
+          pphase = sphase;
+        }
+        ok = __shfl_sync(0xffffffffu, ok ? 1u : 0u, 0) != 0u;
+        if (!ok) break;
+        if (++stage == (uint32_t)S) { stage = 0; sphase ^= 1u; }
+      }
+    }
+    if (leader && lane == 0) {
+      if (ok && pending) copy_scales(pstage, pphase);
+      // the copies this thread issued must be complete before TMEM is released
+      mma_commit_cg<CG>(smem_u32(cp_drain));
+      const WaitCtl wd{zero_word, p.status, p.timeout_ns, 0};
+      mbar_wait(smem_u32(cp_drain), 0, wd, WAIT_DRAIN);
+    }
+  } else if (warp >= 4 && warp < 8) {
     // ------------------------------------------------------------ writeback
     const uint32_t q = warp & 3u;  // TMEM lane quarter this warp may access
     uint8_t* my_staging = staging + q * WARP_STAGING;
@@ -613,7 +749,7 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
       bool ok = true;
 #pragma unroll 1
       for (int cons = 0; cons < NCONS; ++cons) {
-        const uint32_t slot = MX ? 0u : (NCONS == 2) ? (uint32_t)cons : (i & 1u);
+        const uint32_t slot = (NCONS == 2) ? (uint32_t)cons : MX ? 0u : (i & 1u);
         const uint32_t apar = (MX || NCONS == 2) ? (i & 1u) : ((i >> 1) & 1u);
         uint32_t got = 1;
         if (lane == 0) got = mbar_wait(smem_u32(acc_full + slot), apar, w, WAIT_EPI_ACC_FULL) ? 1u : 0u;
@@ -945,13 +1081,14 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
   ws_body<OutT, CG, NCONS, SCHED, EPI, false, false, BN>(&tmA, &tmB, &tmC, nullptr, nullptr, p);
 }
 
-// entry point of the MX block-scaled kernels (one consumer)
-template <typename OutT, int CG, int SCHED, int EPI = -1>
-__global__ void __launch_bounds__(WS_THREADS, 1)
+// entry point of the MX block-scaled kernels (one consumer; or two on the CTA
+// pair's 512 x 224 tile, step 9)
+template <typename OutT, int CG, int SCHED, int EPI = -1, int NCONS = 1, int BN = WS_BN>
+__global__ void __launch_bounds__(mx_threads(NCONS), 1)
     k_ws_mx(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
             const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmSA,
             const __grid_constant__ CUtensorMap tmSB, KParams p) {
-  ws_body<OutT, CG, 1, SCHED, EPI, true>(&tmA, &tmB, &tmC, &tmSA, &tmSB, p);
+  ws_body<OutT, CG, NCONS, SCHED, EPI, true, false, BN>(&tmA, &tmB, &tmC, &tmSA, &tmSB, p);
 }
 
 // entry point of the split-K cluster kernels (step 7 tile, plain writeback)
@@ -975,9 +1112,9 @@ void* ws_kernel_ptr() {
   return reinterpret_cast<void*>(k_ws<OutT, CG, NCONS, SCHED, EPI, BN>);
 }
 
-template <typename OutT, int CG, int SCHED, int EPI = -1>
+template <typename OutT, int CG, int SCHED, int EPI = -1, int NCONS = 1, int BN = WS_BN>
 void* mx_kernel_ptr() {
-  return reinterpret_cast<void*>(k_ws_mx<OutT, CG, SCHED, EPI>);
+  return reinterpret_cast<void*>(k_ws_mx<OutT, CG, SCHED, EPI, NCONS, BN>);
 }
 
 }  // namespace

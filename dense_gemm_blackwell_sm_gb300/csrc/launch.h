@@ -75,13 +75,14 @@ cudaError_t spec_ws(int cg, int consumers, int sched, bool out_f32, int stages, 
 // distributed shared memory; grid = tiles x split
 cudaError_t spec_ws_ks(bool out_f32, int stages, int tiles, int split, LaunchSpec* out);
 
-// steps 7 and 8 with MX block scales (8-bit inputs, UE8M0 scale per 32 K
+// steps 7-9 with MX block scales (8-bit inputs, UE8M0 scale per 32 K
 // elements): cg = 1 (one CTA per 128x256 tile) or 2 (CTA pair, 256x256), one
-// consumer, a single TMEM accumulator
-size_t mx_smem_bytes(int cg, int stages);
-int mx_max_stages(int cg);
+// consumer and a single TMEM accumulator; or cg = 2 with two consumers (step 9:
+// 512x224 tiles, bf16 C, plain writeback, static schedule)
+size_t mx_smem_bytes(int cg, int stages, int consumers = 1);
+int mx_max_stages(int cg, int consumers = 1);
 cudaError_t spec_mx(int cg, int sched, bool out_f32, int stages, int clusters, LaunchSpec* out,
-                    int fused_act = -1);
+                    int fused_act = -1, int consumers = 1);
 
 // decode GEMV, C (M x N) = X (M x K) * B^T for M <= 16, on CUDA cores
 struct GemvParams {

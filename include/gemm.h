@@ -59,7 +59,9 @@ typedef enum {
    * consecutive K elements of a row of A or B share one UE8M0 scale 2^(e-127);
    * run with gemm_plan_run_mx, which takes the two scale arrays.  Variants 7
    * and 8 (one MMA consumer; the automatic plan picks the one whose tiles
-   * finish first, see gemm_auto_variant). */
+   * finish first, see gemm_auto_variant), and on request (opts.variant = 9,
+   * bf16 C, static schedule) variant 9's two consumers on 512 x 224 cluster
+   * tiles; other variants give GEMM_ERR_UNSUPPORTED_SHAPE. */
   GEMM_MXE4M3_F32 = 8,  /* MXFP8 E4M3 in, fp32 out */
   GEMM_MXE4M3_BF16 = 9, /* MXFP8 E4M3 in, bf16 out */
   GEMM_MXE5M2_F32 = 10, /* MXFP8 E5M2 in, fp32 out */

@@ -87,9 +87,17 @@ def test_fp8_row_pitch_rule(lib):
 def test_mx_rules(lib):
     for dt in (gemm.MXE4M3_F32, gemm.MXE4M3_BF16, gemm.MXE5M2_F32, gemm.MXE5M2_BF16):
         assert _plan_status(lib, 64, 64, 24, dt) == gemm.ERR_UNSUPPORTED_SHAPE
-        # block-scaled inputs run on variants 7 and 8 only, K-major only
-        for v in (gemm.S3, gemm.S6, gemm.S9, gemm.GEMV):
+        # block-scaled inputs run on variants 7 and 8, and on 9 with bf16 C and the
+        # static schedule (two consumers, 512 x 224 tiles), K-major only
+        for v in (gemm.S3, gemm.S6, gemm.GEMV):
             assert _plan_status(lib, 256, 256, 256, dt, gemm.make_opts(variant=v)) == gemm.ERR_UNSUPPORTED_SHAPE
+        s9 = _plan_status(lib, 256, 256, 256, dt, gemm.make_opts(variant=gemm.S9))
+        if dt in (gemm.MXE4M3_F32, gemm.MXE5M2_F32):
+            assert s9 == gemm.ERR_UNSUPPORTED_SHAPE
+        else:
+            assert s9 != gemm.ERR_UNSUPPORTED_SHAPE
+            assert _plan_status(lib, 256, 256, 256, dt, gemm.make_opts(variant=gemm.S9, sched=gemm.SCHED_ATOMIC)) == \
+                gemm.ERR_UNSUPPORTED_SHAPE
         assert _plan_status(lib, 256, 256, 256, dt, gemm.make_opts(variant=gemm.S7, layout=gemm.LAYOUT_A_MN)) == \
             gemm.ERR_UNSUPPORTED_SHAPE
         # the one-shot entry points have no scale arguments
@@ -167,7 +175,8 @@ AUTO_CASES = [
     ((256, 14336, 4096, gemm.BF16_BF16), gemm.S8),      # 56 pair tiles beat 112 single tiles
     ((1024, 4096, 4096, gemm.BF16_BF16), gemm.S8),
     ((8, 4096, 4096, gemm.E4M3_BF16), gemm.S7),         # 8-bit inputs have no GEMV (32 K blocks)
-    ((8192, 8192, 8192, gemm.MXE4M3_BF16), gemm.S8),    # block-scaled: step 7 or 8 only
+    ((8192, 8192, 8192, gemm.MXE4M3_BF16), gemm.S8),    # block-scaled, bf16 C: step 8 (step 9 on request)
+    ((8192, 8192, 8192, gemm.MXE4M3_F32), gemm.S8),     # block-scaled, fp32 C: step 7 or 8
     ((128, 25600, 4096, gemm.MXE4M3_BF16), gemm.S7),    # 100 tiles: one wave of 152 CTAs, two of 76 pairs
     ((2048, 2048, 2048, gemm.BF16_BF16), gemm.S7),      # 32 K blocks: the pair's fixed cost per tile shows
     ((2048, 2048, 8192, gemm.BF16_BF16), gemm.S8),      # 128 K blocks: the pair's rate wins

@@ -1,7 +1,8 @@
 """GPU parity of the MX block-scaled GEMM (8-bit float operands with one UE8M0
 scale per 32 consecutive K elements of every row of A and B, tcgen05.mma
-kind::mxf8f6f4 on the step-7 tile and on the step-8 CTA pair) against the CPU
-oracle's fp64 block-scaled product, with the plain and the fused writeback."""
+kind::mxf8f6f4 on the step-7 tile, on the step-8 CTA pair and on step 9's two
+consumers with 512 x 224 tiles) against the CPU oracle's fp64 block-scaled
+product, with the plain and the fused writeback."""
 from __future__ import annotations
 
 import numpy as np
@@ -170,6 +171,74 @@ def test_rejections():
         p2.run_mx(a, a, c, s, s)
     assert e.value.status == gemm.ERR_UNSUPPORTED_DTYPE
     p2.destroy()
+
+
+# step 9: 224-column tiles start B's rows at a multiple of 32 but not of 128, so
+# each tile's B scales are regrouped from three 128-row blocks; N spans several
+# tile columns (tn = 0..8 covers every offset of a tile inside a 128-row block),
+# M several tile rows, K a partial 128-element stage
+S9_SHAPES = [(1100, 2000, 400), (512, 224, 128), (300, 520, 272), (4096, 8192, 1024)]
+
+
+@pytest.mark.parametrize("shape", S9_SHAPES)
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+def test_step9_integer_operands_bit_exact(shape, fmt):
+    M, N, K = shape
+    a, b = inputs.integer_operands(M, N, K, fmt, seed=M + 3 * K, lo=-8, hi=8)
+    sa = inputs.mx_scales(M, K, seed=5, e_lo=125, e_hi=129)
+    sb = inputs.mx_scales(N, K, seed=6, e_lo=125, e_hi=129)
+    c, info = _run(a, b, sa, sb, "bf16", gemm.S9)
+    assert info["variant"] == gemm.S9 and info["tile_n"] == 224 and info["consumers"] == 2
+    C, _ = oracle.gemm_mx(a, b, sa, sb)
+    exp = torch.tensor(C).to(torch.bfloat16).double().numpy()
+    bad = np.argwhere(c.double().cpu().numpy() != exp)
+    assert bad.size == 0, bad[:3]
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+def test_step9_random_parity(fmt):
+    M, N, K = 1100, 2000, 400
+    a, b, sa, sb = inputs.mx_operands(M, N, K, fmt, seed=17)
+    c, info = _run(a, b, sa, sb, "bf16", gemm.S9)
+    C, S = oracle.gemm_mx(a, b, sa, sb)
+    r = parity.check(c.double().cpu().numpy(), C, S, "bf16")
+    assert r["ok"], (info, r)
+
+
+def test_step9_scales_only_touch_their_own_block():
+    # B rows 200 (tile 0, second regrouped block) and 300 (tile 1, which starts at
+    # row 224 inside the second 128-row block): only their columns move
+    M, N, K = 512, 896, 256
+    a, b = inputs.integer_operands(M, N, K, "e4m3", seed=9, lo=-4, hi=4)
+    sa = torch.full((M, K // 32), 127, dtype=torch.uint8)
+    sb = torch.full((N, K // 32), 127, dtype=torch.uint8)
+    sa[77, 5] = 130
+    sb[200, 2] = 124
+    sb[300, 7] = 129
+    c, _ = _run(a, b, sa, sb, "bf16", gemm.S9)
+    C, _ = oracle.gemm_mx(a, b, sa, sb)
+    assert np.array_equal(c.double().cpu().numpy(), torch.tensor(C).to(torch.bfloat16).double().numpy())
+    C0, _ = oracle.gemm(a, b)
+    diff = np.argwhere(C != C0)
+    assert ((diff[:, 0] == 77) | (diff[:, 1] == 200) | (diff[:, 1] == 300)).all()
+    assert (diff[:, 1] == 200).any() and (diff[:, 1] == 300).any()
+
+
+def test_step9_plan_with_fused_epilogue():
+    # a step-9 block-scaled plan runs its fused epilogue on step 8's tile
+    M, N, K = 700, 776, 336
+    a, b, sa, sb = inputs.mx_operands(M, N, K, "e4m3", seed=41)
+    g = torch.Generator().manual_seed(1)
+    bias = torch.randn(N, generator=g).float()
+    res = torch.randn(M, N, generator=g).to(torch.bfloat16)
+    c, info = _run(a, b, sa, sb, "bf16", gemm.S9, bias=bias.to(DEV), residual=res.to(DEV), act=gemm.ACT_SILU)
+    assert info["variant"] == gemm.S9
+    C, S = oracle.gemm_mx(a, b, sa, sb)
+    ref = oracle.epilogue(C, bias, res, gemm.ACT_SILU)
+    pre = oracle.epilogue(C, bias, None, oracle.ACT_NONE)
+    r = parity.check_epilogue(c.double().cpu().numpy(), ref, pre, S, np.abs(res.double().numpy()), "bf16",
+                              gemm.ACT_SILU)
+    assert r["ok"], r
 
 
 def test_bench_workload_sampled_rows():
