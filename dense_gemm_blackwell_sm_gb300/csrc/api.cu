@@ -723,13 +723,13 @@ gemm_status_t run_with_epilogue(gemm_plan_s* plan, const void* A, const void* B,
     } else {
       // The epilogue runs in the writeback warps while the MMAs of the next tile
       // proceed.  Steps 7 and 8 have a TMEM double buffer for that; step 9's two
-      // consumers have one accumulator each, handed back only once the writeback
-      // has read the tile's last chunk.  With an activation that wait costs more
-      // than the second consumer saves (8192^3 bf16 + bias + SiLU + residual: 1305
-      // TFLOP/s on step 9's tile, 1618 on step 8's), so a step-9 plan runs the
-      // activations on step 8's 256 x 256 tile (same operand boxes) and only
-      // bias / residual / scales on its own (+ residual: 1784 against 1712).
-      const int cons = (plan->cg == 2 && plan->consumers == 2 && act == GEMM_ACT_NONE) ? 2 : 1;
+      // consumers have one accumulator each, held while the writeback applies the
+      // epilogue.  For bf16 C the residual is read before the accumulator is
+      // ready and the staging and stores follow the hand-back, so step 9 keeps
+      // its tile; for fp32 C (no such drain) an activation runs on step 8's 256 x
+      // 256 tile (same operand boxes) and bias / residual / scales on step 9's.
+      const int cons =
+          (plan->cg == 2 && plan->consumers == 2 && (act == GEMM_ACT_NONE || !plan->out_f32)) ? 2 : 1;
       plan->epi_stages[act] = ws_max_stages(plan->cg, cons);
       plan->epi_tiles_m[act] = ceil_div(plan->M, 128 * plan->cg * cons);
       plan->epi_tiles_n[act] = ceil_div(plan->N, 256);  // the fused kernels use 256-column tiles

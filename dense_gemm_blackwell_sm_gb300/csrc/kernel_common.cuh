@@ -79,18 +79,33 @@ enum : int32_t {
   EPI_ACT_GELU_ERF = 4,   // 0.5 x (1 + erf(x / sqrt(2)))
 };
 
+// The logistic function 1 / (1 + e^-t) = 1 / (1 + 2^(-t log2 e)) on the special
+// function unit: one ex2.approx and one rcp.approx (each within a few ulp of
+// fp32; the rounding of t log2 e moves the result by at most |t| 2^-24
+// relatively, where it is not already saturated at 0 or 1).  Large negative t
+// gives 2^big = inf and 1 / inf = 0; large positive t gives 1 / (1 + 0) = 1.
+__device__ __forceinline__ float logistic(float t) {
+  float e, r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(t * -1.4426950408889634f));
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.f + e));
+  return r;
+}
+
 // the activation is a compile-time choice: each fused kernel carries the code
 // of one activation only (the writeback code shares the SM's instruction cache
-// with the producer and MMA warps)
+// with the producer and MMA warps).  SiLU is x * logistic(x); the tanh form of
+// GeLU uses 0.5 (1 + tanh(u)) = logistic(2 u), so both cost two SFU operations
+// and a few FMAs per element, which matters on the path that holds an
+// accumulator until its epilogue is done.
 template <int ACT>
 __device__ __forceinline__ float epi_activation(float x) {
   if constexpr (ACT == EPI_ACT_RELU) {
     return fmaxf(x, 0.f);
   } else if constexpr (ACT == EPI_ACT_SILU) {
-    return x * __frcp_rn(1.f + expf(-x));  // correctly rounded reciprocal
+    return x * logistic(x);
   } else if constexpr (ACT == EPI_ACT_GELU_TANH) {
-    const float k0 = 0.7978845608028654f;  // sqrt(2 / pi)
-    return 0.5f * x * (1.f + tanhf(k0 * (x + 0.044715f * x * x * x)));
+    const float k2 = 1.5957691216057308f;  // 2 sqrt(2 / pi)
+    return x * logistic(k2 * (x + 0.044715f * x * x * x));
   } else if constexpr (ACT == EPI_ACT_GELU_ERF) {
     return 0.5f * x * (1.f + erff(x * 0.7071067811865476f));
   } else {
@@ -98,67 +113,124 @@ __device__ __forceinline__ float epi_activation(float x) {
   }
 }
 
-// Applies the fused epilogue to n consecutive fp32 accumulator values of one row
-// (columns col0 .. col0+n-1), in place.  bias is read through L1 (every lane of
-// a warp reads the same columns); the residual row segment with 16-byte loads
-// when it lies wholly inside C, element by element at the edges.
-template <typename OutT, int n, int ACT>
-__device__ __forceinline__ void apply_epilogue(uint32_t* v, const KParams& p, int32_t row, int32_t col0) {
-  float x[n];
+// Loads 128 bytes of row `row` of the residual from column col0 on (64 bf16 or
+// 32 fp32 columns) into 32 words, zero for 16-byte groups past column N (C's
+// rows are 16-byte multiples, so each group lies wholly inside or outside C).
+// The caller checks row < M.
+template <typename OutT>
+__device__ __forceinline__ void load_residual128(uint32_t (&r)[32], const KParams& p, int32_t row, int32_t col0) {
+  constexpr int per16 = 16 / (int)sizeof(OutT);
+  const uint4* src =
+      reinterpret_cast<const uint4*>(reinterpret_cast<const OutT*>(p.residual) + (int64_t)row * p.out_ld + col0);
 #pragma unroll
-  for (int j = 0; j < n; ++j) x[j] = __uint_as_float(v[j]);
+  for (int j = 0; j < 8; ++j) {
+    const uint4 u = (col0 + per16 * j < p.N) ? __ldg(src + j) : make_uint4(0u, 0u, 0u, 0u);
+    r[4 * j] = u.x;
+    r[4 * j + 1] = u.y;
+    r[4 * j + 2] = u.z;
+    r[4 * j + 3] = u.w;
+  }
+}
+
+// Copies columns col0 .. col0+BN-1 of the per-column vector v (N fp32 values,
+// 4-byte aligned) into shared memory dst (BN floats, 16-byte aligned), 0 past
+// column N; the lanes of one warp share the work.
+template <int BN>
+__device__ __forceinline__ void stage_columns(float* dst, const float* v, int32_t col0, int32_t N, uint32_t lane) {
+#pragma unroll
+  for (int j = (int)lane; j < BN; j += 32) dst[j] = (col0 + j < N) ? __ldg(v + col0 + j) : 0.f;
+}
+
+// Applies the fused epilogue to 32 consecutive fp32 accumulator values of one
+// row (columns col0 .. col0+31), in place:
+//   x = act(acc * sa * scale_b[col] + bias[col]) + residual,
+// each term only when present.  sa is scale_a[row] (0 past row M), read by the
+// caller.  r holds the residual of these columns as load_residual128 left it
+// (bf16: 16 words of column pairs; fp32: 32 words), used when has_res.  Bias
+// and scale_b come from sbias / sscale_b when given (shared-memory copies of
+// these 32 columns, 16-byte aligned, staged by the caller), else from global
+// memory: as float4 (every lane of a warp reads the same columns) when the 32
+// columns lie inside C and are 16-byte aligned, else one by one, as 0 past
+// column N.
+template <typename OutT, int ACT>
+__device__ __forceinline__ void apply_epilogue32(uint32_t* v, const KParams& p, int32_t col0, float sa, bool has_res,
+                                                 const uint32_t* r, const float* sbias = nullptr,
+                                                 const float* sscale_b = nullptr) {
+  float x[32];
+#pragma unroll
+  for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(v[j]);
   if (p.scale_a != nullptr) {
-    const float sa = (row < p.M) ? __ldg(p.scale_a + row) : 0.f;
 #pragma unroll
-    for (int j = 0; j < n; ++j) x[j] *= sa;
+    for (int j = 0; j < 32; ++j) x[j] *= sa;
   }
-  if (p.scale_b != nullptr) {
+  const bool whole = col0 + 32 <= p.N;
+  if (p.scale_b != nullptr && sscale_b != nullptr) {
 #pragma unroll
-    for (int j = 0; j < n; ++j) x[j] *= (col0 + j < p.N) ? __ldg(p.scale_b + col0 + j) : 0.f;
-  }
-  if (p.bias != nullptr) {
+    for (int q = 0; q < 8; ++q) {
+      const float4 f = reinterpret_cast<const float4*>(sscale_b)[q];
+      x[4 * q] *= f.x;
+      x[4 * q + 1] *= f.y;
+      x[4 * q + 2] *= f.z;
+      x[4 * q + 3] *= f.w;
+    }
+  } else if (p.scale_b != nullptr) {
+    if (whole && ((reinterpret_cast<uintptr_t>(p.scale_b + col0) & 15u) == 0)) {
 #pragma unroll
-    for (int j = 0; j < n; ++j) x[j] += (col0 + j < p.N) ? __ldg(p.bias + col0 + j) : 0.f;
-  }
-  if constexpr (ACT != EPI_ACT_NONE) {
-#pragma unroll
-    for (int j = 0; j < n; ++j) x[j] = epi_activation<ACT>(x[j]);
-  }
-  if (p.residual != nullptr && row < p.M) {
-    const OutT* r = reinterpret_cast<const OutT*>(p.residual) + (int64_t)row * p.out_ld + col0;
-    constexpr int per16 = 16 / (int)sizeof(OutT);
-    if (col0 + n <= p.N) {
-#pragma unroll
-      for (int q = 0; q < n / per16; ++q) {
-        const uint4 u = __ldg(reinterpret_cast<const uint4*>(r) + q);
-        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-        if constexpr (sizeof(OutT) == 4) {
-#pragma unroll
-          for (int t = 0; t < 4; ++t) x[q * 4 + t] += __uint_as_float(w[t]);
-        } else {
-#pragma unroll
-          for (int t = 0; t < 4; ++t) {
-            const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[t]));
-            x[q * 8 + 2 * t] += f.x;
-            x[q * 8 + 2 * t + 1] += f.y;
-          }
-        }
+      for (int q = 0; q < 8; ++q) {
+        const float4 f = __ldg(reinterpret_cast<const float4*>(p.scale_b + col0) + q);
+        x[4 * q] *= f.x;
+        x[4 * q + 1] *= f.y;
+        x[4 * q + 2] *= f.z;
+        x[4 * q + 3] *= f.w;
       }
     } else {
 #pragma unroll
-      for (int j = 0; j < n; ++j) {
-        if (col0 + j < p.N) {
-          if constexpr (sizeof(OutT) == 4) {
-            x[j] += r[j];
-          } else {
-            x[j] += __bfloat162float(r[j]);
-          }
-        }
+      for (int j = 0; j < 32; ++j) x[j] *= (col0 + j < p.N) ? __ldg(p.scale_b + col0 + j) : 0.f;
+    }
+  }
+  if (p.bias != nullptr && sbias != nullptr) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const float4 f = reinterpret_cast<const float4*>(sbias)[q];
+      x[4 * q] += f.x;
+      x[4 * q + 1] += f.y;
+      x[4 * q + 2] += f.z;
+      x[4 * q + 3] += f.w;
+    }
+  } else if (p.bias != nullptr) {
+    if (whole && ((reinterpret_cast<uintptr_t>(p.bias + col0) & 15u) == 0)) {
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const float4 f = __ldg(reinterpret_cast<const float4*>(p.bias + col0) + q);
+        x[4 * q] += f.x;
+        x[4 * q + 1] += f.y;
+        x[4 * q + 2] += f.z;
+        x[4 * q + 3] += f.w;
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) x[j] += (col0 + j < p.N) ? __ldg(p.bias + col0 + j) : 0.f;
+    }
+  }
+  if constexpr (ACT != EPI_ACT_NONE) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) x[j] = epi_activation<ACT>(x[j]);
+  }
+  if (has_res) {
+    if constexpr (sizeof(OutT) == 4) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) x[j] += __uint_as_float(r[j]);
+    } else {
+#pragma unroll
+      for (int m = 0; m < 16; ++m) {
+        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&r[m]));
+        x[2 * m] += f.x;
+        x[2 * m + 1] += f.y;
       }
     }
   }
 #pragma unroll
-  for (int j = 0; j < n; ++j) v[j] = __float_as_uint(x[j]);
+  for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(x[j]);
 }
 
 // Grouped (L2-aware) raster order: consecutive tile ids walk down a group of

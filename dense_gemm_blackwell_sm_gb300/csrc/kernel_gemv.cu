@@ -69,11 +69,6 @@ __device__ __forceinline__ void pdl_wait_prior_grids() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
-// ask L2 to fetch the 128-byte line holding p (no data returned)
-__device__ __forceinline__ void prefetch_l2_line(const void* p) {
-  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
-}
-
 template <typename InT>
 __device__ __forceinline__ float2 to_f2(uint32_t w) {
   if constexpr (std::is_same<InT, __nv_bfloat16>::value) {

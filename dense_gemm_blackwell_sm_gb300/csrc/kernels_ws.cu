@@ -6,27 +6,28 @@ namespace dgb {
 
 namespace {
 
-template <typename OutT, int CG>
+template <typename OutT, int CG, int NCONS = 1>
 void* pick_fused(int act) {
   switch (act) {
-    case EPI_ACT_RELU: return ws_kernel_ptr<OutT, CG, 1, SCHED_STATIC, EPI_ACT_RELU>();
-    case EPI_ACT_SILU: return ws_kernel_ptr<OutT, CG, 1, SCHED_STATIC, EPI_ACT_SILU>();
-    case EPI_ACT_GELU_TANH: return ws_kernel_ptr<OutT, CG, 1, SCHED_STATIC, EPI_ACT_GELU_TANH>();
-    case EPI_ACT_GELU_ERF: return ws_kernel_ptr<OutT, CG, 1, SCHED_STATIC, EPI_ACT_GELU_ERF>();
-    default: return ws_kernel_ptr<OutT, CG, 1, SCHED_STATIC, EPI_ACT_NONE>();
+    case EPI_ACT_RELU: return ws_kernel_ptr<OutT, CG, NCONS, SCHED_STATIC, EPI_ACT_RELU>();
+    case EPI_ACT_SILU: return ws_kernel_ptr<OutT, CG, NCONS, SCHED_STATIC, EPI_ACT_SILU>();
+    case EPI_ACT_GELU_TANH: return ws_kernel_ptr<OutT, CG, NCONS, SCHED_STATIC, EPI_ACT_GELU_TANH>();
+    case EPI_ACT_GELU_ERF: return ws_kernel_ptr<OutT, CG, NCONS, SCHED_STATIC, EPI_ACT_GELU_ERF>();
+    default: return ws_kernel_ptr<OutT, CG, NCONS, SCHED_STATIC, EPI_ACT_NONE>();
   }
 }
 
 // the fused-epilogue kernels exist for the static scheduler: every activation with
-// one MMA consumer (steps 7 and 8), bias / residual / scales alone with two on the
-// CTA pair (step 9)
+// one MMA consumer (steps 7 and 8) and with two on the CTA pair for bf16 C (step 9,
+// whose writeback applies the epilogue while draining each accumulator); fp32 C
+// on step 9 with bias / residual / scales alone
 template <int CG, int NCONS>
 void* pick_kernel(int sched, bool out_f32, int fused_act) {
   if (fused_act >= 0) {
     if constexpr (NCONS == 2) {
-      if (CG != 2 || fused_act != EPI_ACT_NONE) return nullptr;
-      return out_f32 ? ws_kernel_ptr<float, 2, 2, SCHED_STATIC, EPI_ACT_NONE>()
-                     : ws_kernel_ptr<__nv_bfloat16, 2, 2, SCHED_STATIC, EPI_ACT_NONE>();
+      if (CG != 2) return nullptr;
+      if (out_f32) return fused_act == EPI_ACT_NONE ? ws_kernel_ptr<float, 2, 2, SCHED_STATIC, EPI_ACT_NONE>() : nullptr;
+      return pick_fused<__nv_bfloat16, 2, 2>(fused_act);
     } else {
       return out_f32 ? pick_fused<float, CG>(fused_act) : pick_fused<__nv_bfloat16, CG>(fused_act);
     }

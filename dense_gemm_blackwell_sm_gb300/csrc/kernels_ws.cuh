@@ -214,6 +214,12 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
   // the same for fp32 C on step 9's 224-column tile: two chunks into the staging
   // buffers, the other five into registers
   constexpr bool DRAIN32 = CG == 2 && NCONS == 2 && !SK && !MX && BN == 224 && CW == 32 && EPI < 0;
+  // fused epilogue on step 9: each consumer's single accumulator is held while
+  // the epilogue runs, so the rows are stored straight from registers (no wait
+  // for a staging buffer inside that window), and the staging buffers hold the
+  // tile's bias and scale_b columns instead
+  constexpr bool EPI_DIRECT = EPI >= 0 && NCONS == 2 && !MX && !SK && !KS && BN == WS_BN;
+  static_assert(!EPI_DIRECT || WS_STAGING / 4 >= 2 * WS_BN * 4, "a warp's staging holds two column vectors");
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align_1024(smem_raw);
@@ -747,17 +753,43 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
       int32_t tm, tn;
       raster_tile(tile, p.tiles_m, p.tiles_n, p.raster_group, tm, tn);
       bool ok = true;
+      float* epi_cols = reinterpret_cast<float*>(my_staging);  // EPI_DIRECT: bias, then scale_b
+      if constexpr (EPI_DIRECT) {
+        __syncwarp();  // every lane is done with the previous tile's columns
+        if (p.bias != nullptr) stage_columns<BN>(epi_cols, p.bias, tn * BN, p.N, lane);
+        if (p.scale_b != nullptr) stage_columns<BN>(epi_cols + BN, p.scale_b, tn * BN, p.N, lane);
+        __syncwarp();
+      }
 #pragma unroll 1
       for (int cons = 0; cons < NCONS; ++cons) {
         const uint32_t slot = (NCONS == 2) ? (uint32_t)cons : MX ? 0u : (i & 1u);
         const uint32_t apar = (MX || NCONS == 2) ? (i & 1u) : ((i >> 1) & 1u);
+        const int32_t row0 = tm * Cfg::TILE_M + cons * 128 * CG + (int32_t)rank * 128 + (int32_t)q * 32;
+        const int32_t col_base = tn * BN;
+        // fused epilogue: while the MMAs still run, read the first chunk of the
+        // lane's residual row segment and scale_a, and have L2 fetch the rest of
+        // the segment, so the held accumulator waits on no DRAM round trip
+        uint32_t res_next[EPI >= 0 ? 32 : 1];
+        float epi_sa = 1.f;
+        bool epi_res = false;
+        if constexpr (EPI >= 0) {
+          const int32_t row = row0 + (int32_t)lane;
+          epi_res = p.residual != nullptr && row < p.M;
+          if (epi_res) {
+            load_residual128<OutT>(res_next, p, row, col_base);
+            const uint8_t* seg = reinterpret_cast<const uint8_t*>(reinterpret_cast<const OutT*>(p.residual) +
+                                                                  (int64_t)row * p.out_ld + col_base);
+            const int32_t seg_bytes = min(BN, p.N - col_base) * (int32_t)sizeof(OutT);
+#pragma unroll 1
+            for (int32_t b = 128; b < seg_bytes + 127; b += 128) prefetch_l2_line(seg + min(b, seg_bytes - 1));
+          }
+          if (p.scale_a != nullptr) epi_sa = (row < p.M) ? __ldg(p.scale_a + row) : 0.f;
+        }
         uint32_t got = 1;
         if (lane == 0) got = mbar_wait(smem_u32(acc_full + slot), apar, w, WAIT_EPI_ACC_FULL) ? 1u : 0u;
         got = __shfl_sync(0xffffffffu, got, 0);
         if (!got) { ok = false; break; }
         tc_fence_after();
-        const int32_t row0 = tm * Cfg::TILE_M + cons * 128 * CG + (int32_t)rank * 128 + (int32_t)q * 32;
-        const int32_t col_base = tn * BN;
         const uint32_t tbase = tmem + ((q * 32u) << 16) + slot * 256u;
         // stream-K: this warp's 32 x 256 part of a split tile, in a workspace slot of
         // SK_WARP_FLOATS floats (8 chunks of 32 columns, see sk_add32); the owner adds
@@ -982,6 +1014,13 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
 #pragma unroll 1
           for (int ch = 0; ch < NCH; ++ch) {
             uint32_t v0[32], v1[32];
+            uint32_t res[EPI >= 0 ? 32 : 1];
+            if constexpr (EPI >= 0) {
+              // this chunk's residual, and the next chunk's on its way
+#pragma unroll
+              for (int j = 0; j < 32; ++j) res[j] = res_next[j];
+              if (epi_res && ch + 1 < NCH) load_residual128<OutT>(res_next, p, row0 + (int32_t)lane, col_base + (ch + 1) * CW);
+            }
             tmem_ld_32x32b_x32(tbase + (uint32_t)(ch * CW), v0);
             if constexpr (CW == 64) tmem_ld_32x32b_x32(tbase + (uint32_t)(ch * CW + 32), v1);
             tmem_wait_ld();
@@ -1009,12 +1048,38 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
                 }
               }
             }
+            if constexpr (EPI_DIRECT) {
+              const int32_t col0 = col_base + ch * CW, row = row0 + (int32_t)lane;
+              const float* sb = epi_cols + ch * CW;
+              const float* ss = epi_cols + BN + ch * CW;
+              apply_epilogue32<OutT, EPI>(v0, p, col0, epi_sa, epi_res, res, sb, ss);
+              if constexpr (CW == 64) apply_epilogue32<OutT, EPI>(v1, p, col0 + 32, epi_sa, epi_res, res + 16, sb + 32, ss + 32);
+              // 128 bytes of the lane's row, 16 at a time (C's rows are 16-byte
+              // multiples, so each group lies wholly inside C or outside)
+              if (row < p.M) {
+                uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<OutT*>(p.C) + (int64_t)row * p.out_ld + col0);
+                constexpr int per16 = 16 / (int)sizeof(OutT);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                  uint4 val;
+                  if constexpr (CW == 32) {
+                    val = make_uint4(v0[4 * j], v0[4 * j + 1], v0[4 * j + 2], v0[4 * j + 3]);
+                  } else {
+                    const uint32_t* src = (j < 4) ? (v0 + 8 * j) : (v1 + 8 * (j - 4));
+                    val = make_uint4(pack_bf16x2(src[0], src[1]), pack_bf16x2(src[2], src[3]),
+                                     pack_bf16x2(src[4], src[5]), pack_bf16x2(src[6], src[7]));
+                  }
+                  if (col0 + per16 * j < p.N) dst[j] = val;
+                }
+              }
+              continue;
+            }
             if constexpr (EPI >= 0) {
-              // bias, activation and residual, in fp32, before the single rounding to C's type
-              const int32_t row = row0 + (int32_t)lane;
+              // scales, bias, activation and residual, in fp32, before the single
+              // rounding to C's type
               const int32_t col0 = col_base + ch * CW;
-              apply_epilogue<OutT, 32, EPI>(v0, p, row, col0);
-              if constexpr (CW == 64) apply_epilogue<OutT, 32, EPI>(v1, p, row, col0 + 32);
+              apply_epilogue32<OutT, EPI>(v0, p, col0, epi_sa, epi_res, res);
+              if constexpr (CW == 64) apply_epilogue32<OutT, EPI>(v1, p, col0 + 32, epi_sa, epi_res, res + 16);
             }
             uint8_t* buf = my_staging + (MX ? 0u : (tog & 1u) * 4096u);
             // the store issued from `buf` (two chunks ago; MX: one) is done reading

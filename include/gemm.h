@@ -200,6 +200,9 @@ typedef enum {
   GEMM_ACT_RELU = 1,      /* max(x, 0) */
   GEMM_ACT_SILU = 2,      /* x / (1 + exp(-x)) */
   GEMM_ACT_GELU_TANH = 3, /* 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))) */
+  /* SiLU and the tanh form of GeLU are evaluated as x * logistic(t) with the
+   * hardware's approximate exp2 and reciprocal: within 2^-20 |x| of the exact
+   * value, well inside a bf16 or fp32 rounding of results of that size */
   GEMM_ACT_GELU_ERF = 4   /* 0.5 x (1 + erf(x / sqrt(2))) */
 } gemm_activation_t;
 
@@ -220,10 +223,10 @@ typedef struct {
 
 /* gemm_plan_run with the fused epilogue.  Needs a plan of variant 7, 8 or 9
  * (the automatic plan of most shapes with M > 16); other plans return
- * GEMM_ERR_UNSUPPORTED_SHAPE.  The epilogue kernel uses the static scheduler;
- * with an activation it runs on one MMA consumer per CTA (a variant-9 plan then
- * uses variant 8's 256 x 256 tile), bias / residual / scales alone keep the
- * plan's own variant. */
+ * GEMM_ERR_UNSUPPORTED_SHAPE.  The epilogue kernel uses the static scheduler
+ * and 256-column tiles; a variant-9 plan keeps its two consumers for bf16 C,
+ * and for fp32 C with bias / residual / scales alone (an fp32 activation runs
+ * on variant 8's 256 x 256 tile). */
 GEMM_API gemm_status_t gemm_plan_run_epilogue(gemm_plan_t plan, const void* A, const void* B, void* C,
                                               const gemm_epilogue_t* epilogue, gemm_stream_t stream);
 

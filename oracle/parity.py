@@ -94,7 +94,8 @@ def epilogue_bound(ref_epi, pre, S, residual_abs, out_dtype: str, act: int) -> n
 
     An accumulator error e (|e| <= 2^-10 S, the GEMM rule) moves act(.) by at
     most slope * e; the fp32 additions of bias and residual and the fp32
-    activation (a few ulp of CUDA's expf / tanhf / erff) add at most
+    activation (the kernels' SiLU and tanh-form GeLU go through the hardware's
+    approximate exp2 and reciprocal, the erf form through CUDA's erff) add at most
     2^-17 (|acc + bias| + |residual|), since |act(x)| <= |x| for every
     activation here; bf16 output adds half an ulp of the final value."""
     b = ACT_SLOPE[act] * TOL_REL * np.asarray(S, dtype=np.float64)

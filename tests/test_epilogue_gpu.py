@@ -103,3 +103,34 @@ def test_epilogue_argument_checks():
     assert e.value.status == gemm.ERR_MISALIGNED
     gv.destroy()
     ws.destroy()
+
+
+ACT_SWEEP = np.concatenate([np.linspace(-20.0, 20.0, 3001), -np.logspace(-30, 4, 200), np.logspace(-30, 4, 200),
+                            [0.0, -88.0, -87.0, 88.0, 89.0, -1e4, 1e4]]).astype(np.float32)
+
+
+@pytest.mark.parametrize("variant", [gemm.S7, gemm.S8, gemm.S9])
+@pytest.mark.parametrize("out", ["bf16", "f32"])
+@pytest.mark.parametrize("act", [gemm.ACT_RELU, gemm.ACT_SILU, gemm.ACT_GELU_TANH, gemm.ACT_GELU_ERF])
+def test_activation_over_its_range(variant, out, act):
+    """With A = B = 0 every row of C is act(bias): the activation alone, over a
+    dense sweep of [-20, 20], magnitudes from 1e-30 to 1e4 of both signs, and the
+    points where e^x leaves fp32's range.  fp32 C stays within 2^-20 |x| of the
+    fp64 value (plus its own rounding); bf16 C within the parity bound."""
+    N = ACT_SWEEP.size
+    N += (-N) % 8
+    bias = np.zeros(N, dtype=np.float32)
+    bias[:ACT_SWEEP.size] = ACT_SWEEP
+    M, K = 130, 64
+    a = torch.zeros(M, K, dtype=torch.bfloat16)
+    b = torch.zeros(N, K, dtype=torch.bfloat16)
+    got = _run(variant, a, b, out, torch.from_numpy(bias), None, act)
+    ref = oracle.epilogue(np.zeros((M, N)), bias, None, act)
+    pre = np.broadcast_to(bias.astype(np.float64), (M, N))
+    r = parity.check_epilogue(got, ref, pre, np.zeros((M, N)), np.zeros((M, N)), out, act)
+    assert r["ok"], r
+    if out == "f32":
+        err = np.abs(got - ref)
+        lim = 2.0 ** -20 * np.abs(pre) + 2.0 ** -24 * np.abs(ref)
+        worst = np.unravel_index(np.argmax(err - lim), err.shape)
+        assert (err <= lim).all(), (pre[worst], got[worst], ref[worst])
