@@ -191,9 +191,13 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
                 "split-K clusters: step 7 tile, plain writeback");
   static_assert(!SK || (!MX && EPI < 0 && SCHED == SCHED_STATIC), "stream-K: plain writeback, static schedule");
   // MX on the pair: a separate warp copies the scales and takes tile ids from the ring
-  // (warp 3 of the leader with one consumer; warp 8 of both CTAs on step 9)
+  // (warp 3 of the leader with one consumer).  On step 9 warp 8 of both CTAs
+  // regroups the B scales and also reads the ring, and one thread (warp 1 of the
+  // leader) issues both consumers' MMAs, each stage's scale copies first.
   constexpr bool MX_COPIER = MX && CG == 2 && !MX9;
-  constexpr uint32_t RING_CONS = Cfg::RING_CONSUMERS + (MX_COPIER ? 1u : 0u) + (MX9 ? (uint32_t)CG : 0u);
+  constexpr uint32_t MMA_THREADS = MX9 ? 1u : (uint32_t)NCONS;  // MMA-issuing threads
+  constexpr uint32_t RING_CONS = Cfg::RING_CONSUMERS - (uint32_t)NCONS + MMA_THREADS + (MX_COPIER ? 1u : 0u) +
+                                 (MX9 ? (uint32_t)CG : 0u);
   // TMEM columns: consumer c's accumulator at c * 256; the per-stage scale slots
   // from MX_TMEM_COL, or on step 9 MX in the two 32-column gaps the 224-column
   // accumulators leave (columns 224-255 and 480-511, two 16-column slots each)
@@ -257,14 +261,14 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(smem_u32(full + s), 1);
-      mbar_init(smem_u32(empty + s), NCONS);
-      if constexpr (MX_COPIER || MX9) mbar_init(smem_u32(sf_ready + s), 1);
+      mbar_init(smem_u32(empty + s), MMA_THREADS);
+      if constexpr (MX_COPIER) mbar_init(smem_u32(sf_ready + s), 1);
       if constexpr (MX9) {
         mbar_init(smem_u32(sf_land + s), 1);
         mbar_init(smem_u32(sf_grouped + s), CG);
       }
     }
-    if constexpr (MX_COPIER || MX9) mbar_init(smem_u32(cp_drain), 1);
+    if constexpr (MX_COPIER) mbar_init(smem_u32(cp_drain), 1);
     if constexpr (KS) mbar_init(smem_u32(red_full), 4u * (uint32_t)ks_n);
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(acc_full + i), 1);
@@ -275,7 +279,7 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
       mbar_init(smem_u32(ring_empty + i), RING_CONS);
     }
     mbar_init(smem_u32(clc_bar), 1);
-    mbar_init(smem_u32(drain_bar), NCONS);
+    mbar_init(smem_u32(drain_bar), MMA_THREADS);
     *abort_flag = 0u;
     *zero_word = 0u;
     fence_mbar_init();
@@ -426,6 +430,19 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
           // (step 9: the scales count on this CTA's own barrier instead)
           const uint32_t mx_tx = MX9 ? 0u : MX ? 3u * MX_BLOCK : 0u;
           if (leader) mbar_arrive_expect_tx(fb, (Cfg::STAGE + mx_tx) * CG);
+          if constexpr (MX9) {
+            // step 9 MX: the scales first, on this CTA's own barrier: A's 128-row
+            // block of each consumer (rows m_cta and m_cta + 256) and the three
+            // 128-row blocks of B from the one holding the tile's first row, so the
+            // regrouping warp works on them while the operands are still landing
+            uint8_t* sd = mx_ring + (size_t)stage * Cfg::MX_BYTES;
+            const uint32_t lb = smem_u32(sf_land + stage);
+            mbar_arrive_expect_tx(lb, 5u * MX_BLOCK);
+#pragma unroll
+            for (int c = 0; c < 2; ++c)
+              tma_load_2d(smem_u32(sd + c * MX_BLOCK), tmSA, lb, 0, 4 * (((m_cta + c * 256) / 128) * KB + kb));
+            tma_load_4d(smem_u32(sd + 2 * MX_BLOCK), tmSB, lb, 0, 0, kb, n_tile / 128);
+          }
           uint8_t* st = ring + (size_t)stage * Cfg::STAGE;
 #pragma unroll
           for (int c = 0; c < NCONS; ++c) {
@@ -464,25 +481,14 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
           } else {
             tma_load_2d_pair(smem_u32(bdst), tmB, mapa_shared(fb, 0), kb * BKE, n_cta);
           }
-          if constexpr (MX) {
+          if constexpr (MX && !MX9) {
             // tiled scale layout: block (row block, K block) at ((row block) * KB + kb) * 512,
             // i.e. rows 4 * block .. 4 * block + 3 of A's 128-byte-wide map, and entry
             // (0, 0, kb, row block) of B's 4-D map (whose boxes span two row blocks).
             // Every extra copy on the pair costs throughput, hence the one B box.
             uint8_t* sd = mx_ring + (size_t)stage * Cfg::MX_BYTES;
             const int32_t ya = 4 * ((m_cta / 128) * KB + kb);
-            if constexpr (MX9) {
-              // A: the 128-row block of each consumer (rows m_cta and m_cta + 256);
-              // B: the three 128-row blocks from the one holding the tile's first row;
-              // all on this CTA's own barrier, which the regrouping warp waits on, so
-              // the scales travel to TMEM while the operands are still landing
-              const uint32_t lb = smem_u32(sf_land + stage);
-              mbar_arrive_expect_tx(lb, 5u * MX_BLOCK);
-#pragma unroll
-              for (int c = 0; c < 2; ++c)
-                tma_load_2d(smem_u32(sd + c * MX_BLOCK), tmSA, lb, 0, 4 * (((m_cta + c * 256) / 128) * KB + kb));
-              tma_load_4d(smem_u32(sd + 2 * MX_BLOCK), tmSB, lb, 0, 0, kb, n_tile / 128);
-            } else if constexpr (CG == 1) {
+            if constexpr (CG == 1) {
               tma_load_2d(smem_u32(sd), tmSA, fb, 0, ya);
               tma_load_4d(smem_u32(sd + MX_BLOCK), tmSB, fb, 0, 0, kb, n_tile / 128);
             } else {
@@ -525,7 +531,68 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
         }
       }
     }
-  } else if ((warp == 1 || (NCONS == 2 && warp == 3)) && leader) {
+  } else if (MX9 && warp == 1 && leader) {
+    // -------------------------------------------------- MMA (step 9 MX)
+    // One thread issues the tcgen05.cp of each stage's scales into the stage's
+    // TMEM slot and then both consumers' MMAs: the tensor pipe runs one thread's
+    // tcgen05 operations in order, so no copy completion has to travel back
+    // through an mbarrier before the MMAs may be issued.  A slot was last read
+    // by MMAs this thread issued S stages earlier.
+    if (lane == 0) {
+      uint32_t g = 0;  // stages issued so far (ring position g % S, phase (g / S) & 1)
+      bool ok = true;
+      auto copy_stage = [&](uint32_t gg) {
+        const uint32_t st = gg % (uint32_t)S;
+        const uint32_t sft = tmem + sf_slot_col(st);
+        const uint32_t sfs = smem_u32(mx_ring + (size_t)st * Cfg::MX_BYTES);
+        tmem_cp_32x128b_x4<CG>(sft, sdesc_rows16(sfs));                      // consumer 0's A rows
+        tmem_cp_32x128b_x4<CG>(sft + 4, sdesc_rows16(sfs + MX_BLOCK));       // consumer 1's A rows
+        tmem_cp_32x128b_x4<CG>(sft + 8, sdesc_rows16(sfs + 5 * MX_BLOCK));   // B rows 0-127
+        tmem_cp_32x128b_x4<CG>(sft + 12, sdesc_rows16(sfs + 6 * MX_BLOCK));  // B rows 128-223
+      };
+      for (uint32_t i = 0; ok; ++i) {
+        int32_t tile;
+        if (!ring_get(i, tile) || tile < 0) break;
+        const uint32_t apar = i & 1u;
+        for (int c = 0; c < 2 && ok; ++c)
+          ok = mbar_wait<true>(smem_u32(acc_empty + c), apar ^ 1u, w, WAIT_MMA_ACC_EMPTY);
+        if (!ok) break;
+        tc_fence_after();
+        const bool rev = k_reversed<false>(i);
+        for (int32_t it = 0; it < KB; ++it, ++g) {
+          const int32_t kb = rev ? KB - 1 - it : it;
+          const uint32_t stage = g % (uint32_t)S, sphase = (g / (uint32_t)S) & 1u;
+          const uint32_t acc0 = (it != 0) ? 1u : 0u;
+          if (!mbar_wait(smem_u32(full + stage), sphase, w, WAIT_MMA_FULL)) { ok = false; break; }
+          // the B scales regrouped in both CTAs
+          if (!mbar_wait<true>(smem_u32(sf_grouped + stage), sphase, w, WAIT_MMA_FULL)) { ok = false; break; }
+          tc_fence_after();
+          copy_stage(g);
+          const uint32_t sft = tmem + sf_slot_col(stage);
+          const uint32_t sb = smem_u32(ring + (size_t)stage * Cfg::STAGE + NCONS * WS_A_BYTES);
+          const uint64_t bd = sdesc_k_sw128(sb);
+          const int32_t rem = p.K - kb * BKE;
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            const uint64_t ad = sdesc_k_sw128(smem_u32(ring + (size_t)stage * Cfg::STAGE + c * WS_A_BYTES));
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              if (k * 32 < rem)
+                mma_mxf8f6f4<CG>(tmem + (uint32_t)c * 256u, ad + 2 * k, bd + 2 * k,
+                                 p.idesc | ((uint32_t)k << 4) | ((uint32_t)k << 29), sft + 4u * (uint32_t)c, sft + 8u,
+                                 acc0 | (uint32_t)k);
+          }
+          mma_commit_pair(smem_u32(empty + stage), 3);
+        }
+        if (!ok) break;
+        for (int c = 0; c < 2; ++c) mma_commit_pair(smem_u32(acc_full + c), 3);
+      }
+      // every MMA and copy this thread issued must be complete before TMEM is released
+      mma_commit_cg<CG>(smem_u32(drain_bar));
+      const WaitCtl wd{zero_word, p.status, p.timeout_ns, 0};
+      mbar_wait(smem_u32(drain_bar), 0, wd, WAIT_DRAIN);
+    }
+  } else if ((warp == 1 || (NCONS == 2 && !MX9 && warp == 3)) && leader) {
     // ------------------------------------------------------------------ MMA
     if (lane == 0) {
       const int cons = (warp == 1) ? 0 : 1;
@@ -555,10 +622,8 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
           const uint32_t acc0 = (it != 0) ? 1u : 0u;  // the segment's first MMA overwrites D
           // MX pair: this stage's scales are in TMEM; the copy warp saw the stage land
           // before copying, so this one wait covers the operands too
-          const uint32_t ready = (MX_COPIER || MX9) ? smem_u32(sf_ready + stage) : smem_u32(full + stage);
+          const uint32_t ready = MX_COPIER ? smem_u32(sf_ready + stage) : smem_u32(full + stage);
           if (!mbar_wait(ready, sphase, w, WAIT_MMA_FULL)) { ok = false; break; }
-          // step 9 MX: the scales were copied on their own; the operands land on `full`
-          if (MX9 && !mbar_wait(smem_u32(full + stage), sphase, w, WAIT_MMA_FULL)) { ok = false; break; }
           tc_fence_after();
           const uint32_t sa = smem_u32(ring + (size_t)stage * Cfg::STAGE + cons * WS_A_BYTES);
           const uint32_t sb = smem_u32(ring + (size_t)stage * Cfg::STAGE + NCONS * WS_A_BYTES);
@@ -568,7 +633,7 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
           const uint64_t astep = a_mn ? 128 : 2, bstep = b_mn ? 128 : 2;
           // four MMAs per stage, each over 32 bytes of K (16 x 16-bit or 32 x 8-bit)
           if constexpr (MX) {
-            if constexpr (!MX_COPIER && !MX9) {
+            if constexpr (!MX_COPIER) {
               // one CTA: the scales precede their MMAs in this thread's issue order
               const uint32_t sft0 = tmem + MX_TMEM_COL + stage * MX_TMEM_SLOT;
               const uint32_t sfs = smem_u32(mx_ring + (size_t)stage * Cfg::MX_BYTES);
@@ -577,8 +642,7 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
               tmem_cp_32x128b_x4<CG>(sft0 + 8, sdesc_rows16(sfs + 2 * MX_BLOCK));
             }
             const uint32_t sft = tmem + sf_slot_col(stage);
-            // A scales: 4 columns (step 9: 4 per consumer), then B's
-            const uint32_t sfa = sft + (MX9 ? 4u * (uint32_t)cons : 0u), sfb = sft + (MX9 ? 8u : 4u);
+            const uint32_t sfa = sft, sfb = sft + 4u;  // A scales: 4 columns, then B's
             // byte k of each scale word belongs to the k-th 32-element K block; blocks
             // wholly past K are not issued (their scale bytes are padding)
             const int32_t rem = p.K - kb * BKE;
@@ -643,7 +707,7 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
       mbar_wait(smem_u32(cp_drain), 0, wd, WAIT_DRAIN);
     }
   } else if (MX9 && warp == 8) {
-    // ------------------------------- B scale regrouping and scale copies (step 9 MX)
+    // ------------------------------------------- B scale regrouping (step 9 MX)
     // The tile's 224 B rows start at a multiple of 32 but not of 128, so their
     // scales, loaded as the three 128-row blocks that hold them, are regrouped into
     // the two blocks of 128 rows the MMA reads: in the tiled layout a block holds
@@ -651,27 +715,11 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
     // 32 j + l, so 32-row group G of the tile (global group 7 tn + G) moves from
     // word (7 tn + G) % 4 of loaded block (7 tn + G) / 4 - (7 tn) / 4 to word G % 4
     // of block G / 4; lane l moves row l of every group, and group 7 (rows 224-255,
-    // outside the tile) is zeroed.  Both CTAs regroup their own copy and arrive on
-    // the leader's barrier.  The leader's lane 0 copies a stage's four blocks into
-    // the TMEM slot of both CTAs one stage later, after regrouping the next, so
-    // the other CTA's arrival has a stage's time to travel instead of holding up
-    // every stage; the MMA warps wait for the copies and, separately, the operands.
+    // outside the tile) is zeroed.  Both CTAs regroup their own copy (the copies
+    // into TMEM read each CTA's shared memory) and arrive on the leader's barrier,
+    // which the MMA thread waits on before it copies the stage's scales.
     uint32_t stage = 0, sphase = 0;
-    bool ok = true, pending = false;
-    uint32_t pstage = 0, pphase = 0;
-    // the copies of the stage regrouped last: the leader's lane 0 only
-    auto copy_scales = [&](uint32_t st, uint32_t ph) -> bool {
-      if (!mbar_wait<true>(smem_u32(sf_grouped + st), ph, w, WAIT_MMA_FULL)) return false;
-      tc_fence_after();
-      const uint32_t sft = tmem + sf_slot_col(st);
-      const uint32_t sfs = smem_u32(mx_ring + (size_t)st * Cfg::MX_BYTES);
-      tmem_cp_32x128b_x4<CG>(sft, sdesc_rows16(sfs));                      // consumer 0's A rows
-      tmem_cp_32x128b_x4<CG>(sft + 4, sdesc_rows16(sfs + MX_BLOCK));       // consumer 1's A rows
-      tmem_cp_32x128b_x4<CG>(sft + 8, sdesc_rows16(sfs + 5 * MX_BLOCK));   // B rows 0-127
-      tmem_cp_32x128b_x4<CG>(sft + 12, sdesc_rows16(sfs + 6 * MX_BLOCK));  // B rows 128-223
-      mma_commit_cg<CG>(smem_u32(sf_ready + st));
-      return true;
-    };
+    bool ok = true;
     for (uint32_t i = 0; ok; ++i) {
       int32_t tile = -1;
       uint32_t okr = 1;
@@ -710,25 +758,8 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
             mbar_arrive_cluster(mapa_shared(smem_u32(sf_grouped + stage), 0));
           }
         }
-        if (leader && lane == 0) {
-          // the TMEM slot of a stage was last read by MMAs that completed before this
-          // stage's loads were issued
-          if (pending && !copy_scales(pstage, pphase)) ok = false;
-          pending = true;
-          pstage = stage;
-          pphase = sphase;
-        }
-        ok = __shfl_sync(0xffffffffu, ok ? 1u : 0u, 0) != 0u;
-        if (!ok) break;
         if (++stage == (uint32_t)S) { stage = 0; sphase ^= 1u; }
       }
-    }
-    if (leader && lane == 0) {
-      if (ok && pending) copy_scales(pstage, pphase);
-      // the copies this thread issued must be complete before TMEM is released
-      mma_commit_cg<CG>(smem_u32(cp_drain));
-      const WaitCtl wd{zero_word, p.status, p.timeout_ns, 0};
-      mbar_wait(smem_u32(cp_drain), 0, wd, WAIT_DRAIN);
     }
   } else if (warp >= 4 && warp < 8) {
     // ------------------------------------------------------------ writeback
