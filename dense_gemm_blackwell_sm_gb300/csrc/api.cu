@@ -2,6 +2,7 @@
 // picks a kernel variant / tile / ring depth / raster / launch size, TMA
 // descriptor encoding and caching, launches, and device-status checks.
 #include <algorithm>
+#include <vector>
 #include <cstdio>
 #include <cstring>
 #include <map>
@@ -26,6 +27,7 @@ struct gemm_plan_s {
   bool in_f8, in_e5m2;  // 8-bit float inputs (E4M3 or E5M2)
   bool in_mx;           // ... with MX block scales (gemm_plan_run_mx)
   int variant, sched, stages, raster_group;
+  int wide_cols = 0, wide_n = 0, narrow_n = 0;  // two tile widths (224-column step 9), see KParams
   int device, num_sms;
   int grid_units;  // CTAs (variants 3-6) or clusters (7-9) launched
   int split_k;     // GEMV_TC: requested CTAs per 128-row block along K (0 = automatic)
@@ -247,6 +249,44 @@ int choose_variant(int64_t M, int64_t N, int64_t K, gemm_dtype_t dt, int sms, in
   return v;
 }
 
+// Step 9's 224-column tiles with the static schedule: when N (a multiple of 16)
+// lies between 13 and 14 sixteen-column units per tile column, give the first
+// columns 224 and the rest 208 so that they add up to N exactly, if that lowers
+// the widest total any cluster gets (the clusters take tiles t, t + units, ... of
+// the raster order).  4096^3: 19 tile columns, 9 of 224 and 10 of 208; every CTA
+// pair then runs one of each, 432 columns instead of 448.
+void raster_tile_host(int32_t tile, int32_t tiles_m, int32_t tiles_n, int32_t group, int32_t& tm, int32_t& tn) {
+  const int32_t per_group = group * tiles_n;
+  const int32_t g = tile / per_group;
+  const int32_t first_m = g * group;
+  const int32_t rows = std::min(group, tiles_m - first_m);
+  const int32_t r = tile - g * per_group;
+  tm = first_m + r % rows;
+  tn = r / rows;
+}
+void balance_tile_widths(gemm_plan_s* p) {
+  p->wide_cols = p->wide_n = p->narrow_n = 0;
+  if (p->sched != GEMM_SCHED_STATIC || p->N % 16 != 0 || p->grid_units < 1) return;
+  const int64_t T = p->tiles_n, units16 = p->N / 16;
+  if (units16 < 13 * T || units16 >= 14 * T) return;
+  const int wide_cols = (int)(units16 - 13 * T);  // columns of 224, the others 208
+  auto widest = [&](bool two_widths) {
+    std::vector<int64_t> load((size_t)p->grid_units, 0);
+    const int64_t tiles = (int64_t)p->tiles_m * p->tiles_n;
+    for (int64_t t = 0; t < tiles; ++t) {
+      int32_t tm, tn;
+      raster_tile_host((int32_t)t, p->tiles_m, p->tiles_n, p->raster_group, tm, tn);
+      load[(size_t)(t % p->grid_units)] += (two_widths && tn >= wide_cols) ? 208 : 224;
+    }
+    return *std::max_element(load.begin(), load.end());
+  };
+  if (widest(true) < widest(false)) {
+    p->wide_cols = wide_cols;
+    p->wide_n = 224;
+    p->narrow_n = 208;
+  }
+}
+
 // Fix the kernel, its launch shape and its pointer-independent parameters.
 gemm_status_t prepare_launch(gemm_plan_s* p) {
   cudaError_t e = cudaSuccess;
@@ -270,6 +310,9 @@ gemm_status_t prepare_launch(gemm_plan_s* p) {
     k.tiles_m = p->tiles_m;
     k.tiles_n = p->tiles_n;
     k.raster_group = p->raster_group;
+    k.wide_cols = p->wide_cols;
+    k.wide_n = p->wide_n;
+    k.narrow_n = p->narrow_n;
     k.stages = p->stages;
     k.timeout_ns = p->timeout_ns;
     k.debug_flags = p->debug_flags;
@@ -509,6 +552,7 @@ gemm_status_t build_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, co
       const int64_t kb = (K + (p->in_f8 ? 128 : 64) - 1) / (p->in_f8 ? 128 : 64);
       p->grid_units = (int)std::max<int64_t>(1, std::min<int64_t>(active, (int64_t)tiles * kb / 4));
     }
+    if (p->tile_n == 224 && !p->in_mx) balance_tile_widths(p);
   } else {
     p->grid_units = tiles;
   }
@@ -1032,6 +1076,8 @@ gemm_status_t gemm_plan_info(gemm_plan_t p, gemm_plan_info_t* info) {
   info->smem_bytes = (int32_t)p->spec.smem;
   info->num_sms = p->num_sms;
   info->tiles = p->tiles_m * p->tiles_n;
+  info->narrow_tile_n = p->narrow_n;
+  info->wide_cols = p->wide_cols;
   return GEMM_OK;
 }
 

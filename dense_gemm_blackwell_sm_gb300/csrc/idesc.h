@@ -9,6 +9,12 @@
 
 #include <cstdint>
 
+#if defined(__CUDACC__)
+#define DGB_HD __host__ __device__
+#else
+#define DGB_HD
+#endif
+
 namespace dgb {
 
 // fields common to the three kinds
@@ -40,6 +46,8 @@ inline uint32_t idesc_mx(bool e5m2, int M, int N) {
 }
 
 // the same descriptor with another N
-inline uint32_t idesc_with_n(uint32_t idesc, int N) { return (idesc & ~IDESC_N_MASK) | ((uint32_t)(N >> 3) << 17); }
+DGB_HD inline uint32_t idesc_with_n(uint32_t idesc, int N) {
+  return (idesc & ~IDESC_N_MASK) | ((uint32_t)(N >> 3) << 17);
+}
 
 }  // namespace dgb

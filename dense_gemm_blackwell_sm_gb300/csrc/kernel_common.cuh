@@ -65,6 +65,11 @@ struct KParams {
   // writeback warp of each slot (zero between launches)
   float* sk_ws;
   uint32_t* sk_flags;
+  // step 9's 224-column tile kernel: tile columns 0 .. wide_cols-1 are wide_n wide,
+  // the rest narrow_n (both multiples of 16, at most the kernel's tile width), so
+  // that the CTA pairs' tiles add up to nearly the same width; narrow_n = 0: every
+  // tile column is the kernel's full width
+  int32_t wide_cols, wide_n, narrow_n;
 };
 
 constexpr uint32_t LAYOUT_A_MN = 1u;
@@ -231,6 +236,21 @@ __device__ __forceinline__ void apply_epilogue32(uint32_t* v, const KParams& p, 
   }
 #pragma unroll
   for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(x[j]);
+}
+
+// First column and width of tile column tn: bn wide, or (balanced widths, see
+// KParams) wide_n / narrow_n wide.
+__device__ __forceinline__ void tile_columns(const KParams& p, int32_t tn, int32_t bn, int32_t& c0, int32_t& w) {
+  if (p.narrow_n == 0) {
+    c0 = tn * bn;
+    w = bn;
+  } else if (tn < p.wide_cols) {
+    c0 = tn * p.wide_n;
+    w = p.wide_n;
+  } else {
+    c0 = p.wide_cols * p.wide_n + (tn - p.wide_cols) * p.narrow_n;
+    w = p.narrow_n;
+  }
 }
 
 // Grouped (L2-aware) raster order: consecutive tile ids walk down a group of

@@ -83,6 +83,7 @@
 // issues MMAs, and its commits arrive on the barriers of both CTAs.  No load is
 // multicast.  Every wait is bounded (see ptx.cuh).
 #pragma once
+#include "idesc.h"
 #include "kernel_common.cuh"
 #include "launch.h"
 
@@ -218,6 +219,16 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
   // the same for fp32 C on step 9's 224-column tile: two chunks into the staging
   // buffers, the other five into registers
   constexpr bool DRAIN32 = CG == 2 && NCONS == 2 && !SK && !MX && BN == 224 && CW == 32 && EPI < 0;
+  // the 224-column kernel may run tiles of two widths (KParams wide_n / narrow_n)
+  constexpr bool BAL = BN != WS_BN && !MX;
+  auto tile_cols = [&](int32_t tn, int32_t& c0, int32_t& width) {
+    if constexpr (BAL) {
+      tile_columns(p, tn, BN, c0, width);
+    } else {
+      c0 = tn * BN;
+      width = BN;
+    }
+  };
   // fused epilogue on step 9: each consumer's single accumulator is held while
   // the epilogue runs, so the rows are stored straight from registers (no wait
   // for a staging buffer inside that window), and the staging buffers hold the
@@ -418,7 +429,10 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
         int32_t tm, tn;
         raster_tile(tile, p.tiles_m, p.tiles_n, p.raster_group, tm, tn);
         const int32_t m_cta = tm * Cfg::TILE_M + (int32_t)rank * 128;
-        const int32_t n_cta = tn * BN + (CG == 2 ? (int32_t)rank * (BN / 2) : 0);
+        int32_t tc0, tw;
+        tile_cols(tn, tc0, tw);
+        // the pair's second CTA holds the tile's second half of B rows
+        const int32_t n_cta = tc0 + (CG == 2 ? (int32_t)rank * (tw / 2) : 0);
         const bool rev = k_reversed<SK || KS>(i);
         for (int32_t it = 0; it < kb1 - kb0; ++it) {
           const int32_t kb = rev ? kb1 - 1 - it : kb0 + it;
@@ -612,6 +626,14 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
         }
         const uint32_t slot = (NCONS == 2) ? (uint32_t)cons : MX ? 0u : (i & 1u);
         const uint32_t apar = (MX || NCONS == 2) ? (i & 1u) : ((i >> 1) & 1u);
+        uint32_t idesc = p.idesc;
+        if constexpr (BAL) {
+          // this tile's width as the MMA's N
+          int32_t tm, tn, tc0, tw;
+          raster_tile(tile, p.tiles_m, p.tiles_n, p.raster_group, tm, tn);
+          tile_cols(tn, tc0, tw);
+          if (tw != BN) idesc = idesc_with_n(p.idesc, tw);
+        }
         if (!mbar_wait<CG == 2>(smem_u32(acc_empty + slot), apar ^ 1u, w, WAIT_MMA_ACC_EMPTY)) break;
         tc_fence_after();
         const uint32_t d = tmem + slot * 256u;
@@ -654,11 +676,11 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
           } else if (f8) {
 #pragma unroll
             for (int k = 0; k < 4; ++k)
-              mma_f8f6f4<CG>(d, ad + astep * k, bd + bstep * k, p.idesc, acc0 | (uint32_t)k);
+              mma_f8f6f4<CG>(d, ad + astep * k, bd + bstep * k, idesc, acc0 | (uint32_t)k);
           } else {
 #pragma unroll
             for (int k = 0; k < 4; ++k)
-              mma_f16<CG>(d, ad + astep * k, bd + bstep * k, p.idesc, acc0 | (uint32_t)k);
+              mma_f16<CG>(d, ad + astep * k, bd + bstep * k, idesc, acc0 | (uint32_t)k);
           }
           if constexpr (CG == 1) {
             mma_commit(smem_u32(empty + stage));
@@ -796,7 +818,8 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
         const uint32_t slot = (NCONS == 2) ? (uint32_t)cons : MX ? 0u : (i & 1u);
         const uint32_t apar = (MX || NCONS == 2) ? (i & 1u) : ((i >> 1) & 1u);
         const int32_t row0 = tm * Cfg::TILE_M + cons * 128 * CG + (int32_t)rank * 128 + (int32_t)q * 32;
-        const int32_t col_base = tn * BN;
+        int32_t col_base, tile_w;
+        tile_cols(tn, col_base, tile_w);
         // fused epilogue: while the MMAs still run, read the first chunk of the
         // lane's residual row segment and scale_a, and have L2 fetch the rest of
         // the segment, so the held accumulator waits on no DRAM round trip
@@ -954,6 +977,19 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
           }
 #pragma unroll
           for (int ch = 2; ch < NCH; ++ch) {
+            if (ch * 32 + 32 > tile_w) {
+              // a narrow tile's last 16 columns (208 = 6 x 32 + 16): straight from
+              // registers, so no store reaches into the next tile's columns
+              const int32_t row = row0 + (int32_t)lane, col = col_base + ch * 32;
+              if (ch * 32 < tile_w && row < p.M) {
+                uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<OutT*>(p.C) + (int64_t)row * p.out_ld + col);
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                  if (col + 4 * j < p.N)
+                    dst[j] = make_uint4(r[ch - 2][4 * j], r[ch - 2][4 * j + 1], r[ch - 2][4 * j + 2], r[ch - 2][4 * j + 3]);
+              }
+              continue;
+            }
             uint8_t* buf = my_staging + (ch & 1) * 4096;
             if (lane == 0) bulk_wait_group_read<1>();  // the store issued from `buf` two chunks ago is done reading
             __syncwarp();
@@ -1028,14 +1064,15 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
             ++tog;
           }
           if constexpr (TAIL > 0) {
-            // straight from registers to C: 64 bytes of the lane's row (N % 8 == 0, so each
-            // 8-column group is wholly in or out)
+            // straight from registers to C: 64 bytes of the lane's row, 32 bytes in a
+            // 208-column tile (N % 8 == 0, so each 8-column group is wholly in or out)
             const int32_t row = row0 + (int32_t)lane, col = col_base + NCH * CW;
+            const int32_t col_end = min(p.N, col_base + tile_w);
             if (row < p.M) {
               uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<OutT*>(p.C) + (int64_t)row * p.out_ld + col);
 #pragma unroll
               for (int j = 0; j < 4; ++j)
-                if (col + 8 * j < p.N) dst[j] = make_uint4(pt[4 * j], pt[4 * j + 1], pt[4 * j + 2], pt[4 * j + 3]);
+                if (col + 8 * j < col_end) dst[j] = make_uint4(pt[4 * j], pt[4 * j + 1], pt[4 * j + 2], pt[4 * j + 3]);
             }
           }
           continue;

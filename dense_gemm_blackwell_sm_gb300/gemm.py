@@ -60,7 +60,8 @@ class Opts(ctypes.Structure):
 
 class PlanInfo(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in ("variant", "sched", "stages", "raster_group", "tile_m", "tile_n",
-                                              "cluster", "consumers", "grid", "smem_bytes", "num_sms", "tiles")]
+                                              "cluster", "consumers", "grid", "smem_bytes", "num_sms", "tiles",
+                                              "narrow_tile_n", "wide_cols")]
 
     def as_dict(self) -> dict:
         d = {n: int(getattr(self, n)) for n, _ in self._fields_}

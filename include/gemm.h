@@ -162,6 +162,10 @@ typedef struct {
   int32_t smem_bytes;      /* dynamic shared memory per CTA */
   int32_t num_sms;
   int32_t tiles;           /* output tiles (cluster tiles for variants 8-9) */
+  int32_t narrow_tile_n;   /* variant 9 with tile_n 224: 0, or the width (208) of the tile
+                              columns after the first wide_cols, chosen when the two widths
+                              add up to N and even out the CTA pairs' work */
+  int32_t wide_cols;
 } gemm_plan_info_t;
 
 /* The kernel variant the automatic plan (opts.variant = 0, K-major operands)

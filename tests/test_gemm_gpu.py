@@ -378,8 +378,12 @@ def test_stream_k_is_the_default_when_the_last_wave_is_short():
 
 
 # step 9 with 224-column tiles: chosen when they finish the waves of CTA pairs sooner;
-# N = 18 * 224 + 200 puts the edge inside the last 32-column band of the last tile
-NARROW = [(4096, 4232, 200), (4096, 4096, 136)]
+# N = 18 * 224 + 200 puts the edge inside the last 32-column band of the last tile.
+# N = 4096 and 4080 (multiples of 16, 13-14 sixteen-column units per tile column) run
+# 224- and 208-column tiles: 9 wide columns and 10 narrow, 8 and 11; M = 4000 leaves
+# the last row of tiles ragged
+NARROW = [(4096, 4232, 200), (4096, 4096, 136), (4000, 4080, 200)]
+NARROW_TWO_WIDTHS = {4096: 9, 4080: 8}
 
 
 @pytest.mark.parametrize("shape", NARROW)
@@ -390,6 +394,10 @@ def test_narrow_tiles_integer_bit_exact(shape, ti, to):
     plan = gemm.Plan(M, N, K, gemm.dtype_code(ti, to), gemm.make_opts(variant=gemm.S9))
     info = plan.info()
     assert info["variant"] == gemm.S9 and info["tile_n"] == 224, info
+    if N in NARROW_TWO_WIDTHS:
+        assert info["narrow_tile_n"] == 208 and info["wide_cols"] == NARROW_TWO_WIDTHS[N], info
+    else:
+        assert info["narrow_tile_n"] == 0, info
     c = torch.full((M, N), float("nan"), device=DEV, dtype=inputs.torch_dtype(to))
     plan.run(a.to(DEV), b.to(DEV), c)
     assert plan.check() == gemm.OK
