@@ -122,11 +122,24 @@ __device__ __forceinline__ float epi_activation(float x) {
 // 32 fp32 columns) into 32 words, zero for 16-byte groups past column N (C's
 // rows are 16-byte multiples, so each group lies wholly inside or outside C).
 // The caller checks row < M.
+// With v8 (the row segment 32-byte aligned and 32-column groups wholly inside
+// or outside C, which the caller checks) the loads are 32 bytes wide.
 template <typename OutT>
-__device__ __forceinline__ void load_residual128(uint32_t (&r)[32], const KParams& p, int32_t row, int32_t col0) {
+__device__ __forceinline__ void load_residual128(uint32_t (&r)[32], const KParams& p, int32_t row, int32_t col0,
+                                                 bool v8 = false) {
   constexpr int per16 = 16 / (int)sizeof(OutT);
   const uint4* src =
       reinterpret_cast<const uint4*>(reinterpret_cast<const OutT*>(p.residual) + (int64_t)row * p.out_ld + col0);
+  if (v8) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      uint32_t t[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+      if (col0 + 2 * per16 * j < p.N) ld_global_v8(src + 2 * j, t);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) r[8 * j + e] = t[e];
+    }
+    return;
+  }
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
     const uint4 u = (col0 + per16 * j < p.N) ? __ldg(src + j) : make_uint4(0u, 0u, 0u, 0u);

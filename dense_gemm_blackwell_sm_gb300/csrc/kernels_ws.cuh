@@ -826,11 +826,17 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
         uint32_t res_next[EPI >= 0 ? 32 : 1];
         float epi_sa = 1.f;
         bool epi_res = false;
+        // 32-byte row accesses when C's and the residual's rows allow them (32-byte
+        // aligned and N a multiple of 16 columns, so a 32-byte group lies wholly
+        // inside C or outside)
+        const bool v8_rows = EPI_DIRECT && (p.N % 16 == 0) &&
+                             (((reinterpret_cast<uintptr_t>(p.C) | reinterpret_cast<uintptr_t>(p.residual) |
+                                (uintptr_t)((int64_t)p.out_ld * (int64_t)sizeof(OutT))) & 31u) == 0);
         if constexpr (EPI >= 0) {
           const int32_t row = row0 + (int32_t)lane;
           epi_res = p.residual != nullptr && row < p.M;
           if (epi_res) {
-            load_residual128<OutT>(res_next, p, row, col_base);
+            load_residual128<OutT>(res_next, p, row, col_base, v8_rows);
             const uint8_t* seg = reinterpret_cast<const uint8_t*>(reinterpret_cast<const OutT*>(p.residual) +
                                                                   (int64_t)row * p.out_ld + col_base);
             const int32_t seg_bytes = min(BN, p.N - col_base) * (int32_t)sizeof(OutT);
@@ -1087,7 +1093,8 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
               // this chunk's residual, and the next chunk's on its way
 #pragma unroll
               for (int j = 0; j < 32; ++j) res[j] = res_next[j];
-              if (epi_res && ch + 1 < NCH) load_residual128<OutT>(res_next, p, row0 + (int32_t)lane, col_base + (ch + 1) * CW);
+              if (epi_res && ch + 1 < NCH)
+                load_residual128<OutT>(res_next, p, row0 + (int32_t)lane, col_base + (ch + 1) * CW, v8_rows);
             }
             tmem_ld_32x32b_x32(tbase + (uint32_t)(ch * CW), v0);
             if constexpr (CW == 64) tmem_ld_32x32b_x32(tbase + (uint32_t)(ch * CW + 32), v1);
@@ -1127,17 +1134,26 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
               if (row < p.M) {
                 uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<OutT*>(p.C) + (int64_t)row * p.out_ld + col0);
                 constexpr int per16 = 16 / (int)sizeof(OutT);
+                uint32_t o[32];  // the row's 128 bytes as C's type
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
-                  uint4 val;
                   if constexpr (CW == 32) {
-                    val = make_uint4(v0[4 * j], v0[4 * j + 1], v0[4 * j + 2], v0[4 * j + 3]);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) o[4 * j + e] = v0[4 * j + e];
                   } else {
                     const uint32_t* src = (j < 4) ? (v0 + 8 * j) : (v1 + 8 * (j - 4));
-                    val = make_uint4(pack_bf16x2(src[0], src[1]), pack_bf16x2(src[2], src[3]),
-                                     pack_bf16x2(src[4], src[5]), pack_bf16x2(src[6], src[7]));
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) o[4 * j + e] = pack_bf16x2(src[2 * e], src[2 * e + 1]);
                   }
-                  if (col0 + per16 * j < p.N) dst[j] = val;
+                }
+                if (v8_rows) {
+#pragma unroll
+                  for (int j = 0; j < 4; ++j)
+                    if (col0 + 2 * per16 * j < p.N) st_global_v8(dst + 2 * j, o + 8 * j);
+                } else {
+#pragma unroll
+                  for (int j = 0; j < 8; ++j)
+                    if (col0 + per16 * j < p.N) dst[j] = make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
                 }
               }
               continue;

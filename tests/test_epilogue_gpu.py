@@ -134,3 +134,22 @@ def test_activation_over_its_range(variant, out, act):
         lim = 2.0 ** -20 * np.abs(pre) + 2.0 ** -24 * np.abs(ref)
         worst = np.unravel_index(np.argmax(err - lim), err.shape)
         assert (err <= lim).all(), (pre[worst], got[worst], ref[worst])
+
+
+@pytest.mark.parametrize("out,act,alias", [("bf16", gemm.ACT_RELU, False), ("bf16", gemm.ACT_RELU, True),
+                                           ("f32", gemm.ACT_NONE, False)])
+def test_step9_epilogue_with_32_byte_rows(out, act, alias):
+    """N a multiple of 16 and 32-byte aligned rows: step 9's fused writeback then
+    reads the residual and writes C 32 bytes per lane and access.  Integer inputs,
+    bias and residual: bit-exact, including the last, ragged row tile and the
+    residual given as C itself."""
+    M, N, K = 1040, 2064, 200
+    a, b = inputs.integer_operands(M, N, K, "bf16", seed=77)
+    g = torch.Generator().manual_seed(77)
+    bias = torch.randint(-20, 21, (N,), generator=g).float()
+    res = torch.randint(-8, 9, (M, N), generator=g).to(inputs.torch_dtype(out))
+    C, _ = oracle.gemm(a, b)
+    exp = torch.tensor(oracle.epilogue(C, bias, res, act)).to(inputs.torch_dtype(out)).double().numpy()
+    got = _run(gemm.S9, a, b, out, bias, res, act, alias=alias)
+    bad = np.argwhere(got != exp)
+    assert bad.size == 0, (bad[:3], got[tuple(bad[0])], exp[tuple(bad[0])])
