@@ -290,11 +290,17 @@ def bench_gemm_e2e(w: inputs.Workload, steps: int, dev) -> dict:
             raise gemm.GemmError(st, "gemm_run_host")
 
     once()
-    t0 = time.perf_counter()
-    for _ in range(steps):
-        once()   # synchronises the stream itself
-    secs = time.perf_counter() - t0
+    # three timed windows of `steps` steps; the median window is reported (one window
+    # alone has shown a host hiccup of ~10 ms inflating a 1.6 ms step by 65 %)
+    windows = []
+    for _ in range(3):
+        t0 = time.perf_counter()
+        for _ in range(steps):
+            once()   # synchronises the stream itself
+        windows.append(time.perf_counter() - t0)
+    secs = sorted(windows)[1]
     return {"seconds": secs, "steps": steps, "h2d": ib * (w.M * w.K + w.N * w.K), "d2h": ob * w.M * w.N,
+            "window_ms_per_step": [round(x / steps * 1e3, 3) for x in windows],
             "copy_only": copy_ceiling(dev, [(ah, da), (bh, db)], [(ch, dc)])}
 
 
@@ -345,13 +351,16 @@ def _bench_mx_e2e(w, a, b, code, steps, dev, ib, ob) -> dict:
         torch.cuda.synchronize(dev)
 
     once()
-    t0 = time.perf_counter()
-    for _ in range(steps):
-        once()
-    secs = time.perf_counter() - t0
+    windows = []  # as in bench_gemm_e2e: the median of three timed windows
+    for _ in range(3):
+        t0 = time.perf_counter()
+        for _ in range(steps):
+            once()
+        windows.append(time.perf_counter() - t0)
+    secs = sorted(windows)[1]
     plan.destroy()
     return {"seconds": secs, "steps": steps, "h2d": sum(x.numel() * x.element_size() for x in host),
-            "d2h": ob * w.M * w.N}
+            "d2h": ob * w.M * w.N, "window_ms_per_step": [round(x / steps * 1e3, 3) for x in windows]}
 
 
 def bench_gemv(w: inputs.Workload, steps: int, warmup: int, dev, flags: int = 0, variant: int = 0) -> dict:
@@ -649,6 +658,9 @@ def main(argv=None):
         line["e2e"] = {"value": round(w.flops * e["steps"] / e["seconds"] / 1e12, 3), "unit": "TFLOP/s",
                        "h2d_bytes_per_step": e["h2d"], "d2h_bytes_per_step": e["d2h"],
                        "ms_per_step": round(e["seconds"] / e["steps"] * 1e3, 3)}
+        if e.get("window_ms_per_step"):
+            line["e2e"]["timing"] = "median of 3 windows of %d steps" % e["steps"]
+            line["e2e"]["window_ms_per_step"] = e["window_ms_per_step"]
         if e.get("copy_only"):
             c = e["copy_only"]
             # the step can finish no sooner than its copies alone (both directions at once)
