@@ -159,6 +159,37 @@ __device__ __forceinline__ void stage_columns(float* dst, const float* v, int32_
   for (int j = (int)lane; j < BN; j += 32) dst[j] = (col0 + j < N) ? __ldg(v + col0 + j) : 0.f;
 }
 
+// The residual of 32 columns of row `row` from column col0 (64 bytes of bf16 or 128
+// of fp32) into r (16 or 32 words), 0 for 16-byte groups past column N; with v8 in
+// 32-byte loads (the caller checks that rows are 32-byte aligned and N a multiple
+// of 16).  The caller checks row < M.
+template <typename OutT>
+__device__ __forceinline__ void load_residual_cols32(uint32_t* r, const KParams& p, int32_t row, int32_t col0,
+                                                     bool v8) {
+  constexpr int per16 = 16 / (int)sizeof(OutT);  // columns per 16 bytes
+  constexpr int NQ = 32 / per16;                 // 16-byte groups: 4 (bf16) or 8 (fp32)
+  const uint4* src =
+      reinterpret_cast<const uint4*>(reinterpret_cast<const OutT*>(p.residual) + (int64_t)row * p.out_ld + col0);
+  if (v8) {
+#pragma unroll
+    for (int j = 0; j < NQ / 2; ++j) {
+      uint32_t t[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+      if (col0 + 2 * per16 * j < p.N) ld_global_v8(src + 2 * j, t);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) r[8 * j + e] = t[e];
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < NQ; ++j) {
+      const uint4 u = (col0 + per16 * j < p.N) ? __ldg(src + j) : make_uint4(0u, 0u, 0u, 0u);
+      r[4 * j] = u.x;
+      r[4 * j + 1] = u.y;
+      r[4 * j + 2] = u.z;
+      r[4 * j + 3] = u.w;
+    }
+  }
+}
+
 // Applies the fused epilogue to 32 consecutive fp32 accumulator values of one
 // row (columns col0 .. col0+31), in place:
 //   x = act(acc * sa * scale_b[col] + bias[col]) + residual,

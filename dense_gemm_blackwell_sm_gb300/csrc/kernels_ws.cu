@@ -144,7 +144,7 @@ cudaError_t spec_ws(int cg, int consumers, int sched, bool out_f32, int stages, 
   if (e != cudaSuccess) return e;
   out->func = k;
   out->grid = dim3((unsigned)(clusters * cg), 1, 1);
-  out->block = dim3(WS_THREADS, 1, 1);
+  out->block = dim3((unsigned)ws_threads(consumers, fused_act), 1, 1);
   out->smem = smem;
   out->cluster = (unsigned)cg;
   out->kind = ARGS_ABC_K;

@@ -94,6 +94,9 @@ namespace {
 enum SchedWs { SCHED_STATIC = 0, SCHED_ATOMIC = 1, SCHED_CLC = 2, SCHED_STREAM_K = 3 };
 
 constexpr int WS_THREADS = 256;
+// step 9's fused-epilogue kernels have four writeback warps per consumer, so that both
+// accumulators get their epilogue at the same time: 12 warps
+__host__ __device__ constexpr int ws_threads(int ncons, int epi) { return (ncons == 2 && epi >= 0) ? 384 : WS_THREADS; }
 constexpr int WS_BN = 256;          // tile columns (MMA N)
 constexpr uint32_t WS_A_BYTES = 128u * 128u;  // 128 rows x 128 B
 constexpr int WS_RING = 4;          // depth of the tile-id ring
@@ -197,8 +200,11 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
   // leader) issues both consumers' MMAs, each stage's scale copies first.
   constexpr bool MX_COPIER = MX && CG == 2 && !MX9;
   constexpr uint32_t MMA_THREADS = MX9 ? 1u : (uint32_t)NCONS;  // MMA-issuing threads
+  // step 9 with a fused epilogue: eight writeback warps, four per consumer (see below)
+  constexpr bool WB8 = EPI >= 0 && NCONS == 2 && CG == 2 && !MX && !SK && !KS && BN == WS_BN;
+  static_assert(ws_threads(NCONS, EPI) == (WB8 ? 384 : WS_THREADS) || MX, "thread count of the fused step-9 kernels");
   constexpr uint32_t RING_CONS = Cfg::RING_CONSUMERS - (uint32_t)NCONS + MMA_THREADS + (MX_COPIER ? 1u : 0u) +
-                                 (MX9 ? (uint32_t)CG : 0u);
+                                 (MX9 ? (uint32_t)CG : 0u) + (WB8 ? 4u * (uint32_t)CG : 0u);
   // TMEM columns: consumer c's accumulator at c * 256; the per-stage scale slots
   // from MX_TMEM_COL, or on step 9 MX in the two 32-column gaps the 224-column
   // accumulators leave (columns 224-255 and 480-511, two 16-column slots each)
@@ -233,8 +239,8 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
   // the epilogue runs, so the rows are stored straight from registers (no wait
   // for a staging buffer inside that window), and the staging buffers hold the
   // tile's bias and scale_b columns instead
-  constexpr bool EPI_DIRECT = EPI >= 0 && NCONS == 2 && !MX && !SK && !KS && BN == WS_BN;
-  static_assert(!EPI_DIRECT || WS_STAGING / 4 >= 2 * WS_BN * 4, "a warp's staging holds two column vectors");
+  constexpr bool EPI_DIRECT = WB8;
+  static_assert(!EPI_DIRECT || WS_STAGING / 8 >= 2 * WS_BN * 4, "a warp's staging holds two column vectors");
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align_1024(smem_raw);
@@ -783,10 +789,13 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
         if (++stage == (uint32_t)S) { stage = 0; sphase ^= 1u; }
       }
     }
-  } else if (warp >= 4 && warp < 8) {
+  } else if (warp >= 4 && warp < (WB8 ? 12u : 8u)) {
     // ------------------------------------------------------------ writeback
     const uint32_t q = warp & 3u;  // TMEM lane quarter this warp may access
-    uint8_t* my_staging = staging + q * WARP_STAGING;
+    // step 9 with a fused epilogue: warps 4-7 serve consumer 0 and warps 8-11
+    // consumer 1, each with a quarter of the staging space of its own
+    const int my_cons = WB8 ? (int)((warp - 4u) >> 2) : -1;
+    uint8_t* my_staging = WB8 ? staging + (warp - 4u) * (STAGING / 8u) : staging + q * WARP_STAGING;
     uint32_t tog = 0;
     int64_t sk_it = sk_b;
     for (uint32_t i = 0;; ++i) {
@@ -815,6 +824,7 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
       }
 #pragma unroll 1
       for (int cons = 0; cons < NCONS; ++cons) {
+        if (WB8 && cons != my_cons) continue;
         const uint32_t slot = (NCONS == 2) ? (uint32_t)cons : MX ? 0u : (i & 1u);
         const uint32_t apar = (MX || NCONS == 2) ? (i & 1u) : ((i >> 1) & 1u);
         const int32_t row0 = tm * Cfg::TILE_M + cons * 128 * CG + (int32_t)rank * 128 + (int32_t)q * 32;
@@ -836,7 +846,11 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
           const int32_t row = row0 + (int32_t)lane;
           epi_res = p.residual != nullptr && row < p.M;
           if (epi_res) {
-            load_residual128<OutT>(res_next, p, row, col_base, v8_rows);
+            if constexpr (EPI_DIRECT) {
+              load_residual_cols32<OutT>(res_next, p, row, col_base, v8_rows);
+            } else {
+              load_residual128<OutT>(res_next, p, row, col_base, v8_rows);
+            }
             const uint8_t* seg = reinterpret_cast<const uint8_t*>(reinterpret_cast<const OutT*>(p.residual) +
                                                                   (int64_t)row * p.out_ld + col_base);
             const int32_t seg_bytes = min(BN, p.N - col_base) * (int32_t)sizeof(OutT);
@@ -851,6 +865,48 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
         if (!got) { ok = false; break; }
         tc_fence_after();
         const uint32_t tbase = tmem + ((q * 32u) << 16) + slot * 256u;
+        if constexpr (EPI_DIRECT) {
+          // 32 columns per step: the TMEM load, the epilogue (the residual read one
+          // step ahead; bias and scale_b from the warp's staging copy) and the row's
+          // 64 or 128 bytes stored from registers; the accumulator goes back as soon
+          // as the last step's columns are in registers
+          constexpr int RW = 32 * (int)sizeof(OutT) / 4;  // words of 32 columns
+          constexpr int per16 = 16 / (int)sizeof(OutT);
+          const int32_t row = row0 + (int32_t)lane;
+#pragma unroll 1
+          for (int s32 = 0; s32 < BN / 32; ++s32) {
+            uint32_t res[RW];
+#pragma unroll
+            for (int j = 0; j < RW; ++j) res[j] = res_next[j];
+            if (epi_res && s32 + 1 < BN / 32) load_residual_cols32<OutT>(res_next, p, row, col_base + (s32 + 1) * 32, v8_rows);
+            uint32_t v[32];
+            tmem_ld_32x32b_x32(tbase + (uint32_t)(s32 * 32), v);
+            tmem_wait_ld();
+            if (s32 == BN / 32 - 1) {
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(acc_empty + slot), 0));
+            }
+            const int32_t col0 = col_base + s32 * 32;
+            apply_epilogue32<OutT, EPI>(v, p, col0, epi_sa, epi_res, res, epi_cols + s32 * 32, epi_cols + BN + s32 * 32);
+            if (row < p.M) {
+              uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<OutT*>(p.C) + (int64_t)row * p.out_ld + col0);
+              uint32_t o[RW];  // the row's 32 columns in C's type
+#pragma unroll
+              for (int j = 0; j < RW; ++j) o[j] = (sizeof(OutT) == 4) ? v[j] : pack_bf16x2(v[2 * j], v[2 * j + 1]);
+              if (v8_rows) {
+#pragma unroll
+                for (int j = 0; j < RW / 8; ++j)
+                  if (col0 + 2 * per16 * j < p.N) st_global_v8(dst + 2 * j, o + 8 * j);
+              } else {
+#pragma unroll
+                for (int j = 0; j < RW / 4; ++j)
+                  if (col0 + per16 * j < p.N) dst[j] = make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
+              }
+            }
+          }
+          continue;
+        }
         // stream-K: this warp's 32 x 256 part of a split tile, in a workspace slot of
         // SK_WARP_FLOATS floats (8 chunks of 32 columns, see sk_add32); the owner adds
         // sk_nparts partials from consecutive slots
@@ -1123,41 +1179,6 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
                 }
               }
             }
-            if constexpr (EPI_DIRECT) {
-              const int32_t col0 = col_base + ch * CW, row = row0 + (int32_t)lane;
-              const float* sb = epi_cols + ch * CW;
-              const float* ss = epi_cols + BN + ch * CW;
-              apply_epilogue32<OutT, EPI>(v0, p, col0, epi_sa, epi_res, res, sb, ss);
-              if constexpr (CW == 64) apply_epilogue32<OutT, EPI>(v1, p, col0 + 32, epi_sa, epi_res, res + 16, sb + 32, ss + 32);
-              // 128 bytes of the lane's row, 16 at a time (C's rows are 16-byte
-              // multiples, so each group lies wholly inside C or outside)
-              if (row < p.M) {
-                uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<OutT*>(p.C) + (int64_t)row * p.out_ld + col0);
-                constexpr int per16 = 16 / (int)sizeof(OutT);
-                uint32_t o[32];  // the row's 128 bytes as C's type
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                  if constexpr (CW == 32) {
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) o[4 * j + e] = v0[4 * j + e];
-                  } else {
-                    const uint32_t* src = (j < 4) ? (v0 + 8 * j) : (v1 + 8 * (j - 4));
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) o[4 * j + e] = pack_bf16x2(src[2 * e], src[2 * e + 1]);
-                  }
-                }
-                if (v8_rows) {
-#pragma unroll
-                  for (int j = 0; j < 4; ++j)
-                    if (col0 + 2 * per16 * j < p.N) st_global_v8(dst + 2 * j, o + 8 * j);
-                } else {
-#pragma unroll
-                  for (int j = 0; j < 8; ++j)
-                    if (col0 + per16 * j < p.N) dst[j] = make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
-                }
-              }
-              continue;
-            }
             if constexpr (EPI >= 0) {
               // scales, bias, activation and residual, in fp32, before the single
               // rounding to C's type
@@ -1205,7 +1226,8 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
           }
         }
       }
-      if (p.visits != nullptr && q == 0 && lane == 0 && leader && (!SK || kb0 == 0) && (!KS || ks_r == 0))
+      if (p.visits != nullptr && q == 0 && my_cons <= 0 && lane == 0 && leader && (!SK || kb0 == 0) &&
+          (!KS || ks_r == 0))
         atomicAdd(p.visits + tile, 1);
     }
     if (lane == 0) bulk_wait_group<0>();
@@ -1224,7 +1246,7 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
 
 // entry point of the fp16 / bf16 / 8-bit float kernels
 template <typename OutT, int CG, int NCONS, int SCHED, int EPI = -1, int BN = WS_BN>
-__global__ void __launch_bounds__(WS_THREADS, 1)
+__global__ void __launch_bounds__(ws_threads(NCONS, EPI), 1)
     k_ws(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
          const __grid_constant__ CUtensorMap tmC, KParams p) {
   ws_body<OutT, CG, NCONS, SCHED, EPI, false, false, BN>(&tmA, &tmB, &tmC, nullptr, nullptr, p);
