@@ -381,8 +381,9 @@ def test_stream_k_is_the_default_when_the_last_wave_is_short():
 # N = 18 * 224 + 200 puts the edge inside the last 32-column band of the last tile.
 # N = 4096 and 4080 (multiples of 16, 13-14 sixteen-column units per tile column) run
 # 224- and 208-column tiles: 9 wide columns and 10 narrow, 8 and 11; M = 4000 leaves
-# the last row of tiles ragged
-NARROW = [(4096, 4232, 200), (4096, 4096, 136), (4000, 4080, 200)]
+# the last row of tiles ragged; M = 8192 makes four waves, each pair running four
+# tiles of both widths
+NARROW = [(4096, 4232, 200), (4096, 4096, 136), (4000, 4080, 200), (8192, 4080, 72)]
 NARROW_TWO_WIDTHS = {4096: 9, 4080: 8}
 
 
