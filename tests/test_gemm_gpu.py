@@ -67,6 +67,10 @@ SHAPES = {
     gemm.S9: [(300, 520, 200), (1100, 1288, 264)],
     # GEMV: the K-split kernel (M <= 2 and at most 64 rows per SM) and the row kernel
     gemm.GEMV: [(1, 1000, 520), (3, 264, 72), (8, 1000, 520), (16, 96, 1024), (1, 4096, 4096), (2, 152, 8),
+                # 3 <= M <= 8 with the activations in shared memory: an odd number of load
+                # groups per row group (no prefetch across row groups), several row groups
+                # per warp (prefetch across them), ragged rows
+                (8, 2000, 8200), (4, 20000, 4096), (6, 777, 264),
                 (1, 1, 64), (1, 9000, 16384), (2, 777, 4104), (1, 500, 8), (2, 12000, 520),
                 # one activation row, K a multiple of 1024: the rolling kernel, with a
                 # whole row per load group (K = 1024) and several rows per warp
