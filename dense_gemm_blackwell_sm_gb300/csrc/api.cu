@@ -1070,7 +1070,9 @@ gemm_status_t gemm_plan_info(gemm_plan_t p, gemm_plan_info_t* info) {
   info->raster_group = p->raster_group;
   info->tile_m = p->tile_m;
   info->tile_n = p->tile_n;
-  info->cluster = (p->ks_split >= 2) ? p->ks_split : p->cg;
+  info->cluster = (p->variant == GEMM_VARIANT_GEMV) ? (int32_t)p->spec.cluster
+                  : (p->ks_split >= 2)                ? p->ks_split
+                                                      : p->cg;
   info->consumers = p->consumers;
   info->grid = (int32_t)(p->spec.grid.x * p->spec.grid.y);
   info->smem_bytes = (int32_t)p->spec.smem;

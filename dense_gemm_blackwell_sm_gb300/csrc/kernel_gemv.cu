@@ -38,6 +38,9 @@
 // matching 16-byte activation chunk feed two MMAs; the order of K inside the
 // fragments is free because A and B use the same order.  A CTA owns 8 weight
 // rows; its 8 warps split K and add their 8 x 8 partial sums in shared memory.
+// When the grid fits one wave, a cluster of two CTAs owns 16 rows instead (the
+// fragment's rows 8-15 filled, each activation chunk feeding both rows) and
+// splits K between its CTAs.
 #include <algorithm>
 #include <type_traits>
 
@@ -336,46 +339,89 @@ __global__ void __launch_bounds__(GV_THREADS) k_gemv_mma(GemvParams g) {
   }
 }
 
+template <typename InT>
+__device__ __forceinline__ void mma_16816_full(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                               uint32_t b0, uint32_t b1) {
+  if constexpr (std::is_same<InT, __nv_bfloat16>::value) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  } else {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  }
+}
+
 // B possibly written by the previous kernel: the same product with the weight
-// chunks of each lane in two groups of GM_J loads, each group refilled as soon
-// as it has been consumed; the activation chunks are read when a group is
-// consumed (they are small and stay in L1).  Before the wait, L2 prefetches
-// the first pf groups of each row slice.
-template <typename InT, typename OutT>
+// chunks of each lane in two groups, each group refilled as soon as it has
+// been consumed; the activation chunks are read when a group is consumed
+// (they are small and stay in L1).  Before the wait, L2 prefetches the first
+// pf groups of each row slice.
+//
+// RW weight rows per CTA (or cluster): with 8 the fragment's rows 8-15 are
+// zero and each 16-byte activation chunk serves one 16-byte weight chunk; with
+// 16 a lane also holds the chunk of row gr + 8, so the same activation chunk
+// serves two weight chunks (half the activation reads and MMAs per weight
+// byte).  A group holds 4 chunks of one row (RW = 8) or 2 chunks of each of two
+// rows (RW = 16), so the registers in flight are the same.  With KS = 2 the
+// two CTAs of a cluster take the two halves of K (16 K slices of 8 warps) and
+// the second adds its sums into the first's shared memory, so 16 rows take as
+// many CTAs as 8 rows do with KS = 1.
+template <typename InT, typename OutT, int RW, int KS>
 __global__ void __launch_bounds__(GV_THREADS, 4) k_gemv_mma_roll(GemvParams g) {
-  __shared__ float red[GV_THREADS / 32][GM_ROWS][8];
+  static_assert(RW == 8 || RW == 16, "a CTA owns the 8 or 16 rows of one A fragment");
+  static_assert(KS == 1 || KS == 2, "K split over one CTA or a cluster of two");
+  __shared__ float peer[RW * 8];
+  if constexpr (KS == 2) asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+  const int rank = KS == 2 ? (int)cluster_ctarank() : 0;
+  constexpr int RR = RW / 8;          // weight rows per lane
+  constexpr int GJ = GM_J / RR;       // chunks per row in a group
+  __shared__ float red[GV_THREADS / 32][RW][8];
   constexpr int MG = 2;  // groups in flight per lane
   const int K8 = g.K / 8;
   const int warps = GV_THREADS / 32;
-  const int S = (K8 + warps - 1) / warps;  // chunks of each row in this warp's K slice
+  const int S = (K8 + warps * KS - 1) / (warps * KS);  // chunks of each row in this warp's K slice
   const int w = (int)warp_idx(), lane = (int)lane_idx();
+  const int ws = rank * warps + w;         // K slice
   const int gr = lane >> 2, c = lane & 3;  // fragment row / column group
-  const int n0 = (int)blockIdx.x * GM_ROWS;
-  const int row = n0 + gr;
+  const int n0 = (int)(blockIdx.x / KS) * RW;
   const uint4 zero = make_uint4(0, 0, 0, 0);
   const uint4* X = reinterpret_cast<const uint4*>(g.X);
   const uint4* B = reinterpret_cast<const uint4*>(g.B);
   // chunk j of this lane: 4 consecutive chunks (32 K-elements) per j across c
-  auto chunk = [&](int j) { return w * S + 4 * j + c; };
+  auto chunk = [&](int j) { return ws * S + 4 * j + c; };
   auto valid = [&](int j) { return 4 * j + c < S && chunk(j) < K8; };
   const int JJ = (S + 3) / 4;
-  const int NG = (JJ + GM_J - 1) / GM_J;  // groups of GM_J chunks per lane
-  uint4 bw[MG][GM_J];
-  auto load_grp = [&](int q, uint4 (&b)[GM_J]) {
+  const int NG = (JJ + GJ - 1) / GJ;  // groups of GJ chunks per row and lane
+  uint4 bw[MG][RR][GJ];
+  auto load_grp = [&](int q, uint4 (&b)[RR][GJ]) {
     if (q < NG) {
 #pragma unroll
-      for (int v = 0; v < GM_J; ++v) {
-        const int j = q * GM_J + v;
-        b[v] = (j < JJ && row < g.N && valid(j)) ? ld_stream_v4(B + (int64_t)row * K8 + chunk(j)) : zero;
+      for (int h = 0; h < RR; ++h) {
+        const int row = n0 + gr + 8 * h;
+#pragma unroll
+        for (int v = 0; v < GJ; ++v) {
+          const int j = q * GJ + v;
+          b[h][v] = (j < JJ && row < g.N && valid(j)) ? ld_stream_v4(B + (int64_t)row * K8 + chunk(j)) : zero;
+        }
       }
     }
   };
 
   pdl_launch_dependents();
-  // a group spans 4 * GM_J chunks (two 128-byte lines) of each of the 8 rows
+  // a group spans 4 * GJ chunks (GJ / 2 lines of 128 bytes) of each row
   for (int q = 0; q < g.pf_rows && q < NG; ++q) {
-    const int k8 = w * S + q * 4 * GM_J + 8 * c;
-    if (c < 2 && row < g.N && q * 4 * GM_J + 8 * c < S && k8 < K8) prefetch_l2_line(B + (int64_t)row * K8 + k8);
+    const int k8 = ws * S + q * 4 * GJ + 8 * c;
+#pragma unroll
+    for (int h = 0; h < RR; ++h) {
+      const int row = n0 + gr + 8 * h;
+      if (c < GJ / 2 && row < g.N && q * 4 * GJ + 8 * c < S && k8 < K8) prefetch_l2_line(B + (int64_t)row * K8 + k8);
+    }
   }
   pdl_wait_prior_grids();
 #pragma unroll
@@ -386,36 +432,57 @@ __global__ void __launch_bounds__(GV_THREADS, 4) k_gemv_mma_roll(GemvParams g) {
     for (int i = 0; i < MG; ++i) {
       const int q = q0 + i;
       if (q < NG) {
-        uint4 xv[GM_J];
+        uint4 xv[GJ];
 #pragma unroll
-        for (int v = 0; v < GM_J; ++v) {
-          const int j = q * GM_J + v;
+        for (int v = 0; v < GJ; ++v) {
+          const int j = q * GJ + v;
           xv[v] = (j < JJ && gr < g.M && valid(j)) ? X[(int64_t)gr * K8 + chunk(j)] : zero;
         }
 #pragma unroll
-        for (int v = 0; v < GM_J; ++v) {
-          mma_16816<InT>(d, bw[i][v].x, bw[i][v].y, xv[v].x, xv[v].y);
-          mma_16816<InT>(d, bw[i][v].z, bw[i][v].w, xv[v].z, xv[v].w);
+        for (int v = 0; v < GJ; ++v) {
+          if constexpr (RR == 1) {
+            mma_16816<InT>(d, bw[i][0][v].x, bw[i][0][v].y, xv[v].x, xv[v].y);
+            mma_16816<InT>(d, bw[i][0][v].z, bw[i][0][v].w, xv[v].z, xv[v].w);
+          } else {
+            mma_16816_full<InT>(d, bw[i][0][v].x, bw[i][1][v].x, bw[i][0][v].y, bw[i][1][v].y, xv[v].x, xv[v].y);
+            mma_16816_full<InT>(d, bw[i][0][v].z, bw[i][1][v].z, bw[i][0][v].w, bw[i][1][v].w, xv[v].z, xv[v].w);
+          }
         }
         load_grp(q + MG, bw[i]);
       }
     }
   }
-  // d[0], d[1]: weight row gr, activation rows 2c and 2c + 1 (d[2], d[3]: zero rows)
+  // d[0], d[1]: weight row gr, activation rows 2c and 2c + 1; d[2], d[3]: weight
+  // row gr + 8 (zero rows when RW = 8)
   red[w][gr][2 * c] = d[0];
   red[w][gr][2 * c + 1] = d[1];
+  if constexpr (RR == 2) {
+    red[w][gr + 8][2 * c] = d[2];
+    red[w][gr + 8][2 * c + 1] = d[3];
+  }
   __syncthreads();
-  if ((int)threadIdx.x < GM_ROWS * 8) {
-    const int r = (int)threadIdx.x >> 3, m = (int)threadIdx.x & 7;
-    float v = 0.f;
+  const int t = (int)threadIdx.x;
+  const int r = t >> 3, m = t & 7;
+  float v = 0.f;
+  if (t < RW * 8) {
 #pragma unroll
     for (int q = 0; q < warps; ++q) v += red[q][r][m];
-    if (m < g.M && n0 + r < g.N) {
-      if constexpr (sizeof(OutT) == 4) {
-        reinterpret_cast<float*>(g.Y)[(int64_t)m * g.N + n0 + r] = v;
-      } else {
-        reinterpret_cast<__nv_bfloat16*>(g.Y)[(int64_t)m * g.N + n0 + r] = __float2bfloat16_rn(v);
-      }
+  }
+  if constexpr (KS == 2) {
+    // the second CTA's sums go to the first CTA's shared memory (both CTAs
+    // have started once the wait matching the arrive above returns); the
+    // second barrier orders those stores before the first CTA's reads
+    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+    if (rank == 1 && t < RW * 8) st_cluster_u32(mapa_shared(smem_u32(peer + t), 0), __float_as_uint(v));
+    cluster_sync_all();
+    if (rank == 1) return;
+    if (t < RW * 8) v += peer[t];
+  }
+  if (t < RW * 8 && m < g.M && n0 + r < g.N) {
+    if constexpr (sizeof(OutT) == 4) {
+      reinterpret_cast<float*>(g.Y)[(int64_t)m * g.N + n0 + r] = v;
+    } else {
+      reinterpret_cast<__nv_bfloat16*>(g.Y)[(int64_t)m * g.N + n0 + r] = __float2bfloat16_rn(v);
     }
   }
 }
@@ -426,16 +493,36 @@ __global__ void __launch_bounds__(GV_THREADS, 4) k_gemv_mma_roll(GemvParams g) {
 // prefetched lines compete with the previous kernel's own loads.
 int prefetch_groups(int groups_per_warp) { return groups_per_warp > 4 ? 2 : 1; }
 
+// Without GEMM_FLAG_STATIC_B: 16 weight rows per cluster of two CTAs that
+// split K when that grid is resident in one wave, else 8 rows per CTA.
+// Measured on bf16, 8 activation rows (GB/s, chain of dependent launches):
+//   8 x 4096 x 4096:   8 rows per CTA 4645, 16 rows per CTA 3310, 16 rows per
+//                      cluster of two 4950
+//   8 x 14336 x 4096:  5720-5770, 5390, 5519
+// Half the CTAs (16 rows per CTA) leave half the loads in flight at N = 4096;
+// the cluster form keeps the CTAs and halves the activation reads per weight
+// byte, but its shorter per-warp streams lose where the rows take several
+// waves.
 template <typename InT, typename OutT>
-cudaError_t spec_mma(int N, int K, bool static_b, LaunchSpec* out, int* pf) {
-  out->func = static_b ? (const void*)k_gemv_mma<InT, OutT> : (const void*)k_gemv_mma_roll<InT, OutT>;
-  out->grid = dim3((unsigned)((N + GM_ROWS - 1) / GM_ROWS), 1, 1);
+cudaError_t spec_mma(int N, int K, int num_sms, bool static_b, LaunchSpec* out, int* pf) {
+  int rw = GM_ROWS, ks = 1;
+  if (!static_b) {
+    int per_sm = 0;
+    cudaError_t e =
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_gemv_mma_roll<InT, OutT, 16, 2>, GV_THREADS, 0);
+    if (e != cudaSuccess) return e;
+    if ((int64_t)((N + 15) / 16) * 2 <= (int64_t)per_sm * num_sms) rw = 16, ks = 2;
+  }
+  out->func = static_b ? (const void*)k_gemv_mma<InT, OutT>
+              : ks == 2 ? (const void*)k_gemv_mma_roll<InT, OutT, 16, 2>
+                        : (const void*)k_gemv_mma_roll<InT, OutT, 8, 1>;
+  out->grid = dim3((unsigned)((N + rw - 1) / rw * ks), 1, 1);
   out->block = dim3(GV_THREADS, 1, 1);
   out->smem = 0;
-  out->cluster = 1;
+  out->cluster = (unsigned)ks;
   out->kind = ARGS_GEMV;
-  const int S = (K / 8 + 7) / 8, JJ = (S + 3) / 4;
-  *pf = static_b ? 0 : prefetch_groups((JJ + GM_J - 1) / GM_J);
+  const int S = (K / 8 + 8 * ks - 1) / (8 * ks), JJ = (S + 3) / 4, gj = GM_J / (rw / 8);
+  *pf = static_b ? 0 : prefetch_groups((JJ + gj - 1) / gj);
   return cudaSuccess;
 }
 
@@ -474,7 +561,7 @@ cudaError_t spec_m(int M, int N, int K, int num_sms, bool static_b, LaunchSpec* 
   // 3.99 -> 4.49 TB/s; 14336 x 4096: 5.70 -> 6.05 TB/s)
   if (M <= 1) return spec_t<InT, OutT, 1>(N, K, num_sms, static_b, out, pf);
   if (M <= 2) return spec_t<InT, OutT, 2>(N, K, num_sms, static_b, out, pf);
-  if (M <= 8) return spec_mma<InT, OutT>(N, K, static_b, out, pf);
+  if (M <= 8) return spec_mma<InT, OutT>(N, K, num_sms, static_b, out, pf);
   return spec_t<InT, OutT, 16>(N, K, num_sms, static_b, out, pf);
 }
 

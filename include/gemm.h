@@ -156,7 +156,8 @@ typedef struct gemm_plan_s* gemm_plan_t;
 typedef struct {
   int32_t variant, sched, stages, raster_group;
   int32_t tile_m, tile_n;  /* output tile of one CTA (or CTA pair / cluster) */
-  int32_t cluster;         /* CTAs per cluster (1 or 2) */
+  int32_t cluster;         /* CTAs per cluster (1 or 2; the CUDA-core GEMV for 3 <= M <= 8
+                              takes 2 when its 16-row clusters fit one wave) */
   int32_t consumers;       /* MMA consumers per CTA */
   int32_t grid;            /* CTAs launched */
   int32_t smem_bytes;      /* dynamic shared memory per CTA */

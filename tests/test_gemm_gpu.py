@@ -284,6 +284,26 @@ def test_default_gemv_reads_weights_the_previous_kernel_wrote(M):
     gemv.destroy()
 
 
+@pytest.mark.parametrize("M,N,K,cluster,grid", [(8, 4096, 4096, 2, 512), (5, 4104, 4096, 2, 514),
+                                                 (8, 14336, 4096, 1, 1792), (3, 10000, 1032, 1, 1250)])
+def test_gemv_mma_row_split_by_wave(M, N, K, cluster, grid):
+    """The CUDA-core GEMV for 3 <= M <= 8 gives a cluster of two CTAs 16 weight
+    rows and half of K each when those clusters fit one wave, and one CTA 8 rows
+    otherwise; both forms are bit-exact on integer operands, ragged rows
+    included (N % 16 == 8 for the second case)."""
+    a, b = inputs.integer_operands(M, N, K, "bf16", seed=M + N + K)
+    plan = gemm.Plan(M, N, K, gemm.BF16_F32, gemm.make_opts(variant=gemm.GEMV))
+    info = plan.info()
+    if info["num_sms"] == 152:
+        assert (info["cluster"], info["grid"]) == (cluster, grid), info
+    c = torch.empty((M, N), device=DEV)
+    plan.run(a.to(DEV), b.to(DEV), c)
+    assert plan.check() == gemm.OK
+    ref, _ = oracle.gemm(a, b)
+    assert np.array_equal(c.double().cpu().numpy(), ref)
+    plan.destroy()
+
+
 @pytest.mark.parametrize("split", [1, 2, 4, 8])
 @pytest.mark.parametrize("stages", [2, 4, 8])
 def test_gemv_tc_split_and_ring_depth(split, stages):
