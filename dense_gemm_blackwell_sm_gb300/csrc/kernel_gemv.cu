@@ -25,8 +25,9 @@
 //     1 x 4096 x 4096 launches this took a launch from 7.45 us (whole half
 //     rows in flight, refilled after each half) to 6.5 us.
 //   * B is declared static (GEMM_FLAG_STATIC_B): the first half row of every
-//     warp is loaded into registers before the wait (k_gemv, k_gemv_mma), so
-//     the weights stream while the previous kernel drains.
+//     warp (k_gemv, k_gemv_mma) or the first two groups of every lane (the
+//     16-row cluster form of k_gemv_mma_roll) are loaded into registers before
+//     the wait, so the weights stream while the previous kernel drains.
 //
 // For 3 <= M <= 8 the CUDA cores would need M FMAs per weight element, more
 // than they can issue at HBM speed, and the tcgen05 GEMV is fed by TMA, which
@@ -357,11 +358,12 @@ __device__ __forceinline__ void mma_16816_full(float (&d)[4], uint32_t a0, uint3
   }
 }
 
-// B possibly written by the previous kernel: the same product with the weight
-// chunks of each lane in two groups, each group refilled as soon as it has
-// been consumed; the activation chunks are read when a group is consumed
-// (they are small and stay in L1).  Before the wait, L2 prefetches the first
-// pf groups of each row slice.
+// The same product with the weight chunks of each lane in two groups, each
+// group refilled as soon as it has been consumed; the activation chunks are
+// read when a group is consumed (they are small and stay in L1).  B possibly
+// written by the previous kernel: before the wait, L2 prefetches the first pf
+// groups of each row slice.  B static: the first two groups are loaded before
+// the wait.
 //
 // RW weight rows per CTA (or cluster): with 8 the fragment's rows 8-15 are
 // zero and each 16-byte activation chunk serves one 16-byte weight chunk; with
@@ -423,9 +425,10 @@ __global__ void __launch_bounds__(GV_THREADS, 4) k_gemv_mma_roll(GemvParams g) {
       if (c < GJ / 2 && row < g.N && q * 4 * GJ + 8 * c < S && k8 < K8) prefetch_l2_line(B + (int64_t)row * K8 + k8);
     }
   }
-  pdl_wait_prior_grids();
+  if (!g.early_b) pdl_wait_prior_grids();
 #pragma unroll
   for (int i = 0; i < MG; ++i) load_grp(i, bw[i]);
+  if (g.early_b) pdl_wait_prior_grids();
   float d[4] = {0.f, 0.f, 0.f, 0.f};
   for (int q0 = 0; q0 < NG; q0 += MG) {
 #pragma unroll
@@ -493,29 +496,29 @@ __global__ void __launch_bounds__(GV_THREADS, 4) k_gemv_mma_roll(GemvParams g) {
 // prefetched lines compete with the previous kernel's own loads.
 int prefetch_groups(int groups_per_warp) { return groups_per_warp > 4 ? 2 : 1; }
 
-// Without GEMM_FLAG_STATIC_B: 16 weight rows per cluster of two CTAs that
-// split K when that grid is resident in one wave, else 8 rows per CTA.
-// Measured on bf16, 8 activation rows (GB/s, chain of dependent launches):
+// 16 weight rows per cluster of two CTAs that split K when that grid is
+// resident in one wave, else 8 rows per CTA.  Measured on bf16, 8 activation
+// rows (GB/s, chain of dependent launches):
 //   8 x 4096 x 4096:   8 rows per CTA 4645, 16 rows per CTA 3310, 16 rows per
-//                      cluster of two 4950
+//                      cluster of two 4950, 32 rows per cluster of four 4170
 //   8 x 14336 x 4096:  5720-5770, 5390, 5519
 // Half the CTAs (16 rows per CTA) leave half the loads in flight at N = 4096;
 // the cluster form keeps the CTAs and halves the activation reads per weight
-// byte, but its shorter per-warp streams lose where the rows take several
-// waves.
+// byte, but loses where the rows take several waves.  With static weights the
+// cluster form (its first two groups loaded before the wait) gives 5022-5056
+// at N = 4096 against 4925-4944 for k_gemv_mma; over several waves the
+// rolling kernel with early loads loses (5450 against 5865 at N = 14336).
 template <typename InT, typename OutT>
 cudaError_t spec_mma(int N, int K, int num_sms, bool static_b, LaunchSpec* out, int* pf) {
   int rw = GM_ROWS, ks = 1;
-  if (!static_b) {
-    int per_sm = 0;
-    cudaError_t e =
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_gemv_mma_roll<InT, OutT, 16, 2>, GV_THREADS, 0);
-    if (e != cudaSuccess) return e;
-    if ((int64_t)((N + 15) / 16) * 2 <= (int64_t)per_sm * num_sms) rw = 16, ks = 2;
-  }
-  out->func = static_b ? (const void*)k_gemv_mma<InT, OutT>
-              : ks == 2 ? (const void*)k_gemv_mma_roll<InT, OutT, 16, 2>
-                        : (const void*)k_gemv_mma_roll<InT, OutT, 8, 1>;
+  int per_sm = 0;
+  cudaError_t e =
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_gemv_mma_roll<InT, OutT, 16, 2>, GV_THREADS, 0);
+  if (e != cudaSuccess) return e;
+  if ((int64_t)((N + 15) / 16) * 2 <= (int64_t)per_sm * num_sms) rw = 16, ks = 2;
+  out->func = ks == 2    ? (const void*)k_gemv_mma_roll<InT, OutT, 16, 2>
+              : static_b ? (const void*)k_gemv_mma<InT, OutT>
+                         : (const void*)k_gemv_mma_roll<InT, OutT, 8, 1>;
   out->grid = dim3((unsigned)((N + rw - 1) / rw * ks), 1, 1);
   out->block = dim3(GV_THREADS, 1, 1);
   out->smem = 0;

@@ -218,12 +218,13 @@ def test_run_host_end_to_end():
     assert parity.check(ch.float().numpy(), ref, S, "bf16")["ok"]
 
 
-@pytest.mark.parametrize("variant", [gemm.GEMV, gemm.GEMV_TC])
-def test_static_b_flag_chains_dependent_gemvs(variant):
+@pytest.mark.parametrize("variant,M,K", [(gemm.GEMV, 1, 512), (gemm.GEMV, 1, 1024), (gemm.GEMV, 8, 1024),
+                                         (gemm.GEMV, 5, 520), (gemm.GEMV_TC, 8, 512)])
+def test_static_b_flag_chains_dependent_gemvs(variant, M, K):
     """With GEMM_FLAG_STATIC_B the GEMV launches as a programmatic dependent of
     the previous kernel and may stream B early, but must read its activations
     only after that kernel is done: chain y1 = x B1^T, y2 = y1 B2^T."""
-    M, N1, K = (1 if variant == gemm.GEMV else 8), 1024, 512
+    N1 = 1024
     x, b1 = inputs.make_operands(M, N1, K, "bf16", ("uniform",), ("normal", 0.05), seed=21)
     _, b2 = inputs.make_operands(M, 768, N1, "bf16", ("uniform",), ("normal", 0.05), seed=22)
     opts = gemm.make_opts(variant=variant, flags=gemm.FLAG_STATIC_B)
