@@ -415,7 +415,12 @@ __global__ void __launch_bounds__(GV_THREADS, 4) k_gemv_mma_roll(GemvParams g) {
     }
   };
 
-  pdl_launch_dependents();
+  // the next kernel on the stream may launch at once (8 rows per CTA: its CTAs
+  // take the slots of this grid's later waves as they free up) or once this
+  // CTA has issued its last loads (16-row clusters, one wave: 8 x 4096 x 4096
+  // 4967-4977 -> 5045-5080 GB/s, 5020-5048 -> 5146-5166 with static weights;
+  // the same for 8 rows per CTA at N = 14336: 5770 -> 5246)
+  if constexpr (KS == 1) pdl_launch_dependents();
   // a group spans 4 * GJ chunks (GJ / 2 lines of 128 bytes) of each row
   for (int q = 0; q < g.pf_rows && q < NG; ++q) {
     const int k8 = ws * S + q * 4 * GJ + 8 * c;
@@ -431,6 +436,9 @@ __global__ void __launch_bounds__(GV_THREADS, 4) k_gemv_mma_roll(GemvParams g) {
   if (g.early_b) pdl_wait_prior_grids();
   float d[4] = {0.f, 0.f, 0.f, 0.f};
   for (int q0 = 0; q0 < NG; q0 += MG) {
+    if constexpr (KS == 2) {
+      if (q0 + MG >= NG) pdl_launch_dependents();
+    }
 #pragma unroll
     for (int i = 0; i < MG; ++i) {
       const int q = q0 + i;
@@ -508,6 +516,7 @@ int prefetch_groups(int groups_per_warp) { return groups_per_warp > 4 ? 2 : 1; }
 // cluster form (its first two groups loaded before the wait) gives 5022-5056
 // at N = 4096 against 4925-4944 for k_gemv_mma; over several waves the
 // rolling kernel with early loads loses (5450 against 5865 at N = 14336).
+// (Figures before the cluster form's late trigger of the next launch.)
 template <typename InT, typename OutT>
 cudaError_t spec_mma(int N, int K, int num_sms, bool static_b, LaunchSpec* out, int* pf) {
   int rw = GM_ROWS, ks = 1;
