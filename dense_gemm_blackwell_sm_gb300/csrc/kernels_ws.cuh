@@ -986,15 +986,29 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
             uint32_t v[32];
 #pragma unroll
             for (int j = 0; j < 32; ++j) v[j] = 0u;  // +0.0f
-            for (int32_t pr = 0; pr < ks_n; ++pr) {
-              const uint32_t base = mapa_shared(smem_u32(ring), (uint32_t)pr) + off;
+            // the partials of up to four CTAs are requested together (one round trip
+            // over the cluster instead of one per CTA), then added in rank order
+            for (int32_t pr0 = 0; pr0 < ks_n; pr0 += 4) {
+              float4 a4[4][8];
 #pragma unroll
-              for (int j = 0; j < 8; ++j) {
-                const float4 a4 = ld_cluster_f32x4(base + 512u * j);
-                v[4 * j] = __float_as_uint(__uint_as_float(v[4 * j]) + a4.x);
-                v[4 * j + 1] = __float_as_uint(__uint_as_float(v[4 * j + 1]) + a4.y);
-                v[4 * j + 2] = __float_as_uint(__uint_as_float(v[4 * j + 2]) + a4.z);
-                v[4 * j + 3] = __float_as_uint(__uint_as_float(v[4 * j + 3]) + a4.w);
+              for (int u = 0; u < 4; ++u) {
+                if (pr0 + u < ks_n) {
+                  const uint32_t base = mapa_shared(smem_u32(ring), (uint32_t)(pr0 + u)) + off;
+#pragma unroll
+                  for (int j = 0; j < 8; ++j) a4[u][j] = ld_cluster_f32x4(base + 512u * j);
+                }
+              }
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                if (pr0 + u < ks_n) {
+#pragma unroll
+                  for (int j = 0; j < 8; ++j) {
+                    v[4 * j] = __float_as_uint(__uint_as_float(v[4 * j]) + a4[u][j].x);
+                    v[4 * j + 1] = __float_as_uint(__uint_as_float(v[4 * j + 1]) + a4[u][j].y);
+                    v[4 * j + 2] = __float_as_uint(__uint_as_float(v[4 * j + 2]) + a4[u][j].z);
+                    v[4 * j + 3] = __float_as_uint(__uint_as_float(v[4 * j + 3]) + a4[u][j].w);
+                  }
+                }
               }
             }
             if (row < p.M) store_row32<OutT>(reinterpret_cast<OutT*>(p.C), p.out_ld, row, col_base + 32 * c32, p.N, v);
