@@ -543,7 +543,7 @@ gemm_status_t build_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, co
       if (split >= 2 && split <= kb) {
         p->ks_split = (int)split;
         p->sched = GEMM_SCHED_STATIC;
-        p->stages = std::max(p->stages, 3);
+        if (split == 2) p->stages = std::max(p->stages, 3);  // the partial parks in the ring
         p->smem = ws_smem_bytes(1, 1, p->stages);
         p->grid_units = tiles * (int)split;
       }
@@ -589,6 +589,23 @@ gemm_status_t build_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, co
     }
     p->kbase.sk_ws = p->sk_ws;
     p->kbase.sk_flags = p->sk_flags;
+  }
+  if (p->ks_split > 2) {
+    // split-K over a cluster of more than two: one fp32 partial slot (32 rows x
+    // 256 columns per writeback warp, 128 KB) per CTA; an automatic split launches
+    // at most one CTA per SM (19 MB on 152 SMs), and a forced split that would
+    // need more than 512 MB is refused
+    const size_t bytes = (size_t)p->grid_units * ws_sk_slot_floats(1, 1) * sizeof(float);
+    if (bytes > ((size_t)512 << 20)) {
+      gemm_plan_destroy(p);
+      return GEMM_ERR_UNSUPPORTED_SHAPE;
+    }
+    if (cudaMalloc(reinterpret_cast<void**>(&p->sk_ws), bytes) != cudaSuccess) {
+      cudaGetLastError();
+      gemm_plan_destroy(p);
+      return GEMM_ERR_OOM;
+    }
+    p->kbase.sk_ws = p->sk_ws;
   }
   *out = p;
   return GEMM_OK;

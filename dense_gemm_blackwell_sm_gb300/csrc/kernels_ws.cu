@@ -121,8 +121,12 @@ int ws_max_active_clusters(int cg, int consumers, int sched, bool out_f32, int s
 }
 
 cudaError_t spec_ws_ks(bool out_f32, int stages, int tiles, int split, LaunchSpec* out) {
-  void* k = out_f32 ? reinterpret_cast<void*>(k_ws_ks<float>) : reinterpret_cast<void*>(k_ws_ks<__nv_bfloat16>);
-  if (split < 2 || split > 8 || stages < 3) return cudaErrorInvalidValue;  // partials need 128 KB of ring
+  void* k = split > 2 ? (out_f32 ? reinterpret_cast<void*>(k_ws_ks<float, true>)
+                                 : reinterpret_cast<void*>(k_ws_ks<__nv_bfloat16, true>))
+                      : (out_f32 ? reinterpret_cast<void*>(k_ws_ks<float, false>)
+                                 : reinterpret_cast<void*>(k_ws_ks<__nv_bfloat16, false>));
+  // a cluster of two parks its 128 KB partial in its stage ring
+  if (split < 2 || split > 8 || stages < (split == 2 ? 3 : 1)) return cudaErrorInvalidValue;
   const size_t smem = ws_smem_bytes(1, 1, stages);
   cudaError_t e = allow_dynamic_smem((const void*)k, smem);
   if (e != cudaSuccess) return e;

@@ -70,12 +70,13 @@
 // Split-K within a cluster (KS template flag, step 7's 128x256 tile, plain
 // writeback): for outputs with too few tiles for the GPU, a cluster of 2-8 CTAs
 // shares one tile, CTA r accumulating K blocks [KB r / s, KB (r+1) / s) in its
-// own TMEM.  Every CTA parks its fp32 partial in its own stage ring (idle once
-// its MMAs are done) in the writeback warps' (warp, chunk, lane) order and
-// arrives on the barrier of every CTA of the cluster; then each CTA adds all the
-// partials of its share of the tile's columns over distributed shared memory
-// and stores that share.  The cluster synchronises once more before any CTA
-// exits, so no shared memory is read after its owner has gone.
+// own TMEM.  Every CTA puts its fp32 partial where the others can read it (its
+// idle stage ring for a cluster of two; otherwise, except the columns it owns,
+// its slot of the plan's workspace in L2) in the writeback warps' (warp, chunk,
+// lane) order and arrives on the barrier of every CTA of the cluster; then each
+// CTA adds all the partials of its share of the tile's columns and stores that
+// share.  The cluster synchronises once more before any CTA exits, so no shared
+// memory is read after its owner has gone.
 //
 // In a CTA pair, each CTA loads its own 128 rows of A and its own 128 rows of B
 // (the pair MMA splits A along M and B along N) with the cta_group::2 TMA form,
@@ -180,9 +181,10 @@ struct WsCfg {
 // The kernel body.  EPI < 0: plain writeback; EPI >= 0: fused epilogue with
 // activation EPI.  MX: 8-bit inputs with UE8M0 block scales read through
 // tmSA / tmSB (one consumer only).  The tensor maps are kernel parameters of
-// the entry points below.
+// the entry points below.  KS: K split over a cluster, the partials exchanged
+// over distributed shared memory (1, a cluster of two) or through L2 (2).
 template <typename OutT, int CG, int NCONS, int SCHED, int EPI, bool MX, bool SK = false, int BN = WS_BN,
-          bool KS = false>
+          int KS = 0>
 __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMap* tmB, const CUtensorMap* tmC,
                                         const CUtensorMap* tmSA, const CUtensorMap* tmSB, const KParams& p) {
   using Cfg = WsCfg<CG, NCONS, BN>;
@@ -286,7 +288,7 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
       }
     }
     if constexpr (MX_COPIER) mbar_init(smem_u32(cp_drain), 1);
-    if constexpr (KS) mbar_init(smem_u32(red_full), 4u * (uint32_t)ks_n);
+    if constexpr (KS != 0) mbar_init(smem_u32(red_full), 4u * (uint32_t)ks_n);
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(acc_full + i), 1);
       mbar_init(smem_u32(acc_empty + i), 4 * CG);
@@ -315,7 +317,7 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
     tmem_relinquish<CG>();
   }
   tc_fence_before();
-  if constexpr (CG == 2 || KS) {
+  if constexpr (CG == 2 || KS != 0) {
     cluster_sync_all();
   } else {
     __syncthreads();
@@ -423,7 +425,7 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
         int32_t tile, kb0 = 0, kb1 = KB;
         if constexpr (SK) {
           if (!sk_next(sk_it, tile, kb0, kb1)) break;
-        } else if constexpr (KS) {
+        } else if constexpr (KS != 0) {
           if (i > 0) break;  // one tile per cluster, this CTA's share of K
           tile = (int32_t)(blockIdx.x / (uint32_t)ks_n);
           kb0 = KB * ks_r / ks_n;
@@ -439,7 +441,7 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
         tile_cols(tn, tc0, tw);
         // the pair's second CTA holds the tile's second half of B rows
         const int32_t n_cta = tc0 + (CG == 2 ? (int32_t)rank * (tw / 2) : 0);
-        const bool rev = k_reversed<SK || KS>(i);
+        const bool rev = k_reversed<SK || KS != 0>(i);
         for (int32_t it = 0; it < kb1 - kb0; ++it) {
           const int32_t kb = rev ? kb1 - 1 - it : kb0 + it;
           if (!mbar_wait(smem_u32(empty + stage), sphase ^ 1u, w, WAIT_PRODUCER_EMPTY)) { ok = false; break; }
@@ -622,7 +624,7 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
         int32_t tile, kb0 = 0, kb1 = KB;
         if constexpr (SK) {
           if (!sk_next(sk_it, tile, kb0, kb1)) break;
-        } else if constexpr (KS) {
+        } else if constexpr (KS != 0) {
           if (i > 0) break;
           tile = (int32_t)(blockIdx.x / (uint32_t)ks_n);
           kb0 = KB * ks_r / ks_n;
@@ -644,7 +646,7 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
         tc_fence_after();
         const uint32_t d = tmem + slot * 256u;
         bool ok = true;
-        const bool rev = k_reversed<SK || KS>(i);
+        const bool rev = k_reversed<SK || KS != 0>(i);
         for (int32_t it = 0; it < kb1 - kb0; ++it) {
           const int32_t kb = rev ? kb1 - 1 - it : kb0 + it;
           const uint32_t acc0 = (it != 0) ? 1u : 0u;  // the segment's first MMA overwrites D
@@ -802,7 +804,7 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
       int32_t tile = -1, kb0 = 0, kb1 = KB;
       if constexpr (SK) {
         if (!sk_next(sk_it, tile, kb0, kb1)) break;
-      } else if constexpr (KS) {
+      } else if constexpr (KS != 0) {
         if (i > 0) break;
         tile = (int32_t)(blockIdx.x / (uint32_t)ks_n);
       } else {
@@ -957,20 +959,41 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
             sk_part = p.sk_ws + (own + SK_SLOT_STRIDE) * SK_WARP_FLOATS;
           }
         }
-        if constexpr (KS) {
-          // a tile split over the cluster: every CTA parks its fp32 partial in its own
-          // stage ring (idle now), as [warp quarter][32-column chunk] in the chunk
-          // layout of sk_add32, and arrives on every CTA's barrier; then CTA r adds the
-          // ks_n partials of its share of the 32-column chunks, read over distributed
-          // shared memory, and stores them, so the reads and stores are spread over
-          // the cluster instead of converging on one CTA
-          float* dst = reinterpret_cast<float*>(ring) + (int64_t)q * SK_WARP_FLOATS;
+        if constexpr (KS != 0) {
+          // a tile split over the cluster: CTA r adds, in rank order, the ks_n partials
+          // of its share of the tile's 32-column chunks and stores them.  The partials
+          // are kept as [warp quarter][32-column chunk] in the chunk layout of sk_add32
+          // (each 16-byte access of the warp covers 512 contiguous bytes), and every CTA
+          // arrives on every CTA's barrier once its own are in place.  Distributed shared
+          // memory moves only about 15 bytes per clock per SM, so a cluster of two parks
+          // its partials in its (idle) stage ring and reads the other CTA's there
+          // (512 x 4096 x 4096: 775 TFLOP/s, 747 through L2), while larger clusters write
+          // the chunks other CTAs own to their slots of the plan's workspace in L2 and
+          // read them back from there, each CTA's own chunks straight from TMEM
+          // (1024 x 1024 x 4096 on four CTAs: 541 TFLOP/s, 520 over distributed
+          // shared memory)
+          constexpr bool via_l2 = KS == 2;
+          const int32_t cb = (WS_BN / 32) * ks_r / ks_n, ce = (WS_BN / 32) * (ks_r + 1) / ks_n;
+          const int64_t cta0 = (int64_t)blockIdx.x - ks_r;  // the cluster's first CTA
+          if constexpr (via_l2) {
+            float* mine = p.sk_ws + ((int64_t)blockIdx.x * 4 + q) * SK_WARP_FLOATS;
 #pragma unroll 1
-          for (int c32 = 0; c32 < WS_BN / 32; ++c32) {
-            uint32_t v[32];
-            tmem_ld_32x32b_x32(tbase + (uint32_t)(c32 * 32), v);
-            tmem_wait_ld();
-            sk_store32(dst + c32 * SK_CHUNK_FLOATS, lane, v);
+            for (int c32 = 0; c32 < WS_BN / 32; ++c32) {
+              if (c32 >= cb && c32 < ce) continue;
+              uint32_t v[32];
+              tmem_ld_32x32b_x32(tbase + (uint32_t)(c32 * 32), v);
+              tmem_wait_ld();
+              sk_store32(mine + c32 * SK_CHUNK_FLOATS, lane, v);
+            }
+          } else {
+            float* mine = reinterpret_cast<float*>(ring) + (int64_t)q * SK_WARP_FLOATS;
+#pragma unroll 1
+            for (int c32 = 0; c32 < WS_BN / 32; ++c32) {
+              uint32_t v[32];
+              tmem_ld_32x32b_x32(tbase + (uint32_t)(c32 * 32), v);
+              tmem_wait_ld();
+              sk_store32(mine + c32 * SK_CHUNK_FLOATS, lane, v);
+            }
           }
           fence_cluster();
           __syncwarp();
@@ -981,32 +1004,50 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
           if (!got2) { ok = false; break; }
           const int32_t row = row0 + (int32_t)lane;
 #pragma unroll 1
-          for (int c32 = (WS_BN / 32) * ks_r / ks_n; c32 < (WS_BN / 32) * (ks_r + 1) / ks_n; ++c32) {
-            const uint32_t off = (uint32_t)(((int)q * (WS_BN / 32) + c32) * SK_CHUNK_FLOATS + (int)lane * 4) * 4u;
+          for (int c32 = cb; c32 < ce; ++c32) {
             uint32_t v[32];
 #pragma unroll
             for (int j = 0; j < 32; ++j) v[j] = 0u;  // +0.0f
-            // the partials of up to four CTAs are requested together (one round trip
-            // over the cluster instead of one per CTA), then added in rank order
+            // the partials of up to four CTAs are requested together, then added
             for (int32_t pr0 = 0; pr0 < ks_n; pr0 += 4) {
               float4 a4[4][8];
 #pragma unroll
               for (int u = 0; u < 4; ++u) {
-                if (pr0 + u < ks_n) {
-                  const uint32_t base = mapa_shared(smem_u32(ring), (uint32_t)(pr0 + u)) + off;
+                const int32_t pr = pr0 + u;
+                if (pr < ks_n && !(via_l2 && pr == ks_r)) {
+                  if constexpr (via_l2) {
+                    const float4* src = reinterpret_cast<const float4*>(
+                                            p.sk_ws + ((cta0 + pr) * 4 + q) * SK_WARP_FLOATS + c32 * SK_CHUNK_FLOATS) +
+                                        lane;
 #pragma unroll
-                  for (int j = 0; j < 8; ++j) a4[u][j] = ld_cluster_f32x4(base + 512u * j);
+                    for (int j = 0; j < 8; ++j) a4[u][j] = ld_cg_f32x4(src + j * 32);
+                  } else {
+                    const uint32_t base =
+                        mapa_shared(smem_u32(ring), (uint32_t)pr) +
+                        (uint32_t)(((int)q * (WS_BN / 32) + c32) * SK_CHUNK_FLOATS + (int)lane * 4) * 4u;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) a4[u][j] = ld_cluster_f32x4(base + 512u * j);
+                  }
                 }
               }
 #pragma unroll
               for (int u = 0; u < 4; ++u) {
-                if (pr0 + u < ks_n) {
+                const int32_t pr = pr0 + u;
+                if (pr < ks_n) {
+                  if (via_l2 && pr == ks_r) {
+                    uint32_t o[32];
+                    tmem_ld_32x32b_x32(tbase + (uint32_t)(c32 * 32), o);
+                    tmem_wait_ld();
 #pragma unroll
-                  for (int j = 0; j < 8; ++j) {
-                    v[4 * j] = __float_as_uint(__uint_as_float(v[4 * j]) + a4[u][j].x);
-                    v[4 * j + 1] = __float_as_uint(__uint_as_float(v[4 * j + 1]) + a4[u][j].y);
-                    v[4 * j + 2] = __float_as_uint(__uint_as_float(v[4 * j + 2]) + a4[u][j].z);
-                    v[4 * j + 3] = __float_as_uint(__uint_as_float(v[4 * j + 3]) + a4[u][j].w);
+                    for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) + __uint_as_float(o[j]));
+                  } else {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                      v[4 * j] = __float_as_uint(__uint_as_float(v[4 * j]) + a4[u][j].x);
+                      v[4 * j + 1] = __float_as_uint(__uint_as_float(v[4 * j + 1]) + a4[u][j].y);
+                      v[4 * j + 2] = __float_as_uint(__uint_as_float(v[4 * j + 2]) + a4[u][j].z);
+                      v[4 * j + 3] = __float_as_uint(__uint_as_float(v[4 * j + 3]) + a4[u][j].w);
+                    }
                   }
                 }
               }
@@ -1153,7 +1194,7 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
           }
           continue;
         }
-        if constexpr (!KS && !DRAIN && !DRAIN32) {
+        if constexpr (KS == 0 && !DRAIN && !DRAIN32) {
           static_assert(TAIL == 0, "224-column tiles drain their accumulator first");
 #pragma unroll 1
           for (int ch = 0; ch < NCH; ++ch) {
@@ -1251,7 +1292,7 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
   __syncwarp();
   tc_fence_before();
   __syncthreads();
-  if constexpr (CG == 2 || KS) cluster_sync_all();
+  if constexpr (CG == 2 || KS != 0) cluster_sync_all();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc<CG>(tmem, 512);
@@ -1276,12 +1317,15 @@ __global__ void __launch_bounds__(mx_threads(NCONS), 1)
   ws_body<OutT, CG, NCONS, SCHED, EPI, true, false, BN>(&tmA, &tmB, &tmC, &tmSA, &tmSB, p);
 }
 
-// entry point of the split-K cluster kernels (step 7 tile, plain writeback)
-template <typename OutT>
+// entry point of the split-K cluster kernels (step 7 tile, plain writeback);
+// L2: clusters of more than two CTAs, partials exchanged through L2.  Each form
+// is its own kernel: with both in one, the larger writeback code slowed the
+// two-CTA form by 4 % (512 x 4096 x 4096: 742 against 770 TFLOP/s)
+template <typename OutT, bool L2>
 __global__ void __launch_bounds__(WS_THREADS, 1)
     k_ws_ks(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
             const __grid_constant__ CUtensorMap tmC, KParams p) {
-  ws_body<OutT, 1, 1, SCHED_STATIC, -1, false, false, WS_BN, true>(&tmA, &tmB, &tmC, nullptr, nullptr, p);
+  ws_body<OutT, 1, 1, SCHED_STATIC, -1, false, false, WS_BN, L2 ? 2 : 1>(&tmA, &tmB, &tmC, nullptr, nullptr, p);
 }
 
 // entry point of the stream-K kernels (static schedule, plain writeback)

@@ -322,6 +322,17 @@ __device__ __forceinline__ uint32_t cluster_nctarank() {
 // that other CTAs of the cluster observe
 __device__ __forceinline__ void fence_cluster() { asm volatile("fence.acq_rel.cluster;" ::: "memory"); }
 
+// 16-byte global load served by L2 (not this SM's L1, which may hold a line an
+// earlier launch read before another SM rewrote it)
+__device__ __forceinline__ float4 ld_cg_f32x4(const float4* p) {
+  float4 v;
+  asm volatile("ld.global.cg.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "l"(p)
+               : "memory");
+  return v;
+}
+
 __device__ __forceinline__ float4 ld_cluster_f32x4(uint32_t cluster_addr) {
   float4 v;
   asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"

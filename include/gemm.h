@@ -18,8 +18,11 @@
  * buffers.  A plan owns host state (cached TMA descriptors) and 256 bytes of
  * device scratch (a status word and scheduler counters), plus, for the
  * stream-K schedule, a workspace of one fp32 tile per cluster (about 38 MB on
- * 76 CTA pairs with 512 x 256 tiles), all released by gemm_plan_destroy.  Two
- * launches of one plan must not overlap on the device.
+ * 76 CTA pairs with 512 x 256 tiles), or for a K split over a cluster of 3-8
+ * CTAs one fp32 128 x 256 partial per CTA (19 MB at most for an automatic split
+ * on 152 SMs),
+ * all released by gemm_plan_destroy.  Two launches of one plan must not
+ * overlap on the device.
  *
  * Errors: argument problems are returned at once and nothing is launched.
  * Kernels never trap: every wait inside them is bounded in time, and a wait
@@ -122,8 +125,10 @@ typedef struct {
   int32_t max_ctas;     /* cap on persistent CTAs / clusters, 0 = no cap */
   int32_t split_k;      /* GEMV_TC: CTAs (a cluster) sharing one 128-row block's K range,
                            1, 2, 4 or 8; variant 7: CTAs (a cluster, 2-8) sharing one
-                           128 x 256 tile's K range, their fp32 partials added over
-                           distributed shared memory, 1 = never; 0 = automatic (variant 7
+                           128 x 256 tile's K range, their fp32 partials exchanged over
+                           distributed shared memory (2 CTAs) or through a plan workspace
+                           of 128 KB per CTA (3-8; a split needing over 512 MB gives
+                           GEMM_ERR_UNSUPPORTED_SHAPE), 1 = never; 0 = automatic (variant 7
                            splits when its tiles would fill at most half the SMs,
                            into as many CTAs per tile as fit, at most 4, each
                            keeping at least 16 K blocks) */

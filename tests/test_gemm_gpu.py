@@ -518,7 +518,8 @@ def test_stream_k_small_output_random_parity():
     assert r["ok"] and r["max_excess_rel"] < 2.0 ** -12, r
 
 
-# step 7 with K split over a cluster (partials added over distributed shared memory)
+# step 7 with K split over a cluster (partials exchanged over distributed shared memory for two
+# CTAs, through the plan's L2-resident workspace for more)
 KS_CASES = [(1024, 1024, 4096, 0), (512, 1024, 8192, 0), (256, 512, 2048, 0), (300, 520, 1040, 2),
             (129, 1288, 2056, 3), (640, 264, 4104, 5), (256, 512, 8192, 8)]
 # automatic split: as many CTAs per tile as the SMs hold (152 SMs), at most 4, each keeping
@@ -566,6 +567,10 @@ def test_split_k_cluster_random_parity_and_refusals():
     p1 = gemm.Plan(M, N, K, gemm.BF16_F32, gemm.make_opts(split_k=1))
     assert p1.info()["cluster"] == 1
     p1.destroy()
+    # a forced split whose workspace (128 KB per CTA) would exceed 512 MB:
+    # 64 x 32 tiles x 8 CTAs
+    with pytest.raises(gemm.GemmError):
+        gemm.Plan(8192, 8192, 1024, gemm.BF16_BF16, gemm.make_opts(variant=gemm.S7, split_k=8))
 
 
 # extreme aspect ratios: a 65536-deep K loop, 512 tile columns of one tile row, 256 tile rows
