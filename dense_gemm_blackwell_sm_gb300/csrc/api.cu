@@ -203,6 +203,27 @@ bool ws_stream_k_applies(int64_t M, int64_t N, int units) {
 // Measured against the former rule (the largest tile that gives every CTA pair a
 // tile): 2048 x 4096 x 4096 step 9 1550 TFLOP/s against step 8 1364; 256 x 14336 x
 // 4096 step 8 970 against step 7 862; 1024 x 8192 x 8192 step 9 1682 against 1466.
+// Clusters of c one-CTA-per-SM kernels resident at once (cudaOccupancyMaxActiveClusters
+// on the 152-SM GB300: its GPCs hold 15 clusters of 8 and 23 of 6), scaled to sms.
+int cluster_capacity(int c, int sms) {
+  static const int cap152[9] = {0, 152, 76, 46, 36, 28, 23, 15, 15};
+  if (c < 1 || c > 8) return 0;
+  return (int)((int64_t)cap152[c] * sms / 152);
+}
+
+// The K split (2-4 slices, 0 = none) for tiles of cg CTAs (128 x 256 per CTA: cg 1
+// step 7, cg 2 step 8's pair): the most slices that keep 16 K blocks each, one CTA
+// per SM, and all clusters resident at once (16 clusters of 8 do not fit: the
+// 1024 x 1024 x 4096 pairs split 4 ways ran at 315 TFLOP/s, 3 ways fit).
+int ks_split_for(int64_t M, int64_t N, int64_t kb, int sms, int cg) {
+  const int64_t tiles = ((M + 128 * cg - 1) / (128 * cg)) * ((N + 255) / 256);
+  for (int s = 4; s >= 2; --s) {
+    if (s * cg > 8 || kb / s < 16 || tiles * s * cg > sms || tiles > cluster_capacity(s * cg, sms)) continue;
+    return s;
+  }
+  return 0;
+}
+
 int auto_variant(int64_t M, int64_t N, int64_t K, gemm_dtype_t dt, int sms) {
   if (M <= 2 && gemv_smem_bytes((int)M, (int)K) <= 200 * 1024) return GEMM_VARIANT_GEMV;
   if (M >= 3 && M <= 8) return GEMM_VARIANT_GEMV;
@@ -211,7 +232,16 @@ int auto_variant(int64_t M, int64_t N, int64_t K, gemm_dtype_t dt, int sms) {
   const int pairs = std::max(1, sms / 2);
   const int64_t tiles7 = ((M + 127) / 128) * ((N + 255) / 256);
   const int64_t kb = k_blocks(K, dt);
-  if (tiles7 * 2 <= sms && kb >= 32) return GEMM_VARIANT_S7_WARP_SPECIALIZED;
+  if (tiles7 * 2 <= sms && kb >= 32) {
+    // K split over a cluster: on step 8's CTA pairs (a pair's CTA loads 32 KB per K
+    // block, a step-7 CTA 48 KB) unless they would leave more SMs idle: 512 x 4096 x
+    // 4096 783 -> 869 TFLOP/s, 512 x 1024 x 8192 400 -> 443, but 1024 x 1024 x 4096
+    // 548 on 128 single CTAs against 511 on 96 (16 pairs x 3 slices)
+    const int s7 = ks_split_for(M, N, kb, sms, 1), s8 = ks_split_for(M, N, kb, sms, 2);
+    const int64_t tiles8 = ((M + 255) / 256) * ((N + 255) / 256);
+    if (s8 && (!s7 || tiles8 * s8 * 2 >= tiles7 * s7)) return GEMM_VARIANT_S8_CTA_PAIR;
+    return GEMM_VARIANT_S7_WARP_SPECIALIZED;
+  }
   double c9 = std::min(ws_tile_cost(M, N, 512, 256, 2, pairs, kRate9, kb, kFixed9),
                        ws_tile_cost(M, N, 512, 224, 2, pairs, kRate9, kb, kFixed9));
   if (ws_stream_k_applies(M, N, pairs)) c9 = std::min(c9, ws_stream_k_cost(M, N, pairs, kb));
@@ -341,7 +371,7 @@ gemm_status_t prepare_launch(gemm_plan_s* p) {
     } else if (p->in_mx) {
       e = spec_mx(p->cg, p->sched - 1, p->out_f32, p->stages, p->grid_units, &p->spec, -1, p->consumers);
     } else if (p->ks_split >= 2) {
-      e = spec_ws_ks(p->out_f32, p->stages, p->tiles_m * p->tiles_n, p->ks_split, &p->spec);
+      e = spec_ws_ks(p->cg, p->out_f32, p->stages, p->tiles_m * p->tiles_n, p->ks_split, &p->spec);
     } else {
       e = spec_ws(p->cg, p->consumers, p->sched - 1, p->out_f32, p->stages, p->grid_units, &p->spec, -1, p->tile_n);
     }
@@ -387,8 +417,10 @@ gemm_status_t build_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, co
     if (!is_ws(variant)) return GEMM_ERR_UNSUPPORTED_SHAPE;
   }
   if (o.split_k >= 2 && is_ws(variant) && !is_mx(dtype)) {
-    // a K split over a cluster exists for step 7's tile (and the tensor-core GEMV)
-    if (variant != GEMM_VARIANT_S7_WARP_SPECIALIZED) return GEMM_ERR_UNSUPPORTED_SHAPE;
+    // a K split over a cluster exists for step 7's tile, step 8's pair tile (at
+    // most 4 slices: 8 CTAs per cluster) and the tensor-core GEMV
+    if (variant == GEMM_VARIANT_S8_CTA_PAIR ? o.split_k > 4 : variant != GEMM_VARIANT_S7_WARP_SPECIALIZED)
+      return GEMM_ERR_UNSUPPORTED_SHAPE;
   }
   if (o.layout != 0) {
     // MN-major operands exist in the warp-specialised kernels only
@@ -528,24 +560,27 @@ gemm_status_t build_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, co
       const int waves = (tiles + active - 1) / active;
       if ((double)tiles / ((double)waves * active) < 0.7) p->sched = GEMM_SCHED_STREAM_K;
     }
-    // Step 7 with few tiles for the GPU: split each tile's K over a cluster of CTAs
-    // (opts.split_k = 2-8 asks for it, 1 forbids it).  Automatic: as many CTAs per
-    // tile as the SMs hold at once, at most 4, while each keeps at least 16 K
-    // blocks; with shorter shares the partial sums cost more than the extra SMs
-    // bring (1024 x 1024 x 4096: 320 TFLOP/s whole, 416 split 2, 491 split 4).
-    // Clusters of 8 such CTAs do not all fit at once (512 x 1024 x 8192 on 16
-    // tiles: 416 split 4, 250 split 8).
-    if (variant == GEMM_VARIANT_S7_WARP_SPECIALIZED && !p->in_mx && o.layout == 0 &&
-        (o.sched == 0 || o.sched == GEMM_SCHED_STATIC) && p->sched != GEMM_SCHED_STREAM_K && o.split_k != 1) {
+    // Steps 7 and 8 with few tiles for the GPU: split each tile's K over a cluster
+    // of CTAs (opts.split_k = 2-8 asks for it, 2-4 on step 8's pairs, 1 forbids it).
+    // Automatic (ks_split_for): as many slices as the SMs hold at once, at most 4,
+    // while each keeps at least 16 K blocks; with shorter shares the partial sums
+    // cost more than the extra SMs bring (1024 x 1024 x 4096 on step 7: 320 TFLOP/s
+    // whole, 416 split 2, 491 split 4).  Clusters of 8 single CTAs do not all fit at
+    // once (512 x 1024 x 8192 on 16 tiles: 416 split 4, 250 split 8).
+    if ((variant == GEMM_VARIANT_S7_WARP_SPECIALIZED || variant == GEMM_VARIANT_S8_CTA_PAIR) && !p->in_mx &&
+        o.layout == 0 && (o.sched == 0 || o.sched == GEMM_SCHED_STATIC) && p->sched != GEMM_SCHED_STREAM_K &&
+        o.split_k != 1) {
       const int64_t kb = (K + (p->in_f8 ? 128 : 64) - 1) / (p->in_f8 ? 128 : 64);
       int64_t split = o.split_k;
-      if (!split && tiles > 0) split = std::min<int64_t>(4, std::min<int64_t>(sms / tiles, kb / 16));
-      if (split >= 2 && split <= kb) {
+      if (!split && tiles > 0) split = ks_split_for(M, N, kb, sms, p->cg);
+      if (split >= 2 && split <= kb && split * p->cg <= 8) {
         p->ks_split = (int)split;
         p->sched = GEMM_SCHED_STATIC;
-        if (split == 2) p->stages = std::max(p->stages, 3);  // the partial parks in the ring
-        p->smem = ws_smem_bytes(1, 1, p->stages);
-        p->grid_units = tiles * (int)split;
+        // two slices exchange their 128 KB partials through their stage rings
+        if (split == 2)
+          while ((size_t)p->stages * ws_shape(p->cg, 1).stage_bytes < (size_t)128 * 1024) ++p->stages;
+        p->smem = ws_smem_bytes(p->cg, 1, p->stages);
+        p->grid_units = tiles * (int)split * p->cg;  // CTAs
       }
     }
     if (p->sched == GEMM_SCHED_STREAM_K && !o.max_ctas) {
@@ -1088,7 +1123,7 @@ gemm_status_t gemm_plan_info(gemm_plan_t p, gemm_plan_info_t* info) {
   info->tile_m = p->tile_m;
   info->tile_n = p->tile_n;
   info->cluster = (p->variant == GEMM_VARIANT_GEMV) ? (int32_t)p->spec.cluster
-                  : (p->ks_split >= 2)                ? p->ks_split
+                  : (p->ks_split >= 2)                ? p->ks_split * p->cg
                                                       : p->cg;
   info->consumers = p->consumers;
   info->grid = (int32_t)(p->spec.grid.x * p->spec.grid.y);

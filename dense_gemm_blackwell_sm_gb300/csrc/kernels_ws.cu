@@ -120,21 +120,26 @@ int ws_max_active_clusters(int cg, int consumers, int sched, bool out_f32, int s
   return n;
 }
 
-cudaError_t spec_ws_ks(bool out_f32, int stages, int tiles, int split, LaunchSpec* out) {
-  void* k = split > 2 ? (out_f32 ? reinterpret_cast<void*>(k_ws_ks<float, true>)
-                                 : reinterpret_cast<void*>(k_ws_ks<__nv_bfloat16, true>))
-                      : (out_f32 ? reinterpret_cast<void*>(k_ws_ks<float, false>)
-                                 : reinterpret_cast<void*>(k_ws_ks<__nv_bfloat16, false>));
-  // a cluster of two parks its 128 KB partial in its stage ring
-  if (split < 2 || split > 8 || stages < (split == 2 ? 3 : 1)) return cudaErrorInvalidValue;
-  const size_t smem = ws_smem_bytes(1, 1, stages);
+template <typename OutT, int CG>
+void* ks_kernel(bool l2) {
+  return l2 ? reinterpret_cast<void*>(k_ws_ks<OutT, true, CG>) : reinterpret_cast<void*>(k_ws_ks<OutT, false, CG>);
+}
+
+cudaError_t spec_ws_ks(int cg, bool out_f32, int stages, int tiles, int split, LaunchSpec* out) {
+  if ((cg != 1 && cg != 2) || split < 2 || split * cg > 8) return cudaErrorInvalidValue;
+  const bool l2 = split > 2;
+  void* k = cg == 1 ? (out_f32 ? ks_kernel<float, 1>(l2) : ks_kernel<__nv_bfloat16, 1>(l2))
+                    : (out_f32 ? ks_kernel<float, 2>(l2) : ks_kernel<__nv_bfloat16, 2>(l2));
+  // two slices exchange their 128 KB partials through their stage rings
+  if (!l2 && (size_t)stages * ws_shape(cg, 1).stage_bytes < (size_t)128 * 1024) return cudaErrorInvalidValue;
+  const size_t smem = ws_smem_bytes(cg, 1, stages);
   cudaError_t e = allow_dynamic_smem((const void*)k, smem);
   if (e != cudaSuccess) return e;
   out->func = k;
-  out->grid = dim3((unsigned)(tiles * split), 1, 1);
+  out->grid = dim3((unsigned)(tiles * split * cg), 1, 1);
   out->block = dim3(WS_THREADS, 1, 1);
   out->smem = smem;
-  out->cluster = (unsigned)split;
+  out->cluster = (unsigned)(split * cg);
   out->kind = ARGS_ABC_K;
   return cudaSuccess;
 }

@@ -193,8 +193,8 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
   static_assert(!MX9 || (CG == 2 && BN == 224 && EPI < 0 && sizeof(OutT) == 2 && !SK && !KS),
                 "MX with two consumers: CTA pair, 224-column tiles, plain bf16 writeback");
   static_assert(BN == WS_BN || ((!MX || MX9) && !SK && EPI < 0), "narrow tiles: plain writeback, whole tiles");
-  static_assert(!KS || (CG == 1 && NCONS == 1 && !MX && !SK && EPI < 0 && BN == WS_BN),
-                "split-K clusters: step 7 tile, plain writeback");
+  static_assert(!KS || (NCONS == 1 && !MX && !SK && EPI < 0 && BN == WS_BN),
+                "split-K clusters: step 7 or step 8 tile, plain writeback");
   static_assert(!SK || (!MX && EPI < 0 && SCHED == SCHED_STATIC), "stream-K: plain writeback, static schedule");
   // MX on the pair: a separate warp copies the scales and takes tile ids from the ring
   // (warp 3 of the leader with one consumer).  On step 9 warp 8 of both CTAs
@@ -271,11 +271,17 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
   volatile uint32_t* zero_word = tmem_slot + 2;
 
   const uint32_t warp = warp_idx(), lane = lane_idx();
-  const uint32_t rank = (CG == 2) ? cluster_ctarank() : 0u;
+  // cluster rank; the CTA's half of its pair (ranks 2j and 2j + 1 form a pair), and
+  // the cluster rank of the pair's leader (the CTA itself without pairs)
+  // (compile-time 0 for the kernels whose clusters are one pair or one CTA: a
+  // run-time leader rank in the commit masks and barrier addresses cost step 8 2 %)
+  const uint32_t crank = (CG == 2 || KS != 0) ? cluster_ctarank() : 0u;
+  const uint32_t rank = (CG == 2) ? (KS != 0 ? (crank & 1u) : crank) : 0u;
+  const uint32_t lead = (KS != 0) ? (CG == 2 ? (crank & ~1u) : crank) : 0u;
   const bool leader = (rank == 0);
-  // split-K: this CTA's place in its cluster and the cluster's size
-  const int32_t ks_n = KS ? (int32_t)cluster_nctarank() : 1;
-  const int32_t ks_r = KS ? (int32_t)cluster_ctarank() : 0;
+  // split-K: this CTA's (or pair's) slice of the tile's K blocks and the number of slices
+  const int32_t ks_n = KS ? (int32_t)(cluster_nctarank() / (uint32_t)CG) : 1;
+  const int32_t ks_r = KS ? (int32_t)(crank / (uint32_t)CG) : 0;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -328,7 +334,7 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
   // from here on global memory is read and written
   grid_launch_dependents();
   grid_wait_prior();
-  const uint32_t peer_abort = (CG == 2) ? mapa_shared(smem_u32((const void*)abort_flag), rank ^ 1u) : 0u;
+  const uint32_t peer_abort = (CG == 2) ? mapa_shared(smem_u32((const void*)abort_flag), crank ^ 1u) : 0u;
   const WaitCtl w{abort_flag, p.status, p.timeout_ns, peer_abort};
   // K elements per stage: one 128-byte swizzle row of A / B (64 x 16-bit or 128 x 8-bit)
   const int32_t BKE = (p.bk > 0) ? p.bk : 64;
@@ -359,7 +365,7 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
     if constexpr (CG == 1) {
       mbar_arrive(smem_u32(ring_empty + slot));
     } else {
-      mbar_arrive_cluster(mapa_shared(smem_u32(ring_empty + slot), 0));
+      mbar_arrive_cluster(mapa_shared(smem_u32(ring_empty + slot), lead));
     }
     return true;
   };
@@ -400,8 +406,8 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
         ring_tile[slot] = t;
         mbar_arrive(smem_u32(ring_full + slot));
         if constexpr (CG == 2) {
-          st_cluster_u32(mapa_shared(smem_u32((const void*)(ring_tile + slot)), 1), (uint32_t)t);
-          mbar_arrive_cluster(mapa_shared(smem_u32(ring_full + slot), 1));
+          st_cluster_u32(mapa_shared(smem_u32((const void*)(ring_tile + slot)), lead + 1u), (uint32_t)t);
+          mbar_arrive_cluster(mapa_shared(smem_u32(ring_full + slot), lead + 1u));
         }
         if (t < 0) break;
       }
@@ -427,7 +433,7 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
           if (!sk_next(sk_it, tile, kb0, kb1)) break;
         } else if constexpr (KS != 0) {
           if (i > 0) break;  // one tile per cluster, this CTA's share of K
-          tile = (int32_t)(blockIdx.x / (uint32_t)ks_n);
+          tile = (int32_t)(blockIdx.x / (uint32_t)(ks_n * CG));
           kb0 = KB * ks_r / ks_n;
           kb1 = KB * (ks_r + 1) / ks_n;
         } else {
@@ -477,13 +483,13 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
                 if constexpr (CG == 1) {
                   tma_load_2d(smem_u32(dst + h * 8192), tmA, fb, row + 64 * h, kb * BKE);
                 } else {
-                  tma_load_2d_pair(smem_u32(dst + h * 8192), tmA, mapa_shared(fb, 0), row + 64 * h, kb * BKE);
+                  tma_load_2d_pair(smem_u32(dst + h * 8192), tmA, mapa_shared(fb, lead), row + 64 * h, kb * BKE);
                 }
               }
             } else if constexpr (CG == 1) {
               tma_load_2d(smem_u32(dst), tmA, fb, kb * BKE, row);
             } else {
-              tma_load_2d_pair(smem_u32(dst), tmA, mapa_shared(fb, 0), kb * BKE, row);
+              tma_load_2d_pair(smem_u32(dst), tmA, mapa_shared(fb, lead), kb * BKE, row);
             }
           }
           uint8_t* bdst = st + NCONS * WS_A_BYTES;
@@ -495,13 +501,13 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
               if constexpr (CG == 1) {
                 tma_load_2d(smem_u32(bdst + h * 8192), tmB, fb, n_cta + 64 * h, kb * BKE);
               } else {
-                tma_load_2d_pair(smem_u32(bdst + h * 8192), tmB, mapa_shared(fb, 0), n_cta + 64 * h, kb * BKE);
+                tma_load_2d_pair(smem_u32(bdst + h * 8192), tmB, mapa_shared(fb, lead), n_cta + 64 * h, kb * BKE);
               }
             }
           } else if constexpr (CG == 1) {
             tma_load_2d(smem_u32(bdst), tmB, fb, kb * BKE, n_cta);
           } else {
-            tma_load_2d_pair(smem_u32(bdst), tmB, mapa_shared(fb, 0), kb * BKE, n_cta);
+            tma_load_2d_pair(smem_u32(bdst), tmB, mapa_shared(fb, lead), kb * BKE, n_cta);
           }
           if constexpr (MX && !MX9) {
             // tiled scale layout: block (row block, K block) at ((row block) * KB + kb) * 512,
@@ -514,8 +520,8 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
               tma_load_2d(smem_u32(sd), tmSA, fb, 0, ya);
               tma_load_4d(smem_u32(sd + MX_BLOCK), tmSB, fb, 0, 0, kb, n_tile / 128);
             } else {
-              tma_load_2d_pair(smem_u32(sd), tmSA, mapa_shared(fb, 0), 0, ya);
-              tma_load_4d_pair(smem_u32(sd + MX_BLOCK), tmSB, mapa_shared(fb, 0), 0, 0, kb, n_tile / 128);
+              tma_load_2d_pair(smem_u32(sd), tmSA, mapa_shared(fb, lead), 0, ya);
+              tma_load_4d_pair(smem_u32(sd + MX_BLOCK), tmSB, mapa_shared(fb, lead), 0, 0, kb, n_tile / 128);
             }
           }
           ++issued;
@@ -604,10 +610,10 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
                                  p.idesc | ((uint32_t)k << 4) | ((uint32_t)k << 29), sft + 4u * (uint32_t)c, sft + 8u,
                                  acc0 | (uint32_t)k);
           }
-          mma_commit_pair(smem_u32(empty + stage), 3);
+          mma_commit_pair(smem_u32(empty + stage), 3u << lead);
         }
         if (!ok) break;
-        for (int c = 0; c < 2; ++c) mma_commit_pair(smem_u32(acc_full + c), 3);
+        for (int c = 0; c < 2; ++c) mma_commit_pair(smem_u32(acc_full + c), 3u << lead);
       }
       // every MMA and copy this thread issued must be complete before TMEM is released
       mma_commit_cg<CG>(smem_u32(drain_bar));
@@ -626,7 +632,7 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
           if (!sk_next(sk_it, tile, kb0, kb1)) break;
         } else if constexpr (KS != 0) {
           if (i > 0) break;
-          tile = (int32_t)(blockIdx.x / (uint32_t)ks_n);
+          tile = (int32_t)(blockIdx.x / (uint32_t)(ks_n * CG));
           kb0 = KB * ks_r / ks_n;
           kb1 = KB * (ks_r + 1) / ks_n;
         } else {
@@ -693,7 +699,7 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
           if constexpr (CG == 1) {
             mma_commit(smem_u32(empty + stage));
           } else {
-            mma_commit_pair(smem_u32(empty + stage), 3);
+            mma_commit_pair(smem_u32(empty + stage), 3u << lead);
           }
           if (++stage == (uint32_t)S) { stage = 0; sphase ^= 1u; }
         }
@@ -701,7 +707,7 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
         if constexpr (CG == 1) {
           mma_commit(smem_u32(acc_full + slot));
         } else {
-          mma_commit_pair(smem_u32(acc_full + slot), 3);
+          mma_commit_pair(smem_u32(acc_full + slot), 3u << lead);
         }
       }
       // every MMA this thread issued must be complete before TMEM is released
@@ -785,7 +791,7 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
           if (leader) {
             mbar_arrive(smem_u32(sf_grouped + stage));
           } else {
-            mbar_arrive_cluster(mapa_shared(smem_u32(sf_grouped + stage), 0));
+            mbar_arrive_cluster(mapa_shared(smem_u32(sf_grouped + stage), lead));
           }
         }
         if (++stage == (uint32_t)S) { stage = 0; sphase ^= 1u; }
@@ -806,7 +812,7 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
         if (!sk_next(sk_it, tile, kb0, kb1)) break;
       } else if constexpr (KS != 0) {
         if (i > 0) break;
-        tile = (int32_t)(blockIdx.x / (uint32_t)ks_n);
+        tile = (int32_t)(blockIdx.x / (uint32_t)(ks_n * CG));
       } else {
         uint32_t okr = 1;
         if (lane == 0) okr = ring_get(i, tile) ? 1u : 0u;
@@ -887,7 +893,7 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
             if (s32 == BN / 32 - 1) {
               tc_fence_before();
               __syncwarp();
-              if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(acc_empty + slot), 0));
+              if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(acc_empty + slot), lead));
             }
             const int32_t col0 = col_base + s32 * 32;
             apply_epilogue32<OutT, EPI>(v, p, col0, epi_sa, epi_res, res, epi_cols + s32 * 32, epi_cols + BN + s32 * 32);
@@ -932,7 +938,7 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
                   if constexpr (CG == 1) {
                     mbar_arrive(smem_u32(acc_empty + slot));
                   } else {
-                    mbar_arrive_cluster(mapa_shared(smem_u32(acc_empty + slot), 0));
+                    mbar_arrive_cluster(mapa_shared(smem_u32(acc_empty + slot), lead));
                   }
                 }
               }
@@ -974,7 +980,7 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
           // shared memory)
           constexpr bool via_l2 = KS == 2;
           const int32_t cb = (WS_BN / 32) * ks_r / ks_n, ce = (WS_BN / 32) * (ks_r + 1) / ks_n;
-          const int64_t cta0 = (int64_t)blockIdx.x - ks_r;  // the cluster's first CTA
+          const int64_t cta0 = (int64_t)blockIdx.x - crank + rank;  // slice 0's CTA of this pair half
           if constexpr (via_l2) {
             float* mine = p.sk_ws + ((int64_t)blockIdx.x * 4 + q) * SK_WARP_FLOATS;
 #pragma unroll 1
@@ -997,7 +1003,7 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
           }
           fence_cluster();
           __syncwarp();
-          if (lane < (uint32_t)ks_n) mbar_arrive_cluster(mapa_shared(smem_u32(red_full), lane));
+          if (lane < (uint32_t)ks_n) mbar_arrive_cluster(mapa_shared(smem_u32(red_full), lane * CG + rank));
           uint32_t got2 = 1;
           if (lane == 0) got2 = mbar_wait<true>(smem_u32(red_full), 0, w, WAIT_SK_PARTIAL) ? 1u : 0u;
           got2 = __shfl_sync(0xffffffffu, got2, 0);
@@ -1017,13 +1023,13 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
                 if (pr < ks_n && !(via_l2 && pr == ks_r)) {
                   if constexpr (via_l2) {
                     const float4* src = reinterpret_cast<const float4*>(
-                                            p.sk_ws + ((cta0 + pr) * 4 + q) * SK_WARP_FLOATS + c32 * SK_CHUNK_FLOATS) +
+                                            p.sk_ws + ((cta0 + pr * CG) * 4 + q) * SK_WARP_FLOATS + c32 * SK_CHUNK_FLOATS) +
                                         lane;
 #pragma unroll
                     for (int j = 0; j < 8; ++j) a4[u][j] = ld_cg_f32x4(src + j * 32);
                   } else {
                     const uint32_t base =
-                        mapa_shared(smem_u32(ring), (uint32_t)pr) +
+                        mapa_shared(smem_u32(ring), (uint32_t)pr * CG + rank) +
                         (uint32_t)(((int)q * (WS_BN / 32) + c32) * SK_CHUNK_FLOATS + (int)lane * 4) * 4u;
 #pragma unroll
                     for (int j = 0; j < 8; ++j) a4[u][j] = ld_cluster_f32x4(base + 512u * j);
@@ -1081,7 +1087,7 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
           tmem_wait_ld();
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(acc_empty + slot), 0));
+          if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(acc_empty + slot), lead));
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
@@ -1156,7 +1162,7 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
             if constexpr (CG == 1) {
               mbar_arrive(smem_u32(acc_empty + slot));
             } else {
-              mbar_arrive_cluster(mapa_shared(smem_u32(acc_empty + slot), 0));
+              mbar_arrive_cluster(mapa_shared(smem_u32(acc_empty + slot), lead));
             }
           }
 #pragma unroll
@@ -1230,7 +1236,7 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
                 if constexpr (CG == 1) {
                   mbar_arrive(smem_u32(acc_empty + slot));
                 } else {
-                  mbar_arrive_cluster(mapa_shared(smem_u32(acc_empty + slot), 0));
+                  mbar_arrive_cluster(mapa_shared(smem_u32(acc_empty + slot), lead));
                 }
               }
             }
@@ -1321,11 +1327,11 @@ __global__ void __launch_bounds__(mx_threads(NCONS), 1)
 // L2: clusters of more than two CTAs, partials exchanged through L2.  Each form
 // is its own kernel: with both in one, the larger writeback code slowed the
 // two-CTA form by 4 % (512 x 4096 x 4096: 742 against 770 TFLOP/s)
-template <typename OutT, bool L2>
+template <typename OutT, bool L2, int CG = 1>
 __global__ void __launch_bounds__(WS_THREADS, 1)
     k_ws_ks(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
             const __grid_constant__ CUtensorMap tmC, KParams p) {
-  ws_body<OutT, 1, 1, SCHED_STATIC, -1, false, false, WS_BN, L2 ? 2 : 1>(&tmA, &tmB, &tmC, nullptr, nullptr, p);
+  ws_body<OutT, CG, 1, SCHED_STATIC, -1, false, false, WS_BN, L2 ? 2 : 1>(&tmA, &tmB, &tmC, nullptr, nullptr, p);
 }
 
 // entry point of the stream-K kernels (static schedule, plain writeback)

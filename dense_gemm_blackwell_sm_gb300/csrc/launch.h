@@ -71,10 +71,11 @@ size_t ws_sk_slot_floats(int cg, int consumers);
 // (one MMA consumer, static scheduler); -1: plain writeback
 cudaError_t spec_ws(int cg, int consumers, int sched, bool out_f32, int stages, int clusters, LaunchSpec* out,
                     int fused_act = -1, int bn = 256);
-// step 7 with K split over a cluster of `split` (2-8) CTAs per tile, the partials
-// exchanged over distributed shared memory (2) or through KParams::sk_ws (one
-// 128 KB slot per CTA); grid = tiles x split
-cudaError_t spec_ws_ks(bool out_f32, int stages, int tiles, int split, LaunchSpec* out);
+// step 7 (cg 1) or step 8 (cg 2, CTA pairs) with each tile's K split into `split`
+// slices (split * cg <= 8 CTAs per cluster), the partials exchanged over
+// distributed shared memory (2 slices) or through KParams::sk_ws (one 128 KB slot
+// per CTA); grid = tiles x split x cg
+cudaError_t spec_ws_ks(int cg, bool out_f32, int stages, int tiles, int split, LaunchSpec* out);
 
 // steps 7-9 with MX block scales (8-bit inputs, UE8M0 scale per 32 K
 // elements): cg = 1 (one CTA per 128x256 tile) or 2 (CTA pair, 256x256), one

@@ -124,14 +124,17 @@ typedef struct {
   int32_t raster_group; /* tile rows per L2 raster group, 0 = automatic */
   int32_t max_ctas;     /* cap on persistent CTAs / clusters, 0 = no cap */
   int32_t split_k;      /* GEMV_TC: CTAs (a cluster) sharing one 128-row block's K range,
-                           1, 2, 4 or 8; variant 7: CTAs (a cluster, 2-8) sharing one
-                           128 x 256 tile's K range, their fp32 partials exchanged over
-                           distributed shared memory (2 CTAs) or through a plan workspace
-                           of 128 KB per CTA (3-8; a split needing over 512 MB gives
-                           GEMM_ERR_UNSUPPORTED_SHAPE), 1 = never; 0 = automatic (variant 7
-                           splits when its tiles would fill at most half the SMs,
-                           into as many CTAs per tile as fit, at most 4, each
-                           keeping at least 16 K blocks) */
+                           1, 2, 4 or 8.  Variant 7: CTAs (a cluster, 2-8) sharing one
+                           128 x 256 tile's K range; variant 8: CTA pairs (2-4 slices,
+                           clusters of 4-8 CTAs) sharing one 256 x 256 tile's.  The fp32
+                           partials of two slices are exchanged over distributed shared
+                           memory, of 3-8 through a plan workspace of 128 KB per CTA (a
+                           split needing over 512 MB gives GEMM_ERR_UNSUPPORTED_SHAPE).
+                           1 = never; 0 = automatic: when step 7's tiles would fill at
+                           most half the SMs, the K range is split into as many slices
+                           as the SMs hold with every cluster resident at once, at most
+                           4, each keeping at least 16 K blocks, on step 8's pairs
+                           unless they would occupy fewer SMs than step 7's CTAs */
   int64_t timeout_ns;   /* bound on every device-side wait, 0 = 2 s */
   int32_t debug_flags;  /* test hooks: 1 = leave out one TMA load (forces a timeout) */
   int32_t flags;        /* GEMM_FLAG_* */
@@ -161,8 +164,10 @@ typedef struct gemm_plan_s* gemm_plan_t;
 typedef struct {
   int32_t variant, sched, stages, raster_group;
   int32_t tile_m, tile_n;  /* output tile of one CTA (or CTA pair / cluster) */
-  int32_t cluster;         /* CTAs per cluster (1 or 2; the CUDA-core GEMV for 3 <= M <= 8
-                              takes 2 when its 16-row clusters fit one wave) */
+  int32_t cluster;         /* CTAs per cluster: 1, or 2 for a CTA pair (variants 8-9); with a
+                              K split over a cluster, slices x CTAs per tile (2-8); the
+                              CUDA-core GEMV for 3 <= M <= 8 takes 2 when its 16-row
+                              clusters fit one wave */
   int32_t consumers;       /* MMA consumers per CTA */
   int32_t grid;            /* CTAs launched */
   int32_t smem_bytes;      /* dynamic shared memory per CTA */

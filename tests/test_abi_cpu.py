@@ -170,7 +170,8 @@ AUTO_CASES = [
     ((8192, 14336, 4096, gemm.BF16_BF16), gemm.S9),
     ((4096, 4096, 4096, gemm.F16_F32), gemm.S9),        # (512 x 224 tiles chosen by the plan)
     ((2048, 4096, 4096, gemm.BF16_BF16), gemm.S9),      # one wave of 76 (or 64) pair tiles
-    ((1024, 1024, 4096, gemm.BF16_BF16), gemm.S7),      # 32 tiles: split-K over clusters
+    ((1024, 1024, 4096, gemm.BF16_BF16), gemm.S7),      # 32 tiles: K split 4 ways (16 pairs split 3 ways: fewer SMs)
+    ((512, 4096, 4096, gemm.BF16_BF16), gemm.S8),       # 32 pair tiles: K split 2 ways
     ((1024, 1024, 1024, gemm.BF16_BF16), gemm.S7),      # too few K blocks to split; short K favours step 7
     ((256, 14336, 4096, gemm.BF16_BF16), gemm.S8),      # 56 pair tiles beat 112 single tiles
     ((1024, 4096, 4096, gemm.BF16_BF16), gemm.S8),

@@ -522,18 +522,30 @@ def test_stream_k_small_output_random_parity():
 # CTAs, through the plan's L2-resident workspace for more)
 KS_CASES = [(1024, 1024, 4096, 0), (512, 1024, 8192, 0), (256, 512, 2048, 0), (300, 520, 1040, 2),
             (129, 1288, 2056, 3), (640, 264, 4104, 5), (256, 512, 8192, 8)]
-# automatic split: as many CTAs per tile as the SMs hold (152 SMs), at most 4, each keeping
-# >= 16 K blocks
+# automatic split: as many slices per tile as the SMs hold (152 SMs) with every cluster
+# resident at once, at most 4, each keeping >= 16 K blocks; the automatic plan takes step 8's
+# CTA pairs unless they would occupy fewer SMs (1024 x 1024 x 4096 stays on step 7)
 KS_AUTO = {(1024, 1024, 4096): 4, (512, 1024, 8192): 4, (256, 512, 2048): 2}
 
 
-@pytest.mark.parametrize("M,N,K,split", KS_CASES)
+# step 8's 256 x 256 tile on a CTA pair with K split into 2-4 slices (clusters of 4-8 CTAs)
+KS_PAIR_CASES = [(1024, 1024, 4096, 4), (512, 4096, 4096, 2), (300, 520, 1040, 2), (129, 1288, 2056, 3),
+                 (640, 264, 4104, 4), (256, 512, 8192, 4)]
+KS_AUTO_PAIR = {(1024, 1024, 4096): 3, (512, 1024, 8192): 4, (256, 512, 2048): 2}
+
+
+@pytest.mark.parametrize("M,N,K,split,variant", [c + (gemm.S7,) for c in KS_CASES] +
+                         [c + (gemm.S8,) for c in KS_PAIR_CASES])
 @pytest.mark.parametrize("ti,to", [("bf16", "bf16"), ("f16", "f32")])
-def test_split_k_cluster_bit_exact(M, N, K, split, ti, to):
+def test_split_k_cluster_bit_exact(M, N, K, split, variant, ti, to):
     a, b = inputs.integer_operands(M, N, K, ti, seed=M + split)
-    plan = gemm.Plan(M, N, K, gemm.dtype_code(ti, to), gemm.make_opts(variant=gemm.S7 if split else 0, split_k=split))
+    plan = gemm.Plan(M, N, K, gemm.dtype_code(ti, to), gemm.make_opts(variant=variant if split else 0, split_k=split))
     info = plan.info()
-    assert info["variant"] == gemm.S7 and info["cluster"] == (split or KS_AUTO[(M, N, K)]), info
+    if split:
+        assert info["variant"] == variant, info
+    cg = 2 if info["variant"] == gemm.S8 else 1
+    auto = KS_AUTO_PAIR if cg == 2 else KS_AUTO
+    assert info["variant"] in (gemm.S7, gemm.S8) and info["cluster"] == cg * (split or auto[(M, N, K)]), info
     assert info["grid"] == info["tiles"] * info["cluster"], info
     visits = torch.zeros(info["tiles"], dtype=torch.int32, device=DEV)
     plan.set_visits(visits)
@@ -554,7 +566,8 @@ def test_split_k_cluster_random_parity_and_refusals():
     M, N, K = 512, 4096, 4096
     a, b = inputs.make_operands(M, N, K, "bf16", ("uniform",), ("normal", 1.0), seed=9)
     plan = gemm.Plan(M, N, K, gemm.BF16_F32)
-    assert plan.info()["cluster"] == 2 and plan.info()["variant"] == gemm.S7
+    info = plan.info()
+    assert (info["variant"], info["cluster"]) in ((gemm.S7, 2), (gemm.S8, 4)), info
     c = torch.empty((M, N), device=DEV)
     plan.run(a.to(DEV), b.to(DEV), c)
     assert plan.check() == gemm.OK
@@ -565,7 +578,8 @@ def test_split_k_cluster_random_parity_and_refusals():
     with pytest.raises(gemm.GemmError):
         gemm.Plan(M, N, K, gemm.BF16_F32, gemm.make_opts(variant=gemm.S9, split_k=2))
     p1 = gemm.Plan(M, N, K, gemm.BF16_F32, gemm.make_opts(split_k=1))
-    assert p1.info()["cluster"] == 1
+    i1 = p1.info()
+    assert i1["cluster"] == (2 if i1["variant"] == gemm.S8 else 1), i1  # no K split
     p1.destroy()
     # a forced split whose workspace (128 KB per CTA) would exceed 512 MB:
     # 64 x 32 tiles x 8 CTAs
