@@ -198,7 +198,10 @@ def test_split_k_cluster_integer_bit_exact(M, N, K, split, out):
     opts = gemm.make_opts(variant=gemm.S7 if split else 0, split_k=split)
     plan = gemm.Plan(M, N, K, gemm.dtype_code("e5m2", out), opts)
     info = plan.info()
-    assert info["variant"] == gemm.S7 and info["cluster"] == (split or 2), info
+    if split:
+        assert info["variant"] == gemm.S7 and info["cluster"] == split, info
+    else:  # 32 K blocks: two slices, of step 8's pair tiles (as many SMs as step 7's)
+        assert (info["variant"], info["cluster"]) == (gemm.S8, 4), info
     c = torch.full((M, N), float("nan"), device=DEV, dtype=inputs.torch_dtype(out))
     plan.run(a.to(DEV), b.to(DEV), c)
     assert plan.check() == gemm.OK
