@@ -20,6 +20,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import os
 import subprocess
@@ -64,11 +65,22 @@ def measured_peaks() -> tuple[dict, str]:
     return dict(FALLBACK), "fallback"
 
 
+def code_tokens(src: str) -> str:
+    """A C++/CUDA source without its comments and with runs of whitespace collapsed:
+    what decides whether a kernel changed (string literals hold no comment markers in
+    these files)."""
+    src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", " ", src)
+    return " ".join(src.split())
+
+
 def source_hash(kind: str) -> str:
+    """First 16 hex digits of the sha256 of the kernel sources' code (comments and
+    layout left out), recorded with each ncu traffic capture."""
     h = hashlib.sha256()
     for rel in KERNEL_SOURCES[kind]:
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
+            h.update(code_tokens(f.read()).encode())
     return h.hexdigest()[:16]
 
 

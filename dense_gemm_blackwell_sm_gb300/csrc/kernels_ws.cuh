@@ -67,10 +67,11 @@
 // writeback warp's 32-column chunks in the layout of sk_add32, so both sides
 // move whole 4 KB runs with 512 contiguous bytes per warp access.
 //
-// Split-K within a cluster (KS template flag, step 7's 128x256 tile, plain
-// writeback): for outputs with too few tiles for the GPU, a cluster of 2-8 CTAs
-// shares one tile, CTA r accumulating K blocks [KB r / s, KB (r+1) / s) in its
-// own TMEM.  Every CTA puts its fp32 partial where the others can read it (its
+// Split-K within a cluster (KS template parameter, step 7's 128x256 tile or step
+// 8's 256x256 pair tile, plain writeback): for outputs with too few tiles for the
+// GPU, a cluster of 2-8 CTAs (2-4 pairs) shares one tile, CTA (pair) r
+// accumulating K blocks [KB r / s, KB (r+1) / s) in its own TMEM; in a pair each
+// CTA exchanges partials with the CTAs of the same pair half.  Every CTA puts its fp32 partial where the others can read it (its
 // idle stage ring for a cluster of two; otherwise, except the columns it owns,
 // its slot of the plan's workspace in L2) in the writeback warps' (warp, chunk,
 // lane) order and arrives on the barrier of every CTA of the cluster; then each
@@ -271,10 +272,10 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
   volatile uint32_t* zero_word = tmem_slot + 2;
 
   const uint32_t warp = warp_idx(), lane = lane_idx();
-  // cluster rank; the CTA's half of its pair (ranks 2j and 2j + 1 form a pair), and
-  // the cluster rank of the pair's leader (the CTA itself without pairs)
-  // (compile-time 0 for the kernels whose clusters are one pair or one CTA: a
-  // run-time leader rank in the commit masks and barrier addresses cost step 8 2 %)
+  // cluster rank; the CTA's half of its pair (ranks 2j and 2j + 1 form a pair); the
+  // cluster rank of the pair's leader (the CTA itself without pairs), a compile-time
+  // 0 where a cluster is one pair or one CTA (a run-time leader rank in the commit
+  // masks and barrier addresses cost step 8 2 %)
   const uint32_t crank = (CG == 2 || KS != 0) ? cluster_ctarank() : 0u;
   const uint32_t rank = (CG == 2) ? (KS != 0 ? (crank & 1u) : crank) : 0u;
   const uint32_t lead = (KS != 0) ? (CG == 2 ? (crank & ~1u) : crank) : 0u;
