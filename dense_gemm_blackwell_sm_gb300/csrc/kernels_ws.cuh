@@ -864,7 +864,11 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
                                                                   (int64_t)row * p.out_ld + col_base);
             const int32_t seg_bytes = min(BN, p.N - col_base) * (int32_t)sizeof(OutT);
 #pragma unroll 1
-            for (int32_t b = 128; b < seg_bytes + 127; b += 128) prefetch_l2_line(seg + min(b, seg_bytes - 1));
+            // with evict_last priority, so that less of it is gone again when the epilogue
+            // runs (8192^3 bias + SiLU + residual: DRAM reads 1019 -> 930 MB per launch,
+            // 1840 -> 1847 TFLOP/s)
+            for (int32_t b = 128; b < seg_bytes + 127; b += 128)
+              asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(seg + min(b, seg_bytes - 1)));
           }
           if (p.scale_a != nullptr) epi_sa = (row < p.M) ? __ldg(p.scale_a + row) : 0.f;
         }
