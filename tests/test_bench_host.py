@@ -41,6 +41,20 @@ def test_peaks_and_traffic_lookup():
     assert bench.stored_traffic("ws", "no_such_workload") is None
 
 
+def test_traffic_key_ignores_comments_and_layout_only():
+    a = "int f(int x) {  // doubles\n  return 2 * x; /* twice */ }\n"
+    b = "int f(int x) {\n\treturn 2 * x;\n}"
+    c = "int f(int x) { return 3 * x; }"
+    assert bench.code_tokens(a) == bench.code_tokens(b) == "int f(int x) { return 2 * x; }"
+    assert bench.code_tokens(c) != bench.code_tokens(a)
+    # every stored capture carries the key of the code it was taken on
+    import json
+    with open(bench.TRAFFIC_FILE) as f:
+        d = json.load(f)
+    for kind in ("ws", "mx", "gemv"):
+        assert all(len(e["source_hash"]) == 16 for e in d[kind].values())
+
+
 def _rank_main(rank, world, port, q):
     os.environ.update({"RANK": str(rank), "WORLD_SIZE": str(world), "LOCAL_RANK": str(rank),
                        "MASTER_ADDR": "127.0.0.1", "MASTER_PORT": str(port)})
