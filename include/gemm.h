@@ -274,7 +274,10 @@ GEMM_API gemm_status_t gemm_plan_run_mx(gemm_plan_t plan, const void* A, const v
  * ceil(rows/128) * ceil(K/128) * 512; -1 for rows < 1 or K < 1. */
 GEMM_API int64_t gemm_mx_scale_bytes(int64_t rows, int64_t K);
 
-/* One-shot form: plan (cached per shape, dtype and device) and run. */
+/* One-shot form: plan (cached per shape, dtype and device) and run.  A cached
+ * plan keeps its device scratch, and any stream-K or split-K workspace (at most
+ * about 38 MB), until gemm_clear_cache; launches through one cached plan on
+ * different streams must not overlap. */
 GEMM_API gemm_status_t gemm_run(int64_t M, int64_t N, int64_t K, const void* A, const void* B, void* C,
                        gemm_dtype_t dtype, gemm_stream_t stream);
 
@@ -336,7 +339,8 @@ GEMM_API gemm_status_t gemm_plan_set_visits(gemm_plan_t plan, int32_t* visits);
 /* Release the plan's device scratch and host state.  NULL is ignored. */
 GEMM_API void gemm_plan_destroy(gemm_plan_t plan);
 
-/* Drop every plan cached by gemm_run. */
+/* Drop every plan cached by gemm_run (and gemm_run_host), releasing their device
+ * memory; no launch through them may still be running. */
 GEMM_API void gemm_clear_cache(void);
 
 /* Static description of a status code. */
