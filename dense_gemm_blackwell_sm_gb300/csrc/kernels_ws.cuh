@@ -971,18 +971,18 @@ __device__ __forceinline__ void ws_body(const CUtensorMap* tmA, const CUtensorMa
           }
         }
         if constexpr (KS != 0) {
-          // a tile split over the cluster: CTA r adds, in rank order, the ks_n partials
-          // of its share of the tile's 32-column chunks and stores them.  The partials
-          // are kept as [warp quarter][32-column chunk] in the chunk layout of sk_add32
-          // (each 16-byte access of the warp covers 512 contiguous bytes), and every CTA
-          // arrives on every CTA's barrier once its own are in place.  Distributed shared
-          // memory moves only about 15 bytes per clock per SM, so a cluster of two parks
-          // its partials in its (idle) stage ring and reads the other CTA's there
-          // (512 x 4096 x 4096: 775 TFLOP/s, 747 through L2), while larger clusters write
-          // the chunks other CTAs own to their slots of the plan's workspace in L2 and
-          // read them back from there, each CTA's own chunks straight from TMEM
-          // (1024 x 1024 x 4096 on four CTAs: 541 TFLOP/s, 520 over distributed
-          // shared memory)
+          // a tile split over the cluster: slice r's CTA adds, in slice order, the ks_n
+          // partials of its share of the tile's 32-column chunks (of its pair half) and
+          // stores them.  The partials are kept as [warp quarter][32-column chunk] in the
+          // chunk layout of sk_add32 (each 16-byte access of the warp covers 512
+          // contiguous bytes), and every CTA arrives on the barriers of the CTAs it
+          // exchanges with once its own are in place.  Distributed shared memory moves
+          // only about 15 bytes per clock per SM, so two slices park their partials in
+          // their (idle) stage rings and read each other's there (512 x 4096 x 4096 on
+          // step 7: 775 TFLOP/s, 747 through L2), while more slices write the chunks the
+          // others own to their slots of the plan's workspace in L2 and read them back
+          // from there, each CTA's own chunks straight from TMEM (1024 x 1024 x 4096 on
+          // four CTAs: 541 TFLOP/s, 520 over distributed shared memory)
           constexpr bool via_l2 = KS == 2;
           const int32_t cb = (WS_BN / 32) * ks_r / ks_n, ce = (WS_BN / 32) * (ks_r + 1) / ks_n;
           const int64_t cta0 = (int64_t)blockIdx.x - crank + rank;  // slice 0's CTA of this pair half
