@@ -193,13 +193,32 @@ bool ws_stream_k_applies(int64_t M, int64_t N, int units) {
   return tiles >= units && (double)tiles / ((double)waves * units) < 0.7;
 }
 
+// Launch time at short K (fewer than 32 K blocks, where plans keep whole tiles and
+// never default to stream-K), in microseconds: a ramp per launch plus, per wave of
+// tiles, a fixed part and a part per K block.  Least-squares fits to bf16 launches
+// with whole tiles on 152 SMs (M and N from 2048 to 14336, K from 256 to 2048; every
+// fit within 13 %).  There the fixed costs are a large part of a tile, and
+// ws_tile_cost, whose per-tile costs were set at K >= 1024, overrates step 9:
+// 4096 x 4096 x 512 runs at 880 TFLOP/s on step 7 against 795 on step 9, 2048 x 4096
+// x 512 at 704 against 644, 4096 x 8192 x 1024 at 1327 against 1283.
+struct ShortKFit {
+  double ramp, per_kb, per_wave;
+};
+constexpr ShortKFit kShort9{3.94, 0.592, 3.57}, kShort8{5.49, 0.333, 1.54}, kShort7{3.25, 0.369, 0.98};
+double short_k_time(const ShortKFit& f, int64_t M, int64_t N, int tile_m, int tile_n, int units, int64_t kb) {
+  const int64_t tiles = ((M + tile_m - 1) / tile_m) * ((N + tile_n - 1) / tile_n);
+  const double waves = (double)((tiles + units - 1) / units);
+  return f.ramp + waves * (f.per_kb * (double)kb + f.per_wave);
+}
+
 // Automatic variant: the decode GEMV with CUDA-core FMAs for one or two rows,
 // with warp-level MMAs on registers for up to 8, on the tcgen05 Tensor Core for
 // up to 16 rows; the plain-store persistent kernel when C's rows are not 16-byte
 // aligned for TMA stores; step 7 (with its K split over a cluster) for outputs
 // whose 128 x 256 tiles fill at most half the SMs and have K blocks to split;
 // otherwise the warp-specialised step whose tiles finish soonest by ws_tile_cost
-// (step 9 with 512 x 256 or 512 x 224 tiles or stream-K, step 8, step 7).
+// (step 9 with 512 x 256 or 512 x 224 tiles or stream-K, step 8, step 7), or, below
+// 32 K blocks, by short_k_time.
 // Measured against the former rule (the largest tile that gives every CTA pair a
 // tile): 2048 x 4096 x 4096 step 9 1550 TFLOP/s against step 8 1364; 256 x 14336 x
 // 4096 step 8 970 against step 7 862; 1024 x 8192 x 8192 step 9 1682 against 1466.
@@ -241,6 +260,14 @@ int auto_variant(int64_t M, int64_t N, int64_t K, gemm_dtype_t dt, int sms) {
     const int64_t tiles8 = ((M + 255) / 256) * ((N + 255) / 256);
     if (s8 && (!s7 || tiles8 * s8 * 2 >= tiles7 * s7)) return GEMM_VARIANT_S8_CTA_PAIR;
     return GEMM_VARIANT_S7_WARP_SPECIALIZED;
+  }
+  if (kb < 32) {
+    const double t9 = std::min(short_k_time(kShort9, M, N, 512, 256, pairs, kb),
+                               short_k_time(kShort9, M, N, 512, 224, pairs, kb));
+    const double t8 = short_k_time(kShort8, M, N, 256, 256, pairs, kb);
+    const double t7 = short_k_time(kShort7, M, N, 128, 256, std::max(1, sms), kb);
+    if (t9 <= t8 && t9 <= t7) return GEMM_VARIANT_S9_TWO_CONSUMERS;
+    return (t8 <= t7) ? GEMM_VARIANT_S8_CTA_PAIR : GEMM_VARIANT_S7_WARP_SPECIALIZED;
   }
   double c9 = std::min(ws_tile_cost(M, N, 512, 256, 2, pairs, kRate9, kb, kFixed9),
                        ws_tile_cost(M, N, 512, 224, 2, pairs, kRate9, kb, kFixed9));
@@ -556,7 +583,12 @@ gemm_status_t build_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, co
     // partial sums cost more than the extra SMs bring (1024 x 1024 x 4096 on 152
     // SMs: 319 TFLOP/s with 32 whole tiles, 191 split over all SMs).  An explicit
     // GEMM_SCHED_STREAM_K still spreads such shapes over every resident cluster.
-    if (!o.sched && !p->in_mx && p->tile_n == 256 && tiles >= active && active > 0) {
+    // Nor below 32 K blocks, where a split tile's partial sums outweigh what the
+    // idle clusters lose: 4096 x 2560 x 1024 on step 9 627 TFLOP/s against 771 with
+    // whole tiles, 2048 x 3072 x 512 on step 7 380 against 532 (at 32 K blocks step
+    // 7 gains, 902 -> 952 at 2048 x 3072 x 2048, step 9 still loses, 1014 -> 938).
+    if (!o.sched && !p->in_mx && p->tile_n == 256 && tiles >= active && active > 0 &&
+        k_blocks(K, dtype) >= 32) {
       const int waves = (tiles + active - 1) / active;
       if ((double)tiles / ((double)waves * active) < 0.7) p->sched = GEMM_SCHED_STREAM_K;
     }

@@ -182,6 +182,12 @@ AUTO_CASES = [
     ((2048, 2048, 2048, gemm.BF16_BF16), gemm.S7),      # 32 K blocks: the pair's fixed cost per tile shows
     ((2048, 2048, 8192, gemm.BF16_BF16), gemm.S8),      # 128 K blocks: the pair's rate wins
     ((1024, 8192, 8192, gemm.BF16_BF16), gemm.S9),
+    # short K (fewer than 32 K blocks): launch ramp and per-wave costs decide
+    ((4096, 4096, 512, gemm.BF16_BF16), gemm.S7),       # 4 waves of 128 x 256 beat 2 of 512 x 224
+    ((2048, 4096, 512, gemm.BF16_BF16), gemm.S7),
+    ((4096, 2560, 1024, gemm.BF16_BF16), gemm.S7),      # whole tiles, no stream-K
+    ((4096, 4096, 1024, gemm.BF16_BF16), gemm.S9),
+    ((8192, 8192, 1024, gemm.BF16_BF16), gemm.S9),
 ]
 
 

@@ -393,10 +393,16 @@ def test_stream_k_is_the_default_when_the_last_wave_is_short():
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     pairs = sms // 2
     # step 9 tiles are 512 x 256: a few more tiles than CTA pairs leaves the second wave nearly empty
-    p = gemm.Plan(512 * 8, 256 * ((pairs + 8) // 8), 1024, gemm.BF16_BF16)
+    p = gemm.Plan(512 * 8, 256 * ((pairs + 8) // 8), 8192, gemm.BF16_BF16)
     info = p.info()
     p.destroy()
     assert info["variant"] == gemm.S9 and info["sched"] == gemm.SCHED_STREAM_K, info
+    # below 32 K blocks the partial sums cost more than the idle clusters: whole tiles
+    for K in (512, 1024):
+        p = gemm.Plan(512 * 8, 256 * ((pairs + 8) // 8), K, gemm.BF16_BF16)
+        info = p.info()
+        p.destroy()
+        assert info["sched"] != gemm.SCHED_STREAM_K, info
     p = gemm.Plan(8192, 8192, 8192, gemm.BF16_BF16)
     assert p.info()["sched"] == gemm.SCHED_STATIC       # 512 tiles on 76 pairs: 96 % of seven waves
     p.destroy()
