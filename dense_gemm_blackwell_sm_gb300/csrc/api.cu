@@ -183,14 +183,61 @@ double ws_tile_cost(int64_t M, int64_t N, int tile_m, int tile_n, int cluster_sm
   const int64_t waves = (tiles + units - 1) / units;
   return (double)waves * tile_m * tile_n / cluster_sms * ((double)kb + fixed) / rate;
 }
-double ws_stream_k_cost(int64_t M, int64_t N, int units, int64_t kb) {
-  const int64_t tiles = ((M + 511) / 512) * ((N + 255) / 256);
-  return (double)tiles * 512 * 256 / 2 / units * ((double)kb + kFixed9) / (kRate9 * 0.92);  // partial sums: ~8 %
+// Stream-K on step v's 256-column tiles: `tiles` tiles on `units` resident
+// clusters, kb K blocks.  Its time in K blocks of one tile is the tiles' work spread
+// evenly plus x0 + x1 * kb for the split tiles' partial sums; whole tiles take
+// waves * (kb + fixed).  Fitted on GB300 bf16 with the variants timed interleaved
+// (M 2048 / 4096, N 2560 - 5120, K 2048 - 8192): step 8 with stream-K on 4096 x 2560
+// (160 tiles, 70 % of three waves) 1162 against 1063 TFLOP/s at K = 2048, 1429
+// against 1213 at 4096; step 9 on the same shape (80 tiles, 53 % of two waves) 938
+// against 1014 at 2048 and 1305 against 1198 at 4096 (a split 512 x 256 tile carries
+// twice the partial sums of a step-8 tile).  Returns that time where the automatic
+// plan takes stream-K: it is shorter, whole tiles fill less than max_fill of their
+// waves (at 84 % step 7 lost 3-7 % and step 8 gained at most 5 %), and kb >= min_kb
+// (below, the partial sums outweigh the idle clusters: 4096 x 2560 x 1024 on step 9
+// 627 against 771); otherwise -1.
+struct StreamKModel {
+  double fixed, x0, x1, max_fill;
+  int64_t min_kb;
+};
+StreamKModel stream_k_model(int v) {
+  if (v == GEMM_VARIANT_S9_TWO_CONSUMERS) return {kFixed9, 40.0, 0.0, 0.7, 64};
+  if (v == GEMM_VARIANT_S8_CTA_PAIR) return {kFixed8, 28.0, 0.16, 0.8, 32};
+  return {kFixed7, 28.0, 0.16, 0.8, 32};
 }
-bool ws_stream_k_applies(int64_t M, int64_t N, int units) {
-  const int64_t tiles = ((M + 511) / 512) * ((N + 255) / 256);
+double ws_stream_k_time(int v, int64_t tiles, int64_t units, int64_t kb) {
+  const StreamKModel m = stream_k_model(v);
+  if (units < 1 || tiles < units || kb < m.min_kb) return -1.0;
   const int64_t waves = (tiles + units - 1) / units;
-  return tiles >= units && (double)tiles / ((double)waves * units) < 0.7;
+  if ((double)tiles / ((double)waves * units) >= m.max_fill) return -1.0;
+  const double sk = (double)tiles / units * ((double)kb + m.fixed) + m.x0 + m.x1 * (double)kb;
+  return sk < (double)waves * ((double)kb + m.fixed) ? sk : -1.0;
+}
+// ws_tile_cost of step v (tile_m rows per cluster tile, cluster_sms SMs, rate) with
+// its whole tiles, or with stream-K where the automatic plan takes it
+double ws_cost_with_stream_k(int v, int64_t M, int64_t N, int tile_m, int cluster_sms, int units, double rate,
+                             int64_t kb, double whole) {
+  const int64_t tiles = ((M + tile_m - 1) / tile_m) * ((N + 255) / 256);
+  const double sk = ws_stream_k_time(v, tiles, units, kb);
+  return sk < 0 ? whole : std::min(whole, sk * tile_m * 256 / cluster_sms / rate);
+}
+// Step 9's automatic tiling: 0 = 512 x 256 whole tiles, 1 = 512 x 224 whole tiles
+// (taken when they finish at least 3 % sooner), 2 = stream-K on 512 x 256 tiles
+// (allow_stream_k); *cost receives its ws_tile_cost
+int s9_tiling(int64_t M, int64_t N, int64_t kb, int units, bool allow_stream_k, double* cost) {
+  const double c256 = ws_tile_cost(M, N, 512, 256, 2, units, kRate9, kb, kFixed9);
+  const double c224 = ws_tile_cost(M, N, 512, 224, 2, units, kRate9, kb, kFixed9);
+  int t = (c224 < 0.97 * c256) ? 1 : 0;
+  double c = t ? c224 : c256;
+  if (allow_stream_k) {
+    const double sk = ws_cost_with_stream_k(GEMM_VARIANT_S9_TWO_CONSUMERS, M, N, 512, 2, units, kRate9, kb, c);
+    if (sk < c) {
+      t = 2;
+      c = sk;
+    }
+  }
+  if (cost) *cost = c;
+  return t;
 }
 
 // Launch time at short K (fewer than 32 K blocks, where plans keep whole tiles and
@@ -269,11 +316,12 @@ int auto_variant(int64_t M, int64_t N, int64_t K, gemm_dtype_t dt, int sms) {
     if (t9 <= t8 && t9 <= t7) return GEMM_VARIANT_S9_TWO_CONSUMERS;
     return (t8 <= t7) ? GEMM_VARIANT_S8_CTA_PAIR : GEMM_VARIANT_S7_WARP_SPECIALIZED;
   }
-  double c9 = std::min(ws_tile_cost(M, N, 512, 256, 2, pairs, kRate9, kb, kFixed9),
-                       ws_tile_cost(M, N, 512, 224, 2, pairs, kRate9, kb, kFixed9));
-  if (ws_stream_k_applies(M, N, pairs)) c9 = std::min(c9, ws_stream_k_cost(M, N, pairs, kb));
-  const double c8 = ws_tile_cost(M, N, 256, 256, 2, pairs, kRate8, kb, kFixed8);
-  const double c7 = ws_tile_cost(M, N, 128, 256, 1, std::max(1, sms), kRate7, kb, kFixed7);
+  double c9 = 0;
+  s9_tiling(M, N, kb, pairs, true, &c9);
+  const double c8 = ws_cost_with_stream_k(GEMM_VARIANT_S8_CTA_PAIR, M, N, 256, 2, pairs, kRate8, kb,
+                                          ws_tile_cost(M, N, 256, 256, 2, pairs, kRate8, kb, kFixed8));
+  const double c7 = ws_cost_with_stream_k(GEMM_VARIANT_S7_WARP_SPECIALIZED, M, N, 128, 1, std::max(1, sms), kRate7,
+                                          kb, ws_tile_cost(M, N, 128, 256, 1, std::max(1, sms), kRate7, kb, kFixed7));
   if (c9 <= c8 && c9 <= c7) return GEMM_VARIANT_S9_TWO_CONSUMERS;
   return (c8 <= c7) ? GEMM_VARIANT_S8_CTA_PAIR : GEMM_VARIANT_S7_WARP_SPECIALIZED;
 }
@@ -519,13 +567,9 @@ gemm_status_t build_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, co
     // 84 % of two waves; 152 tiles of 512 x 224 use both, 96 % of the columns useful)
     if (variant == GEMM_VARIANT_S9_TWO_CONSUMERS && !p->in_mx && o.layout == 0 &&
         (o.sched == 0 || o.sched == GEMM_SCHED_STATIC)) {
-      const int units = std::max(1, sms / 2);
-      // (below 70 % wave fill with whole 256-column tiles the automatic plan takes
-      // stream-K instead); the narrower tile needs a clear margin (3 %) by ws_tile_cost
-      const bool stream_k_instead = !o.sched && ws_stream_k_applies(M, N, units);
-      const int64_t kb = k_blocks(K, dtype);
-      if (!stream_k_instead && ws_tile_cost(M, N, 512, 224, 2, units, kRate9, kb, kFixed9) <
-                                   0.97 * ws_tile_cost(M, N, 512, 256, 2, units, kRate9, kb, kFixed9)) {
+      // (the narrower tile needs a clear margin, 3 %, by ws_tile_cost; where stream-K
+      // beats both, the automatic plan keeps 256 columns and takes it below)
+      if (s9_tiling(M, N, k_blocks(K, dtype), std::max(1, sms / 2), !o.sched, nullptr) == 1) {
         p->tile_n = 224;
         const int maxs224 = ws_max_stages(p->cg, p->consumers, 224);
         p->stages = o.stages ? std::min<int>(o.stages, maxs224) : maxs224;
@@ -574,24 +618,19 @@ gemm_status_t build_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, co
     int units = (p->sched == GEMM_SCHED_CLC) ? tiles : std::min(tiles, active);
     if (o.max_ctas && p->sched != GEMM_SCHED_CLC) units = std::max(1, std::min(units, (int)o.max_ctas));
     p->grid_units = units;
-    // stream-K by default when whole tiles would leave the clusters idle for over
-    // 30 % of the waves.  Measured on GB300: 80 tiles on 76 CTA pairs (4096 x 2560 x
-    // 8192, step 9) 1115 -> 1507 TFLOP/s; at 84 % (4096^3) the split tiles' partial
-    // sums cost more than the idle clusters (1494 -> 1242), so whole tiles stay the
-    // default there.  Only when every cluster gets at least a tile's work: with
-    // fewer tiles than clusters the shares shrink below half a tile and the
-    // partial sums cost more than the extra SMs bring (1024 x 1024 x 4096 on 152
-    // SMs: 319 TFLOP/s with 32 whole tiles, 191 split over all SMs).  An explicit
-    // GEMM_SCHED_STREAM_K still spreads such shapes over every resident cluster.
-    // Nor below 32 K blocks, where a split tile's partial sums outweigh what the
-    // idle clusters lose: 4096 x 2560 x 1024 on step 9 627 TFLOP/s against 771 with
-    // whole tiles, 2048 x 3072 x 512 on step 7 380 against 532 (at 32 K blocks step
-    // 7 gains, 902 -> 952 at 2048 x 3072 x 2048, step 9 still loses, 1014 -> 938).
-    if (!o.sched && !p->in_mx && p->tile_n == 256 && tiles >= active && active > 0 &&
-        k_blocks(K, dtype) >= 32) {
-      const int waves = (tiles + active - 1) / active;
-      if ((double)tiles / ((double)waves * active) < 0.7) p->sched = GEMM_SCHED_STREAM_K;
-    }
+    // stream-K by default where ws_stream_k_time takes it: whole tiles would leave
+    // the clusters idle for over 20 % of the waves (30 % on step 9) and the split
+    // tiles' partial sums cost less than that.  Measured on GB300: 80 tiles on 76 CTA
+    // pairs (4096 x 2560 x 8192, step 9) 1115 -> 1507 TFLOP/s; at 84 % (4096^3) the
+    // partial sums cost more than the idle clusters (1494 -> 1242).  Only when every
+    // cluster gets at least a tile's work: with fewer tiles than clusters the shares
+    // shrink below half a tile and the partial sums cost more than the extra SMs
+    // bring (1024 x 1024 x 4096 on 152 SMs: 319 TFLOP/s with 32 whole tiles, 191
+    // split over all SMs).  An explicit GEMM_SCHED_STREAM_K still spreads such shapes
+    // over every resident cluster.
+    if (!o.sched && !p->in_mx && p->tile_n == 256 &&
+        ws_stream_k_time(variant, tiles, active, k_blocks(K, dtype)) >= 0)
+      p->sched = GEMM_SCHED_STREAM_K;
     // Steps 7 and 8 with few tiles for the GPU: split each tile's K over a cluster
     // of CTAs (opts.split_k = 2-8 asks for it, 2-4 on step 8's pairs, 1 forbids it).
     // Automatic (ks_split_for): as many slices as the SMs hold at once, at most 4,

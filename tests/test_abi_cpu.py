@@ -188,6 +188,11 @@ AUTO_CASES = [
     ((4096, 2560, 1024, gemm.BF16_BF16), gemm.S7),      # whole tiles, no stream-K
     ((4096, 4096, 1024, gemm.BF16_BF16), gemm.S9),
     ((8192, 8192, 1024, gemm.BF16_BF16), gemm.S9),
+    # few waves: stream-K on step 8's pairs beats step 9 (with or without it) from 32 K blocks
+    ((4096, 2560, 2048, gemm.BF16_BF16), gemm.S8),
+    ((4096, 2560, 4096, gemm.BF16_BF16), gemm.S8),
+    ((2048, 5120, 2048, gemm.BF16_BF16), gemm.S8),
+    ((4096, 2560, 8192, gemm.BF16_BF16), gemm.S9),      # step 9's stream-K pays from 64 K blocks
 ]
 
 

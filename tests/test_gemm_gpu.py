@@ -397,6 +397,11 @@ def test_stream_k_is_the_default_when_the_last_wave_is_short():
     info = p.info()
     p.destroy()
     assert info["variant"] == gemm.S9 and info["sched"] == gemm.SCHED_STREAM_K, info
+    # step 8's 256 x 256 tiles on the same output: 160 tiles fill 70 % of three waves
+    p = gemm.Plan(512 * 8, 256 * ((pairs + 8) // 8), 4096, gemm.BF16_BF16)
+    info = p.info()
+    p.destroy()
+    assert info["variant"] == gemm.S8 and info["sched"] == gemm.SCHED_STREAM_K, info
     # below 32 K blocks the partial sums cost more than the idle clusters: whole tiles
     for K in (512, 1024):
         p = gemm.Plan(512 * 8, 256 * ((pairs + 8) // 8), K, gemm.BF16_BF16)
