@@ -106,7 +106,10 @@ def aggregate(per_rank_seconds: list[float], units_per_rank: float) -> tuple[flo
 class ClockSampler:
     """nvidia-smi clocks / power / throttle reasons sampled every 50 ms while
     work runs.  Each sample carries nvidia-smi's own timestamp, so a summary
-    can be restricted to the host-time window of one timed region."""
+    can be restricted to the host-time window of one timed region.  power.draw
+    is averaged over about a second, so a timed region of a tenth of a second
+    barely moves it; where the driver offers power.draw.instant, that decides
+    whether a sample was under load."""
     QUERY = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,enforced.power.limit,"
              "clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
@@ -118,22 +121,40 @@ class ClockSampler:
         self.proc = None
         self.lines: list[str] = []
 
+    def _start(self, query: str) -> bool:
+        """Start nvidia-smi on `query`; True once it produces samples."""
+        self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + query,
+                                      "--format=csv,noheader,nounits", "-lms", "50"],
+                                     stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        self._t = threading.Thread(target=self._read, daemon=True)
+        self._t.start()
+        # NVML start-up can hold the driver for a moment: start timing only
+        # once the sampler is producing samples
+        t0 = time.time()
+        while not self.lines and time.time() - t0 < 10.0 and self.proc.poll() is None:
+            time.sleep(0.02)
+        ok = bool(self.parse(self.lines[:1]))
+        if not ok:
+            self._stop()
+            self.lines = []
+        return ok
+
     def __enter__(self):
         try:
-            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.QUERY,
-                                          "--format=csv,noheader,nounits", "-lms", "50"],
-                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-            self._t = threading.Thread(target=self._read, daemon=True)
-            self._t.start()
-            # NVML start-up can hold the driver for a moment: start timing only
-            # once the sampler is producing samples
-            t0 = time.time()
-            while not self.lines and time.time() - t0 < 10.0:
-                time.sleep(0.02)
+            if not self._start(self.QUERY + ",power.draw.instant"):
+                self._start(self.QUERY)
             time.sleep(0.1)
         except OSError:
             self.proc = None
         return self
+
+    def _stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
 
     def _read(self):
         for line in self.proc.stdout:
@@ -142,11 +163,7 @@ class ClockSampler:
     def __exit__(self, *exc):
         if self.proc is not None:
             time.sleep(0.1)
-            self.proc.terminate()
-            try:
-                self.proc.wait(timeout=5)
-            except subprocess.TimeoutExpired:
-                self.proc.kill()
+            self._stop()
         return False
 
     @staticmethod
@@ -168,6 +185,12 @@ class ClockSampler:
                 smp["limit_w"] = float(f[5])
             except ValueError:
                 smp["w"], smp["limit_w"] = None, None
+            smp["w_inst"] = None
+            if len(f) > 11:
+                try:
+                    smp["w_inst"] = float(f[11])
+                except ValueError:
+                    pass
             smp["reasons"] = [n for n, v in zip(ClockSampler.REASONS, f[7:11]) if v.lower().startswith("active")]
             out.append(smp)
         return out
@@ -175,20 +198,29 @@ class ClockSampler:
     def summary(self, t0: float | None = None, t1: float | None = None) -> dict:
         """Median SM clock (all samples and those under load), power and throttle
         reasons, over the samples within [t0, t1] (host time.time()) if given.
-        A sample is under load when it draws more than 40 % of the power limit."""
+        A sample is under load when it draws more than 40 % of the power limit
+        (instantaneous power where sampled, else the averaged draw)."""
         smp = self.parse(self.lines)
         if t0 is not None:
             smp = [x for x in smp if t0 - 0.05 <= x["t"] <= t1 + 0.05]
         if not smp:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "samples_under_load": 0}
         mhz = sorted(x["mhz"] for x in smp)
-        load = sorted(x["mhz"] for x in smp if x["w"] is not None and x["limit_w"] and x["w"] > 0.4 * x["limit_w"])
+
+        def watts(x):
+            return x["w_inst"] if x.get("w_inst") is not None else x["w"]
+
+        load = sorted(x["mhz"] for x in smp if watts(x) is not None and x["limit_w"] and watts(x) > 0.4 * x["limit_w"])
         reasons = sorted({r for x in smp for r in x["reasons"]})
         pw = [x["w"] for x in smp if x["w"] is not None]
-        return {"sm_mhz": mhz[len(mhz) // 2], "sm_max_mhz": max(x["max_mhz"] for x in smp), "reasons": reasons,
-                "samples": len(smp), "samples_under_load": len(load),
-                "sm_mhz_under_load": load[len(load) // 2] if load else None,
-                "power_w_max": max(pw) if pw else None, "power_limit_w": smp[-1]["limit_w"]}
+        pi = [x["w_inst"] for x in smp if x.get("w_inst") is not None]
+        out = {"sm_mhz": mhz[len(mhz) // 2], "sm_max_mhz": max(x["max_mhz"] for x in smp), "reasons": reasons,
+               "samples": len(smp), "samples_under_load": len(load),
+               "sm_mhz_under_load": load[len(load) // 2] if load else None,
+               "power_w_max": max(pw) if pw else None, "power_limit_w": smp[-1]["limit_w"]}
+        if pi:
+            out["power_w_instant_max"] = max(pi)
+        return out
 
 
 # ---------------------------------------------------------------------------

@@ -144,3 +144,13 @@ def test_clock_sampler_windows_and_load():
     assert s["reasons"] == ["sw_power_cap"] and s["power_w_max"] == 1350.0
     a = c.summary()
     assert a["samples"] == 4 and a["samples_under_load"] == 2 and a["sm_max_mhz"] == 2070.0
+    # with instantaneous power sampled, it decides load: the averaged draw lags a
+    # short timed region
+    inst = ["2026/12/03 05:00:00.000, 0, 2070, 2070, 120.0, 1400.0, 0x0, Not Active, Not Active, Not Active, Not Active, 160.0",
+            "2026/12/03 05:00:00.050, 0, 2070, 2070, 177.6, 1400.0, 0x0, Not Active, Not Active, Not Active, Not Active, 1223.3",
+            "2026/12/03 05:00:00.100, 0, 1620, 2070, 307.8, 1400.0, 0x4, Not Active, Not Active, Not Active, Active, 1391.2",
+            "2026/12/03 05:00:00.150, 0, 2070, 2070, 324.6, 1400.0, 0x0, Not Active, Not Active, Not Active, Not Active, [N/A]"]
+    c.lines = inst
+    b = c.summary()
+    assert b["samples"] == 4 and b["samples_under_load"] == 2 and b["power_w_instant_max"] == 1391.2
+    assert b["power_w_max"] == 324.6 and b["sm_mhz_under_load"] in (1620.0, 2070.0)
