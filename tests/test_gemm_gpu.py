@@ -389,6 +389,29 @@ def test_stream_k_random_parity(variant):
     assert r["ok"] and r["max_excess_rel"] < 2.0 ** -12, r
 
 
+@pytest.mark.parametrize("ti,to", [("bf16", "bf16"), ("f16", "f32")])
+def test_automatic_stream_k_on_pairs_integer_bit_exact(ti, to):
+    # a ragged few-wave output (8 x 20 pair tiles, the last row and column partial;
+    # 33 K blocks, the last one partial) that the automatic plan gives step 8's
+    # pairs with stream-K on 152 SMs
+    M, N, K = 2000, 5000, 2056
+    a, b = inputs.integer_operands(M, N, K, ti, seed=K)
+    plan = gemm.Plan(M, N, K, gemm.dtype_code(ti, to))
+    info = plan.info()
+    if torch.cuda.get_device_properties(0).multi_processor_count == 152:
+        assert info["variant"] == gemm.S8 and info["sched"] == gemm.SCHED_STREAM_K, info
+    c = torch.full((M, N), float("nan"), device=DEV, dtype=inputs.torch_dtype(to))
+    for _ in range(2):
+        c.fill_(float("nan"))
+        plan.run(a.to(DEV), b.to(DEV), c)
+        assert plan.check() == gemm.OK
+    plan.destroy()
+    exp = expect_bits(oracle.gemm(a, b)[0], to)
+    got = c.cpu().numpy() if to == "f32" else c.float().cpu().numpy()
+    bad = np.argwhere(got != exp)
+    assert bad.size == 0, (info, bad[:3])
+
+
 def test_stream_k_is_the_default_when_the_last_wave_is_short():
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     pairs = sms // 2
