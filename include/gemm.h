@@ -111,8 +111,11 @@ typedef enum {
                              block) iterations; a tile split between two clusters is finished
                              by the one holding its first K blocks, from the other's fp32
                              partial in a plan-owned workspace.  The automatic plan uses it
-                             when whole tiles would keep the clusters busy for under 70 % of
-                             the waves.  Fused epilogues and MX plans use whole tiles. */
+                             where a fitted cost model says it finishes sooner than whole
+                             tiles: those keep the clusters busy for under 80 % of the waves
+                             (70 % on variant 9), K has at least 32 K blocks (64 on variant
+                             9), and every cluster gets at least a tile's work.  Fused
+                             epilogues and MX plans use whole tiles. */
 } gemm_sched_t;
 
 /* Tuning and test options; zero-initialise and set what you need.
