@@ -188,7 +188,9 @@ typedef struct {
  * are not 16-byte aligned, step 7 with its K split over a cluster for outputs
  * whose 128 x 256 tiles fill at most half the SMs (and K has at least 32 blocks),
  * otherwise step 9, 8 or 7, whichever a cost model (waves of resident clusters x
- * a tile's area per SM / the step's per-SM rate) says finishes soonest.  The tile
+ * a tile's area per SM / the step's per-SM rate, or the stream-K schedule's even
+ * shares plus its partial sums where it applies) says finishes soonest; below 32
+ * K blocks, a fit of launch ramp and per-wave times with whole tiles.  The tile
  * width, schedule and split are settled by gemm_plan with the device's
  * occupancy.  Errors: GEMM_ERR_INVALID_ARG (null variant, sizes out of range,
  * num_sms < 2), GEMM_ERR_UNSUPPORTED_DTYPE, GEMM_ERR_UNSUPPORTED_SHAPE (K's row
